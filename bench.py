@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of the GGUF block-quantized hot path on GB300.
+
+Headline workload: the Q8_0 decode GEMV suite at Llama-3-8B layer shapes,
+M = 1 token -- 4096x4096, 1024x4096, 14336x4096, 4096x14336 and the LM head
+128256x4096 (705 MB of weights). One step = for each layer, quantise the fp32
+activation to Q8_0 (cq_quantize_act) and run the GEMV (cq_gemv). Value: weight
+bytes streamed per second over the whole step (GB/s), inputs resident in HBM.
+The weights of one step (705 MB) exceed the 129 MB L2, so every step streams
+them from HBM.
+
+Also printed in the same JSON line: the prefill GEMM (Q4_K, M=512, K=4096,
+N=14336) in int8-equivalent TOPS, the routed-expert FFN and the Q4_1 LM head at
+M = 1/4/8/16, the single-call latency of the small Q4_0 GEMV, the roofline of
+the dominant kernel, the CPU oracle's rate on the host cores, and the
+end-to-end rate with host buffers.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cq|reference]
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the
+path has no exchange step); the time is the maximum over ranks and the value
+is the aggregate over all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode GEMV weight GB/s (% of HBM peak); prefill GEMM int8 TOPS (% of peak)"
+WORKLOAD = ("Q8_0 decode GEMV suite, Llama-3-8B layer shapes (NxK) 4096x4096, 1024x4096, 14336x4096, "
+            "4096x14336, 128256x4096; M=1 token; activations fp32 N(0,1) quantized to Q8_0 in-step")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def _traffic(kernel_file: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current source of the kernel (the summary records a hash of the sources)."""
+    path = os.path.join(ROOT, "profiles", kernel_file)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256 ([0-9a-f]+)\)", text)
+    if not m:
+        return None
+    from gemm_gguf_block_gb300.build import source_hash
+    return float(m.group(1)) if source_hash() == m.group(2) else None
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.rows = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def window(self, t0, t1):
+        return [r for (t, r) in self.rows if t0 <= t <= t1]
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if len(r) > 5 + i and r[5 + i] == "Active"})
+        pw = [float(r[3]) for r in rows if re.match(r"^[0-9.]+$", r[3])]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def _gpu_query_id(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# --------------------------------------------------------------- CPU oracle
+def _oracle_suite(suite, row_frac=1.0):
+    """The oracle over the suite (or the first row_frac of each matrix's rows).
+    Returns (seconds, weight bytes processed)."""
+    import oracle
+    t = time.perf_counter()
+    nbytes = 0
+    for W, x in suite:
+        K = x.shape[1]
+        rows = max(1, int(W.shape[0] * row_frac))
+        xq = oracle.quantize(oracle.Q8_0, x)
+        oracle.matmul(oracle.Q8_0, W[:rows], xq, K)
+        nbytes += W[:rows].nbytes
+    return time.perf_counter() - t, nbytes
+
+
+def cpu_baseline(suite, min_s=8.0, max_reps=20):
+    dt_total, b_total, reps = 0.0, 0, 0
+    while reps < max_reps and (reps == 0 or dt_total < min_s):
+        dt, b = _oracle_suite(suite)
+        dt_total += dt
+        b_total += b
+        reps += 1
+    return {"value": b_total / dt_total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole Q8_0 suite step (quantise + all 5 matrices), {reps} repetition(s), "
+                      f"{dt_total:.1f} s single-threaded"}
+
+
+# ----------------------------------------------------------------- reference
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from gemm_gguf_block_gb300 import build as gb, synth
+    oracle.build()
+    suite = synth.decode_q8_0_suite(args.seed)
+    frac = 1.0 / 64
+    for _ in range(args.warmup):
+        _oracle_suite(suite, frac)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        _, b = _oracle_suite(suite, frac)
+        nbytes += b
+    dt = time.perf_counter() - t0
+    v = nbytes / dt / 1e9
+    sample = "first 1/64 of the rows of each of the 5 matrices, plus the full activation quantisation, per step"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "i8xi8->i64, f64 scales", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    _ = gb
+
+
+# --------------------------------------------------------------- GPU timing
+def _flush(torch, buf):
+    buf.add_(1)  # touch 256 MB: evicts the 129 MB L2
+
+
+def time_calls(torch, fn, iters, warmup, flush=None):
+    """Median per-call time (ms) with CUDA events on the current stream."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        fn()
+    times = []
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def secondary(torch, cq, synth, peaks, seed):
+    out = {}
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    flushbuf = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+    flush = lambda: _flush(torch, flushbuf)
+    stream = lambda: torch.cuda.current_stream().cuda_stream
+
+    # prefill GEMM: Q4_K, M=512, K=4096, N=14336
+    W, x = synth.prefill_q4_k(seed)
+    M, K = x.shape
+    N = W.shape[0]
+    Wd, xd = dev(W), dev(x)
+    xq = cq.quantize_act_t(xd, cq.Q8_K)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    fn = lambda: cq.cq_gemm(cq.Q4_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
+    ms = time_calls(torch, fn, 10, 3, flush)
+    tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    out["prefill_gemm_q4_k"] = {"shape": f"M={M} N={N} K={K}", "ms": ms, "int8_equiv_tops": tops,
+                                "peak_tflops": peaks["bf16"], "peak_note": "fp16 tensor peak = measured bf16 x 1",
+                                "frac": tops / peaks["bf16"]}
+    del Wd, xd, xq, y
+
+    # routed-expert FFN: 256 tokens, 32 experts, top-4, Q4_0 2048/1792
+    Wg, Wu, Wdn, ids, rw, x = synth.moe_ffn(seed)
+    T, K = x.shape
+    F = Wg.shape[1]
+    tg, tu, td, ti, tr, tx = (dev(a) for a in (Wg, Wu, Wdn, ids, rw, x))
+    xq = cq.quantize_act_t(tx, cq.Q8_0)
+    need = cq.cq_moe_workspace_size(T, K, F, 32, 4)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    fn = lambda: cq.cq_moe_gemv(cq.Q4_0, T, K, F, 32, 4, tg.data_ptr(), tu.data_ptr(), td.data_ptr(),
+                                ti.data_ptr(), tr.data_ptr(), xq.data_ptr(), y.data_ptr(), ws.data_ptr(), need,
+                                stream())
+    ms = time_calls(torch, fn, 10, 3, flush)
+    wbytes = Wg.nbytes + Wu.nbytes + Wdn.nbytes
+    ops = 2.0 * T * 4 * 3 * F * K
+    out["moe_q4_0"] = {"shape": f"T={T} E=32 top4 K={K} F={F}", "ms": ms, "weight_gbs": wbytes / ms / 1e6,
+                       "int8_equiv_tops": ops / (ms * 1e-3) / 1e12, "hbm_frac": wbytes / ms / 1e6 / peaks["hbm"]}
+    del tg, tu, td, ti, tr, tx, xq, ws, y
+
+    # batched LM head verify: Q4_1 128256x4096, M = 1, 4, 8, 16
+    W, x = synth.lm_head_q4_1(seed)
+    N, K = W.shape[0], x.shape[1]
+    Wd, xd = dev(W), dev(x)
+    xq = cq.quantize_act_t(xd, cq.Q8_1)
+    res = {}
+    for M in (1, 4, 8, 16):
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        fn = lambda: cq.cq_gemv(cq.Q4_1, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
+        ms = time_calls(torch, fn, 10, 3, flush)
+        res[str(M)] = {"ms": ms, "weight_gbs": W.nbytes / ms / 1e6}
+    for M in res:
+        res[M]["t_over_t1"] = res[M]["ms"] / res["1"]["ms"]
+    out["lm_head_q4_1"] = res
+    del Wd, xd, xq
+
+    # small Q4_0 GEMV 2048x2048: single-call latency (L2-resident) and rotated copies
+    W, x = synth.decode_q4_0_small(seed)
+    N, K = W.shape
+    K = x.shape[1]
+    copies = 256
+    Wd = dev(np.broadcast_to(W, (copies,) + W.shape).copy())
+    xq = cq.quantize_act_t(dev(x), cq.Q8_0)
+    y = torch.empty((1, 2048), dtype=torch.float32, device="cuda")
+    fn1 = lambda: cq.cq_gemv(cq.Q4_0, 1, 2048, K, Wd[0].data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
+    lat = time_calls(torch, fn1, 50, 10)
+
+    def rot():
+        for i in range(copies):
+            cq.cq_gemv(cq.Q4_0, 1, 2048, K, Wd[i].data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
+    ms = time_calls(torch, rot, 5, 2)
+    out["decode_q4_0_2048"] = {"single_call_us": lat * 1e3, "rotated_gbs": copies * W.nbytes / ms / 1e6,
+                               "rotation": f"{copies} copies ({copies * W.nbytes / 2**20:.0f} MiB > L2)"}
+    return out
+
+
+def run_cq(args, rank, world, local_rank):
+    import torch
+    from gemm_gguf_block_gb300 import build as gb, cq, synth
+
+    gb.build()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    peaks = _peaks()
+    suite = synth.decode_q8_0_suite(args.seed)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    layers = []
+    for W, x in suite:
+        N, K = W.shape[0], x.shape[1]
+        layers.append(dict(
+            N=N, K=K, W=torch.from_numpy(W).cuda(), x=torch.from_numpy(x).cuda(),
+            xq=torch.empty(cq.row_bytes(cq.Q8_0, K), dtype=torch.uint8, device="cuda"),
+            y=torch.empty(N, dtype=torch.float32, device="cuda"),
+            xh=torch.from_numpy(x).pin_memory(), yh=torch.empty(N, dtype=torch.float32).pin_memory(),
+            bytes=W.nbytes + cq.row_bytes(cq.Q8_0, K) + 4 * N))
+    wbytes = sum(W.nbytes for W, _ in suite)
+    lm = layers[-1]
+
+    def step(ev=None):
+        for i, L in enumerate(layers):
+            st = cq.cq_quantize_act(cq.Q8_0, 1, L["K"], L["x"].data_ptr(), L["xq"].data_ptr(), sh)
+            if ev is not None:
+                ev[2 * i].record(stream)
+            st |= cq.cq_gemv(cq.Q8_0, 1, L["N"], L["K"], L["W"].data_ptr(), L["xq"].data_ptr(),
+                             L["y"].data_ptr(), sh)
+            if ev is not None:
+                ev[2 * i + 1].record(stream)
+            if st:
+                raise RuntimeError(f"cq call failed with status {st}")
+
+    for _ in range(args.warmup):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(layers))] for _ in range(args.steps)]
+    sampler = ClockSampler(_gpu_query_id(torch, local_rank))
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t_wall0 = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist:
+        dist.barrier()
+    time.sleep(0.25)
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    ms_step = ms / args.steps
+    value = world * wbytes / (ms_step * 1e-3) / 1e9
+    # per-launch durations of the GEMV kernel over the timed region
+    gemv_ms = [[evs[k][2 * i].elapsed_time(evs[k][2 * i + 1]) for k in range(args.steps)] for i in range(len(layers))]
+    tot_bytes = sum(L["bytes"] for L in layers) * args.steps
+    tot_ms = sum(sum(v) for v in gemv_ms)
+    achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
+    per_shape = {f"{L['N']}x{L['K']}": {"us": 1e3 * statistics.mean(gemv_ms[i]),
+                                         "gbs": L["bytes"] / (statistics.mean(gemv_ms[i]) * 1e-3) / 1e9}
+                 for i, L in enumerate(layers)}
+    clocks = ClockSampler.summary(sampler.window(t_wall0, t_wall1))
+    if clocks["samples"] == 0:
+        clocks = ClockSampler.summary(sampler.rows and [r for _, r in sampler.rows] or [])
+        clocks["window"] = "whole run (timed region shorter than the sampling interval)"
+
+    # end to end: pinned host activations in, logits/outputs back, every step
+    def e2e_step():
+        for L in layers:
+            L["x"].copy_(L["xh"], non_blocking=True)
+            cq.cq_quantize_act(cq.Q8_0, 1, L["K"], L["x"].data_ptr(), L["xq"].data_ptr(), sh)
+            cq.cq_gemv(cq.Q8_0, 1, L["N"], L["K"], L["W"].data_ptr(), L["xq"].data_ptr(), L["y"].data_ptr(), sh)
+            L["yh"].copy_(L["y"], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    b.record(stream)
+    b.synchronize()
+    e2e_ms = a.elapsed_time(b) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    sec = {}
+    cpu = None
+    if rank == 0:
+        if not args.no_secondary:
+            del layers
+            torch.cuda.empty_cache()
+            sec = secondary(torch, cq, synth, peaks, args.seed)
+        cpu = cpu_baseline(suite)
+    if dist:
+        dist.barrier()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "i8xi8->i32, f32 scales", "data": "synthetic",
+        "hbm_frac": value / world / peaks["hbm"],
+        "config": {"workload": WORKLOAD, "weight_bytes_per_step": wbytes,
+                   "l2": "inputs larger than L2: 705 MB of weights streamed per step (L2 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<Q8_0,1> (all 5 launches of a step)",
+                     "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
+                     "peak_src": f"{peaks['src']} hbm_gbs (copy, read+write bytes)",
+                     "traffic": _traffic("gemv_q8_0_decode_suite.md")},
+        "per_shape": per_shape,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": sum(4 * x.shape[1] for _, x in suite),
+                "d2h_bytes_per_step": sum(4 * W.shape[0] for W, _ in suite)},
+        "gpu_launches": 2 * len(suite) * args.steps,
+        "clocks": clocks,
+        "secondary": sec,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="cq", choices=["cq", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_cq(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,199 @@
+// C ABI of libcq: argument validation and dispatch to the kernel launchers.
+// Every check runs before any launch, so an error return means that nothing
+// was launched and nothing was written. See include/cq.h for the contract.
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/cq.h"
+#include "cq_internal.h"
+
+namespace {
+
+// Status word of kernels that take no workspace (cq_gemv / cq_gemm copy waits).
+__device__ int g_cq_status;
+
+constexpr int MAX_DEVICES = 64;
+std::mutex g_dev_mutex;
+bool g_dev_ready[MAX_DEVICES];
+cq::DeviceInfo g_dev[MAX_DEVICES];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool is_weight_fmt(int f) { return f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0 || f == CQ_Q4_K; }
+bool is_act_fmt(int f) { return f == CQ_Q8_0 || f == CQ_Q8_1 || f == CQ_Q8_K; }
+
+// Largest K accepted by the single-pass kernels (activation rows staged in
+// 96 KB of shared memory: 96 KB / 304 B per 256 elements).
+constexpr int64_t K_MAX = 65536;
+
+cq_status check_shape(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return CQ_ERR_INVALID_ARG;
+    if (K == 0 || K % 256 != 0 || K > K_MAX) return CQ_ERR_SHAPE;
+    if (N > (int64_t(1) << 31)) return CQ_ERR_SHAPE;
+    return CQ_OK;
+}
+
+}  // namespace
+
+namespace cq {
+cudaError_t device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d{};
+        e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_cq_status);
+        if (e != cudaSuccess) return e;
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+}  // namespace cq
+
+extern "C" {
+
+const char* cq_status_string(cq_status s) {
+    switch (s) {
+    case CQ_OK: return "ok";
+    case CQ_ERR_INVALID_ARG: return "invalid argument";
+    case CQ_ERR_UNSUPPORTED_FORMAT: return "unsupported format";
+    case CQ_ERR_SHAPE: return "unsupported shape";
+    case CQ_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case CQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case CQ_ERR_CUDA: return "CUDA error";
+    case CQ_ERR_DEVICE_STATUS: return "device reported bad input";
+    case CQ_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+cq_status cq_quantize_act(cq_format act_fmt, int64_t M, int64_t K, const float* x, void* xq, void* stream) {
+    if (!is_act_fmt(act_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, 1, K);
+    if (st != CQ_OK) return st;
+    if (M == 0) return CQ_OK;
+    if (x == nullptr || xq == nullptr) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq)) return CQ_ERR_ALIGNMENT;
+    cudaError_t e = cq::launch_quantize(act_fmt, M, K, x, xq, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
+                  void* stream) {
+    if (!is_weight_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, N, K);
+    if (st != CQ_OK) return st;
+    if (M > 16) return CQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return CQ_OK;
+    if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_gemv(dev, w_fmt, static_cast<int>(M), N, K, W, xq, y,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+cq_status cq_read_global_status(int32_t* out_code, int clear) {
+    if (out_code == nullptr) return CQ_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return CQ_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_cq_status, sizeof v) != cudaSuccess) return CQ_ERR_CUDA;
+    if (clear) {
+        const int z = 0;
+        if (cudaMemcpyToSymbol(g_cq_status, &z, sizeof z) != cudaSuccess) return CQ_ERR_CUDA;
+    }
+    *out_code = v;
+    return v ? CQ_ERR_TIMEOUT : CQ_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
+                  void* stream) {
+    if (w_fmt != CQ_Q4_K) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, N, K);
+    if (st != CQ_OK) return st;
+    if (M == 0 || N == 0) return CQ_OK;
+    if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+}  // extern "C"
+
+extern "C" {
+
+static cq_status moe_check_shape(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk) {
+    if (T < 0 || K < 0 || F < 0 || E < 0 || topk < 0) return CQ_ERR_INVALID_ARG;
+    if (K == 0 || K % 256 != 0 || K > 4096) return CQ_ERR_SHAPE;
+    if (F == 0 || F % 256 != 0 || F > 8192) return CQ_ERR_SHAPE;
+    if (E < 1 || E > 256 || topk < 1 || topk > E) return CQ_ERR_SHAPE;
+    if (T * topk > (int64_t(1) << 20)) return CQ_ERR_SHAPE;
+    return CQ_OK;
+}
+
+size_t cq_moe_workspace_size(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk) {
+    if (moe_check_shape(T, K, F, E, topk) != CQ_OK) return 0;
+    return cq::moe_layout(T, K, F, E, topk).total;
+}
+
+cq_status cq_moe_workspace_offsets(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk, size_t* status_off,
+                                   size_t* h_off, size_t* hq_off) {
+    cq_status st = moe_check_shape(T, K, F, E, topk);
+    if (st != CQ_OK) return st;
+    if (status_off == nullptr || h_off == nullptr || hq_off == nullptr) return CQ_ERR_INVALID_ARG;
+    const cq::MoeLayout L = cq::moe_layout(T, K, F, E, topk);
+    *status_off = L.status;
+    *h_off = L.h;
+    *hq_off = L.hq;
+    return CQ_OK;
+}
+
+cq_status cq_moe_gemv(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk, const void* W_gate,
+                      const void* W_up, const void* W_down, const int32_t* expert_ids, const float* route_w,
+                      const void* xq, float* y, void* workspace, size_t workspace_bytes, void* stream) {
+    if (w_fmt != CQ_Q4_0) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = moe_check_shape(T, K, F, E, topk);
+    if (st != CQ_OK) return st;
+    if (T == 0) return CQ_OK;
+    if (!W_gate || !W_up || !W_down || !expert_ids || !route_w || !xq || !y) return CQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < cq::moe_layout(T, K, F, E, topk).total) return CQ_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CQ_ERR_ALIGNMENT;
+    for (const void* q : {W_gate, W_up, W_down, static_cast<const void*>(expert_ids),
+                          static_cast<const void*>(route_w), xq, static_cast<const void*>(y)})
+        if (!aligned16(q)) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_moe(dev, static_cast<int>(T), static_cast<int>(K), static_cast<int>(F),
+                                   static_cast<int>(E), static_cast<int>(topk), W_gate, W_up, W_down, expert_ids,
+                                   route_w, xq, y, workspace, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+cq_status cq_moe_read_status(const void* workspace, int32_t* out_code, void* stream) {
+    if (workspace == nullptr || out_code == nullptr) return CQ_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CQ_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return CQ_ERR_CUDA;
+    *out_code = v;
+    if (v & CQ_DEV_WAIT_TIMEOUT) return CQ_ERR_TIMEOUT;
+    return v ? CQ_ERR_DEVICE_STATUS : CQ_OK;
+}
+
+}  // extern "C"

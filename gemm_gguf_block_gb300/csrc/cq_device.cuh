@@ -1,0 +1,109 @@
+// Device-side helpers shared by the cq kernels: block-format constants,
+// binary16 loads, and thin inline-PTX wrappers for mbarriers and the bulk
+// (TMA, one-dimensional) global->shared copy engine of sm_90+/sm_100+.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/cq.h"
+
+namespace cq {
+
+// Bytes per 256-element chunk (eight 32-blocks or one superblock).
+constexpr int CHUNK_ELEMS = 256;
+constexpr int WCHUNK_Q4_0 = 8 * 18;   // 144
+constexpr int WCHUNK_Q4_1 = 8 * 20;   // 160
+constexpr int WCHUNK_Q8_0 = 8 * 34;   // 272
+constexpr int WCHUNK_Q4_K = 144;
+constexpr int ACHUNK_Q8_0 = 8 * 34;   // 272
+constexpr int ACHUNK_Q8_1 = 8 * 36;   // 288
+constexpr int ACHUNK_Q8_K = 292;
+
+__host__ __device__ constexpr int wchunk_bytes(int fmt) {
+    return fmt == CQ_Q4_0 ? WCHUNK_Q4_0 : fmt == CQ_Q4_1 ? WCHUNK_Q4_1 : fmt == CQ_Q8_0 ? WCHUNK_Q8_0
+         : fmt == CQ_Q4_K ? WCHUNK_Q4_K : 0;
+}
+__host__ __device__ constexpr int act_fmt_for(int wfmt) {
+    return wfmt == CQ_Q4_0 || wfmt == CQ_Q8_0 ? CQ_Q8_0 : wfmt == CQ_Q4_1 ? CQ_Q8_1 : wfmt == CQ_Q4_K ? CQ_Q8_K : -1;
+}
+__host__ __device__ constexpr int achunk_bytes(int afmt) {
+    return afmt == CQ_Q8_0 ? ACHUNK_Q8_0 : afmt == CQ_Q8_1 ? ACHUNK_Q8_1 : afmt == CQ_Q8_K ? ACHUNK_Q8_K : 0;
+}
+
+__device__ __forceinline__ float h2f(uint32_t bits16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xffffu)));
+}
+
+// Four signed bytes (q - 8) from four nibbles 0..15 held one per byte:
+// q + 0x78 stays below 0x100, and flipping bit 7 maps it to (q - 8) mod 256.
+__device__ __forceinline__ int nib_minus8(uint32_t nibs) {
+    return static_cast<int>((nibs + 0x78787878u) ^ 0x80808080u);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for a phase to complete: gives up after `limit_ns` of wall
+// time (checked every 256 polls) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// One-dimensional bulk copy global -> this CTA's shared memory, completing
+// `bytes` transactions on `bar`. Addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Wall-time limit of any copy-completion wait (a copy that has not landed by
+// then never will): the kernel flags CQ_DEV_WAIT_TIMEOUT and stops.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+}  // namespace cq

@@ -1,0 +1,44 @@
+// Host-side launchers shared between the C-ABI translation unit and the
+// kernel translation units. Arguments are validated by the caller (cq_api.cu).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace cq {
+
+struct DeviceInfo {
+    int sm_count;
+    int smem_optin;   // max dynamic shared memory per block (bytes)
+    int* status;      // device address of the library status word
+};
+
+// Cached per-device properties; status address from cudaGetSymbolAddress.
+cudaError_t device_info(DeviceInfo* out);
+
+cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, void* xq, cudaStream_t s);
+
+cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
+                        const void* xq, float* y, cudaStream_t s);
+
+// Prefill GEMM (any M): y rows equal the cq_gemv rows bit for bit.
+cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
+                        const void* xq, float* y, cudaStream_t s);
+
+// Byte offsets of the routed-FFN workspace sections (each 256-byte aligned).
+struct MoeLayout {
+    size_t status;   // int32 status word (CQ_DEV_* bits)
+    size_t offs;     // int32 [E+1]: start of each expert's pair list in perm
+    size_t perm;     // int32 [T*topk]: pair indices (t*topk + s) grouped by expert
+    size_t valid;    // int32 [T*topk]: 1 if the pair's expert id was accepted
+    size_t h;        // fp32 [T*topk][F]: hidden activations, (token, slot) order
+    size_t hq;       // Q8_0 [T*topk] rows of F/32 blocks
+    size_t out;      // fp32 [T*topk][K]: per-pair down-projection outputs
+    size_t total;
+};
+MoeLayout moe_layout(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk);
+
+cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
+                       const void* Wu, const void* Wd, const int32_t* ids, const float* rw, const void* xq,
+                       float* y, void* ws, cudaStream_t s);
+
+}  // namespace cq

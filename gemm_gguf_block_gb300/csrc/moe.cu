@@ -1,0 +1,362 @@
+// Routed-expert FFN (lfm2moe-style: each token picks topk of E experts).
+//
+// cera README "Supported models": every token routes to 4 of 32 experts and
+// the block's output is the router-weighted sum of the chosen experts'
+// SwiGLU FFNs; the pages note that their GPU kernels re-read an expert's
+// weights once per routed token and name grouping tokens by expert as the
+// follow-up. This file does that grouping: each expert's weights are read
+// once per call, for all the tokens routed to it.
+// alice-llm "WGSL Shader Architecture" (swiglu_fused_q4k): gate and up share
+// one pass over the input.
+//
+// Pipeline (all asynchronous on the caller's stream, no host round trip):
+//   1. route:   validate ids (range, no repeats within a token), counting-sort
+//               the (token, slot) pairs by expert; stable, so deterministic.
+//   2. up:      per (expert, 32-row tile of F): gate and up tiles land in
+//               shared memory by bulk copy; the expert's tokens stream past
+//               them eight at a time; h = silu(g) * u, then Q8_0 of h.
+//   3. down:    per (expert, 32-row tile of K): o = W_down . hq per pair.
+//   4. combine: y[t] = sum over slots in slot order of w * o (fma chain).
+#include <algorithm>
+
+#include "chunk_dot.cuh"
+#include "cq_device.cuh"
+#include "cq_internal.h"
+
+namespace cq {
+
+MoeLayout moe_layout(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk) {
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    MoeLayout L{};
+    const size_t P = static_cast<size_t>(T * topk);
+    size_t o = 0;
+    L.status = o; o += 256;
+    L.offs = o; o = up(o + 4 * static_cast<size_t>(E + 1));
+    L.perm = o; o = up(o + 4 * P);
+    L.valid = o; o = up(o + 4 * P);
+    L.h = o; o = up(o + 4 * P * static_cast<size_t>(F));
+    L.hq = o; o = up(o + P * static_cast<size_t>(F / 32 * 34));
+    L.out = o; o = up(o + 4 * P * static_cast<size_t>(K));
+    L.total = o;
+    return L;
+}
+
+namespace {
+
+constexpr int TILE = 32;      // weight rows per CTA tile
+constexpr int TOKG = 8;       // tokens per pass over a tile
+constexpr int THREADS = 256;
+
+struct MoeParams {
+    const uint8_t* Wg;
+    const uint8_t* Wu;
+    const uint8_t* Wd;
+    const int32_t* ids;
+    const float* rw;
+    const uint8_t* xq;
+    float* y;
+    uint8_t* ws;
+    MoeLayout L;
+    int T, K, F, E, topk;
+};
+
+__device__ __forceinline__ int* ws_status(const MoeParams& p) { return reinterpret_cast<int*>(p.ws + p.L.status); }
+__device__ __forceinline__ int* ws_offs(const MoeParams& p) { return reinterpret_cast<int*>(p.ws + p.L.offs); }
+__device__ __forceinline__ int* ws_perm(const MoeParams& p) { return reinterpret_cast<int*>(p.ws + p.L.perm); }
+__device__ __forceinline__ int* ws_valid(const MoeParams& p) { return reinterpret_cast<int*>(p.ws + p.L.valid); }
+
+// ------------------------------------------------------------------ route
+__global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
+    __shared__ int cnt[256];
+    __shared__ int off[257];
+    const int P = p.T * p.topk;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    int* valid = ws_valid(p);
+    int* status = ws_status(p);
+    if (tid == 0) *status = 0;   // the call's status word starts clear
+    __syncthreads();
+    for (int i = tid; i < P; i += blockDim.x) {
+        const int t = i / p.topk, s = i - t * p.topk;
+        const int e = p.ids[i];
+        int flag = 0;
+        if (e < 0 || e >= p.E) {
+            flag = CQ_DEV_BAD_EXPERT_ID;
+        } else {
+            for (int s2 = 0; s2 < s; ++s2)
+                if (p.ids[t * p.topk + s2] == e) flag = CQ_DEV_DUP_EXPERT_ID;
+        }
+        valid[i] = flag == 0;
+        if (flag) atomicOr(status, flag);
+    }
+    __syncthreads();   // valid[] written by this CTA: visible to it after the barrier
+    for (int e = warp; e < p.E; e += nwarps) {
+        int c = 0;
+        for (int base = 0; base < P; base += 32) {
+            const int i = base + lane;
+            const bool hit = i < P && valid[i] && p.ids[i] == e;
+            c += __popc(__ballot_sync(0xffffffffu, hit));
+        }
+        if (lane == 0) cnt[e] = c;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0;
+        for (int e = 0; e < p.E; ++e) { off[e] = acc; acc += cnt[e]; }
+        off[p.E] = acc;
+    }
+    __syncthreads();
+    int* offs = ws_offs(p);
+    int* perm = ws_perm(p);
+    for (int e = tid; e <= p.E; e += blockDim.x) offs[e] = off[e];
+    for (int e = warp; e < p.E; e += nwarps) {
+        int pos = off[e];
+        for (int base = 0; base < P; base += 32) {
+            const int i = base + lane;
+            const bool hit = i < P && valid[i] && p.ids[i] == e;
+            const unsigned m = __ballot_sync(0xffffffffu, hit);
+            if (hit) perm[pos + __popc(m & ((1u << lane) - 1u))] = i;
+            pos += __popc(m);
+        }
+    }
+}
+
+// Copy `n` 34-byte-block rows (token rows of Q8_0) into shared memory, row i
+// from src_row(i), `words` 32-bit words each, destination pitch `pitch`.
+template <class RowFn>
+__device__ __forceinline__ void stage_rows(uint8_t* dst, int pitch, int n, int words, RowFn src_row) {
+    const int total = n * words;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+        const int r = i / words, w = i - r * words;
+        reinterpret_cast<uint32_t*>(dst + r * pitch)[w] = reinterpret_cast<const uint32_t*>(src_row(r))[w];
+    }
+}
+
+// Wait (all threads) for the weight tile; on timeout flag it, give the copy a
+// second bounded wait to land (so none is in flight when the CTA exits) and
+// report false.
+__device__ __forceinline__ bool wait_tile(uint64_t* bar, int* status) {
+    const bool ok = mbar_wait_bounded(bar, 0, WAIT_LIMIT_NS);
+    if (__syncthreads_and(ok)) return true;
+    if (threadIdx.x == 0) {
+        atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
+        (void)mbar_wait_bounded(bar, 0, WAIT_LIMIT_NS / 8);
+    }
+    __syncthreads();
+    return false;
+}
+
+// ------------------------------------------------------------- gate/up + SwiGLU
+__global__ void __launch_bounds__(THREADS) moe_up_kernel(const MoeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int e = blockIdx.y, f0 = blockIdx.x * TILE;
+    const int* offs = ws_offs(p);
+    const int beg = offs[e], cnt = offs[e + 1] - beg;
+    if (cnt == 0) return;
+    const int nc = p.K / CHUNK_ELEMS;
+    const int rowb = nc * WCHUNK_Q4_0;                 // bytes of one weight row
+    const int tok_pitch = nc * ACHUNK_Q8_0;            // one Q8_0 token row
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* wt = smem + 128;                          // [2*TILE rows][rowb]: gate rows, then up rows
+    uint8_t* xs = wt + (2 * TILE * rowb + 127) / 128 * 128;
+    float* cbuf = reinterpret_cast<float*>(xs + (TOKG * tok_pitch + 127) / 128 * 128);   // [TOKG][2*TILE][nc]
+    float* gu = cbuf + TOKG * 2 * TILE * nc;                                              // [TOKG][2*TILE]
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        const uint32_t half = static_cast<uint32_t>(TILE * rowb);
+        mbar_arrive_expect_tx(bar, 2 * half);
+        const size_t mat = static_cast<size_t>(p.F) * rowb;
+        const uint64_t pol = policy_evict_first();
+        bulk_g2s(wt, p.Wg + e * mat + static_cast<size_t>(f0) * rowb, half, bar, pol);
+        bulk_g2s(wt + half, p.Wu + e * mat + static_cast<size_t>(f0) * rowb, half, bar, pol);
+    }
+    __syncthreads();
+    const int* perm = ws_perm(p) + beg;
+    bool have_tile = false;
+    float* hbase = reinterpret_cast<float*>(p.ws + p.L.h);
+    uint8_t* hqbase = p.ws + p.L.hq;
+    const int hq_row = p.F / 32 * 34;
+    for (int g0 = 0; g0 < cnt; g0 += TOKG) {
+        const int gm = min(TOKG, cnt - g0);
+        stage_rows(xs, tok_pitch, gm, tok_pitch / 4,
+                   [&](int r) { return p.xq + static_cast<size_t>(perm[g0 + r] / p.topk) * tok_pitch; });
+        if (!have_tile) {
+            if (!wait_tile(bar, ws_status(p))) return;
+            have_tile = true;
+        } else {
+            __syncthreads();
+        }
+        const int ntasks = 2 * TILE * nc;
+        for (int t = threadIdx.x; t < ntasks; t += blockDim.x) {
+            const int r = t / nc, j = t - r * nc;
+            float c[TOKG];
+            chunk_dot<CQ_Q4_0, TOKG>(wt + r * rowb + j * WCHUNK_Q4_0, xs + j * ACHUNK_Q8_0, tok_pitch, gm, c);
+#pragma unroll
+            for (int m = 0; m < TOKG; ++m)
+                if (m < gm) cbuf[(m * 2 * TILE + r) * nc + j] = c[m];
+        }
+        __syncthreads();
+        for (int q = threadIdx.x; q < gm * 2 * TILE; q += blockDim.x) {
+            const float* cb = cbuf + q * nc;
+            float acc = 0.0f;
+            for (int j = 0; j < nc; ++j) acc = __fadd_rn(acc, cb[j]);
+            gu[q] = acc;
+        }
+        __syncthreads();
+        // One warp per token: lane f of the 32-row tile; h = silu(g) * u, then
+        // the Q8_0 block of these 32 values (the cq_quantize_act rule).
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        if (warp < gm) {
+            const int pair = perm[g0 + warp];
+            const float g = gu[warp * 2 * TILE + lane];
+            const float u = gu[warp * 2 * TILE + TILE + lane];
+            const float silu = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+            const float h = __fmul_rn(silu, u);
+            hbase[static_cast<size_t>(pair) * p.F + f0 + lane] = h;
+            float amax = fabsf(h);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float d = __fdiv_rn(amax, 127.0f);
+            const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+            float r = roundf(__fmul_rn(h, id));
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            uint8_t* blk = hqbase + static_cast<size_t>(pair) * hq_row + (f0 / 32) * 34;
+            blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(r)));
+            if (lane == 0) *reinterpret_cast<__half*>(blk) = __float2half_rn(d);
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------- down
+__global__ void __launch_bounds__(THREADS) moe_down_kernel(const MoeParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int e = blockIdx.y, k0 = blockIdx.x * TILE;
+    const int* offs = ws_offs(p);
+    const int beg = offs[e], cnt = offs[e + 1] - beg;
+    if (cnt == 0) return;
+    const int nc = p.F / CHUNK_ELEMS;
+    const int rowb = nc * WCHUNK_Q4_0;
+    const int tok_pitch = nc * ACHUNK_Q8_0;            // one hq row
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+    uint8_t* wt = smem + 128;
+    uint8_t* xs = wt + (TILE * rowb + 127) / 128 * 128;
+    float* cbuf = reinterpret_cast<float*>(xs + (TOKG * tok_pitch + 127) / 128 * 128);   // [TOKG][TILE][nc]
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        const uint32_t bytes = static_cast<uint32_t>(TILE * rowb);
+        mbar_arrive_expect_tx(bar, bytes);
+        const size_t mat = static_cast<size_t>(p.K) * rowb;
+        bulk_g2s(wt, p.Wd + e * mat + static_cast<size_t>(k0) * rowb, bytes, bar, policy_evict_first());
+    }
+    __syncthreads();
+    const int* perm = ws_perm(p) + beg;
+    const uint8_t* hq = p.ws + p.L.hq;
+    float* out = reinterpret_cast<float*>(p.ws + p.L.out);
+    bool have_tile = false;
+    for (int g0 = 0; g0 < cnt; g0 += TOKG) {
+        const int gm = min(TOKG, cnt - g0);
+        stage_rows(xs, tok_pitch, gm, tok_pitch / 4,
+                   [&](int r) { return hq + static_cast<size_t>(perm[g0 + r]) * tok_pitch; });
+        if (!have_tile) {
+            if (!wait_tile(bar, ws_status(p))) return;
+            have_tile = true;
+        } else {
+            __syncthreads();
+        }
+        const int ntasks = TILE * nc;
+        for (int t = threadIdx.x; t < ntasks; t += blockDim.x) {
+            const int r = t / nc, j = t - r * nc;
+            float c[TOKG];
+            chunk_dot<CQ_Q4_0, TOKG>(wt + r * rowb + j * WCHUNK_Q4_0, xs + j * ACHUNK_Q8_0, tok_pitch, gm, c);
+#pragma unroll
+            for (int m = 0; m < TOKG; ++m)
+                if (m < gm) cbuf[(m * TILE + r) * nc + j] = c[m];
+        }
+        __syncthreads();
+        for (int q = threadIdx.x; q < gm * TILE; q += blockDim.x) {
+            const int m = q / TILE, r = q - m * TILE;
+            const float* cb = cbuf + q * nc;
+            float acc = 0.0f;
+            for (int j = 0; j < nc; ++j) acc = __fadd_rn(acc, cb[j]);
+            out[static_cast<size_t>(perm[g0 + m]) * p.K + k0 + r] = acc;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- combine
+__global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
+    const int64_t n = static_cast<int64_t>(p.T) * p.K;
+    const int* valid = ws_valid(p);
+    const float* out = reinterpret_cast<const float*>(p.ws + p.L.out);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(i / p.K), k = static_cast<int>(i - static_cast<int64_t>(t) * p.K);
+        float acc = 0.0f;
+        for (int s = 0; s < p.topk; ++s) {
+            const int pair = t * p.topk + s;
+            if (valid[pair]) acc = __fmaf_rn(p.rw[pair], out[static_cast<size_t>(pair) * p.K + k], acc);
+        }
+        p.y[i] = acc;
+    }
+}
+
+}  // namespace
+
+size_t moe_up_smem(int K) {
+    const int nc = K / CHUNK_ELEMS;
+    const int rowb = nc * WCHUNK_Q4_0, tok_pitch = nc * ACHUNK_Q8_0;
+    return 128 + (2 * TILE * rowb + 127) / 128 * 128 + (TOKG * tok_pitch + 127) / 128 * 128 +
+           4 * (TOKG * 2 * TILE * nc + TOKG * 2 * TILE);
+}
+size_t moe_down_smem(int F) {
+    const int nc = F / CHUNK_ELEMS;
+    const int rowb = nc * WCHUNK_Q4_0, tok_pitch = nc * ACHUNK_Q8_0;
+    return 128 + (TILE * rowb + 127) / 128 * 128 + (TOKG * tok_pitch + 127) / 128 * 128 + 4 * (TOKG * TILE * nc);
+}
+
+cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
+                       const void* Wu, const void* Wd, const int32_t* ids, const float* rw, const void* xq,
+                       float* y, void* ws, cudaStream_t s) {
+    MoeParams p{};
+    p.Wg = static_cast<const uint8_t*>(Wg);
+    p.Wu = static_cast<const uint8_t*>(Wu);
+    p.Wd = static_cast<const uint8_t*>(Wd);
+    p.ids = ids;
+    p.rw = rw;
+    p.xq = static_cast<const uint8_t*>(xq);
+    p.y = y;
+    p.ws = static_cast<uint8_t*>(ws);
+    p.L = moe_layout(T, K, F, E, topk);
+    p.T = T; p.K = K; p.F = F; p.E = E; p.topk = topk;
+    moe_route_kernel<<<1, 1024, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int smem_up = static_cast<int>(moe_up_smem(K));
+    const int smem_dn = static_cast<int>(moe_down_smem(F));
+    const int lim = std::min(dev.smem_optin, 227 * 1024);
+    if (smem_up > lim || smem_dn > lim) return cudaErrorInvalidConfiguration;
+    static int raised[64] = {};
+    int devid = 0;
+    if ((e = cudaGetDevice(&devid)) != cudaSuccess) return e;
+    if (devid >= 64 || !raised[devid]) {
+        if ((e = cudaFuncSetAttribute(moe_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess)
+            return e;
+        if ((e = cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
+            cudaSuccess)
+            return e;
+        if (devid < 64) raised[devid] = 1;
+    }
+    moe_up_kernel<<<dim3(F / TILE, E), THREADS, smem_up, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    moe_down_kernel<<<dim3(K / TILE, E), THREADS, smem_dn, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t n = static_cast<int64_t>(T) * K;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4096));
+    moe_combine_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace cq

@@ -1,0 +1,115 @@
+// Activation quantisation fp32 -> Q8_0 / Q8_1 / Q8_K.
+//
+// alice-llm docs, "Phase 4 -- i8 Dynamic Quantization + SDOT": per chunk the
+// absolute maximum, a scale of amax/127, and a rounded int8 per element;
+// "Computation Path (Q4_K)" step 1: Q8_K = 256 elements with an fp32 scale,
+// int8 values and int16 sums of each 16 values; cera README "Quantization":
+// activations quantized dynamically to Q8_0.
+//
+// Every decision is taken in fp32 with IEEE round-to-nearest: d = amax / 127
+// (correctly rounded division), id = 1/d (correctly rounded reciprocal),
+// q = roundf(x * id) (ties away from zero), clamped to [-127, 127]. The fp16
+// scale is d rounded to nearest even, subnormals kept.
+//
+// One warp per block: a 32-block gives one element per lane; a 256-block
+// gives eight consecutive elements per lane (two 16-byte loads).
+#include <algorithm>
+
+#include "cq_device.cuh"
+#include "cq_internal.h"
+
+namespace cq {
+namespace {
+
+__device__ __forceinline__ float warp_max(float a) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    return a;
+}
+__device__ __forceinline__ int warp_sum(int a) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    return a;
+}
+__device__ __forceinline__ int quant1(float v, float id) {
+    float r = roundf(__fmul_rn(v, id));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+
+template <int AF>
+__global__ void __launch_bounds__(256) quantize32_kernel(const float* __restrict__ x, uint8_t* __restrict__ xq,
+                                                         int64_t nblocks) {
+    constexpr int BB = AF == CQ_Q8_0 ? 34 : 36;     // block bytes
+    constexpr int QOFF = AF == CQ_Q8_0 ? 2 : 4;     // offset of the quants
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += stride) {
+        const float v = x[b * 32 + lane];
+        const float amax = warp_max(fabsf(v));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+        const int q = quant1(v, id);
+        uint8_t* blk = xq + b * BB;
+        blk[QOFF + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+        if (AF == CQ_Q8_1) {
+            const int s = warp_sum(q);
+            if (lane == 0)
+                *reinterpret_cast<__half*>(blk + 2) = __float2half_rn(__fmul_rn(d, static_cast<float>(s)));
+        }
+        if (lane == 0) *reinterpret_cast<__half*>(blk) = __float2half_rn(d);
+    }
+}
+
+__global__ void __launch_bounds__(256) quantize_q8k_kernel(const float* __restrict__ x, uint8_t* __restrict__ xq,
+                                                           int64_t nblocks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += stride) {
+        const float4* src = reinterpret_cast<const float4*>(x + b * 256 + 8 * lane);
+        const float4 v0 = src[0], v1 = src[1];
+        const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+        const float amax = warp_max(a);
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+        uint32_t packed[2] = {0u, 0u};
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = quant1(v[i], id);
+            sum += q;
+            packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (i & 3));
+        }
+        uint8_t* blk = xq + b * 292;
+        uint32_t* qw = reinterpret_cast<uint32_t*>(blk + 4 + 8 * lane);
+        qw[0] = packed[0];
+        qw[1] = packed[1];
+        const int pair = sum + __shfl_xor_sync(0xffffffffu, sum, 1);   // 16 consecutive quants
+        if ((lane & 1) == 0)
+            *reinterpret_cast<int16_t*>(blk + 260 + lane) = static_cast<int16_t>(pair);
+        if (lane == 0) *reinterpret_cast<float*>(blk) = d;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, void* xq, cudaStream_t s) {
+    const int bs = act_fmt == CQ_Q8_K ? 256 : 32;
+    const int64_t nblocks = M * (K / bs);
+    if (nblocks == 0) return cudaSuccess;
+    const int64_t warps = nblocks;
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((warps + 7) / 8, 16384));
+    uint8_t* out = static_cast<uint8_t*>(xq);
+    switch (act_fmt) {
+    case CQ_Q8_0: quantize32_kernel<CQ_Q8_0><<<grid, 256, 0, s>>>(x, out, nblocks); break;
+    case CQ_Q8_1: quantize32_kernel<CQ_Q8_1><<<grid, 256, 0, s>>>(x, out, nblocks); break;
+    case CQ_Q8_K: quantize_q8k_kernel<<<grid, 256, 0, s>>>(x, out, nblocks); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace cq

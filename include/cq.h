@@ -1,0 +1,173 @@
+/*
+ * cq.h -- GGUF block-quantized GEMV / GEMM / routed-expert FFN on NVIDIA GB300.
+ *
+ * y = W . x where W is stored in a GGUF block format and x is quantized at run
+ * time to the paired 8-bit format:
+ *
+ *     weight format   activation format   block
+ *     Q4_0            Q8_0                32 elements
+ *     Q8_0            Q8_0                32 elements
+ *     Q4_1            Q8_1                32 elements
+ *     Q4_K            Q8_K                256 elements
+ *
+ * Sources (web pages on GGUF inference engines; sections by name):
+ *   cera README "Quantization" (weight types; activations quantized to Q8_0
+ *   for an integer GEMV); alice-llm docs "Quantization Block Specs" (Q4_K and
+ *   Q8_0 block layouts), "Computation Path (Q4_K)" (Q8_K activations and the
+ *   Q4_K x Q8_K integer formula), "Phase 4 -- i8 Dynamic Quantization + SDOT"
+ *   (per-chunk amax/127 quantisation); cera 0.5 release notes and README
+ *   "Other features" (batched LM-head projection over verified positions;
+ *   Q4_1 decode matching the batched prefill GEMM bit for bit); cera README
+ *   "Supported models" (lfm2moe: 4-of-32 routed experts, grouping tokens by
+ *   expert as the follow-up); alice-llm "WGSL Shader Architecture" (fused
+ *   gate+up SwiGLU).
+ *
+ * Conventions for every call:
+ *   - All data pointers are DEVICE pointers, 16-byte aligned, owned by the
+ *     caller. The library never allocates, frees or synchronises on these
+ *     paths; every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) on the current device.
+ *   - Matrices are row-major. A weight row holds the K/blk blocks of one
+ *     output row contiguously (GGUF order); activations are M rows of blocks;
+ *     outputs are fp32 [M][N] (token-major).
+ *   - K must be a positive multiple of 256. N == 0 or M == 0 is a valid no-op.
+ *   - Arguments are validated before any launch: an error status means
+ *     nothing was launched and nothing was written.
+ *   - Results are deterministic and do not depend on the launch shape: each
+ *     output is accumulated in one fixed fp32 order (below), so a row of a
+ *     multi-token call equals the single-token call bit for bit, and cq_gemv
+ *     and cq_gemm agree bit for bit.
+ *
+ * Fixed fp32 evaluation order (the contract behind the bitwise equalities):
+ *   isum = exact int32 dot of the block's quants.
+ *   Q4_0/Q8_0 block:  c = fma(D(d_w) * D(d_x), (float)isum, c)
+ *   Q4_1 block:       c = fma(D(d_w) * D(d_x), (float)isum, c);
+ *                     c = fma(D(m_w), D(s_x), c)
+ *   Q4_K superblock:  S_j = int dot of sub-block j, isum_sc = sum_j sc_j S_j,
+ *                     isum_m = sum_j m_j (bsum_2j + bsum_2j+1),
+ *                     c = fma(d_x * D(d), (float)isum_sc,
+ *                             -((d_x * D(dmin)) * (float)isum_m))
+ *   Blocks are taken in 256-element chunks; c starts at 0 for every chunk and
+ *   takes the chunk's blocks in increasing k; then y = y + c over the chunks in
+ *   increasing k, starting from y = 0. Every operation rounds to nearest.
+ */
+#ifndef CQ_H
+#define CQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Block formats, numbered as the GGML tensor-type ids. */
+typedef enum {
+    CQ_Q4_0 = 2,
+    CQ_Q4_1 = 3,
+    CQ_Q8_0 = 8,
+    CQ_Q8_1 = 9,
+    CQ_Q4_K = 12,
+    CQ_Q8_K = 15
+} cq_format;
+
+typedef enum {
+    CQ_OK = 0,
+    CQ_ERR_INVALID_ARG = 1,        /* NULL pointer or a negative size */
+    CQ_ERR_UNSUPPORTED_FORMAT = 2, /* a format (pairing) this call does not take */
+    CQ_ERR_SHAPE = 3,              /* K not a positive multiple of 256, M out of range, too large */
+    CQ_ERR_ALIGNMENT = 4,          /* a pointer not 16-byte aligned */
+    CQ_ERR_WORKSPACE = 5,          /* workspace missing or smaller than required */
+    CQ_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+    CQ_ERR_DEVICE_STATUS = 7,      /* a kernel reported bad input (see the status word) */
+    CQ_ERR_TIMEOUT = 8             /* a bounded device wait gave up (see the status word) */
+} cq_status;
+
+/* Device status word bits (written by kernels, read by the cq_read_* calls). */
+#define CQ_DEV_BAD_EXPERT_ID   0x1 /* an expert id outside [0, E): that (token, slot) is skipped */
+#define CQ_DEV_DUP_EXPERT_ID   0x2 /* an expert id repeated within a token: the repeat is skipped */
+#define CQ_DEV_WAIT_TIMEOUT    0x4 /* a copy-completion wait ran out of iterations */
+
+/*
+ * Activation quantisation (alice-llm "Phase 4 -- i8 Dynamic Quantization";
+ * cera "Quantization"; alice-llm "Computation Path (Q4_K)" step 1).
+ * x: fp32 [M][K] -> xq: M rows of act_fmt blocks, per block (all in fp32):
+ *   amax = max|x_i|; d = amax / 127; q_i = round-half-away(x_i * (1/d)),
+ *   clamped to [-127, 127] (q = 0 when d = 0).
+ *   Q8_0 (34 B / 32): fp16(d), q[32].
+ *   Q8_1 (36 B / 32): fp16(d), fp16(d * sum q), q[32].
+ *   Q8_K (292 B / 256): fp32 d, q[256], int16 bsum[16] (sums of 16 quants).
+ * x must be finite. xq must hold M * K/blk * bytes(blk).
+ */
+cq_status cq_quantize_act(cq_format act_fmt, int64_t M, int64_t K, const float* x, void* xq,
+                          void* stream);
+
+/*
+ * Decode GEMV and batched LM-head projection, 1 <= M <= 16 tokens
+ * (cera "Other features": the verify path projects all 1+k positions in one
+ * batched pass so the head is read once; alice-llm "Batch-4 Speculative
+ * Decoding": weights decoded once, one accumulator set per token).
+ * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K}; xq in the paired activation format.
+ * W: N rows of K/blk blocks. y: fp32 [M][N]. M > 16 returns CQ_ERR_SHAPE.
+ */
+cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
+                  float* y, void* stream);
+
+/*
+ * Prefill GEMM, any M >= 0 (cera README "Supported models": batched-GEMM
+ * prefill; alice-llm "Computation Path (Q4_K)"). Same operands and result as
+ * cq_gemv; each row equals the cq_gemv result for that token bit for bit.
+ * w_fmt: Q4_K (tensor-core path). Other formats return
+ * CQ_ERR_UNSUPPORTED_FORMAT.
+ */
+cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
+                  float* y, void* stream);
+
+/*
+ * Routed-expert FFN (cera README "Supported models", lfm2moe; grouping tokens
+ * by expert so each expert's weights are read once per call).
+ * For token t and slot s: e = expert_ids[t][s] (distinct within a token),
+ *   g = W_gate[e] . xq[t],  u = W_up[e] . xq[t]        (F outputs each)
+ *   h = silu(g) * u = g / (1 + exp(-g)) * u              (fp32)
+ *   hq = Q8_0(h) (the cq_quantize_act rule)
+ *   o = W_down[e] . hq                                   (K outputs)
+ *   y[t] = route_w[t][0] * o_0, then y[t] = fma(route_w[t][s], o_s, y[t])
+ *          for s = 1..topk-1 in slot order.
+ * w_fmt: Q4_0. W_gate, W_up: [E][F rows][K]; W_down: [E][K rows][F];
+ * xq: Q8_0 [T][K]; expert_ids: int32 [T][topk]; route_w: fp32 [T][topk];
+ * y: fp32 [T][K]. K and F positive multiples of 256; 1 <= topk <= E <= 256.
+ * workspace: device memory of at least cq_moe_workspace_size(...) bytes,
+ * 256-byte aligned, owned by the caller; its status word is cleared by the
+ * call. Ids outside [0, E) or repeated within a token are skipped and flagged
+ * in the status word (CQ_DEV_*): read it with cq_moe_read_status.
+ */
+size_t cq_moe_workspace_size(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk);
+
+cq_status cq_moe_gemv(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk,
+                      const void* W_gate, const void* W_up, const void* W_down,
+                      const int32_t* expert_ids, const float* route_w, const void* xq, float* y,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Byte offsets inside the MoE workspace, for inspection by tests: the status
+ * word (int32), the hidden activations h (fp32 [T*topk][F], in (token, slot)
+ * order) and their Q8_0 quantisation hq ([T*topk] rows of F/32 blocks).
+ */
+cq_status cq_moe_workspace_offsets(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk,
+                                   size_t* status_off, size_t* h_off, size_t* hq_off);
+
+/* Synchronises `stream`, then copies the MoE workspace status word to *out_code.
+ * Returns CQ_ERR_DEVICE_STATUS if any CQ_DEV_* bit is set, else CQ_OK. */
+cq_status cq_moe_read_status(const void* workspace, int32_t* out_code, void* stream);
+
+/* Synchronises the current device, then reads (and, if clear != 0, zeroes) the
+ * library's own status word, used by kernels that take no workspace (a copy
+ * wait that timed out in cq_gemv / cq_gemm). CQ_ERR_TIMEOUT if set. */
+cq_status cq_read_global_status(int32_t* out_code, int clear);
+
+const char* cq_status_string(cq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CQ_H */

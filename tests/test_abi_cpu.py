@@ -1,0 +1,94 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+include/cq.h declares, and rejects bad arguments before touching the device."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from gemm_gguf_block_gb300 import build, cq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return cq.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "cq.h")).read()
+    return sorted(set(re.findall(r"\b(cq_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in cq.SIGNATURES, f"binding lacks {n}"
+
+
+def test_status_strings(L):
+    for s in range(9):
+        assert cq.status_string(s)
+    assert cq.status_string(0) == "ok"
+
+
+A = 1 << 20   # an aligned fake address: validation fails before it is ever used
+
+
+@pytest.mark.parametrize("fn", ["cq_gemv", "cq_gemm"])
+def test_validation_before_launch(L, fn):
+    f = getattr(cq, fn)
+    fmt = cq.Q4_K
+    assert f(99, 1, 8, 256, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q8_1, 1, 8, 256, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(fmt, 1, 8, 100, A, A, A) == cq.ERR_SHAPE          # K % 256
+    assert f(fmt, 1, 8, 0, A, A, A) == cq.ERR_SHAPE
+    assert f(fmt, -1, 8, 256, A, A, A) == cq.ERR_INVALID_ARG
+    assert f(fmt, 1, 8, 256, A + 4, A, A) == cq.ERR_ALIGNMENT
+    assert f(fmt, 1, 8, 256, A, A + 8, A) == cq.ERR_ALIGNMENT
+    assert f(fmt, 1, 8, 256, A, A, A + 2) == cq.ERR_ALIGNMENT
+    assert f(fmt, 1, 8, 256, None, A, A) == cq.ERR_INVALID_ARG
+    assert f(fmt, 0, 8, 256, None, None, None) == cq.OK       # empty: a no-op
+    assert f(fmt, 3, 0, 256, None, None, None) == cq.OK
+
+
+def test_gemv_token_limit(L):
+    assert cq.cq_gemv(cq.Q8_0, 17, 8, 256, A, A, A) == cq.ERR_SHAPE
+    for fmt in (cq.Q4_0, cq.Q4_1, cq.Q8_0):
+        assert cq.cq_gemm(fmt, 4, 8, 256, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+
+
+def test_quantize_validation(L):
+    assert cq.cq_quantize_act(cq.Q4_0, 1, 256, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert cq.cq_quantize_act(cq.Q8_0, 1, 96, A, A) == cq.ERR_SHAPE
+    assert cq.cq_quantize_act(cq.Q8_K, 1, 256, A + 4, A) == cq.ERR_ALIGNMENT
+    assert cq.cq_quantize_act(cq.Q8_1, 0, 256, None, None) == cq.OK
+
+
+def test_moe_validation(L):
+    ws = cq.cq_moe_workspace_size(256, 2048, 1792, 32, 4)
+    assert ws > 0
+    st, so, ho, qo = cq.cq_moe_workspace_offsets(256, 2048, 1792, 32, 4)
+    assert st == cq.OK and so % 256 == 0 and ho % 256 == 0 and qo % 256 == 0
+    assert max(so, ho, qo) < ws
+    args = dict(T=4, K=256, F=256, E=8, topk=2)
+    need = cq.cq_moe_workspace_size(*args.values())
+
+    def call(fmt=cq.Q4_0, ws_bytes=need, ws=A, **kw):
+        a = {**args, **kw}
+        return cq.cq_moe_gemv(fmt, a["T"], a["K"], a["F"], a["E"], a["topk"], A, A, A, A, A, A, A, ws, ws_bytes)
+
+    assert call(fmt=cq.Q8_0) == cq.ERR_UNSUPPORTED_FORMAT
+    assert call(ws_bytes=need - 1) == cq.ERR_WORKSPACE
+    assert call(ws=None) == cq.ERR_WORKSPACE
+    assert call(ws=A + 16) == cq.ERR_ALIGNMENT      # workspace must be 256-byte aligned
+    assert call(K=300) == cq.ERR_SHAPE
+    assert call(F=200) == cq.ERR_SHAPE
+    assert call(topk=9) == cq.ERR_SHAPE             # topk > E
+    assert call(topk=0) == cq.ERR_SHAPE
+    assert call(E=300) == cq.ERR_SHAPE
+    assert call(T=0) == cq.OK

@@ -1,0 +1,147 @@
+"""cq_gemv / cq_gemm on the GPU against the CPU oracle.
+
+* Random GGUF weights and activations, every format, M = 1..16 tokens, ragged
+  N, K from one chunk to multi-segment rows: |y - y_ref| <= 2e-5 * sum|terms|.
+* Exact-arithmetic inputs (power-of-two scales, partial sums far below 2^24):
+  every fp32 evaluation order is exact, so y must equal the oracle bit for bit
+  -- this pins the integer block dots themselves through the real kernels.
+* Each row of a multi-token call equals the single-token call bit for bit, and
+  cq_gemm rows equal cq_gemv rows bit for bit (the fixed evaluation order).
+"""
+import numpy as np
+import pytest
+
+from gemm_gguf_block_gb300 import synth
+from helpers import W_NAMES, assert_within, cq_built, dev, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [2, 3, 8, 12]
+SHAPES = [(1, 256), (33, 512), (100, 768), (257, 2048), (64, 8448), (40, 16640)]
+
+
+def _case(orc, wfmt, N, K, M, seed):
+    rng = np.random.default_rng(seed)
+    W = synth.GEN[W_NAMES[wfmt]](rng, N, K)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    xq = orc.quantize(orc.ACT_FOR[wfmt], x)
+    return W, xq
+
+
+@pytest.mark.parametrize("wfmt", FMTS)
+@pytest.mark.parametrize("N,K", SHAPES)
+def test_gemv_matches_oracle(orc, wfmt, N, K):
+    torch = torch_cuda()
+    cq = cq_built()
+    W, xq = _case(orc, wfmt, N, K, 16, seed=wfmt * 7919 + N * 31 + K)
+    y_ref, at = orc.matmul(wfmt, W, xq, K)
+    Wd, xd = dev(torch, W), dev(torch, xq)
+    y1 = np.stack([cq.gemv_t(Wd, xd[m:m + 1], wfmt, K).cpu().numpy()[0] for m in range(16)])
+    assert_within(y1, y_ref, at, what=f"fmt {wfmt} M=1")
+    for M in (2, 3, 5, 8, 11, 16):
+        yM = cq.gemv_t(Wd, xd[:M], wfmt, K).cpu().numpy()
+        assert np.array_equal(yM.view(np.uint32), y1[:M].view(np.uint32)), f"M={M} rows differ from M=1"
+
+
+def _exact_case(wfmt, N, K, M, rng):
+    """Weights with scales 2^-8 (and mins / offsets on the same grid), activations
+    x = q * 2^-6 with |q| <= 127 and one 127 per block, so d_x = 2^-6 exactly."""
+    nb = K // 32
+    if wfmt == 2:
+        W = synth.pack_q4_0(np.full((N, nb), 0x1C00, np.uint16), rng.integers(0, 16, (N, K)))
+    elif wfmt == 8:
+        W = synth.pack_q8_0(np.full((N, nb), 0x1C00, np.uint16), rng.integers(-127, 128, (N, K)))
+    elif wfmt == 3:
+        m = (rng.integers(-16, 17, (N, nb)) * 2.0 ** -8).astype(np.float16).view(np.uint16)
+        W = synth.pack_q4_1(np.full((N, nb), 0x1C00, np.uint16), m, rng.integers(0, 16, (N, K)))
+    else:
+        ns = K // 256
+        W = synth.pack_q4_k(np.full((N, ns), 0x1C00, np.uint16), np.full((N, ns), 0x1800, np.uint16),
+                            rng.integers(0, 16, (N, ns, 8)), rng.integers(0, 16, (N, ns, 8)),
+                            rng.integers(0, 16, (N, K)))
+    q = rng.integers(-127, 128, (M, K))
+    bs = 256 if wfmt == 12 else 32
+    q.reshape(M, K // bs, bs)[:, :, 0] = 127
+    x = (q * 2.0 ** -6).astype(np.float32)
+    return W, x
+
+
+@pytest.mark.parametrize("wfmt", FMTS)
+@pytest.mark.parametrize("N,K,M", [(37, 512, 3), (300, 1024, 1), (64, 2048, 16)])
+def test_gemv_exact_arithmetic(orc, wfmt, N, K, M):
+    torch = torch_cuda()
+    cq = cq_built()
+    rng = np.random.default_rng(wfmt * 101 + K)
+    W, x = _exact_case(wfmt, N, K, M, rng)
+    xd = dev(torch, x)
+    xq = cq.quantize_act_t(xd, cq.ACT_FOR[wfmt])
+    xq_np = xq.cpu().numpy()
+    assert np.array_equal(xq_np, orc.quantize(orc.ACT_FOR[wfmt], x))
+    y_ref, at = orc.matmul(wfmt, W, xq_np, K)
+    # Every term is a multiple of 2^-15; with sum|terms| < 2^(24-15) any fp32
+    # evaluation order is exact, so the results must agree exactly.
+    assert at.max() < 2.0 ** 9, "test precondition: partial sums must stay exact in fp32"
+    y = cq.gemv_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
+    assert np.array_equal(y.astype(np.float64), y_ref)
+    if wfmt == 12:
+        y2 = cq.gemm_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
+        assert np.array_equal(y2.astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 100, 512), (64, 257, 2048), (130, 96, 4096)])
+def test_gemm_rows_equal_gemv(orc, M, N, K):
+    torch = torch_cuda()
+    cq = cq_built()
+    W, xq = _case(orc, 12, N, K, M, seed=M + N + K)
+    Wd, xd = dev(torch, W), dev(torch, xq)
+    y = cq.gemm_t(Wd, xd, 12, K).cpu().numpy()
+    y_ref, at = orc.matmul(12, W, xq, K)
+    assert_within(y, y_ref, at, what="gemm")
+    for m in sorted({0, 1, M // 2, M - 1}):
+        y1 = cq.gemv_t(Wd, xd[m:m + 1], 12, K).cpu().numpy()[0]
+        assert np.array_equal(y[m].view(np.uint32), y1.view(np.uint32)), f"row {m}"
+
+
+@pytest.mark.parametrize("wfmt", FMTS)
+def test_zero_scales_and_empty(orc, wfmt):
+    torch = torch_cuda()
+    cq = cq_built()
+    N, K, M = 50, 1024, 4
+    W, xq = _case(orc, wfmt, N, K, M, seed=5)
+    bs, bb = orc.BLOCK[wfmt]
+    Wz = W.copy().reshape(N, K // bs, bb)
+    Wz[:, :, 0:2] = 0
+    if wfmt in (3, 12):
+        Wz[:, :, 2:4] = 0
+    y = cq.gemv_t(dev(torch, Wz.reshape(N, -1)), dev(torch, xq), wfmt, K).cpu().numpy()
+    assert np.all(y == 0)
+    # N = 0 and M = 0 are no-ops that touch nothing
+    out = torch.full((4,), 7.0, device="cuda")
+    assert cq.cq_gemv(wfmt, 0, N, K, dev(torch, W).data_ptr(), 0, out.data_ptr()) == cq.OK
+    assert cq.cq_gemv(wfmt, M, 0, K, 0, dev(torch, xq).data_ptr(), out.data_ptr()) == cq.OK
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
+def test_output_guard_bytes(orc):
+    """Writes stay inside y: guard values around a ragged output survive."""
+    torch = torch_cuda()
+    cq = cq_built()
+    N, K, M = 77, 2048, 3
+    W, xq = _case(orc, 8, N, K, M, seed=9)
+    buf = torch.full((M * N + 64,), 12345.0, device="cuda")
+    y = buf[32:32 + M * N].view(M, N)
+    assert y.data_ptr() % 16 == 0
+    cq.gemv_t(dev(torch, W), dev(torch, xq), 8, K, out=y)
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:32] == 12345.0) and np.all(b[32 + M * N:] == 12345.0)
+    y_ref, at = orc.matmul(8, W, xq, K)
+    assert_within(y.cpu().numpy(), y_ref, at)
+
+
+def test_no_device_status(orc):
+    torch_cuda()
+    cq = cq_built()
+    st, code = cq.cq_read_global_status(1)
+    assert st == cq.OK and code == 0
