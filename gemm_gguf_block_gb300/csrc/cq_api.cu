@@ -20,6 +20,9 @@ bool g_dev_ready[MAX_DEVICES];
 cq::DeviceInfo g_dev[MAX_DEVICES];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Quantized activation rows: Q8_K rows are 292 bytes per 256 elements, so a
+// token's row is only 4-byte aligned; the kernels read activations in 32-bit words.
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 bool is_weight_fmt(int f) { return f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0 || f == CQ_Q4_K; }
 bool is_act_fmt(int f) { return f == CQ_Q8_0 || f == CQ_Q8_1 || f == CQ_Q8_K; }
@@ -96,7 +99,7 @@ cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     if (M > 16) return CQ_ERR_SHAPE;
     if (M == 0 || N == 0) return CQ_OK;
     if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
-    if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
+    if (!aligned16(W) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
     cq::DeviceInfo dev;
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
     cudaError_t e = cq::launch_gemv(dev, w_fmt, static_cast<int>(M), N, K, W, xq, y,
@@ -128,7 +131,7 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     if (st != CQ_OK) return st;
     if (M == 0 || N == 0) return CQ_OK;
     if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
-    if (!aligned16(W) || !aligned16(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
+    if (!aligned16(W) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
     cq::DeviceInfo dev;
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
     cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, static_cast<cudaStream_t>(stream));

@@ -23,8 +23,10 @@
  *   gate+up SwiGLU).
  *
  * Conventions for every call:
- *   - All data pointers are DEVICE pointers, 16-byte aligned, owned by the
- *     caller. The library never allocates, frees or synchronises on these
+ *   - All data pointers are DEVICE pointers owned by the caller, 16-byte
+ *     aligned, except quantized activations (xq) passed to cq_gemv/cq_gemm,
+ *     which need 4-byte alignment (a Q8_K row is 292 bytes per 256
+ *     elements). The library never allocates, frees or synchronises on these
  *     paths; every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) on the current device.
  *   - Matrices are row-major. A weight row holds the K/blk blocks of one
@@ -76,7 +78,7 @@ typedef enum {
     CQ_ERR_INVALID_ARG = 1,        /* NULL pointer or a negative size */
     CQ_ERR_UNSUPPORTED_FORMAT = 2, /* a format (pairing) this call does not take */
     CQ_ERR_SHAPE = 3,              /* K not a positive multiple of 256, M out of range, too large */
-    CQ_ERR_ALIGNMENT = 4,          /* a pointer not 16-byte aligned */
+    CQ_ERR_ALIGNMENT = 4,          /* a pointer not aligned as the call requires */
     CQ_ERR_WORKSPACE = 5,          /* workspace missing or smaller than required */
     CQ_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
     CQ_ERR_DEVICE_STATUS = 7,      /* a kernel reported bad input (see the status word) */

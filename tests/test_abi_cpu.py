@@ -49,7 +49,7 @@ def test_validation_before_launch(L, fn):
     assert f(fmt, 1, 8, 0, A, A, A) == cq.ERR_SHAPE
     assert f(fmt, -1, 8, 256, A, A, A) == cq.ERR_INVALID_ARG
     assert f(fmt, 1, 8, 256, A + 4, A, A) == cq.ERR_ALIGNMENT
-    assert f(fmt, 1, 8, 256, A, A + 8, A) == cq.ERR_ALIGNMENT
+    assert f(fmt, 1, 8, 256, A, A + 2, A) == cq.ERR_ALIGNMENT
     assert f(fmt, 1, 8, 256, A, A, A + 2) == cq.ERR_ALIGNMENT
     assert f(fmt, 1, 8, 256, None, A, A) == cq.ERR_INVALID_ARG
     assert f(fmt, 0, 8, 256, None, None, None) == cq.OK       # empty: a no-op
