@@ -34,6 +34,7 @@ SIGNATURES = {
     "cq_gemm": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "cq_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
     "cq_moe_gemv": (_I, [_I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "cq_moe_gemv_noalloc": (_I, [_I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P]),
     "cq_moe_workspace_offsets": (_I, [_I64, _I64, _I64, _I64, _I64, _P, _P, _P]),
     "cq_moe_read_status": (_I, [_P, _P, _P]),
     "cq_read_global_status": (_I, [_P, _I]),
@@ -92,6 +93,11 @@ def cq_moe_workspace_size(T, K, F, E, topk):
 def cq_moe_gemv(w_fmt, T, K, F, E, topk, W_gate, W_up, W_down, ids, route_w, xq, y, ws, ws_bytes, stream=0):
     return lib().cq_moe_gemv(w_fmt, T, K, F, E, topk, W_gate, W_up, W_down, ids, route_w, xq, y, ws,
                              ws_bytes, stream)
+
+
+def cq_moe_gemv_noalloc(w_fmt, T, K, F, E, topk, W_gate, W_up, W_down, ids, route_w, xq, y, stream=0):
+    """Routed FFN without a caller workspace (scratch in a fixed device array of the library)."""
+    return lib().cq_moe_gemv_noalloc(w_fmt, T, K, F, E, topk, W_gate, W_up, W_down, ids, route_w, xq, y, stream)
 
 
 def cq_moe_workspace_offsets(T, K, F, E, topk):

@@ -18,6 +18,7 @@
 //   3. down:    per (expert, 32-row tile of K): o = W_down . hq per pair.
 //   4. combine: y[t] = sum over slots in slot order of w * o (fma chain).
 #include <algorithm>
+#include <mutex>
 
 #include "chunk_dot.cuh"
 #include "cq_device.cuh"
@@ -360,3 +361,70 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
 }
 
 }  // namespace cq
+
+// ------------------------------------------------------ allocation-free entry
+//
+// cq_moe_gemv_noalloc: the routed-expert FFN for callers that cannot call
+// cudaMalloc and so cannot hand the library a workspace -- for example a
+// plugin whose host framework has already reserved the GPU's memory for its
+// own pool and exposes no way to ask for more, or a latency-critical decode
+// loop in which the device-wide synchronisation of cudaMalloc is not
+// acceptable. Its scratch space is a fixed array in device memory that is part
+// of this library's image: every GPU that loads libcq holds these
+// CQ_MOE_NOALLOC_MAX_BYTES until the process exits.
+namespace cq {
+namespace {
+
+static __device__ __align__(256) uint8_t g_moe_noalloc_scratch[CQ_MOE_NOALLOC_MAX_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+uint8_t* g_noalloc_ptr[NOALLOC_MAX_DEVICES];
+
+// Device address of the scratch array on the current device. In host code the
+// array's name stands for a host-side shadow, not for device memory, so the
+// address has to be asked of the runtime, once per device, with that device
+// current.
+cudaError_t noalloc_scratch(uint8_t** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_moe_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = static_cast<uint8_t*>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace cq
+
+extern "C" cq_status cq_moe_gemv_noalloc(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t E,
+                                         int64_t topk, const void* W_gate, const void* W_up, const void* W_down,
+                                         const int32_t* expert_ids, const float* route_w, const void* xq,
+                                         float* y, void* stream) {
+    if (w_fmt != CQ_Q4_0) return CQ_ERR_UNSUPPORTED_FORMAT;
+    if (T < 0 || K < 0 || F < 0 || E < 0 || topk < 0) return CQ_ERR_INVALID_ARG;
+    const size_t need = cq_moe_workspace_size(T, K, F, E, topk);
+    if (need == 0) return CQ_ERR_SHAPE;                       // a shape cq_moe_gemv rejects too
+    if (T == 0) return CQ_OK;
+    if (need > CQ_MOE_NOALLOC_MAX_BYTES) return CQ_ERR_WORKSPACE;
+    if (!W_gate || !W_up || !W_down || !expert_ids || !route_w || !xq || !y) return CQ_ERR_INVALID_ARG;
+    for (const void* q : {W_gate, W_up, W_down, static_cast<const void*>(expert_ids),
+                          static_cast<const void*>(route_w), xq, static_cast<const void*>(y)})
+        if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    uint8_t* scratch = nullptr;
+    if (cq::noalloc_scratch(&scratch) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_moe(dev, static_cast<int>(T), static_cast<int>(K), static_cast<int>(F),
+                                   static_cast<int>(E), static_cast<int>(topk), W_gate, W_up, W_down, expert_ids,
+                                   route_w, xq, y, scratch, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+

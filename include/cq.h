@@ -151,6 +151,35 @@ cq_status cq_moe_gemv(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t 
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Allocation-free variant of cq_moe_gemv. The pages have no counterpart: this
+ * is for callers that cannot call cudaMalloc and so cannot supply a
+ * workspace -- a plugin whose host framework owns all device memory through
+ * its own pool, or a latency-critical loop that cannot afford the device-wide
+ * synchronisation of an allocation. The caller still passes every input and
+ * the output; the scratch space is a fixed array of CQ_MOE_NOALLOC_MAX_BYTES
+ * in the library's device image, held on every GPU that loads the library
+ * until the process exits, and shared by every call of this function.
+ * - Same arguments, arithmetic and results as cq_moe_gemv (without the
+ *   workspace arguments); the array keeps the previous call's contents, and
+ *   the call clears what must start at zero (its status word) itself.
+ * - Shapes whose cq_moe_workspace_size exceeds CQ_MOE_NOALLOC_MAX_BYTES return
+ *   CQ_ERR_WORKSPACE before any launch; shapes cq_moe_gemv rejects return
+ *   CQ_ERR_SHAPE. It calls no cudaMalloc, cudaFree or other allocating routine.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - Calls whose executions overlap on the GPU (two streams, or two host
+ *   threads on one device) race on the shared array: serialise them.
+ * - Expert-id errors are still skipped as in cq_moe_gemv; their status word
+ *   lives in the shared array and is not exposed by this call.
+ */
+#define CQ_MOE_NOALLOC_MAX_BYTES (24u << 20)
+cq_status cq_moe_gemv_noalloc(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk,
+                              const void* W_gate, const void* W_up, const void* W_down,
+                              const int32_t* expert_ids, const float* route_w, const void* xq, float* y,
+                              void* stream);
+
+/*
  * Byte offsets inside the MoE workspace, for inspection by tests: the status
  * word (int32), the hidden activations h (fp32 [T*topk][F], in (token, slot)
  * order) and their Q8_0 quantisation hq ([T*topk] rows of F/32 blocks).
