@@ -2,36 +2,43 @@
 //
 // cera README "Quantization": integer GEMV over quantized weights with
 // activations quantized to 8 bits; alice-llm "The GPU Optimization Journey"
-// phases 1.5-2 (fused dequant-matvec, register reductions) and "Batch-4
-// Speculative Decoding" (weights decoded once, one accumulator per token);
-// cera README "Other features" (the LM head projected for all verified
-// positions in one pass).
+// phases 1.5-2 (fused dequant-matvec, register-level reductions) and
+// "Batch-4 Speculative Decoding" (weights decoded once, one accumulator per
+// token); cera README "Other features" (the LM head projected for all
+// verified positions in one pass, so it is read once per round).
 //
-// Layout of the work. A row of K elements is nc = K/256 chunks (eight
-// 32-blocks, or one Q4_K superblock). A warp owns "items": R consecutive rows
-// (R = 32/nc when a row has fewer than 32 chunks) or, for very long rows, one
-// row segment of up to SEGC chunks. An item is contiguous in memory, so one
-// bulk copy (cp.async.bulk, the one-dimensional TMA engine) moves it into a
-// per-warp ring of shared-memory stages; the copy for item i+S is issued as
-// soon as item i has been read, so each warp keeps up to S items in flight.
-// Each lane takes whole chunks of the item (task t -> row t/segc, chunk
-// t%segc), unpacks nibbles in registers and forms exact int32 block dots with
-// dp4a against the activations, which the CTA stages once in shared memory
-// (chunk pitch padded to an odd number of 16-byte units so that the lanes'
-// 128-bit loads do not collide on banks). The per-chunk fp32 values go to a
-// small per-warp buffer; lane (r, m) then adds them in increasing k, which is
-// the library's fixed evaluation order (see include/cq.h).
+// The work. A weight row of K elements is nc chunks: 128 elements (four
+// 32-blocks) for Q4_0 / Q4_1 / Q8_0, one 256-element superblock for Q4_K.
+// A warp owns "items" of at most 32 chunks: R = 32/nc whole rows when a row
+// is shorter than 32 chunks, else a 32-chunk segment of one row. An item is
+// one contiguous byte range, so a single bulk copy (cp.async.bulk, the
+// one-dimensional TMA engine) lands it in the warp's ring of shared-memory
+// stages; the copy of item i+S is issued as soon as item i has been read.
+// Lane l takes chunk l of the item: it unpacks its weights in registers and
+// forms exact int32 block dots with dp4a against the activations, which the
+// CTA has staged once in shared memory in an aligned split layout (quants on
+// 16-byte boundaries, scales in the padding, chunk pitch an odd number of
+// 16-byte units so the lanes' 128-bit loads do not collide). Chunk values go
+// to a small per-warp buffer; every B rows, lane (m, r) adds row r's values
+// for token m in increasing k -- the fixed evaluation order of include/cq.h.
 #include <algorithm>
+#include <cstdlib>
 
-#include "chunk_dot.cuh"
 #include "cq_device.cuh"
 #include "cq_internal.h"
 
 namespace cq {
 namespace {
 
-constexpr int WPC_MAX = 16;            // warps per CTA (upper bound)
-constexpr int SEGC_MAX = 64;           // chunks per segment of a long row
+constexpr int WPC_MAX = 16;       // warps per CTA (one CTA per SM)
+constexpr int CBUF_FLOATS = 512;  // per-warp buffer of chunk values (2 KB)
+
+// Weight chunk bytes, chunk elements, staged activation chunk pitch.
+template <int WF> struct G;
+template <> struct G<CQ_Q8_0> { static constexpr int WCH = 136, CE = 128, ACP = 144; };
+template <> struct G<CQ_Q4_0> { static constexpr int WCH = 72, CE = 128, ACP = 144; };
+template <> struct G<CQ_Q4_1> { static constexpr int WCH = 80, CE = 128, ACP = 176; };
+template <> struct G<CQ_Q4_K> { static constexpr int WCH = 144, CE = 256, ACP = 304; };
 
 struct GemvParams {
     const uint8_t* W;
@@ -41,181 +48,464 @@ struct GemvParams {
     int64_t N;
     int64_t row_bytes;
     int M;
-    int nc;            // chunks per row
-    int R;             // rows per item
-    int segc;          // chunks per item segment
-    int nseg;          // segments per row (R == 1 whenever nseg > 1)
+    int nc;           // chunks per row
+    int R;            // rows per item
+    int segc;         // chunks per item
+    int nseg;         // items per row group (R == 1 whenever nseg > 1)
+    int B;            // rows per batch of sequential sums (a multiple of R)
     int stages;
-    int stage_bytes;   // bytes reserved per stage (multiple of 128)
-    int warp_bytes;    // bytes per warp region
-    int act_bytes;     // bytes of the staged activations (multiple of 128)
-    int tok_pitch;     // bytes between tokens in the staged activations
+    int stage_bytes;
+    int warp_bytes;
+    int act_bytes;
+    int tok_pitch;    // bytes per token of staged activations
 };
+
+// Exact float of an int with |i| < 2^22: the bits of 1.5 * 2^23 + i, minus 1.5 * 2^23.
+__device__ __forceinline__ float i2f_exact(int i) {
+    return __fsub_rn(__int_as_float(0x4B400000 + i), 12582912.0f);
+}
+
+template <int N>
+__device__ __forceinline__ void lds64(const uint8_t* p, uint32_t (&u)[2 * N]) {
+    const uint2* q = reinterpret_cast<const uint2*>(p);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const uint2 v = q[i];
+        u[2 * i] = v.x;
+        u[2 * i + 1] = v.y;
+    }
+}
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// ------------------------------------------------------- staging of activations
+// Q8_0 / Q8_1 chunk of 4 blocks -> [qs 128 B][d0..d3 fp32] (Q8_1: [d,s] pairs);
+// Q8_K superblock -> [qs 256 B][d fp32 @256][8 int32 bsum pairs @272].
+template <int WF>
+__device__ void stage_activations(const GemvParams& p, uint8_t* act) {
+    const int nthr = blockDim.x;
+    if constexpr (WF == CQ_Q4_K) {
+        const int ns = p.nc;
+        const int words = p.M * ns * 73;          // 292 bytes per superblock
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.xq);
+        for (int i = threadIdx.x; i < words; i += nthr) {
+            const int sb = i / 73, w = i - sb * 73;     // superblock (over tokens), word in it
+            const int m = sb / ns, c = sb - m * ns;
+            uint8_t* dst = act + m * p.tok_pitch + c * G<WF>::ACP;
+            const uint32_t v = src[i];
+            if (w == 0) {
+                *reinterpret_cast<uint32_t*>(dst + 256) = v;
+            } else if (w <= 64) {
+                *reinterpret_cast<uint32_t*>(dst + 4 * (w - 1)) = v;
+            } else {
+                const int j = w - 65;                    // bsum pair j = bsum[2j] + bsum[2j+1]
+                const int pair = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
+                                 static_cast<int>(static_cast<int16_t>(v >> 16));
+                *reinterpret_cast<int*>(dst + 272 + 4 * j) = pair;
+            }
+        }
+    } else {
+        constexpr int BB = WF == CQ_Q4_1 ? 36 : 34;     // Q8_1 or Q8_0 block bytes
+        constexpr int QO = WF == CQ_Q4_1 ? 4 : 2;       // quant offset in the block
+        const int nblk = p.M * p.nc * 4;
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(p.xq);
+        for (int i = threadIdx.x; i < nblk; i += nthr) {
+            const int m = i / (p.nc * 4), r = i - m * p.nc * 4;
+            const int c = r >> 2, b = r & 3;
+            const uint16_t* s = src + static_cast<int64_t>(i) * (BB / 2);
+            uint8_t* dst = act + m * p.tok_pitch + c * G<WF>::ACP;
+            uint32_t* q = reinterpret_cast<uint32_t*>(dst + 32 * b);
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                q[w] = static_cast<uint32_t>(s[QO / 2 + 2 * w]) | (static_cast<uint32_t>(s[QO / 2 + 2 * w + 1]) << 16);
+            if constexpr (WF == CQ_Q4_1) {
+                reinterpret_cast<float*>(dst + 128)[2 * b] = h2f(s[0]);
+                reinterpret_cast<float*>(dst + 128)[2 * b + 1] = h2f(s[1]);
+            } else {
+                reinterpret_cast<float*>(dst + 128)[b] = h2f(s[0]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------- chunk values
+// wc: weight chunk in shared memory (8-byte aligned; 16 for Q4_K);
+// xa: staged activations of the same chunk for token 0, token m at + m * tp.
+
+template <int MT>
+__device__ __forceinline__ void chunk_q8_0(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    uint32_t w[34];
+    lds64<17>(wc, w);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) c[m] = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int o = 34 * b;                    // block offset in the chunk (0, 34, 68, 102)
+        const int base = o >> 2;
+        const bool odd = (o & 2) != 0;
+        const float dw = h2f(odd ? (w[base] >> 16) : w[base]);
+        int q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            q[i] = static_cast<int>(odd ? w[base + 1 + i] : __funnelshift_r(w[base + i], w[base + i + 1], 16));
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const uint8_t* xm = xa + m * tp;
+                const uint4 a0 = lds128(xm + 32 * b), a1 = lds128(xm + 32 * b + 16);
+                const float dx = reinterpret_cast<const float*>(xm + 128)[b];
+                int s = __dp4a(q[0], static_cast<int>(a0.x), 0);
+                s = __dp4a(q[1], static_cast<int>(a0.y), s);
+                s = __dp4a(q[2], static_cast<int>(a0.z), s);
+                s = __dp4a(q[3], static_cast<int>(a0.w), s);
+                s = __dp4a(q[4], static_cast<int>(a1.x), s);
+                s = __dp4a(q[5], static_cast<int>(a1.y), s);
+                s = __dp4a(q[6], static_cast<int>(a1.z), s);
+                s = __dp4a(q[7], static_cast<int>(a1.w), s);
+                c[m] = __fmaf_rn(__fmul_rn(dw, dx), i2f_exact(s), c[m]);
+            }
+        }
+    }
+}
+
+template <int MT>
+__device__ __forceinline__ void chunk_q4_0(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    uint32_t w[18];
+    lds64<9>(wc, w);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) c[m] = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int o = 18 * b;                    // 0, 18, 36, 54
+        const int base = o >> 2;
+        const bool odd = (o & 2) != 0;
+        const float dw = h2f(odd ? (w[base] >> 16) : w[base]);
+        int lo[4], hi[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t q = odd ? w[base + 1 + i] : __funnelshift_r(w[base + i], w[base + i + 1], 16);
+            lo[i] = nib_minus8(q & 0x0f0f0f0fu);
+            hi[i] = nib_minus8((q >> 4) & 0x0f0f0f0fu);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const uint8_t* xm = xa + m * tp;
+                const uint4 a0 = lds128(xm + 32 * b), a1 = lds128(xm + 32 * b + 16);
+                const float dx = reinterpret_cast<const float*>(xm + 128)[b];
+                int s = __dp4a(lo[0], static_cast<int>(a0.x), 0);
+                s = __dp4a(lo[1], static_cast<int>(a0.y), s);
+                s = __dp4a(lo[2], static_cast<int>(a0.z), s);
+                s = __dp4a(lo[3], static_cast<int>(a0.w), s);
+                s = __dp4a(hi[0], static_cast<int>(a1.x), s);
+                s = __dp4a(hi[1], static_cast<int>(a1.y), s);
+                s = __dp4a(hi[2], static_cast<int>(a1.z), s);
+                s = __dp4a(hi[3], static_cast<int>(a1.w), s);
+                c[m] = __fmaf_rn(__fmul_rn(dw, dx), i2f_exact(s), c[m]);
+            }
+        }
+    }
+}
+
+template <int MT>
+__device__ __forceinline__ void chunk_q4_1(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    uint32_t w[20];
+    lds64<10>(wc, w);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) c[m] = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int base = 5 * b;                  // 20-byte blocks: always word aligned
+        const float dw = h2f(w[base]);
+        const float mw = h2f(w[base] >> 16);
+        int lo[4], hi[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t q = w[base + 1 + i];
+            lo[i] = static_cast<int>(q & 0x0f0f0f0fu);
+            hi[i] = static_cast<int>((q >> 4) & 0x0f0f0f0fu);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const uint8_t* xm = xa + m * tp;
+                const uint4 a0 = lds128(xm + 32 * b), a1 = lds128(xm + 32 * b + 16);
+                const float2 ds = reinterpret_cast<const float2*>(xm + 128)[b];
+                int s = __dp4a(lo[0], static_cast<int>(a0.x), 0);
+                s = __dp4a(lo[1], static_cast<int>(a0.y), s);
+                s = __dp4a(lo[2], static_cast<int>(a0.z), s);
+                s = __dp4a(lo[3], static_cast<int>(a0.w), s);
+                s = __dp4a(hi[0], static_cast<int>(a1.x), s);
+                s = __dp4a(hi[1], static_cast<int>(a1.y), s);
+                s = __dp4a(hi[2], static_cast<int>(a1.z), s);
+                s = __dp4a(hi[3], static_cast<int>(a1.w), s);
+                const float cm = __fmaf_rn(__fmul_rn(dw, ds.x), i2f_exact(s), c[m]);
+                c[m] = __fmaf_rn(mw, ds.y, cm);
+            }
+        }
+    }
+}
+
+// Six-bit scale and min of sub-block j from the twelve scale bytes s0|s1|s2.
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& mn) {
+    auto byte = [](uint32_t w, int i) { return static_cast<int>((w >> (8 * i)) & 0xffu); };
+    if (j < 4) {
+        sc = byte(s0, j) & 63;
+        mn = byte(s1, j) & 63;
+    } else {
+        sc = (byte(s2, j - 4) & 15) | ((byte(s0, j - 4) >> 6) << 4);
+        mn = (byte(s2, j - 4) >> 4) | ((byte(s1, j - 4) >> 6) << 4);
+    }
+}
+
+template <int MT>
+__device__ __forceinline__ void chunk_q4_k(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = lds128(wc + 16 * i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    const float d = h2f(w[0]);
+    const float dmin = h2f(w[0] >> 16);
+    int isc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) isc[m] = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int sc, mn;
+        q4k_scale_min(w[1], w[2], w[3], j, sc, mn);
+        int nib[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t q = w[4 + 8 * (j >> 1) + i];
+            nib[i] = static_cast<int>((j & 1) ? ((q >> 4) & 0x0f0f0f0fu) : (q & 0x0f0f0f0fu));
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const uint8_t* xm = xa + m * tp;
+                const uint4 a0 = lds128(xm + 32 * j), a1 = lds128(xm + 32 * j + 16);
+                int s = __dp4a(nib[0], static_cast<int>(a0.x), 0);
+                s = __dp4a(nib[1], static_cast<int>(a0.y), s);
+                s = __dp4a(nib[2], static_cast<int>(a0.z), s);
+                s = __dp4a(nib[3], static_cast<int>(a0.w), s);
+                s = __dp4a(nib[4], static_cast<int>(a1.x), s);
+                s = __dp4a(nib[5], static_cast<int>(a1.y), s);
+                s = __dp4a(nib[6], static_cast<int>(a1.z), s);
+                s = __dp4a(nib[7], static_cast<int>(a1.w), s);
+                isc[m] += sc * s;
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < M) {
+            const uint8_t* xm = xa + m * tp;
+            const float dx = *reinterpret_cast<const float*>(xm + 256);
+            const uint4 p0 = lds128(xm + 272), p1 = lds128(xm + 288);
+            const int pr[8] = {static_cast<int>(p0.x), static_cast<int>(p0.y), static_cast<int>(p0.z),
+                               static_cast<int>(p0.w), static_cast<int>(p1.x), static_cast<int>(p1.y),
+                               static_cast<int>(p1.z), static_cast<int>(p1.w)};
+            int im = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                int sc, mn;
+                q4k_scale_min(w[1], w[2], w[3], j, sc, mn);
+                im += mn * pr[j];
+            }
+            const float a = __fmul_rn(dx, d);
+            const float bm = __fmul_rn(dx, dmin);
+            c[m] = __fmaf_rn(a, __int2float_rn(isc[m]), -__fmul_rn(bm, __int2float_rn(im)));
+        }
+    }
+}
+
+template <int WF, int MT>
+__device__ __forceinline__ void chunk_value(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    if constexpr (WF == CQ_Q8_0) chunk_q8_0<MT>(wc, xa, tp, M, c);
+    else if constexpr (WF == CQ_Q4_0) chunk_q4_0<MT>(wc, xa, tp, M, c);
+    else if constexpr (WF == CQ_Q4_1) chunk_q4_1<MT>(wc, xa, tp, M, c);
+    else chunk_q4_k<MT>(wc, xa, tp, M, c);
+}
 
 // ------------------------------------------------------------------ kernel
 template <int MT> constexpr int wpc_limit() { return MT <= 4 ? WPC_MAX : WPC_MAX / 2; }
 
 template <int WF, int MT>
 __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvParams p) {
-    using F = Fmt<WF>;
+    using F = G<WF>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wpc = blockDim.x >> 5;
-
-    // Stage this call's activations once per CTA: token m, chunk j at
-    // m * tok_pitch + j * ACP (the chunk bytes, then padding).
-    {
-        const int nc = p.nc;
-        const int words_per_chunk = F::ACH / 4;
-        const int total = p.M * nc * words_per_chunk;
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(p.xq);
-        for (int i = threadIdx.x; i < total; i += blockDim.x) {
-            const int m = i / (nc * words_per_chunk);
-            const int r = i - m * nc * words_per_chunk;
-            const int j = r / words_per_chunk, w = r - j * words_per_chunk;
-            *reinterpret_cast<uint32_t*>(smem + m * p.tok_pitch + j * F::ACP + 4 * w) =
-                src[(static_cast<int64_t>(m) * nc + j) * words_per_chunk + w];
-        }
-    }
-    __syncthreads();
-
     const int64_t groups = (p.N + p.R - 1) / p.R;
     const int64_t wtot = static_cast<int64_t>(gridDim.x) * wpc;
     const int64_t wid = static_cast<int64_t>(blockIdx.x) * wpc + warp;
-    if (wid >= groups) return;
-    const int64_t nsteps = ((groups - 1 - wid) / wtot + 1) * p.nseg;
+    const bool active = wid < groups;
+    const int64_t nsteps = active ? ((groups - 1 - wid) / wtot + 1) * p.nseg : 0;
 
+    uint8_t* act = smem;
     uint8_t* region = smem + p.act_bytes + warp * p.warp_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(region);
     uint8_t* stages = region + 128;
     float* cbuf = reinterpret_cast<float*>(stages + p.stages * p.stage_bytes);
     const int S = p.stages;
-
-    if (lane == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
     const uint64_t policy = policy_evict_first();
 
-    // Issue the copy of step k into stage k % S (lane 0 only).
-    auto issue = [&](int64_t k) {
-        const int64_t g = wid + (k / p.nseg) * wtot;
-        const int seg = static_cast<int>(k % p.nseg);
-        const int64_t row0 = g * p.R;
+    // The warp's steps walk (group, segment) pairs: group wid, wid + wtot, ...,
+    // segments 0..nseg-1 of each. Two cursors walk them without divisions: one
+    // for the copies (ahead by S steps) and one for the compute.
+    struct Cursor {
+        int64_t g;
+        int seg;
+        int stage;
+        uint32_t phase;
+    };
+    auto advance = [&](Cursor& c) {
+        if (++c.seg == p.nseg) { c.seg = 0; c.g += wtot; }
+        if (++c.stage == S) { c.stage = 0; c.phase ^= 1u; }
+    };
+    auto issue = [&](const Cursor& c) {
+        const int64_t row0 = c.g * p.R;
         uint32_t bytes;
         const uint8_t* src;
         if (p.nseg == 1) {
-            const int64_t rows = min(static_cast<int64_t>(p.R), p.N - row0);
-            bytes = static_cast<uint32_t>(rows * p.row_bytes);
+            bytes = static_cast<uint32_t>(min(static_cast<int64_t>(p.R), p.N - row0) * p.row_bytes);
             src = p.W + row0 * p.row_bytes;
         } else {
-            const int c0 = seg * p.segc;
-            const int cn = min(p.segc, p.nc - c0);
-            bytes = static_cast<uint32_t>(cn * F::CH);
-            src = p.W + row0 * p.row_bytes + static_cast<int64_t>(c0) * F::CH;
+            const int c0 = c.seg * 32;
+            bytes = static_cast<uint32_t>(min(32, p.nc - c0) * F::WCH);
+            src = p.W + row0 * p.row_bytes + static_cast<int64_t>(c0) * F::WCH;
         }
-        uint64_t* bar = &bars[k % S];
+        uint64_t* bar = &bars[c.stage];
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(stages + (k % S) * p.stage_bytes, src, bytes, bar, policy);
+        bulk_g2s(stages + c.stage * p.stage_bytes, src, bytes, bar, policy);
     };
 
-    if (lane == 0)
-        for (int64_t k = 0; k < min(static_cast<int64_t>(S), nsteps); ++k) issue(k);
-
-    float ycarry = 0.0f;
-    bool failed = false;
-    int64_t kfail = 0;
-    for (int64_t k = 0; k < nsteps; ++k) {
-        const int s = static_cast<int>(k % S);
-        const uint32_t parity = static_cast<uint32_t>((k / S) & 1);
-        const bool ok = mbar_wait_bounded(&bars[s], parity, WAIT_LIMIT_NS);
-        if (!__all_sync(0xffffffffu, ok)) { failed = true; kfail = k; break; }
-
-        const int64_t g = wid + (k / p.nseg) * wtot;
-        const int seg = static_cast<int>(k % p.nseg);
-        const int64_t row0 = g * p.R;
-        const int c0 = seg * p.segc;
-        const int cn = min(p.segc, p.nc - c0);
-        const int rows_valid = static_cast<int>(min(static_cast<int64_t>(p.R), p.N - row0));
-        const int ntasks = p.R * cn;
-        const uint8_t* st = stages + s * p.stage_bytes;
-        for (int t = lane; t < ntasks; t += 32) {
-            const int r = t / cn, j = t - r * cn;
-            if (r < rows_valid) {
-                float c[MT];
-                chunk_dot<WF, MT>(st + r * static_cast<int>(p.row_bytes) * (p.nseg == 1) + j * F::CH,
-                                  smem + (c0 + j) * F::ACP, p.tok_pitch, p.M, c);
-#pragma unroll
-                for (int m = 0; m < MT; ++m)
-                    if (m < p.M) cbuf[m * ntasks + t] = c[m];
-            }
+    // Start the weight stream first; stage the activations while it flies.
+    Cursor ic{wid, 0, 0, 0u};
+    int64_t issued = 0;
+    if (active && lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+        for (; issued < min(static_cast<int64_t>(S), nsteps); ++issued) {
+            issue(ic);
+            advance(ic);
         }
-        __syncwarp();
-        if (lane == 0 && k + S < nsteps) issue(k + S);
-        // Fixed order: y = y + c over the chunks in increasing k.
-        for (int q = lane; q < p.R * p.M; q += 32) {
-            const int r = q / p.M, m = q - r * p.M;
-            float acc = seg == 0 ? 0.0f : ycarry;
-            const float* cb = cbuf + m * ntasks + r * cn;
-            for (int j = 0; j < cn; ++j) acc = __fadd_rn(acc, cb[j]);
-            if (seg == p.nseg - 1) {
-                if (r < rows_valid) p.y[static_cast<int64_t>(m) * p.N + row0 + r] = acc;
-            } else {
-                ycarry = acc;
-            }
-        }
-        __syncwarp();
     }
-    if (failed) {
+    stage_activations<WF>(p, act);
+    __syncthreads();
+    if (!active) return;
+
+    // This lane's chunk in an item: row lr, chunk lj (one division per launch).
+    const int lr = p.nseg == 1 ? lane / p.nc : 0;
+    const int lj = p.nseg == 1 ? lane - lr * p.nc : lane;
+    Cursor cc{wid, 0, 0, 0u};
+    int64_t kfail = -1;
+    int slot0 = 0;          // batch slots filled so far (R per row group)
+    for (int64_t k = 0; k < nsteps; ++k) {
+        const bool ok = mbar_wait_bounded(&bars[cc.stage], cc.phase, WAIT_LIMIT_NS);
+        if (!__all_sync(0xffffffffu, ok)) { kfail = k; break; }
+
+        const int64_t row0 = cc.g * p.R;
+        const int c0 = cc.seg * 32;
+        const int cn = p.nseg == 1 ? p.nc : min(32, p.nc - c0);
+        const int rows_valid = static_cast<int>(min(static_cast<int64_t>(p.R), p.N - row0));
+        const uint8_t* st = stages + cc.stage * p.stage_bytes;
+        if (lr < rows_valid && lj < cn) {
+            float c[MT];
+            chunk_value<WF, MT>(st + lr * static_cast<int>(p.row_bytes) + lj * F::WCH,
+                                act + (c0 + lj) * F::ACP, p.tok_pitch, p.M, c);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < p.M) cbuf[(m * p.B + slot0 + lr) * p.nc + c0 + lj] = c[m];
+        }
+        __syncwarp();
+        if (lane == 0 && issued < nsteps) {
+            issue(ic);
+            advance(ic);
+            ++issued;
+        }
+        const int64_t g = cc.g;
+        const bool row_done = cc.seg == p.nseg - 1;
+        advance(cc);
+        if (row_done) {
+            slot0 += p.R;
+            if (slot0 == p.B || k == nsteps - 1) {
+                // Fixed order: y = 0, then y = y + c over the row's chunks in increasing k.
+                // Slot r holds row (r % R) of group g - ((slot0 - 1 - r) / R) * wtot.
+                for (int q = lane; q < p.M * slot0; q += 32) {
+                    const int m = q / slot0, r = q - m * slot0;
+                    const float* cb = cbuf + (m * p.B + r) * p.nc;
+                    float acc = 0.0f;
+#pragma unroll 8
+                    for (int j = 0; j < p.nc; ++j) acc = __fadd_rn(acc, cb[j]);
+                    const int back = (slot0 - 1 - r) / p.R;
+                    const int64_t row = (g - back * wtot) * p.R + (r - (r / p.R) * p.R);
+                    if (row < p.N) p.y[static_cast<int64_t>(m) * p.N + row] = acc;
+                }
+                slot0 = 0;
+                __syncwarp();
+            }
+        }
+    }
+    if (kfail >= 0) {
         // A copy never completed: record it, then give the copies still in
         // flight (bounded) time to land before the CTA's shared memory goes.
         if (lane == 0) {
             atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
-            for (int64_t k = kfail; k < min(kfail + S, nsteps); ++k)
-                (void)mbar_wait_bounded(&bars[k % S], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS / 8);
+            for (int64_t k = kfail; k < issued; ++k) {
+                (void)mbar_wait_bounded(&bars[cc.stage], cc.phase, WAIT_LIMIT_NS / 8);
+                advance(cc);
+            }
         }
         __syncwarp();
     }
 }
 
+// Ring depth: CQ_GEMV_STAGES (2..4) overrides the choice, for tuning runs.
+int stage_override() {
+    static const int v = [] {
+        const char* e = std::getenv("CQ_GEMV_STAGES");
+        const int s = e ? std::atoi(e) : 0;
+        return (s >= 2 && s <= 4) ? s : 0;
+    }();
+    return v;
+}
+
 template <int WF, int MT>
-cudaError_t launch_typed(const DeviceInfo& dev, const GemvParams& base, int64_t groups, cudaStream_t s) {
-    GemvParams p = base;
-    const int smem_budget = std::min(dev.smem_optin, 227 * 1024) - 1024;
-    const int per_warp_fixed = 128 + p.M * p.R * p.segc * 4;
-    // Shared memory per warp for S stages; pick the largest warp count (<= 16)
-    // that leaves at least two stages per warp, preferring three or four.
-    int S = 4;
-    int wpc = 0;
-    for (; S >= 2; --S) {
-        p.stages = S;
-        p.warp_bytes = (per_warp_fixed + S * p.stage_bytes + 127) / 128 * 128;
-        wpc = std::min(wpc_limit<MT>(), (smem_budget - p.act_bytes) / p.warp_bytes);
-        if (wpc >= 4 || (S == 2 && wpc >= 1)) break;
+cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cudaStream_t s) {
+    const int lim = std::min(dev.smem_optin, 227 * 1024);
+    const int budget = lim - 1024;
+    // Shared memory per warp: barriers, S stages, chunk-value buffer. Prefer
+    // at least three stages when that still leaves twelve warps or more.
+    auto warp_bytes = [&](int S) { return (128 + S * p.stage_bytes + 4 * CBUF_FLOATS + 127) / 128 * 128; };
+    auto warps_for = [&](int S) { return std::min(wpc_limit<MT>(), (budget - p.act_bytes) / warp_bytes(S)); };
+    int S = stage_override();
+    if (S == 0) {
+        S = 4;
+        while (S > 2 && warps_for(S) < std::min(12, wpc_limit<MT>())) --S;
     }
+    int wpc = warps_for(S);
     if (wpc < 1) return cudaErrorInvalidConfiguration;
-    wpc = std::min(wpc, wpc_limit<MT>());
-    // Spread the groups over all SMs before stacking warps on one SM.
-    const int64_t want_wpc = std::max<int64_t>(1, (groups + dev.sm_count - 1) / dev.sm_count);
-    wpc = static_cast<int>(std::min<int64_t>(wpc, want_wpc));
-    // Balance: every warp gets the same number of groups (give or take one).
+    p.stages = S;
+    p.warp_bytes = warp_bytes(S);
+    // Balance: every warp gets the same number of row groups, give or take one,
+    // spread over all SMs before warps are stacked on one SM.
     const int64_t wmax = static_cast<int64_t>(dev.sm_count) * wpc;
     const int64_t per_warp = (groups + wmax - 1) / wmax;
     const int64_t warps = (groups + per_warp - 1) / per_warp;
+    wpc = static_cast<int>(std::min<int64_t>(wpc, (warps + dev.sm_count - 1) / dev.sm_count));
     const unsigned grid = static_cast<unsigned>((warps + wpc - 1) / wpc);
     const int smem = p.act_bytes + wpc * p.warp_bytes;
-    // Raise the kernel's dynamic shared-memory limit once per device.
     static int raised[64] = {};
     int devid = 0;
     cudaError_t e = cudaGetDevice(&devid);
     if (e != cudaSuccess) return e;
-    if (devid < 64 && raised[devid] < smem) {
-        e = cudaFuncSetAttribute(gemv_kernel<WF, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 std::min(dev.smem_optin, 227 * 1024));
+    if (devid >= 64 || raised[devid] < lim) {
+        e = cudaFuncSetAttribute(gemv_kernel<WF, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
         if (e != cudaSuccess) return e;
-        raised[devid] = std::min(dev.smem_optin, 227 * 1024);
+        if (devid < 64) raised[devid] = lim;
     }
     gemv_kernel<WF, MT><<<grid, wpc * 32, smem, s>>>(p);
     return cudaGetLastError();
@@ -229,57 +519,64 @@ cudaError_t launch_fmt(const DeviceInfo& dev, const GemvParams& p, int64_t group
     return launch_typed<WF, 16>(dev, p, groups, s);
 }
 
+template <int WF>
+cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, const void* W, const void* xq,
+                            float* y, cudaStream_t s) {
+    using F = G<WF>;
+    const int nc = static_cast<int>(K / F::CE);
+    if (nc > CBUF_FLOATS) return cudaErrorInvalidValue;
+    const int64_t row_bytes = static_cast<int64_t>(nc) * F::WCH;
+    const int act_row = static_cast<int>(K / CHUNK_ELEMS) * achunk_bytes(act_fmt_for(WF));
+    const int tok_pitch = nc * F::ACP;
+    // Tokens per launch: staged activations within 100 KB, and the chunk-value
+    // buffer holding at least one row of every token.
+    int max_tok = std::max(1, std::min(M, (100 * 1024) / tok_pitch));
+    max_tok = std::min(max_tok, std::max(1, CBUF_FLOATS / nc));
+    for (int m0 = 0; m0 < M; m0 += max_tok) {
+        GemvParams p{};
+        p.M = std::min(max_tok, M - m0);
+        p.W = static_cast<const uint8_t*>(W);
+        p.xq = static_cast<const uint8_t*>(xq) + static_cast<int64_t>(m0) * act_row;
+        p.y = y + static_cast<int64_t>(m0) * N;
+        p.status = dev.status;
+        p.N = N;
+        p.row_bytes = row_bytes;
+        p.nc = nc;
+        if (nc <= 32) {
+            p.R = 32 / nc;
+            p.segc = nc;
+            p.nseg = 1;
+        } else {
+            p.R = 1;
+            p.segc = 32;
+            p.nseg = (nc + 31) / 32;
+        }
+        p.stage_bytes = static_cast<int>(((p.nseg == 1 ? p.R * row_bytes : int64_t(32) * F::WCH) + 127) / 128 * 128);
+        // Rows per batch of sequential sums: a multiple of R, buffer within CBUF_FLOATS.
+        const int rows_fit = CBUF_FLOATS / (p.M * nc);
+        p.B = std::max(p.R, std::min(32, rows_fit) / p.R * p.R);
+        if (p.B * p.M * nc > CBUF_FLOATS) return cudaErrorInvalidValue;
+        p.tok_pitch = tok_pitch;
+        p.act_bytes = (p.M * tok_pitch + 127) / 128 * 128;
+        const int64_t groups = (N + p.R - 1) / p.R;
+        cudaError_t e = launch_fmt<WF>(dev, p, groups, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
-    const int nc = static_cast<int>(K / CHUNK_ELEMS);
-    const int ch = wchunk_bytes(w_fmt);
-    const int acp = (w_fmt == CQ_Q4_1 || w_fmt == CQ_Q4_K) ? 304 : 272;
-    const int ach = achunk_bytes(act_fmt_for(w_fmt));
-    const int64_t row_bytes = static_cast<int64_t>(nc) * ch;
-    // Token groups so that the staged activations stay within 96 KB.
-    const int tok_pitch = nc * acp;
-    const int max_tok = std::max(1, std::min(M, (96 * 1024) / tok_pitch));
-    if (tok_pitch > 96 * 1024) return cudaErrorInvalidValue;   // K beyond the supported range
-    for (int m0 = 0; m0 < M; m0 += max_tok) {
-        const int mm = std::min(max_tok, M - m0);
-        GemvParams p{};
-        p.W = static_cast<const uint8_t*>(W);
-        p.xq = static_cast<const uint8_t*>(xq) + static_cast<int64_t>(m0) * nc * ach;
-        p.y = y + static_cast<int64_t>(m0) * N;
-        p.status = dev.status;
-        p.N = N;
-        p.row_bytes = row_bytes;
-        p.M = mm;
-        p.nc = nc;
-        if (nc <= SEGC_MAX) {
-            p.R = std::max(1, 32 / nc);
-            p.segc = nc;
-            p.nseg = 1;
-            p.stage_bytes = static_cast<int>((p.R * row_bytes + 127) / 128 * 128);
-        } else {
-            p.R = 1;
-            p.segc = SEGC_MAX;
-            p.nseg = (nc + SEGC_MAX - 1) / SEGC_MAX;
-            p.stage_bytes = (SEGC_MAX * ch + 127) / 128 * 128;
-        }
-        p.tok_pitch = tok_pitch;
-        p.act_bytes = (mm * tok_pitch + 127) / 128 * 128;
-        // The y rows of this token group are [m0, m0 + mm): y stride stays N.
-        const int64_t groups = (N + p.R - 1) / p.R;
-        cudaError_t e;
-        switch (w_fmt) {
-        case CQ_Q4_0: e = launch_fmt<CQ_Q4_0>(dev, p, groups, s); break;
-        case CQ_Q8_0: e = launch_fmt<CQ_Q8_0>(dev, p, groups, s); break;
-        case CQ_Q4_1: e = launch_fmt<CQ_Q4_1>(dev, p, groups, s); break;
-        case CQ_Q4_K: e = launch_fmt<CQ_Q4_K>(dev, p, groups, s); break;
-        default: return cudaErrorInvalidValue;
-        }
-        if (e != cudaSuccess) return e;
+    switch (w_fmt) {
+    case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, xq, y, s);
+    default: return cudaErrorInvalidValue;
     }
-    return cudaSuccess;
 }
 
 }  // namespace cq

@@ -49,9 +49,11 @@
  *                     isum_m = sum_j m_j (bsum_2j + bsum_2j+1),
  *                     c = fma(d_x * D(d), (float)isum_sc,
  *                             -((d_x * D(dmin)) * (float)isum_m))
- *   Blocks are taken in 256-element chunks; c starts at 0 for every chunk and
- *   takes the chunk's blocks in increasing k; then y = y + c over the chunks in
- *   increasing k, starting from y = 0. Every operation rounds to nearest.
+ *   Blocks are taken in chunks -- four 32-blocks (128 elements) for Q4_0,
+ *   Q4_1 and Q8_0, one superblock (256 elements) for Q4_K; c starts at 0 for
+ *   every chunk and takes the chunk's blocks in increasing k; then y = y + c
+ *   over the chunks in increasing k, starting from y = 0. Every operation
+ *   rounds to nearest.
  */
 #ifndef CQ_H
 #define CQ_H
