@@ -1,23 +1,427 @@
-// Prefill GEMM entry (any M). Until the tensor-core kernel lands, tokens are
-// taken sixteen at a time through the GEMV kernel, which follows the same
-// fixed evaluation order, so every row is the cq_gemv row bit for bit.
+// Prefill GEMM, Q4_K weights x Q8_K activations, on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in tensor memory).
+//
+// alice-llm docs, "Computation Path (Q4_K)": per 256-element superblock
+//   y += d_x * d * sum_j(sc_j * S_j) - d_x * dmin * sum_j(m_j * bsum_j),
+// S_j the integer dot of 32-element sub-block j; cera README: batched-GEMM
+// prefill, and decode matching prefill bit for bit (cera 0.5 notes).
+//
+// Exact integer contraction on fp16 tensor cores. tcgen05 has no int8 MMA on
+// sm_103a, so the operands are fp16 values that hold integers exactly:
+//   A[n][k] = sc_j(n) * q4(n, k)   in [0, 945]   (weights, MMA M = 128 rows)
+//   B[m][k] = q8(m, k)             in [-127, 127] (tokens, MMA N = 128)
+// A superblock's products sum to at most 30.7e6 > 2^24 in magnitude, so each
+// superblock is split into two K = 128 halves, each accumulated in its own
+// fp32 tensor-memory accumulator (|partial| <= 15.4e6 < 2^24: exact). The min
+// term sum_j m_j * bsum_j is one more K = 16 MMA: A = [m_0..m_7, m_0..m_7],
+// B = [64 h_0..64 h_7, l_0..l_7] with bsum_j = 64 h_j + l_j, all exact in fp16.
+// The epilogue then applies, per (row, token, superblock), exactly the fixed
+// fp32 order of include/cq.h -- RN(h0 + h1) is (float)isum_sc -- so every row
+// equals the cq_gemv row bit for bit.
+//
+// Warp roles (320 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
+// map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory and
+// one lane issues the MMAs; warps 2-5 convert raw weights and Q8_K
+// activations into fp16 tiles in the canonical K-major no-swizzle layout;
+// warps 6-9 are the epilogue (tensor-memory lanes 32*(warp%4)...). Every wait
+// is bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
+#include <mutex>
+
+#include <cuda_fp16.h>
 
 #include "cq_device.cuh"
 #include "cq_internal.h"
+#include "tc.cuh"
 
 namespace cq {
+namespace {
+
+constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 128;          // tokens per tile (MMA N)
+constexpr int KH = 128;          // K per operand stage (half a superblock)
+constexpr int NSTAGE = 2;        // operand stages
+constexpr int NRAW = 2;          // raw weight superblock stages
+constexpr int RAW_BYTES = BM * 144;
+constexpr int A_BYTES = BM * KH * 2;        // 32 KB
+constexpr int B_BYTES = BN * KH * 2;        // 32 KB
+constexpr int AMIN_BYTES = BM * 16 * 2;     // 4 KB
+constexpr int BMIN_BYTES = BN * 16 * 2;     // 4 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + AMIN_BYTES + BMIN_BYTES;
+constexpr int THREADS = 320;
+constexpr uint32_t TMEM_COLS = 512;         // h0 | h1 | mins | y, 128 columns each
+constexpr uint32_t COL_H0 = 0, COL_H1 = 128, COL_MIN = 256, COL_Y = 384;
+
+// Shared-memory layout (offsets from the 1024-aligned dynamic base).
+constexpr int OFF_BAR = 0;                   // 16 barriers
+constexpr int OFF_TMEM = 128;                // tensor-memory base address
+constexpr int OFF_FLAG = 136;                // abort flag
+constexpr int OFF_DX = 256;                  // [2][BN] floats
+constexpr int OFF_RAW = 2048;
+constexpr int OFF_STAGE = OFF_RAW + NRAW * RAW_BYTES;
+constexpr int SMEM_BYTES = OFF_STAGE + NSTAGE * STAGE_BYTES + 1024;   // + alignment slack
+
+enum { B_RAW_FULL = 0, B_RAW_EMPTY = 2, B_OP_FULL = 4, B_OP_EMPTY = 6, B_ACC_FULL = 8, B_ACC_EMPTY = 9 };
+
+struct GemmParams {
+    const uint8_t* W;
+    const uint8_t* xq;
+    float* y;
+    int* status;
+    int M, N, ns;        // tokens, rows, superblocks per row
+    int64_t wrow;        // bytes per weight row
+    int64_t xrow;        // bytes per activation row
+};
+
+// Offset of element (r, k) in a K-major no-swizzle tile whose rows hold kt elements.
+__device__ __forceinline__ int tile_off(int r, int k, int kt) {
+    return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* flag, int* status) {
+    if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
+    *flag = 1;
+    atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
+    return false;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Four nibble pairs (one byte each of w) -> the low nibbles as two half2 of
+// sl * q and the high nibbles as two half2 of sh * q, each exact:
+// (1024 + q) * s - 1024 * s in one fused multiply-add.
+__device__ __forceinline__ void nibbles_to_half(uint32_t w, __half2 sl, __half2 bl, __half2 sh, __half2 bh,
+                                                uint32_t (&lo)[2], uint32_t (&hi)[2]) {
+    const uint32_t p01 = __byte_perm(w, 0u, 0x4140);   // bytes 0, 1 -> halves 0, 1
+    const uint32_t p23 = __byte_perm(w, 0u, 0x4342);   // bytes 2, 3
+    lo[0] = h2_bits(__hfma2(bits_h2((p01 & 0x000F000Fu) | 0x64006400u), sl, bl));
+    lo[1] = h2_bits(__hfma2(bits_h2((p23 & 0x000F000Fu) | 0x64006400u), sl, bl));
+    hi[0] = h2_bits(__hfma2(bits_h2(((p01 >> 4) & 0x000F000Fu) | 0x64006400u), sh, bh));
+    hi[1] = h2_bits(__hfma2(bits_h2(((p23 >> 4) & 0x000F000Fu) | 0x64006400u), sh, bh));
+}
+// Four signed bytes -> two half2 holding the same integers.
+__device__ __forceinline__ void int8_to_half(uint32_t w, uint32_t (&o)[2]) {
+    const __half2 bias = bits_h2(0x64806480u);          // 1152 = 1024 + 128
+    const uint32_t p01 = __byte_perm(w, 0u, 0x4140);
+    const uint32_t p23 = __byte_perm(w, 0u, 0x4342);
+    o[0] = h2_bits(__hsub2(bits_h2((p01 ^ 0x00800080u) | 0x64006400u), bias));
+    o[1] = h2_bits(__hsub2(bits_h2((p23 ^ 0x00800080u) | 0x64006400u), bias));
+}
+
+__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& mn) {
+    auto byte = [](uint32_t w, int i) { return static_cast<int>((w >> (8 * i)) & 0xffu); };
+    if (j < 4) {
+        sc = byte(s0, j) & 63;
+        mn = byte(s1, j) & 63;
+    } else {
+        sc = (byte(s2, j - 4) & 15) | ((byte(s0, j - 4) >> 6) << 4);
+        mn = (byte(s2, j - 4) >> 4) | ((byte(s1, j - 4) >> 6) << 4);
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_FLAG);
+    float* dxbuf = reinterpret_cast<float*>(smem + OFF_DX);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+    const int ns = p.ns;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NRAW; ++i) {
+            mbar_init(&bars[B_RAW_FULL + i], 1);
+            mbar_init(&bars[B_RAW_EMPTY + i], 128);
+        }
+        for (int i = 0; i < NSTAGE; ++i) {
+            mbar_init(&bars[B_OP_FULL + i], 128);
+            mbar_init(&bars[B_OP_EMPTY + i], 1);
+        }
+        mbar_init(&bars[B_ACC_FULL], 1);
+        mbar_init(&bars[B_ACC_EMPTY], 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_holder, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            for (int s = 0; s < ns && !*abort_flag; ++s) {
+                const int r = s % NRAW;
+                if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAW_BYTES);
+                tc::tma_load_2d(smem + OFF_RAW + r * RAW_BYTES, &wmap, 144 * s, n0, &bars[B_RAW_FULL + r]);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+            const uint32_t stage0 = smem_u32(smem + OFF_STAGE);
+            for (int s = 0; s < ns && !*abort_flag; ++s) {
+                if (!wait_or_abort(&bars[B_ACC_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
+                bool ok = true;
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 2 * s + h, st = q % NSTAGE;
+                    if (!wait_or_abort(&bars[B_OP_FULL + st], (q / NSTAGE) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t a0 = stage0 + st * STAGE_BYTES;
+                    const uint32_t b0 = a0 + A_BYTES;
+                    for (int t = 0; t < KH / 16; ++t)
+                        tc::mma_f16(tmem + (h ? COL_H1 : COL_H0), tc::smem_desc(a0 + 256 * t, 128, KH * 16),
+                                    tc::smem_desc(b0 + 256 * t, 128, KH * 16), idesc, t > 0);
+                    if (h == 1)
+                        tc::mma_f16(tmem + COL_MIN, tc::smem_desc(b0 + B_BYTES, 128, 256),
+                                    tc::smem_desc(b0 + B_BYTES + AMIN_BYTES, 128, 256), idesc, 0);
+                    tc::commit(&bars[B_OP_EMPTY + st]);
+                }
+                if (!ok) break;
+                tc::commit(&bars[B_ACC_FULL]);
+            }
+        }
+    } else if (warp < 6) {
+        // --------------------------------------------------------- converters
+        const int tid = threadIdx.x - 64;               // 0..127: weight row tid, token tid
+        const int token = m0 + tid;
+        const bool tok_ok = token < p.M;
+        const uint8_t* xrow = p.xq + static_cast<int64_t>(tok_ok ? token : 0) * p.xrow;
+        for (int q = 0; q < 2 * ns; ++q) {
+            const int s = q >> 1, h = q & 1, st = q % NSTAGE, r = s % NRAW;
+            if (*abort_flag) break;
+            if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
+            if (!wait_or_abort(&bars[B_RAW_FULL + r], (s / NRAW) & 1, abort_flag, p.status)) break;
+            uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
+            // A: weight row tid, elements [128h, 128h + 128) of superblock s
+            const uint8_t* raw = smem + OFF_RAW + r * RAW_BYTES + tid * 144;
+            const uint4 hdr = *reinterpret_cast<const uint4*>(raw);
+            for (int gi = 0; gi < 2; ++gi) {
+                const int g = 2 * h + gi;
+                int sc_lo, sc_hi, mn_unused;
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g, sc_lo, mn_unused);
+                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g + 1, sc_hi, mn_unused);
+                const __half2 slo = __float2half2_rn(static_cast<float>(sc_lo));
+                const __half2 shi = __float2half2_rn(static_cast<float>(sc_hi));
+                const __half2 blo = __float2half2_rn(-1024.0f * sc_lo);
+                const __half2 bhi = __float2half2_rn(-1024.0f * sc_hi);
+                const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g);
+                const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * g);
+                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {        // 8 elements (2 words) per core-matrix row
+                    uint32_t l0[2], h0[2], l1[2], h1[2];
+                    nibbles_to_half(qw[2 * c], slo, blo, shi, bhi, l0, h0);
+                    nibbles_to_half(qw[2 * c + 1], slo, blo, shi, bhi, l1, h1);
+                    const int klo = 64 * gi + 8 * c, khi = 64 * gi + 32 + 8 * c;
+                    *reinterpret_cast<uint4*>(stg + tile_off(tid, klo, KH)) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
+                    *reinterpret_cast<uint4*>(stg + tile_off(tid, khi, KH)) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
+                }
+            }
+            // B: token tid, elements [128h, 128h + 128) of superblock s
+            uint8_t* bt = stg + A_BYTES;
+            const uint32_t* xs = reinterpret_cast<const uint32_t*>(xrow + 292 * s + 4 + 128 * h);
+#pragma unroll 4
+            for (int c = 0; c < 16; ++c) {
+                uint32_t o0[2], o1[2];
+                const uint32_t w0 = tok_ok ? xs[2 * c] : 0u, w1 = tok_ok ? xs[2 * c + 1] : 0u;
+                int8_to_half(w0, o0);
+                int8_to_half(w1, o1);
+                *reinterpret_cast<uint4*>(bt + tile_off(tid, 8 * c, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+            }
+            if (h == 1) {
+                // mins MMA operands: A_min row tid = [m_0..m_7, m_0..m_7],
+                // B_min token tid = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
+                uint8_t* am = bt + B_BYTES;
+                uint8_t* bm = am + AMIN_BYTES;
+                uint32_t mw[4];
+                for (int j = 0; j < 8; j += 2) {
+                    int sc0, mn0, sc1, mn1;
+                    q4k_scale_min(hdr.y, hdr.z, hdr.w, j, sc0, mn0);
+                    q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, sc1, mn1);
+                    mw[j / 2] = h2_bits(__floats2half2_rn(static_cast<float>(mn0), static_cast<float>(mn1)));
+                }
+                const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                *reinterpret_cast<uint4*>(am + tile_off(tid, 0, 16)) = mv;
+                *reinterpret_cast<uint4*>(am + tile_off(tid, 8, 16)) = mv;
+                const uint32_t* bs = reinterpret_cast<const uint32_t*>(xrow + 292 * s + 260);
+                uint32_t hw[4], lw[4];
+                for (int j = 0; j < 8; j += 2) {
+                    int pr[2];
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t v = tok_ok ? bs[j + u] : 0u;
+                        pr[u] = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
+                                static_cast<int>(static_cast<int16_t>(v >> 16));
+                    }
+                    const int h0 = pr[0] >> 6, h1 = pr[1] >> 6;          // floor division by 64
+                    hw[j / 2] = h2_bits(__floats2half2_rn(64.0f * h0, 64.0f * h1));
+                    lw[j / 2] = h2_bits(__floats2half2_rn(static_cast<float>(pr[0] - 64 * h0),
+                                                          static_cast<float>(pr[1] - 64 * h1)));
+                }
+                *reinterpret_cast<uint4*>(bm + tile_off(tid, 0, 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(bm + tile_off(tid, 8, 16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            fence_proxy_async_smem();
+            tc::mbar_arrive(&bars[B_OP_FULL + st]);
+            if (h == 1) tc::mbar_arrive(&bars[B_RAW_EMPTY + r]);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int et = threadIdx.x - 192;               // 0..127
+        const int quarter = warp & 3;                   // TMEM lanes 32*quarter ..
+        const int row = n0 + quarter * 32 + lane;
+        const bool row_ok = row < p.N;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const int token = m0 + et;
+        for (int s = 0; s < ns; ++s) {
+            // this superblock's activation scales (one token per thread) and row scales
+            dxbuf[(s & 1) * BN + et] = token < p.M ? *reinterpret_cast<const float*>(
+                                                         p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s)
+                                                   : 0.0f;
+            const uint32_t dd = row_ok ? *reinterpret_cast<const uint32_t*>(p.W + row * p.wrow + 144 * s) : 0u;
+            const float d = h2f(dd), ndmin = -h2f(dd >> 16);
+            // A bounded wait, then one decision for all four epilogue warps (the
+            // named barrier also publishes dxbuf).
+            const bool got = mbar_wait_bounded(&bars[B_ACC_FULL], s & 1, WAIT_LIMIT_NS);
+            if (!tc::named_and(1, 128, got)) {
+                if (et == 0) { *abort_flag = 1; atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
+                break;
+            }
+            tc::fence_after();
+            const uint64_t d2 = tc::pk(d, d), nm2 = tc::pk(ndmin, ndmin);
+            const float* dx = dxbuf + (s & 1) * BN;
+            for (int cb = 0; cb < BN; cb += 16) {
+                uint32_t h0[16], h1[16], mi[16], yv[16];
+                tc::ld16(lane_addr + COL_H0 + cb, h0);
+                tc::ld16(lane_addr + COL_H1 + cb, h1);
+                tc::ld16(lane_addr + COL_MIN + cb, mi);
+                if (s > 0) tc::ld16(lane_addr + COL_Y + cb, yv);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; i += 2) {
+                    const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
+                                                tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
+                    const uint64_t x2 = tc::pk(dx[cb + i], dx[cb + i + 1]);
+                    const uint64_t a = tc::mul2(x2, d2);
+                    const uint64_t nb = tc::mul2(x2, nm2);
+                    const uint64_t tn = tc::mul2(nb, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
+                    const uint64_t c = tc::fma2(a, S, tn);
+                    const uint64_t yp = s > 0 ? tc::pk(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1]))
+                                              : tc::pk(0.0f, 0.0f);
+                    float lo, hi;
+                    tc::upk(tc::add2(yp, c), lo, hi);
+                    yv[i] = __float_as_uint(lo);
+                    yv[i + 1] = __float_as_uint(hi);
+                }
+                tc::st16(lane_addr + COL_Y + cb, yv);
+            }
+            tc::wait_st();
+            tc::fence_before();
+            tc::mbar_arrive(&bars[B_ACC_EMPTY]);
+        }
+        if (__all_sync(0xffffffffu, !*abort_flag)) {
+            // y[m][n] for this row: 16 tokens per TMEM load; a warp's stores to one
+            // token are 32 consecutive floats.
+            for (int cb = 0; cb < BN; cb += 16) {
+                uint32_t yv[16];
+                tc::ld16(lane_addr + COL_Y + cb, yv);
+                tc::wait_ld();
+                if (row_ok) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (m0 + cb + i < p.M) p.y[static_cast<int64_t>(m0 + cb + i) * p.N + row] = __uint_as_float(yv[i]);
+                }
+            }
+        }
+    }
+
+    // Wind down: every role has left its loop; make sure no copy or MMA is in
+    // flight before the tensor memory and the CTA's shared memory go.
+    tc::fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        for (int i = 0; i < NRAW; ++i) (void)mbar_wait_bounded(&bars[B_RAW_FULL + i], 0, WAIT_LIMIT_NS / 8);
+        (void)mbar_wait_bounded(&bars[B_ACC_FULL], 0, WAIT_LIMIT_NS / 8);
+    }
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+}  // namespace
 
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, cudaStream_t s) {
-    const int64_t act_row = K / CHUNK_ELEMS * achunk_bytes(act_fmt_for(w_fmt));
-    for (int64_t m0 = 0; m0 < M; m0 += 16) {
-        const int mm = static_cast<int>(std::min<int64_t>(16, M - m0));
-        cudaError_t e = launch_gemv(dev, w_fmt, mm, N, K, W, static_cast<const uint8_t*>(xq) + m0 * act_row,
-                                    y + m0 * N, s);
+    if (w_fmt != CQ_Q4_K) return cudaErrorInvalidValue;
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    GemmParams p{};
+    p.W = static_cast<const uint8_t*>(W);
+    p.xq = static_cast<const uint8_t*>(xq);
+    p.y = y;
+    p.status = dev.status;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.ns = static_cast<int>(K / 256);
+    p.wrow = static_cast<int64_t>(p.ns) * 144;
+    p.xrow = static_cast<int64_t>(p.ns) * 292;
+    // Raw weights as a 2-D byte tensor [N rows][wrow bytes]; a box is one
+    // superblock (144 bytes) of 128 rows; rows past N read as zero.
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.wrow), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.wrow)};
+    const cuuint32_t box[2] = {144, BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    static int raised[64] = {};
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e != cudaSuccess) return e;
+    if (devid >= 64 || !raised[devid]) {
+        e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        if (devid < 64) raised[devid] = 1;
     }
-    return cudaSuccess;
+    if (SMEM_BYTES > dev.smem_optin) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>((M + BN - 1) / BN));
+    gemm_q4k_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(map, p);
+    return cudaGetLastError();
 }
 
 }  // namespace cq
