@@ -6,7 +6,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/cq.h"
+#include "cq.h"
 #include "cq_internal.h"
 
 namespace {

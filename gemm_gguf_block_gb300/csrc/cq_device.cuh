@@ -6,7 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/cq.h"
+#include "cq.h"
 
 namespace cq {
 

@@ -16,14 +16,15 @@
 // term sum_j m_j * bsum_j is one more K = 16 MMA: A = [m_0..m_7, m_0..m_7],
 // B = [64 h_0..64 h_7, l_0..l_7] with bsum_j = 64 h_j + l_j, all exact in fp16.
 // The epilogue then applies, per (row, token, superblock), exactly the fixed
-// fp32 order of include/cq.h -- RN(h0 + h1) is (float)isum_sc -- so every row
-// equals the cq_gemv row bit for bit.
+// fp32 order of include/cq.h -- RN(h0 + h1) is (float)isum_sc; then
+// t = fma(d, S, -(dmin * I)) and y = fma(d_x, t, y) -- so every row equals the
+// cq_gemv row bit for bit.
 //
-// Warp roles (320 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
+// Warp roles (576 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
 // map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory and
-// one lane issues the MMAs; warps 2-5 convert raw weights and Q8_K
+// one lane issues the MMAs; warps 2-9 convert raw weights and Q8_K
 // activations into fp16 tiles in the canonical K-major no-swizzle layout;
-// warps 6-9 are the epilogue (tensor-memory lanes 32*(warp%4)...). Every wait
+// warps 10-17 are the epilogue (tensor-memory lanes 32*(warp%4)...). Every wait
 // is bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
 #include <mutex>
@@ -41,14 +42,16 @@ constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;          // tokens per tile (MMA N)
 constexpr int KH = 128;          // K per operand stage (half a superblock)
 constexpr int NSTAGE = 2;        // operand stages
-constexpr int NRAW = 2;          // raw weight superblock stages
+constexpr int NRAW = 3;          // raw weight superblock stages
 constexpr int RAW_BYTES = BM * 144;
 constexpr int A_BYTES = BM * KH * 2;        // 32 KB
 constexpr int B_BYTES = BN * KH * 2;        // 32 KB
 constexpr int AMIN_BYTES = BM * 16 * 2;     // 4 KB
 constexpr int BMIN_BYTES = BN * 16 * 2;     // 4 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + AMIN_BYTES + BMIN_BYTES;
-constexpr int THREADS = 320;
+constexpr int THREADS = 576;     // 2 + 8 converter + 8 epilogue warps
+constexpr int NEPI = 256;        // epilogue threads
+constexpr int NCONV = 256;       // converter threads
 constexpr uint32_t TMEM_COLS = 512;         // h0 | h1 | mins | y, 128 columns each
 constexpr uint32_t COL_H0 = 0, COL_H1 = 128, COL_MIN = 256, COL_Y = 384;
 
@@ -61,7 +64,7 @@ constexpr int OFF_RAW = 2048;
 constexpr int OFF_STAGE = OFF_RAW + NRAW * RAW_BYTES;
 constexpr int SMEM_BYTES = OFF_STAGE + NSTAGE * STAGE_BYTES + 1024;   // + alignment slack
 
-enum { B_RAW_FULL = 0, B_RAW_EMPTY = 2, B_OP_FULL = 4, B_OP_EMPTY = 6, B_ACC_FULL = 8, B_ACC_EMPTY = 9 };
+enum { B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 8, B_ACC_FULL = 10, B_ACC_EMPTY = 11 };
 
 struct GemmParams {
     const uint8_t* W;
@@ -135,14 +138,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(&bars[B_RAW_FULL + i], 1);
-            mbar_init(&bars[B_RAW_EMPTY + i], 128);
+            mbar_init(&bars[B_RAW_EMPTY + i], NCONV);
         }
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], 128);
+            mbar_init(&bars[B_OP_FULL + i], NCONV);
             mbar_init(&bars[B_OP_EMPTY + i], 1);
         }
         mbar_init(&bars[B_ACC_FULL], 1);
-        mbar_init(&bars[B_ACC_EMPTY], 128);
+        mbar_init(&bars[B_ACC_EMPTY], NEPI);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -194,155 +197,200 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 tc::commit(&bars[B_ACC_FULL]);
             }
         }
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // --------------------------------------------------------- converters
-        const int tid = threadIdx.x - 64;               // 0..127: weight row tid, token tid
-        const int token = m0 + tid;
-        const bool tok_ok = token < p.M;
-        const uint8_t* xrow = p.xq + static_cast<int64_t>(tok_ok ? token : 0) * p.xrow;
+        // Weights: a thread pair per weight row (one 64-element group each),
+        // from the raw stage in shared memory. Activations: warp w converts
+        // tokens 16w..16w+15; each load instruction reads 16 bytes of 8 tokens
+        // (few cache lines) and each store fills whole core-matrix rows; the
+        // next stage's words are loaded one stage ahead.
+        const int tid = threadIdx.x - 64;               // 0..255
+        const int r = tid >> 1, part = tid & 1;         // weight row r, group part
+        const int cw = warp - 2;                        // converter warp 0..7
+        const int a_row = (r >> 3) * (KH * 16) + (r & 7) * 16 + part * 1024;   // A tile row base (+ k offsets)
+        uint32_t cur[16], nxt[16], bcur[4], bnxt[4];
+        auto fetch = [&](int q, uint32_t (&dst)[16], uint32_t (&bs)[4]) {
+            const int s = q >> 1, h = q & 1;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int token = m0 + 16 * cw + 8 * (i & 1) + (lane & 7);
+                const int word = 4 * (i >> 1) + (lane >> 3);
+                dst[i] = token < p.M ? __ldg(reinterpret_cast<const uint32_t*>(
+                                           p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s + 4 + 128 * h) + word)
+                                     : 0u;
+            }
+            if (h == 1) {
+                // bsum words: token 16cw + 4i + (lane >> 3), word lane & 7
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int token = m0 + 16 * cw + 4 * i + (lane >> 3);
+                    bs[i] = token < p.M ? __ldg(reinterpret_cast<const uint32_t*>(
+                                              p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s + 260) + (lane & 7))
+                                        : 0u;
+                }
+            }
+        };
+        fetch(0, cur, bcur);
         for (int q = 0; q < 2 * ns; ++q) {
-            const int s = q >> 1, h = q & 1, st = q % NSTAGE, r = s % NRAW;
+            const int s = q >> 1, h = q & 1, st = q % NSTAGE, rs = s % NRAW;
             if (*abort_flag) break;
+            if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt);
             if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
-            if (!wait_or_abort(&bars[B_RAW_FULL + r], (s / NRAW) & 1, abort_flag, p.status)) break;
+            if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
-            // A: weight row tid, elements [128h, 128h + 128) of superblock s
-            const uint8_t* raw = smem + OFF_RAW + r * RAW_BYTES + tid * 144;
+            // A: weight row r, group g = 2h + part: 32 low nibbles (sub-block 2g) and
+            // 32 high nibbles (sub-block 2g + 1)
+            const uint8_t* raw = smem + OFF_RAW + rs * RAW_BYTES + r * 144;
             const uint4 hdr = *reinterpret_cast<const uint4*>(raw);
-            for (int gi = 0; gi < 2; ++gi) {
-                const int g = 2 * h + gi;
+            {
+                const int g = 2 * h + part;
                 int sc_lo, sc_hi, mn_unused;
                 q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g, sc_lo, mn_unused);
                 q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g + 1, sc_hi, mn_unused);
-                const __half2 slo = __float2half2_rn(static_cast<float>(sc_lo));
-                const __half2 shi = __float2half2_rn(static_cast<float>(sc_hi));
-                const __half2 blo = __float2half2_rn(-1024.0f * sc_lo);
-                const __half2 bhi = __float2half2_rn(-1024.0f * sc_hi);
+                const __half2 slo = __half2half2(__int2half_rn(sc_lo));
+                const __half2 shi = __half2half2(__int2half_rn(sc_hi));
+                const __half2 blo = __half2half2(__int2half_rn(-1024 * sc_lo));
+                const __half2 bhi = __half2half2(__int2half_rn(-1024 * sc_hi));
                 const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g);
                 const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * g);
                 const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                uint8_t* arow = stg + a_row;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {        // 8 elements (2 words) per core-matrix row
                     uint32_t l0[2], h0[2], l1[2], h1[2];
                     nibbles_to_half(qw[2 * c], slo, blo, shi, bhi, l0, h0);
                     nibbles_to_half(qw[2 * c + 1], slo, blo, shi, bhi, l1, h1);
-                    const int klo = 64 * gi + 8 * c, khi = 64 * gi + 32 + 8 * c;
-                    *reinterpret_cast<uint4*>(stg + tile_off(tid, klo, KH)) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
-                    *reinterpret_cast<uint4*>(stg + tile_off(tid, khi, KH)) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
+                    *reinterpret_cast<uint4*>(arow + c * 128) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
+                    *reinterpret_cast<uint4*>(arow + (4 + c) * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
                 }
             }
-            // B: token tid, elements [128h, 128h + 128) of superblock s
+            // B: tokens 16cw .. 16cw + 15; load i holds token 16cw + 8(i&1) + lane%8,
+            // quant word 4(i>>1) + lane/8 (elements 4*word .. +3 of the half), so a
+            // half-warp's 8-byte stores fill one 128-byte core matrix.
             uint8_t* bt = stg + A_BYTES;
-            const uint32_t* xs = reinterpret_cast<const uint32_t*>(xrow + 292 * s + 4 + 128 * h);
-#pragma unroll 4
-            for (int c = 0; c < 16; ++c) {
-                uint32_t o0[2], o1[2];
-                const uint32_t w0 = tok_ok ? xs[2 * c] : 0u, w1 = tok_ok ? xs[2 * c + 1] : 0u;
-                int8_to_half(w0, o0);
-                int8_to_half(w1, o1);
-                *reinterpret_cast<uint4*>(bt + tile_off(tid, 8 * c, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int t = 16 * cw + 8 * (i & 1) + (lane & 7);
+                const int word = 4 * (i >> 1) + (lane >> 3);
+                uint32_t o[2];
+                int8_to_half(cur[i], o);
+                *reinterpret_cast<uint2*>(bt + (t >> 3) * (KH * 16) + (t & 7) * 16 + (word >> 1) * 128 +
+                                          (word & 1) * 8) = make_uint2(o[0], o[1]);
             }
             if (h == 1) {
-                // mins MMA operands: A_min row tid = [m_0..m_7, m_0..m_7],
-                // B_min token tid = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
+                // mins MMA operands: A_min row r = [m_0..m_7, m_0..m_7] (part 0 threads),
+                // B_min token t = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
                 uint8_t* am = bt + B_BYTES;
                 uint8_t* bm = am + AMIN_BYTES;
-                uint32_t mw[4];
-                for (int j = 0; j < 8; j += 2) {
-                    int sc0, mn0, sc1, mn1;
-                    q4k_scale_min(hdr.y, hdr.z, hdr.w, j, sc0, mn0);
-                    q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, sc1, mn1);
-                    mw[j / 2] = h2_bits(__floats2half2_rn(static_cast<float>(mn0), static_cast<float>(mn1)));
-                }
-                const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-                *reinterpret_cast<uint4*>(am + tile_off(tid, 0, 16)) = mv;
-                *reinterpret_cast<uint4*>(am + tile_off(tid, 8, 16)) = mv;
-                const uint32_t* bs = reinterpret_cast<const uint32_t*>(xrow + 292 * s + 260);
-                uint32_t hw[4], lw[4];
-                for (int j = 0; j < 8; j += 2) {
-                    int pr[2];
-                    for (int u = 0; u < 2; ++u) {
-                        const uint32_t v = tok_ok ? bs[j + u] : 0u;
-                        pr[u] = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
-                                static_cast<int>(static_cast<int16_t>(v >> 16));
+                if (part == 0) {
+                    uint32_t mw[4];
+#pragma unroll
+                    for (int j = 0; j < 8; j += 2) {
+                        int sc0, mn0, sc1, mn1;
+                        q4k_scale_min(hdr.y, hdr.z, hdr.w, j, sc0, mn0);
+                        q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, sc1, mn1);
+                        mw[j / 2] = h2_bits(__halves2half2(__int2half_rn(mn0), __int2half_rn(mn1)));
                     }
-                    const int h0 = pr[0] >> 6, h1 = pr[1] >> 6;          // floor division by 64
-                    hw[j / 2] = h2_bits(__floats2half2_rn(64.0f * h0, 64.0f * h1));
-                    lw[j / 2] = h2_bits(__floats2half2_rn(static_cast<float>(pr[0] - 64 * h0),
-                                                          static_cast<float>(pr[1] - 64 * h1)));
+                    const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                    *reinterpret_cast<uint4*>(am + tile_off(r, 0, 16)) = mv;
+                    *reinterpret_cast<uint4*>(am + tile_off(r, 8, 16)) = mv;
                 }
-                *reinterpret_cast<uint4*>(bm + tile_off(tid, 0, 16)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(bm + tile_off(tid, 8, 16)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int t = 16 * cw + 4 * i + (lane >> 3), j = lane & 7;
+                    const uint32_t v = bcur[i];
+                    const int pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
+                                   static_cast<int>(static_cast<int16_t>(v >> 16));
+                    const int hq = pr >> 6;                                  // floor division by 64
+                    __half* bh = reinterpret_cast<__half*>(bm + tile_off(t, 0, 16));
+                    bh[j] = __int2half_rn(64 * hq);
+                    bh[64 + j] = __int2half_rn(pr - 64 * hq);                // k = 8 + j: next core matrix (+128 B)
+                }
             }
             fence_proxy_async_smem();
             tc::mbar_arrive(&bars[B_OP_FULL + st]);
-            if (h == 1) tc::mbar_arrive(&bars[B_RAW_EMPTY + r]);
+            if (h == 1) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) bcur[i] = bnxt[i];
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        const int et = threadIdx.x - 192;               // 0..127
-        const int quarter = warp & 3;                   // TMEM lanes 32*quarter ..
+        // Eight warps: warp w reads tensor-memory lanes 32*(w%4)..+31 (weight
+        // rows) and half of the 128 token columns.
+        const int et = threadIdx.x - 320;               // 0..255
+        const int quarter = warp & 3;
+        const int c0 = ((warp - 10) >> 2) * 64;         // first token column of this warp
         const int row = n0 + quarter * 32 + lane;
         const bool row_ok = row < p.N;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int token = m0 + et;
+        const int token = m0 + et;                      // et < 128: loads one token's scale
+        auto fetch_scales = [&](int s, float& dxv, uint32_t& ddv) {
+            dxv = (et < BN && token < p.M)
+                      ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s))
+                      : 0.0f;
+            ddv = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(p.W + row * p.wrow + 144 * s)) : 0u;
+        };
+        float dx_next;
+        uint32_t dd_next;
+        fetch_scales(0, dx_next, dd_next);
         for (int s = 0; s < ns; ++s) {
-            // this superblock's activation scales (one token per thread) and row scales
-            dxbuf[(s & 1) * BN + et] = token < p.M ? *reinterpret_cast<const float*>(
-                                                         p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s)
-                                                   : 0.0f;
-            const uint32_t dd = row_ok ? *reinterpret_cast<const uint32_t*>(p.W + row * p.wrow + 144 * s) : 0u;
+            // this superblock's activation scales and row scales, fetched one superblock ahead
+            if (et < BN) dxbuf[(s & 1) * BN + et] = dx_next;
+            const uint32_t dd = dd_next;
+            if (s + 1 < ns) fetch_scales(s + 1, dx_next, dd_next);
             const float d = h2f(dd), ndmin = -h2f(dd >> 16);
-            // A bounded wait, then one decision for all four epilogue warps (the
-            // named barrier also publishes dxbuf).
+            // A bounded wait, then one decision for all epilogue warps (the named
+            // barrier also publishes dxbuf).
             const bool got = mbar_wait_bounded(&bars[B_ACC_FULL], s & 1, WAIT_LIMIT_NS);
-            if (!tc::named_and(1, 128, got)) {
+            if (!tc::named_and(1, NEPI, got)) {
                 if (et == 0) { *abort_flag = 1; atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
                 break;
             }
             tc::fence_after();
+            // Fixed order: t = fma(d, RN(h0 + h1), -(dmin * I)); y = fma(d_x, t, y).
             const uint64_t d2 = tc::pk(d, d), nm2 = tc::pk(ndmin, ndmin);
-            const float* dx = dxbuf + (s & 1) * BN;
-            for (int cb = 0; cb < BN; cb += 16) {
+            const float2* dx2 = reinterpret_cast<const float2*>(dxbuf + (s & 1) * BN + c0);
+            for (int cb = 0; cb < 64; cb += 16) {
                 uint32_t h0[16], h1[16], mi[16], yv[16];
-                tc::ld16(lane_addr + COL_H0 + cb, h0);
-                tc::ld16(lane_addr + COL_H1 + cb, h1);
-                tc::ld16(lane_addr + COL_MIN + cb, mi);
-                if (s > 0) tc::ld16(lane_addr + COL_Y + cb, yv);
+                tc::ld16(lane_addr + COL_H0 + c0 + cb, h0);
+                tc::ld16(lane_addr + COL_H1 + c0 + cb, h1);
+                tc::ld16(lane_addr + COL_MIN + c0 + cb, mi);
+                if (s > 0) tc::ld16(lane_addr + COL_Y + c0 + cb, yv);
                 tc::wait_ld();
 #pragma unroll
                 for (int i = 0; i < 16; i += 2) {
                     const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
                                                 tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
-                    const uint64_t x2 = tc::pk(dx[cb + i], dx[cb + i + 1]);
-                    const uint64_t a = tc::mul2(x2, d2);
-                    const uint64_t nb = tc::mul2(x2, nm2);
-                    const uint64_t tn = tc::mul2(nb, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
-                    const uint64_t c = tc::fma2(a, S, tn);
+                    const uint64_t tn = tc::mul2(nm2, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
+                    const uint64_t t = tc::fma2(d2, S, tn);
+                    const float2 x = dx2[(cb + i) >> 1];
                     const uint64_t yp = s > 0 ? tc::pk(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1]))
                                               : tc::pk(0.0f, 0.0f);
                     float lo, hi;
-                    tc::upk(tc::add2(yp, c), lo, hi);
+                    tc::upk(tc::fma2(tc::pk(x.x, x.y), t, yp), lo, hi);
                     yv[i] = __float_as_uint(lo);
                     yv[i + 1] = __float_as_uint(hi);
                 }
-                tc::st16(lane_addr + COL_Y + cb, yv);
+                tc::st16(lane_addr + COL_Y + c0 + cb, yv);
             }
             tc::wait_st();
             tc::fence_before();
             tc::mbar_arrive(&bars[B_ACC_EMPTY]);
         }
         if (__all_sync(0xffffffffu, !*abort_flag)) {
-            // y[m][n] for this row: 16 tokens per TMEM load; a warp's stores to one
-            // token are 32 consecutive floats.
-            for (int cb = 0; cb < BN; cb += 16) {
+            // y[m][n] for this row: a warp's stores to one token are 32 consecutive floats.
+            for (int cb = 0; cb < 64; cb += 16) {
                 uint32_t yv[16];
-                tc::ld16(lane_addr + COL_Y + cb, yv);
+                tc::ld16(lane_addr + COL_Y + c0 + cb, yv);
                 tc::wait_ld();
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (m0 + cb + i < p.M) p.y[static_cast<int64_t>(m0 + cb + i) * p.N + row] = __uint_as_float(yv[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = m0 + c0 + cb + i;
+                        if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = __uint_as_float(yv[i]);
+                    }
                 }
             }
         }

@@ -20,7 +20,8 @@
 // 16-byte boundaries, scales in the padding, chunk pitch an odd number of
 // 16-byte units so the lanes' 128-bit loads do not collide). Chunk values go
 // to a small per-warp buffer; every B rows, lane (m, r) adds row r's values
-// for token m in increasing k -- the fixed evaluation order of include/cq.h.
+// for token m in increasing k (for Q4_K: y = fma(d_x, t, y) per superblock) --
+// the fixed evaluation order of include/cq.h.
 #include <algorithm>
 #include <cstdlib>
 
@@ -313,9 +314,8 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* wc, const uint8_t* xa,
                 q4k_scale_min(w[1], w[2], w[3], j, sc, mn);
                 im += mn * pr[j];
             }
-            const float a = __fmul_rn(dx, d);
-            const float bm = __fmul_rn(dx, dmin);
-            c[m] = __fmaf_rn(a, __int2float_rn(isc[m]), -__fmul_rn(bm, __int2float_rn(im)));
+            (void)dx;
+            c[m] = __fmaf_rn(d, __int2float_rn(isc[m]), -__fmul_rn(dmin, __int2float_rn(im)));
         }
     }
 }
@@ -438,8 +438,16 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
                     const int m = q / slot0, r = q - m * slot0;
                     const float* cb = cbuf + (m * p.B + r) * p.nc;
                     float acc = 0.0f;
+                    if constexpr (WF == CQ_Q4_K) {
+                        // y = fma(d_x, t, y) per superblock, d_x from the staged activations
+                        const uint8_t* xd = act + m * p.tok_pitch + 256;
 #pragma unroll 8
-                    for (int j = 0; j < p.nc; ++j) acc = __fadd_rn(acc, cb[j]);
+                        for (int j = 0; j < p.nc; ++j)
+                            acc = __fmaf_rn(*reinterpret_cast<const float*>(xd + j * F::ACP), cb[j], acc);
+                    } else {
+#pragma unroll 8
+                        for (int j = 0; j < p.nc; ++j) acc = __fadd_rn(acc, cb[j]);
+                    }
                     const int back = (slot0 - 1 - r) / p.R;
                     const int64_t row = (g - back * wtot) * p.R + (r - (r / p.R) * p.R);
                     if (row < p.N) p.y[static_cast<int64_t>(m) * p.N + row] = acc;

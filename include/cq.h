@@ -45,15 +45,15 @@
  *   Q4_0/Q8_0 block:  c = fma(D(d_w) * D(d_x), (float)isum, c)
  *   Q4_1 block:       c = fma(D(d_w) * D(d_x), (float)isum, c);
  *                     c = fma(D(m_w), D(s_x), c)
- *   Q4_K superblock:  S_j = int dot of sub-block j, isum_sc = sum_j sc_j S_j,
+ *   Q4_0/Q4_1/Q8_0: blocks are taken in chunks of four (128 elements); c
+ *   starts at 0 for every chunk and takes the chunk's blocks in increasing k;
+ *   then y = y + c over the chunks in increasing k, starting from y = 0.
+ *   Q4_K, per superblock in increasing k, from y = 0:
+ *                     S_j = int dot of sub-block j, isum_sc = sum_j sc_j S_j,
  *                     isum_m = sum_j m_j (bsum_2j + bsum_2j+1),
- *                     c = fma(d_x * D(d), (float)isum_sc,
- *                             -((d_x * D(dmin)) * (float)isum_m))
- *   Blocks are taken in chunks -- four 32-blocks (128 elements) for Q4_0,
- *   Q4_1 and Q8_0, one superblock (256 elements) for Q4_K; c starts at 0 for
- *   every chunk and takes the chunk's blocks in increasing k; then y = y + c
- *   over the chunks in increasing k, starting from y = 0. Every operation
- *   rounds to nearest.
+ *                     t = fma(D(d), (float)isum_sc, -(D(dmin) * (float)isum_m)),
+ *                     y = fma(d_x, t, y).
+ *   Every operation rounds to nearest.
  */
 #ifndef CQ_H
 #define CQ_H
