@@ -20,6 +20,12 @@ cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, v
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, cudaStream_t s);
 
+// Tensor-core batched GEMV (2 <= M <= 16; Q4_0, Q4_1, Q8_0) and the shared
+// memory it needs (0 when the format has no such path).
+int gemv_mma_smem(int w_fmt, int M, int64_t K);
+cudaError_t launch_gemv_mma(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
+                            const void* xq, float* y, cudaStream_t s);
+
 // Prefill GEMM (any M): y rows equal the cq_gemv rows bit for bit.
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, cudaStream_t s);
@@ -36,6 +42,12 @@ struct MoeLayout {
     size_t total;
 };
 MoeLayout moe_layout(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk);
+
+// Grouped tensor-core projections of the routed FFN: gate/up + SwiGLU into h,
+// Q8_0 of h into hq, down into o (all in the caller's workspace).
+cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
+                                   const void* Wu, const void* Wd, const void* xq, const int* offs, const int* perm,
+                                   float* h, const void* hq, float* o, cudaStream_t s);
 
 cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
                        const void* Wu, const void* Wd, const int32_t* ids, const float* rw, const void* xq,

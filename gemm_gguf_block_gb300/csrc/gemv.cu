@@ -471,6 +471,15 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
     }
 }
 
+// CQ_GEMV_MMA=0 keeps several-token calls on the dp4a kernel (for A/B runs).
+bool mma_enabled() {
+    static const bool v = [] {
+        const char* e = std::getenv("CQ_GEMV_MMA");
+        return !(e && e[0] == '0');
+    }();
+    return v;
+}
+
 // Ring depth: CQ_GEMV_STAGES (2..4) overrides the choice, for tuning runs.
 int stage_override() {
     static const int v = [] {
@@ -578,6 +587,11 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
+    // Several tokens: the tensor-core kernel when the activations fit its
+    // shared memory (same fixed order, so the same bits).
+    const int need = gemv_mma_smem(w_fmt, M, K);
+    if (M >= 2 && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled())
+        return launch_gemv_mma(dev, w_fmt, M, N, K, W, xq, y, s);
     switch (w_fmt) {
     case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, s);
     case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, s);

@@ -18,6 +18,7 @@
 //   3. down:    per (expert, 32-row tile of K): o = W_down . hq per pair.
 //   4. combine: y[t] = sum over slots in slot order of w * o (fma chain).
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "chunk_dot.cuh"
@@ -306,6 +307,15 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
 
 }  // namespace
 
+// CQ_MOE_MMA=0 runs the dp4a projections instead of the tensor-core ones (A/B runs).
+bool moe_mma_enabled() {
+    static const bool v = [] {
+        const char* e = std::getenv("CQ_MOE_MMA");
+        return !(e && e[0] == '0');
+    }();
+    return v;
+}
+
 size_t moe_up_smem(int K) {
     const int nc = K / CHUNK_ELEMS;
     const int rowb = nc * WCHUNK_Q4_0, tok_pitch = nc * ACHUNK_Q8_0;
@@ -335,25 +345,33 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
     moe_route_kernel<<<1, 1024, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int smem_up = static_cast<int>(moe_up_smem(K));
-    const int smem_dn = static_cast<int>(moe_down_smem(F));
-    const int lim = std::min(dev.smem_optin, 227 * 1024);
-    if (smem_up > lim || smem_dn > lim) return cudaErrorInvalidConfiguration;
-    static int raised[64] = {};
-    int devid = 0;
-    if ((e = cudaGetDevice(&devid)) != cudaSuccess) return e;
-    if (devid >= 64 || !raised[devid]) {
-        if ((e = cudaFuncSetAttribute(moe_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) != cudaSuccess)
-            return e;
-        if ((e = cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
-            cudaSuccess)
-            return e;
-        if (devid < 64) raised[devid] = 1;
+    if (moe_mma_enabled()) {
+        e = launch_moe_projections(dev, T, K, F, E, topk, Wg, Wu, Wd, xq, reinterpret_cast<const int*>(p.ws + p.L.offs),
+                                   reinterpret_cast<const int*>(p.ws + p.L.perm), reinterpret_cast<float*>(p.ws + p.L.h),
+                                   p.ws + p.L.hq, reinterpret_cast<float*>(p.ws + p.L.out), s);
+        if (e != cudaSuccess) return e;
+    } else {
+        const int smem_up = static_cast<int>(moe_up_smem(K));
+        const int smem_dn = static_cast<int>(moe_down_smem(F));
+        const int lim = std::min(dev.smem_optin, 227 * 1024);
+        if (smem_up > lim || smem_dn > lim) return cudaErrorInvalidConfiguration;
+        static int raised[64] = {};
+        int devid = 0;
+        if ((e = cudaGetDevice(&devid)) != cudaSuccess) return e;
+        if (devid >= 64 || !raised[devid]) {
+            if ((e = cudaFuncSetAttribute(moe_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
+                cudaSuccess)
+                return e;
+            if ((e = cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
+                cudaSuccess)
+                return e;
+            if (devid < 64) raised[devid] = 1;
+        }
+        moe_up_kernel<<<dim3(F / TILE, E), THREADS, smem_up, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        moe_down_kernel<<<dim3(K / TILE, E), THREADS, smem_dn, s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    moe_up_kernel<<<dim3(F / TILE, E), THREADS, smem_up, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    moe_down_kernel<<<dim3(K / TILE, E), THREADS, smem_dn, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t n = static_cast<int64_t>(T) * K;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4096));
     moe_combine_kernel<<<grid, 256, 0, s>>>(p);

@@ -1,0 +1,366 @@
+// Routed-expert FFN projections on the tensor cores, grouped by expert.
+//
+// cera README "Supported models" (lfm2moe): each token routes to 4 of 32
+// experts; grouping tokens by expert -- the follow-up the page names -- lets
+// each expert's weights be read once for all its tokens. alice-llm "WGSL
+// Shader Architecture" (swiglu_fused_q4k): gate and up share one pass.
+//
+// One CTA = (expert e, 128 weight rows). The expert's (token, slot) pairs,
+// sorted by the routing kernel, are taken up to 64 at a time. Q4_0 weights
+// stream through a ring of 2-D TMA boxes (128 rows x 8 blocks; for the up
+// projection the gate and up rows of the same f land in one stage); the
+// pairs' Q8_0 activation rows are bulk-copied per 256-element segment (one
+// 272-byte copy per pair) into the same stage, then converted to fp16 in
+// shared memory. Per 32-block the integer dot is an exact fp16
+// mma.sync m16n8k16 product (two k-steps), and the block's scale term is
+// accumulated as y = fma(d_w * d_x, isum, y) in increasing k.
+//   up:   warp w computes gate and up rows f0+16w.. for the pairs, then writes
+//         h = silu(g) * u (fp32) for the valid pairs into the workspace.
+//   down: o = W_down[e] . hq for the pairs, written into the workspace.
+#include <algorithm>
+#include <mutex>
+
+#include <cuda_fp16.h>
+
+#include "cq_device.cuh"
+#include "cq_internal.h"
+#include "tc.cuh"
+
+namespace cq {
+namespace {
+
+constexpr int ROWS = 128;
+constexpr int SEGB = 8;              // 32-blocks per segment
+constexpr int TOK = 64;              // pairs per pass (8 n-tiles)
+constexpr int NTM = TOK / 8;
+constexpr int CONSUMERS = 8;
+constexpr int THREADS = (CONSUMERS + 1) * 32;
+constexpr int BOX_BYTES = ROWS * SEGB * 18;        // one matrix, one segment: 18432
+constexpr int ACT_PITCH = 512 + 64;                 // bytes per token per segment (fp16) + pad:
+                                                    // 36 x 16 B, so lanes' 16-byte reads miss each other's banks
+constexpr int ACT_BYTES = TOK * ACT_PITCH;          // 36864
+constexpr int SCL_BYTES = TOK * SEGB * 4;           // 2048
+constexpr int RAWA = SEGB * 34;                     // one token's Q8_0 segment: 272 bytes
+constexpr int RAWA_BYTES = TOK * RAWA;              // 17408
+
+struct MoeMmaParams {
+    const uint8_t* xq;          // up: token activations (Q8_0 [T][K]); down: hq rows (Q8_0 [P][F])
+    const int* offs;            // [E+1]
+    const int* perm;            // pairs grouped by expert
+    float* out;                 // up: h [P][F]; down: o [P][Kout]
+    int* status;
+    int topk;
+    int rows_per_expert;        // up: F; down: K (d_model)
+    int kin;                    // up: K; down: F
+    int64_t xrow;               // bytes per activation row
+    int stages;
+};
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f), "f"(0.0f),
+          "f"(0.0f));
+}
+
+// Q4_0 nibbles of two bytes (low or high) as a half2 of (q - 8).
+__device__ __forceinline__ uint32_t q4_pair(uint32_t two_bytes, bool hi) {
+    const uint32_t p = __byte_perm(two_bytes, 0u, 0x4140);
+    const uint32_t n = (hi ? (p >> 4) : p) & 0x000F000Fu;
+    return h2u(__hsub2(u2h(n | 0x64006400u), u2h(0x64086408u)));     // (1024 + q) - 1032
+}
+// Four signed bytes as two half2.
+__device__ __forceinline__ void s8x4_to_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
+    o0 = h2u(__hsub2(u2h((__byte_perm(w, 0u, 0x4140) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
+    o1 = h2u(__hsub2(u2h((__byte_perm(w, 0u, 0x4342) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
+}
+
+template <bool UP>
+__global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_constant__ CUtensorMap map0,
+                                                             const __grid_constant__ CUtensorMap map1,
+                                                             const MoeMmaParams p) {
+    constexpr int NMAT = UP ? 2 : 1;
+    constexpr int STAGE = NMAT * BOX_BYTES + RAWA_BYTES;      // weight boxes, then the tokens' raw segments
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + 8;
+    int* pairs = reinterpret_cast<int*>(smem + 256);                   // [TOK] pair ids of the pass
+    uint8_t* act = smem + 1024;                                         // [TOK][ACT_PITCH] fp16
+    float* scl = reinterpret_cast<float*>(act + ACT_BYTES);             // [TOK][SEGB]
+    uint8_t* wst = smem + 1024 + ACT_BYTES + SCL_BYTES;                 // [S][STAGE]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.y, r0 = blockIdx.x * ROWS;
+    const int beg = p.offs[e], cnt = p.offs[e + 1] - beg;
+    if (cnt == 0) return;
+    const int nseg = p.kin / 256;
+    const int passes = (cnt + TOK - 1) / TOK;
+    const int64_t steps = static_cast<int64_t>(passes) * nseg;
+    const int row_base = e * p.rows_per_expert + r0;                   // row in the [E * rows] tensor
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], CONSUMERS);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == CONSUMERS) {
+        // ------------------------------------------------------- producer
+        // Per segment: the weight boxes (2-D TMA) and, for each of the pass's
+        // pairs, its activation row's 272-byte segment (1-D bulk copy).
+        const uint64_t pol = policy_evict_first();
+        int seg = 0, pass = 0;
+        for (int64_t k = 0; k < steps; ++k) {
+            const int st = static_cast<int>(k % S);
+            const int np = min(TOK, cnt - pass * TOK);
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((k / S) & 1) ^ 1), WAIT_LIMIT_NS);
+                if (!ok) {
+                    atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
+                } else {
+                    mbar_arrive_expect_tx(&full[st], NMAT * BOX_BYTES + np * RAWA);
+                    uint8_t* dst = wst + st * STAGE;
+                    tc::tma_load_2d(dst, &map0, seg * SEGB * 9, row_base, &full[st]);   // 9 = 18 bytes / 2
+                    if (UP) tc::tma_load_2d(dst + BOX_BYTES, &map1, seg * SEGB * 9, row_base, &full[st]);
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            uint8_t* raw = wst + st * STAGE + NMAT * BOX_BYTES;
+            for (int i = lane; i < np; i += 32) {
+                const int pr = p.perm[beg + pass * TOK + i];
+                const int64_t row = UP ? pr / p.topk : pr;
+                bulk_g2s(raw + i * RAWA, p.xq + row * p.xrow + static_cast<int64_t>(seg) * RAWA, RAWA, &full[st], pol);
+            }
+            if (++seg == nseg) { seg = 0; ++pass; }
+        }
+        return;   // the producer takes no part in the consumers' named barriers
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int ct = threadIdx.x;              // 0..255
+    const int g = lane >> 2, t = lane & 3;
+    int64_t k = 0;
+    for (int pass = 0; pass < passes; ++pass) {
+        const int np = min(TOK, cnt - pass * TOK);
+        const int nt = (np + 7) >> 3;
+        if (ct < TOK) pairs[ct] = ct < np ? p.perm[beg + pass * TOK + ct] : -1;
+        float ya[NTM][4], yb[NTM][4];
+#pragma unroll
+        for (int n = 0; n < NTM; ++n)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) { ya[n][i] = 0.0f; yb[n][i] = 0.0f; }
+        bool ok = true;
+        for (int seg = 0; seg < nseg; ++seg, ++k) {
+            const int st = static_cast<int>(k % S);
+            const bool got = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS);
+            if (!tc::named_and(2, CONSUMERS * 32, got)) {
+                if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
+                ok = false;
+                break;
+            }
+            // Convert the stage's raw Q8_0 segments: item i = (token i / 8, block i % 8),
+            // fp16 in the order lane t of an n-tile reads as one 16-byte load:
+            // [k=2t,2t+1 | 2t+8,+9 | 16+2t,+1 | 24+2t,+1] per t. Tokens past np are zero.
+            const uint8_t* raw = wst + st * (NMAT * BOX_BYTES + RAWA_BYTES) + NMAT * BOX_BYTES;
+            for (int it = ct; it < TOK * SEGB; it += CONSUMERS * 32) {
+                const int tk = it >> 3, b = it & 7;
+                uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                float d = 0.0f;
+                if (tk < np) {
+                    const uint16_t* src = reinterpret_cast<const uint16_t*>(raw + tk * RAWA + b * 34);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        w[j] = static_cast<uint32_t>(src[1 + 2 * j]) | (static_cast<uint32_t>(src[2 + 2 * j]) << 16);
+                    d = h2f(src[0]);
+                }
+                uint32_t hv[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) s8x4_to_half(w[j], hv[2 * j], hv[2 * j + 1]);
+                uint4* dst = reinterpret_cast<uint4*>(act + tk * ACT_PITCH + 64 * b);
+#pragma unroll
+                for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hv[tt], hv[tt + 4], hv[tt + 8], hv[tt + 12]);
+                scl[tk * SEGB + b] = d;
+            }
+            tc::named_and(1, CONSUMERS * 32, true);
+            const uint8_t* wa = wst + st * (NMAT * BOX_BYTES + RAWA_BYTES) + (16 * warp + g) * (SEGB * 18);
+#pragma unroll 1
+            for (int b = 0; b < SEGB; ++b) {
+                uint32_t fa0[4], fa1[4], fb0[4], fb1[4];
+                float dwa0, dwa1, dwb0 = 0.0f, dwb1 = 0.0f;
+                {
+                    const uint8_t* w0 = wa + b * 18;
+                    const uint8_t* w1 = w0 + 8 * (SEGB * 18);
+                    const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + 2);
+                    const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + 2);
+                    const uint32_t x0 = q0[t], x1 = q0[t + 4], z0 = q1[t], z1 = q1[t + 4];
+                    fa0[0] = q4_pair(x0, false); fa0[1] = q4_pair(z0, false);
+                    fa0[2] = q4_pair(x1, false); fa0[3] = q4_pair(z1, false);
+                    fa1[0] = q4_pair(x0, true); fa1[1] = q4_pair(z0, true);
+                    fa1[2] = q4_pair(x1, true); fa1[3] = q4_pair(z1, true);
+                    dwa0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
+                    dwa1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
+                }
+                if constexpr (UP) {
+                    const uint8_t* w0 = wa + BOX_BYTES + b * 18;
+                    const uint8_t* w1 = w0 + 8 * (SEGB * 18);
+                    const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + 2);
+                    const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + 2);
+                    const uint32_t x0 = q0[t], x1 = q0[t + 4], z0 = q1[t], z1 = q1[t + 4];
+                    fb0[0] = q4_pair(x0, false); fb0[1] = q4_pair(z0, false);
+                    fb0[2] = q4_pair(x1, false); fb0[3] = q4_pair(z1, false);
+                    fb1[0] = q4_pair(x0, true); fb1[1] = q4_pair(z0, true);
+                    fb1[2] = q4_pair(x1, true); fb1[3] = q4_pair(z1, true);
+                    dwb0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
+                    dwb1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
+                }
+#pragma unroll
+                for (int n = 0; n < NTM; ++n) {
+                    if (n < nt) {
+                        const uint4 bv = *reinterpret_cast<const uint4*>(act + (8 * n + g) * ACT_PITCH + 64 * b + 16 * t);
+                        const float dx0 = scl[(8 * n + 2 * t) * SEGB + b];
+                        const float dx1 = scl[(8 * n + 2 * t + 1) * SEGB + b];
+                        float c0[4], c1[4];
+                        mma16816(c0, fa0, bv.x, bv.y);
+                        mma16816(c1, fa1, bv.z, bv.w);
+                        ya[n][0] = __fmaf_rn(__fmul_rn(dwa0, dx0), c0[0] + c1[0], ya[n][0]);
+                        ya[n][1] = __fmaf_rn(__fmul_rn(dwa0, dx1), c0[1] + c1[1], ya[n][1]);
+                        ya[n][2] = __fmaf_rn(__fmul_rn(dwa1, dx0), c0[2] + c1[2], ya[n][2]);
+                        ya[n][3] = __fmaf_rn(__fmul_rn(dwa1, dx1), c0[3] + c1[3], ya[n][3]);
+                        if constexpr (UP) {
+                            mma16816(c0, fb0, bv.x, bv.y);
+                            mma16816(c1, fb1, bv.z, bv.w);
+                            yb[n][0] = __fmaf_rn(__fmul_rn(dwb0, dx0), c0[0] + c1[0], yb[n][0]);
+                            yb[n][1] = __fmaf_rn(__fmul_rn(dwb0, dx1), c0[1] + c1[1], yb[n][1]);
+                            yb[n][2] = __fmaf_rn(__fmul_rn(dwb1, dx0), c0[2] + c1[2], yb[n][2]);
+                            yb[n][3] = __fmaf_rn(__fmul_rn(dwb1, dx1), c0[3] + c1[3], yb[n][3]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[st]);
+            tc::named_and(1, CONSUMERS * 32, true);     // the fp16 tile is rewritten by the next segment
+        }
+        if (!ok) break;
+        // Results: rows r0 + 16w + g (+8), pairs 8n + 2t (+1).
+        const int f = r0 + 16 * warp + g;
+#pragma unroll
+        for (int n = 0; n < NTM; ++n) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tk = 8 * n + 2 * t + (i & 1);
+                const int pr = tk < np ? pairs[tk] : -1;
+                if (n < nt && pr >= 0) {
+                    const int row = f + (i >= 2 ? 8 : 0);
+                    float v;
+                    if constexpr (UP) {
+                        const float gg = ya[n][i], uu = yb[n][i];
+                        v = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg))), uu);
+                    } else {
+                        v = ya[n][i];
+                    }
+                    p.out[static_cast<int64_t>(pr) * p.rows_per_expert + row] = v;
+                }
+            }
+        }
+        tc::named_and(1, CONSUMERS * 32, true);     // pairs[] is rewritten by the next pass
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    });
+    return fn;
+}
+
+// Q4_0 weights of all experts as one 2-D tensor of 2-byte elements:
+// [E * rows][kin / 32 * 18 bytes]; box = 8 blocks x 128 rows.
+bool make_map(CUtensorMap* map, const void* W, int64_t rows, int kin) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const int64_t rb = static_cast<int64_t>(kin / 32) * 18;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(rb)};
+    const cuuint32_t box[2] = {SEGB * 9, ROWS};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool UP>
+cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUtensorMap& m1, MoeMmaParams p, int E,
+                       cudaStream_t s) {
+    const int lim = std::min(dev.smem_optin, 227 * 1024);
+    const int fixed = 1024 + ACT_BYTES + SCL_BYTES;
+    const int per_stage = (UP ? 2 : 1) * BOX_BYTES + RAWA_BYTES;
+    p.stages = std::min(8, (lim - fixed) / per_stage);
+    if (p.stages < 2) return cudaErrorInvalidConfiguration;
+    const int smem = fixed + p.stages * per_stage;
+    static int raised[64] = {};
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e != cudaSuccess) return e;
+    if (devid >= 64 || !raised[devid]) {
+        e = cudaFuncSetAttribute(moe_mma_kernel<UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+        if (e != cudaSuccess) return e;
+        if (devid < 64) raised[devid] = 1;
+    }
+    moe_mma_kernel<UP><<<dim3(p.rows_per_expert / ROWS, E), THREADS, smem, s>>>(m0, m1, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
+                                   const void* Wu, const void* Wd, const void* xq, const int* offs, const int* perm,
+                                   float* h, const void* hq, float* o, cudaStream_t s) {
+    CUtensorMap mg, mu, md;
+    if (!make_map(&mg, Wg, static_cast<int64_t>(E) * F, K) || !make_map(&mu, Wu, static_cast<int64_t>(E) * F, K) ||
+        !make_map(&md, Wd, static_cast<int64_t>(E) * K, F))
+        return cudaErrorInvalidValue;
+    MoeMmaParams up{};
+    up.xq = static_cast<const uint8_t*>(xq);
+    up.offs = offs;
+    up.perm = perm;
+    up.out = h;
+    up.status = dev.status;
+    up.topk = topk;
+    up.rows_per_expert = F;
+    up.kin = K;
+    up.xrow = static_cast<int64_t>(K / 32) * 34;
+    cudaError_t e = launch_one<true>(dev, mg, mu, up, E, s);
+    if (e != cudaSuccess) return e;
+    e = launch_quantize(CQ_Q8_0, static_cast<int64_t>(T) * topk, F, h, const_cast<void*>(hq), s);
+    if (e != cudaSuccess) return e;
+    MoeMmaParams dn = up;
+    dn.xq = static_cast<const uint8_t*>(hq);
+    dn.out = o;
+    dn.rows_per_expert = K;
+    dn.kin = F;
+    dn.xrow = static_cast<int64_t>(F / 32) * 34;
+    return launch_one<false>(dev, md, md, dn, E, s);
+}
+
+}  // namespace cq
