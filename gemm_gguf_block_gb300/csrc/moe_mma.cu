@@ -12,8 +12,9 @@
 // pairs' Q8_0 activation rows are bulk-copied per 256-element segment (one
 // 272-byte copy per pair) into the same stage, then converted to fp16 in
 // shared memory. Per 32-block the integer dot is an exact fp16
-// mma.sync m16n8k16 product (two k-steps), and the block's scale term is
-// accumulated as y = fma(d_w * d_x, isum, y) in increasing k.
+// mma.sync m16n8k16 product (two chained k-steps; every partial sum is an
+// integer below 2^23), and the block's scale term is accumulated as
+// y = fma(d_w * d_x, isum, y) in increasing k.
 //   up:   warp w computes gate and up rows f0+16w.. for the pairs, then writes
 //         h = silu(g) * u (fp32) for the valid pairs into the workspace.
 //   down: o = W_down[e] . hq for the pairs, written into the workspace.
@@ -32,14 +33,16 @@ namespace {
 constexpr int ROWS = 128;
 constexpr int SEGB = 8;              // 32-blocks per segment
 constexpr int TOK = 64;              // pairs per pass (8 n-tiles)
-constexpr int NTM = TOK / 8;
 constexpr int CONSUMERS = 8;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr int BOX_BYTES = ROWS * SEGB * 18;        // one matrix, one segment: 18432
 constexpr int ACT_PITCH = 512 + 64;                 // bytes per token per segment (fp16) + pad:
                                                     // 36 x 16 B, so lanes' 16-byte reads miss each other's banks
 constexpr int ACT_BYTES = TOK * ACT_PITCH;          // 36864
-constexpr int SCL_BYTES = TOK * SEGB * 4;           // 2048
+// Scale table: per (32-block b, token pair j) {d_x[2j], d_x[2j+1], bias[2j],
+// bias[2j+1]}, pitch 33 entries per block so the converters' stores spread over banks.
+constexpr int SCL_PITCH = TOK / 2 + 1;
+constexpr int SCL_BYTES = SEGB * SCL_PITCH * 16;    // 4224
 constexpr int RAWA = SEGB * 34;                     // one token's Q8_0 segment: 272 bytes
 constexpr int RAWA_BYTES = TOK * RAWA;              // 17408
 
@@ -59,20 +62,31 @@ struct MoeMmaParams {
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+// D = A * B + C (C given), and D += A * B.
+__device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
+                                          float c1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
+        "{%10,%11,%10,%11};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f), "f"(0.0f),
-          "f"(0.0f));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mma16816acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Q4_0 nibbles of two bytes (low or high) as a half2 of (q - 8).
-__device__ __forceinline__ uint32_t q4_pair(uint32_t two_bytes, bool hi) {
+// Q4_0 nibbles n of two bytes as half2 (1024 + n): the low nibbles (elements
+// j, j+1 of the block) and the high ones (j+16, j+17). 1024 + n is exact in
+// binary16 and costs no subtraction; the offset 1024 + 8 per element comes
+// back out through the accumulator's starting value, -1032 * sum(x).
+__device__ __forceinline__ void q4_biased(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
     const uint32_t p = __byte_perm(two_bytes, 0u, 0x4140);
-    const uint32_t n = (hi ? (p >> 4) : p) & 0x000F000Fu;
-    return h2u(__hsub2(u2h(n | 0x64006400u), u2h(0x64086408u)));     // (1024 + q) - 1032
+    lo = (p & 0x000F000Fu) | 0x64006400u;
+    hi = ((p >> 4) & 0x000F000Fu) | 0x64006400u;
 }
 // Four signed bytes as two half2.
 __device__ __forceinline__ void s8x4_to_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
@@ -80,20 +94,169 @@ __device__ __forceinline__ void s8x4_to_half(uint32_t w, uint32_t& o0, uint32_t&
     o1 = h2u(__hsub2(u2h((__byte_perm(w, 0u, 0x4342) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
 }
 
+struct Smem {
+    uint64_t* full;
+    uint64_t* empty;
+    int* pairs;        // [TOK] pair ids of the pass
+    uint8_t* act;      // [TOK][ACT_PITCH] fp16 activations of one segment
+    float4* scl;       // [SEGB][SCL_PITCH] scales and accumulator biases
+    uint8_t* wst;      // [stages][stage bytes]
+};
+
+// fp16 position of chunk c (16 bytes) of block b in a token's row: chunks are
+// XOR-rotated by block pair so that eight converters writing the same chunk of
+// blocks 0..7, and eight readers of one block, hit eight different bank groups.
+__device__ __forceinline__ int chunk_pos(int b, int c) { return 64 * b + 16 * (c ^ ((b >> 1) & 3)); }
+
+// Converts the stage's raw Q8_0 segments (272 bytes per pair, pairs past np
+// read as zero) for the first 8 * NT pairs: item = (token it / 8, block it % 8).
+// Chunk c of a block holds k = [2c, 2c+1 | 2c+8, 2c+9 | 16+2c, 17+2c | 24+2c, 25+2c],
+// the order lane t = c of an m16n8k16 B fragment reads with one 16-byte load.
+template <int NT>
+__device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, int np, int ct) {
+    float* sclf = reinterpret_cast<float*>(sm.scl);
+    for (int it = ct; it < 8 * NT * SEGB; it += CONSUMERS * 32) {
+        const int tk = it >> 3, b = it & 7;
+        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        float d = 0.0f;
+        int sx = 0;
+        if (tk < np) {
+            const uint16_t* src = reinterpret_cast<const uint16_t*>(raw + tk * RAWA + b * 34);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                w[j] = static_cast<uint32_t>(src[1 + 2 * j]) | (static_cast<uint32_t>(src[2 + 2 * j]) << 16);
+                sx = __dp4a(static_cast<int>(w[j]), 0x01010101, sx);
+            }
+            d = h2f(src[0]);
+        }
+        uint32_t hv[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s8x4_to_half(w[j], hv[2 * j], hv[2 * j + 1]);
+        uint8_t* row = sm.act + tk * ACT_PITCH;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(row + chunk_pos(b, c)) = make_uint4(hv[c], hv[c + 4], hv[c + 8], hv[c + 12]);
+        float* e = sclf + (b * SCL_PITCH + (tk >> 1)) * 4 + (tk & 1);
+        e[0] = d;
+        e[2] = static_cast<float>(-1032 * sx);
+    }
+}
+
+// Row g and g + 8 of a 16-row slice, one 32-block: the two k-steps' A
+// fragments (1024 + n) and the rows' d_w as (d, d) pairs.
+__device__ __forceinline__ void load_wfrag(const uint8_t* w0, int t, uint32_t (&f0)[4], uint32_t (&f1)[4],
+                                           uint64_t& d0, uint64_t& d1) {
+    const uint8_t* w1 = w0 + 8 * (SEGB * 18);
+    const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + 2);
+    const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + 2);
+    q4_biased(q0[t], f0[0], f1[0]);
+    q4_biased(q1[t], f0[1], f1[1]);
+    q4_biased(q0[t + 4], f0[2], f1[2]);
+    q4_biased(q1[t + 4], f0[3], f1[3]);
+    const float a = h2f(*reinterpret_cast<const uint16_t*>(w0));
+    const float c = h2f(*reinterpret_cast<const uint16_t*>(w1));
+    d0 = tc::pk(a, a);
+    d1 = tc::pk(c, c);
+}
+
+// One pass over the expert's K for up to 8 * NT pairs. Accumulators hold
+// (pair 8n + 2t, 8n + 2t + 1) of rows g (index 0) and g + 8 (index 1); per
+// 32-block, isum comes exactly out of two chained fp16 MMAs and
+// y = fma(d_w * d_x, isum, y) runs two pairs per f32x2 instruction.
+template <bool UP, int NT>
+__device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, int S, int nseg, int64_t& k, int np,
+                                      int r0) {
+    constexpr int NMAT = UP ? 2 : 1;
+    constexpr int STAGE = NMAT * BOX_BYTES + RAWA_BYTES;
+    const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
+    const int g = lane >> 2, t = lane & 3;
+    uint64_t ya[NT][2], yb[NT][2];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) ya[n][0] = ya[n][1] = yb[n][0] = yb[n][1] = 0;
+    for (int seg = 0; seg < nseg; ++seg, ++k) {
+        const int st = static_cast<int>(k % S);
+        const bool got = mbar_wait_bounded(&sm.full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS);
+        if (!tc::named_and(2, CONSUMERS * 32, got)) {
+            if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+        const uint8_t* stage = sm.wst + st * STAGE;
+        convert_acts<NT>(stage + NMAT * BOX_BYTES, sm, np, ct);
+        tc::named_and(1, CONSUMERS * 32, true);
+        const uint8_t* wa = stage + (16 * warp + g) * (SEGB * 18);
+#pragma unroll 1
+        for (int b = 0; b < SEGB; ++b) {
+            uint32_t fa0[4], fa1[4], fb0[4], fb1[4];
+            uint64_t dwa0, dwa1, dwb0 = 0, dwb1 = 0;
+            load_wfrag(wa + b * 18, t, fa0, fa1, dwa0, dwa1);
+            if constexpr (UP) load_wfrag(wa + BOX_BYTES + b * 18, t, fb0, fb1, dwb0, dwb1);
+            const uint8_t* ab = sm.act + g * ACT_PITCH + chunk_pos(b, t);
+            const float4* sb = sm.scl + b * SCL_PITCH + t;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const uint4 bv = *reinterpret_cast<const uint4*>(ab + 8 * n * ACT_PITCH);
+                const float4 sv = sb[4 * n];
+                const uint64_t dx = tc::pk(sv.x, sv.y);
+                float c[4];
+                mma16816c(c, fa0, bv.x, bv.y, sv.z, sv.w);
+                mma16816acc(c, fa1, bv.z, bv.w);
+                ya[n][0] = tc::fma2(tc::mul2(dwa0, dx), tc::pk(c[0], c[1]), ya[n][0]);
+                ya[n][1] = tc::fma2(tc::mul2(dwa1, dx), tc::pk(c[2], c[3]), ya[n][1]);
+                if constexpr (UP) {
+                    mma16816c(c, fb0, bv.x, bv.y, sv.z, sv.w);
+                    mma16816acc(c, fb1, bv.z, bv.w);
+                    yb[n][0] = tc::fma2(tc::mul2(dwb0, dx), tc::pk(c[0], c[1]), yb[n][0]);
+                    yb[n][1] = tc::fma2(tc::mul2(dwb1, dx), tc::pk(c[2], c[3]), yb[n][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&sm.empty[st]);
+        tc::named_and(1, CONSUMERS * 32, true);     // the fp16 tile is rewritten by the next segment
+    }
+    // Results: rows r0 + 16w + g (+8), pairs 8n + 2t (+1).
+    const int f = r0 + 16 * warp + g;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float a[2], u[2];
+            tc::upk(ya[n][h], a[0], a[1]);
+            tc::upk(yb[n][h], u[0], u[1]);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int tk = 8 * n + 2 * t + i;
+                const int pr = tk < np ? sm.pairs[tk] : -1;
+                if (pr >= 0) {
+                    float v;
+                    if constexpr (UP) {
+                        v = __fmul_rn(__fdiv_rn(a[i], __fadd_rn(1.0f, expf(-a[i]))), u[i]);
+                    } else {
+                        v = a[i];
+                    }
+                    p.out[static_cast<int64_t>(pr) * p.rows_per_expert + f + 8 * h] = v;
+                }
+            }
+        }
+    }
+    return true;
+}
+
 template <bool UP>
 __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_constant__ CUtensorMap map0,
                                                              const __grid_constant__ CUtensorMap map1,
                                                              const MoeMmaParams p) {
     constexpr int NMAT = UP ? 2 : 1;
-    constexpr int STAGE = NMAT * BOX_BYTES + RAWA_BYTES;      // weight boxes, then the tokens' raw segments
+    constexpr int STAGE = NMAT * BOX_BYTES + RAWA_BYTES;      // weight boxes, then the pairs' raw segments
     extern __shared__ __align__(1024) uint8_t smem[];
     const int S = p.stages;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + 8;
-    int* pairs = reinterpret_cast<int*>(smem + 256);                   // [TOK] pair ids of the pass
-    uint8_t* act = smem + 1024;                                         // [TOK][ACT_PITCH] fp16
-    float* scl = reinterpret_cast<float*>(act + ACT_BYTES);             // [TOK][SEGB]
-    uint8_t* wst = smem + 1024 + ACT_BYTES + SCL_BYTES;                 // [S][STAGE]
+    Smem sm;
+    sm.full = reinterpret_cast<uint64_t*>(smem);
+    sm.empty = sm.full + 8;
+    sm.pairs = reinterpret_cast<int*>(smem + 256);
+    sm.act = smem + 1024;
+    sm.scl = reinterpret_cast<float4*>(sm.act + ACT_BYTES);
+    sm.wst = smem + 1024 + ACT_BYTES + SCL_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.y, r0 = blockIdx.x * ROWS;
     const int beg = p.offs[e], cnt = p.offs[e + 1] - beg;
@@ -105,8 +268,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], CONSUMERS);
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], CONSUMERS);
         }
         fence_mbar_init();
     }
@@ -123,22 +286,23 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
             const int np = min(TOK, cnt - pass * TOK);
             bool ok = true;
             if (lane == 0) {
-                ok = mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((k / S) & 1) ^ 1), WAIT_LIMIT_NS);
+                ok = mbar_wait_bounded(&sm.empty[st], static_cast<uint32_t>(((k / S) & 1) ^ 1), WAIT_LIMIT_NS);
                 if (!ok) {
                     atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
                 } else {
-                    mbar_arrive_expect_tx(&full[st], NMAT * BOX_BYTES + np * RAWA);
-                    uint8_t* dst = wst + st * STAGE;
-                    tc::tma_load_2d(dst, &map0, seg * SEGB * 9, row_base, &full[st]);   // 9 = 18 bytes / 2
-                    if (UP) tc::tma_load_2d(dst + BOX_BYTES, &map1, seg * SEGB * 9, row_base, &full[st]);
+                    mbar_arrive_expect_tx(&sm.full[st], NMAT * BOX_BYTES + np * RAWA);
+                    uint8_t* dst = sm.wst + st * STAGE;
+                    tc::tma_load_2d(dst, &map0, seg * SEGB * 9, row_base, &sm.full[st]);   // 9 = 18 bytes / 2
+                    if (UP) tc::tma_load_2d(dst + BOX_BYTES, &map1, seg * SEGB * 9, row_base, &sm.full[st]);
                 }
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            uint8_t* raw = wst + st * STAGE + NMAT * BOX_BYTES;
+            uint8_t* raw = sm.wst + st * STAGE + NMAT * BOX_BYTES;
             for (int i = lane; i < np; i += 32) {
                 const int pr = p.perm[beg + pass * TOK + i];
                 const int64_t row = UP ? pr / p.topk : pr;
-                bulk_g2s(raw + i * RAWA, p.xq + row * p.xrow + static_cast<int64_t>(seg) * RAWA, RAWA, &full[st], pol);
+                bulk_g2s(raw + i * RAWA, p.xq + row * p.xrow + static_cast<int64_t>(seg) * RAWA, RAWA, &sm.full[st],
+                         pol);
             }
             if (++seg == nseg) { seg = 0; ++pass; }
         }
@@ -146,132 +310,22 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
     }
 
     // ---------------------------------------------------------- consumers
-    const int ct = threadIdx.x;              // 0..255
-    const int g = lane >> 2, t = lane & 3;
     int64_t k = 0;
     for (int pass = 0; pass < passes; ++pass) {
         const int np = min(TOK, cnt - pass * TOK);
-        const int nt = (np + 7) >> 3;
-        if (ct < TOK) pairs[ct] = ct < np ? p.perm[beg + pass * TOK + ct] : -1;
-        float ya[NTM][4], yb[NTM][4];
-#pragma unroll
-        for (int n = 0; n < NTM; ++n)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { ya[n][i] = 0.0f; yb[n][i] = 0.0f; }
-        bool ok = true;
-        for (int seg = 0; seg < nseg; ++seg, ++k) {
-            const int st = static_cast<int>(k % S);
-            const bool got = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS);
-            if (!tc::named_and(2, CONSUMERS * 32, got)) {
-                if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
-                ok = false;
-                break;
-            }
-            // Convert the stage's raw Q8_0 segments: item i = (token i / 8, block i % 8),
-            // fp16 in the order lane t of an n-tile reads as one 16-byte load:
-            // [k=2t,2t+1 | 2t+8,+9 | 16+2t,+1 | 24+2t,+1] per t. Tokens past np are zero.
-            const uint8_t* raw = wst + st * (NMAT * BOX_BYTES + RAWA_BYTES) + NMAT * BOX_BYTES;
-            for (int it = ct; it < TOK * SEGB; it += CONSUMERS * 32) {
-                const int tk = it >> 3, b = it & 7;
-                uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                float d = 0.0f;
-                if (tk < np) {
-                    const uint16_t* src = reinterpret_cast<const uint16_t*>(raw + tk * RAWA + b * 34);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        w[j] = static_cast<uint32_t>(src[1 + 2 * j]) | (static_cast<uint32_t>(src[2 + 2 * j]) << 16);
-                    d = h2f(src[0]);
-                }
-                uint32_t hv[16];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) s8x4_to_half(w[j], hv[2 * j], hv[2 * j + 1]);
-                uint4* dst = reinterpret_cast<uint4*>(act + tk * ACT_PITCH + 64 * b);
-#pragma unroll
-                for (int tt = 0; tt < 4; ++tt) dst[tt] = make_uint4(hv[tt], hv[tt + 4], hv[tt + 8], hv[tt + 12]);
-                scl[tk * SEGB + b] = d;
-            }
-            tc::named_and(1, CONSUMERS * 32, true);
-            const uint8_t* wa = wst + st * (NMAT * BOX_BYTES + RAWA_BYTES) + (16 * warp + g) * (SEGB * 18);
-#pragma unroll 1
-            for (int b = 0; b < SEGB; ++b) {
-                uint32_t fa0[4], fa1[4], fb0[4], fb1[4];
-                float dwa0, dwa1, dwb0 = 0.0f, dwb1 = 0.0f;
-                {
-                    const uint8_t* w0 = wa + b * 18;
-                    const uint8_t* w1 = w0 + 8 * (SEGB * 18);
-                    const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + 2);
-                    const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + 2);
-                    const uint32_t x0 = q0[t], x1 = q0[t + 4], z0 = q1[t], z1 = q1[t + 4];
-                    fa0[0] = q4_pair(x0, false); fa0[1] = q4_pair(z0, false);
-                    fa0[2] = q4_pair(x1, false); fa0[3] = q4_pair(z1, false);
-                    fa1[0] = q4_pair(x0, true); fa1[1] = q4_pair(z0, true);
-                    fa1[2] = q4_pair(x1, true); fa1[3] = q4_pair(z1, true);
-                    dwa0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
-                    dwa1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
-                }
-                if constexpr (UP) {
-                    const uint8_t* w0 = wa + BOX_BYTES + b * 18;
-                    const uint8_t* w1 = w0 + 8 * (SEGB * 18);
-                    const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + 2);
-                    const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + 2);
-                    const uint32_t x0 = q0[t], x1 = q0[t + 4], z0 = q1[t], z1 = q1[t + 4];
-                    fb0[0] = q4_pair(x0, false); fb0[1] = q4_pair(z0, false);
-                    fb0[2] = q4_pair(x1, false); fb0[3] = q4_pair(z1, false);
-                    fb1[0] = q4_pair(x0, true); fb1[1] = q4_pair(z0, true);
-                    fb1[2] = q4_pair(x1, true); fb1[3] = q4_pair(z1, true);
-                    dwb0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
-                    dwb1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
-                }
-#pragma unroll
-                for (int n = 0; n < NTM; ++n) {
-                    if (n < nt) {
-                        const uint4 bv = *reinterpret_cast<const uint4*>(act + (8 * n + g) * ACT_PITCH + 64 * b + 16 * t);
-                        const float dx0 = scl[(8 * n + 2 * t) * SEGB + b];
-                        const float dx1 = scl[(8 * n + 2 * t + 1) * SEGB + b];
-                        float c0[4], c1[4];
-                        mma16816(c0, fa0, bv.x, bv.y);
-                        mma16816(c1, fa1, bv.z, bv.w);
-                        ya[n][0] = __fmaf_rn(__fmul_rn(dwa0, dx0), c0[0] + c1[0], ya[n][0]);
-                        ya[n][1] = __fmaf_rn(__fmul_rn(dwa0, dx1), c0[1] + c1[1], ya[n][1]);
-                        ya[n][2] = __fmaf_rn(__fmul_rn(dwa1, dx0), c0[2] + c1[2], ya[n][2]);
-                        ya[n][3] = __fmaf_rn(__fmul_rn(dwa1, dx1), c0[3] + c1[3], ya[n][3]);
-                        if constexpr (UP) {
-                            mma16816(c0, fb0, bv.x, bv.y);
-                            mma16816(c1, fb1, bv.z, bv.w);
-                            yb[n][0] = __fmaf_rn(__fmul_rn(dwb0, dx0), c0[0] + c1[0], yb[n][0]);
-                            yb[n][1] = __fmaf_rn(__fmul_rn(dwb0, dx1), c0[1] + c1[1], yb[n][1]);
-                            yb[n][2] = __fmaf_rn(__fmul_rn(dwb1, dx0), c0[2] + c1[2], yb[n][2]);
-                            yb[n][3] = __fmaf_rn(__fmul_rn(dwb1, dx1), c0[3] + c1[3], yb[n][3]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[st]);
-            tc::named_and(1, CONSUMERS * 32, true);     // the fp16 tile is rewritten by the next segment
+        if (threadIdx.x < TOK) sm.pairs[threadIdx.x] = threadIdx.x < np ? p.perm[beg + pass * TOK + threadIdx.x] : -1;
+        bool ok;
+        switch ((np + 7) >> 3) {
+            case 1: ok = run_pass<UP, 1>(p, sm, S, nseg, k, np, r0); break;
+            case 2: ok = run_pass<UP, 2>(p, sm, S, nseg, k, np, r0); break;
+            case 3: ok = run_pass<UP, 3>(p, sm, S, nseg, k, np, r0); break;
+            case 4: ok = run_pass<UP, 4>(p, sm, S, nseg, k, np, r0); break;
+            case 5: ok = run_pass<UP, 5>(p, sm, S, nseg, k, np, r0); break;
+            case 6: ok = run_pass<UP, 6>(p, sm, S, nseg, k, np, r0); break;
+            case 7: ok = run_pass<UP, 7>(p, sm, S, nseg, k, np, r0); break;
+            default: ok = run_pass<UP, 8>(p, sm, S, nseg, k, np, r0); break;
         }
         if (!ok) break;
-        // Results: rows r0 + 16w + g (+8), pairs 8n + 2t (+1).
-        const int f = r0 + 16 * warp + g;
-#pragma unroll
-        for (int n = 0; n < NTM; ++n) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tk = 8 * n + 2 * t + (i & 1);
-                const int pr = tk < np ? pairs[tk] : -1;
-                if (n < nt && pr >= 0) {
-                    const int row = f + (i >= 2 ? 8 : 0);
-                    float v;
-                    if constexpr (UP) {
-                        const float gg = ya[n][i], uu = yb[n][i];
-                        v = __fmul_rn(__fdiv_rn(gg, __fadd_rn(1.0f, expf(-gg))), uu);
-                    } else {
-                        v = ya[n][i];
-                    }
-                    p.out[static_cast<int64_t>(pr) * p.rows_per_expert + row] = v;
-                }
-            }
-        }
         tc::named_and(1, CONSUMERS * 32, true);     // pairs[] is rewritten by the next pass
     }
 }
