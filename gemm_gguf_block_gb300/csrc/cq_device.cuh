@@ -31,6 +31,16 @@ __host__ __device__ constexpr int achunk_bytes(int afmt) {
     return afmt == CQ_Q8_0 ? ACHUNK_Q8_0 : afmt == CQ_Q8_1 ? ACHUNK_Q8_1 : afmt == CQ_Q8_K ? ACHUNK_Q8_K : 0;
 }
 
+// One int8 quant of a Q8 block: round(v * id) to nearest, ties away from
+// zero, clamped to [-127, 127]; id = 1/d, d = amax / 127, all fp32 RN.
+__device__ __forceinline__ int quant_q8(float v, float id) {
+    float r = roundf(__fmul_rn(v, id));
+    r = fminf(fmaxf(r, -127.0f), 127.0f);
+    return static_cast<int>(r);
+}
+__device__ __forceinline__ float q8_scale(float amax) { return __fdiv_rn(amax, 127.0f); }
+__device__ __forceinline__ float q8_inv(float d) { return d != 0.0f ? __frcp_rn(d) : 0.0f; }
+
 __device__ __forceinline__ float h2f(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xffffu)));
 }

@@ -68,10 +68,16 @@ __device__ __forceinline__ int* ws_perm(const MoeParams& p) { return reinterpret
 __device__ __forceinline__ int* ws_valid(const MoeParams& p) { return reinterpret_cast<int*>(p.ws + p.L.valid); }
 
 // ------------------------------------------------------------------ route
+// Pairs whose routing keys are staged in shared memory; larger batches read
+// them from global memory instead.
+constexpr int ROUTE_SMEM_PAIRS = 8192;
+
 __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
     __shared__ int cnt[256];
     __shared__ int off[257];
+    __shared__ int key_s[ROUTE_SMEM_PAIRS];   // expert of a valid pair, -1 for an invalid one
     const int P = p.T * p.topk;
+    const bool staged = P <= ROUTE_SMEM_PAIRS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     int* valid = ws_valid(p);
     int* status = ws_status(p);
@@ -88,15 +94,16 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
                 if (p.ids[t * p.topk + s2] == e) flag = CQ_DEV_DUP_EXPERT_ID;
         }
         valid[i] = flag == 0;
+        if (staged) key_s[i] = flag == 0 ? e : -1;
         if (flag) atomicOr(status, flag);
     }
-    __syncthreads();   // valid[] written by this CTA: visible to it after the barrier
+    __syncthreads();   // valid[] and key_s[] written by this CTA: visible to it after the barrier
+    auto key = [&](int i) { return staged ? key_s[i] : (valid[i] ? p.ids[i] : -1); };
     for (int e = warp; e < p.E; e += nwarps) {
         int c = 0;
         for (int base = 0; base < P; base += 32) {
             const int i = base + lane;
-            const bool hit = i < P && valid[i] && p.ids[i] == e;
-            c += __popc(__ballot_sync(0xffffffffu, hit));
+            c += __popc(__ballot_sync(0xffffffffu, i < P && key(i) == e));
         }
         if (lane == 0) cnt[e] = c;
     }
@@ -114,7 +121,7 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
         int pos = off[e];
         for (int base = 0; base < P; base += 32) {
             const int i = base + lane;
-            const bool hit = i < P && valid[i] && p.ids[i] == e;
+            const bool hit = i < P && key(i) == e;
             const unsigned m = __ballot_sync(0xffffffffu, hit);
             if (hit) perm[pos + __popc(m & ((1u << lane) - 1u))] = i;
             pos += __popc(m);
@@ -218,12 +225,10 @@ __global__ void __launch_bounds__(THREADS) moe_up_kernel(const MoeParams p) {
             float amax = fabsf(h);
 #pragma unroll
             for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float d = __fdiv_rn(amax, 127.0f);
-            const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
-            float r = roundf(__fmul_rn(h, id));
-            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            const float d = q8_scale(amax);
+            const float id = q8_inv(d);
             uint8_t* blk = hqbase + static_cast<size_t>(pair) * hq_row + (f0 / 32) * 34;
-            blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(r)));
+            blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(quant_q8(h, id)));
             if (lane == 0) *reinterpret_cast<__half*>(blk) = __float2half_rn(d);
         }
         __syncthreads();
@@ -289,20 +294,26 @@ __global__ void __launch_bounds__(THREADS) moe_down_kernel(const MoeParams p) {
 }
 
 // ---------------------------------------------------------------- combine
+// y[t] = sum over the token's valid slots s, in increasing s, of rw * o; one
+// CTA row per token, four consecutive outputs per thread.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
-    const int64_t n = static_cast<int64_t>(p.T) * p.K;
+    const int t = blockIdx.x;
+    const int k = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
+    if (k >= p.K) return;
     const int* valid = ws_valid(p);
     const float* out = reinterpret_cast<const float*>(p.ws + p.L.out);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / p.K), k = static_cast<int>(i - static_cast<int64_t>(t) * p.K);
-        float acc = 0.0f;
-        for (int s = 0; s < p.topk; ++s) {
-            const int pair = t * p.topk + s;
-            if (valid[pair]) acc = __fmaf_rn(p.rw[pair], out[static_cast<size_t>(pair) * p.K + k], acc);
-        }
-        p.y[i] = acc;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.topk; ++s) {
+        const int pair = t * p.topk + s;
+        if (!valid[pair]) continue;
+        const float w = p.rw[pair];
+        const float4 o = *reinterpret_cast<const float4*>(out + static_cast<size_t>(pair) * p.K + k);
+        acc.x = __fmaf_rn(w, o.x, acc.x);
+        acc.y = __fmaf_rn(w, o.y, acc.y);
+        acc.z = __fmaf_rn(w, o.z, acc.z);
+        acc.w = __fmaf_rn(w, o.w, acc.w);
     }
+    *reinterpret_cast<float4*>(p.y + static_cast<size_t>(t) * p.K + k) = acc;
 }
 
 }  // namespace
@@ -372,9 +383,7 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
         moe_down_kernel<<<dim3(K / TILE, E), THREADS, smem_dn, s>>>(p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const int64_t n = static_cast<int64_t>(T) * K;
-    const unsigned grid = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 4096));
-    moe_combine_kernel<<<grid, 256, 0, s>>>(p);
+    moe_combine_kernel<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>((K / 4 + 255) / 256)), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

@@ -15,8 +15,9 @@
 // mma.sync m16n8k16 product (two chained k-steps; every partial sum is an
 // integer below 2^23), and the block's scale term is accumulated as
 // y = fma(d_w * d_x, isum, y) in increasing k.
-//   up:   warp w computes gate and up rows f0+16w.. for the pairs, then writes
-//         h = silu(g) * u (fp32) for the valid pairs into the workspace.
+//   up:   warp w computes gate and up rows f0+16w.. for the pairs; the CTA
+//         then writes h = silu(g) * u (fp32) and its Q8_0 blocks hq for the
+//         valid pairs into the workspace.
 //   down: o = W_down[e] . hq for the pairs, written into the workspace.
 #include <algorithm>
 #include <mutex>
@@ -51,6 +52,7 @@ struct MoeMmaParams {
     const int* offs;            // [E+1]
     const int* perm;            // pairs grouped by expert
     float* out;                 // up: h [P][F]; down: o [P][Kout]
+    uint8_t* hq;                // up: Q8_0 of h, [P] rows of F/32 blocks
     int* status;
     int topk;
     int rows_per_expert;        // up: F; down: K (d_model)
@@ -214,27 +216,66 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
         if (lane == 0) tc::mbar_arrive(&sm.empty[st]);
         tc::named_and(1, CONSUMERS * 32, true);     // the fp16 tile is rewritten by the next segment
     }
-    // Results: rows r0 + 16w + g (+8), pairs 8n + 2t (+1).
-    const int f = r0 + 16 * warp + g;
+    if constexpr (UP) {
+        // h = silu(g) * u goes to a [pair][HS_PITCH] fp32 tile in the activation
+        // tile's space (free: every consumer is past the last segment's
+        // barrier). Then eight lanes per (pair, 32-row block) write the slice of
+        // h and its Q8_0 block -- the same rule as the activation quantiser.
+        constexpr int HS_PITCH = ROWS + 4;
+        static_assert(TOK * HS_PITCH * 4 <= ACT_BYTES, "h tile does not fit");
+        float* hs = reinterpret_cast<float*>(sm.act);
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
+        for (int n = 0; n < NT; ++n) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float a[2], u[2];
-            tc::upk(ya[n][h], a[0], a[1]);
-            tc::upk(yb[n][h], u[0], u[1]);
+            for (int h = 0; h < 2; ++h) {
+                float a[2], u[2];
+                tc::upk(ya[n][h], a[0], a[1]);
+                tc::upk(yb[n][h], u[0], u[1]);
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int tk = 8 * n + 2 * t + i;
-                const int pr = tk < np ? sm.pairs[tk] : -1;
-                if (pr >= 0) {
-                    float v;
-                    if constexpr (UP) {
-                        v = __fmul_rn(__fdiv_rn(a[i], __fadd_rn(1.0f, expf(-a[i]))), u[i]);
-                    } else {
-                        v = a[i];
-                    }
-                    p.out[static_cast<int64_t>(pr) * p.rows_per_expert + f + 8 * h] = v;
+                for (int i = 0; i < 2; ++i)
+                    hs[(8 * n + 2 * t + i) * HS_PITCH + 16 * warp + g + 8 * h] =
+                        __fmul_rn(__fdiv_rn(a[i], __fadd_rn(1.0f, expf(-a[i]))), u[i]);
+            }
+        }
+        tc::named_and(1, CONSUMERS * 32, true);
+        const int sub = lane & 7;
+        const int64_t hq_row = static_cast<int64_t>(p.rows_per_expert / 32) * 34;
+        // 4 * np items, four per warp and iteration: the trip count is warp-uniform.
+        for (int it = 4 * warp + (lane >> 3); it < 4 * np; it += 4 * CONSUMERS) {
+            const int tk = it >> 2, j = it & 3;
+            const int pr = sm.pairs[tk];
+            const float4 v = *reinterpret_cast<const float4*>(hs + tk * HS_PITCH + 32 * j + 4 * sub);
+            *reinterpret_cast<float4*>(p.out + static_cast<int64_t>(pr) * p.rows_per_expert + r0 + 32 * j + 4 * sub) = v;
+            float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+            const float d = q8_scale(a);
+            const float id = q8_inv(d);
+            const uint32_t q = (static_cast<uint32_t>(quant_q8(v.x, id)) & 0xffu) |
+                               ((static_cast<uint32_t>(quant_q8(v.y, id)) & 0xffu) << 8) |
+                               ((static_cast<uint32_t>(quant_q8(v.z, id)) & 0xffu) << 16) |
+                               (static_cast<uint32_t>(quant_q8(v.w, id)) << 24);
+            uint8_t* blk = p.hq + pr * hq_row + ((r0 >> 5) + j) * 34;
+            uint16_t* q16 = reinterpret_cast<uint16_t*>(blk + 2 + 4 * sub);     // 2 mod 4: 16-bit stores
+            q16[0] = static_cast<uint16_t>(q);
+            q16[1] = static_cast<uint16_t>(q >> 16);
+            if (sub == 0) *reinterpret_cast<__half*>(blk) = __float2half_rn(d);
+        }
+    } else {
+        // o rows r0 + 16w + g (+8), pairs 8n + 2t (+1).
+        const int f = r0 + 16 * warp + g;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float a[2];
+                tc::upk(ya[n][h], a[0], a[1]);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int tk = 8 * n + 2 * t + i;
+                    const int pr = tk < np ? sm.pairs[tk] : -1;
+                    if (pr >= 0) p.out[static_cast<int64_t>(pr) * p.rows_per_expert + f + 8 * h] = a[i];
                 }
             }
         }
@@ -399,14 +440,13 @@ cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, i
     up.offs = offs;
     up.perm = perm;
     up.out = h;
+    up.hq = static_cast<uint8_t*>(const_cast<void*>(hq));
     up.status = dev.status;
     up.topk = topk;
     up.rows_per_expert = F;
     up.kin = K;
     up.xrow = static_cast<int64_t>(K / 32) * 34;
     cudaError_t e = launch_one<true>(dev, mg, mu, up, E, s);
-    if (e != cudaSuccess) return e;
-    e = launch_quantize(CQ_Q8_0, static_cast<int64_t>(T) * topk, F, h, const_cast<void*>(hq), s);
     if (e != cudaSuccess) return e;
     MoeMmaParams dn = up;
     dn.xq = static_cast<const uint8_t*>(hq);
