@@ -181,6 +181,32 @@ def run_reference(args, rank, world):
     _ = gb
 
 
+# ------------------------------------------------------------- multi-rank
+def dist_init(world):
+    """gloo process group for the replicas' barrier and timing reduction (None at N=1)."""
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, v):
+    """The largest of every rank's value (a no-op without a process group)."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def aggregate_gbs(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job rate: every rank streams its own replica's bytes per step."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------- GPU timing
 def _flush(torch, buf):
     buf.add_(1)  # touch 256 MB: evicts the 129 MB L2
@@ -204,81 +230,142 @@ def time_calls(torch, fn, iters, warmup, flush=None):
     return statistics.median(times)
 
 
-def secondary(torch, cq, synth, peaks, seed):
-    out = {}
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-    flushbuf = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
-    flush = lambda: _flush(torch, flushbuf)
-    stream = lambda: torch.cuda.current_stream().cuda_stream
+class _Ctx:
+    """Device helpers shared by the secondary workloads."""
 
-    # prefill GEMM: Q4_K, M=512, K=4096, N=14336
+    def __init__(self, torch, iters=10, warmup=3):
+        self.torch = torch
+        self.iters, self.warmup = iters, warmup
+        self.flushbuf = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+
+    def dev(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    def flush(self):
+        _flush(self.torch, self.flushbuf)
+
+    def stream(self):
+        return self.torch.cuda.current_stream().cuda_stream
+
+    def time(self, fn, flush=True):
+        return time_calls(self.torch, fn, self.iters, self.warmup, self.flush if flush else None)
+
+
+def case_gemm(c, cq, synth, peaks, seed):
+    """Prefill GEMM: Q4_K, M=512, K=4096, N=14336."""
     W, x = synth.prefill_q4_k(seed)
     M, K = x.shape
     N = W.shape[0]
-    Wd, xd = dev(W), dev(x)
+    Wd, xd = c.dev(W), c.dev(x)
     xq = cq.quantize_act_t(xd, cq.Q8_K)
-    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    fn = lambda: cq.cq_gemm(cq.Q4_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
-    ms = time_calls(torch, fn, 10, 3, flush)
+    y = c.torch.empty((M, N), dtype=c.torch.float32, device="cuda")
+    ms = c.time(lambda: cq.cq_gemm(cq.Q4_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
     tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
-    out["prefill_gemm_q4_k"] = {"shape": f"M={M} N={N} K={K}", "ms": ms, "int8_equiv_tops": tops,
-                                "peak_tflops": peaks["bf16"], "peak_note": "fp16 tensor peak = measured bf16 x 1",
-                                "frac": tops / peaks["bf16"]}
-    del Wd, xd, xq, y
+    return {"shape": f"M={M} N={N} K={K}", "ms": ms, "int8_equiv_tops": tops, "peak_tflops": peaks["bf16"],
+            "peak_note": "fp16 tensor peak = measured bf16 x 1", "frac": tops / peaks["bf16"]}
 
-    # routed-expert FFN: 256 tokens, 32 experts, top-4, Q4_0 2048/1792
+
+def case_moe(c, cq, synth, peaks, seed):
+    """Routed-expert FFN: 256 tokens, 32 experts, top-4, Q4_0 2048/1792."""
     Wg, Wu, Wdn, ids, rw, x = synth.moe_ffn(seed)
     T, K = x.shape
-    F = Wg.shape[1]
-    tg, tu, td, ti, tr, tx = (dev(a) for a in (Wg, Wu, Wdn, ids, rw, x))
+    F, E = Wg.shape[1], Wg.shape[0]
+    tg, tu, td, ti, tr, tx = (c.dev(a) for a in (Wg, Wu, Wdn, ids, rw, x))
     xq = cq.quantize_act_t(tx, cq.Q8_0)
-    need = cq.cq_moe_workspace_size(T, K, F, 32, 4)
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    y = torch.empty((T, K), dtype=torch.float32, device="cuda")
-    fn = lambda: cq.cq_moe_gemv(cq.Q4_0, T, K, F, 32, 4, tg.data_ptr(), tu.data_ptr(), td.data_ptr(),
-                                ti.data_ptr(), tr.data_ptr(), xq.data_ptr(), y.data_ptr(), ws.data_ptr(), need,
-                                stream())
-    ms = time_calls(torch, fn, 10, 3, flush)
+    need = cq.cq_moe_workspace_size(T, K, F, E, 4)
+    ws = c.torch.empty(need, dtype=c.torch.uint8, device="cuda")
+    y = c.torch.empty((T, K), dtype=c.torch.float32, device="cuda")
+    ms = c.time(lambda: cq.cq_moe_gemv(cq.Q4_0, T, K, F, E, 4, tg.data_ptr(), tu.data_ptr(), td.data_ptr(),
+                                       ti.data_ptr(), tr.data_ptr(), xq.data_ptr(), y.data_ptr(), ws.data_ptr(),
+                                       need, c.stream()))
     wbytes = Wg.nbytes + Wu.nbytes + Wdn.nbytes
     ops = 2.0 * T * 4 * 3 * F * K
-    out["moe_q4_0"] = {"shape": f"T={T} E=32 top4 K={K} F={F}", "ms": ms, "weight_gbs": wbytes / ms / 1e6,
-                       "int8_equiv_tops": ops / (ms * 1e-3) / 1e12, "hbm_frac": wbytes / ms / 1e6 / peaks["hbm"]}
-    del tg, tu, td, ti, tr, tx, xq, ws, y
+    return {"shape": f"T={T} E={E} top4 K={K} F={F}", "ms": ms, "weight_gbs": wbytes / ms / 1e6,
+            "int8_equiv_tops": ops / (ms * 1e-3) / 1e12, "hbm_frac": wbytes / ms / 1e6 / peaks["hbm"]}
 
-    # batched LM head verify: Q4_1 128256x4096, M = 1, 4, 8, 16
+
+def case_lm_head(c, cq, synth, peaks, seed, ms_list=(1, 4, 8, 16)):
+    """Batched LM head: Q4_1 128256x4096 at M tokens."""
     W, x = synth.lm_head_q4_1(seed)
     N, K = W.shape[0], x.shape[1]
-    Wd, xd = dev(W), dev(x)
+    Wd, xd = c.dev(W), c.dev(x)
     xq = cq.quantize_act_t(xd, cq.Q8_1)
     res = {}
-    for M in (1, 4, 8, 16):
-        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        fn = lambda: cq.cq_gemv(cq.Q4_1, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
-        ms = time_calls(torch, fn, 10, 3, flush)
-        res[str(M)] = {"ms": ms, "weight_gbs": W.nbytes / ms / 1e6}
-    for M in res:
-        res[M]["t_over_t1"] = res[M]["ms"] / res["1"]["ms"]
-    out["lm_head_q4_1"] = res
-    del Wd, xd, xq
+    for M in ms_list:
+        y = c.torch.empty((M, N), dtype=c.torch.float32, device="cuda")
+        ms = c.time(lambda: cq.cq_gemv(cq.Q4_1, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
+        res[str(M)] = {"ms": ms, "weight_gbs": W.nbytes / ms / 1e6, "hbm_frac": W.nbytes / ms / 1e6 / peaks["hbm"]}
+    if "1" in res:
+        for M in res:
+            res[M]["t_over_t1"] = res[M]["ms"] / res["1"]["ms"]
+    return res
 
-    # small Q4_0 GEMV 2048x2048: single-call latency (L2-resident) and rotated copies
+
+def case_q4_0_small(c, cq, synth, peaks, seed):
+    """Small Q4_0 GEMV 2048x2048 (2.4 MB, fits in L2): the device time of one
+    call, and the rate over 256 distinct copies (576 MiB > L2) replayed
+    back to back as one CUDA graph."""
+    torch = c.torch
     W, x = synth.decode_q4_0_small(seed)
-    N, K = W.shape
     K = x.shape[1]
     copies = 256
-    Wd = dev(np.broadcast_to(W, (copies,) + W.shape).copy())
-    xq = cq.quantize_act_t(dev(x), cq.Q8_0)
+    Wd = c.dev(np.broadcast_to(W, (copies,) + W.shape).copy())
+    xq = cq.quantize_act_t(c.dev(x), cq.Q8_0)
     y = torch.empty((1, 2048), dtype=torch.float32, device="cuda")
-    fn1 = lambda: cq.cq_gemv(cq.Q4_0, 1, 2048, K, Wd[0].data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
-    lat = time_calls(torch, fn1, 50, 10)
-
-    def rot():
+    one = lambda i=0, sh=None: cq.cq_gemv(cq.Q4_0, 1, 2048, K, Wd[i].data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                          sh if sh is not None else c.stream())
+    for _ in range(c.warmup):
+        one()
+    # device time of one call: the stream is held busy while the events and
+    # the call are queued, so host launch overhead stays outside the interval
+    s = torch.cuda.current_stream()
+    lat = []
+    for _ in range(5 * c.iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)
+        a.record(s)
+        one()
+        b.record(s)
+        b.synchronize()
+        lat.append(a.elapsed_time(b))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream().cuda_stream
         for i in range(copies):
-            cq.cq_gemv(cq.Q4_0, 1, 2048, K, Wd[i].data_ptr(), xq.data_ptr(), y.data_ptr(), stream())
-    ms = time_calls(torch, rot, 5, 2)
-    out["decode_q4_0_2048"] = {"single_call_us": lat * 1e3, "rotated_gbs": copies * W.nbytes / ms / 1e6,
-                               "rotation": f"{copies} copies ({copies * W.nbytes / 2**20:.0f} MiB > L2)"}
+            one(i, cs)
+    g.replay()
+    torch.cuda.synchronize()
+    ms = time_calls(torch, g.replay, max(3, c.iters), 2)
+    return {"device_us_one_call": 1e3 * statistics.median(lat), "rotated_gbs": copies * W.nbytes / ms / 1e6,
+            "rotated_us_per_call": 1e3 * ms / copies,
+            "rotation": f"{copies} copies ({copies * W.nbytes / 2**20:.0f} MiB > L2) in one CUDA graph"}
+
+
+CASES = {"prefill_gemm_q4_k": case_gemm, "moe_q4_0": case_moe, "lm_head_q4_1": case_lm_head,
+         "decode_q4_0_2048": case_q4_0_small}
+
+
+def secondary(torch, cq, synth, peaks, seed):
+    c = _Ctx(torch)
+    out = {}
+    for name, fn in CASES.items():
+        out[name] = fn(c, cq, synth, peaks, seed)
+        torch.cuda.empty_cache()
     return out
+
+
+def run_case(args):
+    """One secondary workload alone, `steps` timed calls after `warmup` (for profiling)."""
+    import torch
+    from gemm_gguf_block_gb300 import build as gb, cq, synth
+    gb.build()
+    c = _Ctx(torch, iters=args.steps, warmup=args.warmup)
+    fn = CASES[args.case]
+    kw = {}
+    if args.case == "lm_head_q4_1" and args.m:
+        kw["ms_list"] = tuple(int(v) for v in args.m.split(","))
+    r = fn(c, cq, synth, _peaks(), args.seed, **kw)
+    print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup, "result": r}))
 
 
 def run_cq(args, rank, world, local_rank):
@@ -287,10 +374,7 @@ def run_cq(args, rank, world, local_rank):
 
     gb.build()
     torch.cuda.set_device(local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
+    dist = dist_init(world)
     peaks = _peaks()
     suite = synth.decode_q8_0_suite(args.seed)
     stream = torch.cuda.current_stream()
@@ -368,13 +452,9 @@ def run_cq(args, rank, world, local_rank):
         dist.barrier()
     time.sleep(0.25)
     sampler.stop()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
+    ms = max_over_ranks(dist, e0.elapsed_time(e1))
     ms_step = ms / args.steps
-    value = world * wbytes / (ms_step * 1e-3) / 1e9
+    value = aggregate_gbs(world, wbytes, ms_step)
 
     # Per-launch GEMV durations: the same graph, instrumented with timing events
     # around every GEMV launch (recorded inside the graph), replayed right after
@@ -398,6 +478,8 @@ def run_cq(args, rank, world, local_rank):
     tot_ms = sum(sum(v) for v in gemv_ms)
     achieved = tot_bytes / (tot_ms * 1e-3) / 1e9
     lm_ms = statistics.mean(gemv_ms[-1])
+    lm_bytes = layers[-1]["bytes"]
+    alg_bytes_per_launch = sum(L["bytes"] for L in layers) / len(layers)
     per_shape = {f"{L['N']}x{L['K']}": {"us": 1e3 * statistics.mean(gemv_ms[i]),
                                          "gbs": L["bytes"] / (statistics.mean(gemv_ms[i]) * 1e-3) / 1e9}
                  for i, L in enumerate(layers)}
@@ -423,11 +505,7 @@ def run_cq(args, rank, world, local_rank):
         e2e_step()
     b.record(stream)
     b.synchronize()
-    e2e_ms = a.elapsed_time(b) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / args.steps)
 
     sec = {}
     cpu = None
@@ -452,13 +530,14 @@ def run_cq(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel<Q8_0,1> (all 5 launches of a step)",
                      "timing": timing_src,
                      "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s", "frac": achieved / peaks["hbm"],
-                     "lm_head_launch": {"us": lm_ms * 1e3, "gbs": layers[-1]["bytes"] / (lm_ms * 1e-3) / 1e9,
-                                        "frac": layers[-1]["bytes"] / (lm_ms * 1e-3) / 1e9 / peaks["hbm"]},
+                     "algorithmic_bytes_per_launch": alg_bytes_per_launch,
+                     "lm_head_launch": {"us": lm_ms * 1e3, "gbs": lm_bytes / (lm_ms * 1e-3) / 1e9,
+                                        "frac": lm_bytes / (lm_ms * 1e-3) / 1e9 / peaks["hbm"]},
                      "peak_src": f"{peaks['src']} hbm_gbs (copy, read+write bytes)",
                      "traffic": _traffic("gemv_q8_0_decode_suite.md")},
         "per_shape": per_shape,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * wbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": aggregate_gbs(world, wbytes, e2e_ms), "unit": "GB/s",
                 "h2d_bytes_per_step": sum(4 * x.shape[1] for _, x in suite),
                 "d2h_bytes_per_step": sum(4 * W.shape[0] for W, _ in suite)},
         "gpu_launches": 2 * len(suite) * args.steps,
@@ -477,8 +556,13 @@ def main():
     ap.add_argument("--impl", default="cq", choices=["cq", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--case", choices=sorted(CASES), help="run one secondary workload alone (for profiling)")
+    ap.add_argument("--m", default="", help="with --case lm_head_q4_1: comma-separated token counts")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.case:
+        run_case(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
