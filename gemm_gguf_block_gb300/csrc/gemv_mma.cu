@@ -6,13 +6,16 @@
 // Decoding": weights decoded once, one accumulator set per position, and the
 // batched result equal to the single-position one.
 //
-// Per 32-element block the integer dot is an exact fp16 tensor-core product
-// (quants are small integers, exact in fp16; 32 products sum far below 2^24
-// in the fp32 accumulator), mma.sync m16n8k16 twice per block. The block's
-// scale terms are then applied on the CUDA cores in the library's fixed
-// order (include/cq.h): c = fma(d_w * d_x, isum, c) [+ fma(m_w, s_x, c) for
-// Q4_1] over four blocks, y = y + c per chunk. Every (row, token) chain lives
-// in one thread, so each row equals the single-token GEMV row bit for bit.
+// Per 32-element block the integer dot is an exact fp16 tensor-core product,
+// mma.sync m16n8k16 twice per block. The weight operand holds BIAS + v for a
+// quant of value v, built from the packed bytes by one lop3 per pair, and
+// the accumulator starts at -BIAS * sum(x): every operand and partial sum is
+// an integer below 2^23, so the result is the exact integer dot. The block's
+// scale terms are then applied on the CUDA cores, two tokens per f32x2
+// instruction, in the library's fixed order (include/cq.h):
+// c = fma(d_w * d_x, isum, c) [+ fma(m_w, s_x, c) for Q4_1] over four
+// blocks, y = y + c per chunk. Every (row, token) chain lives in one thread,
+// so each row equals the single-token GEMV row bit for bit.
 //
 // A persistent CTA (8 consumer warps of 16 rows each + 1 producer warp)
 // stages the tokens' activations once as fp16 in shared memory, then streams
@@ -29,16 +32,20 @@
 namespace cq {
 namespace {
 
-constexpr int ROWS = 128;           // rows per tile
 constexpr int SEG_BLOCKS = 8;       // 32-blocks per stage (256 elements)
-constexpr int NSTAGE = 4;
-constexpr int CONSUMERS = 8;        // warps, 16 rows each
-constexpr int THREADS = (CONSUMERS + 1) * 32;
+constexpr int MAX_STAGES = 4;
+// Consumer warps (16 rows each) per CTA.
+__host__ __device__ constexpr int consumers(int) { return 8; }
+__host__ __device__ constexpr int tile_rows(int NT) { return 16 * consumers(NT); }
 
+// BB / QO: weight block bytes and offset of its quants; ABB / AQO: the same
+// for the paired activation block; BIAS: the fp16 A operand holds BIAS + v
+// for a weight quant of value v (see a_frags), so the accumulator starts at
+// -BIAS * sum(x).
 template <int WF> struct MF;
-template <> struct MF<CQ_Q4_0> { static constexpr int BB = 18, QO = 2, ABB = 34, AQO = 2; };
-template <> struct MF<CQ_Q4_1> { static constexpr int BB = 20, QO = 4, ABB = 36, AQO = 4; };
-template <> struct MF<CQ_Q8_0> { static constexpr int BB = 34, QO = 2, ABB = 34, AQO = 2; };
+template <> struct MF<CQ_Q4_0> { static constexpr int BB = 18, QO = 2, ABB = 34, AQO = 2, BIAS = 1032; };
+template <> struct MF<CQ_Q4_1> { static constexpr int BB = 20, QO = 4, ABB = 36, AQO = 4, BIAS = 1024; };
+template <> struct MF<CQ_Q8_0> { static constexpr int BB = 34, QO = 2, ABB = 34, AQO = 2, BIAS = 1152; };
 
 struct MmaParams {
     const uint8_t* W;
@@ -50,86 +57,143 @@ struct MmaParams {
     int64_t wrow;       // bytes per weight row
     int act_pitch;      // bytes per staged token row (fp16, padded)
     int stage_bytes;
+    int stages;
     int smem_act;       // offset of the staged activations
-    int smem_scale;     // offset of the staged activation scales (float2 per token-block)
+    int smem_scale;     // offset of the per-(block, token pair) scale table
     int smem_stage;     // offset of the weight stages
 };
+
+// D = A * B + (c0, c1, c0, c1), and D += A * B.
+__device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
+                                          float c1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%10,%11};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mma16816acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f), "f"(0.0f),
-          "f"(0.0f));
+// (w & sel) with bits of `set` forced on: one lop3. With sel = 0x000F000F and
+// set = 0x64006400 the two 16-bit lanes become the binary16 values 1024 + n of
+// the nibbles in bits 0-3 and 16-19.
+__device__ __forceinline__ uint32_t and_or(uint32_t w, uint32_t sel, uint32_t set) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(sel), "r"(set));   // (a & b) | c
+    return r;
+}
+// The same for signed bytes in bits 0-7 and 16-23: 1024 + (b + 128) = 1152 + b.
+__device__ __forceinline__ uint32_t s8pair_1152(uint32_t w) {
+    return and_or(w ^ 0x00800080u, 0x00FF00FFu, 0x64006400u);
 }
 
-// Two bytes (quants of elements k, k+1) as a half2 of their integer values.
-// Q4: the low (hi=false) or high nibbles, minus `off` (8 for Q4_0, 0 for Q4_1);
-// Q8: the signed bytes.
+// The k order inside a 32-block. mma k-step 0 takes elements 0..15, k-step 1
+// elements 16..31; within a k-step, fragment column 2t holds element 4t,
+// 2t+1 -> 4t+2, 2t+8 -> 4t+1, 2t+9 -> 4t+3. Both operands use this order, so
+// the products are the same; what it buys is that lane t's weight quants are
+// the four consecutive bytes 4t..4t+3 of a 16-element run.
+//
+// A fragments of rows g (q0) and g+8 (q1) for one block: BIAS + value per element.
 template <int WF>
-__device__ __forceinline__ uint32_t pair_to_half2(uint32_t two_bytes, bool hi) {
-    const uint32_t p = __byte_perm(two_bytes, 0u, 0x4140);     // byte 0 -> half 0, byte 1 -> half 1
+__device__ __forceinline__ void a_frags(uint32_t q0a, uint32_t q1a, uint32_t q0b, uint32_t q1b, uint32_t (&a0)[4],
+                                        uint32_t (&a1)[4]) {
     if constexpr (WF == CQ_Q8_0) {
-        return h2u(__hsub2(u2h((p ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));   // - 1152
+        // q?a: quants 4t..4t+3, q?b: 16+4t..16+4t+3 (signed bytes)
+        a0[0] = s8pair_1152(q0a);        a0[1] = s8pair_1152(q1a);
+        a0[2] = s8pair_1152(q0a >> 8);   a0[3] = s8pair_1152(q1a >> 8);
+        a1[0] = s8pair_1152(q0b);        a1[1] = s8pair_1152(q1b);
+        a1[2] = s8pair_1152(q0b >> 8);   a1[3] = s8pair_1152(q1b >> 8);
     } else {
-        const uint32_t n = (hi ? (p >> 4) : p) & 0x000F000Fu;
-        const uint32_t bias = WF == CQ_Q4_0 ? 0x64086408u : 0x64006400u;                // 1032 or 1024
-        return h2u(__hsub2(u2h(n | 0x64006400u), u2h(bias)));
+        // q?a: bytes 4t..4t+3; low nibbles = elements 4t.., high = 16+4t..
+        constexpr uint32_t SEL = 0x000F000Fu, SET = 0x64006400u;
+        a0[0] = and_or(q0a, SEL, SET);         a0[1] = and_or(q1a, SEL, SET);
+        a0[2] = and_or(q0a >> 8, SEL, SET);    a0[3] = and_or(q1a >> 8, SEL, SET);
+        a1[0] = and_or(q0a >> 4, SEL, SET);    a1[1] = and_or(q1a >> 4, SEL, SET);
+        a1[2] = and_or(q0a >> 12, SEL, SET);   a1[3] = and_or(q1a >> 12, SEL, SET);
+        (void)q0b;
+        (void)q1b;
     }
 }
 
+// Four bytes at a 2-byte-aligned shared-memory address.
+__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
+    return __byte_perm(h[0], h[1], 0x5410);
+}
+
 template <int WF, int NT>
-__global__ void __launch_bounds__(THREADS, 1) gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                              const MmaParams p) {
+__global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const MmaParams p) {
     using F = MF<WF>;
+    constexpr int NPAIR = NT * 4;                  // token pairs
+    constexpr int CONSUMERS = consumers(NT);
+    constexpr int ROWS = tile_rows(NT);
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + NSTAGE;
+    uint64_t* empty = full + MAX_STAGES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.stages;
     const int tiles = (p.N + ROWS - 1) / ROWS;
     const int nseg = p.nb / SEG_BLOCKS;
     const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t steps = static_cast<int64_t>(my_tiles) * nseg;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NSTAGE; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], CONSUMERS);
         }
         fence_mbar_init();
     }
-    // Stage the activations once: fp16 quants [token][k] (padded pitch) and
-    // per-block scales (d, s) as floats; tokens >= M are zero.
+    // Stage the activations once. Per (token m, block b): the 32 quants as
+    // fp16 in four 16-byte chunks, chunk t = elements [4t, 4t+2, 4t+1, 4t+3,
+    // 16+4t, 18+4t, 17+4t, 19+4t] (lane t's B fragments of both k-steps);
+    // per (block b, token pair j): {d_x, d_x', -BIAS*sum(q), -BIAS*sum(q')}
+    // and, for Q8_1, {s_x, s_x'}. Tokens >= M are zero.
     {
-        __half* act = reinterpret_cast<__half*>(smem + p.smem_act);
-        float2* sc = reinterpret_cast<float2*>(smem + p.smem_scale);
-        const int tokens = NT * 8;
-        const int total = tokens * p.nb;
+        float* sc = reinterpret_cast<float*>(smem + p.smem_scale);
+        const int total = NT * 8 * p.nb;
         for (int i = threadIdx.x; i < total; i += blockDim.x) {
             const int m = i / p.nb, b = i - m * p.nb;
             uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            float2 ds = make_float2(0.0f, 0.0f);
+            float d = 0.0f, sx = 0.0f;
+            int sum = 0;
             if (m < p.M) {
-                const uint16_t* s = reinterpret_cast<const uint16_t*>(p.xq + (static_cast<int64_t>(m) * p.nb + b) * F::ABB);
+                const uint8_t* blk = p.xq + (static_cast<int64_t>(m) * p.nb + b) * F::ABB;
+                const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    w[j] = static_cast<uint32_t>(s[F::AQO / 2 + 2 * j]) | (static_cast<uint32_t>(s[F::AQO / 2 + 2 * j + 1]) << 16);
-                ds.x = h2f(s[0]);
-                ds.y = WF == CQ_Q4_1 ? h2f(s[1]) : 0.0f;
+                for (int j = 0; j < 8; ++j) {
+                    w[j] = __byte_perm(h[F::AQO / 2 + 2 * j], h[F::AQO / 2 + 2 * j + 1], 0x5410);
+                    sum = __dp4a(static_cast<int>(w[j]), 0x01010101, sum);
+                }
+                d = h2f(h[0]);
+                if constexpr (WF == CQ_Q4_1) sx = h2f(h[1]);
             }
-            uint32_t* dst = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(act) + m * p.act_pitch + 64 * b);
+            uint4* dst = reinterpret_cast<uint4*>(smem + p.smem_act + m * p.act_pitch + 64 * b);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t o0 = h2u(__hsub2(u2h((__byte_perm(w[j], 0u, 0x4140) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
-                uint32_t o1 = h2u(__hsub2(u2h((__byte_perm(w[j], 0u, 0x4342) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
-                dst[2 * j] = o0;
-                dst[2 * j + 1] = o1;
+            for (int t = 0; t < 4; ++t) {
+                // exact fp16 of the signed bytes: (1152 + b) - 1152
+                const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+                const uint32_t e02 = h2u(__hsub2(u2h(s8pair_1152(w[t])), k1152));
+                const uint32_t e13 = h2u(__hsub2(u2h(s8pair_1152(w[t] >> 8)), k1152));
+                const uint32_t f02 = h2u(__hsub2(u2h(s8pair_1152(w[t + 4])), k1152));
+                const uint32_t f13 = h2u(__hsub2(u2h(s8pair_1152(w[t + 4] >> 8)), k1152));
+                dst[t] = make_uint4(e02, e13, f02, f13);
             }
-            sc[m * p.nb + b] = ds;
+            const int j = m >> 1, hi = m & 1;
+            float* e = sc + (b * NPAIR + j) * 4;
+            e[hi] = d;
+            e[2 + hi] = static_cast<float>(-F::BIAS * sum);
+            if constexpr (WF == CQ_Q4_1) sc[p.nb * NPAIR * 4 + (b * NPAIR + j) * 2 + hi] = sx;
         }
     }
     __syncthreads();
@@ -138,8 +202,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_mma_kernel(const __grid_const
         // -------------------------------------------------------- producer
         if (lane == 0) {
             for (int64_t k = 0; k < steps; ++k) {
-                const int st = static_cast<int>(k % NSTAGE);
-                if (!mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((k / NSTAGE) & 1) ^ 1), WAIT_LIMIT_NS)) {
+                const int st = static_cast<int>(k % S);
+                if (!mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((k / S) & 1) ^ 1), WAIT_LIMIT_NS)) {
                     atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
                     break;
                 }
@@ -154,102 +218,88 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_mma_kernel(const __grid_const
     } else {
         // -------------------------------------------------------- consumers
         const int g = lane >> 2, t = lane & 3;
-        const uint8_t* act = smem + p.smem_act;
-        const float2* sc = reinterpret_cast<const float2*>(smem + p.smem_scale);
+        const uint8_t* act = smem + p.smem_act + g * p.act_pitch + 16 * t;
+        const float4* sc4 = reinterpret_cast<const float4*>(smem + p.smem_scale) + t;
+        const float2* sx2 = reinterpret_cast<const float2*>(smem + p.smem_scale + p.nb * NPAIR * 16) + t;
         const int seg_row_bytes = SEG_BLOCKS * F::BB;
-        float c[NT][4], y[NT][4];
+        uint64_t c[NT][2], y[NT][2];   // (row g | row g+8) x (token 8n+2t, 8n+2t+1)
         int64_t k = 0;
         bool ok = true;
         for (int ti = 0; ti < my_tiles && ok; ++ti) {
             const int tile = blockIdx.x + ti * gridDim.x;
 #pragma unroll
-            for (int n = 0; n < NT; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) y[n][e] = 0.0f;
+            for (int n = 0; n < NT; ++n) y[n][0] = y[n][1] = 0;
             for (int seg = 0; seg < nseg; ++seg, ++k) {
-                const int st = static_cast<int>(k % NSTAGE);
-                if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / NSTAGE) & 1), WAIT_LIMIT_NS)) {
+                const int st = static_cast<int>(k % S);
+                if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS)) {
                     if (lane == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
                     ok = false;
                     break;
                 }
                 const uint8_t* rg = smem + p.smem_stage + st * p.stage_bytes + (16 * warp + g) * seg_row_bytes;
                 const uint8_t* rg8 = rg + 8 * seg_row_bytes;
-#pragma unroll 2
+#pragma unroll 4
                 for (int bi = 0; bi < SEG_BLOCKS; ++bi) {
                     const int b = seg * SEG_BLOCKS + bi;          // block index along K
                     const uint8_t* w0 = rg + bi * F::BB;
                     const uint8_t* w1 = rg8 + bi * F::BB;
-                    // A fragments: k-step 0 = elements 0..15, k-step 1 = 16..31.
-                    uint32_t a0[4], a1[4];
-                    if constexpr (WF == CQ_Q8_0) {
-                        const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + F::QO);
-                        const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + F::QO);
-                        a0[0] = pair_to_half2<WF>(q0[t], false);
-                        a0[1] = pair_to_half2<WF>(q1[t], false);
-                        a0[2] = pair_to_half2<WF>(q0[t + 4], false);
-                        a0[3] = pair_to_half2<WF>(q1[t + 4], false);
-                        a1[0] = pair_to_half2<WF>(q0[t + 8], false);
-                        a1[1] = pair_to_half2<WF>(q1[t + 8], false);
-                        a1[2] = pair_to_half2<WF>(q0[t + 12], false);
-                        a1[3] = pair_to_half2<WF>(q1[t + 12], false);
-                    } else {
-                        const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + F::QO);
-                        const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + F::QO);
-                        const uint32_t r0a = q0[t], r0b = q0[t + 4], r1a = q1[t], r1b = q1[t + 4];
-                        a0[0] = pair_to_half2<WF>(r0a, false);
-                        a0[1] = pair_to_half2<WF>(r1a, false);
-                        a0[2] = pair_to_half2<WF>(r0b, false);
-                        a0[3] = pair_to_half2<WF>(r1b, false);
-                        a1[0] = pair_to_half2<WF>(r0a, true);
-                        a1[1] = pair_to_half2<WF>(r1a, true);
-                        a1[2] = pair_to_half2<WF>(r0b, true);
-                        a1[3] = pair_to_half2<WF>(r1b, true);
-                    }
-                    const float dw0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
-                    const float dw1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
-                    float mw0 = 0.0f, mw1 = 0.0f;
+                    uint32_t q0a, q1a, q0b = 0, q1b = 0;
                     if constexpr (WF == CQ_Q4_1) {
-                        mw0 = h2f(*reinterpret_cast<const uint16_t*>(w0 + 2));
-                        mw1 = h2f(*reinterpret_cast<const uint16_t*>(w1 + 2));
+                        q0a = *reinterpret_cast<const uint32_t*>(w0 + F::QO + 4 * t);
+                        q1a = *reinterpret_cast<const uint32_t*>(w1 + F::QO + 4 * t);
+                    } else {
+                        q0a = ld_u32_a2(w0 + F::QO + 4 * t);
+                        q1a = ld_u32_a2(w1 + F::QO + 4 * t);
+                        if constexpr (WF == CQ_Q8_0) {
+                            q0b = ld_u32_a2(w0 + F::QO + 16 + 4 * t);
+                            q1b = ld_u32_a2(w1 + F::QO + 16 + 4 * t);
+                        }
+                    }
+                    uint32_t a0[4], a1[4];
+                    a_frags<WF>(q0a, q1a, q0b, q1b, a0, a1);
+                    uint64_t dw0, dw1, mw0 = 0, mw1 = 0;
+                    if constexpr (WF == CQ_Q4_1) {
+                        const uint32_t dm0 = *reinterpret_cast<const uint32_t*>(w0);
+                        const uint32_t dm1 = *reinterpret_cast<const uint32_t*>(w1);
+                        const float d0 = h2f(dm0), d1 = h2f(dm1), m0 = h2f(dm0 >> 16), m1 = h2f(dm1 >> 16);
+                        dw0 = tc::pk(d0, d0);
+                        dw1 = tc::pk(d1, d1);
+                        mw0 = tc::pk(m0, m0);
+                        mw1 = tc::pk(m1, m1);
+                    } else {
+                        const float d0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
+                        const float d1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
+                        dw0 = tc::pk(d0, d0);
+                        dw1 = tc::pk(d1, d1);
                     }
                     if ((b & 3) == 0) {
 #pragma unroll
-                        for (int n = 0; n < NT; ++n)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) c[n][e] = 0.0f;
+                        for (int n = 0; n < NT; ++n) c[n][0] = c[n][1] = 0;
                     }
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
-                        const uint8_t* tok = act + (8 * n + g) * p.act_pitch + 64 * b + 4 * t;
-                        float acc0[4], acc1[4];
-                        mma16816(acc0, a0, *reinterpret_cast<const uint32_t*>(tok),
-                                 *reinterpret_cast<const uint32_t*>(tok + 16));
-                        mma16816(acc1, a1, *reinterpret_cast<const uint32_t*>(tok + 32),
-                                 *reinterpret_cast<const uint32_t*>(tok + 48));
-                        // C fragment: e=0 (row g, token 2t), e=1 (row g, 2t+1),
-                        // e=2 (row g+8, 2t), e=3 (row g+8, 2t+1). The two k-steps'
-                        // exact integer partials add exactly.
-                        const float2 s0 = sc[(8 * n + 2 * t) * p.nb + b];
-                        const float2 s1 = sc[(8 * n + 2 * t + 1) * p.nb + b];
-                        const float is0 = acc0[0] + acc1[0], is1 = acc0[1] + acc1[1];
-                        const float is2 = acc0[2] + acc1[2], is3 = acc0[3] + acc1[3];
-                        c[n][0] = __fmaf_rn(__fmul_rn(dw0, s0.x), is0, c[n][0]);
-                        c[n][1] = __fmaf_rn(__fmul_rn(dw0, s1.x), is1, c[n][1]);
-                        c[n][2] = __fmaf_rn(__fmul_rn(dw1, s0.x), is2, c[n][2]);
-                        c[n][3] = __fmaf_rn(__fmul_rn(dw1, s1.x), is3, c[n][3]);
+                        const uint4 bv = *reinterpret_cast<const uint4*>(act + 8 * n * p.act_pitch + 64 * b);
+                        const float4 s4 = sc4[b * NPAIR + 4 * n];
+                        float acc[4];
+                        mma16816c(acc, a0, bv.x, bv.y, s4.z, s4.w);
+                        mma16816acc(acc, a1, bv.z, bv.w);
+                        const uint64_t dx = tc::pk(s4.x, s4.y);
+                        // c = fma(d_w * d_x, isum, c) per element, two tokens per instruction
+                        c[n][0] = tc::fma2(tc::mul2(dw0, dx), tc::pk(acc[0], acc[1]), c[n][0]);
+                        c[n][1] = tc::fma2(tc::mul2(dw1, dx), tc::pk(acc[2], acc[3]), c[n][1]);
                         if constexpr (WF == CQ_Q4_1) {
-                            c[n][0] = __fmaf_rn(mw0, s0.y, c[n][0]);
-                            c[n][1] = __fmaf_rn(mw0, s1.y, c[n][1]);
-                            c[n][2] = __fmaf_rn(mw1, s0.y, c[n][2]);
-                            c[n][3] = __fmaf_rn(mw1, s1.y, c[n][3]);
+                            const float2 s2 = sx2[b * NPAIR + 4 * n];
+                            const uint64_t sx = tc::pk(s2.x, s2.y);
+                            c[n][0] = tc::fma2(mw0, sx, c[n][0]);
+                            c[n][1] = tc::fma2(mw1, sx, c[n][1]);
                         }
                     }
                     if ((b & 3) == 3) {
 #pragma unroll
-                        for (int n = 0; n < NT; ++n)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) y[n][e] = __fadd_rn(y[n][e], c[n][e]);
+                        for (int n = 0; n < NT; ++n) {
+                            y[n][0] = tc::add2(y[n][0], c[n][0]);
+                            y[n][1] = tc::add2(y[n][1], c[n][1]);
+                        }
                     }
                 }
                 __syncwarp();
@@ -262,9 +312,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_mma_kernel(const __grid_const
             for (int n = 0; n < NT; ++n) {
                 const int m0 = 8 * n + 2 * t;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = r0 + (e >= 2 ? 8 : 0), m = m0 + (e & 1);
-                    if (row < p.N && m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = y[n][e];
+                for (int h = 0; h < 2; ++h) {
+                    float v[2];
+                    tc::upk(y[n][h], v[0], v[1]);
+                    const int row = r0 + 8 * h;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        if (row < p.N && m0 + i < p.M) p.y[static_cast<int64_t>(m0 + i) * p.N + row] = v[i];
                 }
             }
         }
@@ -272,8 +326,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_mma_kernel(const __grid_const
     // Let the producer's last copies land before the CTA's shared memory goes.
     __syncthreads();
     if (threadIdx.x == 0) {
-        for (int64_t k = steps > NSTAGE ? steps - NSTAGE : 0; k < steps; ++k)
-            (void)mbar_wait_bounded(&full[k % NSTAGE], static_cast<uint32_t>((k / NSTAGE) & 1), WAIT_LIMIT_NS / 8);
+        for (int64_t k = steps > S ? steps - S : 0; k < steps; ++k)
+            (void)mbar_wait_bounded(&full[k % S], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS / 8);
     }
 }
 
@@ -295,9 +349,29 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// Shared-memory layout for M tokens, K columns: barriers, the fp16
+// activation tile, the scale table, then `stages` weight stages.
+struct MmaSmem {
+    int act_pitch, act, scale, stage, stage_bytes, fixed;
+};
+MmaSmem mma_smem(int bb, int M, int64_t K) {
+    MmaSmem m{};
+    const int NT = M <= 8 ? 1 : 2;
+    const int ROWS = tile_rows(NT);
+    const int nb = static_cast<int>(K / 32);
+    m.act_pitch = static_cast<int>(K) * 2 + 64;      // 64 mod 128: token rows g, g+1 on different bank halves
+    m.act = 1024;
+    m.scale = m.act + (NT * 8 * m.act_pitch + 127) / 128 * 128;
+    const int scale_bytes = nb * NT * 4 * (bb == 20 ? 24 : 16);
+    m.stage = m.scale + (scale_bytes + 1023) / 1024 * 1024;
+    m.stage_bytes = ROWS * SEG_BLOCKS * bb;
+    m.fixed = m.stage;
+    return m;
+}
+
 template <int WF, int NT>
 cudaError_t launch_mma_typed(const DeviceInfo& dev, MmaParams p, const CUtensorMap& map, cudaStream_t s) {
-    const int smem = p.smem_stage + NSTAGE * p.stage_bytes;
+    const int smem = p.smem_stage + p.stages * p.stage_bytes;
     static int raised[64] = {};
     int devid = 0;
     cudaError_t e = cudaGetDevice(&devid);
@@ -308,9 +382,9 @@ cudaError_t launch_mma_typed(const DeviceInfo& dev, MmaParams p, const CUtensorM
         if (e != cudaSuccess) return e;
         if (devid < 64) raised[devid] = std::min(dev.smem_optin, 227 * 1024);
     }
-    const int tiles = (p.N + ROWS - 1) / ROWS;
+    const int tiles = (p.N + tile_rows(NT) - 1) / tile_rows(NT);
     const int grid = std::min(tiles, dev.sm_count);
-    gemv_mma_kernel<WF, NT><<<grid, THREADS, smem, s>>>(map, p);
+    gemv_mma_kernel<WF, NT><<<grid, (consumers(NT) + 1) * 32, smem, s>>>(map, p);
     return cudaGetLastError();
 }
 
@@ -331,17 +405,22 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
     p.nb = static_cast<int>(K / 32);
     p.wrow = static_cast<int64_t>(p.nb) * F::BB;
     const int NT = M <= 8 ? 1 : 2;
-    p.act_pitch = static_cast<int>(K) * 2 + 16;       // +16 bytes: tokens land on different banks
-    p.stage_bytes = ROWS * SEG_BLOCKS * F::BB;
-    p.smem_act = 1024;
-    p.smem_scale = p.smem_act + (NT * 8 * p.act_pitch + 127) / 128 * 128;
-    p.smem_stage = p.smem_scale + (NT * 8 * p.nb * 8 + 1023) / 1024 * 1024;
+    const MmaSmem L = mma_smem(F::BB, M, K);
+    const int lim = std::min(dev.smem_optin, 227 * 1024);
+    p.act_pitch = L.act_pitch;
+    p.stage_bytes = L.stage_bytes;
+    p.smem_act = L.act;
+    p.smem_scale = L.scale;
+    p.smem_stage = L.stage;
+    p.stages = std::min(MAX_STAGES, (lim - L.fixed) / L.stage_bytes);
+    if (p.stages < 2) return cudaErrorInvalidConfiguration;
     // Raw weights as a 2-D tensor of 2-byte elements [N rows][wrow/2]; a box is
-    // 8 blocks of 128 rows.
+    // 8 blocks of one tile's rows.
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.wrow / 2), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.wrow)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(SEG_BLOCKS * F::BB / 2), ROWS};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(SEG_BLOCKS * F::BB / 2),
+                               static_cast<cuuint32_t>(tile_rows(NT))};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -352,16 +431,13 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
 
 }  // namespace
 
-// Shared memory the tensor-core GEMV needs for M tokens and K columns (0 when
-// the format has no tensor-core path).
+// Shared memory the tensor-core GEMV needs for M tokens and K columns with
+// the minimum of two weight stages (0 when the format has no tensor-core path).
 int gemv_mma_smem(int w_fmt, int M, int64_t K) {
     if (w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) return 0;
     const int bb = w_fmt == CQ_Q4_0 ? 18 : w_fmt == CQ_Q4_1 ? 20 : 34;
-    const int NT = M <= 8 ? 1 : 2;
-    const int nb = static_cast<int>(K / 32);
-    const int act = (NT * 8 * (static_cast<int>(K) * 2 + 16) + 127) / 128 * 128;
-    const int scale = (NT * 8 * nb * 8 + 1023) / 1024 * 1024;
-    return 1024 + act + scale + NSTAGE * ROWS * SEG_BLOCKS * bb;
+    const MmaSmem L = mma_smem(bb, M, K);
+    return L.fixed + 2 * L.stage_bytes;
 }
 
 cudaError_t launch_gemv_mma(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
