@@ -32,6 +32,8 @@ SIGNATURES = {
     "cq_quantize_act": (_I, [_I, _I64, _I64, _P, _P, _P]),
     "cq_gemv": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "cq_gemm": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "cq_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
+    "cq_gemm_ws": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "cq_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
     "cq_moe_gemv": (_I, [_I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "cq_moe_gemv_noalloc": (_I, [_I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -84,6 +86,14 @@ def cq_gemv(w_fmt, M, N, K, W, xq, y, stream=0):
 
 def cq_gemm(w_fmt, M, N, K, W, xq, y, stream=0):
     return lib().cq_gemm(w_fmt, M, N, K, W, xq, y, stream)
+
+
+def cq_gemm_workspace_size(w_fmt, M, N, K):
+    return lib().cq_gemm_workspace_size(w_fmt, M, N, K)
+
+
+def cq_gemm_ws(w_fmt, M, N, K, W, xq, y, ws, ws_bytes, stream=0):
+    return lib().cq_gemm_ws(w_fmt, M, N, K, W, xq, y, ws, ws_bytes, stream)
 
 
 def cq_moe_workspace_size(T, K, F, E, topk):
@@ -161,6 +171,19 @@ def gemm_t(W, xq, w_fmt: int, K: int, out=None):
     N, M = W.shape[0], xq.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=W.device)
     _check("cq_gemm", cq_gemm(w_fmt, M, N, K, W.data_ptr(), xq.data_ptr(), y.data_ptr(), _stream_handle()))
+    return y
+
+
+def gemm_ws_t(W, xq, w_fmt: int, K: int, ws=None, out=None):
+    """cq_gemm_ws with a workspace tensor (allocated here when not given)."""
+    torch = _torch()
+    N, M = W.shape[0], xq.shape[0]
+    need = cq_gemm_workspace_size(w_fmt, M, N, K)
+    if ws is None:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=W.device)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=W.device)
+    _check("cq_gemm_ws", cq_gemm_ws(w_fmt, M, N, K, W.data_ptr(), xq.data_ptr(), y.data_ptr(), ws.data_ptr(),
+                                    ws.numel(), _stream_handle()))
     return y
 
 

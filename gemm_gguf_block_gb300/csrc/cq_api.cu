@@ -134,7 +134,28 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     if (!aligned16(W) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
     cq::DeviceInfo dev;
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
-    cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, static_cast<cudaStream_t>(stream));
+    cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, nullptr, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+size_t cq_gemm_workspace_size(cq_format w_fmt, int64_t M, int64_t N, int64_t K) {
+    if (w_fmt != CQ_Q4_K || check_shape(M, N, K) != CQ_OK) return 0;
+    return cq::gemm_workspace_size(w_fmt, M, K);
+}
+
+cq_status cq_gemm_ws(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (w_fmt != CQ_Q4_K) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, N, K);
+    if (st != CQ_OK) return st;
+    if (M == 0 || N == 0) return CQ_OK;
+    if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
+    if (workspace == nullptr || workspace_bytes < cq::gemm_workspace_size(w_fmt, M, K)) return CQ_ERR_WORKSPACE;
+    if (!aligned16(W) || !aligned4(xq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, workspace, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 

@@ -26,9 +26,12 @@ int gemv_mma_smem(int w_fmt, int M, int64_t K);
 cudaError_t launch_gemv_mma(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                             const void* xq, float* y, cudaStream_t s);
 
-// Prefill GEMM (any M): y rows equal the cq_gemv rows bit for bit.
+// Prefill GEMM (any M): y rows equal the cq_gemv rows bit for bit. With a
+// workspace (gemm_workspace_size bytes, 256-byte aligned) the activations are
+// converted once up front instead of in every CTA.
+size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K);
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
-                        const void* xq, float* y, cudaStream_t s);
+                        const void* xq, float* y, void* workspace, cudaStream_t s);
 
 // Byte offsets of the routed-FFN workspace sections (each 256-byte aligned).
 struct MoeLayout {

@@ -74,7 +74,14 @@ struct GemmParams {
     int M, N, ns;        // tokens, rows, superblocks per row
     int64_t wrow;        // bytes per weight row
     int64_t xrow;        // bytes per activation row
+    const uint8_t* bimg; // pre-converted B operands: [token tile][superblock] images of IMG_BYTES
+    const float* dxs;    // pre-gathered activation scales: [token tile][superblock][BN]
 };
+
+// One (token tile, superblock) image of the pre-converted activations, laid
+// out exactly as the B part of two operand stages: the K-half 0 and K-half 1
+// fp16 tiles, then the mins operand.
+constexpr int IMG_BYTES = 2 * (BN * KH * 2) + BN * 16 * 2;     // 69632
 
 // Offset of element (r, k) in a K-major no-swizzle tile whose rows hold kt elements.
 __device__ __forceinline__ int tile_off(int r, int k, int kt) {
@@ -123,6 +130,9 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
     }
 }
 
+// PRE: the activations come pre-converted (cq_gemm_ws): the producer
+// bulk-copies each stage's B operand and the converters handle only weights.
+template <bool PRE>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -141,7 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             mbar_init(&bars[B_RAW_EMPTY + i], NCONV);
         }
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], NCONV);
+            mbar_init(&bars[B_OP_FULL + i], PRE ? NCONV + 1 : NCONV);   // + the producer's copy
             mbar_init(&bars[B_OP_EMPTY + i], 1);
         }
         mbar_init(&bars[B_ACC_FULL], 1);
@@ -161,11 +171,30 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
             for (int s = 0; s < ns && !*abort_flag; ++s) {
                 const int r = s % NRAW;
                 if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAW_BYTES);
                 tc::tma_load_2d(smem + OFF_RAW + r * RAW_BYTES, &wmap, 144 * s, n0, &bars[B_RAW_FULL + r]);
+                if constexpr (PRE) {
+                    const uint8_t* img = p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES;
+                    bool ok = true;
+                    for (int h = 0; h < 2; ++h) {
+                        const int q = 2 * s + h, st = q % NSTAGE;
+                        if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
+                        mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES + (h ? BMIN_BYTES : 0));
+                        bulk_g2s(stg + A_BYTES, img + h * B_BYTES, B_BYTES, &bars[B_OP_FULL + st], pol);
+                        if (h)
+                            bulk_g2s(stg + A_BYTES + B_BYTES + AMIN_BYTES, img + 2 * B_BYTES, BMIN_BYTES,
+                                     &bars[B_OP_FULL + st], pol);
+                    }
+                    if (!ok) break;
+                }
             }
         }
     } else if (warp == 1) {
@@ -230,11 +259,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 }
             }
         };
-        fetch(0, cur, bcur);
+        if constexpr (!PRE) fetch(0, cur, bcur);
         for (int q = 0; q < 2 * ns; ++q) {
             const int s = q >> 1, h = q & 1, st = q % NSTAGE, rs = s % NRAW;
             if (*abort_flag) break;
-            if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt);
+            if constexpr (!PRE)
+                if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt);
             if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
             if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
@@ -269,7 +299,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             // half-warp's 8-byte stores fill one 128-byte core matrix.
             uint8_t* bt = stg + A_BYTES;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 16 && !PRE; ++i) {
                 const int t = 16 * cw + 8 * (i & 1) + (lane & 7);
                 const int word = 4 * (i >> 1) + (lane >> 3);
                 uint32_t o[2];
@@ -296,7 +326,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     *reinterpret_cast<uint4*>(am + tile_off(r, 8, 16)) = mv;
                 }
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 4 && !PRE; ++i) {
                     const int t = 16 * cw + 4 * i + (lane >> 3), j = lane & 7;
                     const uint32_t v = bcur[i];
                     const int pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
@@ -327,9 +357,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const int token = m0 + et;                      // et < 128: loads one token's scale
         auto fetch_scales = [&](int s, float& dxv, uint32_t& ddv) {
-            dxv = (et < BN && token < p.M)
-                      ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s))
-                      : 0.0f;
+            if constexpr (PRE)
+                dxv = et < BN ? __ldg(p.dxs + (static_cast<int64_t>(blockIdx.y) * ns + s) * BN + et) : 0.0f;
+            else
+                dxv = (et < BN && token < p.M)
+                          ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(token) * p.xrow +
+                                                                 292 * s))
+                          : 0.0f;
             ddv = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(p.W + row * p.wrow + 144 * s)) : 0u;
         };
         float dx_next;
@@ -409,6 +443,47 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// Pre-conversion of Q8_K activations for cq_gemm_ws: one CTA per (superblock
+// s, token tile), thread (token t, K-half h). Writes the tile's B operand
+// images -- the same values and layout the in-kernel converters produce --
+// and the activation scales.
+__global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint8_t* bimg, float* dxs) {
+    const int s = blockIdx.x, tile = blockIdx.y, ns = p.ns;
+    const int t = threadIdx.x >> 1, h = threadIdx.x & 1;
+    const int m = tile * BN + t;
+    const bool on = m < p.M;
+    const uint8_t* blk = p.xq + static_cast<int64_t>(m) * p.xrow + 292 * s;
+    uint8_t* img = bimg + (static_cast<int64_t>(tile) * ns + s) * IMG_BYTES;
+    const uint32_t* qw = reinterpret_cast<const uint32_t*>(blk + 4 + 128 * h);
+    uint8_t* bt = img + h * (BN * KH * 2);
+#pragma unroll 4
+    for (int g = 0; g < KH / 8; ++g) {       // 8 elements (one core-matrix row) per store
+        uint32_t o0[2] = {0u, 0u}, o1[2] = {0u, 0u};
+        if (on) {
+            int8_to_half(__ldg(qw + 2 * g), o0);
+            int8_to_half(__ldg(qw + 2 * g + 1), o1);
+        }
+        *reinterpret_cast<uint4*>(bt + tile_off(t, 8 * g, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+    }
+    if (h == 0) {
+        dxs[(static_cast<int64_t>(tile) * ns + s) * BN + t] = on ? __ldg(reinterpret_cast<const float*>(blk)) : 0.0f;
+    } else {
+        // mins operand: token t = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
+        __half* bh = reinterpret_cast<__half*>(img + 2 * (BN * KH * 2) + tile_off(t, 0, 16));
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int pr = 0;
+            if (on) {
+                const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(blk + 260) + j);
+                pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) + static_cast<int>(static_cast<int16_t>(v >> 16));
+            }
+            const int hq = pr >> 6;                                  // floor division by 64
+            bh[j] = __int2half_rn(64 * hq);
+            bh[64 + j] = __int2half_rn(pr - 64 * hq);                // k = 8 + j: next core matrix (+128 B)
+        }
+    }
+}
+
 // ------------------------------------------------------------ host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -430,8 +505,14 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K) {
+    if (w_fmt != CQ_Q4_K || M <= 0) return 0;
+    const int64_t cells = (M + BN - 1) / BN * (K / 256);
+    return static_cast<size_t>(cells) * (IMG_BYTES + BN * 4);
+}
+
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
-                        const void* xq, float* y, cudaStream_t s) {
+                        const void* xq, float* y, void* workspace, cudaStream_t s) {
     if (w_fmt != CQ_Q4_K) return cudaErrorInvalidValue;
     if (M <= 0 || N <= 0) return cudaSuccess;
     EncodeTiledFn enc = encode_fn();
@@ -446,6 +527,12 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
     p.ns = static_cast<int>(K / 256);
     p.wrow = static_cast<int64_t>(p.ns) * 144;
     p.xrow = static_cast<int64_t>(p.ns) * 292;
+    const int tiles_m = static_cast<int>((M + BN - 1) / BN);
+    if (workspace != nullptr) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        p.bimg = ws;
+        p.dxs = reinterpret_cast<const float*>(ws + static_cast<int64_t>(tiles_m) * p.ns * IMG_BYTES);
+    }
     // Raw weights as a 2-D byte tensor [N rows][wrow bytes]; a box is one
     // superblock (144 bytes) of 128 rows; rows past N read as zero.
     CUtensorMap map;
@@ -457,18 +544,27 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    static int raised[64] = {};
+    if (SMEM_BYTES > dev.smem_optin) return cudaErrorInvalidConfiguration;
+    static int raised[64][2] = {};
     int devid = 0;
     cudaError_t e = cudaGetDevice(&devid);
     if (e != cudaSuccess) return e;
-    if (devid >= 64 || !raised[devid]) {
-        e = cudaFuncSetAttribute(gemm_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    const int pre = workspace != nullptr;
+    if (devid >= 64 || !raised[devid][pre]) {
+        e = cudaFuncSetAttribute(pre ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = 1;
+        if (devid < 64) raised[devid][pre] = 1;
     }
-    if (SMEM_BYTES > dev.smem_optin) return cudaErrorInvalidConfiguration;
-    const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>((M + BN - 1) / BN));
-    gemm_q4k_kernel<<<grid, THREADS, SMEM_BYTES, s>>>(map, p);
+    const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
+    if (pre) {
+        gemm_prep_kernel<<<dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)), 256, 0, s>>>(
+            p, p.bimg == nullptr ? nullptr : const_cast<uint8_t*>(p.bimg), const_cast<float*>(p.dxs));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        gemm_q4k_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(map, p);
+    } else {
+        gemm_q4k_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(map, p);
+    }
     return cudaGetLastError();
 }
 

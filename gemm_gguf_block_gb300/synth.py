@@ -175,14 +175,16 @@ def decode_q4_0_small(seed: int = 0):
     return W, x
 
 
+def decode_q8_0_layer(seed: int, i: int, N: int, K: int):
+    """Layer i of the Q8_0 decode suite: W [N, K] and x [1, K]."""
+    W = gen_q8_0(stream(seed, 2, 2 * i), N, K)
+    x = gen_x(stream(seed, 2, 2 * i + 1), 1, K)
+    return W, x
+
+
 def decode_q8_0_suite(seed: int = 0, shapes=None):
     """Q8_0 decode GEMVs at Llama-3-8B shapes (N, K), M=1: list of (W, x)."""
-    out = []
-    for i, (N, K) in enumerate(shapes or DECODE_SUITE_Q8_0):
-        W = gen_q8_0(stream(seed, 2, 2 * i), N, K)
-        x = gen_x(stream(seed, 2, 2 * i + 1), 1, K)
-        out.append((W, x))
-    return out
+    return [decode_q8_0_layer(seed, i, N, K) for i, (N, K) in enumerate(shapes or DECODE_SUITE_Q8_0)]
 
 
 def prefill_q4_k(seed: int = 0, M: int = 512, N: int = 14336, K: int = 4096):

@@ -128,6 +128,21 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
                   float* y, void* stream);
 
 /*
+ * cq_gemm with a caller-owned device workspace: the quantized activations are
+ * converted once, into the workspace, to the tensor-core operand layout,
+ * instead of in every weight tile. Same result, bit for bit, as cq_gemm.
+ * cq_gemm_workspace_size returns the bytes needed (0 for an unsupported
+ * format or shape): ceil(M/128) * (K/256) * 70144 for Q4_K. The workspace
+ * must be 256-byte aligned; it is scratch (no state is kept between calls),
+ * and two calls that may overlap on the GPU need separate workspaces.
+ * Errors as cq_gemm, plus CQ_ERR_WORKSPACE (NULL or too small) and
+ * CQ_ERR_ALIGNMENT for a misaligned workspace.
+ */
+size_t cq_gemm_workspace_size(cq_format w_fmt, int64_t M, int64_t N, int64_t K);
+cq_status cq_gemm_ws(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
+                     float* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Routed-expert FFN (cera README "Supported models", lfm2moe; grouping tokens
  * by expert so each expert's weights are read once per call).
  * For token t and slot s: e = expert_ids[t][s] (distinct within a token),

@@ -62,6 +62,23 @@ def test_gemv_token_limit(L):
         assert cq.cq_gemm(fmt, 4, 8, 256, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
 
 
+def test_gemm_ws_validation(L):
+    need = cq.cq_gemm_workspace_size(cq.Q4_K, 512, 14336, 4096)
+    assert need == 4 * 16 * (69632 + 512)
+    assert cq.cq_gemm_workspace_size(cq.Q4_0, 512, 14336, 4096) == 0
+    assert cq.cq_gemm_workspace_size(cq.Q4_K, 512, 14336, 100) == 0
+    f = cq.cq_gemm_ws
+    assert f(cq.Q4_0, 4, 8, 256, A, A, A, A, need) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q4_K, 4, 8, 100, A, A, A, A, need) == cq.ERR_SHAPE
+    small = cq.cq_gemm_workspace_size(cq.Q4_K, 4, 8, 256)
+    assert small > 0
+    assert f(cq.Q4_K, 4, 8, 256, A, A, A, None, small) == cq.ERR_WORKSPACE
+    assert f(cq.Q4_K, 4, 8, 256, A, A, A, A, small - 1) == cq.ERR_WORKSPACE
+    assert f(cq.Q4_K, 4, 8, 256, A, A, A, A + 16, small) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_K, 4, 8, 256, A, A + 2, A, A, small) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_K, 0, 8, 256, None, None, None, None, 0) == cq.OK
+
+
 def test_quantize_validation(L):
     assert cq.cq_quantize_act(cq.Q4_0, 1, 256, A, A) == cq.ERR_UNSUPPORTED_FORMAT
     assert cq.cq_quantize_act(cq.Q8_0, 1, 96, A, A) == cq.ERR_SHAPE

@@ -86,6 +86,8 @@ def test_gemv_exact_arithmetic(orc, wfmt, N, K, M):
     if wfmt == 12:
         y2 = cq.gemm_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
         assert np.array_equal(y2.astype(np.float64), y_ref)
+        y3 = cq.gemm_ws_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
+        assert np.array_equal(y3.astype(np.float64), y_ref)
 
 
 @pytest.mark.parametrize("M,N,K", [(17, 100, 512), (64, 257, 2048), (130, 96, 4096)])
@@ -97,6 +99,8 @@ def test_gemm_rows_equal_gemv(orc, M, N, K):
     y = cq.gemm_t(Wd, xd, 12, K).cpu().numpy()
     y_ref, at = orc.matmul(12, W, xq, K)
     assert_within(y, y_ref, at, what="gemm")
+    y_ws = cq.gemm_ws_t(Wd, xd, 12, K).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y_ws.view(np.uint32)), "cq_gemm_ws differs from cq_gemm"
     for m in sorted({0, 1, M // 2, M - 1}):
         y1 = cq.gemv_t(Wd, xd[m:m + 1], 12, K).cpu().numpy()[0]
         assert np.array_equal(y[m].view(np.uint32), y1.view(np.uint32)), f"row {m}"
