@@ -41,7 +41,10 @@ SIGNATURES = {
     "cq_moe_read_status": (_I, [_P, _P, _P]),
     "cq_read_global_status": (_I, [_P, _I]),
     "cq_status_string": (C.c_char_p, [_I]),
+    "cq_set_option": (_I, [_I, _I64]),
 }
+
+OPT_WEIGHTS_CONST = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -86,6 +89,10 @@ def cq_gemv(w_fmt, M, N, K, W, xq, y, stream=0):
 
 def cq_gemm(w_fmt, M, N, K, W, xq, y, stream=0):
     return lib().cq_gemm(w_fmt, M, N, K, W, xq, y, stream)
+
+
+def cq_set_option(opt, value):
+    return lib().cq_set_option(opt, value)
 
 
 def cq_gemm_workspace_size(w_fmt, M, N, K):

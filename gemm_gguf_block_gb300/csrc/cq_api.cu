@@ -2,6 +2,8 @@
 // Every check runs before any launch, so an error return means that nothing
 // was launched and nothing was written. See include/cq.h for the contract.
 #include <cstdint>
+#include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -41,6 +43,17 @@ cq_status check_shape(int64_t M, int64_t N, int64_t K) {
 }  // namespace
 
 namespace cq {
+std::atomic<int> g_weights_const{0};
+bool weights_const() { return g_weights_const.load(std::memory_order_relaxed) != 0; }
+
+bool pdl_enabled() {
+    static const bool v = [] {
+        const char* e = std::getenv("CQ_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return v;
+}
+
 cudaError_t device_info(DeviceInfo* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -105,6 +118,12 @@ cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     cudaError_t e = cq::launch_gemv(dev, w_fmt, static_cast<int>(M), N, K, W, xq, y,
                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+cq_status cq_set_option(cq_option opt, int64_t value) {
+    if (opt != CQ_OPT_WEIGHTS_CONST || (value != 0 && value != 1)) return CQ_ERR_INVALID_ARG;
+    cq::g_weights_const.store(static_cast<int>(value), std::memory_order_relaxed);
+    return CQ_OK;
 }
 
 cq_status cq_read_global_status(int32_t* out_code, int clear) {

@@ -61,6 +61,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// Programmatic dependent launch. pdl_trigger lets the next grid in the stream
+// begin launching (its CTAs take SM resources as this grid's CTAs leave; its
+// own griddepcontrol.wait still waits for this grid to complete). pdl_wait
+// returns once the grids this one depends on have completed and their writes
+// are visible (at once for a grid launched without such a dependency): no
+// kernel reads or writes global memory before it, except the GEMV's weight
+// prefetch under the weights-constant option.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -2,9 +2,38 @@
 // kernel translation units. Arguments are validated by the caller (cq_api.cu).
 #pragma once
 #include <cstdint>
+#include <utility>
+
 #include <cuda_runtime.h>
 
 namespace cq {
+
+// Programmatic dependent launch (on unless CQ_PDL=0): every kernel of the
+// library is launched so that it may start while the previous grid in the
+// stream is still running; each kernel's first act is griddepcontrol.wait
+// (pdl_wait), which returns once the grids it depends on have completed and
+// their memory is visible, before any global memory is read or written. The
+// launch latency and the kernel's setup thus overlap the previous kernel's
+// tail, with the same ordering guarantees as a plain launch.
+bool pdl_enabled();
+// CQ_OPT_WEIGHTS_CONST (see include/cq.h).
+bool weights_const();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct DeviceInfo {
     int sm_count;

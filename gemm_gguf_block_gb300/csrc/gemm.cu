@@ -135,6 +135,8 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
 template <bool PRE>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -448,6 +450,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
 // images -- the same values and layout the in-kernel converters produce --
 // and the activation scales.
 __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint8_t* bimg, float* dxs) {
+    pdl_trigger();
+    pdl_wait();
     const int s = blockIdx.x, tile = blockIdx.y, ns = p.ns;
     const int t = threadIdx.x >> 1, h = threadIdx.x & 1;
     const int m = tile * BN + t;
@@ -558,14 +562,12 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
     }
     const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
     if (pre) {
-        gemm_prep_kernel<<<dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)), 256, 0, s>>>(
-            p, p.bimg == nullptr ? nullptr : const_cast<uint8_t*>(p.bimg), const_cast<float*>(p.dxs));
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        gemm_q4k_kernel<true><<<grid, THREADS, SMEM_BYTES, s>>>(map, p);
-    } else {
-        gemm_q4k_kernel<false><<<grid, THREADS, SMEM_BYTES, s>>>(map, p);
+        e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
+                          dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg), const_cast<float*>(p.dxs));
+        if (e != cudaSuccess) return e;
+        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
     }
-    return cudaGetLastError();
+    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
 }
 
 }  // namespace cq

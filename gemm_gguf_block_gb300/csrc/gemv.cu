@@ -59,6 +59,7 @@ struct GemvParams {
     int warp_bytes;
     int act_bytes;
     int tok_pitch;    // bytes per token of staged activations
+    int wconst;       // weights constant in flight: prefetch them before the dependency wait
 };
 
 // Exact float of an int with |i| < 2^22: the bits of 1.5 * 2^23 + i, minus 1.5 * 2^23.
@@ -333,6 +334,7 @@ template <int MT> constexpr int wpc_limit() { return MT <= 4 ? WPC_MAX : WPC_MAX
 
 template <int WF, int MT>
 __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvParams p) {
+    pdl_trigger();
     using F = G<WF>;
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -383,6 +385,9 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
     };
 
     // Start the weight stream first; stage the activations while it flies.
+    // The weights may be requested before the preceding grid has completed
+    // only when the caller has declared them constant.
+    if (!p.wconst) pdl_wait();
     Cursor ic{wid, 0, 0, 0u};
     int64_t issued = 0;
     if (active && lane == 0) {
@@ -393,6 +398,7 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
             advance(ic);
         }
     }
+    if (p.wconst) pdl_wait();
     stage_activations<WF>(p, act);
     __syncthreads();
     if (!active) return;
@@ -524,7 +530,8 @@ cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cu
         if (e != cudaSuccess) return e;
         if (devid < 64) raised[devid] = lim;
     }
-    gemv_kernel<WF, MT><<<grid, wpc * 32, smem, s>>>(p);
+    cudaError_t le = launch_kernel(gemv_kernel<WF, MT>, dim3(grid), dim3(wpc * 32), smem, s, p);
+    if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
@@ -574,6 +581,7 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         p.B = std::max(p.R, std::min(32, rows_fit) / p.R * p.R);
         if (p.B * p.M * nc > CBUF_FLOATS) return cudaErrorInvalidValue;
         p.tok_pitch = tok_pitch;
+        p.wconst = weights_const() ? 1 : 0;
         p.act_bytes = (p.M * tok_pitch + 127) / 128 * 128;
         const int64_t groups = (N + p.R - 1) / p.R;
         cudaError_t e = launch_fmt<WF>(dev, p, groups, s);

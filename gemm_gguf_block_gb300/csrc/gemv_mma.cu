@@ -133,6 +133,8 @@ __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
 template <int WF, int NT>
 __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const MmaParams p) {
+    pdl_trigger();
+    pdl_wait();
     using F = MF<WF>;
     constexpr int NPAIR = NT * 4;                  // token pairs
     constexpr int CONSUMERS = consumers(NT);
@@ -384,8 +386,7 @@ cudaError_t launch_mma_typed(const DeviceInfo& dev, MmaParams p, const CUtensorM
     }
     const int tiles = (p.N + tile_rows(NT) - 1) / tile_rows(NT);
     const int grid = std::min(tiles, dev.sm_count);
-    gemv_mma_kernel<WF, NT><<<grid, (consumers(NT) + 1) * 32, smem, s>>>(map, p);
-    return cudaGetLastError();
+    return launch_kernel(gemv_mma_kernel<WF, NT>, dim3(grid), dim3((consumers(NT) + 1) * 32), smem, s, map, p);
 }
 
 template <int WF>

@@ -73,6 +73,8 @@ __device__ __forceinline__ int* ws_valid(const MoeParams& p) { return reinterpre
 constexpr int ROUTE_SMEM_PAIRS = 8192;
 
 __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ int cnt[256];
     __shared__ int off[257];
     __shared__ int key_s[ROUTE_SMEM_PAIRS];   // expert of a valid pair, -1 for an invalid one
@@ -156,6 +158,8 @@ __device__ __forceinline__ bool wait_tile(uint64_t* bar, int* status) {
 
 // ------------------------------------------------------------- gate/up + SwiGLU
 __global__ void __launch_bounds__(THREADS) moe_up_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(128) uint8_t smem[];
     const int e = blockIdx.y, f0 = blockIdx.x * TILE;
     const int* offs = ws_offs(p);
@@ -237,6 +241,8 @@ __global__ void __launch_bounds__(THREADS) moe_up_kernel(const MoeParams p) {
 
 // ------------------------------------------------------------------- down
 __global__ void __launch_bounds__(THREADS) moe_down_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(128) uint8_t smem[];
     const int e = blockIdx.y, k0 = blockIdx.x * TILE;
     const int* offs = ws_offs(p);
@@ -297,6 +303,8 @@ __global__ void __launch_bounds__(THREADS) moe_down_kernel(const MoeParams p) {
 // y[t] = sum over the token's valid slots s, in increasing s, of rw * o; one
 // CTA row per token, four consecutive outputs per thread.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const int k = 4 * (blockIdx.y * blockDim.x + threadIdx.x);
     if (k >= p.K) return;
@@ -353,8 +361,7 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
     p.ws = static_cast<uint8_t*>(ws);
     p.L = moe_layout(T, K, F, E, topk);
     p.T = T; p.K = K; p.F = F; p.E = E; p.topk = topk;
-    moe_route_kernel<<<1, 1024, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(1024), 0, s, p);
     if (e != cudaSuccess) return e;
     if (moe_mma_enabled()) {
         e = launch_moe_projections(dev, T, K, F, E, topk, Wg, Wu, Wd, xq, reinterpret_cast<const int*>(p.ws + p.L.offs),
@@ -378,13 +385,13 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
                 return e;
             if (devid < 64) raised[devid] = 1;
         }
-        moe_up_kernel<<<dim3(F / TILE, E), THREADS, smem_up, s>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        moe_down_kernel<<<dim3(K / TILE, E), THREADS, smem_dn, s>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_kernel(moe_up_kernel, dim3(F / TILE, E), dim3(THREADS), smem_up, s, p)) != cudaSuccess)
+            return e;
+        if ((e = launch_kernel(moe_down_kernel, dim3(K / TILE, E), dim3(THREADS), smem_dn, s, p)) != cudaSuccess)
+            return e;
     }
-    moe_combine_kernel<<<dim3(static_cast<unsigned>(T), static_cast<unsigned>((K / 4 + 255) / 256)), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(T), static_cast<unsigned>((K / 4 + 255) / 256)),
+                         dim3(256), 0, s, p);
 }
 
 }  // namespace cq

@@ -287,6 +287,8 @@ template <bool UP>
 __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_constant__ CUtensorMap map0,
                                                              const __grid_constant__ CUtensorMap map1,
                                                              const MoeMmaParams p) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int NMAT = UP ? 2 : 1;
     constexpr int STAGE = NMAT * BOX_BYTES + RAWA_BYTES;      // weight boxes, then the pairs' raw segments
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -422,7 +424,8 @@ cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUten
         if (e != cudaSuccess) return e;
         if (devid < 64) raised[devid] = 1;
     }
-    moe_mma_kernel<UP><<<dim3(p.rows_per_expert / ROWS, E), THREADS, smem, s>>>(m0, m1, p);
+    e = launch_kernel(moe_mma_kernel<UP>, dim3(p.rows_per_expert / ROWS, E), dim3(THREADS), smem, s, m0, m1, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

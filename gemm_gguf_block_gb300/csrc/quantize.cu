@@ -30,6 +30,8 @@ __device__ __forceinline__ float warp_max(float a) {
 template <int AF>
 __global__ void __launch_bounds__(256) quantize32_kernel(const float* __restrict__ x, uint8_t* __restrict__ xq,
                                                          int64_t nblocks) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int BB = AF == CQ_Q8_0 ? 34 : 36;     // block bytes
     constexpr int QOFF = AF == CQ_Q8_0 ? 2 : 4;     // offset of the quants
     const int lane = threadIdx.x & 31, sub = lane & 3;
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(256) quantize32_kernel(const float* __restrict
 
 __global__ void __launch_bounds__(256) quantize_q8k_kernel(const float* __restrict__ x, uint8_t* __restrict__ xq,
                                                            int64_t nblocks) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t b = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; b < nblocks; b += stride) {
@@ -128,12 +132,11 @@ cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, v
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>((warps + 7) / 8, 16384));
     uint8_t* out = static_cast<uint8_t*>(xq);
     switch (act_fmt) {
-    case CQ_Q8_0: quantize32_kernel<CQ_Q8_0><<<grid, 256, 0, s>>>(x, out, nblocks); break;
-    case CQ_Q8_1: quantize32_kernel<CQ_Q8_1><<<grid, 256, 0, s>>>(x, out, nblocks); break;
-    case CQ_Q8_K: quantize_q8k_kernel<<<grid, 256, 0, s>>>(x, out, nblocks); break;
+    case CQ_Q8_0: return launch_kernel(quantize32_kernel<CQ_Q8_0>, dim3(grid), dim3(256), 0, s, x, out, nblocks);
+    case CQ_Q8_1: return launch_kernel(quantize32_kernel<CQ_Q8_1>, dim3(grid), dim3(256), 0, s, x, out, nblocks);
+    case CQ_Q8_K: return launch_kernel(quantize_q8k_kernel, dim3(grid), dim3(256), 0, s, x, out, nblocks);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace cq

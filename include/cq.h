@@ -215,6 +215,23 @@ cq_status cq_read_global_status(int32_t* out_code, int clear);
 
 const char* cq_status_string(cq_status s);
 
+/*
+ * Library-wide options (process-wide, all devices; set them before the calls
+ * they should affect, not while calls are being issued from other threads).
+ *
+ * CQ_OPT_WEIGHTS_CONST (default 0): 1 is the caller's promise that no weight
+ * buffer passed to cq_gemv is written by work that may still be in flight on
+ * the stream of the call (the weights of an inference model). The GEMV then
+ * starts streaming its weight tiles while the preceding kernel in the stream
+ * is still finishing, and waits for that kernel only before it reads the
+ * activations or writes its output. With 0, every kernel waits for the
+ * preceding one before touching any global memory.
+ *
+ * Returns CQ_ERR_INVALID_ARG for an unknown option or value.
+ */
+typedef enum { CQ_OPT_WEIGHTS_CONST = 1 } cq_option;
+cq_status cq_set_option(cq_option opt, int64_t value);
+
 #ifdef __cplusplus
 }
 #endif

@@ -79,6 +79,13 @@ def test_gemm_ws_validation(L):
     assert f(cq.Q4_K, 0, 8, 256, None, None, None, None, 0) == cq.OK
 
 
+def test_set_option(L):
+    assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 1) == cq.OK
+    assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 0) == cq.OK
+    assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 2) == cq.ERR_INVALID_ARG
+    assert cq.cq_set_option(99, 1) == cq.ERR_INVALID_ARG
+
+
 def test_quantize_validation(L):
     assert cq.cq_quantize_act(cq.Q4_0, 1, 256, A, A) == cq.ERR_UNSUPPORTED_FORMAT
     assert cq.cq_quantize_act(cq.Q8_0, 1, 96, A, A) == cq.ERR_SHAPE

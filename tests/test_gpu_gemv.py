@@ -149,3 +149,33 @@ def test_no_device_status(orc):
     cq = cq_built()
     st, code = cq.cq_read_global_status(1)
     assert st == cq.OK and code == 0
+
+
+def test_weights_const_option_same_bits(orc):
+    """Prefetching weights ahead of the dependency wait changes no result: a
+    chain of quantise -> GEMV calls, each GEMV's activation produced by the
+    kernel right before it, gives the same bits with the option on and off."""
+    torch = torch_cuda()
+    cq = cq_built()
+    rng = np.random.default_rng(7)
+    shapes = [(4096, 4096), (1024, 4096), (2048, 8192)]
+    Ws = [dev(torch, synth.gen_q8_0(rng, N, K)) for N, K in shapes]
+    xs = [dev(torch, rng.standard_normal((1, K)).astype(np.float32)) for _, K in shapes]
+
+    def run():
+        outs = []
+        for W, x, (N, K) in zip(Ws, xs, shapes):
+            xq = cq.quantize_act_t(x, cq.Q8_0)
+            outs.append(cq.gemv_t(W, xq, cq.Q8_0, K))
+        torch.cuda.synchronize()
+        return [o.cpu().numpy() for o in outs]
+
+    try:
+        assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 0) == cq.OK
+        a = run()
+        assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 1) == cq.OK
+        b = run()
+    finally:
+        cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 0)
+    for u, v in zip(a, b):
+        assert np.array_equal(u.view(np.uint32), v.view(np.uint32))
