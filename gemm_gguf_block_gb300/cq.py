@@ -31,6 +31,7 @@ _P, _I64, _I, _SZ = C.c_void_p, C.c_int64, C.c_int, C.c_size_t
 SIGNATURES = {
     "cq_quantize_act": (_I, [_I, _I64, _I64, _P, _P, _P]),
     "cq_gemv": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "cq_gemv_x": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "cq_gemm": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "cq_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
     "cq_gemm_ws": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
@@ -85,6 +86,10 @@ def cq_quantize_act(act_fmt, M, K, x, xq, stream=0):
 
 def cq_gemv(w_fmt, M, N, K, W, xq, y, stream=0):
     return lib().cq_gemv(w_fmt, M, N, K, W, xq, y, stream)
+
+
+def cq_gemv_x(w_fmt, M, N, K, W, x, xq, y, stream=0):
+    return lib().cq_gemv_x(w_fmt, M, N, K, W, x, xq, y, stream)
 
 
 def cq_gemm(w_fmt, M, N, K, W, xq, y, stream=0):
@@ -171,6 +176,18 @@ def gemv_t(W, xq, w_fmt: int, K: int, out=None):
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=W.device)
     _check("cq_gemv", cq_gemv(w_fmt, M, N, K, W.data_ptr(), xq.data_ptr(), y.data_ptr(), _stream_handle()))
     return y
+
+
+def gemv_x_t(W, x, w_fmt: int, out=None):
+    """cq_gemv_x: x fp32 [M, K] (M <= 16) -> (y fp32 [M, N], xq uint8 [M, act_row_bytes])."""
+    torch = _torch()
+    M, K = x.shape
+    N = W.shape[0]
+    xq = torch.empty((M, row_bytes(ACT_FOR[w_fmt], K)), dtype=torch.uint8, device=x.device)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check("cq_gemv_x", cq_gemv_x(w_fmt, M, N, K, W.data_ptr(), x.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                  _stream_handle()))
+    return y, xq
 
 
 def gemm_t(W, xq, w_fmt: int, K: int, out=None):

@@ -115,7 +115,7 @@ cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     if (!aligned16(W) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
     cq::DeviceInfo dev;
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
-    cudaError_t e = cq::launch_gemv(dev, w_fmt, static_cast<int>(M), N, K, W, xq, y,
+    cudaError_t e = cq::launch_gemv(dev, w_fmt, static_cast<int>(M), N, K, W, xq, y, nullptr,
                                     static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
@@ -124,6 +124,22 @@ cq_status cq_set_option(cq_option opt, int64_t value) {
     if (opt != CQ_OPT_WEIGHTS_CONST || (value != 0 && value != 1)) return CQ_ERR_INVALID_ARG;
     cq::g_weights_const.store(static_cast<int>(value), std::memory_order_relaxed);
     return CQ_OK;
+}
+
+cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const float* x, void* xq,
+                    float* y, void* stream) {
+    if (!is_weight_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, N, K);
+    if (st != CQ_OK) return st;
+    if (M > 16) return CQ_ERR_SHAPE;
+    if (M == 0) return CQ_OK;
+    if (x == nullptr || xq == nullptr || (N > 0 && (W == nullptr || y == nullptr))) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(xq) || (N > 0 && (!aligned16(W) || !aligned16(y)))) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_gemv(dev, w_fmt, static_cast<int>(M), N, K, W, xq, y, x,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 
 cq_status cq_read_global_status(int32_t* out_code, int clear) {

@@ -46,8 +46,10 @@ cudaError_t device_info(DeviceInfo* out);
 
 cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, void* xq, cudaStream_t s);
 
+// With x (fp32 [M][K]) non-null the activations are quantized on the way
+// (cq_gemv_x): xq receives them and y is the same as from xq.
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
-                        const void* xq, float* y, cudaStream_t s);
+                        const void* xq, float* y, const float* x, cudaStream_t s);
 
 // Tensor-core batched GEMV (2 <= M <= 16; Q4_0, Q4_1, Q8_0) and the shared
 // memory it needs (0 when the format has no such path).

@@ -60,6 +60,8 @@ struct GemvParams {
     int act_bytes;
     int tok_pitch;    // bytes per token of staged activations
     int wconst;       // weights constant in flight: prefetch them before the dependency wait
+    const float* x;   // fp32 activations to quantize in the kernel (cq_gemv_x), else null
+    uint8_t* xq_out;  // where CTA 0 writes their quantisation (with x)
 };
 
 // Exact float of an int with |i| < 2^22: the bits of 1.5 * 2^23 + i, minus 1.5 * 2^23.
@@ -124,6 +126,118 @@ __device__ void stage_activations(const GemvParams& p, uint8_t* act) {
                 reinterpret_cast<float*>(dst + 128)[2 * b + 1] = h2f(s[1]);
             } else {
                 reinterpret_cast<float*>(dst + 128)[b] = h2f(s[0]);
+            }
+        }
+    }
+}
+
+// Quantise fp32 activations (cq_gemv_x) and stage them exactly as
+// stage_activations stages the output of cq_quantize_act: the same rule in the
+// same fp32 operations (q8_scale, q8_inv, quant_q8, RN fp16 scales), so the
+// same bits. CTA 0 also writes the quantized rows to p.xq_out.
+template <int WF>
+__device__ void stage_activations_x(const GemvParams& p, uint8_t* act) {
+    const int nthr = blockDim.x;
+    const bool out = blockIdx.x == 0;
+    const int64_t K = static_cast<int64_t>(p.nc) * G<WF>::CE;
+    if constexpr (WF == CQ_Q4_K) {
+        // A warp per superblock, eight consecutive elements per lane.
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nthr >> 5;
+        const int ns = p.nc;
+        for (int sb = warp; sb < p.M * ns; sb += nw) {
+            const int m = sb / ns, c = sb - m * ns;
+            const float4* src = reinterpret_cast<const float4*>(p.x + m * K + c * 256 + 8 * lane);
+            const float4 v0 = src[0], v1 = src[1];
+            const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            float a = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+#pragma unroll
+            for (int o = 16; o; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const float d = q8_scale(a);
+            const float id = q8_inv(d);
+            uint32_t packed[2] = {0u, 0u};
+            int sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int q = quant_q8(v[i], id);
+                sum += q;
+                packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (i & 3));
+            }
+            const int s16 = sum + __shfl_xor_sync(0xffffffffu, sum, 1);      // 16 consecutive quants
+            const int s32 = s16 + __shfl_xor_sync(0xffffffffu, s16, 2);      // 32: a bsum pair
+            uint8_t* dst = act + m * p.tok_pitch + c * G<WF>::ACP;
+            reinterpret_cast<uint32_t*>(dst + 8 * lane)[0] = packed[0];
+            reinterpret_cast<uint32_t*>(dst + 8 * lane)[1] = packed[1];
+            if (lane == 0) *reinterpret_cast<float*>(dst + 256) = d;
+            if ((lane & 3) == 0) *reinterpret_cast<int*>(dst + 272 + lane) = s32;
+            if (out) {
+                uint8_t* blk = p.xq_out + static_cast<int64_t>(sb) * 292;
+                uint32_t* qw = reinterpret_cast<uint32_t*>(blk + 4 + 8 * lane);
+                qw[0] = packed[0];
+                qw[1] = packed[1];
+                if ((lane & 1) == 0) *reinterpret_cast<int16_t*>(blk + 260 + lane) = static_cast<int16_t>(s16);
+                if (lane == 0) *reinterpret_cast<float*>(blk) = d;
+            }
+        }
+    } else {
+        constexpr int BB = WF == CQ_Q4_1 ? 36 : 34;     // Q8_1 or Q8_0 block bytes
+        constexpr int QO = WF == CQ_Q4_1 ? 4 : 2;       // quant offset in the block
+        const int nblk = p.M * p.nc * 4;
+        for (int i = threadIdx.x; i < nblk; i += nthr) {
+            const int m = i / (p.nc * 4), r = i - m * p.nc * 4;
+            const int c = r >> 2, b = r & 3;
+            const float4* src = reinterpret_cast<const float4*>(p.x + m * K + 32 * r);
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 f = src[j];
+                v[4 * j] = f.x;
+                v[4 * j + 1] = f.y;
+                v[4 * j + 2] = f.z;
+                v[4 * j + 3] = f.w;
+            }
+            float a = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) a = fmaxf(a, fabsf(v[j]));
+            const float d = q8_scale(a);
+            const float id = q8_inv(d);
+            uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            int sum = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int q = quant_q8(v[j], id);
+                sum += q;
+                w[j >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (j & 3));
+            }
+            const __half dh = __float2half_rn(d);
+            uint8_t* dst = act + m * p.tok_pitch + c * G<WF>::ACP;
+            uint32_t* q = reinterpret_cast<uint32_t*>(dst + 32 * b);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) q[j] = w[j];
+            __half sh = __float2half_rn(0.0f);
+            if constexpr (WF == CQ_Q4_1) {
+                sh = __float2half_rn(__fmul_rn(d, static_cast<float>(sum)));
+                reinterpret_cast<float*>(dst + 128)[2 * b] = __half2float(dh);
+                reinterpret_cast<float*>(dst + 128)[2 * b + 1] = __half2float(sh);
+            } else {
+                reinterpret_cast<float*>(dst + 128)[b] = __half2float(dh);
+            }
+            if (out) {
+                uint8_t* blk = p.xq_out + static_cast<int64_t>(i) * BB;
+                *reinterpret_cast<__half*>(blk) = dh;
+                if constexpr (WF == CQ_Q4_1) {
+                    *reinterpret_cast<__half*>(blk + 2) = sh;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) reinterpret_cast<uint32_t*>(blk + QO)[j] = w[j];
+                } else {
+                    uint16_t* h = reinterpret_cast<uint16_t*>(blk + QO);     // 2 mod 4: 16-bit stores
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        h[2 * j] = static_cast<uint16_t>(w[j]);
+                        h[2 * j + 1] = static_cast<uint16_t>(w[j] >> 16);
+                    }
+                }
             }
         }
     }
@@ -399,7 +513,10 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
         }
     }
     if (p.wconst) pdl_wait();
-    stage_activations<WF>(p, act);
+    if (p.x != nullptr)
+        stage_activations_x<WF>(p, act);
+    else
+        stage_activations<WF>(p, act);
     __syncthreads();
     if (!active) return;
 
@@ -545,7 +662,7 @@ cudaError_t launch_fmt(const DeviceInfo& dev, const GemvParams& p, int64_t group
 
 template <int WF>
 cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, const void* W, const void* xq,
-                            float* y, cudaStream_t s) {
+                            float* y, const float* x, cudaStream_t s) {
     using F = G<WF>;
     const int nc = static_cast<int>(K / F::CE);
     if (nc > CBUF_FLOATS) return cudaErrorInvalidValue;
@@ -561,6 +678,10 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         p.M = std::min(max_tok, M - m0);
         p.W = static_cast<const uint8_t*>(W);
         p.xq = static_cast<const uint8_t*>(xq) + static_cast<int64_t>(m0) * act_row;
+        if (x != nullptr) {
+            p.x = x + static_cast<int64_t>(m0) * K;
+            p.xq_out = const_cast<uint8_t*>(p.xq);
+        }
         p.y = y + static_cast<int64_t>(m0) * N;
         p.status = dev.status;
         p.N = N;
@@ -593,18 +714,27 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
 }  // namespace
 
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
-                        const void* xq, float* y, cudaStream_t s) {
-    if (M <= 0 || N <= 0) return cudaSuccess;
+                        const void* xq, float* y, const float* x, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    const int afmt = act_fmt_for(w_fmt);
+    if (afmt < 0) return cudaErrorInvalidValue;
+    if (N <= 0) return x != nullptr ? launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s) : cudaSuccess;
     // Several tokens: the tensor-core kernel when the activations fit its
-    // shared memory (same fixed order, so the same bits).
+    // shared memory (same fixed order, so the same bits). It stages quantized
+    // activations, so fp32 ones are quantized by their own launch first.
     const int need = gemv_mma_smem(w_fmt, M, K);
-    if (M >= 2 && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled())
+    if (M >= 2 && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled()) {
+        if (x != nullptr) {
+            const cudaError_t e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
+            if (e != cudaSuccess) return e;
+        }
         return launch_gemv_mma(dev, w_fmt, M, N, K, W, xq, y, s);
+    }
     switch (w_fmt) {
-    case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, x, s);
+    case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, x, s);
+    case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, x, s);
+    case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, xq, y, x, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -118,6 +118,19 @@ cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
                   float* y, void* stream);
 
 /*
+ * cq_quantize_act followed by cq_gemv, as one call: x (fp32 [M][K], DEVICE,
+ * 16-byte aligned) is quantized to the activation format paired with w_fmt
+ * and written to xq (16-byte aligned, M rows of blocks, byte for byte what
+ * cq_quantize_act writes), and y = W . xq as cq_gemv computes it, bit for bit.
+ * For one token the quantisation happens inside the GEMV kernel (each CTA
+ * quantizes the row it needs; the first also writes xq), which takes a
+ * launch and a dependency off the decode path. M <= 16; N == 0 only
+ * quantizes. Errors as cq_gemv.
+ */
+cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const float* x,
+                    void* xq, float* y, void* stream);
+
+/*
  * Prefill GEMM, any M >= 0 (cera README "Supported models": batched-GEMM
  * prefill; alice-llm "Computation Path (Q4_K)"). Same operands and result as
  * cq_gemv; each row equals the cq_gemv result for that token bit for bit.

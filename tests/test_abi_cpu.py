@@ -79,6 +79,19 @@ def test_gemm_ws_validation(L):
     assert f(cq.Q4_K, 0, 8, 256, None, None, None, None, 0) == cq.OK
 
 
+def test_gemv_x_validation(L):
+    f = cq.cq_gemv_x
+    assert f(99, 1, 8, 256, A, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q8_0, 17, 8, 256, A, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q8_0, 1, 8, 100, A, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q8_0, 1, 8, 256, A, None, A, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q8_0, 1, 8, 256, A, A, None, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q8_0, 1, 8, 256, A, A + 4, A, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q8_0, 1, 8, 256, A, A, A + 4, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q8_0, 1, 8, 256, A, A, A, A + 4) == cq.ERR_ALIGNMENT
+    assert f(cq.Q8_0, 0, 8, 256, None, None, None, None) == cq.OK
+
+
 def test_set_option(L):
     assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 1) == cq.OK
     assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 0) == cq.OK

@@ -179,3 +179,33 @@ def test_weights_const_option_same_bits(orc):
         cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 0)
     for u, v in zip(a, b):
         assert np.array_equal(u.view(np.uint32), v.view(np.uint32))
+
+
+@pytest.mark.parametrize("wfmt", FMTS)
+@pytest.mark.parametrize("N,K", [(33, 512), (100, 768), (257, 2048), (64, 8448)])
+@pytest.mark.parametrize("M", [1, 3, 16])
+def test_gemv_x_equals_quantize_then_gemv(orc, wfmt, N, K, M):
+    """cq_gemv_x writes the bytes cq_quantize_act writes and the y cq_gemv computes, bit for bit."""
+    torch = torch_cuda()
+    cq = cq_built()
+    rng = np.random.default_rng(N * 7 + K + M)
+    W = dev(torch, synth.GEN[W_NAMES[wfmt]](rng, N, K))
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[0, :32] = 0.0                                  # an all-zero block
+    xd = dev(torch, x)
+    y, xq = cq.gemv_x_t(W, xd, wfmt)
+    xq_ref = cq.quantize_act_t(xd, cq.ACT_FOR[wfmt])
+    y_ref = cq.gemv_t(W, xq_ref, wfmt, K)
+    assert np.array_equal(xq.cpu().numpy(), xq_ref.cpu().numpy())
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ref.cpu().numpy().view(np.uint32))
+    assert np.array_equal(xq.cpu().numpy(), orc.quantize(orc.ACT_FOR[wfmt], x))
+
+
+def test_gemv_x_quantize_only():
+    torch = torch_cuda()
+    cq = cq_built()
+    x = dev(torch, np.random.default_rng(3).standard_normal((2, 1024)).astype(np.float32))
+    xq = torch.zeros((2, cq.row_bytes(cq.Q8_0, 1024)), dtype=torch.uint8, device="cuda")
+    assert cq.cq_gemv_x(cq.Q4_0, 2, 0, 1024, None, x.data_ptr(), xq.data_ptr(), None,
+                        torch.cuda.current_stream().cuda_stream) == cq.OK
+    assert torch.equal(xq, cq.quantize_act_t(x, cq.Q8_0))
