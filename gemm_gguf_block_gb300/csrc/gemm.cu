@@ -20,11 +20,12 @@
 // t = fma(d, S, -(dmin * I)) and y = fma(d_x, t, y) -- so every row equals the
 // cq_gemv row bit for bit.
 //
-// Warp roles (576 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
+// Warp roles (576 or 832 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
 // map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory and
 // one lane issues the MMAs; warps 2-9 convert raw weights and Q8_K
 // activations into fp16 tiles in the canonical K-major no-swizzle layout;
-// warps 10-17 are the epilogue (tensor-memory lanes 32*(warp%4)...). Every wait
+// warps 10-17 (10-25 with the workspace) are the epilogue (tensor-memory
+// lanes 32*(warp%4)...). Every wait
 // is bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
 #include <mutex>
@@ -49,9 +50,18 @@ constexpr int B_BYTES = BN * KH * 2;        // 32 KB
 constexpr int AMIN_BYTES = BM * 16 * 2;     // 4 KB
 constexpr int BMIN_BYTES = BN * 16 * 2;     // 4 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + AMIN_BYTES + BMIN_BYTES;
-constexpr int THREADS = 576;     // 2 + 8 converter + 8 epilogue warps
-constexpr int NEPI = 256;        // epilogue threads
-constexpr int NCONV = 256;       // converter threads
+constexpr int NCONV = 256;       // converter threads (warps 2-9)
+// Epilogue warps (from warp 10): 16 when the activations come pre-converted
+// (the converters then need few registers), each thread draining 32 token
+// columns of its row per superblock in 8-column loads; else 8 warps of 64
+// columns in 16-column loads.
+template <bool PRE> struct Epi {
+    static constexpr int WARPS = PRE ? 16 : 8;
+    static constexpr int THREADS = WARPS * 32;
+    static constexpr int COLS = BN / (WARPS / 4);      // token columns per thread
+    static constexpr int CW = PRE ? 8 : 16;            // columns per tensor-memory load
+};
+template <bool PRE> constexpr int kernel_threads() { return (2 + 8) * 32 + Epi<PRE>::THREADS; }
 constexpr uint32_t TMEM_COLS = 512;         // h0 | h1 | mins | y, 128 columns each
 constexpr uint32_t COL_H0 = 0, COL_H1 = 128, COL_MIN = 256, COL_Y = 384;
 
@@ -133,8 +143,9 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
 // PRE: the activations come pre-converted (cq_gemm_ws): the producer
 // bulk-copies each stage's B operand and the converters handle only weights.
 template <bool PRE>
-__global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                              const GemmParams p) {
+__global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                             const GemmParams p) {
+    constexpr int NEPI = Epi<PRE>::THREADS;
     pdl_trigger();
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
@@ -349,11 +360,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        // Eight warps: warp w reads tensor-memory lanes 32*(w%4)..+31 (weight
-        // rows) and half of the 128 token columns.
-        const int et = threadIdx.x - 320;               // 0..255
+        // Warp w reads tensor-memory lanes 32*(w%4)..+31 (weight rows); the
+        // warps of column group (w-10)/4 take COLS consecutive token columns.
+        constexpr int COLS = Epi<PRE>::COLS, CW = Epi<PRE>::CW;
+        const int et = threadIdx.x - 320;               // 0..NEPI-1
         const int quarter = warp & 3;
-        const int c0 = ((warp - 10) >> 2) * 64;         // first token column of this warp
+        const int c0 = ((warp - 10) >> 2) * COLS;       // first token column of this warp
         const int row = n0 + quarter * 32 + lane;
         const bool row_ok = row < p.N;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -371,6 +383,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         float dx_next;
         uint32_t dd_next;
         fetch_scales(0, dx_next, dd_next);
+        float yr[PRE ? COLS : 1];                       // PRE: this thread's outputs
+#pragma unroll
+        for (int i = 0; i < (PRE ? COLS : 1); ++i) yr[i] = 0.0f;
         for (int s = 0; s < ns; ++s) {
             // this superblock's activation scales and row scales, fetched one superblock ahead
             if (et < BN) dxbuf[(s & 1) * BN + et] = dx_next;
@@ -388,44 +403,79 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             // Fixed order: t = fma(d, RN(h0 + h1), -(dmin * I)); y = fma(d_x, t, y).
             const uint64_t d2 = tc::pk(d, d), nm2 = tc::pk(ndmin, ndmin);
             const float2* dx2 = reinterpret_cast<const float2*>(dxbuf + (s & 1) * BN + c0);
-            for (int cb = 0; cb < 64; cb += 16) {
-                uint32_t h0[16], h1[16], mi[16], yv[16];
-                tc::ld16(lane_addr + COL_H0 + c0 + cb, h0);
-                tc::ld16(lane_addr + COL_H1 + c0 + cb, h1);
-                tc::ld16(lane_addr + COL_MIN + c0 + cb, mi);
-                if (s > 0) tc::ld16(lane_addr + COL_Y + c0 + cb, yv);
-                tc::wait_ld();
+            if constexpr (PRE) {
+                // y stays in registers (COLS per thread); three loads per chunk.
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
-                                                tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
-                    const uint64_t tn = tc::mul2(nm2, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
-                    const uint64_t t = tc::fma2(d2, S, tn);
-                    const float2 x = dx2[(cb + i) >> 1];
-                    const uint64_t yp = s > 0 ? tc::pk(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1]))
-                                              : tc::pk(0.0f, 0.0f);
-                    float lo, hi;
-                    tc::upk(tc::fma2(tc::pk(x.x, x.y), t, yp), lo, hi);
-                    yv[i] = __float_as_uint(lo);
-                    yv[i + 1] = __float_as_uint(hi);
+                for (int cb = 0; cb < COLS; cb += CW) {
+                    uint32_t h0[CW], h1[CW], mi[CW];
+                    tc::ldw<CW>(lane_addr + COL_H0 + c0 + cb, h0);
+                    tc::ldw<CW>(lane_addr + COL_H1 + c0 + cb, h1);
+                    tc::ldw<CW>(lane_addr + COL_MIN + c0 + cb, mi);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < CW; i += 2) {
+                        const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
+                                                    tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
+                        const uint64_t tn =
+                            tc::mul2(nm2, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
+                        const uint64_t t = tc::fma2(d2, S, tn);
+                        const float2 x = dx2[(cb + i) >> 1];
+                        tc::upk(tc::fma2(tc::pk(x.x, x.y), t, tc::pk(yr[cb + i], yr[cb + i + 1])), yr[cb + i],
+                                yr[cb + i + 1]);
+                    }
                 }
-                tc::st16(lane_addr + COL_Y + c0 + cb, yv);
+            } else {
+#pragma unroll 1
+                for (int cb = 0; cb < COLS; cb += CW) {
+                    uint32_t h0[CW], h1[CW], mi[CW], yv[CW];
+                    tc::ldw<CW>(lane_addr + COL_H0 + c0 + cb, h0);
+                    tc::ldw<CW>(lane_addr + COL_H1 + c0 + cb, h1);
+                    tc::ldw<CW>(lane_addr + COL_MIN + c0 + cb, mi);
+                    if (s > 0) tc::ldw<CW>(lane_addr + COL_Y + c0 + cb, yv);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < CW; i += 2) {
+                        const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
+                                                    tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
+                        const uint64_t tn =
+                            tc::mul2(nm2, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
+                        const uint64_t t = tc::fma2(d2, S, tn);
+                        const float2 x = dx2[(cb + i) >> 1];
+                        const uint64_t yp = s > 0 ? tc::pk(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1]))
+                                                  : tc::pk(0.0f, 0.0f);
+                        float lo, hi;
+                        tc::upk(tc::fma2(tc::pk(x.x, x.y), t, yp), lo, hi);
+                        yv[i] = __float_as_uint(lo);
+                        yv[i + 1] = __float_as_uint(hi);
+                    }
+                    tc::stw<CW>(lane_addr + COL_Y + c0 + cb, yv);
+                }
+                tc::wait_st();
             }
-            tc::wait_st();
             tc::fence_before();
             tc::mbar_arrive(&bars[B_ACC_EMPTY]);
         }
         if (__all_sync(0xffffffffu, !*abort_flag)) {
             // y[m][n] for this row: a warp's stores to one token are 32 consecutive floats.
-            for (int cb = 0; cb < 64; cb += 16) {
-                uint32_t yv[16];
-                tc::ld16(lane_addr + COL_Y + c0 + cb, yv);
-                tc::wait_ld();
+            if constexpr (PRE) {
                 if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + c0 + cb + i;
-                        if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = __uint_as_float(yv[i]);
+                    for (int i = 0; i < COLS; ++i) {
+                        const int m = m0 + c0 + i;
+                        if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = yr[i];
+                    }
+                }
+            } else {
+                for (int cb = 0; cb < COLS; cb += CW) {
+                    uint32_t yv[CW];
+                    tc::ldw<CW>(lane_addr + COL_Y + c0 + cb, yv);
+                    tc::wait_ld();
+                    if (row_ok) {
+#pragma unroll
+                        for (int i = 0; i < CW; ++i) {
+                            const int m = m0 + c0 + cb + i;
+                            if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = __uint_as_float(yv[i]);
+                        }
                     }
                 }
             }
@@ -565,9 +615,9 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
                           dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg), const_cast<float*>(p.dxs));
         if (e != cudaSuccess) return e;
-        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
+        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(kernel_threads<true>()), SMEM_BYTES, s, map, p);
     }
-    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
+    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(kernel_threads<false>()), SMEM_BYTES, s, map, p);
 }
 
 }  // namespace cq
