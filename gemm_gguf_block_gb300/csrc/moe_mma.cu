@@ -40,10 +40,13 @@ constexpr int BOX_BYTES = ROWS * SEGB * 18;        // one matrix, one segment: 1
 constexpr int ACT_PITCH = 512 + 64;                 // bytes per token per segment (fp16) + pad:
                                                     // 36 x 16 B, so lanes' 16-byte reads miss each other's banks
 constexpr int ACT_BYTES = TOK * ACT_PITCH;          // 36864
-// Scale table: per (32-block b, token pair j) {d_x[2j], d_x[2j+1], bias[2j],
-// bias[2j+1]}, pitch 33 entries per block so the converters' stores spread over banks.
+// Scale tables, per (32-block b, token pair j), pitch 33 entries per block so
+// the converters' stores spread over banks: the accumulator biases as the
+// quad {bias[2j], bias[2j+1], bias[2j], bias[2j+1]} -- the mma's C fragment
+// as loaded, four consecutive registers -- and the scales {d_x[2j], d_x[2j+1]}.
 constexpr int SCL_PITCH = TOK / 2 + 1;
-constexpr int SCL_BYTES = SEGB * SCL_PITCH * 16;    // 4224
+constexpr int BQ_BYTES = SEGB * SCL_PITCH * 16;     // 4224
+constexpr int SCL_BYTES = (BQ_BYTES + SEGB * SCL_PITCH * 8 + 127) / 128 * 128;   // keeps the stages 128-byte aligned
 constexpr int RAWA = SEGB * 34;                     // one token's Q8_0 segment: 272 bytes
 constexpr int RAWA_BYTES = TOK * RAWA;              // 17408
 
@@ -65,13 +68,13 @@ __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<ui
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 // D = A * B + C (C given), and D += A * B.
-__device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
-                                          float c1) {
+__device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
+                                          const float4& c) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%10,%11};"
+        "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
 }
 __device__ __forceinline__ void mma16816acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -101,7 +104,8 @@ struct Smem {
     uint64_t* empty;
     int* pairs;        // [TOK] pair ids of the pass
     uint8_t* act;      // [TOK][ACT_PITCH] fp16 activations of one segment
-    float4* scl;       // [SEGB][SCL_PITCH] scales and accumulator biases
+    float4* bq;        // [SEGB][SCL_PITCH] accumulator bias quads
+    float2* dx;        // [SEGB][SCL_PITCH] activation scale pairs
     uint8_t* wst;      // [stages][stage bytes]
 };
 
@@ -116,7 +120,8 @@ __device__ __forceinline__ int chunk_pos(int b, int c) { return 64 * b + 16 * (c
 // the order lane t = c of an m16n8k16 B fragment reads with one 16-byte load.
 template <int NT>
 __device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, int np, int ct) {
-    float* sclf = reinterpret_cast<float*>(sm.scl);
+    float* bqf = reinterpret_cast<float*>(sm.bq);
+    float* dxf = reinterpret_cast<float*>(sm.dx);
     for (int it = ct; it < 8 * NT * SEGB; it += CONSUMERS * 32) {
         const int tk = it >> 3, b = it & 7;
         uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
@@ -138,9 +143,11 @@ __device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, 
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             *reinterpret_cast<uint4*>(row + chunk_pos(b, c)) = make_uint4(hv[c], hv[c + 4], hv[c + 8], hv[c + 12]);
-        float* e = sclf + (b * SCL_PITCH + (tk >> 1)) * 4 + (tk & 1);
-        e[0] = d;
-        e[2] = static_cast<float>(-1032 * sx);
+        const int j = b * SCL_PITCH + (tk >> 1), hi = tk & 1;
+        const float bias = static_cast<float>(-1032 * sx);
+        bqf[4 * j + hi] = bias;
+        bqf[4 * j + 2 + hi] = bias;
+        dxf[2 * j + hi] = d;
     }
 }
 
@@ -193,19 +200,21 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
             load_wfrag(wa + b * 18, t, fa0, fa1, dwa0, dwa1);
             if constexpr (UP) load_wfrag(wa + BOX_BYTES + b * 18, t, fb0, fb1, dwb0, dwb1);
             const uint8_t* ab = sm.act + g * ACT_PITCH + chunk_pos(b, t);
-            const float4* sb = sm.scl + b * SCL_PITCH + t;
+            const float4* sq = sm.bq + b * SCL_PITCH + t;
+            const float2* sd = sm.dx + b * SCL_PITCH + t;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 const uint4 bv = *reinterpret_cast<const uint4*>(ab + 8 * n * ACT_PITCH);
-                const float4 sv = sb[4 * n];
-                const uint64_t dx = tc::pk(sv.x, sv.y);
+                const float4 bias = sq[4 * n];
+                const float2 dv = sd[4 * n];
+                const uint64_t dx = tc::pk(dv.x, dv.y);
                 float c[4];
-                mma16816c(c, fa0, bv.x, bv.y, sv.z, sv.w);
+                mma16816c(c, fa0, bv.x, bv.y, bias);
                 mma16816acc(c, fa1, bv.z, bv.w);
                 ya[n][0] = tc::fma2(tc::mul2(dwa0, dx), tc::pk(c[0], c[1]), ya[n][0]);
                 ya[n][1] = tc::fma2(tc::mul2(dwa1, dx), tc::pk(c[2], c[3]), ya[n][1]);
                 if constexpr (UP) {
-                    mma16816c(c, fb0, bv.x, bv.y, sv.z, sv.w);
+                    mma16816c(c, fb0, bv.x, bv.y, bias);
                     mma16816acc(c, fb1, bv.z, bv.w);
                     yb[n][0] = tc::fma2(tc::mul2(dwb0, dx), tc::pk(c[0], c[1]), yb[n][0]);
                     yb[n][1] = tc::fma2(tc::mul2(dwb1, dx), tc::pk(c[2], c[3]), yb[n][1]);
@@ -298,7 +307,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
     sm.empty = sm.full + 8;
     sm.pairs = reinterpret_cast<int*>(smem + 256);
     sm.act = smem + 1024;
-    sm.scl = reinterpret_cast<float4*>(sm.act + ACT_BYTES);
+    sm.bq = reinterpret_cast<float4*>(sm.act + ACT_BYTES);
+    sm.dx = reinterpret_cast<float2*>(sm.act + ACT_BYTES + BQ_BYTES);
     sm.wst = smem + 1024 + ACT_BYTES + SCL_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.y, r0 = blockIdx.x * ROWS;
