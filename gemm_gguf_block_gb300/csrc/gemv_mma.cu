@@ -42,6 +42,12 @@ __host__ __device__ constexpr int tile_rows(int NT) { return 16 * consumers(NT);
 // for the paired activation block; BIAS: the fp16 A operand holds BIAS + v
 // for a weight quant of value v (see a_frags), so the accumulator starts at
 // -BIAS * sum(x).
+// Bytes per weight row in a stage: the segment's 8 blocks, padded for Q4_1
+// (160 -> 176 bytes: 44 words, so the 8 rows one load instruction touches fall
+// in 8 different bank groups; the padding is the start of the next segment,
+// or zero fill past the end of the row).
+__host__ __device__ constexpr int stage_pitch(int bb) { return bb == 20 ? 176 : SEG_BLOCKS * bb; }
+
 template <int WF> struct MF;
 template <> struct MF<CQ_Q4_0> { static constexpr int BB = 18, QO = 2, ABB = 34, AQO = 2, BIAS = 1032; };
 template <> struct MF<CQ_Q4_1> { static constexpr int BB = 20, QO = 4, ABB = 36, AQO = 4, BIAS = 1024; };
@@ -223,7 +229,7 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
         const uint8_t* act = smem + p.smem_act + g * p.act_pitch + 16 * t;
         const float4* sc4 = reinterpret_cast<const float4*>(smem + p.smem_scale) + t;
         const float2* sx2 = reinterpret_cast<const float2*>(smem + p.smem_scale + p.nb * NPAIR * 16) + t;
-        const int seg_row_bytes = SEG_BLOCKS * F::BB;
+        const int seg_row_bytes = stage_pitch(F::BB);
         uint64_t c[NT][2], y[NT][2];   // (row g | row g+8) x (token 8n+2t, 8n+2t+1)
         int64_t k = 0;
         bool ok = true;
@@ -366,7 +372,7 @@ MmaSmem mma_smem(int bb, int M, int64_t K) {
     m.scale = m.act + (NT * 8 * m.act_pitch + 127) / 128 * 128;
     const int scale_bytes = nb * NT * 4 * (bb == 20 ? 24 : 16);
     m.stage = m.scale + (scale_bytes + 1023) / 1024 * 1024;
-    m.stage_bytes = ROWS * SEG_BLOCKS * bb;
+    m.stage_bytes = ROWS * stage_pitch(bb);
     m.fixed = m.stage;
     return m;
 }
@@ -420,7 +426,7 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.wrow / 2), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.wrow)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(SEG_BLOCKS * F::BB / 2),
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(stage_pitch(F::BB) / 2),
                                static_cast<cuuint32_t>(tile_rows(NT))};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
