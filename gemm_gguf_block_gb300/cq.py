@@ -43,6 +43,7 @@ SIGNATURES = {
     "cq_read_global_status": (_I, [_P, _I]),
     "cq_status_string": (C.c_char_p, [_I]),
     "cq_set_option": (_I, [_I, _I64]),
+    "cq_selftest_wait_timeout": (_I, [_I64, _P, _P]),
 }
 
 OPT_WEIGHTS_CONST = 1
@@ -94,6 +95,13 @@ def cq_gemv_x(w_fmt, M, N, K, W, x, xq, y, stream=0):
 
 def cq_gemm(w_fmt, M, N, K, W, xq, y, stream=0):
     return lib().cq_gemm(w_fmt, M, N, K, W, xq, y, stream)
+
+
+def cq_selftest_wait_timeout(limit_ns, stream=0):
+    """(status, device code) of the bounded-wait self-test."""
+    code = C.c_int32(0)
+    st = lib().cq_selftest_wait_timeout(limit_ns, C.byref(code), stream)
+    return st, code.value
 
 
 def cq_set_option(opt, value):

@@ -142,6 +142,16 @@ cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 
+cq_status cq_selftest_wait_timeout(int64_t limit_ns, int32_t* out_code, void* stream) {
+    if (out_code == nullptr || limit_ns < 1000 || limit_ns > 1000000000) return CQ_ERR_INVALID_ARG;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    if (cq::launch_wait_timeout_probe(static_cast<uint64_t>(limit_ns), dev.status,
+                                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return CQ_ERR_CUDA;
+    return cq_read_global_status(out_code, 1);
+}
+
 cq_status cq_read_global_status(int32_t* out_code, int clear) {
     if (out_code == nullptr) return CQ_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return CQ_ERR_CUDA;

@@ -46,6 +46,9 @@ cudaError_t device_info(DeviceInfo* out);
 
 cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, void* xq, cudaStream_t s);
 
+// Bounded-wait self-test (cq_selftest_wait_timeout).
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, int* status, cudaStream_t s);
+
 // With x (fp32 [M][K]) non-null the activations are quantized on the way
 // (cq_gemv_x): xq receives them and y is the same as from xq.
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,

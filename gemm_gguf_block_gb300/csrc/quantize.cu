@@ -122,7 +122,24 @@ __global__ void __launch_bounds__(256) quantize_q8k_kernel(const float* __restri
     }
 }
 
+// Self-test of the bounded wait every kernel uses: one thread waits, with
+// the given limit, on an mbarrier phase that nothing completes, then sets the
+// timeout bit in the status word -- the path a kernel takes when a copy never
+// lands. Nothing faults and the context stays usable.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns, int* status) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ uint64_t bar;
+    mbar_init(&bar, 1);                       // one arrival expected; none comes
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0, limit_ns)) atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, int* status, cudaStream_t s) {
+    return launch_kernel(wait_timeout_probe_kernel, dim3(1), dim3(1), 0, s, limit_ns, status);
+}
 
 cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, void* xq, cudaStream_t s) {
     const int bs = act_fmt == CQ_Q8_K ? 256 : 32;

@@ -229,6 +229,16 @@ cq_status cq_read_global_status(int32_t* out_code, int clear);
 const char* cq_status_string(cq_status s);
 
 /*
+ * Self-test of the bounded waits (no counterpart on the pages): launches one
+ * thread that waits, with a limit of limit_ns (1e3 .. 1e9 ns), on an mbarrier
+ * phase that nothing completes -- as a kernel whose copy never lands would --
+ * then reads and clears the library status word like cq_read_global_status.
+ * Expected result: CQ_ERR_TIMEOUT with CQ_DEV_WAIT_TIMEOUT in *out_code, and
+ * a device that keeps working. Synchronises the current device.
+ */
+cq_status cq_selftest_wait_timeout(int64_t limit_ns, int32_t* out_code, void* stream);
+
+/*
  * Library-wide options (process-wide, all devices; set them before the calls
  * they should affect, not while calls are being issued from other threads).
  *

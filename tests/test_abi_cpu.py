@@ -92,6 +92,11 @@ def test_gemv_x_validation(L):
     assert f(cq.Q8_0, 0, 8, 256, None, None, None, None) == cq.OK
 
 
+def test_selftest_validation(L):
+    assert cq.cq_selftest_wait_timeout(10)[0] == cq.ERR_INVALID_ARG
+    assert cq.cq_selftest_wait_timeout(2_000_000_000)[0] == cq.ERR_INVALID_ARG
+
+
 def test_set_option(L):
     assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 1) == cq.OK
     assert cq.cq_set_option(cq.OPT_WEIGHTS_CONST, 0) == cq.OK

@@ -209,3 +209,18 @@ def test_gemv_x_quantize_only():
     assert cq.cq_gemv_x(cq.Q4_0, 2, 0, 1024, None, x.data_ptr(), xq.data_ptr(), None,
                         torch.cuda.current_stream().cuda_stream) == cq.OK
     assert torch.equal(xq, cq.quantize_act_t(x, cq.Q8_0))
+
+
+def test_bounded_wait_times_out_and_device_keeps_working(orc):
+    """The bounded wait every kernel uses gives up after its limit and reports
+    CQ_DEV_WAIT_TIMEOUT (no fault, no hang); a GEMV afterwards is still right."""
+    torch = torch_cuda()
+    cq = cq_built()
+    st, code = cq.cq_selftest_wait_timeout(50_000_000)          # 50 ms
+    assert st == cq.ERR_TIMEOUT and code & cq.DEV_WAIT_TIMEOUT
+    st, code = cq.cq_read_global_status(clear=0)
+    assert st == cq.OK and code == 0                            # the self-test cleared it
+    W, xq = _case(orc, 8, 100, 512, 1, seed=9)
+    y = cq.gemv_t(dev(torch, W), dev(torch, xq), 8, 512).cpu().numpy()
+    y_ref, at = orc.matmul(8, W, xq, 512)
+    assert_within(y, y_ref, at, what="after timeout")
