@@ -54,7 +54,8 @@ def _peaks():
 
 def _traffic(kernel_file: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on the
-    current source of the kernel (the summary records a hash of the sources)."""
+    current source of the kernels it covers (the summary records a hash of the
+    decode step's sources: the quantiser, the GEMV and their headers)."""
     path = os.path.join(ROOT, "profiles", kernel_file)
     if not os.path.exists(path):
         return None
@@ -62,8 +63,8 @@ def _traffic(kernel_file: str):
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256 ([0-9a-f]+)\)", text)
     if not m:
         return None
-    from gemm_gguf_block_gb300.build import source_hash
-    return float(m.group(1)) if source_hash() == m.group(2) else None
+    from gemm_gguf_block_gb300.build import GEMV_STEP_SOURCES, source_hash
+    return float(m.group(1)) if source_hash(GEMV_STEP_SOURCES) == m.group(2) else None
 
 
 # --------------------------------------------------------------------- clocks

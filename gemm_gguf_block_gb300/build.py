@@ -37,13 +37,19 @@ def _headers():
         glob.glob(os.path.join(ROOT, "include", "*.h"))
 
 
-def source_hash() -> str:
-    """sha256 over the CUDA sources and headers (identifies the kernels a profile was taken on)."""
+# The sources the decode GEMV step (activation quantiser + GEMV) is built from.
+GEMV_STEP_SOURCES = ("gemv.cu", "quantize.cu", "cq_device.cuh", "cq_internal.h", "cq.h")
+
+
+def source_hash(names=None) -> str:
+    """sha256 over CUDA sources and headers (identifies the kernels a profile was
+    taken on): all of them, or only the named files."""
     import hashlib
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(f).encode())
+        base = os.path.basename(f)
+        if f.endswith((".cu", ".cuh", ".h")) and (names is None or base in names):
+            h.update(base.encode())
             h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
