@@ -224,3 +224,17 @@ def test_bounded_wait_times_out_and_device_keeps_working(orc):
     y = cq.gemv_t(dev(torch, W), dev(torch, xq), 8, 512).cpu().numpy()
     y_ref, at = orc.matmul(8, W, xq, 512)
     assert_within(y, y_ref, at, what="after timeout")
+
+
+@pytest.mark.parametrize("wfmt", FMTS)
+def test_gemv_largest_k(orc, wfmt):
+    """K at the library's limit (65536): rows split into many segments."""
+    torch = torch_cuda()
+    cq = cq_built()
+    N, K = 20, 65536
+    W, xq = _case(orc, wfmt, N, K, 2, seed=17)
+    y = cq.gemv_t(dev(torch, W), dev(torch, xq), wfmt, K).cpu().numpy()
+    y_ref, at = orc.matmul(wfmt, W, xq, K)
+    assert_within(y, y_ref, at, what=f"K={K}")
+    y1 = cq.gemv_t(dev(torch, W), dev(torch, xq[1:2]), wfmt, K).cpu().numpy()[0]
+    assert np.array_equal(y[1].view(np.uint32), y1.view(np.uint32))

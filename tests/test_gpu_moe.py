@@ -136,6 +136,36 @@ def test_moe_small(orc):
     _check(c, 512, 768)
 
 
+def test_moe_many_pairs_per_expert(orc):
+    """More routed pairs per expert than one pass of the grouped kernels takes
+    (64): 192 tokens, 4 experts, top-2 -> ~96 pairs per expert, two passes;
+    also an expert with no pairs at all (5 experts, ids drawn from 4)."""
+    torch = torch_cuda()
+    cq = cq_built()
+    T, E, topk, K, F = 192, 5, 2, 512, 512
+    rng = np.random.default_rng(21)
+    Wg = np.stack([synth.gen_q4_0(rng, F, K) for _ in range(E)])
+    Wu = np.stack([synth.gen_q4_0(rng, F, K) for _ in range(E)])
+    Wd = np.stack([synth.gen_q4_0(rng, K, F) for _ in range(E)])
+    ids = np.stack([rng.permutation(4)[:topk] for _ in range(T)]).astype(np.int32)   # expert 4 unused
+    rw = rng.random((T, topk)).astype(np.float32)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    xq = orc.quantize(orc.Q8_0, x)
+    y, ws = cq.moe_t(dev(torch, Wg), dev(torch, Wu), dev(torch, Wd), dev(torch, ids), dev(torch, rw),
+                     dev(torch, xq), K, F)
+    st, code = cq.cq_moe_read_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == cq.OK and code == 0
+    assert np.bincount(ids.ravel(), minlength=E).max() > 64
+    st, so, ho, qo = cq.cq_moe_workspace_offsets(T, K, F, E, topk)
+    wsn = ws.cpu().numpy()
+    P = T * topk
+    c = dict(Wd=Wd, ids=ids, rw=rw, y=y.cpu().numpy(),
+             h=wsn[ho:ho + 4 * P * F].view(np.float32).reshape(T, topk, F),
+             hq=wsn[qo:qo + P * (F // 32) * 34].reshape(T, topk, -1),
+             r=orc.moe(Wg, Wu, Wd, ids, rw, xq, K, F))
+    _check(c, K, F)
+
+
 def test_moe_config_sampled(orc):
     """The routed-FFN workload (256 tokens, 32 experts, top-4, 2048/1792, Q4_0):
     the GPU runs the whole batch; the oracle checks a sample of 12 tokens."""
