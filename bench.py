@@ -405,7 +405,7 @@ def run_cq(args, rank, world, local_rank):
         N, K = W.shape[0], x.shape[1]
         xh_all[ko:ko + K].copy_(torch.from_numpy(x[0]))
         layers.append(dict(
-            N=N, K=K, W=torch.from_numpy(W).cuda(), x=x_all[ko:ko + K],
+            N=N, K=K, ko=ko, no=no, W=torch.from_numpy(W).cuda(), x=x_all[ko:ko + K],
             xq=torch.empty(cq.row_bytes(cq.Q8_0, K), dtype=torch.uint8, device="cuda"),
             y=y_all[no:no + N], bytes=W.nbytes + cq.row_bytes(cq.Q8_0, K) + 4 * N))
         ko += K
@@ -549,7 +549,65 @@ def run_cq(args, rank, world, local_rank):
         g_e2e.replay()
     b.record(stream)
     b.synchronize()
-    e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / (reps * U))
+    e2e_seq_ms = max_over_ranks(dist, a.elapsed_time(b) / (reps * U))
+
+    # Pipelined, as a serving loop would run it: two sets of activation and
+    # output buffers, the copies on a side stream, so that step i+1's inputs
+    # come in and step i's outputs go out while the neighbouring step's kernels
+    # run. Every step still copies its own inputs in and its outputs back.
+    xb = [x_all, torch.empty_like(x_all)]
+    yb = [y_all, torch.empty_like(y_all)]
+    xhb = [xh_all, xh_all.clone().pin_memory()]
+    yhb = [yh_all, torch.empty_like(yh_all).pin_memory()]
+
+    def kernels(bi, stream_handle):
+        for L in layers:
+            xv = xb[bi][L["ko"]:L["ko"] + L["K"]]
+            yv = yb[bi][L["no"]:L["no"] + L["N"]]
+            cq.cq_quantize_act(cq.Q8_0, 1, L["K"], xv.data_ptr(), L["xq"].data_ptr(), stream_handle)
+            cq.cq_gemv(cq.Q8_0, 1, L["N"], L["K"], L["W"].data_ptr(), L["xq"].data_ptr(), yv.data_ptr(),
+                       stream_handle)
+
+    UP_ = 2 * U
+    side = torch.cuda.Stream()
+    g_pipe = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pipe):
+        cs = torch.cuda.current_stream()
+        side.wait_stream(cs)
+        xr = [torch.cuda.Event() for _ in range(UP_)]
+        done = [torch.cuda.Event() for _ in range(UP_)]
+        yfree = [torch.cuda.Event() for _ in range(UP_)]
+        with torch.cuda.stream(side):
+            xb[0].copy_(xhb[0], non_blocking=True)
+            xr[0].record(side)
+        for i in range(UP_):
+            bi = i % 2
+            cs.wait_event(xr[i])
+            if i >= 2:
+                cs.wait_event(yfree[i - 2])          # step i-2's outputs have left y[bi]
+            kernels(bi, cs.cuda_stream)
+            done[i].record(cs)
+            with torch.cuda.stream(side):
+                if i + 1 < UP_:
+                    if i >= 1:
+                        side.wait_event(done[i - 1])  # step i-1 has read x[(i+1) % 2]
+                    xb[(i + 1) % 2].copy_(xhb[(i + 1) % 2], non_blocking=True)
+                    xr[i + 1].record(side)
+                side.wait_event(done[i])
+                yhb[bi].copy_(yb[bi], non_blocking=True)
+                yfree[i].record(side)
+        cs.wait_stream(side)
+    for _ in range(3):
+        g_pipe.replay()
+    torch.cuda.synchronize()
+    reps_p = max(1, args.steps // UP_)
+    a.record(stream)
+    for _ in range(reps_p):
+        g_pipe.replay()
+    b.record(stream)
+    b.synchronize()
+    e2e_ms = max_over_ranks(dist, a.elapsed_time(b) / (reps_p * UP_))
+    same_out = bool(torch.equal(yhb[0], yhb[1]))
 
     sec = {}
     cpu = None
@@ -582,7 +640,13 @@ def run_cq(args, rank, world, local_rank):
         "per_shape": per_shape,
         "cpu_baseline": cpu,
         "e2e": {"value": aggregate_gbs(world, wbytes, e2e_ms), "unit": "GB/s",
-                "timing": f"CUDA graph of {U} steps (H2D copies, calls, D2H copies) replayed {reps}x",
+                "timing": (f"CUDA graph of {UP_} pipelined steps replayed {reps_p}x: per step one H2D copy of the "
+                           f"activations, the quantise + GEMV calls, one D2H copy of the outputs; the copies run on "
+                           f"a side stream into double buffers, overlapping the neighbouring steps' kernels"),
+                "outputs_equal_across_buffers": same_out,
+                "sequential": {"value": aggregate_gbs(world, wbytes, e2e_seq_ms), "unit": "GB/s",
+                               "ms_per_step": e2e_seq_ms,
+                               "timing": f"CUDA graph of {U} steps, copies and kernels in one stream"},
                 "stream_launched": {"value": aggregate_gbs(world, wbytes, e2e_stream_ms), "unit": "GB/s",
                                     "ms_per_step": e2e_stream_ms},
                 "h2d_bytes_per_step": 4 * k_tot, "d2h_bytes_per_step": 4 * n_tot,
