@@ -12,16 +12,15 @@
 // Pipeline (all asynchronous on the caller's stream, no host round trip):
 //   1. route:   validate ids (range, no repeats within a token), counting-sort
 //               the (token, slot) pairs by expert; stable, so deterministic.
-//   2. up:      per (expert, 32-row tile of F): gate and up tiles land in
-//               shared memory by bulk copy; the expert's tokens stream past
-//               them eight at a time; h = silu(g) * u, then Q8_0 of h.
-//   3. down:    per (expert, 32-row tile of K): o = W_down . hq per pair.
+//   2. up:      per (expert, 128 rows of F), on the tensor cores
+//               (moe_mma.cu): gate and up for the expert's pairs, h =
+//               silu(g) * u, then Q8_0 of h.
+//   3. down:    per (expert, 128 rows of K), on the tensor cores: o = W_down . hq.
 //   4. combine: y[t] = sum over slots in slot order of w * o (fma chain).
 #include <algorithm>
 #include <cstdlib>
 #include <mutex>
 
-#include "chunk_dot.cuh"
 #include "cq_device.cuh"
 #include "cq_internal.h"
 
@@ -44,10 +43,6 @@ MoeLayout moe_layout(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk) {
 }
 
 namespace {
-
-constexpr int TILE = 32;      // weight rows per CTA tile
-constexpr int TOKG = 8;       // tokens per pass over a tile
-constexpr int THREADS = 256;
 
 struct MoeParams {
     const uint8_t* Wg;
@@ -131,174 +126,6 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
     }
 }
 
-// Copy `n` 34-byte-block rows (token rows of Q8_0) into shared memory, row i
-// from src_row(i), `words` 32-bit words each, destination pitch `pitch`.
-template <class RowFn>
-__device__ __forceinline__ void stage_rows(uint8_t* dst, int pitch, int n, int words, RowFn src_row) {
-    const int total = n * words;
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-        const int r = i / words, w = i - r * words;
-        reinterpret_cast<uint32_t*>(dst + r * pitch)[w] = reinterpret_cast<const uint32_t*>(src_row(r))[w];
-    }
-}
-
-// Wait (all threads) for the weight tile; on timeout flag it, give the copy a
-// second bounded wait to land (so none is in flight when the CTA exits) and
-// report false.
-__device__ __forceinline__ bool wait_tile(uint64_t* bar, int* status) {
-    const bool ok = mbar_wait_bounded(bar, 0, WAIT_LIMIT_NS);
-    if (__syncthreads_and(ok)) return true;
-    if (threadIdx.x == 0) {
-        atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
-        (void)mbar_wait_bounded(bar, 0, WAIT_LIMIT_NS / 8);
-    }
-    __syncthreads();
-    return false;
-}
-
-// ------------------------------------------------------------- gate/up + SwiGLU
-__global__ void __launch_bounds__(THREADS) moe_up_kernel(const MoeParams p) {
-    pdl_trigger();
-    pdl_wait();
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int e = blockIdx.y, f0 = blockIdx.x * TILE;
-    const int* offs = ws_offs(p);
-    const int beg = offs[e], cnt = offs[e + 1] - beg;
-    if (cnt == 0) return;
-    const int nc = p.K / CHUNK_ELEMS;
-    const int rowb = nc * WCHUNK_Q4_0;                 // bytes of one weight row
-    const int tok_pitch = nc * ACHUNK_Q8_0;            // one Q8_0 token row
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    uint8_t* wt = smem + 128;                          // [2*TILE rows][rowb]: gate rows, then up rows
-    uint8_t* xs = wt + (2 * TILE * rowb + 127) / 128 * 128;
-    float* cbuf = reinterpret_cast<float*>(xs + (TOKG * tok_pitch + 127) / 128 * 128);   // [TOKG][2*TILE][nc]
-    float* gu = cbuf + TOKG * 2 * TILE * nc;                                              // [TOKG][2*TILE]
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        const uint32_t half = static_cast<uint32_t>(TILE * rowb);
-        mbar_arrive_expect_tx(bar, 2 * half);
-        const size_t mat = static_cast<size_t>(p.F) * rowb;
-        const uint64_t pol = policy_evict_first();
-        bulk_g2s(wt, p.Wg + e * mat + static_cast<size_t>(f0) * rowb, half, bar, pol);
-        bulk_g2s(wt + half, p.Wu + e * mat + static_cast<size_t>(f0) * rowb, half, bar, pol);
-    }
-    __syncthreads();
-    const int* perm = ws_perm(p) + beg;
-    bool have_tile = false;
-    float* hbase = reinterpret_cast<float*>(p.ws + p.L.h);
-    uint8_t* hqbase = p.ws + p.L.hq;
-    const int hq_row = p.F / 32 * 34;
-    for (int g0 = 0; g0 < cnt; g0 += TOKG) {
-        const int gm = min(TOKG, cnt - g0);
-        stage_rows(xs, tok_pitch, gm, tok_pitch / 4,
-                   [&](int r) { return p.xq + static_cast<size_t>(perm[g0 + r] / p.topk) * tok_pitch; });
-        if (!have_tile) {
-            if (!wait_tile(bar, ws_status(p))) return;
-            have_tile = true;
-        } else {
-            __syncthreads();
-        }
-        const int ntasks = 2 * TILE * nc;
-        for (int t = threadIdx.x; t < ntasks; t += blockDim.x) {
-            const int r = t / nc, j = t - r * nc;
-            float c[TOKG];
-            chunk_dot<CQ_Q4_0, TOKG>(wt + r * rowb + j * WCHUNK_Q4_0, xs + j * ACHUNK_Q8_0, tok_pitch, gm, c);
-#pragma unroll
-            for (int m = 0; m < TOKG; ++m)
-                if (m < gm) cbuf[(m * 2 * TILE + r) * nc + j] = c[m];
-        }
-        __syncthreads();
-        for (int q = threadIdx.x; q < gm * 2 * TILE; q += blockDim.x) {
-            const float* cb = cbuf + q * nc;
-            float acc = 0.0f;
-            for (int j = 0; j < nc; ++j) acc = __fadd_rn(acc, cb[j]);
-            gu[q] = acc;
-        }
-        __syncthreads();
-        // One warp per token: lane f of the 32-row tile; h = silu(g) * u, then
-        // the Q8_0 block of these 32 values (the cq_quantize_act rule).
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        if (warp < gm) {
-            const int pair = perm[g0 + warp];
-            const float g = gu[warp * 2 * TILE + lane];
-            const float u = gu[warp * 2 * TILE + TILE + lane];
-            const float silu = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-            const float h = __fmul_rn(silu, u);
-            hbase[static_cast<size_t>(pair) * p.F + f0 + lane] = h;
-            float amax = fabsf(h);
-#pragma unroll
-            for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float d = q8_scale(amax);
-            const float id = q8_inv(d);
-            uint8_t* blk = hqbase + static_cast<size_t>(pair) * hq_row + (f0 / 32) * 34;
-            blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(quant_q8(h, id)));
-            if (lane == 0) *reinterpret_cast<__half*>(blk) = __float2half_rn(d);
-        }
-        __syncthreads();
-    }
-}
-
-// ------------------------------------------------------------------- down
-__global__ void __launch_bounds__(THREADS) moe_down_kernel(const MoeParams p) {
-    pdl_trigger();
-    pdl_wait();
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int e = blockIdx.y, k0 = blockIdx.x * TILE;
-    const int* offs = ws_offs(p);
-    const int beg = offs[e], cnt = offs[e + 1] - beg;
-    if (cnt == 0) return;
-    const int nc = p.F / CHUNK_ELEMS;
-    const int rowb = nc * WCHUNK_Q4_0;
-    const int tok_pitch = nc * ACHUNK_Q8_0;            // one hq row
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    uint8_t* wt = smem + 128;
-    uint8_t* xs = wt + (TILE * rowb + 127) / 128 * 128;
-    float* cbuf = reinterpret_cast<float*>(xs + (TOKG * tok_pitch + 127) / 128 * 128);   // [TOKG][TILE][nc]
-    if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        const uint32_t bytes = static_cast<uint32_t>(TILE * rowb);
-        mbar_arrive_expect_tx(bar, bytes);
-        const size_t mat = static_cast<size_t>(p.K) * rowb;
-        bulk_g2s(wt, p.Wd + e * mat + static_cast<size_t>(k0) * rowb, bytes, bar, policy_evict_first());
-    }
-    __syncthreads();
-    const int* perm = ws_perm(p) + beg;
-    const uint8_t* hq = p.ws + p.L.hq;
-    float* out = reinterpret_cast<float*>(p.ws + p.L.out);
-    bool have_tile = false;
-    for (int g0 = 0; g0 < cnt; g0 += TOKG) {
-        const int gm = min(TOKG, cnt - g0);
-        stage_rows(xs, tok_pitch, gm, tok_pitch / 4,
-                   [&](int r) { return hq + static_cast<size_t>(perm[g0 + r]) * tok_pitch; });
-        if (!have_tile) {
-            if (!wait_tile(bar, ws_status(p))) return;
-            have_tile = true;
-        } else {
-            __syncthreads();
-        }
-        const int ntasks = TILE * nc;
-        for (int t = threadIdx.x; t < ntasks; t += blockDim.x) {
-            const int r = t / nc, j = t - r * nc;
-            float c[TOKG];
-            chunk_dot<CQ_Q4_0, TOKG>(wt + r * rowb + j * WCHUNK_Q4_0, xs + j * ACHUNK_Q8_0, tok_pitch, gm, c);
-#pragma unroll
-            for (int m = 0; m < TOKG; ++m)
-                if (m < gm) cbuf[(m * TILE + r) * nc + j] = c[m];
-        }
-        __syncthreads();
-        for (int q = threadIdx.x; q < gm * TILE; q += blockDim.x) {
-            const int m = q / TILE, r = q - m * TILE;
-            const float* cb = cbuf + q * nc;
-            float acc = 0.0f;
-            for (int j = 0; j < nc; ++j) acc = __fadd_rn(acc, cb[j]);
-            out[static_cast<size_t>(perm[g0 + m]) * p.K + k0 + r] = acc;
-        }
-        __syncthreads();
-    }
-}
-
 // ---------------------------------------------------------------- combine
 // y[t] = sum over the token's valid slots s, in increasing s, of rw * o; one
 // CTA row per token, four consecutive outputs per thread.
@@ -326,27 +153,6 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const MoeParams p) {
 
 }  // namespace
 
-// CQ_MOE_MMA=0 runs the dp4a projections instead of the tensor-core ones (A/B runs).
-bool moe_mma_enabled() {
-    static const bool v = [] {
-        const char* e = std::getenv("CQ_MOE_MMA");
-        return !(e && e[0] == '0');
-    }();
-    return v;
-}
-
-size_t moe_up_smem(int K) {
-    const int nc = K / CHUNK_ELEMS;
-    const int rowb = nc * WCHUNK_Q4_0, tok_pitch = nc * ACHUNK_Q8_0;
-    return 128 + (2 * TILE * rowb + 127) / 128 * 128 + (TOKG * tok_pitch + 127) / 128 * 128 +
-           4 * (TOKG * 2 * TILE * nc + TOKG * 2 * TILE);
-}
-size_t moe_down_smem(int F) {
-    const int nc = F / CHUNK_ELEMS;
-    const int rowb = nc * WCHUNK_Q4_0, tok_pitch = nc * ACHUNK_Q8_0;
-    return 128 + (TILE * rowb + 127) / 128 * 128 + (TOKG * tok_pitch + 127) / 128 * 128 + 4 * (TOKG * TILE * nc);
-}
-
 cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
                        const void* Wu, const void* Wd, const int32_t* ids, const float* rw, const void* xq,
                        float* y, void* ws, cudaStream_t s) {
@@ -363,33 +169,10 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
     p.T = T; p.K = K; p.F = F; p.E = E; p.topk = topk;
     cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(1024), 0, s, p);
     if (e != cudaSuccess) return e;
-    if (moe_mma_enabled()) {
-        e = launch_moe_projections(dev, T, K, F, E, topk, Wg, Wu, Wd, xq, reinterpret_cast<const int*>(p.ws + p.L.offs),
-                                   reinterpret_cast<const int*>(p.ws + p.L.perm), reinterpret_cast<float*>(p.ws + p.L.h),
-                                   p.ws + p.L.hq, reinterpret_cast<float*>(p.ws + p.L.out), s);
-        if (e != cudaSuccess) return e;
-    } else {
-        const int smem_up = static_cast<int>(moe_up_smem(K));
-        const int smem_dn = static_cast<int>(moe_down_smem(F));
-        const int lim = std::min(dev.smem_optin, 227 * 1024);
-        if (smem_up > lim || smem_dn > lim) return cudaErrorInvalidConfiguration;
-        static int raised[64] = {};
-        int devid = 0;
-        if ((e = cudaGetDevice(&devid)) != cudaSuccess) return e;
-        if (devid >= 64 || !raised[devid]) {
-            if ((e = cudaFuncSetAttribute(moe_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
-                cudaSuccess)
-                return e;
-            if ((e = cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lim)) !=
-                cudaSuccess)
-                return e;
-            if (devid < 64) raised[devid] = 1;
-        }
-        if ((e = launch_kernel(moe_up_kernel, dim3(F / TILE, E), dim3(THREADS), smem_up, s, p)) != cudaSuccess)
-            return e;
-        if ((e = launch_kernel(moe_down_kernel, dim3(K / TILE, E), dim3(THREADS), smem_dn, s, p)) != cudaSuccess)
-            return e;
-    }
+    e = launch_moe_projections(dev, T, K, F, E, topk, Wg, Wu, Wd, xq, reinterpret_cast<const int*>(p.ws + p.L.offs),
+                               reinterpret_cast<const int*>(p.ws + p.L.perm), reinterpret_cast<float*>(p.ws + p.L.h),
+                               p.ws + p.L.hq, reinterpret_cast<float*>(p.ws + p.L.out), s);
+    if (e != cudaSuccess) return e;
     return launch_kernel(moe_combine_kernel, dim3(static_cast<unsigned>(T), static_cast<unsigned>((K / 4 + 255) / 256)),
                          dim3(256), 0, s, p);
 }
