@@ -71,6 +71,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
 struct MoeLayout {
     size_t status;   // int32 status word (CQ_DEV_* bits)
     size_t offs;     // int32 [E+1]: start of each expert's pair list in perm
+    size_t order;    // int32 [E]: experts by decreasing pair count (ties by id)
     size_t perm;     // int32 [T*topk]: pair indices (t*topk + s) grouped by expert
     size_t valid;    // int32 [T*topk]: 1 if the pair's expert id was accepted
     size_t h;        // fp32 [T*topk][F]: hidden activations, (token, slot) order
@@ -81,10 +82,11 @@ struct MoeLayout {
 MoeLayout moe_layout(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk);
 
 // Grouped tensor-core projections of the routed FFN: gate/up + SwiGLU into h,
-// Q8_0 of h into hq, down into o (all in the caller's workspace).
+// Q8_0 of h into hq, down into o (all in the caller's workspace). CTAs take
+// the experts in `order` (largest first).
 cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
-                                   const void* Wu, const void* Wd, const void* xq, const int* offs, const int* perm,
-                                   float* h, const void* hq, float* o, cudaStream_t s);
+                                   const void* Wu, const void* Wd, const void* xq, const int* offs, const int* order,
+                                   const int* perm, float* h, const void* hq, float* o, cudaStream_t s);
 
 cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
                        const void* Wu, const void* Wd, const int32_t* ids, const float* rw, const void* xq,

@@ -33,6 +33,7 @@ MoeLayout moe_layout(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk) {
     size_t o = 0;
     L.status = o; o += 256;
     L.offs = o; o = up(o + 4 * static_cast<size_t>(E + 1));
+    L.order = o; o = up(o + 4 * static_cast<size_t>(E));
     L.perm = o; o = up(o + 4 * P);
     L.valid = o; o = up(o + 4 * P);
     L.h = o; o = up(o + 4 * P * static_cast<size_t>(F));
@@ -114,6 +115,16 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const MoeParams p) {
     int* offs = ws_offs(p);
     int* perm = ws_perm(p);
     for (int e = tid; e <= p.E; e += blockDim.x) offs[e] = off[e];
+    // Experts by decreasing pair count (ties by id): the projection CTAs take
+    // them in this order, so the largest start first and the small ones fill
+    // the last wave.
+    int* order = reinterpret_cast<int*>(p.ws + p.L.order);
+    for (int e = tid; e < p.E; e += blockDim.x) {
+        const int c = cnt[e];
+        int rank = 0;
+        for (int e2 = 0; e2 < p.E; ++e2) rank += (cnt[e2] > c) || (cnt[e2] == c && e2 < e);
+        order[rank] = e;
+    }
     for (int e = warp; e < p.E; e += nwarps) {
         int pos = off[e];
         for (int base = 0; base < P; base += 32) {
@@ -170,6 +181,7 @@ cudaError_t launch_moe(const DeviceInfo& dev, int T, int K, int F, int E, int to
     cudaError_t e = launch_kernel(moe_route_kernel, dim3(1), dim3(1024), 0, s, p);
     if (e != cudaSuccess) return e;
     e = launch_moe_projections(dev, T, K, F, E, topk, Wg, Wu, Wd, xq, reinterpret_cast<const int*>(p.ws + p.L.offs),
+                               reinterpret_cast<const int*>(p.ws + p.L.order),
                                reinterpret_cast<const int*>(p.ws + p.L.perm), reinterpret_cast<float*>(p.ws + p.L.h),
                                p.ws + p.L.hq, reinterpret_cast<float*>(p.ws + p.L.out), s);
     if (e != cudaSuccess) return e;

@@ -53,6 +53,7 @@ constexpr int RAWA_BYTES = TOK * RAWA;              // 17408
 struct MoeMmaParams {
     const uint8_t* xq;          // up: token activations (Q8_0 [T][K]); down: hq rows (Q8_0 [P][F])
     const int* offs;            // [E+1]
+    const int* order;           // [E] experts, largest first
     const int* perm;            // pairs grouped by expert
     float* out;                 // up: h [P][F]; down: o [P][Kout]
     uint8_t* hq;                // up: Q8_0 of h, [P] rows of F/32 blocks
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
     sm.dx = reinterpret_cast<float2*>(sm.act + ACT_BYTES + BQ_BYTES);
     sm.wst = smem + 1024 + ACT_BYTES + SCL_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.y, r0 = blockIdx.x * ROWS;
+    const int e = p.order[blockIdx.y], r0 = blockIdx.x * ROWS;
     const int beg = p.offs[e], cnt = p.offs[e + 1] - beg;
     if (cnt == 0) return;
     const int nseg = p.kin / 256;
@@ -442,8 +443,8 @@ cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUten
 }  // namespace
 
 cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, int E, int topk, const void* Wg,
-                                   const void* Wu, const void* Wd, const void* xq, const int* offs, const int* perm,
-                                   float* h, const void* hq, float* o, cudaStream_t s) {
+                                   const void* Wu, const void* Wd, const void* xq, const int* offs, const int* order,
+                                   const int* perm, float* h, const void* hq, float* o, cudaStream_t s) {
     CUtensorMap mg, mu, md;
     if (!make_map(&mg, Wg, static_cast<int64_t>(E) * F, K) || !make_map(&mu, Wu, static_cast<int64_t>(E) * F, K) ||
         !make_map(&md, Wd, static_cast<int64_t>(E) * K, F))
@@ -451,6 +452,7 @@ cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, i
     MoeMmaParams up{};
     up.xq = static_cast<const uint8_t*>(xq);
     up.offs = offs;
+    up.order = order;
     up.perm = perm;
     up.out = h;
     up.hq = static_cast<uint8_t*>(const_cast<void*>(hq));
