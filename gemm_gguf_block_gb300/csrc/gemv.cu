@@ -13,7 +13,7 @@
 // is shorter than 32 chunks, else a 32-chunk segment of one row. An item is
 // one contiguous byte range, so a single bulk copy (cp.async.bulk, the
 // one-dimensional TMA engine) lands it in the warp's ring of shared-memory
-// stages; the copy of item i+S is issued as soon as item i has been read.
+// stages; the copy of item i+S is issued as soon as item i is in registers.
 // Lane l takes chunk l of the item: it unpacks its weights in registers and
 // forms exact int32 block dots with dp4a against the activations, which the
 // CTA has staged once in shared memory in an aligned split layout (quants on
@@ -50,6 +50,7 @@ struct GemvParams {
     int64_t row_bytes;
     int M;
     int nc;           // chunks per row
+    int cpitch;       // floats per row in the chunk-value buffer (odd where it fits: no bank conflicts)
     int R;            // rows per item
     int segc;         // chunks per item
     int nseg;         // items per row group (R == 1 whenever nseg > 1)
@@ -62,6 +63,7 @@ struct GemvParams {
     int wconst;       // weights constant in flight: prefetch them before the dependency wait
     const float* x;   // fp32 activations to quantize in the kernel (cq_gemv_x), else null
     uint8_t* xq_out;  // where CTA 0 writes their quantisation (with x)
+    int xreg;         // one token, whole rows per item: the lane's chunk of x held in registers
 };
 
 // Exact float of an int with |i| < 2^22: the bits of 1.5 * 2^23 + i, minus 1.5 * 2^23.
@@ -80,6 +82,10 @@ __device__ __forceinline__ void lds64(const uint8_t* p, uint32_t (&u)[2 * N]) {
     }
 }
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void ld_f4(const uint8_t* p, float* f) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
 
 // ------------------------------------------------------- staging of activations
 // Q8_0 / Q8_1 chunk of 4 blocks -> [qs 128 B][d0..d3 fp32] (Q8_1: [d,s] pairs);
@@ -244,13 +250,55 @@ __device__ void stage_activations_x(const GemvParams& p, uint8_t* act) {
 }
 
 // ------------------------------------------------------------- chunk values
-// wc: weight chunk in shared memory (8-byte aligned; 16 for Q4_K);
-// xa: staged activations of the same chunk for token 0, token m at + m * tp.
+// w: weight chunk in registers. x: the staged activations of the same chunk,
+// read through an activation source: q(m, i) is the 16-byte piece i of token
+// m's 128 quants, d(m, b) / s(m, b) block b's scale / Q8_1 sum.
 
-template <int MT>
-__device__ __forceinline__ void chunk_q8_0(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
-    uint32_t w[34];
-    lds64<17>(wc, w);
+// Activations read from shared memory: token m at xa + m * tp.
+template <bool PAIRS>
+struct SmemX {
+    const uint8_t* xa;
+    int tp;
+    __device__ __forceinline__ uint4 q(int m, int i) const { return lds128(xa + m * tp + 16 * i); }
+    __device__ __forceinline__ float d(int m, int b) const {
+        return reinterpret_cast<const float*>(xa + m * tp + 128)[PAIRS ? 2 * b : b];
+    }
+    __device__ __forceinline__ float s(int m, int b) const {
+        return reinterpret_cast<const float*>(xa + m * tp + 128)[2 * b + 1];
+    }
+};
+
+// One token's activation chunk held in registers: when every item of a warp
+// uses the same chunk of x (rows no longer than 32 chunks), it is read once.
+template <bool PAIRS>
+struct RegX {
+    uint4 qv[8];
+    float sc[PAIRS ? 8 : 4];
+    __device__ __forceinline__ void load(const uint8_t* a) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qv[i] = lds128(a + 16 * i);
+        ld_f4(a + 128, sc);
+        if constexpr (PAIRS) ld_f4(a + 144, sc + 4);
+    }
+    __device__ __forceinline__ uint4 q(int, int i) const { return qv[i]; }
+    __device__ __forceinline__ float d(int, int b) const { return sc[PAIRS ? 2 * b : b]; }
+    __device__ __forceinline__ float s(int, int b) const { return sc[2 * b + 1]; }
+};
+
+// Block dot of 32 signed bytes (as eight words) with an activation block.
+__device__ __forceinline__ int dot32(const int (&q)[8], const uint4& a0, const uint4& a1) {
+    int s = __dp4a(q[0], static_cast<int>(a0.x), 0);
+    s = __dp4a(q[1], static_cast<int>(a0.y), s);
+    s = __dp4a(q[2], static_cast<int>(a0.z), s);
+    s = __dp4a(q[3], static_cast<int>(a0.w), s);
+    s = __dp4a(q[4], static_cast<int>(a1.x), s);
+    s = __dp4a(q[5], static_cast<int>(a1.y), s);
+    s = __dp4a(q[6], static_cast<int>(a1.z), s);
+    return __dp4a(q[7], static_cast<int>(a1.w), s);
+}
+
+template <int MT, class X>
+__device__ __forceinline__ void chunk_q8_0(const uint32_t (&w)[34], const X& x, int M, float (&c)[MT]) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) c[m] = 0.0f;
 #pragma unroll
@@ -266,27 +314,15 @@ __device__ __forceinline__ void chunk_q8_0(const uint8_t* wc, const uint8_t* xa,
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
-                const uint8_t* xm = xa + m * tp;
-                const uint4 a0 = lds128(xm + 32 * b), a1 = lds128(xm + 32 * b + 16);
-                const float dx = reinterpret_cast<const float*>(xm + 128)[b];
-                int s = __dp4a(q[0], static_cast<int>(a0.x), 0);
-                s = __dp4a(q[1], static_cast<int>(a0.y), s);
-                s = __dp4a(q[2], static_cast<int>(a0.z), s);
-                s = __dp4a(q[3], static_cast<int>(a0.w), s);
-                s = __dp4a(q[4], static_cast<int>(a1.x), s);
-                s = __dp4a(q[5], static_cast<int>(a1.y), s);
-                s = __dp4a(q[6], static_cast<int>(a1.z), s);
-                s = __dp4a(q[7], static_cast<int>(a1.w), s);
-                c[m] = __fmaf_rn(__fmul_rn(dw, dx), i2f_exact(s), c[m]);
+                const int s = dot32(q, x.q(m, 2 * b), x.q(m, 2 * b + 1));
+                c[m] = __fmaf_rn(__fmul_rn(dw, x.d(m, b)), i2f_exact(s), c[m]);
             }
         }
     }
 }
 
-template <int MT>
-__device__ __forceinline__ void chunk_q4_0(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
-    uint32_t w[18];
-    lds64<9>(wc, w);
+template <int MT, class X>
+__device__ __forceinline__ void chunk_q4_0(const uint32_t (&w)[18], const X& x, int M, float (&c)[MT]) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) c[m] = 0.0f;
 #pragma unroll
@@ -295,37 +331,25 @@ __device__ __forceinline__ void chunk_q4_0(const uint8_t* wc, const uint8_t* xa,
         const int base = o >> 2;
         const bool odd = (o & 2) != 0;
         const float dw = h2f(odd ? (w[base] >> 16) : w[base]);
-        int lo[4], hi[4];
+        int q[8];                                // low nibbles (elements 0..15), then high (16..31)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t q = odd ? w[base + 1 + i] : __funnelshift_r(w[base + i], w[base + i + 1], 16);
-            lo[i] = nib_minus8(q & 0x0f0f0f0fu);
-            hi[i] = nib_minus8((q >> 4) & 0x0f0f0f0fu);
+            const uint32_t v = odd ? w[base + 1 + i] : __funnelshift_r(w[base + i], w[base + i + 1], 16);
+            q[i] = nib_minus8(v & 0x0f0f0f0fu);
+            q[4 + i] = nib_minus8((v >> 4) & 0x0f0f0f0fu);
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
-                const uint8_t* xm = xa + m * tp;
-                const uint4 a0 = lds128(xm + 32 * b), a1 = lds128(xm + 32 * b + 16);
-                const float dx = reinterpret_cast<const float*>(xm + 128)[b];
-                int s = __dp4a(lo[0], static_cast<int>(a0.x), 0);
-                s = __dp4a(lo[1], static_cast<int>(a0.y), s);
-                s = __dp4a(lo[2], static_cast<int>(a0.z), s);
-                s = __dp4a(lo[3], static_cast<int>(a0.w), s);
-                s = __dp4a(hi[0], static_cast<int>(a1.x), s);
-                s = __dp4a(hi[1], static_cast<int>(a1.y), s);
-                s = __dp4a(hi[2], static_cast<int>(a1.z), s);
-                s = __dp4a(hi[3], static_cast<int>(a1.w), s);
-                c[m] = __fmaf_rn(__fmul_rn(dw, dx), i2f_exact(s), c[m]);
+                const int s = dot32(q, x.q(m, 2 * b), x.q(m, 2 * b + 1));
+                c[m] = __fmaf_rn(__fmul_rn(dw, x.d(m, b)), i2f_exact(s), c[m]);
             }
         }
     }
 }
 
-template <int MT>
-__device__ __forceinline__ void chunk_q4_1(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
-    uint32_t w[20];
-    lds64<10>(wc, w);
+template <int MT, class X>
+__device__ __forceinline__ void chunk_q4_1(const uint32_t (&w)[20], const X& x, int M, float (&c)[MT]) {
 #pragma unroll
     for (int m = 0; m < MT; ++m) c[m] = 0.0f;
 #pragma unroll
@@ -333,29 +357,19 @@ __device__ __forceinline__ void chunk_q4_1(const uint8_t* wc, const uint8_t* xa,
         const int base = 5 * b;                  // 20-byte blocks: always word aligned
         const float dw = h2f(w[base]);
         const float mw = h2f(w[base] >> 16);
-        int lo[4], hi[4];
+        int q[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t q = w[base + 1 + i];
-            lo[i] = static_cast<int>(q & 0x0f0f0f0fu);
-            hi[i] = static_cast<int>((q >> 4) & 0x0f0f0f0fu);
+            const uint32_t v = w[base + 1 + i];
+            q[i] = static_cast<int>(v & 0x0f0f0f0fu);
+            q[4 + i] = static_cast<int>((v >> 4) & 0x0f0f0f0fu);
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < M) {
-                const uint8_t* xm = xa + m * tp;
-                const uint4 a0 = lds128(xm + 32 * b), a1 = lds128(xm + 32 * b + 16);
-                const float2 ds = reinterpret_cast<const float2*>(xm + 128)[b];
-                int s = __dp4a(lo[0], static_cast<int>(a0.x), 0);
-                s = __dp4a(lo[1], static_cast<int>(a0.y), s);
-                s = __dp4a(lo[2], static_cast<int>(a0.z), s);
-                s = __dp4a(lo[3], static_cast<int>(a0.w), s);
-                s = __dp4a(hi[0], static_cast<int>(a1.x), s);
-                s = __dp4a(hi[1], static_cast<int>(a1.y), s);
-                s = __dp4a(hi[2], static_cast<int>(a1.z), s);
-                s = __dp4a(hi[3], static_cast<int>(a1.w), s);
-                const float cm = __fmaf_rn(__fmul_rn(dw, ds.x), i2f_exact(s), c[m]);
-                c[m] = __fmaf_rn(mw, ds.y, cm);
+                const int s = dot32(q, x.q(m, 2 * b), x.q(m, 2 * b + 1));
+                const float cm = __fmaf_rn(__fmul_rn(dw, x.d(m, b)), i2f_exact(s), c[m]);
+                c[m] = __fmaf_rn(mw, x.s(m, b), cm);
             }
         }
     }
@@ -374,13 +388,7 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
 }
 
 template <int MT>
-__device__ __forceinline__ void chunk_q4_k(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
-    uint32_t w[36];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) {
-        const uint4 v = lds128(wc + 16 * i);
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-    }
+__device__ __forceinline__ void chunk_q4_k(const uint32_t (&w)[36], const uint8_t* xa, int tp, int M, float (&c)[MT]) {
     const float d = h2f(w[0]);
     const float dmin = h2f(w[0] >> 16);
     int isc[MT];
@@ -435,19 +443,41 @@ __device__ __forceinline__ void chunk_q4_k(const uint8_t* wc, const uint8_t* xa,
     }
 }
 
-template <int WF, int MT>
-__device__ __forceinline__ void chunk_value(const uint8_t* wc, const uint8_t* xa, int tp, int M, float (&c)[MT]) {
-    if constexpr (WF == CQ_Q8_0) chunk_q8_0<MT>(wc, xa, tp, M, c);
-    else if constexpr (WF == CQ_Q4_0) chunk_q4_0<MT>(wc, xa, tp, M, c);
-    else if constexpr (WF == CQ_Q4_1) chunk_q4_1<MT>(wc, xa, tp, M, c);
-    else chunk_q4_k<MT>(wc, xa, tp, M, c);
+// The weight chunk, copied from its stage to registers (so the stage can be
+// refilled while the chunk value is formed).
+template <int WF>
+__device__ __forceinline__ void chunk_load(const uint8_t* wc, uint32_t (&w)[G<WF>::WCH / 4]) {
+    if constexpr (WF == CQ_Q4_K) {
+#pragma unroll
+        for (int i = 0; i < 9; ++i) {
+            const uint4 v = lds128(wc + 16 * i);
+            w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+    } else {
+        lds64<G<WF>::WCH / 8>(wc, w);
+    }
+}
+
+template <int WF, int MT, class X>
+__device__ __forceinline__ void chunk_value(const uint32_t (&wc)[G<WF>::WCH / 4], const X& x, int M, float (&c)[MT]) {
+    if constexpr (WF == CQ_Q8_0) chunk_q8_0<MT>(wc, x, M, c);
+    else if constexpr (WF == CQ_Q4_0) chunk_q4_0<MT>(wc, x, M, c);
+    else if constexpr (WF == CQ_Q4_1) chunk_q4_1<MT>(wc, x, M, c);
+    else chunk_q4_k<MT>(wc, x.xa, x.tp, M, c);
 }
 
 // ------------------------------------------------------------------ kernel
-template <int MT> constexpr int wpc_limit() { return MT <= 4 ? WPC_MAX : WPC_MAX / 2; }
+// Warps per CTA at most (the launch bound, so the register budget). One
+// token: Q8_0 and Q4_1 hold the lane's chunk of x in registers (see
+// gemv_kernel) and need the registers of 16 / 20 warps; Q4_0 and Q4_K read x
+// from shared memory and run 24 warps.
+template <int WF, int MT> __host__ __device__ constexpr bool x_in_regs() { return MT == 1 && (WF == CQ_Q8_0 || WF == CQ_Q4_1); }
+template <int WF, int MT> __host__ __device__ constexpr int wpc_limit() {
+    return MT == 1 ? (WF == CQ_Q8_0 ? 16 : WF == CQ_Q4_1 ? 20 : 24) : MT <= 4 ? WPC_MAX : WPC_MAX / 2;
+}
 
 template <int WF, int MT>
-__global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const GemvParams p) {
     pdl_trigger();
     using F = G<WF>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -523,6 +553,11 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
     // This lane's chunk in an item: row lr, chunk lj (one division per launch).
     const int lr = p.nseg == 1 ? lane / p.nc : 0;
     const int lj = p.nseg == 1 ? lane - lr * p.nc : lane;
+    // One token and whole rows in an item: the lane's chunk of x never changes.
+    constexpr bool PAIRS = WF == CQ_Q4_1;
+    constexpr bool XREG = x_in_regs<WF, MT>();
+    RegX<PAIRS> xr;
+    if (XREG && p.xreg) xr.load(act + lj * F::ACP);
     Cursor cc{wid, 0, 0, 0u};
     int64_t kfail = -1;
     int slot0 = 0;          // batch slots filled so far (R per row group)
@@ -535,19 +570,28 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
         const int cn = p.nseg == 1 ? p.nc : min(32, p.nc - c0);
         const int rows_valid = static_cast<int>(min(static_cast<int64_t>(p.R), p.N - row0));
         const uint8_t* st = stages + cc.stage * p.stage_bytes;
-        if (lr < rows_valid && lj < cn) {
-            float c[MT];
-            chunk_value<WF, MT>(st + lr * static_cast<int>(p.row_bytes) + lj * F::WCH,
-                                act + (c0 + lj) * F::ACP, p.tok_pitch, p.M, c);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-                if (m < p.M) cbuf[(m * p.B + slot0 + lr) * p.nc + c0 + lj] = c[m];
-        }
+        const bool have = lr < rows_valid && lj < cn;
+        uint32_t wr[F::WCH / 4];
+        if (have) chunk_load<WF>(st + lr * static_cast<int>(p.row_bytes) + lj * F::WCH, wr);
+        // The stage is read: refill it before the arithmetic.
         __syncwarp();
         if (lane == 0 && issued < nsteps) {
             issue(ic);
             advance(ic);
             ++issued;
+        }
+        if (have) {
+            float c[MT];
+            const SmemX<PAIRS> xs{act + (c0 + lj) * F::ACP, p.tok_pitch};
+            if constexpr (XREG) {
+                if (p.xreg) chunk_value<WF, MT>(wr, xr, p.M, c);
+                else chunk_value<WF, MT>(wr, xs, p.M, c);
+            } else {
+                chunk_value<WF, MT>(wr, xs, p.M, c);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                if (m < p.M) cbuf[(m * p.B + slot0 + lr) * p.cpitch + c0 + lj] = c[m];
         }
         const int64_t g = cc.g;
         const bool row_done = cc.seg == p.nseg - 1;
@@ -555,11 +599,12 @@ __global__ void __launch_bounds__(wpc_limit<MT>() * 32) gemv_kernel(const GemvPa
         if (row_done) {
             slot0 += p.R;
             if (slot0 == p.B || k == nsteps - 1) {
+                __syncwarp();       // every lane's chunk values are in the buffer
                 // Fixed order: y = 0, then y = y + c over the row's chunks in increasing k.
                 // Slot r holds row (r % R) of group g - ((slot0 - 1 - r) / R) * wtot.
                 for (int q = lane; q < p.M * slot0; q += 32) {
                     const int m = q / slot0, r = q - m * slot0;
-                    const float* cb = cbuf + (m * p.B + r) * p.nc;
+                    const float* cb = cbuf + (m * p.B + r) * p.cpitch;
                     float acc = 0.0f;
                     if constexpr (WF == CQ_Q4_K) {
                         // y = fma(d_x, t, y) per superblock, d_x from the staged activations
@@ -603,6 +648,15 @@ bool mma_enabled() {
     return v;
 }
 
+// CQ_GEMV_XREG=0 reads x from shared memory on every item (for A/B runs).
+bool xreg_enabled() {
+    static const bool v = [] {
+        const char* e = std::getenv("CQ_GEMV_XREG");
+        return !(e && e[0] == '0');
+    }();
+    return v;
+}
+
 // Ring depth: CQ_GEMV_STAGES (2..4) overrides the choice, for tuning runs.
 int stage_override() {
     static const int v = [] {
@@ -613,20 +667,27 @@ int stage_override() {
     return v;
 }
 
+// Warps per CTA cap: CQ_GEMV_WPC overrides, for tuning runs.
+int wpc_override() {
+    static const int v = [] {
+        const char* e = std::getenv("CQ_GEMV_WPC");
+        return e ? std::atoi(e) : 0;
+    }();
+    return v;
+}
+
 template <int WF, int MT>
 cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cudaStream_t s) {
     const int lim = std::min(dev.smem_optin, 227 * 1024);
     const int budget = lim - 1024;
-    // Shared memory per warp: barriers, S stages, chunk-value buffer. Prefer
-    // at least three stages when that still leaves twelve warps or more.
+    // Shared memory per warp: barriers, S stages, chunk-value buffer.
     auto warp_bytes = [&](int S) { return (128 + S * p.stage_bytes + 4 * CBUF_FLOATS + 127) / 128 * 128; };
-    auto warps_for = [&](int S) { return std::min(wpc_limit<MT>(), (budget - p.act_bytes) / warp_bytes(S)); };
-    int S = stage_override();
-    if (S == 0) {
-        S = 4;
-        while (S > 2 && warps_for(S) < std::min(12, wpc_limit<MT>())) --S;
-    }
+    auto warps_for = [&](int S) { return std::min(wpc_limit<WF, MT>(), (budget - p.act_bytes) / warp_bytes(S)); };
+    // Two stages a warp and as many warps as fit: at equal bytes in flight,
+    // deeper rings ran slower (a landed stage waits behind an earlier one).
+    const int S = stage_override() > 0 ? stage_override() : 2;
     int wpc = warps_for(S);
+    if (wpc_override() > 0) wpc = std::min(wpc, wpc_override());
     if (wpc < 1) return cudaErrorInvalidConfiguration;
     p.stages = S;
     p.warp_bytes = warp_bytes(S);
@@ -698,10 +759,14 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         }
         p.stage_bytes = static_cast<int>(((p.nseg == 1 ? p.R * row_bytes : int64_t(32) * F::WCH) + 127) / 128 * 128);
         // Rows per batch of sequential sums: a multiple of R, buffer within CBUF_FLOATS.
-        const int rows_fit = CBUF_FLOATS / (p.M * nc);
+        // An odd row pitch in the chunk-value buffer where one item still fits.
+        p.cpitch = (nc % 2 == 0 && p.R * p.M * (nc + 1) <= CBUF_FLOATS) ? nc + 1 : nc;
+        const int cpitch = p.cpitch;
+        const int rows_fit = CBUF_FLOATS / (p.M * cpitch);
         p.B = std::max(p.R, std::min(32, rows_fit) / p.R * p.R);
-        if (p.B * p.M * nc > CBUF_FLOATS) return cudaErrorInvalidValue;
+        if (p.B * p.M * cpitch > CBUF_FLOATS) return cudaErrorInvalidValue;
         p.tok_pitch = tok_pitch;
+        p.xreg = x_in_regs<WF, 1>() && p.M == 1 && p.nseg == 1 && xreg_enabled() ? 1 : 0;
         p.wconst = weights_const() ? 1 : 0;
         p.act_bytes = (p.M * tok_pitch + 127) / 128 * 128;
         const int64_t groups = (N + p.R - 1) / p.R;
