@@ -155,12 +155,26 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
     const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t steps = static_cast<int64_t>(my_tiles) * nseg;
 
-    if (threadIdx.x == 0) {
+    const bool producer = warp == CONSUMERS && lane == 0;
+    auto issue = [&](int64_t k) {
+        const int st = static_cast<int>(k % S);
+        const int tile = blockIdx.x + static_cast<int>(k / nseg) * gridDim.x;
+        const int seg = static_cast<int>(k % nseg);
+        mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(p.stage_bytes));
+        // x counts 2-byte elements of the row
+        tc::tma_load_2d(smem + p.smem_stage + st * p.stage_bytes, &wmap, seg * SEG_BLOCKS * F::BB / 2, tile * ROWS,
+                        &full[st]);
+    };
+    // The weight stream starts before the activations are staged: the first
+    // S stages need no release.
+    int64_t k0 = 0;
+    if (producer) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], CONSUMERS);
         }
         fence_mbar_init();
+        for (; k0 < steps && k0 < S; ++k0) issue(k0);
     }
     // Stage the activations once. Per (token m, block b): the 32 quants as
     // fp16 in four 16-byte chunks, chunk t = elements [4t, 4t+2, 4t+1, 4t+3,
@@ -208,19 +222,14 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
 
     if (warp == CONSUMERS) {
         // -------------------------------------------------------- producer
-        if (lane == 0) {
-            for (int64_t k = 0; k < steps; ++k) {
+        if (producer) {
+            for (int64_t k = k0; k < steps; ++k) {
                 const int st = static_cast<int>(k % S);
                 if (!mbar_wait_bounded(&empty[st], static_cast<uint32_t>(((k / S) & 1) ^ 1), WAIT_LIMIT_NS)) {
                     atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
                     break;
                 }
-                const int tile = blockIdx.x + static_cast<int>(k / nseg) * gridDim.x;
-                const int seg = static_cast<int>(k % nseg);
-                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(p.stage_bytes));
-                // x counts 2-byte elements of the row
-                tc::tma_load_2d(smem + p.smem_stage + st * p.stage_bytes, &wmap, seg * SEG_BLOCKS * F::BB / 2,
-                                tile * ROWS, &full[st]);
+                issue(k);
             }
         }
     } else {
