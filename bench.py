@@ -209,8 +209,12 @@ def aggregate_gbs(world, bytes_per_rank_step, ms_per_step):
 
 
 # --------------------------------------------------------------- GPU timing
-def _flush(torch, buf):
-    buf.add_(1)  # touch 256 MB: evicts the 129 MB L2
+def _flush(torch, buf, rbuf):
+    """Evict the 129 MB L2 between timed calls: write a 256 MB buffer, then read
+    another 256 MB one, so the L2 is left holding clean lines and the timed
+    call does not pay for writing the flush's dirty lines back."""
+    buf.add_(1)
+    rbuf.sum()
 
 
 def time_calls(torch, fn, iters, warmup, flush=None):
@@ -238,12 +242,13 @@ class _Ctx:
         self.torch = torch
         self.iters, self.warmup = iters, warmup
         self.flushbuf = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+        self.flushread = torch.zeros(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
 
     def dev(self, a):
         return self.torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
     def flush(self):
-        _flush(self.torch, self.flushbuf)
+        _flush(self.torch, self.flushbuf, self.flushread)
 
     def stream(self):
         return self.torch.cuda.current_stream().cuda_stream
