@@ -67,7 +67,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // returns once the grids this one depends on have completed and their writes
 // are visible (at once for a grid launched without such a dependency): no
 // kernel reads or writes global memory before it, except the GEMV's weight
-// prefetch under the weights-constant option.
+// prefetches -- into L2 always (L2 is coherent, so nothing stale can reach
+// shared memory through it), into shared memory only under the
+// weights-constant option.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
@@ -115,6 +117,11 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
         ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+// Prefetch [gsrc, gsrc + bytes) from global memory into L2 (no completion to
+// wait for). Address 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

@@ -64,6 +64,7 @@ struct GemvParams {
     const float* x;   // fp32 activations to quantize in the kernel (cq_gemv_x), else null
     uint8_t* xq_out;  // where CTA 0 writes their quantisation (with x)
     int xreg;         // one token, whole rows per item: the lane's chunk of x held in registers
+    int l2pf;         // items past the ring prefetched into L2 before the dependency wait
 };
 
 // Exact float of an int with |i| < 2^22: the bits of 1.5 * 2^23 + i, minus 1.5 * 2^23.
@@ -510,10 +511,8 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
         if (++c.seg == p.nseg) { c.seg = 0; c.g += wtot; }
         if (++c.stage == S) { c.stage = 0; c.phase ^= 1u; }
     };
-    auto issue = [&](const Cursor& c) {
+    auto item = [&](const Cursor& c, const uint8_t*& src, uint32_t& bytes) {
         const int64_t row0 = c.g * p.R;
-        uint32_t bytes;
-        const uint8_t* src;
         if (p.nseg == 1) {
             bytes = static_cast<uint32_t>(min(static_cast<int64_t>(p.R), p.N - row0) * p.row_bytes);
             src = p.W + row0 * p.row_bytes;
@@ -522,6 +521,11 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
             bytes = static_cast<uint32_t>(min(32, p.nc - c0) * F::WCH);
             src = p.W + row0 * p.row_bytes + static_cast<int64_t>(c0) * F::WCH;
         }
+    };
+    auto issue = [&](const Cursor& c) {
+        uint32_t bytes;
+        const uint8_t* src;
+        item(c, src, bytes);
         uint64_t* bar = &bars[c.stage];
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, bytes);
@@ -529,20 +533,40 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
     };
 
     // Start the weight stream first; stage the activations while it flies.
-    // The weights may be requested before the preceding grid has completed
-    // only when the caller has declared them constant.
-    if (!p.wconst) pdl_wait();
+    // Shared-memory copies of the weights may start before the preceding grid
+    // has completed only when the caller has declared them constant; the L2
+    // prefetch of the items after them may always (L2 is coherent, so a later
+    // write by that grid still reaches the copies made after the wait).
     Cursor ic{wid, 0, 0, 0u};
     int64_t issued = 0;
+    auto prefetch = [&](int64_t from, int64_t count) {
+        Cursor pc = ic;
+        for (int64_t j = from; j < min(from + count, nsteps); ++j) {
+            uint32_t bytes;
+            const uint8_t* src;
+            item(pc, src, bytes);
+            bulk_prefetch_l2(src, bytes);
+            advance(pc);
+        }
+    };
     if (active && lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_mbar_init();
+        if (p.wconst) {
+            for (; issued < min(static_cast<int64_t>(S), nsteps); ++issued) {
+                issue(ic);
+                advance(ic);
+            }
+        }
+        prefetch(issued, p.l2pf + (p.wconst ? 0 : S));
+    }
+    pdl_wait();
+    if (active && lane == 0 && !p.wconst) {
         for (; issued < min(static_cast<int64_t>(S), nsteps); ++issued) {
             issue(ic);
             advance(ic);
         }
     }
-    if (p.wconst) pdl_wait();
     if (p.x != nullptr)
         stage_activations_x<WF>(p, act);
     else
@@ -657,6 +681,18 @@ bool xreg_enabled() {
     return v;
 }
 
+// Items a warp prefetches into L2 past its ring before the dependency wait,
+// so DRAM stays busy while the preceding grids drain: 8 for Q8_0 (decode
+// step 118.9 -> 111.7 us), 4 for the 4-bit formats, whose CTAs run more
+// warps (more than that crowds the L2). CQ_GEMV_L2PF overrides.
+int l2_prefetch_items(int w_fmt) {
+    static const int v = [] {
+        const char* e = std::getenv("CQ_GEMV_L2PF");
+        return e ? std::max(0, std::atoi(e)) : -1;
+    }();
+    return v >= 0 ? v : w_fmt == CQ_Q8_0 ? 8 : 4;
+}
+
 // Ring depth: CQ_GEMV_STAGES (2..4) overrides the choice, for tuning runs.
 int stage_override() {
     static const int v = [] {
@@ -768,6 +804,7 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         p.tok_pitch = tok_pitch;
         p.xreg = x_in_regs<WF, 1>() && p.M == 1 && p.nseg == 1 && xreg_enabled() ? 1 : 0;
         p.wconst = weights_const() ? 1 : 0;
+        p.l2pf = l2_prefetch_items(WF);
         p.act_bytes = (p.M * tok_pitch + 127) / 128 * 128;
         const int64_t groups = (N + p.R - 1) / p.R;
         cudaError_t e = launch_fmt<WF>(dev, p, groups, s);
