@@ -9,9 +9,9 @@
 // sorted by the routing kernel, are taken up to 64 at a time. Q4_0 weights
 // stream through a ring of 2-D TMA boxes (128 rows x 8 blocks; for the up
 // projection the gate and up rows of the same f land in one stage); the
-// pairs' Q8_0 activation rows are bulk-copied per 256-element segment (one
-// 272-byte copy per pair) into the same stage, then converted to fp16 in
-// shared memory. Per 32-block the integer dot is an exact fp16
+// pairs' 272-byte Q8_0 activation segments arrive in the same stage, four
+// rows per TMA gather4 (64 single copies per segment cost as much as the
+// rest of the weight stream), then are converted to fp16 in shared memory. Per 32-block the integer dot is an exact fp16
 // mma.sync m16n8k16 product (two chained k-steps; every partial sum is an
 // integer below 2^23), and the block's scale term is accumulated as
 // y = fma(d_w * d_x, isum, y) in increasing k.
@@ -48,7 +48,11 @@ constexpr int SCL_PITCH = TOK / 2 + 1;
 constexpr int BQ_BYTES = SEGB * SCL_PITCH * 16;     // 4224
 constexpr int SCL_BYTES = (BQ_BYTES + SEGB * SCL_PITCH * 8 + 127) / 128 * 128;   // keeps the stages 128-byte aligned
 constexpr int RAWA = SEGB * 34;                     // one token's Q8_0 segment: 272 bytes
-constexpr int RAWA_BYTES = TOK * RAWA;              // 17408
+// The pairs' raw segments arrive four at a time (one TMA gather4 of four
+// activation rows); each group of four starts on a 128-byte boundary.
+constexpr int RAWG = (4 * RAWA + 127) / 128 * 128;  // 1152
+constexpr int RAWA_BYTES = TOK / 4 * RAWG;          // 18432
+__host__ __device__ constexpr int raw_off(int tk) { return (tk >> 2) * RAWG + (tk & 3) * RAWA; }
 
 struct MoeMmaParams {
     const uint8_t* xq;          // up: token activations (Q8_0 [T][K]); down: hq rows (Q8_0 [P][F])
@@ -129,7 +133,7 @@ __device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, 
         float d = 0.0f;
         int sx = 0;
         if (tk < np) {
-            const uint16_t* src = reinterpret_cast<const uint16_t*>(raw + tk * RAWA + b * 34);
+            const uint16_t* src = reinterpret_cast<const uint16_t*>(raw + raw_off(tk) + b * 34);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 w[j] = static_cast<uint32_t>(src[1 + 2 * j]) | (static_cast<uint32_t>(src[2 + 2 * j]) << 16);
@@ -296,6 +300,7 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
 template <bool UP>
 __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_constant__ CUtensorMap map0,
                                                              const __grid_constant__ CUtensorMap map1,
+                                                             const __grid_constant__ CUtensorMap amap,
                                                              const MoeMmaParams p) {
     pdl_trigger();
     pdl_wait();
@@ -331,9 +336,8 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
 
     if (warp == CONSUMERS) {
         // ------------------------------------------------------- producer
-        // Per segment: the weight boxes (2-D TMA) and, for each of the pass's
-        // pairs, its activation row's 272-byte segment (1-D bulk copy).
-        const uint64_t pol = policy_evict_first();
+        // Per segment: the weight boxes (2-D TMA) and the pass's pairs'
+        // 272-byte activation segments, four rows per TMA gather4.
         int seg = 0, pass = 0;
         for (int64_t k = 0; k < steps; ++k) {
             const int st = static_cast<int>(k % S);
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
                 if (!ok) {
                     atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
                 } else {
-                    mbar_arrive_expect_tx(&sm.full[st], NMAT * BOX_BYTES + np * RAWA);
+                    mbar_arrive_expect_tx(&sm.full[st], NMAT * BOX_BYTES + (np + 3) / 4 * 4 * RAWA);
                     uint8_t* dst = sm.wst + st * STAGE;
                     tc::tma_load_2d(dst, &map0, seg * SEGB * 9, row_base, &sm.full[st]);   // 9 = 18 bytes / 2
                     if (UP) tc::tma_load_2d(dst + BOX_BYTES, &map1, seg * SEGB * 9, row_base, &sm.full[st]);
@@ -352,11 +356,16 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             uint8_t* raw = sm.wst + st * STAGE + NMAT * BOX_BYTES;
-            for (int i = lane; i < np; i += 32) {
-                const int pr = p.perm[beg + pass * TOK + i];
-                const int64_t row = UP ? pr / p.topk : pr;
-                bulk_g2s(raw + i * RAWA, p.xq + row * p.xrow + static_cast<int64_t>(seg) * RAWA, RAWA, &sm.full[st],
-                         pol);
+            // Four pairs per gather4; a short last group repeats its last
+            // pair into slots that the conversion reads as zero.
+            for (int q = lane; 4 * q < np; q += 32) {
+                int r[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int pr = p.perm[beg + pass * TOK + min(4 * q + j, np - 1)];
+                    r[j] = UP ? pr / p.topk : pr;
+                }
+                tc::tma_gather4(raw + q * RAWG, &amap, seg * (RAWA / 2), r[0], r[1], r[2], r[3], &sm.full[st]);
             }
             if (++seg == nseg) { seg = 0; ++pass; }
         }
@@ -417,9 +426,23 @@ bool make_map(CUtensorMap* map, const void* W, int64_t rows, int kin) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q8_0 activation rows as a 2-D tensor of 2-byte elements [rows][xrow / 2];
+// box = one 272-byte segment of one row (the gather4 form takes four rows).
+bool make_act_map(CUtensorMap* map, const void* X, int64_t rows, int64_t xrow) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(xrow / 2), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(xrow)};
+    const cuuint32_t box[2] = {RAWA / 2, 1};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool UP>
-cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUtensorMap& m1, MoeMmaParams p, int E,
-                       cudaStream_t s) {
+cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUtensorMap& m1, const CUtensorMap& am,
+                       MoeMmaParams p, int E, cudaStream_t s) {
     const int lim = std::min(dev.smem_optin, 227 * 1024);
     const int fixed = 1024 + ACT_BYTES + SCL_BYTES;
     const int per_stage = (UP ? 2 : 1) * BOX_BYTES + RAWA_BYTES;
@@ -435,7 +458,7 @@ cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUten
         if (e != cudaSuccess) return e;
         if (devid < 64) raised[devid] = 1;
     }
-    e = launch_kernel(moe_mma_kernel<UP>, dim3(p.rows_per_expert / ROWS, E), dim3(THREADS), smem, s, m0, m1, p);
+    e = launch_kernel(moe_mma_kernel<UP>, dim3(p.rows_per_expert / ROWS, E), dim3(THREADS), smem, s, m0, m1, am, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -461,7 +484,11 @@ cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, i
     up.rows_per_expert = F;
     up.kin = K;
     up.xrow = static_cast<int64_t>(K / 32) * 34;
-    cudaError_t e = launch_one<true>(dev, mg, mu, up, E, s);
+    CUtensorMap ax, ah;
+    if (!make_act_map(&ax, xq, T, up.xrow) ||
+        !make_act_map(&ah, hq, static_cast<int64_t>(T) * topk, static_cast<int64_t>(F / 32) * 34))
+        return cudaErrorInvalidValue;
+    cudaError_t e = launch_one<true>(dev, mg, mu, ax, up, E, s);
     if (e != cudaSuccess) return e;
     MoeMmaParams dn = up;
     dn.xq = static_cast<const uint8_t*>(hq);
@@ -469,7 +496,7 @@ cudaError_t launch_moe_projections(const DeviceInfo& dev, int T, int K, int F, i
     dn.rows_per_expert = K;
     dn.kin = F;
     dn.xrow = static_cast<int64_t>(F / 32) * 34;
-    return launch_one<false>(dev, md, md, dn, E, s);
+    return launch_one<false>(dev, md, md, ah, dn, E, s);
 }
 
 }  // namespace cq
