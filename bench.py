@@ -11,7 +11,8 @@ them from HBM.
 
 Also printed in the same JSON line: the prefill GEMM (Q4_K, M=512, K=4096,
 N=14336) in int8-equivalent TOPS, the routed-expert FFN and the Q4_1 LM head at
-M = 1/4/8/16, the single-call latency of the small Q4_0 GEMV, the roofline of
+M = 1/4/8/16, the single-call latency of the small Q4_0 GEMV, the fused dense
+SwiGLU gate + up projection (Q4_K 14336x4096 each, M = 1/4), the roofline of
 the dominant kernel, the CPU oracle's rate on the host cores, and the
 end-to-end rate with host buffers.
 
@@ -314,6 +315,34 @@ def case_lm_head(c, cq, synth, peaks, seed, ms_list=(1, 4, 8, 16)):
     return res
 
 
+def case_swiglu(c, cq, synth, peaks, seed, ms_list=(1, 4)):
+    """Dense SwiGLU FFN gate + up in one call (cq_gemv_swiglu): Q4_K 14336x4096
+    each, M tokens; beside it the same result from two cq_gemv calls and a
+    torch silu * mul."""
+    torch = c.torch
+    Wg, Wu, x = synth.ffn_swiglu_q4_k(seed)
+    F, K = Wg.shape[0], x.shape[1]
+    tg, tu = c.dev(Wg), c.dev(Wu)
+    xq = cq.quantize_act_t(c.dev(x), cq.Q8_K)
+    wbytes = Wg.nbytes + Wu.nbytes
+    res = {"shape": f"F={F} K={K} (gate + up)", "weight_bytes": wbytes}
+    for M in ms_list:
+        h = torch.empty((M, F), dtype=torch.float32, device="cuda")
+        g = torch.empty((M, F), dtype=torch.float32, device="cuda")
+        u = torch.empty((M, F), dtype=torch.float32, device="cuda")
+        ms = c.time(lambda: cq.cq_gemv_swiglu(cq.Q4_K, M, F, K, tg.data_ptr(), tu.data_ptr(), xq.data_ptr(),
+                                              h.data_ptr(), c.stream()))
+
+        def separate():
+            cq.cq_gemv(cq.Q4_K, M, F, K, tg.data_ptr(), xq.data_ptr(), g.data_ptr(), c.stream())
+            cq.cq_gemv(cq.Q4_K, M, F, K, tu.data_ptr(), xq.data_ptr(), u.data_ptr(), c.stream())
+            torch.mul(torch.nn.functional.silu(g), u, out=h)
+        ms_sep = c.time(separate)
+        res[str(M)] = {"ms": ms, "weight_gbs": wbytes / ms / 1e6, "hbm_frac": wbytes / ms / 1e6 / peaks["hbm"],
+                       "separate_calls_ms": ms_sep}
+    return res
+
+
 def case_q4_0_small(c, cq, synth, peaks, seed):
     """Small Q4_0 GEMV 2048x2048 (2.4 MB, fits in L2): the device time of one
     call, and the rate over 256 distinct copies (576 MiB > L2) replayed
@@ -355,7 +384,7 @@ def case_q4_0_small(c, cq, synth, peaks, seed):
 
 
 CASES = {"prefill_gemm_q4_k": case_gemm, "moe_q4_0": case_moe, "lm_head_q4_1": case_lm_head,
-         "decode_q4_0_2048": case_q4_0_small}
+         "decode_q4_0_2048": case_q4_0_small, "ffn_swiglu_q4_k": case_swiglu}
 
 
 def secondary(torch, cq, synth, peaks, seed):
@@ -375,7 +404,7 @@ def run_case(args):
     c = _Ctx(torch, iters=args.steps, warmup=args.warmup)
     fn = CASES[args.case]
     kw = {}
-    if args.case == "lm_head_q4_1" and args.m:
+    if args.case in ("lm_head_q4_1", "ffn_swiglu_q4_k") and args.m:
         kw["ms_list"] = tuple(int(v) for v in args.m.split(","))
     r = fn(c, cq, synth, _peaks(), args.seed, **kw)
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup, "result": r}))
@@ -673,7 +702,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--case", choices=sorted(CASES), help="run one secondary workload alone (for profiling)")
-    ap.add_argument("--m", default="", help="with --case lm_head_q4_1: comma-separated token counts")
+    ap.add_argument("--m", default="", help="with --case lm_head_q4_1 or ffn_swiglu_q4_k: comma-separated token counts")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.case:

@@ -32,6 +32,7 @@ SIGNATURES = {
     "cq_quantize_act": (_I, [_I, _I64, _I64, _P, _P, _P]),
     "cq_gemv": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "cq_gemv_x": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
+    "cq_gemv_swiglu": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "cq_gemm": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "cq_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
     "cq_gemm_ws": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
@@ -91,6 +92,10 @@ def cq_gemv(w_fmt, M, N, K, W, xq, y, stream=0):
 
 def cq_gemv_x(w_fmt, M, N, K, W, x, xq, y, stream=0):
     return lib().cq_gemv_x(w_fmt, M, N, K, W, x, xq, y, stream)
+
+
+def cq_gemv_swiglu(w_fmt, M, F, K, W_gate, W_up, xq, h, stream=0):
+    return lib().cq_gemv_swiglu(w_fmt, M, F, K, W_gate, W_up, xq, h, stream)
 
 
 def cq_gemm(w_fmt, M, N, K, W, xq, y, stream=0):
@@ -196,6 +201,17 @@ def gemv_x_t(W, x, w_fmt: int, out=None):
     _check("cq_gemv_x", cq_gemv_x(w_fmt, M, N, K, W.data_ptr(), x.data_ptr(), xq.data_ptr(), y.data_ptr(),
                                   _stream_handle()))
     return y, xq
+
+
+def gemv_swiglu_t(Wg, Wu, xq, w_fmt: int, K: int, out=None):
+    """cq_gemv_swiglu: Wg, Wu uint8 [F, row_bytes]; xq uint8 [M, act_row_bytes] (M <= 16)
+    -> h fp32 [M, F] = silu(Wg . x) * (Wu . x)."""
+    torch = _torch()
+    F, M = Wg.shape[0], xq.shape[0]
+    h = out if out is not None else torch.empty((M, F), dtype=torch.float32, device=Wg.device)
+    _check("cq_gemv_swiglu", cq_gemv_swiglu(w_fmt, M, F, K, Wg.data_ptr(), Wu.data_ptr(), xq.data_ptr(),
+                                            h.data_ptr(), _stream_handle()))
+    return h
 
 
 def gemm_t(W, xq, w_fmt: int, K: int, out=None):

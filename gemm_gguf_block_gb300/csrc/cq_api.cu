@@ -142,6 +142,23 @@ cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 
+cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const void* W_gate, const void* W_up,
+                         const void* xq, float* h, void* stream) {
+    if (!is_weight_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, F, K);
+    if (st != CQ_OK) return st;
+    if (M < 1 || M > 16 || F < 1) return CQ_ERR_SHAPE;
+    const int64_t ce = w_fmt == CQ_Q4_K ? 256 : 128;
+    if (2 * (K / ce) > 512) return CQ_ERR_SHAPE;
+    if (W_gate == nullptr || W_up == nullptr || xq == nullptr || h == nullptr) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(W_gate) || !aligned16(W_up) || !aligned4(xq) || !aligned16(h)) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    cudaError_t e = cq::launch_gemv_swiglu(dev, w_fmt, static_cast<int>(M), F, K, W_gate, W_up, xq, h,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
 cq_status cq_selftest_wait_timeout(int64_t limit_ns, int32_t* out_code, void* stream) {
     if (out_code == nullptr || limit_ns < 1000 || limit_ns > 1000000000) return CQ_ERR_INVALID_ARG;
     cq::DeviceInfo dev;

@@ -54,6 +54,11 @@ cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, int* status, cudaStream
 cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, const float* x, cudaStream_t s);
 
+// Paired gate / up GEMV of a dense SwiGLU FFN: h = silu(Wg . xq) * (Wu . xq),
+// each product as launch_gemv computes it (the dp4a kernel, any M <= 16).
+cudaError_t launch_gemv_swiglu(const DeviceInfo& dev, int w_fmt, int M, int64_t F, int64_t K, const void* Wg,
+                               const void* Wu, const void* xq, float* h, cudaStream_t s);
+
 // Tensor-core batched GEMV (2 <= M <= 16; Q4_0, Q4_1, Q8_0) and the shared
 // memory it needs (0 when the format has no such path).
 int gemv_mma_smem(int w_fmt, int M, int64_t K);

@@ -49,7 +49,10 @@ struct GemvParams {
     int64_t N;
     int64_t row_bytes;
     int M;
-    int nc;           // chunks per row
+    int nc;           // chunks per row (paired: gate row then up row, 2 * nca)
+    int nca;          // chunks of x (== nc unpaired)
+    const uint8_t* W2;  // paired: the up matrix (W is the gate matrix)
+    int64_t wrow;     // paired: bytes per gate / up row
     int cpitch;       // floats per row in the chunk-value buffer (odd where it fits: no bank conflicts)
     int R;            // rows per item
     int segc;         // chunks per item
@@ -95,7 +98,7 @@ template <int WF>
 __device__ void stage_activations(const GemvParams& p, uint8_t* act) {
     const int nthr = blockDim.x;
     if constexpr (WF == CQ_Q4_K) {
-        const int ns = p.nc;
+        const int ns = p.nca;
         const int words = p.M * ns * 73;          // 292 bytes per superblock
         const uint32_t* src = reinterpret_cast<const uint32_t*>(p.xq);
         for (int i = threadIdx.x; i < words; i += nthr) {
@@ -117,10 +120,10 @@ __device__ void stage_activations(const GemvParams& p, uint8_t* act) {
     } else {
         constexpr int BB = WF == CQ_Q4_1 ? 36 : 34;     // Q8_1 or Q8_0 block bytes
         constexpr int QO = WF == CQ_Q4_1 ? 4 : 2;       // quant offset in the block
-        const int nblk = p.M * p.nc * 4;
+        const int nblk = p.M * p.nca * 4;
         const uint16_t* src = reinterpret_cast<const uint16_t*>(p.xq);
         for (int i = threadIdx.x; i < nblk; i += nthr) {
-            const int m = i / (p.nc * 4), r = i - m * p.nc * 4;
+            const int m = i / (p.nca * 4), r = i - m * p.nca * 4;
             const int c = r >> 2, b = r & 3;
             const uint16_t* s = src + static_cast<int64_t>(i) * (BB / 2);
             uint8_t* dst = act + m * p.tok_pitch + c * G<WF>::ACP;
@@ -146,11 +149,11 @@ template <int WF>
 __device__ void stage_activations_x(const GemvParams& p, uint8_t* act) {
     const int nthr = blockDim.x;
     const bool out = blockIdx.x == 0;
-    const int64_t K = static_cast<int64_t>(p.nc) * G<WF>::CE;
+    const int64_t K = static_cast<int64_t>(p.nca) * G<WF>::CE;
     if constexpr (WF == CQ_Q4_K) {
         // A warp per superblock, eight consecutive elements per lane.
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nthr >> 5;
-        const int ns = p.nc;
+        const int ns = p.nca;
         for (int sb = warp; sb < p.M * ns; sb += nw) {
             const int m = sb / ns, c = sb - m * ns;
             const float4* src = reinterpret_cast<const float4*>(p.x + m * K + c * 256 + 8 * lane);
@@ -190,9 +193,9 @@ __device__ void stage_activations_x(const GemvParams& p, uint8_t* act) {
     } else {
         constexpr int BB = WF == CQ_Q4_1 ? 36 : 34;     // Q8_1 or Q8_0 block bytes
         constexpr int QO = WF == CQ_Q4_1 ? 4 : 2;       // quant offset in the block
-        const int nblk = p.M * p.nc * 4;
+        const int nblk = p.M * p.nca * 4;
         for (int i = threadIdx.x; i < nblk; i += nthr) {
-            const int m = i / (p.nc * 4), r = i - m * p.nc * 4;
+            const int m = i / (p.nca * 4), r = i - m * p.nca * 4;
             const int c = r >> 2, b = r & 3;
             const float4* src = reinterpret_cast<const float4*>(p.x + m * K + 32 * r);
             float v[32];
@@ -477,7 +480,9 @@ template <int WF, int MT> __host__ __device__ constexpr int wpc_limit() {
     return MT == 1 ? (WF == CQ_Q8_0 ? 16 : WF == CQ_Q4_1 ? 20 : 24) : MT <= 4 ? WPC_MAX : WPC_MAX / 2;
 }
 
-template <int WF, int MT>
+// SWI (paired): the rows are (gate row f | up row f) of two matrices, one
+// virtual row of 2 * nca chunks each; y[m][f] = silu(g) * u from the two sums.
+template <int WF, int MT, bool SWI>
 __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const GemvParams p) {
     pdl_trigger();
     using F = G<WF>;
@@ -511,25 +516,54 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
         if (++c.seg == p.nseg) { c.seg = 0; c.g += wtot; }
         if (++c.stage == S) { c.stage = 0; c.phase ^= 1u; }
     };
-    auto item = [&](const Cursor& c, const uint8_t*& src, uint32_t& bytes) {
+    // An item is one contiguous byte range, or (paired) up to two: the gate
+    // part and the up part, landing at their places in the stage.
+    struct Range {
+        const uint8_t* src;
+        uint32_t bytes;
+        uint32_t dst;
+    };
+    auto item = [&](const Cursor& c, Range (&r)[2]) -> int {
         const int64_t row0 = c.g * p.R;
-        if (p.nseg == 1) {
-            bytes = static_cast<uint32_t>(min(static_cast<int64_t>(p.R), p.N - row0) * p.row_bytes);
-            src = p.W + row0 * p.row_bytes;
+        if constexpr (!SWI) {
+            if (p.nseg == 1) {
+                r[0] = {p.W + row0 * p.row_bytes,
+                        static_cast<uint32_t>(min(static_cast<int64_t>(p.R), p.N - row0) * p.row_bytes), 0u};
+            } else {
+                const int c0 = c.seg * 32;
+                r[0] = {p.W + row0 * p.row_bytes + static_cast<int64_t>(c0) * F::WCH,
+                        static_cast<uint32_t>(min(32, p.nc - c0) * F::WCH), 0u};
+            }
+            return 1;
         } else {
-            const int c0 = c.seg * 32;
-            bytes = static_cast<uint32_t>(min(32, p.nc - c0) * F::WCH);
-            src = p.W + row0 * p.row_bytes + static_cast<int64_t>(c0) * F::WCH;
+            if (p.nseg == 1) {
+                // R gate rows, then R up rows
+                const uint32_t b = static_cast<uint32_t>(min(static_cast<int64_t>(p.R), p.N - row0) * p.wrow);
+                r[0] = {p.W + row0 * p.wrow, b, 0u};
+                r[1] = {p.W2 + row0 * p.wrow, b, static_cast<uint32_t>(p.R * p.wrow)};
+                return 2;
+            }
+            const int c0 = c.seg * 32, c1 = min(c0 + 32, p.nc);
+            int n = 0;
+            if (c0 < p.nca)
+                r[n++] = {p.W + row0 * p.wrow + static_cast<int64_t>(c0) * F::WCH,
+                          static_cast<uint32_t>((min(c1, p.nca) - c0) * F::WCH), 0u};
+            if (c1 > p.nca) {
+                const int u0 = max(c0, p.nca);
+                r[n++] = {p.W2 + row0 * p.wrow + static_cast<int64_t>(u0 - p.nca) * F::WCH,
+                          static_cast<uint32_t>((c1 - u0) * F::WCH), static_cast<uint32_t>((u0 - c0) * F::WCH)};
+            }
+            return n;
         }
     };
     auto issue = [&](const Cursor& c) {
-        uint32_t bytes;
-        const uint8_t* src;
-        item(c, src, bytes);
+        Range r[2];
+        const int n = item(c, r);
         uint64_t* bar = &bars[c.stage];
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, bytes);
-        bulk_g2s(stages + c.stage * p.stage_bytes, src, bytes, bar, policy);
+        mbar_arrive_expect_tx(bar, n == 2 ? r[0].bytes + r[1].bytes : r[0].bytes);
+        for (int i = 0; i < n; ++i)
+            bulk_g2s(stages + c.stage * p.stage_bytes + r[i].dst, r[i].src, r[i].bytes, bar, policy);
     };
 
     // Start the weight stream first; stage the activations while it flies.
@@ -542,10 +576,9 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
     auto prefetch = [&](int64_t from, int64_t count) {
         Cursor pc = ic;
         for (int64_t j = from; j < min(from + count, nsteps); ++j) {
-            uint32_t bytes;
-            const uint8_t* src;
-            item(pc, src, bytes);
-            bulk_prefetch_l2(src, bytes);
+            Range r[2];
+            const int n = item(pc, r);
+            for (int i = 0; i < n; ++i) bulk_prefetch_l2(r[i].src, r[i].bytes);
             advance(pc);
         }
     };
@@ -580,8 +613,20 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
     // One token and whole rows in an item: the lane's chunk of x never changes.
     constexpr bool PAIRS = WF == CQ_Q4_1;
     constexpr bool XREG = x_in_regs<WF, MT>();
+    // The x chunk of virtual chunk c (paired: the up part reuses x from 0).
+    auto xchunk = [&](int c) { return SWI && c >= p.nca ? c - p.nca : c; };
+    // Offset of (row lr, chunk lj) in a stage: rows of row_bytes, or (paired,
+    // whole rows) R gate rows then R up rows.
+    auto woff = [&](int lr_, int lj_) -> int {
+        if constexpr (SWI) {
+            if (p.nseg == 1)
+                return lj_ < p.nca ? lr_ * static_cast<int>(p.wrow) + lj_ * F::WCH
+                                   : (p.R + lr_) * static_cast<int>(p.wrow) + (lj_ - p.nca) * F::WCH;
+        }
+        return lr_ * static_cast<int>(p.row_bytes) + lj_ * F::WCH;
+    };
     RegX<PAIRS> xr;
-    if (XREG && p.xreg) xr.load(act + lj * F::ACP);
+    if (XREG && p.xreg) xr.load(act + xchunk(lj) * F::ACP);
     Cursor cc{wid, 0, 0, 0u};
     int64_t kfail = -1;
     int slot0 = 0;          // batch slots filled so far (R per row group)
@@ -596,7 +641,7 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
         const uint8_t* st = stages + cc.stage * p.stage_bytes;
         const bool have = lr < rows_valid && lj < cn;
         uint32_t wr[F::WCH / 4];
-        if (have) chunk_load<WF>(st + lr * static_cast<int>(p.row_bytes) + lj * F::WCH, wr);
+        if (have) chunk_load<WF>(st + woff(lr, lj), wr);
         // The stage is read: refill it before the arithmetic.
         __syncwarp();
         if (lane == 0 && issued < nsteps) {
@@ -606,7 +651,7 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
         }
         if (have) {
             float c[MT];
-            const SmemX<PAIRS> xs{act + (c0 + lj) * F::ACP, p.tok_pitch};
+            const SmemX<PAIRS> xs{act + xchunk(c0 + lj) * F::ACP, p.tok_pitch};
             if constexpr (XREG) {
                 if (p.xreg) chunk_value<WF, MT>(wr, xr, p.M, c);
                 else chunk_value<WF, MT>(wr, xs, p.M, c);
@@ -629,16 +674,28 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
                 for (int q = lane; q < p.M * slot0; q += 32) {
                     const int m = q / slot0, r = q - m * slot0;
                     const float* cb = cbuf + (m * p.B + r) * p.cpitch;
-                    float acc = 0.0f;
-                    if constexpr (WF == CQ_Q4_K) {
-                        // y = fma(d_x, t, y) per superblock, d_x from the staged activations
-                        const uint8_t* xd = act + m * p.tok_pitch + 256;
+                    // The sum over chunks [j0, j0 + n) of the row, x chunks from 0.
+                    auto rowsum = [&](int j0, int n) {
+                        float acc = 0.0f;
+                        if constexpr (WF == CQ_Q4_K) {
+                            // y = fma(d_x, t, y) per superblock, d_x from the staged activations
+                            const uint8_t* xd = act + m * p.tok_pitch + 256;
 #pragma unroll 8
-                        for (int j = 0; j < p.nc; ++j)
-                            acc = __fmaf_rn(*reinterpret_cast<const float*>(xd + j * F::ACP), cb[j], acc);
+                            for (int j = 0; j < n; ++j)
+                                acc = __fmaf_rn(*reinterpret_cast<const float*>(xd + j * F::ACP), cb[j0 + j], acc);
+                        } else {
+#pragma unroll 8
+                            for (int j = 0; j < n; ++j) acc = __fadd_rn(acc, cb[j0 + j]);
+                        }
+                        return acc;
+                    };
+                    float acc;
+                    if constexpr (SWI) {
+                        // h = silu(g) * u, silu(g) = g / (1 + exp(-g)), all fp32
+                        const float gs = rowsum(0, p.nca), us = rowsum(p.nca, p.nca);
+                        acc = __fmul_rn(__fdiv_rn(gs, __fadd_rn(1.0f, expf(-gs))), us);
                     } else {
-#pragma unroll 8
-                        for (int j = 0; j < p.nc; ++j) acc = __fadd_rn(acc, cb[j]);
+                        acc = rowsum(0, p.nc);
                     }
                     const int back = (slot0 - 1 - r) / p.R;
                     const int64_t row = (g - back * wtot) * p.R + (r - (r / p.R) * p.R);
@@ -712,7 +769,7 @@ int wpc_override() {
     return v;
 }
 
-template <int WF, int MT>
+template <int WF, int MT, bool SWI>
 cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cudaStream_t s) {
     const int lim = std::min(dev.smem_optin, 227 * 1024);
     const int budget = lim - 1024;
@@ -740,32 +797,36 @@ cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cu
     cudaError_t e = cudaGetDevice(&devid);
     if (e != cudaSuccess) return e;
     if (devid >= 64 || raised[devid] < lim) {
-        e = cudaFuncSetAttribute(gemv_kernel<WF, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+        e = cudaFuncSetAttribute(gemv_kernel<WF, MT, SWI>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
         if (e != cudaSuccess) return e;
         if (devid < 64) raised[devid] = lim;
     }
-    cudaError_t le = launch_kernel(gemv_kernel<WF, MT>, dim3(grid), dim3(wpc * 32), smem, s, p);
+    cudaError_t le = launch_kernel(gemv_kernel<WF, MT, SWI>, dim3(grid), dim3(wpc * 32), smem, s, p);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
 }
 
-template <int WF>
+template <int WF, bool SWI>
 cudaError_t launch_fmt(const DeviceInfo& dev, const GemvParams& p, int64_t groups, cudaStream_t s) {
-    if (p.M <= 1) return launch_typed<WF, 1>(dev, p, groups, s);
-    if (p.M <= 4) return launch_typed<WF, 4>(dev, p, groups, s);
-    if (p.M <= 8) return launch_typed<WF, 8>(dev, p, groups, s);
-    return launch_typed<WF, 16>(dev, p, groups, s);
+    if (p.M <= 1) return launch_typed<WF, 1, SWI>(dev, p, groups, s);
+    if (p.M <= 4) return launch_typed<WF, 4, SWI>(dev, p, groups, s);
+    if (p.M <= 8) return launch_typed<WF, 8, SWI>(dev, p, groups, s);
+    return launch_typed<WF, 16, SWI>(dev, p, groups, s);
 }
 
+// W2 != null: paired (gate W, up W2), y = silu(W . x) * (W2 . x).
 template <int WF>
-cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, const void* W, const void* xq,
-                            float* y, const float* x, cudaStream_t s) {
+cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, const void* W, const void* W2,
+                            const void* xq, float* y, const float* x, cudaStream_t s) {
     using F = G<WF>;
-    const int nc = static_cast<int>(K / F::CE);
+    const bool swi = W2 != nullptr;
+    const int nca = static_cast<int>(K / F::CE);
+    const int nc = swi ? 2 * nca : nca;
     if (nc > CBUF_FLOATS) return cudaErrorInvalidValue;
+    const int64_t wrow = static_cast<int64_t>(nca) * F::WCH;
     const int64_t row_bytes = static_cast<int64_t>(nc) * F::WCH;
     const int act_row = static_cast<int>(K / CHUNK_ELEMS) * achunk_bytes(act_fmt_for(WF));
-    const int tok_pitch = nc * F::ACP;
+    const int tok_pitch = nca * F::ACP;
     // Tokens per launch: staged activations within 100 KB, and the chunk-value
     // buffer holding at least one row of every token.
     int max_tok = std::max(1, std::min(M, (100 * 1024) / tok_pitch));
@@ -784,6 +845,9 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         p.N = N;
         p.row_bytes = row_bytes;
         p.nc = nc;
+        p.nca = nca;
+        p.W2 = static_cast<const uint8_t*>(W2);
+        p.wrow = wrow;
         if (nc <= 32) {
             p.R = 32 / nc;
             p.segc = nc;
@@ -807,7 +871,7 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         p.l2pf = l2_prefetch_items(WF);
         p.act_bytes = (p.M * tok_pitch + 127) / 128 * 128;
         const int64_t groups = (N + p.R - 1) / p.R;
-        cudaError_t e = launch_fmt<WF>(dev, p, groups, s);
+        cudaError_t e = swi ? launch_fmt<WF, true>(dev, p, groups, s) : launch_fmt<WF, false>(dev, p, groups, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -833,10 +897,22 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
         return launch_gemv_mma(dev, w_fmt, M, N, K, W, xq, y, s);
     }
     switch (w_fmt) {
-    case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, x, s);
-    case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, x, s);
-    case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, x, s);
-    case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, xq, y, x, s);
+    case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, N, K, W, nullptr, xq, y, x, s);
+    case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, nullptr, xq, y, x, s);
+    case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, nullptr, xq, y, x, s);
+    case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, nullptr, xq, y, x, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemv_swiglu(const DeviceInfo& dev, int w_fmt, int M, int64_t F, int64_t K, const void* Wg,
+                               const void* Wu, const void* xq, float* h, cudaStream_t s) {
+    if (M <= 0 || F <= 0) return cudaSuccess;
+    switch (w_fmt) {
+    case CQ_Q4_0: return launch_gemv_fmt<CQ_Q4_0>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
+    case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
+    case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
+    case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -207,3 +207,11 @@ def lm_head_q4_1(seed: int = 0, N: int = 128256, K: int = 4096, M: int = 16):
     W = gen_q4_1(stream(seed, 5, 0), N, K)
     x = gen_x(stream(seed, 5, 1), M, K)
     return W, x
+
+
+def ffn_swiglu_q4_k(seed: int = 0, F: int = 14336, K: int = 4096, M: int = 4):
+    """Dense SwiGLU FFN gate and up projections, Q4_K [F, K] each (Llama-3-8B shapes)."""
+    Wg = gen_q4_k(stream(seed, 6, 0), F, K)
+    Wu = gen_q4_k(stream(seed, 6, 1), F, K)
+    x = gen_x(stream(seed, 6, 2), M, K)
+    return Wg, Wu, x

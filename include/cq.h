@@ -131,6 +131,24 @@ cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void
                     void* xq, float* y, void* stream);
 
 /*
+ * Gate and up projections of a dense SwiGLU FFN in one pass, and their
+ * combination (alice-llm docs "WGSL Shader Architecture": swiglu_fused_q4k;
+ * "The GPU Optimization Journey", phase 4: gate and up read in one pass):
+ *   g = W_gate . xq,  u = W_up . xq   (each exactly as cq_gemv computes it)
+ *   h[m][f] = silu(g) * u = g / (1 + exp(-g)) * u   (fp32: RN divide,
+ *             RN add, RN multiply; exp is CUDA's expf)
+ * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K}; xq in the paired activation format;
+ * W_gate, W_up: F rows of K/blk blocks each (16-byte aligned); h: fp32
+ * [M][F] (16-byte aligned). 1 <= M <= 16 (else CQ_ERR_SHAPE); F >= 1;
+ * K a positive multiple of 256 with 2 * K / 128 <= 512 chunks (K <= 32768;
+ * Q4_K: K <= 65536). Errors as cq_gemv. g and u never leave the kernel: one
+ * launch reads both matrices, combines the two sums of each (row, token) and
+ * writes only h.
+ */
+cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const void* W_gate,
+                         const void* W_up, const void* xq, float* h, void* stream);
+
+/*
  * Prefill GEMM, any M >= 0 (cera README "Supported models": batched-GEMM
  * prefill; alice-llm "Computation Path (Q4_K)"). Same operands and result as
  * cq_gemv; each row equals the cq_gemv result for that token bit for bit.

@@ -70,6 +70,8 @@ def lib():
             L.oracle_matmul_rows.restype = I
             L.oracle_moe.argtypes = [I64] * 5 + [P] * 12
             L.oracle_moe.restype = I
+            L.oracle_swiglu.argtypes = [I, I64, I64, I64, P, P, P, P, P]
+            L.oracle_swiglu.restype = I
             _lib = L
     return _lib
 
@@ -128,6 +130,20 @@ def matmul(wfmt: int, W: np.ndarray, xq: np.ndarray, K: int, rows=None):
     if rc != 0:
         raise ValueError("oracle_matmul rejected its arguments")
     return y, at
+
+
+def swiglu(wfmt: int, Wg: np.ndarray, Wu: np.ndarray, xq: np.ndarray, K: int):
+    """Dense SwiGLU gate / up in fp64: h [M, F] = silu(Wg . x) * (Wu . x), and
+    aux [M, F, 4] = (g, u, sum|terms| of g, sum|terms| of u)."""
+    Wg, Wu = (np.ascontiguousarray(a, dtype=np.uint8) for a in (Wg, Wu))
+    xq = np.ascontiguousarray(xq, dtype=np.uint8)
+    F, M = Wg.shape[0], xq.shape[0]
+    h = np.zeros((M, F))
+    aux = np.zeros((M, F, 4))
+    rc = lib().oracle_swiglu(wfmt, M, F, K, _p(Wg), _p(Wu), _p(xq), _p(h), _p(aux))
+    if rc != 0:
+        raise ValueError("oracle_swiglu rejected its arguments")
+    return h, aux
 
 
 def moe(Wg, Wu, Wd, ids, rw, xq, K: int, F: int):

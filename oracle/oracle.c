@@ -329,6 +329,34 @@ int oracle_matmul(int wfmt, int64_t M, int64_t N, int64_t K, const uint8_t* W,
     return oracle_matmul_rows(wfmt, M, N, K, W, X, 0, N, y, absterms);
 }
 
+/* ------------------------------------------------------ dense SwiGLU gate / up */
+
+/* The gate and up projections of a dense SwiGLU FFN and their combination
+ * (alice-llm docs "WGSL Shader Architecture": swiglu_fused_q4k computes
+ * silu(gate) * up; "The GPU Optimization Journey" phase 4):
+ *   g = W_gate[f] . X[m],  u = W_up[f] . X[m]    (the block formula, fp64)
+ *   h[m][f] = silu(g) * u = g / (1 + exp(-g)) * u (fp64)
+ * gu_aux [M][F][4] = (g, u, absterms(g), absterms(u)); may be NULL. */
+int oracle_swiglu(int wfmt, int64_t M, int64_t F, int64_t K, const uint8_t* Wg, const uint8_t* Wu,
+                  const uint8_t* X, double* h, double* gu_aux)
+{
+    int afmt = act_fmt_for(wfmt);
+    if (afmt < 0 || K % 256 != 0 || M < 0 || F < 0) return ORC_BAD;
+    int64_t wr = wrow_bytes(wfmt, K), xr = xrow_bytes(afmt, K);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t f = 0; f < F; f++) {
+            double ag, au;
+            double g = row_dot(wfmt, Wg + f * wr, X + m * xr, K, &ag);
+            double u = row_dot(wfmt, Wu + f * wr, X + m * xr, K, &au);
+            h[m * F + f] = g / (1.0 + exp(-g)) * u;
+            if (gu_aux) {
+                double* a = gu_aux + (m * F + f) * 4;
+                a[0] = g; a[1] = u; a[2] = ag; a[3] = au;
+            }
+        }
+    return ORC_OK;
+}
+
 /* --------------------------------------------------------- routed expert FFN */
 
 /* For each token t and slot s (expert e = ids[t][s], router weight w = rw[t][s]):

@@ -92,6 +92,24 @@ def test_gemv_x_validation(L):
     assert f(cq.Q8_0, 0, 8, 256, None, None, None, None) == cq.OK
 
 
+def test_gemv_swiglu_validation(L):
+    f = cq.cq_gemv_swiglu
+    assert f(99, 1, 8, 256, A, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q8_1, 1, 8, 256, A, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q4_K, 17, 8, 256, A, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q4_K, 0, 8, 256, A, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q4_K, 1, 0, 256, A, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q4_K, 1, 8, 100, A, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q8_0, 1, 8, 65536, A, A, A, A) == cq.ERR_SHAPE        # 1024 chunks > 512
+    assert f(cq.Q4_K, 1, 8, 256, None, A, A, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_K, 1, 8, 256, A, None, A, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_K, 1, 8, 256, A, A, A, None) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_K, 1, 8, 256, A + 4, A, A, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_K, 1, 8, 256, A, A + 8, A, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_K, 1, 8, 256, A, A, A + 2, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_K, 1, 8, 256, A, A, A, A + 4) == cq.ERR_ALIGNMENT
+
+
 def test_selftest_validation(L):
     assert cq.cq_selftest_wait_timeout(10)[0] == cq.ERR_INVALID_ARG
     assert cq.cq_selftest_wait_timeout(2_000_000_000)[0] == cq.ERR_INVALID_ARG

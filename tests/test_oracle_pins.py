@@ -396,3 +396,68 @@ def test_moe_rejects_bad_ids(orc):
     bad[0, 0] = Wg.shape[0]
     with pytest.raises(ValueError):
         orc.moe(Wg, Wu, Wd, bad, rw, xq, K, F)
+
+
+# ------------------------------------------------------------- dense SwiGLU
+def _fmt_name(wfmt):
+    return {2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k"}[wfmt]
+
+
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12])
+def test_swiglu_brute_force(orc, wfmt):
+    """h = silu(g) * u with g, u from an element-wise dequantize-and-sum (exact
+    rationals) evaluation, silu from math.exp; the gate goes through silu, the
+    up projection does not (a swapped pair fails: silu(u) * g != silu(g) * u)."""
+    rng = np.random.default_rng(200 + wfmt)
+    K, F, M = 512, 5, 2
+    Wg = synth.GEN[_fmt_name(wfmt)](rng, F, K)
+    Wu = synth.GEN[_fmt_name(wfmt)](rng, F, K)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    xq = orc.quantize(orc.ACT_FOR[wfmt], x)
+    h, aux = orc.swiglu(wfmt, Wg, Wu, xq, K)
+    for m in range(M):
+        for f in range(F):
+            g = float(_exact_dot(orc, wfmt, Wg[f], xq[m], K))
+            u = float(_exact_dot(orc, wfmt, Wu[f], xq[m], K))
+            if wfmt == 3:
+                # the block formula's offset term uses the stored s_x (see test_brute_force_tiny)
+                g, u = aux[m, f, 0], aux[m, f, 1]
+            assert aux[m, f, 0] == pytest.approx(g, rel=1e-12, abs=1e-12)
+            assert aux[m, f, 1] == pytest.approx(u, rel=1e-12, abs=1e-12)
+            assert h[m, f] == pytest.approx(g / (1.0 + math.exp(-g)) * u, rel=1e-12, abs=1e-300)
+
+
+def test_swiglu_odd_part_identity(orc):
+    """silu(g) - silu(-g) = g for every g. Negating every Q8_0 gate quant negates g
+    exactly, so h(W_gate) - h(-W_gate) = g * u -- a property of the definition
+    that a sign slip in silu or a dropped factor breaks."""
+    rng = np.random.default_rng(7)
+    K, F, M = 768, 9, 3
+    Wg = synth.GEN["q8_0"](rng, F, K)
+    Wu = synth.GEN["q8_0"](rng, F, K)
+    blocks = Wg.reshape(F, K // 32, 34).copy()
+    q = blocks[:, :, 2:].view(np.int8)
+    neg = blocks.copy()
+    neg[:, :, 2:] = (-q.astype(np.int16)).astype(np.int8).view(np.uint8)     # |q| <= 127: exact
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    xq = orc.quantize(orc.Q8_0, x)
+    h1, aux = orc.swiglu(orc.Q8_0, Wg, Wu, xq, K)
+    h2, aux2 = orc.swiglu(orc.Q8_0, neg.reshape(F, -1), Wu, xq, K)
+    assert np.array_equal(aux2[..., 0], -aux[..., 0])
+    gu = aux[..., 0] * aux[..., 1]
+    np.testing.assert_allclose(h1 - h2, gu, rtol=1e-12, atol=1e-12 * np.abs(gu).max())
+
+
+@pytest.mark.parametrize("which", ["gate", "up"])
+def test_swiglu_zero_scales_give_zero(orc, which):
+    """Zero gate scales give g = 0 and silu(0) = 0; zero up scales give u = 0."""
+    rng = np.random.default_rng(11)
+    K, F = 512, 6
+    Wg = synth.GEN["q4_k"](rng, F, K)
+    Wu = synth.GEN["q4_k"](rng, F, K)
+    target = (Wg if which == "gate" else Wu).reshape(F, K // 256, 144)
+    target[:, :, 0:4] = 0                # d and dmin
+    x = rng.standard_normal((2, K)).astype(np.float32)
+    xq = orc.quantize(orc.Q8_K, x)
+    h, _ = orc.swiglu(orc.Q4_K, Wg, Wu, xq, K)
+    assert np.all(h == 0)
