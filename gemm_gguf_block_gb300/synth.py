@@ -20,8 +20,13 @@ Byte layouts (little endian, fp16 = IEEE binary16), element i of a 32-block:
   group g uses qs[32g:32g+32], low nibbles for elements 64g..64g+31 (sub-block
   2g), high nibbles for 64g+32..64g+63 (sub-block 2g+1); six-bit scale and min
   of sub-block j packed in scales[12] as described in ``pack_q4_k``.
+* Q6_K, 210 B per 256: ql[128], qh[64], scales[16] int8, d f16; element i
+  (half h = i // 128, quadrant q = i % 128 // 32, l = i % 32) has its low four
+  bits in ql[64h + l + 32 (q & 1)] (low nibble for q < 2, high for q >= 2)
+  and its high two bits in qh[32h + l] bits 2q, 2q+1; sub-block i // 16 has
+  scale scales[i // 16].
 
-Field order of Q4_K and Q8_0 follows alice-llm's "Quantization Block Specs"
+Field order of Q4_K, Q6_K and Q8_0 follows alice-llm's "Quantization Block Specs"
 table; the nibble order and the Q4_0/Q4_1 layouts are the standard GGUF ones
 (the pages name the formats without printing them).
 """
@@ -115,6 +120,25 @@ def gen_q4_0(rng, N: int, K: int, scale: float = 0.01) -> np.ndarray:
     return pack_q4_0(d, q)
 
 
+def pack_q6_k(d_bits, sc, q) -> np.ndarray:
+    """Pack Q6_K superblocks. d_bits: [N, ns] uint16; sc: [N, ns, 16] ints
+    -128..127; q: [N, ns*256] ints 0..63 (the six-bit quants)."""
+    N, ns = d_bits.shape
+    qq = q.reshape(N, ns, 2, 4, 32).astype(np.uint8)      # [half][quadrant][l]
+    out = np.zeros((N, ns, 210), np.uint8)
+    lo = qq & 15
+    ql = np.zeros((N, ns, 2, 64), np.uint8)
+    ql[..., 0:32] = lo[:, :, :, 0, :] | (lo[:, :, :, 2, :] << 4)
+    ql[..., 32:64] = lo[:, :, :, 1, :] | (lo[:, :, :, 3, :] << 4)
+    hi = qq >> 4
+    qh = hi[:, :, :, 0, :] | (hi[:, :, :, 1, :] << 2) | (hi[:, :, :, 2, :] << 4) | (hi[:, :, :, 3, :] << 6)
+    out[:, :, 0:128] = ql.reshape(N, ns, 128)
+    out[:, :, 128:192] = qh.reshape(N, ns, 64)
+    out[:, :, 192:208] = sc.astype(np.int8).view(np.uint8)
+    out[:, :, 208:210] = d_bits.astype("<u2").reshape(N, ns, 1).view(np.uint8)
+    return out.reshape(N, ns * 210)
+
+
 def gen_q4_1(rng, N: int, K: int, scale: float = 0.01) -> np.ndarray:
     nb = K // QK
     d = _f16_bits(np.abs(rng.standard_normal((N, nb))) * scale)
@@ -140,8 +164,16 @@ def gen_q4_k(rng, N: int, K: int, scale: float = 0.01) -> np.ndarray:
     return pack_q4_k(d, dmin, sc, mn, q)
 
 
-GEN = {"q4_0": gen_q4_0, "q4_1": gen_q4_1, "q8_0": gen_q8_0, "q4_k": gen_q4_k}
-ACT_FOR = {"q4_0": "q8_0", "q8_0": "q8_0", "q4_1": "q8_1", "q4_k": "q8_k"}
+def gen_q6_k(rng, N: int, K: int, scale: float = 0.001) -> np.ndarray:
+    ns = K // QK_K
+    d = _f16_bits(np.abs(rng.standard_normal((N, ns))) * scale)
+    sc = rng.integers(-64, 64, size=(N, ns, 16), dtype=np.int8)
+    q = rng.integers(0, 64, size=(N, K), dtype=np.uint8)
+    return pack_q6_k(d, sc, q)
+
+
+GEN = {"q4_0": gen_q4_0, "q4_1": gen_q4_1, "q8_0": gen_q8_0, "q4_k": gen_q4_k, "q6_k": gen_q6_k}
+ACT_FOR = {"q4_0": "q8_0", "q8_0": "q8_0", "q4_1": "q8_1", "q4_k": "q8_k", "q6_k": "q8_k"}
 
 
 def gen_weights(fmt: str, rng, N: int, K: int) -> np.ndarray:

@@ -12,7 +12,12 @@
  *  - cera README, "Quantization": weights in Q4_0/Q4_1/Q8_0/Q4_K, activations
  *    quantized dynamically to Q8_0 for an integer GEMV.
  *  - alice-llm docs, "Quantization Block Specs" table: Q4_K = d(f16) + dmin(f16)
- *    + scales[12] + qs[128] per 256 elements; Q8_0 = d(f16) + qs[32].
+ *    + scales[12] + qs[128] per 256 elements; Q8_0 = d(f16) + qs[32]; Q6_K =
+ *    ql[128] + qh[64] + scales[16] + d(f16) per 256 elements (210 bytes).
+ *  - alice-llm docs, "aarch64 NEON Quantized Matvec Bench", design notes: the
+ *    Q6_K six-bit quants are assembled from ql and qh, qh's bit pairs feeding
+ *    the four quadrants; "Computation Path (Q4_K)" item 2: Q6_K x Q8_K is an
+ *    integer dot, multiplied out only at the scales.
  *  - alice-llm docs, "Computation Path (Q4_K)": quantize the input to Q8_K
  *    (256 elements, f32 scale, i8 values, i16 block sums); 8 sub-blocks x 32
  *    integer accumulation with 6-bit packed scales and mins; result
@@ -29,6 +34,11 @@
  *    x * (1/d) clamped to [-127, 127], d stored as fp16 (round to nearest
  *    even) for Q8_0/Q8_1 and as fp32 for Q8_K; Q8_1 also stores
  *    s = fp16(d * sum(q)) and the Q4_1 x Q8_1 dot uses s for its offset term.
+ *  - Q6_K element order: the standard GGUF one. Half h = i / 128 of the
+ *    superblock, quadrant q = (i % 128) / 32, l = i % 32: low four bits from
+ *    ql[64h + l + 32(q & 1)] (low nibble for q < 2, high for q >= 2), high
+ *    two bits from qh[32h + l] bits 2q, 2q+1; value = d * scales[i / 16] *
+ *    (q6 - 32) with int8 scales.
  *  - Quantization decisions are taken in fp32, the precision the pages'
  *    quantizer works in. Everything after the integer block dots is fp64.
  *
@@ -40,7 +50,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_Q4_0 = 2, ORC_Q4_1 = 3, ORC_Q8_0 = 8, ORC_Q8_1 = 9, ORC_Q4_K = 12, ORC_Q8_K = 15 };
+enum { ORC_Q4_0 = 2, ORC_Q4_1 = 3, ORC_Q8_0 = 8, ORC_Q8_1 = 9, ORC_Q4_K = 12, ORC_Q6_K = 14, ORC_Q8_K = 15 };
 enum { ORC_OK = 0, ORC_BAD = -1 };
 
 /* ------------------------------------------------------------------ binary16 */
@@ -185,6 +195,16 @@ static int nib256(const uint8_t* qs, int i)
     return r < 32 ? (qs[32 * g + r] & 15) : (qs[32 * g + r - 32] >> 4);
 }
 
+/* Six-bit quant (0..63) of element i (0..255) of a Q6_K superblock. */
+static int q6k_quant(const uint8_t* blk, int i)
+{
+    int h = i / 128, q = (i % 128) / 32, l = i % 32;
+    int b = blk[64 * h + l + 32 * (q & 1)];
+    int lo = q < 2 ? (b & 15) : (b >> 4);
+    int hi = (blk[128 + 32 * h + l] >> (2 * q)) & 3;
+    return lo | (hi << 4);
+}
+
 /* Dequantized value of element k of a weight row, in fp64 (exact). */
 double oracle_weight_value(int fmt, const uint8_t* row, int64_t k)
 {
@@ -197,6 +217,11 @@ double oracle_weight_value(int fmt, const uint8_t* row, int64_t k)
         int i = (int)(k % 256), sc, mn;
         oracle_q4k_scale_min(b + 4, i / 32, &sc, &mn);
         return rd_h(b) * sc * nib256(b + 16, i) - rd_h(b + 2) * mn;
+    }
+    case ORC_Q6_K: {
+        const uint8_t* b = row + (k / 256) * 210;
+        int i = (int)(k % 256);
+        return rd_h(b + 208) * (int8_t)b[192 + i / 16] * (q6k_quant(b, i) - 32);
     }
     }
     return NAN;
@@ -269,6 +294,22 @@ static double row_dot(int wfmt, const uint8_t* w, const uint8_t* x, int64_t K, d
             y += t1 - t2;
             at += fabs(t1) + fabs(t2);
         }
+    } else if (wfmt == ORC_Q6_K) {
+        /* per superblock: isum = sum_j sc_j * sum_{i in sub-block j} (q6_i - 32) * qx_i */
+        for (int64_t s = 0; s < K / 256; s++) {
+            const uint8_t* wbk = w + s * 210;
+            const uint8_t* xbk = x + s * 292;
+            int64_t isum = 0;
+            for (int j = 0; j < 16; j++) {
+                int64_t sj = 0;
+                for (int i = 16 * j; i < 16 * j + 16; i++)
+                    sj += (int64_t)(q6k_quant(wbk, i) - 32) * (int8_t)xbk[4 + i];
+                isum += (int64_t)(int8_t)wbk[192 + j] * sj;
+            }
+            double t = (double)rd_f32(xbk) * rd_h(wbk + 208) * (double)isum;
+            y += t;
+            at += fabs(t);
+        }
     }
     *absterms = at;
     return y;
@@ -281,6 +322,7 @@ static int64_t wrow_bytes(int fmt, int64_t K)
     case ORC_Q4_1: return K / 32 * 20;
     case ORC_Q8_0: return K / 32 * 34;
     case ORC_Q4_K: return K / 256 * 144;
+    case ORC_Q6_K: return K / 256 * 210;
     }
     return -1;
 }
@@ -290,7 +332,7 @@ static int act_fmt_for(int wfmt)
     switch (wfmt) {
     case ORC_Q4_0: case ORC_Q8_0: return ORC_Q8_0;
     case ORC_Q4_1: return ORC_Q8_1;
-    case ORC_Q4_K: return ORC_Q8_K;
+    case ORC_Q4_K: case ORC_Q6_K: return ORC_Q8_K;
     }
     return -1;
 }

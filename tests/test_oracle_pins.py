@@ -74,7 +74,7 @@ def test_half_encode_matches_numpy(orc):
 
 
 # ------------------------------------------------------------- block decoding
-FMT = {"q4_0": 2, "q4_1": 3, "q8_0": 8, "q4_k": 12}
+FMT = {"q4_0": 2, "q4_1": 3, "q8_0": 8, "q4_k": 12, "q6_k": 14}
 
 
 @pytest.mark.parametrize("rec", _records("blocks.txt"), ids=lambda r: r["name"])
@@ -114,6 +114,17 @@ def test_generator_packs_fixture_layouts():
     hi = [1, 3, 5, 7, 9, 11, 13, 15, 0, 2, 4, 6, 8, 10, 12, 14]
     packed = synth.pack_q4_0(np.array([[0x3800]], np.uint16), np.array([lo + hi]))
     assert np.array_equal(packed[0], raw40)
+    # Q6_K: ql[i] = i, every qh byte 0xe4, scales[j] = j - 8, d = 1.0, worked
+    # back into six-bit quants element by element from the fixture's layout.
+    raw6 = np.array([int(b, 16) for b in recs["q6_k_quadrants"]["bytes"].split()], np.uint8)
+    q6 = np.zeros(256, int)
+    for i in range(256):
+        h, qd, l = i // 128, (i % 128) // 32, i % 32
+        b = 64 * h + l + 32 * (qd & 1)
+        q6[i] = (b & 15 if qd < 2 else b >> 4) | (qd << 4)
+    packed = synth.pack_q6_k(np.array([[0x3C00]], np.uint16), (np.arange(16) - 8).reshape(1, 1, 16),
+                             q6.reshape(1, 256))
+    assert np.array_equal(packed[0], raw6)
 
 
 def test_q4k_scale_packing_roundtrip(orc):
@@ -232,7 +243,7 @@ def test_constant_nibble_q4_0(orc):
             assert abs(Fraction(y[0, n]) - want[n]) <= abs(want[n]) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 200)
 
 
-@pytest.mark.parametrize("wfmt", [2, 3, 8, 12])
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 14])
 def test_one_hot_activation(orc, wfmt):
     """x = e_k: the block holding k has d_x = fp16(1/127) (Q8_K: fp32 1/127), q_k = 127 and
     all other quants 0, so y_n = d_x * 127 * W[n,k] exactly -- plus, for Q4_1, the offset
@@ -240,7 +251,7 @@ def test_one_hot_activation(orc, wfmt):
     inside the value formula."""
     rng = np.random.default_rng(wfmt)
     K, N = 512, 7
-    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k"}[wfmt]](rng, N, K)
+    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 14: "q6_k"}[wfmt]](rng, N, K)
     afmt = orc.ACT_FOR[wfmt]
     for k in (0, 31, 100, 511):
         x = np.zeros((1, K), np.float32)
@@ -263,14 +274,17 @@ def test_one_hot_activation(orc, wfmt):
             assert y[0, n] == pytest.approx(want, rel=1e-14, abs=1e-300)
 
 
-@pytest.mark.parametrize("wfmt", [2, 3, 8, 12])
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 14])
 def test_zero_scales_give_zero(orc, wfmt):
     rng = np.random.default_rng(3)
     K, N = 512, 4
-    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k"}[wfmt]](rng, N, K)
+    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 14: "q6_k"}[wfmt]](rng, N, K)
     bs, bb = orc.BLOCK[wfmt]
     Wz = W.copy().reshape(N, K // bs, bb)
-    Wz[:, :, 0:2] = 0                   # d
+    if wfmt == 14:
+        Wz[:, :, 208:210] = 0           # Q6_K: d is the last field
+    else:
+        Wz[:, :, 0:2] = 0               # d
     if wfmt in (3, 12):
         Wz[:, :, 2:4] = 0               # m / dmin
     x = rng.standard_normal((2, K)).astype(np.float32)
@@ -286,7 +300,7 @@ def _exact_dot(orc, wfmt, wrow, xrow, K):
                for k in range(K))
 
 
-@pytest.mark.parametrize("wfmt", [2, 3, 8, 12])
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 14])
 def test_brute_force_tiny(orc, wfmt):
     """Dequantize every element and sum exactly; compare with the block formula.
 
@@ -294,7 +308,7 @@ def test_brute_force_tiny(orc, wfmt):
     for the offset term, so the exact reference replaces m_w d_x sum(q_x) by m_w s_x."""
     rng = np.random.default_rng(100 + wfmt)
     K, N, M = 512, 6, 3
-    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k"}[wfmt]](rng, N, K)
+    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 14: "q6_k"}[wfmt]](rng, N, K)
     x = rng.standard_normal((M, K)).astype(np.float32)
     afmt = orc.ACT_FOR[wfmt]
     xq = orc.quantize(afmt, x)
