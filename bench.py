@@ -12,7 +12,8 @@ them from HBM.
 Also printed in the same JSON line: the prefill GEMM (Q4_K, M=512, K=4096,
 N=14336) in int8-equivalent TOPS, the routed-expert FFN and the Q4_1 LM head at
 M = 1/4/8/16, the single-call latency of the small Q4_0 GEMV, the fused dense
-SwiGLU gate + up projection (Q4_K 14336x4096 each, M = 1/4), the roofline of
+SwiGLU gate + up projection (Q4_K 14336x4096 each, M = 1/4), the Q6_K
+tied-embedding LM head (128256x2048, M = 1/4), the roofline of
 the dominant kernel, the CPU oracle's rate on the host cores, and the
 end-to-end rate with host buffers.
 
@@ -343,6 +344,20 @@ def case_swiglu(c, cq, synth, peaks, seed, ms_list=(1, 4)):
     return res
 
 
+def case_lm_head_q6k(c, cq, synth, peaks, seed, ms_list=(1, 4)):
+    """Tied-embedding LM head in Q6_K: 128256x2048 (Llama-3.2-1B) at M tokens."""
+    W, x = synth.lm_head_q6_k(seed)
+    N, K = W.shape[0], x.shape[1]
+    Wd = c.dev(W)
+    xq = cq.quantize_act_t(c.dev(x), cq.Q8_K)
+    res = {"shape": f"N={N} K={K}"}
+    for M in ms_list:
+        y = c.torch.empty((M, N), dtype=c.torch.float32, device="cuda")
+        ms = c.time(lambda: cq.cq_gemv(cq.Q6_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
+        res[str(M)] = {"ms": ms, "weight_gbs": W.nbytes / ms / 1e6, "hbm_frac": W.nbytes / ms / 1e6 / peaks["hbm"]}
+    return res
+
+
 def case_q4_0_small(c, cq, synth, peaks, seed):
     """Small Q4_0 GEMV 2048x2048 (2.4 MB, fits in L2): the device time of one
     call, and the rate over 256 distinct copies (576 MiB > L2) replayed
@@ -384,7 +399,7 @@ def case_q4_0_small(c, cq, synth, peaks, seed):
 
 
 CASES = {"prefill_gemm_q4_k": case_gemm, "moe_q4_0": case_moe, "lm_head_q4_1": case_lm_head,
-         "decode_q4_0_2048": case_q4_0_small, "ffn_swiglu_q4_k": case_swiglu}
+         "decode_q4_0_2048": case_q4_0_small, "ffn_swiglu_q4_k": case_swiglu, "lm_head_q6_k": case_lm_head_q6k}
 
 
 def secondary(torch, cq, synth, peaks, seed):
@@ -404,7 +419,7 @@ def run_case(args):
     c = _Ctx(torch, iters=args.steps, warmup=args.warmup)
     fn = CASES[args.case]
     kw = {}
-    if args.case in ("lm_head_q4_1", "ffn_swiglu_q4_k") and args.m:
+    if args.case in ("lm_head_q4_1", "ffn_swiglu_q4_k", "lm_head_q6_k") and args.m:
         kw["ms_list"] = tuple(int(v) for v in args.m.split(","))
     r = fn(c, cq, synth, _peaks(), args.seed, **kw)
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup, "result": r}))

@@ -26,7 +26,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // token's row is only 4-byte aligned; the kernels read activations in 32-bit words.
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-bool is_weight_fmt(int f) { return f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0 || f == CQ_Q4_K; }
+bool is_weight_fmt(int f) { return f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0 || f == CQ_Q4_K || f == CQ_Q6_K; }
+// Q6_K rows of 210-byte superblocks meet the bulk copies' 16-byte rule only
+// eight superblocks at a time: K a multiple of 2048.
+bool fmt_shape_ok(int f, int64_t K) { return f != CQ_Q6_K || K % 2048 == 0; }
 bool is_act_fmt(int f) { return f == CQ_Q8_0 || f == CQ_Q8_1 || f == CQ_Q8_K; }
 
 // Largest K accepted by the single-pass kernels (activation rows staged in
@@ -109,7 +112,7 @@ cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     if (!is_weight_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
     cq_status st = check_shape(M, N, K);
     if (st != CQ_OK) return st;
-    if (M > 16) return CQ_ERR_SHAPE;
+    if (M > 16 || !fmt_shape_ok(w_fmt, K)) return CQ_ERR_SHAPE;
     if (M == 0 || N == 0) return CQ_OK;
     if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
     if (!aligned16(W) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
@@ -131,7 +134,7 @@ cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void
     if (!is_weight_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
     cq_status st = check_shape(M, N, K);
     if (st != CQ_OK) return st;
-    if (M > 16) return CQ_ERR_SHAPE;
+    if (M > 16 || !fmt_shape_ok(w_fmt, K)) return CQ_ERR_SHAPE;
     if (M == 0) return CQ_OK;
     if (x == nullptr || xq == nullptr || (N > 0 && (W == nullptr || y == nullptr))) return CQ_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(xq) || (N > 0 && (!aligned16(W) || !aligned16(y)))) return CQ_ERR_ALIGNMENT;
@@ -147,8 +150,8 @@ cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const
     if (!is_weight_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
     cq_status st = check_shape(M, F, K);
     if (st != CQ_OK) return st;
-    if (M < 1 || M > 16 || F < 1) return CQ_ERR_SHAPE;
-    const int64_t ce = w_fmt == CQ_Q4_K ? 256 : 128;
+    if (M < 1 || M > 16 || F < 1 || !fmt_shape_ok(w_fmt, K)) return CQ_ERR_SHAPE;
+    const int64_t ce = w_fmt == CQ_Q4_K || w_fmt == CQ_Q6_K ? 256 : 128;
     if (2 * (K / ce) > 512) return CQ_ERR_SHAPE;
     if (W_gate == nullptr || W_up == nullptr || xq == nullptr || h == nullptr) return CQ_ERR_INVALID_ARG;
     if (!aligned16(W_gate) || !aligned16(W_up) || !aligned4(xq) || !aligned16(h)) return CQ_ERR_ALIGNMENT;

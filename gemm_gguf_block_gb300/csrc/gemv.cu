@@ -34,12 +34,15 @@ namespace {
 constexpr int WPC_MAX = 16;       // warps per CTA (one CTA per SM)
 constexpr int CBUF_FLOATS = 512;  // per-warp buffer of chunk values (2 KB)
 
-// Weight chunk bytes, chunk elements, staged activation chunk pitch.
+// Weight chunk bytes, chunk elements, staged activation chunk pitch, and the
+// 32-bit words a lane holds the chunk in (Q6_K's 210 bytes: 53).
 template <int WF> struct G;
-template <> struct G<CQ_Q8_0> { static constexpr int WCH = 136, CE = 128, ACP = 144; };
-template <> struct G<CQ_Q4_0> { static constexpr int WCH = 72, CE = 128, ACP = 144; };
-template <> struct G<CQ_Q4_1> { static constexpr int WCH = 80, CE = 128, ACP = 176; };
-template <> struct G<CQ_Q4_K> { static constexpr int WCH = 144, CE = 256, ACP = 304; };
+template <> struct G<CQ_Q8_0> { static constexpr int WCH = 136, CE = 128, ACP = 144, WR = 34; };
+template <> struct G<CQ_Q4_0> { static constexpr int WCH = 72, CE = 128, ACP = 144, WR = 18; };
+template <> struct G<CQ_Q4_1> { static constexpr int WCH = 80, CE = 128, ACP = 176, WR = 20; };
+template <> struct G<CQ_Q4_K> { static constexpr int WCH = 144, CE = 256, ACP = 304, WR = 36; };
+template <> struct G<CQ_Q6_K> { static constexpr int WCH = 210, CE = 256, ACP = 336, WR = 53; };
+template <int WF> __host__ __device__ constexpr bool superblock_fmt() { return WF == CQ_Q4_K || WF == CQ_Q6_K; }
 
 struct GemvParams {
     const uint8_t* W;
@@ -93,11 +96,12 @@ __device__ __forceinline__ void ld_f4(const uint8_t* p, float* f) {
 
 // ------------------------------------------------------- staging of activations
 // Q8_0 / Q8_1 chunk of 4 blocks -> [qs 128 B][d0..d3 fp32] (Q8_1: [d,s] pairs);
-// Q8_K superblock -> [qs 256 B][d fp32 @256][8 int32 bsum pairs @272].
+// Q8_K superblock -> [qs 256 B][d fp32 @256][8 int32 bsum pairs @272] for
+// Q4_K, [16 int32 bsums @272] for Q6_K (its sub-blocks are 16 elements).
 template <int WF>
 __device__ void stage_activations(const GemvParams& p, uint8_t* act) {
     const int nthr = blockDim.x;
-    if constexpr (WF == CQ_Q4_K) {
+    if constexpr (superblock_fmt<WF>()) {
         const int ns = p.nca;
         const int words = p.M * ns * 73;          // 292 bytes per superblock
         const uint32_t* src = reinterpret_cast<const uint32_t*>(p.xq);
@@ -111,10 +115,14 @@ __device__ void stage_activations(const GemvParams& p, uint8_t* act) {
             } else if (w <= 64) {
                 *reinterpret_cast<uint32_t*>(dst + 4 * (w - 1)) = v;
             } else {
-                const int j = w - 65;                    // bsum pair j = bsum[2j] + bsum[2j+1]
-                const int pair = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
-                                 static_cast<int>(static_cast<int16_t>(v >> 16));
-                *reinterpret_cast<int*>(dst + 272 + 4 * j) = pair;
+                const int j = w - 65;                    // bsum[2j] and bsum[2j+1]
+                const int b0 = static_cast<int16_t>(v & 0xffffu), b1 = static_cast<int16_t>(v >> 16);
+                if constexpr (WF == CQ_Q6_K) {
+                    reinterpret_cast<int*>(dst + 272)[2 * j] = b0;
+                    reinterpret_cast<int*>(dst + 272)[2 * j + 1] = b1;
+                } else {
+                    *reinterpret_cast<int*>(dst + 272 + 4 * j) = b0 + b1;
+                }
             }
         }
     } else {
@@ -150,7 +158,7 @@ __device__ void stage_activations_x(const GemvParams& p, uint8_t* act) {
     const int nthr = blockDim.x;
     const bool out = blockIdx.x == 0;
     const int64_t K = static_cast<int64_t>(p.nca) * G<WF>::CE;
-    if constexpr (WF == CQ_Q4_K) {
+    if constexpr (superblock_fmt<WF>()) {
         // A warp per superblock, eight consecutive elements per lane.
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nthr >> 5;
         const int ns = p.nca;
@@ -180,7 +188,11 @@ __device__ void stage_activations_x(const GemvParams& p, uint8_t* act) {
             reinterpret_cast<uint32_t*>(dst + 8 * lane)[0] = packed[0];
             reinterpret_cast<uint32_t*>(dst + 8 * lane)[1] = packed[1];
             if (lane == 0) *reinterpret_cast<float*>(dst + 256) = d;
-            if ((lane & 3) == 0) *reinterpret_cast<int*>(dst + 272 + lane) = s32;
+            if constexpr (WF == CQ_Q6_K) {
+                if ((lane & 1) == 0) *reinterpret_cast<int*>(dst + 272 + 2 * lane) = s16;
+            } else {
+                if ((lane & 3) == 0) *reinterpret_cast<int*>(dst + 272 + lane) = s32;
+            }
             if (out) {
                 uint8_t* blk = p.xq_out + static_cast<int64_t>(sb) * 292;
                 uint32_t* qw = reinterpret_cast<uint32_t*>(blk + 4 + 8 * lane);
@@ -447,11 +459,69 @@ __device__ __forceinline__ void chunk_q4_k(const uint32_t (&w)[36], const uint8_
     }
 }
 
+// Q6_K superblock (words of the 210-byte chunk): ql at word 0, qh at word 32,
+// the sixteen int8 scales at word 48, d in the low half of word 52. Sub-block
+// j (16 elements) lies in half h = j / 8, quadrant q = (j / 2) % 4, elements
+// l = 16 (j % 2) .. +15 of that quadrant; four consecutive elements' six-bit
+// quants are one word: the ql nibbles (low for q < 2, high otherwise) or'd
+// with qh's bit pair q moved to bits 4-5 of each byte. Per sub-block
+// S_j = sum q6 * q8 - 32 * bsum_j exactly; isum = sum_j sc_j S_j; the chunk
+// value is t = D(d) * (float)isum, folded into y as fma(d_x, t, y).
+template <int MT>
+__device__ __forceinline__ void chunk_q6_k(const uint32_t (&w)[53], const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    int isum[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) isum[m] = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int h = j >> 3, q = (j >> 1) & 3, l0 = 16 * (j & 1);
+        int v[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int l = l0 + 4 * p;
+            const uint32_t qlw = w[16 * h + (l >> 2) + 8 * (q & 1)];
+            const uint32_t lo = q < 2 ? (qlw & 0x0f0f0f0fu) : ((qlw >> 4) & 0x0f0f0f0fu);
+            const uint32_t hi = ((w[32 + 8 * h + (l >> 2)] >> (2 * q)) & 0x03030303u) << 4;
+            v[p] = static_cast<int>(lo | hi);
+        }
+        const int sc = static_cast<int>(static_cast<int8_t>((w[48 + (j >> 2)] >> (8 * (j & 3))) & 0xffu));
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < M) {
+                const uint8_t* xm = xa + m * tp;
+                const uint4 a = lds128(xm + 16 * j);
+                int sj = __dp4a(v[0], static_cast<int>(a.x), 0);
+                sj = __dp4a(v[1], static_cast<int>(a.y), sj);
+                sj = __dp4a(v[2], static_cast<int>(a.z), sj);
+                sj = __dp4a(v[3], static_cast<int>(a.w), sj);
+                sj -= 32 * reinterpret_cast<const int*>(xm + 272)[j];
+                isum[m] += sc * sj;
+            }
+        }
+    }
+    const float d = h2f(w[52]);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) c[m] = __fmul_rn(d, __int2float_rn(isum[m]));
+}
+
 // The weight chunk, copied from its stage to registers (so the stage can be
 // refilled while the chunk value is formed).
 template <int WF>
-__device__ __forceinline__ void chunk_load(const uint8_t* wc, uint32_t (&w)[G<WF>::WCH / 4]) {
-    if constexpr (WF == CQ_Q4_K) {
+__device__ __forceinline__ void chunk_load(const uint8_t* wc, uint32_t (&w)[G<WF>::WR]) {
+    if constexpr (WF == CQ_Q6_K) {
+        // 210-byte chunks sit on 2-byte boundaries: 54 aligned words, each
+        // pair funnel-shifted by the chunk's offset (0 or 16 bits).
+        const uintptr_t a = reinterpret_cast<uintptr_t>(wc);
+        const uint32_t* base = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+        const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+        uint32_t prev = base[0];
+#pragma unroll
+        for (int i = 0; i < 53; ++i) {
+            const uint32_t next = base[i + 1];
+            w[i] = __funnelshift_r(prev, next, sh);
+            prev = next;
+        }
+    } else if constexpr (WF == CQ_Q4_K) {
 #pragma unroll
         for (int i = 0; i < 9; ++i) {
             const uint4 v = lds128(wc + 16 * i);
@@ -463,10 +533,11 @@ __device__ __forceinline__ void chunk_load(const uint8_t* wc, uint32_t (&w)[G<WF
 }
 
 template <int WF, int MT, class X>
-__device__ __forceinline__ void chunk_value(const uint32_t (&wc)[G<WF>::WCH / 4], const X& x, int M, float (&c)[MT]) {
+__device__ __forceinline__ void chunk_value(const uint32_t (&wc)[G<WF>::WR], const X& x, int M, float (&c)[MT]) {
     if constexpr (WF == CQ_Q8_0) chunk_q8_0<MT>(wc, x, M, c);
     else if constexpr (WF == CQ_Q4_0) chunk_q4_0<MT>(wc, x, M, c);
     else if constexpr (WF == CQ_Q4_1) chunk_q4_1<MT>(wc, x, M, c);
+    else if constexpr (WF == CQ_Q6_K) chunk_q6_k<MT>(wc, x.xa, x.tp, M, c);
     else chunk_q4_k<MT>(wc, x.xa, x.tp, M, c);
 }
 
@@ -477,7 +548,7 @@ __device__ __forceinline__ void chunk_value(const uint32_t (&wc)[G<WF>::WCH / 4]
 // from shared memory and run 24 warps.
 template <int WF, int MT> __host__ __device__ constexpr bool x_in_regs() { return MT == 1 && (WF == CQ_Q8_0 || WF == CQ_Q4_1); }
 template <int WF, int MT> __host__ __device__ constexpr int wpc_limit() {
-    return MT == 1 ? (WF == CQ_Q8_0 ? 16 : WF == CQ_Q4_1 ? 20 : 24) : MT <= 4 ? WPC_MAX : WPC_MAX / 2;
+    return MT == 1 ? (WF == CQ_Q8_0 || WF == CQ_Q6_K ? 16 : WF == CQ_Q4_1 ? 20 : 24) : MT <= 4 ? WPC_MAX : WPC_MAX / 2;
 }
 
 // SWI (paired): the rows are (gate row f | up row f) of two matrices, one
@@ -640,7 +711,7 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
         const int rows_valid = static_cast<int>(min(static_cast<int64_t>(p.R), p.N - row0));
         const uint8_t* st = stages + cc.stage * p.stage_bytes;
         const bool have = lr < rows_valid && lj < cn;
-        uint32_t wr[F::WCH / 4];
+        uint32_t wr[F::WR];
         if (have) chunk_load<WF>(st + woff(lr, lj), wr);
         // The stage is read: refill it before the arithmetic.
         __syncwarp();
@@ -677,7 +748,7 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
                     // The sum over chunks [j0, j0 + n) of the row, x chunks from 0.
                     auto rowsum = [&](int j0, int n) {
                         float acc = 0.0f;
-                        if constexpr (WF == CQ_Q4_K) {
+                        if constexpr (superblock_fmt<WF>()) {
                             // y = fma(d_x, t, y) per superblock, d_x from the staged activations
                             const uint8_t* xd = act + m * p.tok_pitch + 256;
 #pragma unroll 8
@@ -741,13 +812,15 @@ bool xreg_enabled() {
 // Items a warp prefetches into L2 past its ring before the dependency wait,
 // so DRAM stays busy while the preceding grids drain: 8 for Q8_0 (decode
 // step 118.9 -> 111.7 us), 4 for the 4-bit formats, whose CTAs run more
-// warps (more than that crowds the L2). CQ_GEMV_L2PF overrides.
+// warps (more than that crowds the L2), none for Q6_K, whose items of four
+// rows already fill the L2 at four (standalone LM head 41.0 us with none,
+// 43.0 with 4, 47.1 with 8). CQ_GEMV_L2PF overrides.
 int l2_prefetch_items(int w_fmt) {
     static const int v = [] {
         const char* e = std::getenv("CQ_GEMV_L2PF");
         return e ? std::max(0, std::atoi(e)) : -1;
     }();
-    return v >= 0 ? v : w_fmt == CQ_Q8_0 ? 8 : 4;
+    return v >= 0 ? v : w_fmt == CQ_Q8_0 ? 8 : w_fmt == CQ_Q6_K ? 0 : 4;
 }
 
 // Ring depth: CQ_GEMV_STAGES (2..4) overrides the choice, for tuning runs.
@@ -901,6 +974,7 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, nullptr, xq, y, x, s);
     case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, nullptr, xq, y, x, s);
     case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, nullptr, xq, y, x, s);
+    case CQ_Q6_K: return launch_gemv_fmt<CQ_Q6_K>(dev, M, N, K, W, nullptr, xq, y, x, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -913,6 +987,7 @@ cudaError_t launch_gemv_swiglu(const DeviceInfo& dev, int w_fmt, int M, int64_t 
     case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
+    case CQ_Q6_K: return launch_gemv_fmt<CQ_Q6_K>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     default: return cudaErrorInvalidValue;
     }
 }

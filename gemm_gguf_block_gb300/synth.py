@@ -241,6 +241,13 @@ def lm_head_q4_1(seed: int = 0, N: int = 128256, K: int = 4096, M: int = 16):
     return W, x
 
 
+def lm_head_q6_k(seed: int = 0, N: int = 128256, K: int = 2048, M: int = 4):
+    """Tied-embedding LM head in Q6_K (Llama-3.2-1B: vocabulary x hidden 2048)."""
+    W = gen_q6_k(stream(seed, 7, 0), N, K)
+    x = gen_x(stream(seed, 7, 1), M, K)
+    return W, x
+
+
 def ffn_swiglu_q4_k(seed: int = 0, F: int = 14336, K: int = 4096, M: int = 4):
     """Dense SwiGLU FFN gate and up projections, Q4_K [F, K] each (Llama-3-8B shapes)."""
     Wg = gen_q4_k(stream(seed, 6, 0), F, K)

@@ -9,6 +9,7 @@
  *     Q8_0            Q8_0                32 elements
  *     Q4_1            Q8_1                32 elements
  *     Q4_K            Q8_K                256 elements
+ *     Q6_K            Q8_K                256 elements (GEMV only)
  *
  * Sources (web pages on GGUF inference engines; sections by name):
  *   cera README "Quantization" (weight types; activations quantized to Q8_0
@@ -20,7 +21,13 @@
  *   Q4_1 decode matching the batched prefill GEMM bit for bit); cera README
  *   "Supported models" (lfm2moe: 4-of-32 routed experts, grouping tokens by
  *   expert as the follow-up); alice-llm "WGSL Shader Architecture" (fused
- *   gate+up SwiGLU).
+ *   gate+up SwiGLU); alice-llm "Quantization Block Specs" (Q6_K = ql[128] +
+ *   qh[64] + scales[16] + d per 256 elements), "aarch64 NEON Quantized Matvec
+ *   Bench" (qh's bit pairs feed the four quadrants) and cera README (the
+ *   tied Q6_K embedding as the LM head). Q6_K element i: half h = i/128,
+ *   quadrant q = (i%128)/32, l = i%32; low four bits in ql[64h + l + 32(q&1)]
+ *   (low nibble for q < 2, high for q >= 2), high two bits in qh[32h + l]
+ *   bits 2q, 2q+1; value = d * (int8)scales[i/16] * (q6 - 32).
  *
  * Conventions for every call:
  *   - All data pointers are DEVICE pointers owned by the caller, 16-byte
@@ -32,7 +39,9 @@
  *   - Matrices are row-major. A weight row holds the K/blk blocks of one
  *     output row contiguously (GGUF order); activations are M rows of blocks;
  *     outputs are fp32 [M][N] (token-major).
- *   - K must be a positive multiple of 256. N == 0 or M == 0 is a valid no-op.
+ *   - K must be a positive multiple of 256 (2048 for Q6_K, whose 210-byte
+ *     superblocks reach a 16-byte boundary every eight). N == 0 or M == 0 is
+ *     a valid no-op.
  *   - Arguments are validated before any launch: an error status means
  *     nothing was launched and nothing was written.
  *   - Results are deterministic and do not depend on the launch shape: each
@@ -53,6 +62,10 @@
  *                     isum_m = sum_j m_j (bsum_2j + bsum_2j+1),
  *                     t = fma(D(d), (float)isum_sc, -(D(dmin) * (float)isum_m)),
  *                     y = fma(d_x, t, y).
+ *   Q6_K, per superblock in increasing k, from y = 0:
+ *                     S_j = int dot of sub-block j (16 elements) of (q6 - 32)
+ *                     with q8, isum = sum_j sc_j S_j, t = D(d) * (float)isum,
+ *                     y = fma(d_x, t, y).
  *   Every operation rounds to nearest.
  */
 #ifndef CQ_H
@@ -72,6 +85,7 @@ typedef enum {
     CQ_Q8_0 = 8,
     CQ_Q8_1 = 9,
     CQ_Q4_K = 12,
+    CQ_Q6_K = 14,
     CQ_Q8_K = 15
 } cq_format;
 
@@ -111,7 +125,7 @@ cq_status cq_quantize_act(cq_format act_fmt, int64_t M, int64_t K, const float* 
  * (cera "Other features": the verify path projects all 1+k positions in one
  * batched pass so the head is read once; alice-llm "Batch-4 Speculative
  * Decoding": weights decoded once, one accumulator set per token).
- * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K}; xq in the paired activation format.
+ * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K, Q6_K}; xq in the paired activation format.
  * W: N rows of K/blk blocks. y: fp32 [M][N]. M > 16 returns CQ_ERR_SHAPE.
  */
 cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
@@ -137,11 +151,11 @@ cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void
  *   g = W_gate . xq,  u = W_up . xq   (each exactly as cq_gemv computes it)
  *   h[m][f] = silu(g) * u = g / (1 + exp(-g)) * u   (fp32: RN divide,
  *             RN add, RN multiply; exp is CUDA's expf)
- * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K}; xq in the paired activation format;
+ * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K, Q6_K}; xq in the paired activation format;
  * W_gate, W_up: F rows of K/blk blocks each (16-byte aligned); h: fp32
  * [M][F] (16-byte aligned). 1 <= M <= 16 (else CQ_ERR_SHAPE); F >= 1;
  * K a positive multiple of 256 with 2 * K / 128 <= 512 chunks (K <= 32768;
- * Q4_K: K <= 65536). Errors as cq_gemv. g and u never leave the kernel: one
+ * Q4_K, Q6_K: K <= 65536). Errors as cq_gemv. g and u never leave the kernel: one
  * launch reads both matrices, combines the two sums of each (row, token) and
  * writes only h.
  */

@@ -92,6 +92,16 @@ def test_gemv_x_validation(L):
     assert f(cq.Q8_0, 0, 8, 256, None, None, None, None) == cq.OK
 
 
+def test_q6k_shape_rule(L):
+    """Q6_K rows reach a 16-byte boundary only every eight superblocks: K % 2048."""
+    assert cq.cq_gemv(cq.Q6_K, 1, 8, 256, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemv(cq.Q6_K, 1, 8, 3072, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemv_x(cq.Q6_K, 1, 8, 1024, A, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemv_swiglu(cq.Q6_K, 1, 8, 512, A, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemm(cq.Q6_K, 4, 8, 2048, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert cq.cq_gemv(cq.Q6_K, 0, 8, 2048, None, None, None) == cq.OK
+
+
 def test_gemv_swiglu_validation(L):
     f = cq.cq_gemv_swiglu
     assert f(99, 1, 8, 256, A, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT

@@ -10,6 +10,7 @@ oracle on sampled outputs.
   calls equal bit for bit, and sampled tokens equal to their cq_gemv rows.
 * Q4_1 LM head 128256 x 4096 at M = 1, 4, 8, 16: the oracle on sampled rows;
   every row of an M>1 call bitwise equal to the M=1 call of that position.
+* Q6_K tied-embedding LM head 128256 x 2048 at M = 1 and 4, the same checks.
 """
 import numpy as np
 import pytest
@@ -98,3 +99,22 @@ def test_lm_head_q4_1_batched(orc):
         y = cq.gemv_t(Wd, xq[:M], cq.Q4_1, K).cpu().numpy()
         for m in range(M):
             assert np.array_equal(y[m].view(np.uint32), single[m].view(np.uint32)), f"M={M} row {m}"
+
+
+def test_lm_head_q6_k(orc):
+    torch = torch_cuda()
+    cq = cq_built()
+    W, x = synth.lm_head_q6_k(0)
+    K = x.shape[1]
+    N = W.shape[0]
+    Wd = dev(torch, W)
+    xq = cq.quantize_act_t(dev(torch, x), cq.Q8_K)
+    xq_np = xq.cpu().numpy()
+    assert np.array_equal(xq_np, orc.quantize(orc.Q8_K, x))
+    single = [cq.gemv_t(Wd, xq[m:m + 1], cq.Q6_K, K).cpu().numpy()[0] for m in range(4)]
+    idx = _rows(N)
+    y_ref, at = _oracle_rows(orc, cq.Q6_K, W, xq_np, K, idx)
+    assert_within(np.stack(single)[:, idx], y_ref, at, what="q6_k lm head")
+    y = cq.gemv_t(Wd, xq[:4], cq.Q6_K, K).cpu().numpy()
+    for m in range(4):
+        assert np.array_equal(y[m].view(np.uint32), single[m].view(np.uint32)), f"M=4 row {m}"
