@@ -20,13 +20,16 @@ Byte layouts (little endian, fp16 = IEEE binary16), element i of a 32-block:
   group g uses qs[32g:32g+32], low nibbles for elements 64g..64g+31 (sub-block
   2g), high nibbles for 64g+32..64g+63 (sub-block 2g+1); six-bit scale and min
   of sub-block j packed in scales[12] as described in ``pack_q4_k``.
+* Q5_K, 176 B per 256: d f16, dmin f16, scales[12], qh[32], qs[128]; the
+  low four bits and the scale/min packing as Q4_K, the fifth bit of element
+  i in qh[i % 32], bit i // 32.
 * Q6_K, 210 B per 256: ql[128], qh[64], scales[16] int8, d f16; element i
   (half h = i // 128, quadrant q = i % 128 // 32, l = i % 32) has its low four
   bits in ql[64h + l + 32 (q & 1)] (low nibble for q < 2, high for q >= 2)
   and its high two bits in qh[32h + l] bits 2q, 2q+1; sub-block i // 16 has
   scale scales[i // 16].
 
-Field order of Q4_K, Q6_K and Q8_0 follows alice-llm's "Quantization Block Specs"
+Field order of Q4_K, Q5_K, Q6_K and Q8_0 follows alice-llm's "Quantization Block Specs"
 table; the nibble order and the Q4_0/Q4_1 layouts are the standard GGUF ones
 (the pages name the formats without printing them).
 """
@@ -120,6 +123,24 @@ def gen_q4_0(rng, N: int, K: int, scale: float = 0.01) -> np.ndarray:
     return pack_q4_0(d, q)
 
 
+def pack_q5_k(d_bits, dmin_bits, sc, mn, q) -> np.ndarray:
+    """Pack Q5_K superblocks: as pack_q4_k for the low four bits of q (ints
+    0..31, [N, ns*256]), plus qh[32] holding bit 4 of element i in qh[i % 32]
+    bit i // 32."""
+    N, ns = d_bits.shape
+    q = q.reshape(N, ns, 256).astype(np.uint8)
+    q4 = pack_q4_k(d_bits, dmin_bits, sc, mn, (q & 15).reshape(N, ns * 256)).reshape(N, ns, 144)
+    hi = (q >> 4).reshape(N, ns, 8, 32)                   # [sub-block][l]
+    qh = np.zeros((N, ns, 32), np.uint8)
+    for j in range(8):
+        qh |= (hi[:, :, j, :] << j).astype(np.uint8)
+    out = np.zeros((N, ns, 176), np.uint8)
+    out[:, :, 0:16] = q4[:, :, 0:16]
+    out[:, :, 16:48] = qh
+    out[:, :, 48:176] = q4[:, :, 16:144]
+    return out.reshape(N, ns * 176)
+
+
 def pack_q6_k(d_bits, sc, q) -> np.ndarray:
     """Pack Q6_K superblocks. d_bits: [N, ns] uint16; sc: [N, ns, 16] ints
     -128..127; q: [N, ns*256] ints 0..63 (the six-bit quants)."""
@@ -164,6 +185,16 @@ def gen_q4_k(rng, N: int, K: int, scale: float = 0.01) -> np.ndarray:
     return pack_q4_k(d, dmin, sc, mn, q)
 
 
+def gen_q5_k(rng, N: int, K: int, scale: float = 0.01) -> np.ndarray:
+    ns = K // QK_K
+    d = _f16_bits(np.abs(rng.standard_normal((N, ns))) * scale)
+    dmin = _f16_bits(np.abs(rng.standard_normal((N, ns))) * scale)
+    sc = rng.integers(0, 64, size=(N, ns, 8), dtype=np.uint8)
+    mn = rng.integers(0, 64, size=(N, ns, 8), dtype=np.uint8)
+    q = rng.integers(0, 32, size=(N, K), dtype=np.uint8)
+    return pack_q5_k(d, dmin, sc, mn, q)
+
+
 def gen_q6_k(rng, N: int, K: int, scale: float = 0.001) -> np.ndarray:
     ns = K // QK_K
     d = _f16_bits(np.abs(rng.standard_normal((N, ns))) * scale)
@@ -172,8 +203,8 @@ def gen_q6_k(rng, N: int, K: int, scale: float = 0.001) -> np.ndarray:
     return pack_q6_k(d, sc, q)
 
 
-GEN = {"q4_0": gen_q4_0, "q4_1": gen_q4_1, "q8_0": gen_q8_0, "q4_k": gen_q4_k, "q6_k": gen_q6_k}
-ACT_FOR = {"q4_0": "q8_0", "q8_0": "q8_0", "q4_1": "q8_1", "q4_k": "q8_k", "q6_k": "q8_k"}
+GEN = {"q4_0": gen_q4_0, "q4_1": gen_q4_1, "q8_0": gen_q8_0, "q4_k": gen_q4_k, "q5_k": gen_q5_k, "q6_k": gen_q6_k}
+ACT_FOR = {"q4_0": "q8_0", "q8_0": "q8_0", "q4_1": "q8_1", "q4_k": "q8_k", "q5_k": "q8_k", "q6_k": "q8_k"}
 
 
 def gen_weights(fmt: str, rng, N: int, K: int) -> np.ndarray:

@@ -12,7 +12,8 @@
  *  - cera README, "Quantization": weights in Q4_0/Q4_1/Q8_0/Q4_K, activations
  *    quantized dynamically to Q8_0 for an integer GEMV.
  *  - alice-llm docs, "Quantization Block Specs" table: Q4_K = d(f16) + dmin(f16)
- *    + scales[12] + qs[128] per 256 elements; Q8_0 = d(f16) + qs[32]; Q6_K =
+ *    + scales[12] + qs[128] per 256 elements; Q8_0 = d(f16) + qs[32]; Q5_K =
+ *    d(f16) + dmin(f16) + scales[12] + qh[32] + qs[128] (176 bytes); Q6_K =
  *    ql[128] + qh[64] + scales[16] + d(f16) per 256 elements (210 bytes).
  *  - alice-llm docs, "aarch64 NEON Quantized Matvec Bench", design notes: the
  *    Q6_K six-bit quants are assembled from ql and qh, qh's bit pairs feeding
@@ -34,6 +35,8 @@
  *    x * (1/d) clamped to [-127, 127], d stored as fp16 (round to nearest
  *    even) for Q8_0/Q8_1 and as fp32 for Q8_K; Q8_1 also stores
  *    s = fp16(d * sum(q)) and the Q4_1 x Q8_1 dot uses s for its offset term.
+ *  - Q5_K: Q4_K's nibbles, scales and mins, with a fifth bit for element i
+ *    in qh[i % 32], bit i / 32 (the sub-block); value = d * sc * q5 - dmin * m.
  *  - Q6_K element order: the standard GGUF one. Half h = i / 128 of the
  *    superblock, quadrant q = (i % 128) / 32, l = i % 32: low four bits from
  *    ql[64h + l + 32(q & 1)] (low nibble for q < 2, high for q >= 2), high
@@ -50,7 +53,8 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_Q4_0 = 2, ORC_Q4_1 = 3, ORC_Q8_0 = 8, ORC_Q8_1 = 9, ORC_Q4_K = 12, ORC_Q6_K = 14, ORC_Q8_K = 15 };
+enum { ORC_Q4_0 = 2, ORC_Q4_1 = 3, ORC_Q8_0 = 8, ORC_Q8_1 = 9, ORC_Q4_K = 12, ORC_Q5_K = 13, ORC_Q6_K = 14,
+       ORC_Q8_K = 15 };
 enum { ORC_OK = 0, ORC_BAD = -1 };
 
 /* ------------------------------------------------------------------ binary16 */
@@ -195,6 +199,12 @@ static int nib256(const uint8_t* qs, int i)
     return r < 32 ? (qs[32 * g + r] & 15) : (qs[32 * g + r - 32] >> 4);
 }
 
+/* Five-bit quant (0..31) of element i (0..255) of a Q5_K superblock. */
+static int q5k_quant(const uint8_t* blk, int i)
+{
+    return nib256(blk + 48, i) | (((blk[16 + i % 32] >> (i / 32)) & 1) << 4);
+}
+
 /* Six-bit quant (0..63) of element i (0..255) of a Q6_K superblock. */
 static int q6k_quant(const uint8_t* blk, int i)
 {
@@ -217,6 +227,12 @@ double oracle_weight_value(int fmt, const uint8_t* row, int64_t k)
         int i = (int)(k % 256), sc, mn;
         oracle_q4k_scale_min(b + 4, i / 32, &sc, &mn);
         return rd_h(b) * sc * nib256(b + 16, i) - rd_h(b + 2) * mn;
+    }
+    case ORC_Q5_K: {
+        const uint8_t* b = row + (k / 256) * 176;
+        int i = (int)(k % 256), sc, mn;
+        oracle_q4k_scale_min(b + 4, i / 32, &sc, &mn);
+        return rd_h(b) * sc * q5k_quant(b, i) - rd_h(b + 2) * mn;
     }
     case ORC_Q6_K: {
         const uint8_t* b = row + (k / 256) * 210;
@@ -271,9 +287,10 @@ static double row_dot(int wfmt, const uint8_t* w, const uint8_t* x, int64_t K, d
             y += t1 + t2;
             at += fabs(t1) + fabs(t2);
         }
-    } else if (wfmt == ORC_Q4_K) {
+    } else if (wfmt == ORC_Q4_K || wfmt == ORC_Q5_K) {
+        int sb = wfmt == ORC_Q4_K ? 144 : 176;
         for (int64_t s = 0; s < K / 256; s++) {
-            const uint8_t* wbk = w + s * 144;
+            const uint8_t* wbk = w + s * sb;
             const uint8_t* xbk = x + s * 292;
             double dx = (double)rd_f32(xbk);
             int64_t isum_sc = 0, isum_m = 0;
@@ -283,7 +300,8 @@ static double row_dot(int wfmt, const uint8_t* w, const uint8_t* x, int64_t K, d
                 int64_t sj = 0, xs = 0;
                 for (int i = 32 * j; i < 32 * j + 32; i++) {
                     int qx = (int8_t)xbk[4 + i];
-                    sj += (int64_t)nib256(wbk + 16, i) * qx;
+                    int qw = wfmt == ORC_Q4_K ? nib256(wbk + 16, i) : q5k_quant(wbk, i);
+                    sj += (int64_t)qw * qx;
                     xs += qx;
                 }
                 isum_sc += sc * sj;
@@ -322,6 +340,7 @@ static int64_t wrow_bytes(int fmt, int64_t K)
     case ORC_Q4_1: return K / 32 * 20;
     case ORC_Q8_0: return K / 32 * 34;
     case ORC_Q4_K: return K / 256 * 144;
+    case ORC_Q5_K: return K / 256 * 176;
     case ORC_Q6_K: return K / 256 * 210;
     }
     return -1;
@@ -332,7 +351,7 @@ static int act_fmt_for(int wfmt)
     switch (wfmt) {
     case ORC_Q4_0: case ORC_Q8_0: return ORC_Q8_0;
     case ORC_Q4_1: return ORC_Q8_1;
-    case ORC_Q4_K: case ORC_Q6_K: return ORC_Q8_K;
+    case ORC_Q4_K: case ORC_Q5_K: case ORC_Q6_K: return ORC_Q8_K;
     }
     return -1;
 }

@@ -74,7 +74,7 @@ def test_half_encode_matches_numpy(orc):
 
 
 # ------------------------------------------------------------- block decoding
-FMT = {"q4_0": 2, "q4_1": 3, "q8_0": 8, "q4_k": 12, "q6_k": 14}
+FMT = {"q4_0": 2, "q4_1": 3, "q8_0": 8, "q4_k": 12, "q5_k": 13, "q6_k": 14}
 
 
 @pytest.mark.parametrize("rec", _records("blocks.txt"), ids=lambda r: r["name"])
@@ -91,7 +91,7 @@ def test_block_fixture(orc, rec):
     if "scalemin" in rec:
         sm = [int(v) for v in rec["scalemin"].split()]
         for j in range(8):
-            assert orc.q4k_scale_min(raw[4:16].tobytes(), j) == (sm[2 * j], sm[2 * j + 1])
+            assert orc.q4k_scale_min(raw[4:16].tobytes(), j) == (sm[2 * j], sm[2 * j + 1])     # Q4_K and Q5_K
 
 
 def test_generator_packs_fixture_layouts():
@@ -125,6 +125,15 @@ def test_generator_packs_fixture_layouts():
     packed = synth.pack_q6_k(np.array([[0x3C00]], np.uint16), (np.arange(16) - 8).reshape(1, 1, 16),
                              q6.reshape(1, 256))
     assert np.array_equal(packed[0], raw6)
+    # Q5_K: the q4_k_scales scales, qs[i] = i, qh[l] = l (l < 16) or 0xff
+    raw5 = np.array([int(b, 16) for b in recs["q5_k_fifth_bit"]["bytes"].split()], np.uint8)
+    qh = [l if l < 16 else 0xFF for l in range(32)]
+    q5 = q.copy()
+    for e in range(256):
+        q5[e] |= ((qh[e % 32] >> (e // 32)) & 1) << 4
+    packed = synth.pack_q5_k(np.array([[0x3C00]], np.uint16), np.array([[0x3800]], np.uint16), sc, mn,
+                             q5.reshape(1, 256))
+    assert np.array_equal(packed[0], raw5)
 
 
 def test_q4k_scale_packing_roundtrip(orc):
@@ -243,7 +252,7 @@ def test_constant_nibble_q4_0(orc):
             assert abs(Fraction(y[0, n]) - want[n]) <= abs(want[n]) * Fraction(1, 2 ** 50) + Fraction(1, 2 ** 200)
 
 
-@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 14])
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 13, 14])
 def test_one_hot_activation(orc, wfmt):
     """x = e_k: the block holding k has d_x = fp16(1/127) (Q8_K: fp32 1/127), q_k = 127 and
     all other quants 0, so y_n = d_x * 127 * W[n,k] exactly -- plus, for Q4_1, the offset
@@ -251,7 +260,7 @@ def test_one_hot_activation(orc, wfmt):
     inside the value formula."""
     rng = np.random.default_rng(wfmt)
     K, N = 512, 7
-    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 14: "q6_k"}[wfmt]](rng, N, K)
+    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 13: "q5_k", 14: "q6_k"}[wfmt]](rng, N, K)
     afmt = orc.ACT_FOR[wfmt]
     for k in (0, 31, 100, 511):
         x = np.zeros((1, K), np.float32)
@@ -274,18 +283,18 @@ def test_one_hot_activation(orc, wfmt):
             assert y[0, n] == pytest.approx(want, rel=1e-14, abs=1e-300)
 
 
-@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 14])
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 13, 14])
 def test_zero_scales_give_zero(orc, wfmt):
     rng = np.random.default_rng(3)
     K, N = 512, 4
-    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 14: "q6_k"}[wfmt]](rng, N, K)
+    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 13: "q5_k", 14: "q6_k"}[wfmt]](rng, N, K)
     bs, bb = orc.BLOCK[wfmt]
     Wz = W.copy().reshape(N, K // bs, bb)
     if wfmt == 14:
         Wz[:, :, 208:210] = 0           # Q6_K: d is the last field
     else:
         Wz[:, :, 0:2] = 0               # d
-    if wfmt in (3, 12):
+    if wfmt in (3, 12, 13):
         Wz[:, :, 2:4] = 0               # m / dmin
     x = rng.standard_normal((2, K)).astype(np.float32)
     xq = orc.quantize(orc.ACT_FOR[wfmt], x)
@@ -300,7 +309,7 @@ def _exact_dot(orc, wfmt, wrow, xrow, K):
                for k in range(K))
 
 
-@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 14])
+@pytest.mark.parametrize("wfmt", [2, 3, 8, 12, 13, 14])
 def test_brute_force_tiny(orc, wfmt):
     """Dequantize every element and sum exactly; compare with the block formula.
 
@@ -308,7 +317,7 @@ def test_brute_force_tiny(orc, wfmt):
     for the offset term, so the exact reference replaces m_w d_x sum(q_x) by m_w s_x."""
     rng = np.random.default_rng(100 + wfmt)
     K, N, M = 512, 6, 3
-    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 14: "q6_k"}[wfmt]](rng, N, K)
+    W = synth.GEN[{2: "q4_0", 3: "q4_1", 8: "q8_0", 12: "q4_k", 13: "q5_k", 14: "q6_k"}[wfmt]](rng, N, K)
     x = rng.standard_normal((M, K)).astype(np.float32)
     afmt = orc.ACT_FOR[wfmt]
     xq = orc.quantize(afmt, x)
