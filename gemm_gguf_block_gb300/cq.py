@@ -17,11 +17,12 @@ import threading
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libcq.so")
 
-Q4_0, Q4_1, Q8_0, Q8_1, Q4_K, Q6_K, Q8_K = 2, 3, 8, 9, 12, 14, 15
-ACT_FOR = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_1: Q8_1, Q4_K: Q8_K, Q6_K: Q8_K}
-BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q8_0: (32, 34), Q8_1: (32, 36), Q4_K: (256, 144), Q6_K: (256, 210),
-         Q8_K: (256, 292)}
-FMT = {"q4_0": Q4_0, "q4_1": Q4_1, "q8_0": Q8_0, "q8_1": Q8_1, "q4_k": Q4_K, "q6_k": Q6_K, "q8_k": Q8_K}
+Q4_0, Q4_1, Q8_0, Q8_1, Q4_K, Q5_K, Q6_K, Q8_K = 2, 3, 8, 9, 12, 13, 14, 15
+ACT_FOR = {Q4_0: Q8_0, Q8_0: Q8_0, Q4_1: Q8_1, Q4_K: Q8_K, Q5_K: Q8_K, Q6_K: Q8_K}
+BLOCK = {Q4_0: (32, 18), Q4_1: (32, 20), Q8_0: (32, 34), Q8_1: (32, 36), Q4_K: (256, 144), Q5_K: (256, 176),
+         Q6_K: (256, 210), Q8_K: (256, 292)}
+FMT = {"q4_0": Q4_0, "q4_1": Q4_1, "q8_0": Q8_0, "q8_1": Q8_1, "q4_k": Q4_K, "q5_k": Q5_K, "q6_k": Q6_K,
+       "q8_k": Q8_K}
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_FORMAT, ERR_SHAPE, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CUDA, \
     ERR_DEVICE_STATUS, ERR_TIMEOUT = range(9)

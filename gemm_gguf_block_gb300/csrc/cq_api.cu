@@ -26,7 +26,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // token's row is only 4-byte aligned; the kernels read activations in 32-bit words.
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-bool is_weight_fmt(int f) { return f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0 || f == CQ_Q4_K || f == CQ_Q6_K; }
+bool is_weight_fmt(int f) {
+    return f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0 || f == CQ_Q4_K || f == CQ_Q5_K || f == CQ_Q6_K;
+}
 // Q6_K rows of 210-byte superblocks meet the bulk copies' 16-byte rule only
 // eight superblocks at a time: K a multiple of 2048.
 bool fmt_shape_ok(int f, int64_t K) { return f != CQ_Q6_K || K % 2048 == 0; }
@@ -151,7 +153,7 @@ cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const
     cq_status st = check_shape(M, F, K);
     if (st != CQ_OK) return st;
     if (M < 1 || M > 16 || F < 1 || !fmt_shape_ok(w_fmt, K)) return CQ_ERR_SHAPE;
-    const int64_t ce = w_fmt == CQ_Q4_K || w_fmt == CQ_Q6_K ? 256 : 128;
+    const int64_t ce = w_fmt == CQ_Q4_K || w_fmt == CQ_Q5_K || w_fmt == CQ_Q6_K ? 256 : 128;
     if (2 * (K / ce) > 512) return CQ_ERR_SHAPE;
     if (W_gate == nullptr || W_up == nullptr || xq == nullptr || h == nullptr) return CQ_ERR_INVALID_ARG;
     if (!aligned16(W_gate) || !aligned16(W_up) || !aligned4(xq) || !aligned16(h)) return CQ_ERR_ALIGNMENT;

@@ -16,6 +16,7 @@ constexpr int WCHUNK_Q4_0 = 8 * 18;   // 144
 constexpr int WCHUNK_Q4_1 = 8 * 20;   // 160
 constexpr int WCHUNK_Q8_0 = 8 * 34;   // 272
 constexpr int WCHUNK_Q4_K = 144;
+constexpr int WCHUNK_Q5_K = 176;
 constexpr int WCHUNK_Q6_K = 210;
 constexpr int ACHUNK_Q8_0 = 8 * 34;   // 272
 constexpr int ACHUNK_Q8_1 = 8 * 36;   // 288
@@ -23,11 +24,11 @@ constexpr int ACHUNK_Q8_K = 292;
 
 __host__ __device__ constexpr int wchunk_bytes(int fmt) {
     return fmt == CQ_Q4_0 ? WCHUNK_Q4_0 : fmt == CQ_Q4_1 ? WCHUNK_Q4_1 : fmt == CQ_Q8_0 ? WCHUNK_Q8_0
-         : fmt == CQ_Q4_K ? WCHUNK_Q4_K : fmt == CQ_Q6_K ? WCHUNK_Q6_K : 0;
+         : fmt == CQ_Q4_K ? WCHUNK_Q4_K : fmt == CQ_Q5_K ? WCHUNK_Q5_K : fmt == CQ_Q6_K ? WCHUNK_Q6_K : 0;
 }
 __host__ __device__ constexpr int act_fmt_for(int wfmt) {
     return wfmt == CQ_Q4_0 || wfmt == CQ_Q8_0 ? CQ_Q8_0 : wfmt == CQ_Q4_1 ? CQ_Q8_1
-         : wfmt == CQ_Q4_K || wfmt == CQ_Q6_K ? CQ_Q8_K : -1;
+         : wfmt == CQ_Q4_K || wfmt == CQ_Q5_K || wfmt == CQ_Q6_K ? CQ_Q8_K : -1;
 }
 __host__ __device__ constexpr int achunk_bytes(int afmt) {
     return afmt == CQ_Q8_0 ? ACHUNK_Q8_0 : afmt == CQ_Q8_1 ? ACHUNK_Q8_1 : afmt == CQ_Q8_K ? ACHUNK_Q8_K : 0;

@@ -41,8 +41,11 @@ template <> struct G<CQ_Q8_0> { static constexpr int WCH = 136, CE = 128, ACP = 
 template <> struct G<CQ_Q4_0> { static constexpr int WCH = 72, CE = 128, ACP = 144, WR = 18; };
 template <> struct G<CQ_Q4_1> { static constexpr int WCH = 80, CE = 128, ACP = 176, WR = 20; };
 template <> struct G<CQ_Q4_K> { static constexpr int WCH = 144, CE = 256, ACP = 304, WR = 36; };
+template <> struct G<CQ_Q5_K> { static constexpr int WCH = 176, CE = 256, ACP = 304, WR = 44; };
 template <> struct G<CQ_Q6_K> { static constexpr int WCH = 210, CE = 256, ACP = 336, WR = 53; };
-template <int WF> __host__ __device__ constexpr bool superblock_fmt() { return WF == CQ_Q4_K || WF == CQ_Q6_K; }
+template <int WF> __host__ __device__ constexpr bool superblock_fmt() {
+    return WF == CQ_Q4_K || WF == CQ_Q5_K || WF == CQ_Q6_K;
+}
 
 struct GemvParams {
     const uint8_t* W;
@@ -403,8 +406,12 @@ __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t
     }
 }
 
-template <int MT>
-__device__ __forceinline__ void chunk_q4_k(const uint32_t (&w)[36], const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+// Q4_K and Q5_K: d / dmin in word 0, the twelve scale bytes in words 1-3,
+// then (Q5_K) qh[32] in words 4-11, then qs[128]. A Q5_K quant is the Q4_K
+// nibble with bit j of qh[l] (sub-block j, element l of it) as bit 4.
+template <int MT, bool Q5, int NW>
+__device__ __forceinline__ void chunk_q4_k(const uint32_t (&w)[NW], const uint8_t* xa, int tp, int M, float (&c)[MT]) {
+    constexpr int QS = Q5 ? 12 : 4;
     const float d = h2f(w[0]);
     const float dmin = h2f(w[0] >> 16);
     int isc[MT];
@@ -417,8 +424,10 @@ __device__ __forceinline__ void chunk_q4_k(const uint32_t (&w)[36], const uint8_
         int nib[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t q = w[4 + 8 * (j >> 1) + i];
-            nib[i] = static_cast<int>((j & 1) ? ((q >> 4) & 0x0f0f0f0fu) : (q & 0x0f0f0f0fu));
+            const uint32_t q = w[QS + 8 * (j >> 1) + i];
+            uint32_t v = (j & 1) ? ((q >> 4) & 0x0f0f0f0fu) : (q & 0x0f0f0f0fu);
+            if constexpr (Q5) v |= ((w[4 + i] >> j) & 0x01010101u) << 4;
+            nib[i] = static_cast<int>(v);
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
@@ -521,9 +530,9 @@ __device__ __forceinline__ void chunk_load(const uint8_t* wc, uint32_t (&w)[G<WF
             w[i] = __funnelshift_r(prev, next, sh);
             prev = next;
         }
-    } else if constexpr (WF == CQ_Q4_K) {
+    } else if constexpr (WF == CQ_Q4_K || WF == CQ_Q5_K) {
 #pragma unroll
-        for (int i = 0; i < 9; ++i) {
+        for (int i = 0; i < G<WF>::WR / 4; ++i) {
             const uint4 v = lds128(wc + 16 * i);
             w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
@@ -538,7 +547,8 @@ __device__ __forceinline__ void chunk_value(const uint32_t (&wc)[G<WF>::WR], con
     else if constexpr (WF == CQ_Q4_0) chunk_q4_0<MT>(wc, x, M, c);
     else if constexpr (WF == CQ_Q4_1) chunk_q4_1<MT>(wc, x, M, c);
     else if constexpr (WF == CQ_Q6_K) chunk_q6_k<MT>(wc, x.xa, x.tp, M, c);
-    else chunk_q4_k<MT>(wc, x.xa, x.tp, M, c);
+    else if constexpr (WF == CQ_Q5_K) chunk_q4_k<MT, true>(wc, x.xa, x.tp, M, c);
+    else chunk_q4_k<MT, false>(wc, x.xa, x.tp, M, c);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -974,6 +984,7 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, N, K, W, nullptr, xq, y, x, s);
     case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, N, K, W, nullptr, xq, y, x, s);
     case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, N, K, W, nullptr, xq, y, x, s);
+    case CQ_Q5_K: return launch_gemv_fmt<CQ_Q5_K>(dev, M, N, K, W, nullptr, xq, y, x, s);
     case CQ_Q6_K: return launch_gemv_fmt<CQ_Q6_K>(dev, M, N, K, W, nullptr, xq, y, x, s);
     default: return cudaErrorInvalidValue;
     }
@@ -987,6 +998,7 @@ cudaError_t launch_gemv_swiglu(const DeviceInfo& dev, int w_fmt, int M, int64_t 
     case CQ_Q8_0: return launch_gemv_fmt<CQ_Q8_0>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     case CQ_Q4_1: return launch_gemv_fmt<CQ_Q4_1>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     case CQ_Q4_K: return launch_gemv_fmt<CQ_Q4_K>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
+    case CQ_Q5_K: return launch_gemv_fmt<CQ_Q5_K>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     case CQ_Q6_K: return launch_gemv_fmt<CQ_Q6_K>(dev, M, F, K, Wg, Wu, xq, h, nullptr, s);
     default: return cudaErrorInvalidValue;
     }

@@ -9,6 +9,7 @@
  *     Q8_0            Q8_0                32 elements
  *     Q4_1            Q8_1                32 elements
  *     Q4_K            Q8_K                256 elements
+ *     Q5_K            Q8_K                256 elements (GEMV only)
  *     Q6_K            Q8_K                256 elements (GEMV only)
  *
  * Sources (web pages on GGUF inference engines; sections by name):
@@ -27,7 +28,9 @@
  *   tied Q6_K embedding as the LM head). Q6_K element i: half h = i/128,
  *   quadrant q = (i%128)/32, l = i%32; low four bits in ql[64h + l + 32(q&1)]
  *   (low nibble for q < 2, high for q >= 2), high two bits in qh[32h + l]
- *   bits 2q, 2q+1; value = d * (int8)scales[i/16] * (q6 - 32).
+ *   bits 2q, 2q+1; value = d * (int8)scales[i/16] * (q6 - 32). Q5_K = d +
+ *   dmin + scales[12] + qh[32] + qs[128] ("Quantization Block Specs"): Q4_K's
+ *   nibbles, scales and mins with bit 4 of element i in qh[i%32], bit i/32.
  *
  * Conventions for every call:
  *   - All data pointers are DEVICE pointers owned by the caller, 16-byte
@@ -62,6 +65,7 @@
  *                     isum_m = sum_j m_j (bsum_2j + bsum_2j+1),
  *                     t = fma(D(d), (float)isum_sc, -(D(dmin) * (float)isum_m)),
  *                     y = fma(d_x, t, y).
+ *   Q5_K: as Q4_K, with the five-bit quants.
  *   Q6_K, per superblock in increasing k, from y = 0:
  *                     S_j = int dot of sub-block j (16 elements) of (q6 - 32)
  *                     with q8, isum = sum_j sc_j S_j, t = D(d) * (float)isum,
@@ -85,6 +89,7 @@ typedef enum {
     CQ_Q8_0 = 8,
     CQ_Q8_1 = 9,
     CQ_Q4_K = 12,
+    CQ_Q5_K = 13,
     CQ_Q6_K = 14,
     CQ_Q8_K = 15
 } cq_format;
@@ -125,7 +130,7 @@ cq_status cq_quantize_act(cq_format act_fmt, int64_t M, int64_t K, const float* 
  * (cera "Other features": the verify path projects all 1+k positions in one
  * batched pass so the head is read once; alice-llm "Batch-4 Speculative
  * Decoding": weights decoded once, one accumulator set per token).
- * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K, Q6_K}; xq in the paired activation format.
+ * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K, Q5_K, Q6_K}; xq in the paired activation format.
  * W: N rows of K/blk blocks. y: fp32 [M][N]. M > 16 returns CQ_ERR_SHAPE.
  */
 cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
@@ -151,11 +156,11 @@ cq_status cq_gemv_x(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void
  *   g = W_gate . xq,  u = W_up . xq   (each exactly as cq_gemv computes it)
  *   h[m][f] = silu(g) * u = g / (1 + exp(-g)) * u   (fp32: RN divide,
  *             RN add, RN multiply; exp is CUDA's expf)
- * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K, Q6_K}; xq in the paired activation format;
+ * w_fmt in {Q4_0, Q8_0, Q4_1, Q4_K, Q5_K, Q6_K}; xq in the paired activation format;
  * W_gate, W_up: F rows of K/blk blocks each (16-byte aligned); h: fp32
  * [M][F] (16-byte aligned). 1 <= M <= 16 (else CQ_ERR_SHAPE); F >= 1;
  * K a positive multiple of 256 with 2 * K / 128 <= 512 chunks (K <= 32768;
- * Q4_K, Q6_K: K <= 65536). Errors as cq_gemv. g and u never leave the kernel: one
+ * Q4_K, Q5_K, Q6_K: K <= 65536). Errors as cq_gemv. g and u never leave the kernel: one
  * launch reads both matrices, combines the two sums of each (row, token) and
  * writes only h.
  */

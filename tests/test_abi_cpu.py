@@ -102,6 +102,17 @@ def test_q6k_shape_rule(L):
     assert cq.cq_gemv(cq.Q6_K, 0, 8, 2048, None, None, None) == cq.OK
 
 
+def test_q5k_shape_rule(L):
+    """Q5_K rows are 176 bytes a superblock, so any K % 256 == 0 keeps them aligned."""
+    assert cq.cq_gemv(cq.Q5_K, 1, 8, 128, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemv(cq.Q5_K, 1, 8, 300, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemv_x(cq.Q5_K, 1, 8, 1000, A, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemv_swiglu(cq.Q5_K, 1, 8, 640, A, A, A, A) == cq.ERR_SHAPE
+    assert cq.cq_gemm(cq.Q5_K, 4, 8, 2048, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert cq.cq_gemv(cq.Q5_K, 0, 8, 256, None, None, None) == cq.OK
+    assert cq.cq_gemv_x(cq.Q5_K, 0, 8, 768, None, None, None, None) == cq.OK
+
+
 def test_gemv_swiglu_validation(L):
     f = cq.cq_gemv_swiglu
     assert f(99, 1, 8, 256, A, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
