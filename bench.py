@@ -280,6 +280,26 @@ def case_gemm(c, cq, synth, peaks, seed):
             "cq_gemm_tops": 2.0 * M * N * K / (ms_plain * 1e-3) / 1e12}
 
 
+def case_gemm_32(c, cq, synth, peaks, seed, fmts=("q8_0", "q4_0", "q4_1")):
+    """Prefill GEMM of the 32-element formats (cq_gemm, mma.sync kernel):
+    M=512, K=4096, N=14336 per format."""
+    res = {}
+    for fmt in fmts:
+        wfmt = cq.FMT[fmt]
+        W, x = synth.prefill_32(fmt, seed)
+        M, K = x.shape
+        N = W.shape[0]
+        Wd = c.dev(W)
+        xq = cq.quantize_act_t(c.dev(x), cq.ACT_FOR[wfmt])
+        y = c.torch.empty((M, N), dtype=c.torch.float32, device="cuda")
+        ms = c.time(lambda: cq.cq_gemm(wfmt, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
+        tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        res[fmt] = {"shape": f"M={M} N={N} K={K}", "ms": ms, "int8_equiv_tops": tops,
+                    "frac_of_fp16_peak": tops / peaks["bf16"], "weight_gbs": W.nbytes / ms / 1e6}
+        del Wd, xq, y
+    return res
+
+
 def case_moe(c, cq, synth, peaks, seed):
     """Routed-expert FFN: 256 tokens, 32 experts, top-4, Q4_0 2048/1792."""
     Wg, Wu, Wdn, ids, rw, x = synth.moe_ffn(seed)
@@ -344,18 +364,28 @@ def case_swiglu(c, cq, synth, peaks, seed, ms_list=(1, 4)):
     return res
 
 
-def case_lm_head_q6k(c, cq, synth, peaks, seed, ms_list=(1, 4)):
-    """Tied-embedding LM head in Q6_K: 128256x2048 (Llama-3.2-1B) at M tokens."""
-    W, x = synth.lm_head_q6_k(seed)
+def _kquant_gemv(c, cq, peaks, wfmt, W, x, ms_list):
     N, K = W.shape[0], x.shape[1]
     Wd = c.dev(W)
     xq = cq.quantize_act_t(c.dev(x), cq.Q8_K)
     res = {"shape": f"N={N} K={K}"}
     for M in ms_list:
         y = c.torch.empty((M, N), dtype=c.torch.float32, device="cuda")
-        ms = c.time(lambda: cq.cq_gemv(cq.Q6_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
+        ms = c.time(lambda: cq.cq_gemv(wfmt, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
         res[str(M)] = {"ms": ms, "weight_gbs": W.nbytes / ms / 1e6, "hbm_frac": W.nbytes / ms / 1e6 / peaks["hbm"]}
     return res
+
+
+def case_lm_head_q6k(c, cq, synth, peaks, seed, ms_list=(1, 4)):
+    """Tied-embedding LM head in Q6_K: 128256x2048 (Llama-3.2-1B) at M tokens."""
+    W, x = synth.lm_head_q6_k(seed)
+    return _kquant_gemv(c, cq, peaks, cq.Q6_K, W, x, ms_list)
+
+
+def case_ffn_q5k(c, cq, synth, peaks, seed, ms_list=(1, 4)):
+    """Dense FFN gate projection in Q5_K: 14336x4096 at M tokens."""
+    W, x = synth.ffn_q5_k(seed)
+    return _kquant_gemv(c, cq, peaks, cq.Q5_K, W, x, ms_list)
 
 
 def case_q4_0_small(c, cq, synth, peaks, seed):
@@ -398,8 +428,9 @@ def case_q4_0_small(c, cq, synth, peaks, seed):
             "rotation": f"{copies} copies ({copies * W.nbytes / 2**20:.0f} MiB > L2) in one CUDA graph"}
 
 
-CASES = {"prefill_gemm_q4_k": case_gemm, "moe_q4_0": case_moe, "lm_head_q4_1": case_lm_head,
-         "decode_q4_0_2048": case_q4_0_small, "ffn_swiglu_q4_k": case_swiglu, "lm_head_q6_k": case_lm_head_q6k}
+CASES = {"prefill_gemm_q4_k": case_gemm, "prefill_gemm_32": case_gemm_32, "moe_q4_0": case_moe, "lm_head_q4_1": case_lm_head,
+         "decode_q4_0_2048": case_q4_0_small, "ffn_swiglu_q4_k": case_swiglu, "lm_head_q6_k": case_lm_head_q6k,
+         "ffn_q5_k": case_ffn_q5k}
 
 
 def secondary(torch, cq, synth, peaks, seed):
@@ -419,7 +450,7 @@ def run_case(args):
     c = _Ctx(torch, iters=args.steps, warmup=args.warmup)
     fn = CASES[args.case]
     kw = {}
-    if args.case in ("lm_head_q4_1", "ffn_swiglu_q4_k", "lm_head_q6_k") and args.m:
+    if args.case in ("lm_head_q4_1", "ffn_swiglu_q4_k", "lm_head_q6_k", "ffn_q5_k") and args.m:
         kw["ms_list"] = tuple(int(v) for v in args.m.split(","))
     r = fn(c, cq, synth, _peaks(), args.seed, **kw)
     print(json.dumps({"case": args.case, "steps": args.steps, "warmup": args.warmup, "result": r}))
@@ -717,7 +748,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--case", choices=sorted(CASES), help="run one secondary workload alone (for profiling)")
-    ap.add_argument("--m", default="", help="with --case lm_head_q4_1 or ffn_swiglu_q4_k: comma-separated token counts")
+    ap.add_argument("--m", default="", help="with --case lm_head_q4_1, ffn_swiglu_q4_k, lm_head_q6_k or ffn_q5_k: comma-separated token counts")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.case:

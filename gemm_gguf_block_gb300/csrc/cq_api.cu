@@ -189,41 +189,52 @@ cq_status cq_read_global_status(int32_t* out_code, int clear) {
 
 }  // extern "C"
 
+namespace {
+
+// cq_gemm formats: Q4_K (tcgen05 kernel, optional workspace) and the 32-element
+// formats (mma.sync kernel, no workspace; their activation rows are read by TMA,
+// so xq must be 16-byte aligned).
+bool is_gemm_fmt(int f) { return f == CQ_Q4_K || f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0; }
+
+cq_status gemm_common(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
+                      void* workspace, size_t workspace_bytes, bool with_ws, void* stream) {
+    if (!is_gemm_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, N, K);
+    if (st != CQ_OK) return st;
+    if (M > (int64_t(1) << 31) - 1) return CQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return CQ_OK;
+    if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
+    const size_t need = with_ws ? cq::gemm_workspace_size(w_fmt, M, K) : 0;
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return CQ_ERR_WORKSPACE;
+    const bool xq_ok = w_fmt == CQ_Q4_K ? aligned4(xq) : aligned16(xq);
+    if (!aligned16(W) || !xq_ok || !aligned16(y)) return CQ_ERR_ALIGNMENT;
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = w_fmt == CQ_Q4_K
+                              ? cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, need > 0 ? workspace : nullptr, s)
+                              : cq::launch_gemm_mma(dev, w_fmt, M, N, K, W, xq, y, s);
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
                   void* stream) {
-    if (w_fmt != CQ_Q4_K) return CQ_ERR_UNSUPPORTED_FORMAT;
-    cq_status st = check_shape(M, N, K);
-    if (st != CQ_OK) return st;
-    if (M == 0 || N == 0) return CQ_OK;
-    if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
-    if (!aligned16(W) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
-    cq::DeviceInfo dev;
-    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
-    cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, nullptr, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+    return gemm_common(w_fmt, M, N, K, W, xq, y, nullptr, 0, false, stream);
 }
 
 size_t cq_gemm_workspace_size(cq_format w_fmt, int64_t M, int64_t N, int64_t K) {
-    if (w_fmt != CQ_Q4_K || check_shape(M, N, K) != CQ_OK) return 0;
+    if (!is_gemm_fmt(w_fmt) || check_shape(M, N, K) != CQ_OK) return 0;
     return cq::gemm_workspace_size(w_fmt, M, K);
 }
 
 cq_status cq_gemm_ws(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
                      void* workspace, size_t workspace_bytes, void* stream) {
-    if (w_fmt != CQ_Q4_K) return CQ_ERR_UNSUPPORTED_FORMAT;
-    cq_status st = check_shape(M, N, K);
-    if (st != CQ_OK) return st;
-    if (M == 0 || N == 0) return CQ_OK;
-    if (W == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
-    if (workspace == nullptr || workspace_bytes < cq::gemm_workspace_size(w_fmt, M, K)) return CQ_ERR_WORKSPACE;
-    if (!aligned16(W) || !aligned4(xq) || !aligned16(y) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return CQ_ERR_ALIGNMENT;
-    cq::DeviceInfo dev;
-    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
-    cudaError_t e = cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, workspace, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+    return gemm_common(w_fmt, M, N, K, W, xq, y, workspace, workspace_bytes, true, stream);
 }
 
 }  // extern "C"

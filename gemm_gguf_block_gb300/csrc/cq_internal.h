@@ -72,6 +72,11 @@ size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K);
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, void* workspace, cudaStream_t s);
 
+// Prefill GEMM of the 32-element formats (Q4_0, Q4_1, Q8_0; any M) on
+// mma.sync: y rows equal the cq_gemv rows bit for bit. No workspace.
+cudaError_t launch_gemm_mma(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
+                            const void* xq, float* y, cudaStream_t s);
+
 // Byte offsets of the routed-FFN workspace sections (each 256-byte aligned).
 struct MoeLayout {
     size_t status;   // int32 status word (CQ_DEV_* bits)

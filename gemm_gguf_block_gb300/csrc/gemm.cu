@@ -28,7 +28,6 @@
 // lanes 32*(warp%4)...). Every wait
 // is bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
-#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -539,24 +538,6 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
 }
 
 // ------------------------------------------------------------ host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
 }  // namespace
 
 size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K) {
@@ -569,7 +550,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
                         const void* xq, float* y, void* workspace, cudaStream_t s) {
     if (w_fmt != CQ_Q4_K) return cudaErrorInvalidValue;
     if (M <= 0 || N <= 0) return cudaSuccess;
-    EncodeTiledFn enc = encode_fn();
+    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     GemmParams p{};
     p.W = static_cast<const uint8_t*>(W);

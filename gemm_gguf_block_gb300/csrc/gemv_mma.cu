@@ -21,12 +21,12 @@
 // stages the tokens' activations once as fp16 in shared memory, then streams
 // 128-row weight tiles through a ring of 2-D TMA boxes (128 rows x 8 blocks).
 #include <algorithm>
-#include <mutex>
 
 #include <cuda_fp16.h>
 
 #include "cq_device.cuh"
 #include "cq_internal.h"
+#include "mma_frag.cuh"
 #include "tc.cuh"
 
 namespace cq {
@@ -38,20 +38,8 @@ constexpr int MAX_STAGES = 4;
 __host__ __device__ constexpr int consumers(int) { return 8; }
 __host__ __device__ constexpr int tile_rows(int NT) { return 16 * consumers(NT); }
 
-// BB / QO: weight block bytes and offset of its quants; ABB / AQO: the same
-// for the paired activation block; BIAS: the fp16 A operand holds BIAS + v
-// for a weight quant of value v (see a_frags), so the accumulator starts at
-// -BIAS * sum(x).
-// Bytes per weight row in a stage: the segment's 8 blocks, padded for Q4_1
-// (160 -> 176 bytes: 44 words, so the 8 rows one load instruction touches fall
-// in 8 different bank groups; the padding is the start of the next segment,
-// or zero fill past the end of the row).
-__host__ __device__ constexpr int stage_pitch(int bb) { return bb == 20 ? 176 : SEG_BLOCKS * bb; }
-
-template <int WF> struct MF;
-template <> struct MF<CQ_Q4_0> { static constexpr int BB = 18, QO = 2, ABB = 34, AQO = 2, BIAS = 1032; };
-template <> struct MF<CQ_Q4_1> { static constexpr int BB = 20, QO = 4, ABB = 36, AQO = 4, BIAS = 1024; };
-template <> struct MF<CQ_Q8_0> { static constexpr int BB = 34, QO = 2, ABB = 34, AQO = 2, BIAS = 1152; };
+using mf::MF;
+using mf::stage_pitch;
 
 struct MmaParams {
     const uint8_t* W;
@@ -68,73 +56,6 @@ struct MmaParams {
     int smem_scale;     // offset of the per-(block, token pair) scale table
     int smem_stage;     // offset of the weight stages
 };
-
-// D = A * B + (c0, c1, c0, c1), and D += A * B.
-__device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1, float c0,
-                                          float c1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%10,%11};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1));
-}
-__device__ __forceinline__ void mma16816acc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-// (w & sel) with bits of `set` forced on: one lop3. With sel = 0x000F000F and
-// set = 0x64006400 the two 16-bit lanes become the binary16 values 1024 + n of
-// the nibbles in bits 0-3 and 16-19.
-__device__ __forceinline__ uint32_t and_or(uint32_t w, uint32_t sel, uint32_t set) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "r"(sel), "r"(set));   // (a & b) | c
-    return r;
-}
-// The same for signed bytes in bits 0-7 and 16-23: 1024 + (b + 128) = 1152 + b.
-__device__ __forceinline__ uint32_t s8pair_1152(uint32_t w) {
-    return and_or(w ^ 0x00800080u, 0x00FF00FFu, 0x64006400u);
-}
-
-// The k order inside a 32-block. mma k-step 0 takes elements 0..15, k-step 1
-// elements 16..31; within a k-step, fragment column 2t holds element 4t,
-// 2t+1 -> 4t+2, 2t+8 -> 4t+1, 2t+9 -> 4t+3. Both operands use this order, so
-// the products are the same; what it buys is that lane t's weight quants are
-// the four consecutive bytes 4t..4t+3 of a 16-element run.
-//
-// A fragments of rows g (q0) and g+8 (q1) for one block: BIAS + value per element.
-template <int WF>
-__device__ __forceinline__ void a_frags(uint32_t q0a, uint32_t q1a, uint32_t q0b, uint32_t q1b, uint32_t (&a0)[4],
-                                        uint32_t (&a1)[4]) {
-    if constexpr (WF == CQ_Q8_0) {
-        // q?a: quants 4t..4t+3, q?b: 16+4t..16+4t+3 (signed bytes)
-        a0[0] = s8pair_1152(q0a);        a0[1] = s8pair_1152(q1a);
-        a0[2] = s8pair_1152(q0a >> 8);   a0[3] = s8pair_1152(q1a >> 8);
-        a1[0] = s8pair_1152(q0b);        a1[1] = s8pair_1152(q1b);
-        a1[2] = s8pair_1152(q0b >> 8);   a1[3] = s8pair_1152(q1b >> 8);
-    } else {
-        // q?a: bytes 4t..4t+3; low nibbles = elements 4t.., high = 16+4t..
-        constexpr uint32_t SEL = 0x000F000Fu, SET = 0x64006400u;
-        a0[0] = and_or(q0a, SEL, SET);         a0[1] = and_or(q1a, SEL, SET);
-        a0[2] = and_or(q0a >> 8, SEL, SET);    a0[3] = and_or(q1a >> 8, SEL, SET);
-        a1[0] = and_or(q0a >> 4, SEL, SET);    a1[1] = and_or(q1a >> 4, SEL, SET);
-        a1[2] = and_or(q0a >> 12, SEL, SET);   a1[3] = and_or(q1a >> 12, SEL, SET);
-        (void)q0b;
-        (void)q1b;
-    }
-}
-
-// Four bytes at a 2-byte-aligned shared-memory address.
-__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
-    const uint16_t* h = reinterpret_cast<const uint16_t*>(p);
-    return __byte_perm(h[0], h[1], 0x5410);
-}
 
 template <int WF, int NT>
 __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
@@ -186,31 +107,13 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
         const int total = NT * 8 * p.nb;
         for (int i = threadIdx.x; i < total; i += blockDim.x) {
             const int m = i / p.nb, b = i - m * p.nb;
-            uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            uint4 ch[4] = {};
             float d = 0.0f, sx = 0.0f;
             int sum = 0;
-            if (m < p.M) {
-                const uint8_t* blk = p.xq + (static_cast<int64_t>(m) * p.nb + b) * F::ABB;
-                const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    w[j] = __byte_perm(h[F::AQO / 2 + 2 * j], h[F::AQO / 2 + 2 * j + 1], 0x5410);
-                    sum = __dp4a(static_cast<int>(w[j]), 0x01010101, sum);
-                }
-                d = h2f(h[0]);
-                if constexpr (WF == CQ_Q4_1) sx = h2f(h[1]);
-            }
+            if (m < p.M) mf::act_frags<WF>(p.xq + (static_cast<int64_t>(m) * p.nb + b) * F::ABB, ch, d, sx, sum);
             uint4* dst = reinterpret_cast<uint4*>(smem + p.smem_act + m * p.act_pitch + 64 * b);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                // exact fp16 of the signed bytes: (1152 + b) - 1152
-                const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-                const uint32_t e02 = h2u(__hsub2(u2h(s8pair_1152(w[t])), k1152));
-                const uint32_t e13 = h2u(__hsub2(u2h(s8pair_1152(w[t] >> 8)), k1152));
-                const uint32_t f02 = h2u(__hsub2(u2h(s8pair_1152(w[t + 4])), k1152));
-                const uint32_t f13 = h2u(__hsub2(u2h(s8pair_1152(w[t + 4] >> 8)), k1152));
-                dst[t] = make_uint4(e02, e13, f02, f13);
-            }
+            for (int t = 0; t < 4; ++t) dst[t] = ch[t];
             const int j = m >> 1, hi = m & 1;
             float* e = sc + (b * NPAIR + j) * 4;
             e[hi] = d;
@@ -258,37 +161,9 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
 #pragma unroll 4
                 for (int bi = 0; bi < SEG_BLOCKS; ++bi) {
                     const int b = seg * SEG_BLOCKS + bi;          // block index along K
-                    const uint8_t* w0 = rg + bi * F::BB;
-                    const uint8_t* w1 = rg8 + bi * F::BB;
-                    uint32_t q0a, q1a, q0b = 0, q1b = 0;
-                    if constexpr (WF == CQ_Q4_1) {
-                        q0a = *reinterpret_cast<const uint32_t*>(w0 + F::QO + 4 * t);
-                        q1a = *reinterpret_cast<const uint32_t*>(w1 + F::QO + 4 * t);
-                    } else {
-                        q0a = ld_u32_a2(w0 + F::QO + 4 * t);
-                        q1a = ld_u32_a2(w1 + F::QO + 4 * t);
-                        if constexpr (WF == CQ_Q8_0) {
-                            q0b = ld_u32_a2(w0 + F::QO + 16 + 4 * t);
-                            q1b = ld_u32_a2(w1 + F::QO + 16 + 4 * t);
-                        }
-                    }
                     uint32_t a0[4], a1[4];
-                    a_frags<WF>(q0a, q1a, q0b, q1b, a0, a1);
-                    uint64_t dw0, dw1, mw0 = 0, mw1 = 0;
-                    if constexpr (WF == CQ_Q4_1) {
-                        const uint32_t dm0 = *reinterpret_cast<const uint32_t*>(w0);
-                        const uint32_t dm1 = *reinterpret_cast<const uint32_t*>(w1);
-                        const float d0 = h2f(dm0), d1 = h2f(dm1), m0 = h2f(dm0 >> 16), m1 = h2f(dm1 >> 16);
-                        dw0 = tc::pk(d0, d0);
-                        dw1 = tc::pk(d1, d1);
-                        mw0 = tc::pk(m0, m0);
-                        mw1 = tc::pk(m1, m1);
-                    } else {
-                        const float d0 = h2f(*reinterpret_cast<const uint16_t*>(w0));
-                        const float d1 = h2f(*reinterpret_cast<const uint16_t*>(w1));
-                        dw0 = tc::pk(d0, d0);
-                        dw1 = tc::pk(d1, d1);
-                    }
+                    uint64_t dw0, dw1, mw0, mw1;
+                    mf::weight_frags<WF>(rg + bi * F::BB, rg8 + bi * F::BB, t, a0, a1, dw0, dw1, mw0, mw1);
                     if ((b & 3) == 0) {
 #pragma unroll
                         for (int n = 0; n < NT; ++n) c[n][0] = c[n][1] = 0;
@@ -298,8 +173,8 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
                         const uint4 bv = *reinterpret_cast<const uint4*>(act + 8 * n * p.act_pitch + 64 * b);
                         const float4 s4 = sc4[b * NPAIR + 4 * n];
                         float acc[4];
-                        mma16816c(acc, a0, bv.x, bv.y, s4.z, s4.w);
-                        mma16816acc(acc, a1, bv.z, bv.w);
+                        mf::mma16816c(acc, a0, bv.x, bv.y, s4.z, s4.w);
+                        mf::mma16816acc(acc, a1, bv.z, bv.w);
                         const uint64_t dx = tc::pk(s4.x, s4.y);
                         // c = fma(d_w * d_x, isum, c) per element, two tokens per instruction
                         c[n][0] = tc::fma2(tc::mul2(dw0, dx), tc::pk(acc[0], acc[1]), c[n][0]);
@@ -348,24 +223,6 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* q = nullptr;
-        cudaDriverEntryPointQueryResult r;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
-                cudaSuccess &&
-            r == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(q);
-    });
-    return fn;
-}
-
 // Shared-memory layout for M tokens, K columns: barriers, the fp16
 // activation tile, the scale table, then `stages` weight stages.
 struct MmaSmem {
@@ -408,7 +265,7 @@ template <int WF>
 cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, const void* W, const void* xq,
                            float* y, cudaStream_t s) {
     using F = MF<WF>;
-    EncodeTiledFn enc = encode_fn();
+    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     MmaParams p{};
     p.W = static_cast<const uint8_t*>(W);

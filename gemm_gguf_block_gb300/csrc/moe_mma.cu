@@ -20,7 +20,6 @@
 //         valid pairs into the workspace.
 //   down: o = W_down[e] . hq for the pairs, written into the workspace.
 #include <algorithm>
-#include <mutex>
 
 #include <cuda_fp16.h>
 
@@ -393,28 +392,10 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
     }
 }
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* q = nullptr;
-        cudaDriverEntryPointQueryResult r;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault, &r) ==
-                cudaSuccess &&
-            r == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(q);
-    });
-    return fn;
-}
-
 // Q4_0 weights of all experts as one 2-D tensor of 2-byte elements:
 // [E * rows][kin / 32 * 18 bytes]; box = 8 blocks x 128 rows.
 bool make_map(CUtensorMap* map, const void* W, int64_t rows, int kin) {
-    EncodeTiledFn enc = encode_fn();
+    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return false;
     const int64_t rb = static_cast<int64_t>(kin / 32) * 18;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(rb / 2), static_cast<cuuint64_t>(rows)};
@@ -429,7 +410,7 @@ bool make_map(CUtensorMap* map, const void* W, int64_t rows, int kin) {
 // Q8_0 activation rows as a 2-D tensor of 2-byte elements [rows][xrow / 2];
 // box = one 272-byte segment of one row (the gather4 form takes four rows).
 bool make_act_map(CUtensorMap* map, const void* X, int64_t rows, int64_t xrow) {
-    EncodeTiledFn enc = encode_fn();
+    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return false;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(xrow / 2), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(xrow)};

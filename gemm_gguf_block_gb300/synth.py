@@ -256,6 +256,15 @@ def prefill_q4_k(seed: int = 0, M: int = 512, N: int = 14336, K: int = 4096):
     return W, x
 
 
+def prefill_32(fmt: str, seed: int = 0, M: int = 512, N: int = 14336, K: int = 4096):
+    """Prefill GEMM of a 32-element format (q4_0, q4_1, q8_0): Llama-3-8B FFN
+    gate shape, 512 prompt tokens."""
+    tid = {"q4_0": 0, "q4_1": 2, "q8_0": 4}[fmt]
+    W = GEN[fmt](stream(seed, 9, tid), N, K)
+    x = gen_x(stream(seed, 9, tid + 1), M, K)
+    return W, x
+
+
 def moe_ffn(seed: int = 0, T: int = 256, E: int = 32, topk: int = 4, K: int = 2048, F: int = 1792):
     """Routed FFN: per expert Q4_0 gate/up [F, K] and down [K, F]."""
     Wg = np.stack([gen_q4_0(stream(seed, 4, 10 + e), F, K) for e in range(E)])
@@ -276,6 +285,13 @@ def lm_head_q6_k(seed: int = 0, N: int = 128256, K: int = 2048, M: int = 4):
     """Tied-embedding LM head in Q6_K (Llama-3.2-1B: vocabulary x hidden 2048)."""
     W = gen_q6_k(stream(seed, 7, 0), N, K)
     x = gen_x(stream(seed, 7, 1), M, K)
+    return W, x
+
+
+def ffn_q5_k(seed: int = 0, N: int = 14336, K: int = 4096, M: int = 4):
+    """Dense FFN gate projection in Q5_K [N, K] (Llama-3-8B shapes)."""
+    W = gen_q5_k(stream(seed, 8, 0), N, K)
+    x = gen_x(stream(seed, 8, 1), M, K)
     return W, x
 
 

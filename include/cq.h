@@ -34,9 +34,9 @@
  *
  * Conventions for every call:
  *   - All data pointers are DEVICE pointers owned by the caller, 16-byte
- *     aligned, except quantized activations (xq) passed to cq_gemv/cq_gemm,
- *     which need 4-byte alignment (a Q8_K row is 292 bytes per 256
- *     elements). The library never allocates, frees or synchronises on these
+ *     aligned, except quantized activations (xq) passed to cq_gemv, and to
+ *     cq_gemm with Q4_K weights, which need 4-byte alignment (a Q8_K row is
+ *     292 bytes per 256 elements). The library never allocates, frees or synchronises on these
  *     paths; every call is asynchronous on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) on the current device.
  *   - Matrices are row-major. A weight row holds the K/blk blocks of one
@@ -171,8 +171,12 @@ cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const
  * Prefill GEMM, any M >= 0 (cera README "Supported models": batched-GEMM
  * prefill; alice-llm "Computation Path (Q4_K)"). Same operands and result as
  * cq_gemv; each row equals the cq_gemv result for that token bit for bit.
- * w_fmt: Q4_K (tensor-core path). Other formats return
- * CQ_ERR_UNSUPPORTED_FORMAT.
+ * w_fmt: Q4_K (tcgen05 path) or Q4_0 / Q4_1 / Q8_0 (mma.sync path; cera
+ * 0.5.3 README "Breaking changes in 0.4.0" holds a Q4_1 decode equal to
+ * the batched prefill bit for bit). For Q4_0 / Q4_1 / Q8_0
+ * the activation rows are read by TMA, so xq must be 16-byte aligned
+ * (CQ_ERR_ALIGNMENT otherwise); they need no workspace. M < 2^31. Other
+ * formats return CQ_ERR_UNSUPPORTED_FORMAT.
  */
 cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
                   float* y, void* stream);
@@ -182,7 +186,9 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
  * converted once, into the workspace, to the tensor-core operand layout,
  * instead of in every weight tile. Same result, bit for bit, as cq_gemm.
  * cq_gemm_workspace_size returns the bytes needed (0 for an unsupported
- * format or shape): ceil(M/128) * (K/256) * 70144 for Q4_K. The workspace
+ * format or shape, and 0 for Q4_0 / Q4_1 / Q8_0, which take no workspace:
+ * cq_gemm_ws then accepts a NULL workspace and behaves as cq_gemm):
+ * ceil(M/128) * (K/256) * 70144 for Q4_K. The workspace
  * must be 256-byte aligned; it is scratch (no state is kept between calls),
  * and two calls that may overlap on the GPU need separate workspaces.
  * Errors as cq_gemm, plus CQ_ERR_WORKSPACE (NULL or too small) and

@@ -8,6 +8,8 @@ oracle on sampled outputs.
 * Q4_K prefill GEMM, M=512 N=14336 K=4096: cq_gemm and cq_gemm_ws over the
   whole problem; the oracle on sampled weight rows for all 512 tokens; the two
   calls equal bit for bit, and sampled tokens equal to their cq_gemv rows.
+* Q4_0 / Q4_1 / Q8_0 prefill GEMM, M=512 N=14336 K=4096: sampled rows
+  against the oracle, sampled tokens equal to their cq_gemv rows.
 * Q4_1 LM head 128256 x 4096 at M = 1, 4, 8, 16: the oracle on sampled rows;
   every row of an M>1 call bitwise equal to the M=1 call of that position.
 * Q6_K tied-embedding LM head 128256 x 2048 at M = 1 and 4, the same checks.
@@ -78,6 +80,28 @@ def test_prefill_gemm_sampled(orc):
     assert_within(y[:, idx], y_ref, at, what="q4_k gemm")
     for m in (0, 1, 127, 128, 300, M - 1):
         y1 = cq.gemv_t(Wd, xq[m:m + 1], cq.Q4_K, K).cpu().numpy()[0]
+        assert np.array_equal(y[m].view(np.uint32), y1.view(np.uint32)), f"token {m}: gemm row != gemv row"
+
+
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q8_0"])
+def test_prefill_gemm_32_sampled(orc, fmt):
+    """The mma.sync GEMM of a 32-element format at M=512 N=14336 K=4096."""
+    torch = torch_cuda()
+    cq = cq_built()
+    wfmt = cq.FMT[fmt]
+    W, x = synth.prefill_32(fmt, 0)
+    M, K = x.shape
+    N = W.shape[0]
+    xq = cq.quantize_act_t(dev(torch, x), cq.ACT_FOR[wfmt])
+    xq_np = xq.cpu().numpy()
+    assert np.array_equal(xq_np, orc.quantize(orc.ACT_FOR[wfmt], x))
+    Wd = dev(torch, W)
+    y = cq.gemm_t(Wd, xq, wfmt, K).cpu().numpy()
+    idx = _rows(N, 24)
+    y_ref, at = _oracle_rows(orc, wfmt, W, xq_np, K, idx)
+    assert_within(y[:, idx], y_ref, at, what=f"{fmt} gemm")
+    for m in (0, 1, 63, 64, 300, M - 1):
+        y1 = cq.gemv_t(Wd, xq[m:m + 1], wfmt, K).cpu().numpy()[0]
         assert np.array_equal(y[m].view(np.uint32), y1.view(np.uint32)), f"token {m}: gemm row != gemv row"
 
 

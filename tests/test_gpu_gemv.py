@@ -83,27 +83,34 @@ def test_gemv_exact_arithmetic(orc, wfmt, N, K, M):
     assert at.max() < 2.0 ** 9, "test precondition: partial sums must stay exact in fp32"
     y = cq.gemv_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
     assert np.array_equal(y.astype(np.float64), y_ref)
-    if wfmt == 12:
-        y2 = cq.gemm_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
-        assert np.array_equal(y2.astype(np.float64), y_ref)
-        y3 = cq.gemm_ws_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
-        assert np.array_equal(y3.astype(np.float64), y_ref)
+    y2 = cq.gemm_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
+    assert np.array_equal(y2.astype(np.float64), y_ref)
+    y3 = cq.gemm_ws_t(dev(torch, W), xq, wfmt, K).cpu().numpy()
+    assert np.array_equal(y3.astype(np.float64), y_ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(17, 100, 512), (64, 257, 2048), (130, 96, 4096)])
-def test_gemm_rows_equal_gemv(orc, M, N, K):
+@pytest.mark.parametrize("wfmt", FMTS)
+@pytest.mark.parametrize("M,N,K", [(1, 33, 256), (17, 100, 512), (64, 257, 2048), (65, 129, 768),
+                                   (130, 96, 4096), (200, 300, 1024)])
+def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
+    """cq_gemm (tcgen05 for Q4_K, mma.sync for the 32-element formats) against
+    the oracle, and each row against the single-token cq_gemv bit for bit;
+    M and N ragged against the 64-token / 128-row tiles."""
     torch = torch_cuda()
     cq = cq_built()
-    W, xq = _case(orc, 12, N, K, M, seed=M + N + K)
+    W, xq = _case(orc, wfmt, N, K, M, seed=wfmt * 31 + M + N + K)
     Wd, xd = dev(torch, W), dev(torch, xq)
-    y = cq.gemm_t(Wd, xd, 12, K).cpu().numpy()
-    y_ref, at = orc.matmul(12, W, xq, K)
-    assert_within(y, y_ref, at, what="gemm")
-    y_ws = cq.gemm_ws_t(Wd, xd, 12, K).cpu().numpy()
+    y = cq.gemm_t(Wd, xd, wfmt, K).cpu().numpy()
+    y_ref, at = orc.matmul(wfmt, W, xq, K)
+    assert_within(y, y_ref, at, what=f"gemm fmt {wfmt}")
+    y_ws = cq.gemm_ws_t(Wd, xd, wfmt, K).cpu().numpy()
     assert np.array_equal(y.view(np.uint32), y_ws.view(np.uint32)), "cq_gemm_ws differs from cq_gemm"
-    for m in sorted({0, 1, M // 2, M - 1}):
-        y1 = cq.gemv_t(Wd, xd[m:m + 1], 12, K).cpu().numpy()[0]
+    for m in sorted({0, 1, M // 2, M - 1} & set(range(M))):
+        y1 = cq.gemv_t(Wd, xd[m:m + 1], wfmt, K).cpu().numpy()[0]
         assert np.array_equal(y[m].view(np.uint32), y1.view(np.uint32)), f"row {m}"
+    if M >= 16:
+        y16 = cq.gemv_t(Wd, xd[:16], wfmt, K).cpu().numpy()
+        assert np.array_equal(y[:16].view(np.uint32), y16.view(np.uint32)), "batched GEMV rows differ"
 
 
 @pytest.mark.parametrize("wfmt", FMTS)
