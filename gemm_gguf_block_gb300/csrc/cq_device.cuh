@@ -131,6 +131,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+// L2 policy for data many CTAs re-read (kept ahead of streamed weights).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
 
 // Wall-time limit of any copy-completion wait (a copy that has not landed by
 // then never will): the kernel flags CQ_DEV_WAIT_TIMEOUT and stops.

@@ -541,7 +541,8 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
 }  // namespace
 
 size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K) {
-    if (w_fmt != CQ_Q4_K || M <= 0) return 0;
+    if (w_fmt != CQ_Q4_K) return gemm32_workspace_size(w_fmt, M, K);
+    if (M <= 0) return 0;
     const int64_t cells = (M + BN - 1) / BN * (K / 256);
     return static_cast<size_t>(cells) * (IMG_BYTES + BN * 4);
 }

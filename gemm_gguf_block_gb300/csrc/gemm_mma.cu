@@ -9,14 +9,17 @@
 // thread per (row, token), so it equals the cq_gemv row bit for bit.
 //
 // One CTA = 128 weight rows x 64 tokens. Per 8-block segment a producer warp
-// TMA-loads the weight box (128 rows x 8 blocks, raw GGUF bytes) and the
-// tokens' raw activation blocks (64 rows x 8 blocks) into one stage of a
-// ring. The 8 consumer warps convert the activations to the fp16 B operand
-// and a scale table, then each takes 16 weight rows: per block the integer
-// dot is an exact fp16 mma.sync m16n8k16 product (see mma_frag.cuh) and the
-// scale terms run two tokens per f32x2 instruction. The grid walks the token
-// tiles of one row tile next to each other, so a weight tile is read from
-// DRAM once and from L2 by the other token tiles.
+// TMA-loads the weight box (128 rows x 8 blocks, raw GGUF bytes) into one
+// stage of a ring, together with the tokens' activations. The activations'
+// B-operand image (fp16 fragments + a scale table, one per 64 tokens and
+// segment) is either built once per call by gemm32_prep_kernel into the
+// caller's workspace and bulk-copied (cq_gemm_ws), or built by the consumer
+// warps from the raw Q8_0 / Q8_1 blocks in every CTA (cq_gemm). The 8
+// consumer warps each take 16 weight rows: per block the integer dot is an
+// exact fp16 mma.sync m16n8k16 product (see mma_frag.cuh) and the scale terms
+// run two tokens per f32x2 instruction. The grid walks the token tiles of one
+// row tile next to each other, so a weight tile is read from DRAM once and
+// from L2 by the other token tiles.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -38,34 +41,87 @@ constexpr int NT = TOK / 8;
 constexpr int CONSUMERS = 8;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr int MAX_STAGES = 8;
-constexpr int ACT_PITCH = SEGB * 64 + 64;             // fp16 bytes per token per segment + pad (64 mod 128)
-constexpr int ACT_BYTES = TOK * ACT_PITCH;            // 36864
-// Scale table per (block b, token pair j), pitch SCL_PITCH pairs per block:
-// {d_x, d_x', bias, bias'} as one float4 (bias = -BIAS * sum of the quants)
-// and, for Q8_1, {s_x, s_x'}.
-constexpr int SCL_PITCH = TOK / 2 + 1;
-constexpr int SC4_BYTES = SEGB * SCL_PITCH * 16;
-constexpr int SX_BYTES = SEGB * SCL_PITCH * 8;
-constexpr int SCL_BYTES = (SC4_BYTES + SX_BYTES + 127) / 128 * 128;
-constexpr int FIXED = 1024 + ACT_BYTES + SCL_BYTES;   // barriers, fp16 tile, scale table
-
+// B-operand image of 64 tokens x one segment (the layout is the same in the
+// workspace and in shared memory):
+//   fp16 quants, 512 bytes per token: chunk c (16 bytes, lane t = c's B
+//     fragments of both k-steps, see act_frags) of block b of token tk at
+//     img_pos(tk, b, c);
+//   scale table per (block b, token pair j), SCL_PITCH pairs per block:
+//     {d_x, d_x', bias, bias'} as one float4 (bias = -BIAS * sum of the
+//     quants) and, for Q8_1, {s_x, s_x'}.
+constexpr int ACT_BYTES = TOK * SEGB * 64;            // 32768
+constexpr int SCL_PITCH = TOK / 2 + 1;                // +1: converters' stores spread over banks
+constexpr int SC4_BYTES = SEGB * SCL_PITCH * 16;      // 4224
+constexpr int SX_BYTES = SEGB * SCL_PITCH * 8;        // 2112
+__host__ __device__ constexpr int img_bytes(bool q8_1) {
+    return (ACT_BYTES + SC4_BYTES + (q8_1 ? SX_BYTES : 0) + 127) / 128 * 128;
+}
 __host__ __device__ constexpr int wbox_bytes(int bb) { return ROWS * mf::stage_pitch(bb); }
 __host__ __device__ constexpr int abox_bytes(int abb) { return TOK * SEGB * abb; }
+// Shared memory ahead of the stages: barriers, and without a workspace the
+// CTA's own image of the current segment.
+__host__ __device__ constexpr int fixed_bytes(bool pre, bool q8_1) { return 1024 + (pre ? 0 : img_bytes(q8_1)); }
+__host__ __device__ constexpr int stage_bytes(bool pre, int bb, int abb) {
+    return wbox_bytes(bb) + (pre ? img_bytes(abb == 36) : abox_bytes(abb));
+}
 
 struct GemmMmaParams {
+    const uint8_t* xq;      // activations (prep kernel)
+    const uint8_t* img;     // workspace: [token tile][segment] images (cq_gemm_ws)
     float* y;
     int* status;
     int M, N;
-    int nseg;           // 8-block segments per row
+    int nb;                 // 32-blocks per row
+    int nseg;               // 8-block segments per row
     int stages;
 };
 
-// fp16 position of chunk c (16 bytes) of block b in a token's row: chunks are
-// XOR-rotated by block pair, so eight converters writing chunk c of blocks
-// 0..7 and eight readers of one block hit eight different bank groups.
-__device__ __forceinline__ int chunk_pos(int b, int c) { return 64 * b + 16 * (c ^ ((b >> 1) & 3)); }
+// Byte position of chunk c of block b of token tk in an image. Blocks swap
+// places within a pair for odd tokens, so tokens g and g+1 (one 8-lane
+// shared-memory phase of a fragment load) fall in different halves of the
+// 128-byte bank window; chunks are XOR-rotated by block pair, so eight
+// converters writing chunk c of blocks 0..7 hit eight different bank groups.
+__host__ __device__ constexpr int img_pos(int tk, int b, int c) {
+    return tk * (SEGB * 64) + 64 * (b ^ (tk & 1)) + 16 * (c ^ ((b >> 1) & 3));
+}
 
+// Converts one activation block (token tk of the tile, block b of the
+// segment) into the image at img.
 template <int WF>
+__device__ __forceinline__ void put_block(uint8_t* img, const uint8_t* blk, int tk, int b, bool valid) {
+    using F = MF<WF>;
+    uint4 ch[4] = {};
+    float d = 0.0f, s = 0.0f;
+    int sum = 0;
+    if (valid) mf::act_frags<WF>(blk, ch, d, s, sum);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(img + img_pos(tk, b, cc)) = ch[cc];
+    float* sc4f = reinterpret_cast<float*>(img + ACT_BYTES);
+    float* sx2f = reinterpret_cast<float*>(img + ACT_BYTES + SC4_BYTES);
+    const int j = b * SCL_PITCH + (tk >> 1), hi = tk & 1;
+    sc4f[4 * j + hi] = d;
+    sc4f[4 * j + 2 + hi] = static_cast<float>(-F::BIAS * sum);
+    if constexpr (WF == CQ_Q4_1) sx2f[2 * j + hi] = s;
+}
+
+// The workspace images: one CTA per (segment, token tile); tokens past M
+// become zero blocks (d = 0, no quants).
+template <int WF>
+__global__ void __launch_bounds__(256) gemm32_prep_kernel(const GemmMmaParams p, uint8_t* img) {
+    pdl_trigger();
+    pdl_wait();
+    using F = MF<WF>;
+    constexpr int IMG = img_bytes(WF == CQ_Q4_1);
+    const int seg = blockIdx.x, tile = blockIdx.y;
+    uint8_t* dst = img + (static_cast<int64_t>(tile) * p.nseg + seg) * IMG;
+    for (int it = threadIdx.x; it < TOK * SEGB; it += blockDim.x) {
+        const int tk = it >> 3, b = it & 7;
+        const int m = tile * TOK + tk;
+        put_block<WF>(dst, p.xq + (static_cast<int64_t>(m) * p.nb + seg * SEGB + b) * F::ABB, tk, b, m < p.M);
+    }
+}
+
+template <int WF, bool PRE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                     const GemmMmaParams p) {
@@ -73,15 +129,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     pdl_wait();
     using F = MF<WF>;
     constexpr int WBOX = wbox_bytes(F::BB);
-    constexpr int STAGE = WBOX + abox_bytes(F::ABB);
+    constexpr int IMG = img_bytes(WF == CQ_Q4_1);
+    constexpr int STAGE = stage_bytes(PRE, F::BB, F::ABB);
     constexpr int PITCH = mf::stage_pitch(F::BB);
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + MAX_STAGES;
-    uint8_t* act = smem + 1024;
-    float4* sc4 = reinterpret_cast<float4*>(act + ACT_BYTES);
-    float2* sx2 = reinterpret_cast<float2*>(act + ACT_BYTES + SC4_BYTES);
-    uint8_t* wst = smem + FIXED;
+    uint8_t* own_img = smem + 1024;                    // without a workspace
+    uint8_t* wst = smem + fixed_bytes(PRE, WF == CQ_Q4_1);
     const int S = p.stages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tok0 = blockIdx.x * TOK, r0 = blockIdx.y * ROWS;
@@ -108,7 +163,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(STAGE));
                 // x counts 2-byte elements; rows past N / tokens past M read as zero
                 tc::tma_load_2d(dst, &wmap, k * SEGB * F::BB / 2, r0, &full[st]);
-                tc::tma_load_2d(dst + WBOX, &amap, k * SEGB * F::ABB / 2, tok0, &full[st]);
+                if constexpr (PRE)
+                    bulk_g2s(dst + WBOX, p.img + (static_cast<int64_t>(blockIdx.x) * p.nseg + k) * IMG, IMG,
+                             &full[st], policy_evict_last());
+                else
+                    tc::tma_load_2d(dst + WBOX, &amap, k * SEGB * F::ABB / 2, tok0, &full[st]);
             }
         }
         return;   // the producer takes no part in the consumers' named barriers
@@ -116,8 +175,6 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     // ---------------------------------------------------------- consumers
     const int ct = threadIdx.x, g = lane >> 2, t = lane & 3;
-    float* sc4f = reinterpret_cast<float*>(sc4);
-    float* sx2f = reinterpret_cast<float*>(sx2);
     uint64_t c[NT][2], y[NT][2];   // (row g | row g+8) x (token 8n+2t, 8n+2t+1)
 #pragma unroll
     for (int n = 0; n < NT; ++n) y[n][0] = y[n][1] = 0;
@@ -125,28 +182,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int k = 0; k < p.nseg; ++k) {
         const int st = k % S;
         const bool got = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS);
-        if (!tc::named_and(2, CONSUMERS * 32, got)) {
-            if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
-            ok = false;
-            break;
-        }
         const uint8_t* stage = wst + st * STAGE;
-        // The tokens' blocks of this segment as fp16 B fragments + scale table.
-        for (int it = ct; it < TOK * SEGB; it += CONSUMERS * 32) {
-            const int tk = it >> 3, b = it & 7;
-            uint4 ch[4];
-            float d, s;
-            int sum;
-            mf::act_frags<WF>(stage + WBOX + it * F::ABB, ch, d, s, sum);
-            uint8_t* row = act + tk * ACT_PITCH;
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(row + chunk_pos(b, cc)) = ch[cc];
-            const int j = b * SCL_PITCH + (tk >> 1), hi = tk & 1;
-            sc4f[4 * j + hi] = d;
-            sc4f[4 * j + 2 + hi] = static_cast<float>(-F::BIAS * sum);
-            if constexpr (WF == CQ_Q4_1) sx2f[2 * j + hi] = s;
+        const uint8_t* img;
+        if constexpr (PRE) {
+            // a warp that timed out stops here; the others finish their copies
+            if (!got) {
+                if (lane == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
+                ok = false;
+                break;
+            }
+            img = stage + WBOX;
+        } else {
+            if (!tc::named_and(2, CONSUMERS * 32, got)) {
+                if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
+                ok = false;
+                break;
+            }
+            // The tokens' blocks of this segment as the CTA's own image.
+            for (int it = ct; it < TOK * SEGB; it += CONSUMERS * 32)
+                put_block<WF>(own_img, stage + WBOX + it * F::ABB, it >> 3, it & 7, true);
+            tc::named_and(1, CONSUMERS * 32, true);
+            img = own_img;
         }
-        tc::named_and(1, CONSUMERS * 32, true);
+        const float4* sc4 = reinterpret_cast<const float4*>(img + ACT_BYTES);
+        const float2* sx2 = reinterpret_cast<const float2*>(img + ACT_BYTES + SC4_BYTES);
         const uint8_t* rg = stage + (16 * warp + g) * PITCH;
         const uint8_t* rg8 = rg + 8 * PITCH;
 #pragma unroll 1
@@ -158,12 +217,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int n = 0; n < NT; ++n) c[n][0] = c[n][1] = 0;
             }
-            const uint8_t* ab = act + g * ACT_PITCH + chunk_pos(bi, t);
+            const uint8_t* ab = img + img_pos(g, bi, t);
             const float4* s4p = sc4 + bi * SCL_PITCH + t;
             const float2* sxp = sx2 + bi * SCL_PITCH + t;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const uint4 bv = *reinterpret_cast<const uint4*>(ab + 8 * n * ACT_PITCH);
+                const uint4 bv = *reinterpret_cast<const uint4*>(ab + 8 * n * (SEGB * 64));
                 const float4 s4 = s4p[4 * n];
                 float acc[4];
                 mf::mma16816c(acc, a0, bv.x, bv.y, s4.z, s4.w);
@@ -189,7 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[st]);
-        tc::named_and(1, CONSUMERS * 32, true);     // the fp16 tile is rewritten by the next segment
+        if constexpr (!PRE) tc::named_and(1, CONSUMERS * 32, true);   // the image is rewritten next segment
     }
     if (ok) {
         // y[token][row]: rows r0 + 16w + g (+8), tokens tok0 + 8n + 2t (+1)
@@ -215,9 +274,40 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+template <int WF, bool PRE>
+cudaError_t launch_typed(const DeviceInfo& dev, const CUtensorMap& wmap, const CUtensorMap& amap, GemmMmaParams p,
+                         int64_t M, int64_t N, cudaStream_t s) {
+    using F = MF<WF>;
+    constexpr int STAGE = stage_bytes(PRE, F::BB, F::ABB);
+    constexpr int FIXED = fixed_bytes(PRE, WF == CQ_Q4_1);
+    const int lim = std::min(dev.smem_optin, 227 * 1024);
+    p.stages = std::min(MAX_STAGES, (lim - FIXED) / STAGE);
+    if (p.stages < 2) return cudaErrorInvalidConfiguration;
+    const int smem = FIXED + p.stages * STAGE;
+    static int raised[64] = {};
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e != cudaSuccess) return e;
+    if (devid >= 64 || raised[devid] < smem) {
+        e = cudaFuncSetAttribute(gemm_mma_kernel<WF, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (devid < 64) raised[devid] = smem;
+    }
+    const int64_t row_tiles = (N + ROWS - 1) / ROWS;
+    if (row_tiles > 65535) return cudaErrorInvalidValue;      // grid y limit (N above 8.4 M rows)
+    const unsigned tok_tiles = static_cast<unsigned>((M + TOK - 1) / TOK);
+    if constexpr (PRE) {
+        e = launch_kernel(gemm32_prep_kernel<WF>, dim3(static_cast<unsigned>(p.nseg), tok_tiles), dim3(256), 0, s,
+                          p, const_cast<uint8_t*>(p.img));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(gemm_mma_kernel<WF, PRE>, dim3(tok_tiles, static_cast<unsigned>(row_tiles)),
+                         dim3(THREADS), smem, s, wmap, amap, p);
+}
+
 template <int WF>
 cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
-                       float* y, cudaStream_t s) {
+                       float* y, void* workspace, cudaStream_t s) {
     using F = MF<WF>;
     tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
@@ -246,41 +336,34 @@ cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, c
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    constexpr int STAGE = wbox_bytes(F::BB) + abox_bytes(F::ABB);
-    const int lim = std::min(dev.smem_optin, 227 * 1024);
     GemmMmaParams p{};
+    p.xq = static_cast<const uint8_t*>(xq);
+    p.img = static_cast<const uint8_t*>(workspace);
     p.y = y;
     p.status = dev.status;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
+    p.nb = nb;
     p.nseg = nb / SEGB;
-    p.stages = std::min(MAX_STAGES, (lim - FIXED) / STAGE);
-    if (p.stages < 2) return cudaErrorInvalidConfiguration;
-    const int smem = FIXED + p.stages * STAGE;
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
-    if (e != cudaSuccess) return e;
-    if (devid >= 64 || raised[devid] < smem) {
-        e = cudaFuncSetAttribute(gemm_mma_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = smem;
-    }
-    const int64_t row_tiles = (N + ROWS - 1) / ROWS;
-    if (row_tiles > 65535) return cudaErrorInvalidValue;      // grid y limit (N above 8.4 M rows)
-    const dim3 grid(static_cast<unsigned>((M + TOK - 1) / TOK), static_cast<unsigned>(row_tiles));
-    return launch_kernel(gemm_mma_kernel<WF>, grid, dim3(THREADS), smem, s, wmap, amap, p);
+    return workspace != nullptr ? launch_typed<WF, true>(dev, wmap, amap, p, M, N, s)
+                                : launch_typed<WF, false>(dev, wmap, amap, p, M, N, s);
 }
 
 }  // namespace
 
+size_t gemm32_workspace_size(int w_fmt, int64_t M, int64_t K) {
+    if ((w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) || M <= 0) return 0;
+    return static_cast<size_t>((M + TOK - 1) / TOK) * static_cast<size_t>(K / 256) *
+           static_cast<size_t>(img_bytes(w_fmt == CQ_Q4_1));
+}
+
 cudaError_t launch_gemm_mma(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
-                            const void* xq, float* y, cudaStream_t s) {
+                            const void* xq, float* y, void* workspace, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     switch (w_fmt) {
-    case CQ_Q4_0: return launch_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q4_1: return launch_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q8_0: return launch_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q4_0: return launch_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, workspace, s);
+    case CQ_Q4_1: return launch_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, workspace, s);
+    case CQ_Q8_0: return launch_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, workspace, s);
     default: return cudaErrorInvalidValue;
     }
 }

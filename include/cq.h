@@ -175,8 +175,8 @@ cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const
  * 0.5.3 README "Breaking changes in 0.4.0" holds a Q4_1 decode equal to
  * the batched prefill bit for bit). For Q4_0 / Q4_1 / Q8_0
  * the activation rows are read by TMA, so xq must be 16-byte aligned
- * (CQ_ERR_ALIGNMENT otherwise); they need no workspace. M < 2^31. Other
- * formats return CQ_ERR_UNSUPPORTED_FORMAT.
+ * (CQ_ERR_ALIGNMENT otherwise). M < 2^31. Other formats return
+ * CQ_ERR_UNSUPPORTED_FORMAT.
  */
 cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
                   float* y, void* stream);
@@ -186,9 +186,9 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
  * converted once, into the workspace, to the tensor-core operand layout,
  * instead of in every weight tile. Same result, bit for bit, as cq_gemm.
  * cq_gemm_workspace_size returns the bytes needed (0 for an unsupported
- * format or shape, and 0 for Q4_0 / Q4_1 / Q8_0, which take no workspace:
- * cq_gemm_ws then accepts a NULL workspace and behaves as cq_gemm):
- * ceil(M/128) * (K/256) * 70144 for Q4_K. The workspace
+ * format or shape): ceil(M/128) * (K/256) * 70144 for Q4_K;
+ * ceil(M/64) * (K/256) * 36992 for Q4_0 and Q8_0 (Q8_0 activations) and
+ * ceil(M/64) * (K/256) * 39168 for Q4_1 (Q8_1 activations). The workspace
  * must be 256-byte aligned; it is scratch (no state is kept between calls),
  * and two calls that may overlap on the GPU need separate workspaces.
  * Errors as cq_gemm, plus CQ_ERR_WORKSPACE (NULL or too small) and

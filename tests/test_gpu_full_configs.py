@@ -97,6 +97,8 @@ def test_prefill_gemm_32_sampled(orc, fmt):
     assert np.array_equal(xq_np, orc.quantize(orc.ACT_FOR[wfmt], x))
     Wd = dev(torch, W)
     y = cq.gemm_t(Wd, xq, wfmt, K).cpu().numpy()
+    y_ws = cq.gemm_ws_t(Wd, xq, wfmt, K).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y_ws.view(np.uint32)), "cq_gemm_ws differs from cq_gemm"
     idx = _rows(N, 24)
     y_ref, at = _oracle_rows(orc, wfmt, W, xq_np, K, idx)
     assert_within(y[:, idx], y_ref, at, what=f"{fmt} gemm")
