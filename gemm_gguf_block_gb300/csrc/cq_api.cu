@@ -213,8 +213,9 @@ cq_status gemm_common(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const vo
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* ws = need > 0 ? workspace : nullptr;
-    const cudaError_t e = w_fmt == CQ_Q4_K ? cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, ws, s)
-                                           : cq::launch_gemm_mma(dev, w_fmt, M, N, K, W, xq, y, ws, s);
+    const cudaError_t e = w_fmt == CQ_Q4_K  ? cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, ws, s)
+                          : ws != nullptr ? cq::launch_gemm_tc32(dev, w_fmt, M, N, K, W, xq, y, ws, s)
+                                          : cq::launch_gemm_mma(dev, w_fmt, M, N, K, W, xq, y, s);
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 

@@ -72,13 +72,16 @@ size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K);
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, void* workspace, cudaStream_t s);
 
-// Prefill GEMM of the 32-element formats (Q4_0, Q4_1, Q8_0; any M) on
-// mma.sync: y rows equal the cq_gemv rows bit for bit. With a workspace
-// (gemm32_workspace_size bytes, 256-byte aligned) the activations' operand
-// images are built once up front instead of in every CTA.
-size_t gemm32_workspace_size(int w_fmt, int64_t M, int64_t K);
+// Prefill GEMM of the 32-element formats (Q4_0, Q4_1, Q8_0; any M); y rows
+// equal the cq_gemv rows bit for bit. Without a workspace: mma.sync, each CTA
+// converting its activations. With one (gemm32_workspace_size bytes, 256-byte
+// aligned): the activation operand images are built once, and the tcgen05
+// kernel keeps one tensor-memory accumulator per 32-block.
 cudaError_t launch_gemm_mma(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
-                            const void* xq, float* y, void* workspace, cudaStream_t s);
+                            const void* xq, float* y, cudaStream_t s);
+size_t gemm32_workspace_size(int w_fmt, int64_t M, int64_t K);
+cudaError_t launch_gemm_tc32(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
+                             const void* xq, float* y, void* workspace, cudaStream_t s);
 
 // Byte offsets of the routed-FFN workspace sections (each 256-byte aligned).
 struct MoeLayout {

@@ -1,5 +1,6 @@
 // Prefill GEMM of Q4_0, Q4_1 and Q8_0 weights (x Q8_0 / Q8_1 activations)
-// for any number of tokens, on mma.sync.
+// for any number of tokens, on mma.sync, without a workspace (cq_gemm; with a
+// workspace, cq_gemm_ws runs the tensor-memory kernel of gemm_tc32.cu).
 //
 // cera README "Supported models": prompts are prefilled by a batched GEMM;
 // cera 0.5.3 README "Breaking changes in 0.4.0": the batched and the
@@ -9,13 +10,11 @@
 // thread per (row, token), so it equals the cq_gemv row bit for bit.
 //
 // One CTA = 128 weight rows x 64 tokens. Per 8-block segment a producer warp
-// TMA-loads the weight box (128 rows x 8 blocks, raw GGUF bytes) into one
-// stage of a ring, together with the tokens' activations. The activations'
-// B-operand image (fp16 fragments + a scale table, one per 64 tokens and
-// segment) is either built once per call by gemm32_prep_kernel into the
-// caller's workspace and bulk-copied (cq_gemm_ws), or built by the consumer
-// warps from the raw Q8_0 / Q8_1 blocks in every CTA (cq_gemm). The 8
-// consumer warps each take 16 weight rows: per block the integer dot is an
+// TMA-loads the weight box (128 rows x 8 blocks, raw GGUF bytes) and the
+// tokens' raw activation blocks (64 rows x 8 blocks) into one stage of a
+// ring. The consumer warps convert the activations into the CTA's B-operand
+// image (fp16 fragments + a scale table); then each of the 8 takes 16 weight
+// rows: per block the integer dot is an
 // exact fp16 mma.sync m16n8k16 product (see mma_frag.cuh) and the scale terms
 // run two tokens per f32x2 instruction. The grid walks the token tiles of one
 // row tile next to each other, so a weight tile is read from DRAM once and
@@ -41,8 +40,7 @@ constexpr int NT = TOK / 8;
 constexpr int CONSUMERS = 8;
 constexpr int THREADS = (CONSUMERS + 1) * 32;
 constexpr int MAX_STAGES = 8;
-// B-operand image of 64 tokens x one segment (the layout is the same in the
-// workspace and in shared memory):
+// B-operand image of 64 tokens x one segment, in shared memory:
 //   fp16 quants, 512 bytes per token: chunk c (16 bytes, lane t = c's B
 //     fragments of both k-steps, see act_frags) of block b of token tk at
 //     img_pos(tk, b, c);
@@ -58,20 +56,14 @@ __host__ __device__ constexpr int img_bytes(bool q8_1) {
 }
 __host__ __device__ constexpr int wbox_bytes(int bb) { return ROWS * mf::stage_pitch(bb); }
 __host__ __device__ constexpr int abox_bytes(int abb) { return TOK * SEGB * abb; }
-// Shared memory ahead of the stages: barriers, and without a workspace the
-// CTA's own image of the current segment.
-__host__ __device__ constexpr int fixed_bytes(bool pre, bool q8_1) { return 1024 + (pre ? 0 : img_bytes(q8_1)); }
-__host__ __device__ constexpr int stage_bytes(bool pre, int bb, int abb) {
-    return wbox_bytes(bb) + (pre ? img_bytes(abb == 36) : abox_bytes(abb));
-}
+// Shared memory ahead of the stages: barriers and the CTA's image of the
+// current segment.
+__host__ __device__ constexpr int fixed_bytes(bool q8_1) { return 1024 + img_bytes(q8_1); }
 
 struct GemmMmaParams {
-    const uint8_t* xq;      // activations (prep kernel)
-    const uint8_t* img;     // workspace: [token tile][segment] images (cq_gemm_ws)
     float* y;
     int* status;
     int M, N;
-    int nb;                 // 32-blocks per row
     int nseg;               // 8-block segments per row
     int stages;
 };
@@ -88,12 +80,12 @@ __host__ __device__ constexpr int img_pos(int tk, int b, int c) {
 // Converts one activation block (token tk of the tile, block b of the
 // segment) into the image at img.
 template <int WF>
-__device__ __forceinline__ void put_block(uint8_t* img, const uint8_t* blk, int tk, int b, bool valid) {
+__device__ __forceinline__ void put_block(uint8_t* img, const uint8_t* blk, int tk, int b) {
     using F = MF<WF>;
-    uint4 ch[4] = {};
-    float d = 0.0f, s = 0.0f;
-    int sum = 0;
-    if (valid) mf::act_frags<WF>(blk, ch, d, s, sum);
+    uint4 ch[4];
+    float d, s;
+    int sum;
+    mf::act_frags<WF>(blk, ch, d, s, sum);
 #pragma unroll
     for (int cc = 0; cc < 4; ++cc) *reinterpret_cast<uint4*>(img + img_pos(tk, b, cc)) = ch[cc];
     float* sc4f = reinterpret_cast<float*>(img + ACT_BYTES);
@@ -104,24 +96,7 @@ __device__ __forceinline__ void put_block(uint8_t* img, const uint8_t* blk, int 
     if constexpr (WF == CQ_Q4_1) sx2f[2 * j + hi] = s;
 }
 
-// The workspace images: one CTA per (segment, token tile); tokens past M
-// become zero blocks (d = 0, no quants).
 template <int WF>
-__global__ void __launch_bounds__(256) gemm32_prep_kernel(const GemmMmaParams p, uint8_t* img) {
-    pdl_trigger();
-    pdl_wait();
-    using F = MF<WF>;
-    constexpr int IMG = img_bytes(WF == CQ_Q4_1);
-    const int seg = blockIdx.x, tile = blockIdx.y;
-    uint8_t* dst = img + (static_cast<int64_t>(tile) * p.nseg + seg) * IMG;
-    for (int it = threadIdx.x; it < TOK * SEGB; it += blockDim.x) {
-        const int tk = it >> 3, b = it & 7;
-        const int m = tile * TOK + tk;
-        put_block<WF>(dst, p.xq + (static_cast<int64_t>(m) * p.nb + seg * SEGB + b) * F::ABB, tk, b, m < p.M);
-    }
-}
-
-template <int WF, bool PRE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                     const GemmMmaParams p) {
@@ -129,14 +104,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     pdl_wait();
     using F = MF<WF>;
     constexpr int WBOX = wbox_bytes(F::BB);
-    constexpr int IMG = img_bytes(WF == CQ_Q4_1);
-    constexpr int STAGE = stage_bytes(PRE, F::BB, F::ABB);
+    constexpr int STAGE = WBOX + abox_bytes(F::ABB);
     constexpr int PITCH = mf::stage_pitch(F::BB);
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + MAX_STAGES;
-    uint8_t* own_img = smem + 1024;                    // without a workspace
-    uint8_t* wst = smem + fixed_bytes(PRE, WF == CQ_Q4_1);
+    uint8_t* img = smem + 1024;
+    uint8_t* wst = smem + fixed_bytes(WF == CQ_Q4_1);
     const int S = p.stages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tok0 = blockIdx.x * TOK, r0 = blockIdx.y * ROWS;
@@ -163,11 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(STAGE));
                 // x counts 2-byte elements; rows past N / tokens past M read as zero
                 tc::tma_load_2d(dst, &wmap, k * SEGB * F::BB / 2, r0, &full[st]);
-                if constexpr (PRE)
-                    bulk_g2s(dst + WBOX, p.img + (static_cast<int64_t>(blockIdx.x) * p.nseg + k) * IMG, IMG,
-                             &full[st], policy_evict_last());
-                else
-                    tc::tma_load_2d(dst + WBOX, &amap, k * SEGB * F::ABB / 2, tok0, &full[st]);
+                tc::tma_load_2d(dst + WBOX, &amap, k * SEGB * F::ABB / 2, tok0, &full[st]);
             }
         }
         return;   // the producer takes no part in the consumers' named barriers
@@ -182,28 +152,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int k = 0; k < p.nseg; ++k) {
         const int st = k % S;
         const bool got = mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS);
-        const uint8_t* stage = wst + st * STAGE;
-        const uint8_t* img;
-        if constexpr (PRE) {
-            // a warp that timed out stops here; the others finish their copies
-            if (!got) {
-                if (lane == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
-                ok = false;
-                break;
-            }
-            img = stage + WBOX;
-        } else {
-            if (!tc::named_and(2, CONSUMERS * 32, got)) {
-                if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
-                ok = false;
-                break;
-            }
-            // The tokens' blocks of this segment as the CTA's own image.
-            for (int it = ct; it < TOK * SEGB; it += CONSUMERS * 32)
-                put_block<WF>(own_img, stage + WBOX + it * F::ABB, it >> 3, it & 7, true);
-            tc::named_and(1, CONSUMERS * 32, true);
-            img = own_img;
+        if (!tc::named_and(2, CONSUMERS * 32, got)) {
+            if (ct == 0) atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT);
+            ok = false;
+            break;
         }
+        const uint8_t* stage = wst + st * STAGE;
+        // The tokens' blocks of this segment as the CTA's image (tokens past M
+        // arrive as zero blocks).
+        for (int it = ct; it < TOK * SEGB; it += CONSUMERS * 32)
+            put_block<WF>(img, stage + WBOX + it * F::ABB, it >> 3, it & 7);
+        tc::named_and(1, CONSUMERS * 32, true);
         const float4* sc4 = reinterpret_cast<const float4*>(img + ACT_BYTES);
         const float2* sx2 = reinterpret_cast<const float2*>(img + ACT_BYTES + SC4_BYTES);
         const uint8_t* rg = stage + (16 * warp + g) * PITCH;
@@ -248,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[st]);
-        if constexpr (!PRE) tc::named_and(1, CONSUMERS * 32, true);   // the image is rewritten next segment
+        tc::named_and(1, CONSUMERS * 32, true);     // the image is rewritten by the next segment
     }
     if (ok) {
         // y[token][row]: rows r0 + 16w + g (+8), tokens tok0 + 8n + 2t (+1)
@@ -274,40 +233,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-template <int WF, bool PRE>
-cudaError_t launch_typed(const DeviceInfo& dev, const CUtensorMap& wmap, const CUtensorMap& amap, GemmMmaParams p,
-                         int64_t M, int64_t N, cudaStream_t s) {
-    using F = MF<WF>;
-    constexpr int STAGE = stage_bytes(PRE, F::BB, F::ABB);
-    constexpr int FIXED = fixed_bytes(PRE, WF == CQ_Q4_1);
-    const int lim = std::min(dev.smem_optin, 227 * 1024);
-    p.stages = std::min(MAX_STAGES, (lim - FIXED) / STAGE);
-    if (p.stages < 2) return cudaErrorInvalidConfiguration;
-    const int smem = FIXED + p.stages * STAGE;
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
-    if (e != cudaSuccess) return e;
-    if (devid >= 64 || raised[devid] < smem) {
-        e = cudaFuncSetAttribute(gemm_mma_kernel<WF, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = smem;
-    }
-    const int64_t row_tiles = (N + ROWS - 1) / ROWS;
-    if (row_tiles > 65535) return cudaErrorInvalidValue;      // grid y limit (N above 8.4 M rows)
-    const unsigned tok_tiles = static_cast<unsigned>((M + TOK - 1) / TOK);
-    if constexpr (PRE) {
-        e = launch_kernel(gemm32_prep_kernel<WF>, dim3(static_cast<unsigned>(p.nseg), tok_tiles), dim3(256), 0, s,
-                          p, const_cast<uint8_t*>(p.img));
-        if (e != cudaSuccess) return e;
-    }
-    return launch_kernel(gemm_mma_kernel<WF, PRE>, dim3(tok_tiles, static_cast<unsigned>(row_tiles)),
-                         dim3(THREADS), smem, s, wmap, amap, p);
-}
-
 template <int WF>
 cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
-                       float* y, void* workspace, cudaStream_t s) {
+                       float* y, cudaStream_t s) {
     using F = MF<WF>;
     tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
@@ -336,34 +264,43 @@ cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, c
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    constexpr int STAGE = wbox_bytes(F::BB) + abox_bytes(F::ABB);
+    constexpr int FIXED = fixed_bytes(WF == CQ_Q4_1);
+    const int lim = std::min(dev.smem_optin, 227 * 1024);
     GemmMmaParams p{};
-    p.xq = static_cast<const uint8_t*>(xq);
-    p.img = static_cast<const uint8_t*>(workspace);
     p.y = y;
     p.status = dev.status;
     p.M = static_cast<int>(M);
     p.N = static_cast<int>(N);
-    p.nb = nb;
     p.nseg = nb / SEGB;
-    return workspace != nullptr ? launch_typed<WF, true>(dev, wmap, amap, p, M, N, s)
-                                : launch_typed<WF, false>(dev, wmap, amap, p, M, N, s);
+    p.stages = std::min(MAX_STAGES, (lim - FIXED) / STAGE);
+    if (p.stages < 2) return cudaErrorInvalidConfiguration;
+    const int smem = FIXED + p.stages * STAGE;
+    static int raised[64] = {};
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e != cudaSuccess) return e;
+    if (devid >= 64 || raised[devid] < smem) {
+        e = cudaFuncSetAttribute(gemm_mma_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (devid < 64) raised[devid] = smem;
+    }
+    const int64_t row_tiles = (N + ROWS - 1) / ROWS;
+    if (row_tiles > 65535) return cudaErrorInvalidValue;      // grid y limit (N above 8.4 M rows)
+    return launch_kernel(gemm_mma_kernel<WF>, dim3(static_cast<unsigned>((M + TOK - 1) / TOK),
+                                                   static_cast<unsigned>(row_tiles)),
+                         dim3(THREADS), smem, s, wmap, amap, p);
 }
 
 }  // namespace
 
-size_t gemm32_workspace_size(int w_fmt, int64_t M, int64_t K) {
-    if ((w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) || M <= 0) return 0;
-    return static_cast<size_t>((M + TOK - 1) / TOK) * static_cast<size_t>(K / 256) *
-           static_cast<size_t>(img_bytes(w_fmt == CQ_Q4_1));
-}
-
 cudaError_t launch_gemm_mma(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
-                            const void* xq, float* y, void* workspace, cudaStream_t s) {
+                            const void* xq, float* y, cudaStream_t s) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     switch (w_fmt) {
-    case CQ_Q4_0: return launch_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, workspace, s);
-    case CQ_Q4_1: return launch_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, workspace, s);
-    case CQ_Q8_0: return launch_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, workspace, s);
+    case CQ_Q4_0: return launch_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q4_1: return launch_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q8_0: return launch_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, s);
     default: return cudaErrorInvalidValue;
     }
 }

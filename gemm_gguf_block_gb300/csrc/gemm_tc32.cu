@@ -1,0 +1,450 @@
+// Prefill GEMM of Q4_0, Q4_1 and Q8_0 weights on the 5th-generation tensor
+// cores (tcgen05.mma, accumulators in tensor memory), with a workspace.
+//
+// cera README "Supported models": prompts are prefilled by a batched GEMM;
+// cera 0.5.3 README "Breaking changes in 0.4.0": the batched and the
+// per-token paths give the same bits. The library's fixed fp32 order
+// (include/cq.h) needs the exact integer dot of every 32-element block on its
+// own -- c = fma(D(d_w) * D(d_x), isum, c) [+ fma(D(m_w), D(s_x), c)] per
+// block, y = y + c per four blocks -- so every block gets its own accumulator:
+//   A[n][k] = q(n, k) as fp16 (the weight quant's integer value: Q8_0 int8,
+//             Q4_0 nibble - 8, Q4_1 nibble; exact), MMA M = 128 rows
+//   B[m][k] = q8(m, k) as fp16 (exact), MMA N = 64 tokens
+// and |isum| <= 32 * 127 * 127 < 2^24, so each fp32 accumulator holds the
+// exact integer. One chunk (four blocks) uses 4 x 64 tensor-memory columns;
+// two chunk slots fill the 512 columns, so the MMAs of one chunk run while the
+// epilogue drains the other.
+//
+// Warp roles (832 threads): warp 0 is the producer (TMA boxes of raw weights,
+// 128 rows x 8 blocks, and bulk copies of the activation images that
+// gemm32_tc_prep_kernel wrote into the workspace); warp 1 allocates tensor
+// memory and one lane issues the MMAs; warps 2-9 convert the raw weights to
+// the fp16 A tile (K-major, no swizzle) and the per-row scale table; warps
+// 10-25 are the epilogue: tensor-memory lanes 32*(warp%4).. (weight rows),
+// 16 token columns each, y in registers. Every wait is bounded; a timeout
+// flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
+#include <algorithm>
+
+#include <cuda_fp16.h>
+
+#include "cq_device.cuh"
+#include "cq_internal.h"
+#include "mma_frag.cuh"
+#include "tc.cuh"
+
+namespace cq {
+namespace {
+
+using mf::MF;
+
+constexpr int BM = 128;          // weight rows per tile (MMA M, tensor-memory lanes)
+constexpr int BN = 64;           // tokens per tile (MMA N)
+constexpr int KC = 128;          // K per chunk: four 32-blocks
+constexpr int NRAW = 2;          // raw weight stages (one 8-block segment each)
+constexpr int NOP = 3;           // operand stages (one chunk each)
+constexpr int NCONV = 256;       // converter threads (warps 2-9)
+constexpr int EPI_WARPS = 16;
+constexpr int THREADS = (2 + 8 + EPI_WARPS) * 32;
+constexpr int EPI_COLS = BN / (EPI_WARPS / 4);          // 16 token columns per epilogue thread
+constexpr uint32_t TMEM_COLS = 512;                     // 2 chunk slots x 4 blocks x 64 columns
+constexpr int A_BYTES = BM * KC * 2;                    // 32 KB
+constexpr int B_BYTES = BN * KC * 2;                    // 16 KB
+
+// Activation image of (64-token tile, chunk): the B tile, then d_x [4][64]
+// and, for Q8_1, s_x [4][64] (fp32).
+__host__ __device__ constexpr int img_bytes(bool q8_1) { return B_BYTES + (q8_1 ? 2 : 1) * 4 * BN * 4; }
+// Per-row scales of a chunk: d_w [4][128] and, for Q4_1, m_w [4][128] (fp32).
+__host__ __device__ constexpr int wsc_bytes(bool q4_1) { return (q4_1 ? 2 : 1) * 4 * BM * 4; }
+__host__ __device__ constexpr int op_bytes(bool q4_1) { return A_BYTES + img_bytes(q4_1) + wsc_bytes(q4_1); }
+__host__ __device__ constexpr int raw_bytes(int bb) { return BM * mf::stage_pitch(bb); }
+
+enum { B_RAW_FULL = 0, B_RAW_EMPTY = 2, B_OP_FULL = 4, B_OP_EMPTY = 7, B_ACC_FULL = 10, B_ACC_EMPTY = 12 };
+constexpr int OFF_BAR = 0;
+constexpr int OFF_TMEM = 128;
+constexpr int OFF_FLAG = 136;
+constexpr int OFF_RAW = 1024;
+__host__ __device__ constexpr int off_op(int bb) { return OFF_RAW + NRAW * raw_bytes(bb); }
+__host__ __device__ constexpr int smem_bytes(int bb, bool q4_1) {
+    return off_op(bb) + NOP * op_bytes(q4_1) + 1024;     // + alignment slack of the dynamic base
+}
+
+struct Tc32Params {
+    const uint8_t* xq;
+    const uint8_t* img;     // workspace: [token tile][chunk] activation images
+    float* y;
+    int* status;
+    int M, N;
+    int nb;                 // 32-blocks per row
+    int nchunk;             // chunks (128 columns) per row
+};
+
+// Offset of element (r, k) in a K-major no-swizzle tile whose rows hold kt elements.
+__host__ __device__ constexpr int tile_off(int r, int k, int kt) {
+    return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* flag, int* status) {
+    if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
+    *flag = 1;
+    atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
+    return false;
+}
+
+// Four signed bytes -> two half2 holding the same integers, in byte order
+// (bytes 0, 1 | bytes 2, 3): (1152 + b) - 1152.
+__device__ __forceinline__ void s8x4_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
+    const __half2 k1152 = mf::u2h(0x64806480u);
+    o0 = mf::h2u(__hsub2(mf::u2h(mf::s8pair_1152(__byte_perm(w, 0u, 0x4140))), k1152));
+    o1 = mf::h2u(__hsub2(mf::u2h(mf::s8pair_1152(__byte_perm(w, 0u, 0x4342))), k1152));
+}
+// Nibbles of four bytes (selected by shift 0 = low, 4 = high) -> two half2
+// holding nibble - off (off = 1024 + bias: Q4_0 1032, Q4_1 1024).
+__device__ __forceinline__ void nib4_half(uint32_t w, int shift, __half2 off, uint32_t& o0, uint32_t& o1) {
+    const uint32_t p01 = __byte_perm(w, 0u, 0x4140) >> shift;
+    const uint32_t p23 = __byte_perm(w, 0u, 0x4342) >> shift;
+    o0 = mf::h2u(__hsub2(mf::u2h(mf::and_or(p01, 0x000F000Fu, 0x64006400u)), off));
+    o1 = mf::h2u(__hsub2(mf::u2h(mf::and_or(p23, 0x000F000Fu, 0x64006400u)), off));
+}
+
+template <int WF>
+__global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                               const Tc32Params p) {
+    pdl_trigger();
+    pdl_wait();
+    using F = MF<WF>;
+    constexpr bool Q41 = WF == CQ_Q4_1;
+    constexpr int PITCH = mf::stage_pitch(F::BB);
+    constexpr int RAWB = raw_bytes(F::BB);
+    constexpr int IMG = img_bytes(Q41);
+    constexpr int OPB = op_bytes(Q41);
+    constexpr int OFF_OP = off_op(F::BB);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_FLAG);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BN, n0 = blockIdx.y * BM;
+    const int nq = p.nchunk;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NRAW; ++i) {
+            mbar_init(&bars[B_RAW_FULL + i], 1);
+            mbar_init(&bars[B_RAW_EMPTY + i], NCONV);
+        }
+        for (int i = 0; i < NOP; ++i) {
+            mbar_init(&bars[B_OP_FULL + i], NCONV + 1);        // converters + the producer's image copy
+            mbar_init(&bars[B_OP_EMPTY + i], 1 + EPI_WARPS);   // the MMA commit + the epilogue's scale reads
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_ACC_FULL + i], 1);
+            mbar_init(&bars[B_ACC_EMPTY + i], EPI_WARPS);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_holder, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int s = 0; 2 * s < nq && !*abort_flag; ++s) {
+                const int r = s % NRAW;
+                if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAWB);
+                tc::tma_load_2d(smem + OFF_RAW + r * RAWB, &wmap, s * 8 * F::BB / 2, n0, &bars[B_RAW_FULL + r]);
+                bool ok = true;
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 2 * s + h, st = q % NOP;
+                    if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&bars[B_OP_FULL + st], IMG);
+                    bulk_g2s(smem + OFF_OP + st * OPB + A_BYTES,
+                             p.img + (static_cast<int64_t>(blockIdx.x) * nq + q) * IMG, IMG, &bars[B_OP_FULL + st],
+                             policy_evict_last());
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+            const uint32_t op0 = smem_u32(smem + OFF_OP);
+            for (int q = 0; q < nq && !*abort_flag; ++q) {
+                const int slot = q & 1, st = q % NOP;
+                if (!wait_or_abort(&bars[B_ACC_EMPTY + slot], ((q >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!wait_or_abort(&bars[B_OP_FULL + st], (q / NOP) & 1, abort_flag, p.status)) break;
+                tc::fence_after();
+                const uint32_t a0 = op0 + st * OPB, b0 = a0 + A_BYTES;
+                for (int b = 0; b < 4; ++b)
+                    for (int t = 0; t < 2; ++t)
+                        tc::mma_f16(tmem + slot * 256 + 64 * b, tc::smem_desc(a0 + 512 * b + 256 * t, 128, KC * 16),
+                                    tc::smem_desc(b0 + 512 * b + 256 * t, 128, KC * 16), idesc, t);
+                tc::commit(&bars[B_OP_EMPTY + st]);
+                tc::commit(&bars[B_ACC_FULL + slot]);
+            }
+        }
+    } else if (warp < 10) {
+        // --------------------------------------------------------- converters
+        // Thread (row r, half `part` of the chunk): blocks 2*part, 2*part + 1
+        // of the chunk, 32 elements each, as four 8-element core-matrix rows.
+        const int tid = threadIdx.x - 64;               // 0..255
+        const int r = tid & (BM - 1), part = tid >> 7;
+        for (int q = 0; q < nq; ++q) {
+            const int s = q >> 1, h = q & 1, st = q % NOP, rs = s % NRAW;
+            if (*abort_flag) break;
+            if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) break;
+            if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+            uint8_t* stg = smem + OFF_OP + st * OPB;
+            float* wsd = reinterpret_cast<float*>(stg + A_BYTES + IMG);
+            const uint8_t* row = smem + OFF_RAW + rs * RAWB + r * PITCH;
+#pragma unroll
+            for (int bb = 0; bb < 2; ++bb) {
+                const int cb = 2 * part + bb;                       // block within the chunk
+                const uint8_t* blk = row + (4 * h + cb) * F::BB;    // block within the segment
+                uint8_t* dst = stg + tile_off(r, 32 * cb, KC);
+                if constexpr (WF == CQ_Q8_0) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t o[4];
+                        s8x4_half(mf::ld_u32_a2(blk + 2 + 8 * i), o[0], o[1]);
+                        s8x4_half(mf::ld_u32_a2(blk + 6 + 8 * i), o[2], o[3]);
+                        *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    wsd[cb * BM + r] = h2f(*reinterpret_cast<const uint16_t*>(blk));
+                } else {
+                    const __half2 off = mf::u2h(Q41 ? 0x64006400u : 0x64086408u);   // 1024 or 1032
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = Q41 ? *reinterpret_cast<const uint32_t*>(blk + F::QO + 4 * i)
+                                   : mf::ld_u32_a2(blk + F::QO + 4 * i);
+                    // core rows 0, 1: low nibbles of bytes 0-7, 8-15; rows 2, 3: high nibbles
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int sh = i < 2 ? 0 : 4, wi = 2 * (i & 1);
+                        uint32_t o[4];
+                        nib4_half(w[wi], sh, off, o[0], o[1]);
+                        nib4_half(w[wi + 1], sh, off, o[2], o[3]);
+                        *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                    if constexpr (Q41) {
+                        const uint32_t dm = *reinterpret_cast<const uint32_t*>(blk);
+                        wsd[cb * BM + r] = h2f(dm);
+                        wsd[4 * BM + cb * BM + r] = h2f(dm >> 16);
+                    } else {
+                        wsd[cb * BM + r] = h2f(*reinterpret_cast<const uint16_t*>(blk));
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc::mbar_arrive(&bars[B_OP_FULL + st]);
+            if (h == 1) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+        }
+    } else {
+        // ----------------------------------------------------------- epilogue
+        const int quarter = warp & 3;
+        const int c0 = ((warp - 10) >> 2) * EPI_COLS;   // first token column of this warp
+        const int rl = quarter * 32 + lane;             // row within the tile
+        const int row = n0 + rl;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint64_t y[EPI_COLS / 2], c[EPI_COLS / 2];
+#pragma unroll
+        for (int i = 0; i < EPI_COLS / 2; ++i) y[i] = 0;
+        bool ok = true;
+        for (int q = 0; q < nq; ++q) {
+            const int slot = q & 1, st = q % NOP;
+            const bool got = mbar_wait_bounded(&bars[B_ACC_FULL + slot], (q >> 1) & 1, WAIT_LIMIT_NS) &&
+                             mbar_wait_bounded(&bars[B_OP_FULL + st], (q / NOP) & 1, WAIT_LIMIT_NS);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) { *abort_flag = 1; atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
+                ok = false;
+                break;
+            }
+            tc::fence_after();
+            const uint8_t* stg = smem + OFF_OP + st * OPB;
+            const float* dxs = reinterpret_cast<const float*>(stg + A_BYTES + B_BYTES);
+            const float* wsd = reinterpret_cast<const float*>(stg + A_BYTES + IMG);
+#pragma unroll
+            for (int i = 0; i < EPI_COLS / 2; ++i) c[i] = 0;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                uint32_t is[EPI_COLS];
+                tc::ld16(lane_addr + slot * 256 + 64 * b + c0, is);
+                const float dw = wsd[b * BM + rl];
+                const uint64_t dw2 = tc::pk(dw, dw);
+                const float4* dx4 = reinterpret_cast<const float4*>(dxs + b * BN + c0);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < EPI_COLS / 4; ++i) {
+                    const float4 x = dx4[i];
+                    // c = fma(d_w * d_x, isum, c), two tokens per instruction
+                    c[2 * i] = tc::fma2(tc::mul2(dw2, tc::pk(x.x, x.y)),
+                                        tc::pk(__uint_as_float(is[4 * i]), __uint_as_float(is[4 * i + 1])), c[2 * i]);
+                    c[2 * i + 1] =
+                        tc::fma2(tc::mul2(dw2, tc::pk(x.z, x.w)),
+                                 tc::pk(__uint_as_float(is[4 * i + 2]), __uint_as_float(is[4 * i + 3])), c[2 * i + 1]);
+                }
+                if constexpr (Q41) {
+                    const float mw = wsd[4 * BM + b * BM + rl];
+                    const uint64_t mw2 = tc::pk(mw, mw);
+                    const float4* sx4 = reinterpret_cast<const float4*>(dxs + 4 * BN + b * BN + c0);
+#pragma unroll
+                    for (int i = 0; i < EPI_COLS / 4; ++i) {
+                        const float4 x = sx4[i];
+                        c[2 * i] = tc::fma2(mw2, tc::pk(x.x, x.y), c[2 * i]);
+                        c[2 * i + 1] = tc::fma2(mw2, tc::pk(x.z, x.w), c[2 * i + 1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < EPI_COLS / 2; ++i) y[i] = tc::add2(y[i], c[i]);
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&bars[B_ACC_EMPTY + slot]);
+                tc::mbar_arrive(&bars[B_OP_EMPTY + st]);
+            }
+        }
+        if (ok && row < p.N) {
+            // y[m][row]: a warp's stores to one token are 32 consecutive floats
+#pragma unroll
+            for (int i = 0; i < EPI_COLS / 2; ++i) {
+                float v[2];
+                tc::upk(y[i], v[0], v[1]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int m = m0 + c0 + 2 * i + j;
+                    if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = v[j];
+                }
+            }
+        }
+    }
+
+    // Wind down: every role has left its loop; make sure no copy or MMA is in
+    // flight before the tensor memory and the CTA's shared memory go.
+    tc::fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) {
+        for (int i = 0; i < NRAW; ++i) (void)mbar_wait_bounded(&bars[B_RAW_FULL + i], 0, WAIT_LIMIT_NS / 8);
+        for (int i = 0; i < 2; ++i) (void)mbar_wait_bounded(&bars[B_ACC_FULL + i], 0, WAIT_LIMIT_NS / 8);
+    }
+    __syncthreads();
+    tc::fence_after();
+    if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// The workspace images: one CTA per (chunk q, token tile), thread (token t,
+// block b): the block's 32 quants as fp16 into the K-major B tile, and its
+// d_x (and s_x for Q8_1). Tokens past M become zeros.
+template <int WF>
+__global__ void __launch_bounds__(256) gemm32_tc_prep_kernel(const Tc32Params p, uint8_t* img) {
+    pdl_trigger();
+    pdl_wait();
+    using F = MF<WF>;
+    constexpr int IMG = img_bytes(WF == CQ_Q4_1);
+    const int q = blockIdx.x, tile = blockIdx.y;
+    const int t = threadIdx.x >> 2, b = threadIdx.x & 3;
+    const int m = tile * BN + t;
+    uint8_t* dst = img + (static_cast<int64_t>(tile) * p.nchunk + q) * IMG;
+    float* dxs = reinterpret_cast<float*>(dst + B_BYTES);
+    float d = 0.0f, s = 0.0f;
+    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (m < p.M) {
+        const uint8_t* blk = p.xq + (static_cast<int64_t>(m) * p.nb + 4 * q + b) * F::ABB;
+        const uint16_t* hw = reinterpret_cast<const uint16_t*>(blk);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = __byte_perm(hw[F::AQO / 2 + 2 * j], hw[F::AQO / 2 + 2 * j + 1], 0x5410);
+        d = h2f(hw[0]);
+        s = WF == CQ_Q4_1 ? h2f(hw[1]) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t o[4];
+        s8x4_half(w[2 * i], o[0], o[1]);
+        s8x4_half(w[2 * i + 1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + tile_off(t, 32 * b + 8 * i, KC)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    dxs[b * BN + t] = d;
+    if constexpr (WF == CQ_Q4_1) dxs[4 * BN + b * BN + t] = s;
+}
+
+template <int WF>
+cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
+                       float* y, void* workspace, cudaStream_t s) {
+    using F = MF<WF>;
+    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
+    const int nb = static_cast<int>(K / 32);
+    const int64_t wrow = static_cast<int64_t>(nb) * F::BB;
+    // Raw weights as a 2-D tensor of 2-byte elements [N rows][wrow / 2]; a box
+    // is one 8-block segment of 128 rows; rows past N read as zero.
+    CUtensorMap wmap;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(wrow / 2), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(wrow)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mf::stage_pitch(F::BB) / 2), BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    constexpr int SMEM = smem_bytes(F::BB, WF == CQ_Q4_1);
+    if (SMEM > dev.smem_optin) return cudaErrorInvalidConfiguration;
+    const int64_t row_tiles = (N + BM - 1) / BM;
+    if (row_tiles > 65535) return cudaErrorInvalidValue;      // grid y limit (N above 8.4 M rows)
+    static int raised[64] = {};
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e != cudaSuccess) return e;
+    if (devid >= 64 || !raised[devid]) {
+        e = cudaFuncSetAttribute(gemm32_tc_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        if (devid < 64) raised[devid] = 1;
+    }
+    Tc32Params p{};
+    p.xq = static_cast<const uint8_t*>(xq);
+    p.img = static_cast<const uint8_t*>(workspace);
+    p.y = y;
+    p.status = dev.status;
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.nb = nb;
+    p.nchunk = nb / 4;
+    const unsigned tok_tiles = static_cast<unsigned>((M + BN - 1) / BN);
+    e = launch_kernel(gemm32_tc_prep_kernel<WF>, dim3(static_cast<unsigned>(p.nchunk), tok_tiles), dim3(256), 0, s, p,
+                      static_cast<uint8_t*>(workspace));
+    if (e != cudaSuccess) return e;
+    return launch_kernel(gemm32_tc_kernel<WF>, dim3(tok_tiles, static_cast<unsigned>(row_tiles)), dim3(THREADS),
+                         SMEM, s, wmap, p);
+}
+
+}  // namespace
+
+size_t gemm32_workspace_size(int w_fmt, int64_t M, int64_t K) {
+    if ((w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) || M <= 0) return 0;
+    return static_cast<size_t>((M + BN - 1) / BN) * static_cast<size_t>(K / KC) *
+           static_cast<size_t>(img_bytes(w_fmt == CQ_Q4_1));
+}
+
+cudaError_t launch_gemm_tc32(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
+                             const void* xq, float* y, void* workspace, cudaStream_t s) {
+    if (M <= 0 || N <= 0) return cudaSuccess;
+    switch (w_fmt) {
+    case CQ_Q4_0: return launch_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, workspace, s);
+    case CQ_Q4_1: return launch_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, workspace, s);
+    case CQ_Q8_0: return launch_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, workspace, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace cq

@@ -187,8 +187,11 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
  * instead of in every weight tile. Same result, bit for bit, as cq_gemm.
  * cq_gemm_workspace_size returns the bytes needed (0 for an unsupported
  * format or shape): ceil(M/128) * (K/256) * 70144 for Q4_K;
- * ceil(M/64) * (K/256) * 36992 for Q4_0 and Q8_0 (Q8_0 activations) and
- * ceil(M/64) * (K/256) * 39168 for Q4_1 (Q8_1 activations). The workspace
+ * ceil(M/64) * (K/128) * 17408 for Q4_0 and Q8_0 (Q8_0 activations) and
+ * ceil(M/64) * (K/128) * 18432 for Q4_1 (Q8_1 activations). For these three
+ * formats cq_gemm_ws runs a different kernel from cq_gemm (tcgen05 with one
+ * tensor-memory accumulator per 32-block, against mma.sync); the results
+ * are the same bits. The workspace
  * must be 256-byte aligned; it is scratch (no state is kept between calls),
  * and two calls that may overlap on the GPU need separate workspaces.
  * Errors as cq_gemm, plus CQ_ERR_WORKSPACE (NULL or too small) and

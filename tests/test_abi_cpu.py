@@ -63,20 +63,22 @@ def test_gemv_token_limit(L):
 def test_gemm_32_block_formats(L):
     """cq_gemm takes Q4_0 / Q4_1 / Q8_0 at any M; their activation rows go
     through TMA, so xq must be 16-byte aligned. cq_gemm_ws takes one operand
-    image per 64 tokens and 256 columns: 36992 bytes (Q8_0 activations) or
-    39168 (Q8_1, with the s table)."""
-    for fmt, img in ((cq.Q4_0, 36992), (cq.Q4_1, 39168), (cq.Q8_0, 36992)):
-        assert cq.cq_gemm_workspace_size(fmt, 512, 4096, 4096) == 8 * 16 * img
-        assert cq.cq_gemm_workspace_size(fmt, 65, 8, 256) == 2 * 1 * img
+    image per 64 tokens and 128 columns: 17408 bytes (Q8_0 activations) or
+    18432 (Q8_1, with the s table)."""
+    for fmt, img in ((cq.Q4_0, 17408), (cq.Q4_1, 18432), (cq.Q8_0, 17408)):
+        assert cq.cq_gemm_workspace_size(fmt, 512, 4096, 4096) == 8 * 32 * img
+        assert cq.cq_gemm_workspace_size(fmt, 65, 8, 256) == 2 * 2 * img
         assert cq.cq_gemm(fmt, 4, 8, 100, A, A, A) == cq.ERR_SHAPE
         assert cq.cq_gemm(fmt, 4, 8, 256, A, A + 4, A) == cq.ERR_ALIGNMENT
         assert cq.cq_gemm(fmt, 4, 8, 256, A + 2, A, A) == cq.ERR_ALIGNMENT
         assert cq.cq_gemm(fmt, 4, 8, 256, A, None, A) == cq.ERR_INVALID_ARG
         assert cq.cq_gemm(fmt, 0, 8, 256, None, None, None) == cq.OK
-        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A, A, None, img) == cq.ERR_WORKSPACE
-        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A, A, A, img - 1) == cq.ERR_WORKSPACE
-        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A, A, A + 128, img) == cq.ERR_ALIGNMENT
-        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A + 8, A, A, img) == cq.ERR_ALIGNMENT
+        need = cq.cq_gemm_workspace_size(fmt, 4, 8, 256)
+        assert need == 2 * img
+        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A, A, None, need) == cq.ERR_WORKSPACE
+        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A, A, A, need - 1) == cq.ERR_WORKSPACE
+        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A, A, A + 128, need) == cq.ERR_ALIGNMENT
+        assert cq.cq_gemm_ws(fmt, 4, 8, 256, A, A + 8, A, A, need) == cq.ERR_ALIGNMENT
         assert cq.cq_gemm_ws(fmt, 0, 8, 256, None, None, None, None, 0) == cq.OK
 
 
