@@ -106,6 +106,76 @@ __device__ __forceinline__ void nib4_half(uint32_t w, int shift, __half2 off, ui
     o1 = mf::h2u(__hsub2(mf::u2h(mf::and_or(p23, 0x000F000Fu, 0x64006400u)), off));
 }
 
+// Four bytes at byte offset B (even) of a register window of words.
+template <int B, int NW>
+__device__ __forceinline__ uint32_t win_u32(const uint32_t (&w)[NW]) {
+    static_assert(B + 4 <= 4 * NW, "window too short");
+    if constexpr (B % 4 == 0) return w[B / 4];
+    else return __funnelshift_r(w[B / 4], w[B / 4 + 1], 8 * (B % 4));
+}
+template <int B, int NW>
+__device__ __forceinline__ uint32_t win_u16(const uint32_t (&w)[NW]) {
+    static_assert(B % 2 == 0 && B + 2 <= 4 * NW, "bad half-word offset");
+    return B % 4 == 0 ? (w[B / 4] & 0xffffu) : (w[B / 4] >> 16);
+}
+
+// One weight block starting at byte BASE of the window: its 32 quants as
+// four 8-element core-matrix rows of the A tile (dst = the block's first
+// row), and its d_w (and m_w for Q4_1).
+template <int WF, int BASE, int NW>
+__device__ __forceinline__ void convert_block(const uint32_t (&w)[NW], uint8_t* dst, float& d, float& mn) {
+    if constexpr (WF == CQ_Q8_0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t o[4];
+            // i is unrolled: the offsets are compile-time after unrolling
+            const uint32_t a = i == 0 ? win_u32<BASE + 2, NW>(w) : i == 1 ? win_u32<BASE + 10, NW>(w)
+                             : i == 2 ? win_u32<BASE + 18, NW>(w) : win_u32<BASE + 26, NW>(w);
+            const uint32_t b = i == 0 ? win_u32<BASE + 6, NW>(w) : i == 1 ? win_u32<BASE + 14, NW>(w)
+                             : i == 2 ? win_u32<BASE + 22, NW>(w) : win_u32<BASE + 30, NW>(w);
+            s8x4_half(a, o[0], o[1]);
+            s8x4_half(b, o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        d = h2f(win_u16<BASE, NW>(w));
+        mn = 0.0f;
+    } else {
+        constexpr bool Q41 = WF == CQ_Q4_1;
+        constexpr int QO = Q41 ? 4 : 2;
+        const __half2 off = mf::u2h(Q41 ? 0x64006400u : 0x64086408u);   // 1024 or 1032
+        const uint32_t q[4] = {win_u32<BASE + QO, NW>(w), win_u32<BASE + QO + 4, NW>(w),
+                               win_u32<BASE + QO + 8, NW>(w), win_u32<BASE + QO + 12, NW>(w)};
+        // core rows 0, 1: low nibbles of bytes 0-7, 8-15; rows 2, 3: high nibbles
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int sh = i < 2 ? 0 : 4, wi = 2 * (i & 1);
+            uint32_t o[4];
+            nib4_half(q[wi], sh, off, o[0], o[1]);
+            nib4_half(q[wi + 1], sh, off, o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if constexpr (Q41) {
+            const uint32_t dm = win_u32<BASE, NW>(w);
+            d = h2f(dm);
+            mn = h2f(dm >> 16);
+        } else {
+            d = h2f(win_u16<BASE, NW>(w));
+            mn = 0.0f;
+        }
+    }
+}
+
+// A converter thread's two consecutive blocks, which start at byte OFF of its
+// 16-byte-aligned window.
+template <int WF, int OFF, int NW>
+__device__ __forceinline__ void convert_pair(const uint32_t (&w)[NW], uint8_t* dst, float (&d)[2], float (&mn)[2]) {
+    constexpr int BB = MF<WF>::BB;
+    if constexpr (OFF + 2 * BB + (WF == CQ_Q8_0 ? 0 : 0) <= 4 * NW) {
+        convert_block<WF, OFF, NW>(w, dst, d[0], mn[0]);
+        convert_block<WF, OFF + BB, NW>(w, dst + 512, d[1], mn[1]);   // next block: 4 core matrices on
+    }
+}
+
 template <int WF>
 __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                                                                const Tc32Params p) {
@@ -198,6 +268,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
         // --------------------------------------------------------- converters
         // Thread (row r, half `part` of the chunk): blocks 2*part, 2*part + 1
         // of the chunk, 32 elements each, as four 8-element core-matrix rows.
+        // The thread loads the 16-byte-aligned window that holds its two
+        // blocks with 128-bit loads: the raw rows are a multiple of 16 bytes
+        // and an odd multiple of 16 modulo 128, so the 8 rows of a load phase
+        // fall in 8 different bank groups. Its byte offset in the window
+        // depends only on (h, part), so it is uniform across the warp.
+        constexpr int NW = WF == CQ_Q8_0 ? 20 : WF == CQ_Q4_1 ? 16 : 12;
         const int tid = threadIdx.x - 64;               // 0..255
         const int r = tid & (BM - 1), part = tid >> 7;
         for (int q = 0; q < nq; ++q) {
@@ -207,45 +283,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_OP + st * OPB;
             float* wsd = reinterpret_cast<float*>(stg + A_BYTES + IMG);
-            const uint8_t* row = smem + OFF_RAW + rs * RAWB + r * PITCH;
+            const int off = (4 * h + 2 * part) * F::BB;         // the two blocks' byte offset in the row
+            const uint8_t* win = smem + OFF_RAW + rs * RAWB + r * PITCH + (off & ~15);
+            uint32_t w[NW];
+#pragma unroll
+            for (int i = 0; i < NW / 4; ++i) {
+                const uint4 v = *reinterpret_cast<const uint4*>(win + 16 * i);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+            uint8_t* dst = stg + tile_off(r, 64 * part, KC);
+            float d[2], mn[2];
+            switch (off & 15) {
+            case 0: convert_pair<WF, 0>(w, dst, d, mn); break;
+            case 4: convert_pair<WF, 4>(w, dst, d, mn); break;
+            case 8: convert_pair<WF, 8>(w, dst, d, mn); break;
+            default: convert_pair<WF, 12>(w, dst, d, mn); break;
+            }
 #pragma unroll
             for (int bb = 0; bb < 2; ++bb) {
-                const int cb = 2 * part + bb;                       // block within the chunk
-                const uint8_t* blk = row + (4 * h + cb) * F::BB;    // block within the segment
-                uint8_t* dst = stg + tile_off(r, 32 * cb, KC);
-                if constexpr (WF == CQ_Q8_0) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t o[4];
-                        s8x4_half(mf::ld_u32_a2(blk + 2 + 8 * i), o[0], o[1]);
-                        s8x4_half(mf::ld_u32_a2(blk + 6 + 8 * i), o[2], o[3]);
-                        *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                    wsd[cb * BM + r] = h2f(*reinterpret_cast<const uint16_t*>(blk));
-                } else {
-                    const __half2 off = mf::u2h(Q41 ? 0x64006400u : 0x64086408u);   // 1024 or 1032
-                    uint32_t w[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        w[i] = Q41 ? *reinterpret_cast<const uint32_t*>(blk + F::QO + 4 * i)
-                                   : mf::ld_u32_a2(blk + F::QO + 4 * i);
-                    // core rows 0, 1: low nibbles of bytes 0-7, 8-15; rows 2, 3: high nibbles
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int sh = i < 2 ? 0 : 4, wi = 2 * (i & 1);
-                        uint32_t o[4];
-                        nib4_half(w[wi], sh, off, o[0], o[1]);
-                        nib4_half(w[wi + 1], sh, off, o[2], o[3]);
-                        *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
-                    if constexpr (Q41) {
-                        const uint32_t dm = *reinterpret_cast<const uint32_t*>(blk);
-                        wsd[cb * BM + r] = h2f(dm);
-                        wsd[4 * BM + cb * BM + r] = h2f(dm >> 16);
-                    } else {
-                        wsd[cb * BM + r] = h2f(*reinterpret_cast<const uint16_t*>(blk));
-                    }
-                }
+                wsd[(2 * part + bb) * BM + r] = d[bb];
+                if constexpr (Q41) wsd[4 * BM + (2 * part + bb) * BM + r] = mn[bb];
             }
             fence_proxy_async_smem();
             tc::mbar_arrive(&bars[B_OP_FULL + st]);
