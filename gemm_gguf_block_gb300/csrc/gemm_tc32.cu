@@ -21,7 +21,7 @@
 // memory and one lane issues the MMAs; warps 2-9 convert the raw weights to
 // the fp16 A tile (K-major, no swizzle) and the per-row scale table; warps
 // 10-25 are the epilogue: tensor-memory lanes 32*(warp%4).. (weight rows),
-// 16 token columns each, y in registers. Every wait is bounded; a timeout
+// 16 token columns each, read as 16x256b fragments, y in registers. Every wait is bounded; a timeout
 // flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
 
@@ -310,14 +310,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
         }
     } else {
         // ----------------------------------------------------------- epilogue
+        // Warp w drains tensor-memory lanes 32*(w%4).. (weight rows) for the 16
+        // token columns of its column group, in 16x256b fragments: thread t holds
+        // rows 16h + t/4 + 8e (h, e in {0, 1}) and tokens 8j + 2(t%4) + u (j, u in
+        // {0, 1}) of that slice, so it reads only its own two token pairs' scales
+        // (a warp-uniform scale vector would cost one shared-memory wavefront per
+        // quarter warp).
         const int quarter = warp & 3;
         const int c0 = ((warp - 10) >> 2) * EPI_COLS;   // first token column of this warp
-        const int rl = quarter * 32 + lane;             // row within the tile
-        const int row = n0 + rl;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        uint64_t y[EPI_COLS / 2], c[EPI_COLS / 2];
+        const int g = lane >> 2, tq = lane & 3;
+        uint64_t y[8], c[8];                            // [h][e][j], token pair u = 0, 1
 #pragma unroll
-        for (int i = 0; i < EPI_COLS / 2; ++i) y[i] = 0;
+        for (int i = 0; i < 8; ++i) y[i] = 0;
         bool ok = true;
         for (int q = 0; q < nq; ++q) {
             const int slot = q & 1, st = q % NOP;
@@ -333,39 +337,55 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             const float* dxs = reinterpret_cast<const float*>(stg + A_BYTES + B_BYTES);
             const float* wsd = reinterpret_cast<const float*>(stg + A_BYTES + IMG);
 #pragma unroll
-            for (int i = 0; i < EPI_COLS / 2; ++i) c[i] = 0;
+            for (int i = 0; i < 8; ++i) c[i] = 0;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
-                uint32_t is[EPI_COLS];
-                tc::ld16(lane_addr + slot * 256 + 64 * b + c0, is);
-                const float dw = wsd[b * BM + rl];
-                const uint64_t dw2 = tc::pk(dw, dw);
-                const float4* dx4 = reinterpret_cast<const float4*>(dxs + b * BN + c0);
+                uint32_t is[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tc::ld16x256b_x2(tmem + (static_cast<uint32_t>(quarter * 32 + 16 * h) << 16) + slot * 256 + 64 * b +
+                                         c0,
+                                     is[h]);
+                float dw[2][2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) dw[h][e] = wsd[b * BM + quarter * 32 + 16 * h + 8 * e + g];
+                float2 dx[2];
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+                    dx[jj] = *reinterpret_cast<const float2*>(dxs + b * BN + c0 + 8 * jj + 2 * tq);
                 tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < EPI_COLS / 4; ++i) {
-                    const float4 x = dx4[i];
-                    // c = fma(d_w * d_x, isum, c), two tokens per instruction
-                    c[2 * i] = tc::fma2(tc::mul2(dw2, tc::pk(x.x, x.y)),
-                                        tc::pk(__uint_as_float(is[4 * i]), __uint_as_float(is[4 * i + 1])), c[2 * i]);
-                    c[2 * i + 1] =
-                        tc::fma2(tc::mul2(dw2, tc::pk(x.z, x.w)),
-                                 tc::pk(__uint_as_float(is[4 * i + 2]), __uint_as_float(is[4 * i + 3])), c[2 * i + 1]);
-                }
-                if constexpr (Q41) {
-                    const float mw = wsd[4 * BM + b * BM + rl];
-                    const uint64_t mw2 = tc::pk(mw, mw);
-                    const float4* sx4 = reinterpret_cast<const float4*>(dxs + 4 * BN + b * BN + c0);
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int i = 0; i < EPI_COLS / 4; ++i) {
-                        const float4 x = sx4[i];
-                        c[2 * i] = tc::fma2(mw2, tc::pk(x.x, x.y), c[2 * i]);
-                        c[2 * i + 1] = tc::fma2(mw2, tc::pk(x.z, x.w), c[2 * i + 1]);
+                    for (int e = 0; e < 2; ++e)
+#pragma unroll
+                        for (int jj = 0; jj < 2; ++jj) {
+                            uint64_t& cc = c[4 * h + 2 * e + jj];
+                            // c = fma(d_w * d_x, isum, c), two tokens per instruction
+                            cc = tc::fma2(tc::mul2(tc::pk(dw[h][e], dw[h][e]), tc::pk(dx[jj].x, dx[jj].y)),
+                                          tc::pk(__uint_as_float(is[h][4 * jj + 2 * e]),
+                                                 __uint_as_float(is[h][4 * jj + 2 * e + 1])),
+                                          cc);
+                        }
+                if constexpr (Q41) {
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const float2 sx = *reinterpret_cast<const float2*>(dxs + 4 * BN + b * BN + c0 + 8 * jj + 2 * tq);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const float mw = wsd[4 * BM + b * BM + quarter * 32 + 16 * h + 8 * e + g];
+                                uint64_t& cc = c[4 * h + 2 * e + jj];
+                                cc = tc::fma2(tc::pk(mw, mw), tc::pk(sx.x, sx.y), cc);
+                            }
                     }
                 }
             }
 #pragma unroll
-            for (int i = 0; i < EPI_COLS / 2; ++i) y[i] = tc::add2(y[i], c[i]);
+            for (int i = 0; i < 8; ++i) y[i] = tc::add2(y[i], c[i]);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -373,18 +393,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
                 tc::mbar_arrive(&bars[B_OP_EMPTY + st]);
             }
         }
-        if (ok && row < p.N) {
-            // y[m][row]: a warp's stores to one token are 32 consecutive floats
+        if (ok) {
 #pragma unroll
-            for (int i = 0; i < EPI_COLS / 2; ++i) {
-                float v[2];
-                tc::upk(y[i], v[0], v[1]);
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    const int m = m0 + c0 + 2 * i + j;
-                    if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = v[j];
+                for (int e = 0; e < 2; ++e) {
+                    const int row = n0 + quarter * 32 + 16 * h + 8 * e + g;
+                    if (row >= p.N) continue;
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        float v[2];
+                        tc::upk(y[4 * h + 2 * e + jj], v[0], v[1]);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int m = m0 + c0 + 8 * jj + 2 * tq + u;
+                            if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = v[u];
+                        }
+                    }
                 }
-            }
         }
     }
 

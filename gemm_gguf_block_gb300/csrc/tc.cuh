@@ -87,6 +87,15 @@ __device__ __forceinline__ void st8(uint32_t taddr, const uint32_t (&r)[8]) {
                  ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                  : "memory");
 }
+// 16 lanes x 256 bits, twice along the columns: per 8-column group, thread t
+// holds (lane t/4, columns 2(t%4), 2(t%4)+1) and (lane t/4 + 8, the same
+// columns) -- the layout of an mma.sync m16n8 accumulator; r[4g..4g+3] is
+// column group g.
+__device__ __forceinline__ void ld16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 // Column-count-generic forms (8 or 16).
 template <int W> __device__ __forceinline__ void ldw(uint32_t taddr, uint32_t (&r)[W]) {
     if constexpr (W == 8) ld8(taddr, r); else ld16(taddr, r);
