@@ -101,6 +101,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// A flag word in this CTA's shared memory, read and written with explicit
+// shared-space instructions: a pointer rebuilt from an aligned integer address
+// would otherwise be accessed as generic memory, a long-latency load on every
+// check.
+struct SmemFlag {
+    uint32_t addr;
+    __device__ __forceinline__ int get() const {
+        int v;
+        asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+        return v;
+    }
+    __device__ __forceinline__ void set(int v) const {
+        asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+    }
+};
+
 // Bounded wait for a phase to complete: gives up after `limit_ns` of wall
 // time (checked every 256 polls) and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {

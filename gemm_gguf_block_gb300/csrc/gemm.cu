@@ -97,9 +97,9 @@ __device__ __forceinline__ int tile_off(int r, int k, int kt) {
     return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* flag, int* status) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
     if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
-    *flag = 1;
+    flag.set(1);
     atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
     return false;
 }
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_FLAG);
+    const SmemFlag abort_flag{smem_u32(smem + OFF_FLAG)};
     float* dxbuf = reinterpret_cast<float*>(smem + OFF_DX);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
         }
         mbar_init(&bars[B_ACC_FULL], 1);
         mbar_init(&bars[B_ACC_EMPTY], NEPI);
-        *abort_flag = 0;
+        abort_flag.set(0);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            for (int s = 0; s < ns && !*abort_flag; ++s) {
+            for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 const int r = s % NRAW;
                 if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAW_BYTES);
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
             const uint32_t stage0 = smem_u32(smem + OFF_STAGE);
-            for (int s = 0; s < ns && !*abort_flag; ++s) {
+            for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 if (!wait_or_abort(&bars[B_ACC_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
                 bool ok = true;
                 for (int h = 0; h < 2; ++h) {
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
         if constexpr (!PRE) fetch(0, cur, bcur);
         for (int q = 0; q < 2 * ns; ++q) {
             const int s = q >> 1, h = q & 1, st = q % NSTAGE, rs = s % NRAW;
-            if (*abort_flag) break;
+            if (abort_flag.get()) break;
             if constexpr (!PRE)
                 if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt);
             if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
             // barrier also publishes dxbuf).
             const bool got = mbar_wait_bounded(&bars[B_ACC_FULL], s & 1, WAIT_LIMIT_NS);
             if (!tc::named_and(1, NEPI, got)) {
-                if (et == 0) { *abort_flag = 1; atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
+                if (et == 0) { abort_flag.set(1); atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
                 break;
             }
             tc::fence_after();
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
             tc::fence_before();
             tc::mbar_arrive(&bars[B_ACC_EMPTY]);
         }
-        if (__all_sync(0xffffffffu, !*abort_flag)) {
+        if (__all_sync(0xffffffffu, !abort_flag.get())) {
             // y[m][n] for this row: a warp's stores to one token are 32 consecutive floats.
             if constexpr (PRE) {
                 if (row_ok) {
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
     // flight before the tensor memory and the CTA's shared memory go.
     tc::fence_before();
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
+    if (abort_flag.get() && threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) (void)mbar_wait_bounded(&bars[B_RAW_FULL + i], 0, WAIT_LIMIT_NS / 8);
         (void)mbar_wait_bounded(&bars[B_ACC_FULL], 0, WAIT_LIMIT_NS / 8);
     }

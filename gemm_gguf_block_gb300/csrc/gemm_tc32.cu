@@ -83,9 +83,9 @@ __host__ __device__ constexpr int tile_off(int r, int k, int kt) {
     return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* flag, int* status) {
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
     if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
-    *flag = 1;
+    flag.set(1);
     atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
     return false;
 }
@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_FLAG);
+    const SmemFlag abort_flag{smem_u32(smem + OFF_FLAG)};
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BN, n0 = blockIdx.y * BM;
     const int nq = p.nchunk;
@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             mbar_init(&bars[B_ACC_FULL + i], 1);
             mbar_init(&bars[B_ACC_EMPTY + i], EPI_WARPS);
         }
-        *abort_flag = 0;
+        abort_flag.set(0);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
     if (warp == 0) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
-            for (int s = 0; 2 * s < nq && !*abort_flag; ++s) {
+            for (int s = 0; 2 * s < nq && !abort_flag.get(); ++s) {
                 const int r = s % NRAW;
                 if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAWB);
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
             const uint32_t op0 = smem_u32(smem + OFF_OP);
-            for (int q = 0; q < nq && !*abort_flag; ++q) {
+            for (int q = 0; q < nq && !abort_flag.get(); ++q) {
                 const int slot = q & 1, st = q % NOP;
                 if (!wait_or_abort(&bars[B_ACC_EMPTY + slot], ((q >> 1) & 1) ^ 1, abort_flag, p.status)) break;
                 if (!wait_or_abort(&bars[B_OP_FULL + st], (q / NOP) & 1, abort_flag, p.status)) break;
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
         const int r = tid & (BM - 1), part = tid >> 7;
         for (int q = 0; q < nq; ++q) {
             const int s = q >> 1, h = q & 1, st = q % NOP, rs = s % NRAW;
-            if (*abort_flag) break;
+            if (abort_flag.get()) break;
             if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) break;
             if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_OP + st * OPB;
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             const bool got = mbar_wait_bounded(&bars[B_ACC_FULL + slot], (q >> 1) & 1, WAIT_LIMIT_NS) &&
                              mbar_wait_bounded(&bars[B_OP_FULL + st], (q / NOP) & 1, WAIT_LIMIT_NS);
             if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0) { *abort_flag = 1; atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
+                if (lane == 0) { abort_flag.set(1); atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
                 ok = false;
                 break;
             }
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
     // flight before the tensor memory and the CTA's shared memory go.
     tc::fence_before();
     __syncthreads();
-    if (*abort_flag && threadIdx.x == 0) {
+    if (abort_flag.get() && threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) (void)mbar_wait_bounded(&bars[B_RAW_FULL + i], 0, WAIT_LIMIT_NS / 8);
         for (int i = 0; i < 2; ++i) (void)mbar_wait_bounded(&bars[B_ACC_FULL + i], 0, WAIT_LIMIT_NS / 8);
     }
