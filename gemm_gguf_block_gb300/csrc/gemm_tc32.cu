@@ -91,19 +91,21 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
 }
 
 // Four signed bytes -> two half2 holding the same integers, in byte order
-// (bytes 0, 1 | bytes 2, 3): (1152 + b) - 1152.
+// (bytes 0, 1 | bytes 2, 3): the sign bits flipped (b + 128 as an unsigned
+// byte), each byte placed under a 0x64 high byte (binary16 1024 + (b + 128),
+// exact), then 1152 subtracted.
 __device__ __forceinline__ void s8x4_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
     const __half2 k1152 = mf::u2h(0x64806480u);
-    o0 = mf::h2u(__hsub2(mf::u2h(mf::s8pair_1152(__byte_perm(w, 0u, 0x4140))), k1152));
-    o1 = mf::h2u(__hsub2(mf::u2h(mf::s8pair_1152(__byte_perm(w, 0u, 0x4342))), k1152));
+    const uint32_t u = w ^ 0x80808080u;
+    o0 = mf::h2u(__hsub2(mf::u2h(__byte_perm(u, 0x64646464u, 0x4140)), k1152));
+    o1 = mf::h2u(__hsub2(mf::u2h(__byte_perm(u, 0x64646464u, 0x4342)), k1152));
 }
 // Nibbles of four bytes (selected by shift 0 = low, 4 = high) -> two half2
 // holding nibble - off (off = 1024 + bias: Q4_0 1032, Q4_1 1024).
 __device__ __forceinline__ void nib4_half(uint32_t w, int shift, __half2 off, uint32_t& o0, uint32_t& o1) {
-    const uint32_t p01 = __byte_perm(w, 0u, 0x4140) >> shift;
-    const uint32_t p23 = __byte_perm(w, 0u, 0x4342) >> shift;
-    o0 = mf::h2u(__hsub2(mf::u2h(mf::and_or(p01, 0x000F000Fu, 0x64006400u)), off));
-    o1 = mf::h2u(__hsub2(mf::u2h(mf::and_or(p23, 0x000F000Fu, 0x64006400u)), off));
+    const uint32_t n = (w >> shift) & 0x0F0F0F0Fu;
+    o0 = mf::h2u(__hsub2(mf::u2h(__byte_perm(n, 0x64646464u, 0x4140)), off));
+    o1 = mf::h2u(__hsub2(mf::u2h(__byte_perm(n, 0x64646464u, 0x4342)), off));
 }
 
 // Four bytes at byte offset B (even) of a register window of words.
