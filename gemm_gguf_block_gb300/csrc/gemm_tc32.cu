@@ -45,7 +45,7 @@ constexpr int NOP = 3;           // operand stages (one chunk each)
 constexpr int NCONV = 256;       // converter threads (warps 2-9)
 constexpr int EPI_WARPS = 16;
 constexpr int THREADS = (2 + 8 + EPI_WARPS) * 32;
-constexpr int EPI_COLS = BN / (EPI_WARPS / 4);          // 16 token columns per epilogue thread
+constexpr int EPI_COLS = BN / (EPI_WARPS / 4);          // 16 token columns per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;                     // 2 chunk slots x 4 blocks x 64 columns
 constexpr int A_BYTES = BM * KC * 2;                    // 32 KB
 constexpr int B_BYTES = BN * KC * 2;                    // 16 KB
@@ -172,10 +172,9 @@ __device__ __forceinline__ void convert_block(const uint32_t (&w)[NW], uint8_t* 
 template <int WF, int OFF, int NW>
 __device__ __forceinline__ void convert_pair(const uint32_t (&w)[NW], uint8_t* dst, float (&d)[2], float (&mn)[2]) {
     constexpr int BB = MF<WF>::BB;
-    if constexpr (OFF + 2 * BB + (WF == CQ_Q8_0 ? 0 : 0) <= 4 * NW) {
-        convert_block<WF, OFF, NW>(w, dst, d[0], mn[0]);
-        convert_block<WF, OFF + BB, NW>(w, dst + 512, d[1], mn[1]);   // next block: 4 core matrices on
-    }
+    static_assert(OFF + 2 * BB <= 4 * NW, "the window must hold both blocks");
+    convert_block<WF, OFF, NW>(w, dst, d[0], mn[0]);
+    convert_block<WF, OFF + BB, NW>(w, dst + 512, d[1], mn[1]);   // next block: 4 core matrices on
 }
 
 template <int WF>
