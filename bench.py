@@ -9,13 +9,14 @@ bytes streamed per second over the whole step (GB/s), inputs resident in HBM.
 The weights of one step (705 MB) exceed the 129 MB L2, so every step streams
 them from HBM.
 
-Also printed in the same JSON line: the prefill GEMM (Q4_K, M=512, K=4096,
-N=14336) in int8-equivalent TOPS, the routed-expert FFN and the Q4_1 LM head at
-M = 1/4/8/16, the single-call latency of the small Q4_0 GEMV, the fused dense
-SwiGLU gate + up projection (Q4_K 14336x4096 each, M = 1/4), the Q6_K
-tied-embedding LM head (128256x2048, M = 1/4), the roofline of
-the dominant kernel, the CPU oracle's rate on the host cores, and the
-end-to-end rate with host buffers.
+Also printed in the same JSON line: the prefill GEMMs (Q4_K, and Q8_0 / Q4_0 /
+Q4_1; M=512, K=4096, N=14336) in int8-equivalent TOPS, the routed-expert FFN
+and the Q4_1 LM head at M = 1/4/8/16, the single-call latency of the small
+Q4_0 GEMV, the fused dense SwiGLU gate + up projection (Q4_K 14336x4096 each,
+M = 1/4), the Q6_K tied-embedding LM head (128256x2048, M = 1/4), the Q5_K
+FFN gate projection (14336x4096, M = 1/4), the roofline of the dominant
+kernel, the CPU oracle's rate on the host cores, and the end-to-end rate with
+host buffers.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cq|reference]
 
@@ -281,9 +282,9 @@ def case_gemm(c, cq, synth, peaks, seed):
 
 
 def case_gemm_32(c, cq, synth, peaks, seed, fmts=("q8_0", "q4_0", "q4_1")):
-    """Prefill GEMM of the 32-element formats (mma.sync kernel): M=512,
-    K=4096, N=14336 per format, through cq_gemm_ws (activation operand images
-    built once into a workspace) and through cq_gemm (built in every CTA)."""
+    """Prefill GEMM of the 32-element formats (tcgen05 kernel): M=512, K=4096,
+    N=14336 per format, through cq_gemm_ws (activation operand images built
+    once into a workspace) and through cq_gemm (built in every CTA)."""
     res = {}
     for fmt in fmts:
         wfmt = cq.FMT[fmt]

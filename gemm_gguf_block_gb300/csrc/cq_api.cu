@@ -191,9 +191,9 @@ cq_status cq_read_global_status(int32_t* out_code, int clear) {
 
 namespace {
 
-// cq_gemm formats: Q4_K (tcgen05 kernel) and the 32-element formats (mma.sync
-// kernel; their activation rows are read by TMA, so xq must be 16-byte
-// aligned). Both take an optional workspace (cq_gemm_ws).
+// cq_gemm formats: Q4_K and the 32-element formats (their activation rows are
+// read by TMA, so xq must be 16-byte aligned), all on tcgen05 kernels that
+// take an optional workspace (cq_gemm_ws).
 bool is_gemm_fmt(int f) { return f == CQ_Q4_K || f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0; }
 
 cq_status gemm_common(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
@@ -213,9 +213,8 @@ cq_status gemm_common(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const vo
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* ws = need > 0 ? workspace : nullptr;
-    const cudaError_t e = w_fmt == CQ_Q4_K  ? cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, ws, s)
-                          : ws != nullptr ? cq::launch_gemm_tc32(dev, w_fmt, M, N, K, W, xq, y, ws, s)
-                                          : cq::launch_gemm_mma(dev, w_fmt, M, N, K, W, xq, y, s);
+    const cudaError_t e = w_fmt == CQ_Q4_K ? cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, ws, s)
+                                           : cq::launch_gemm_tc32(dev, w_fmt, M, N, K, W, xq, y, ws, s);
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 

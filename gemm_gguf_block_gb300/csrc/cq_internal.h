@@ -72,13 +72,11 @@ size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K);
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
                         const void* xq, float* y, void* workspace, cudaStream_t s);
 
-// Prefill GEMM of the 32-element formats (Q4_0, Q4_1, Q8_0; any M); y rows
-// equal the cq_gemv rows bit for bit. Without a workspace: mma.sync, each CTA
-// converting its activations. With one (gemm32_workspace_size bytes, 256-byte
-// aligned): the activation operand images are built once, and the tcgen05
-// kernel keeps one tensor-memory accumulator per 32-block.
-cudaError_t launch_gemm_mma(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
-                            const void* xq, float* y, cudaStream_t s);
+// Prefill GEMM of the 32-element formats (Q4_0, Q4_1, Q8_0; any M) on
+// tcgen05, one tensor-memory accumulator per 32-block; y rows equal the
+// cq_gemv rows bit for bit. With a workspace (gemm32_workspace_size bytes,
+// 256-byte aligned) the activation operand images are built once per call;
+// without one (workspace == nullptr) every CTA builds its own.
 size_t gemm32_workspace_size(int w_fmt, int64_t M, int64_t K);
 cudaError_t launch_gemm_tc32(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
                              const void* xq, float* y, void* workspace, cudaStream_t s);

@@ -40,8 +40,10 @@ using mf::MF;
 constexpr int BM = 128;          // weight rows per tile (MMA M, tensor-memory lanes)
 constexpr int BN = 64;           // tokens per tile (MMA N)
 constexpr int KC = 128;          // K per chunk: four 32-blocks
-constexpr int NRAW = 2;          // raw weight stages (one 8-block segment each)
-constexpr int NOP = 3;           // operand stages (one chunk each)
+constexpr int NRAW = 2;          // raw stages (one 8-block segment each)
+// Operand stages (one chunk each): three with a workspace; two without, where
+// the raw stages also hold the tokens' activation blocks.
+__host__ __device__ constexpr int nop(bool pre) { return pre ? 3 : 2; }
 constexpr int NCONV = 256;       // converter threads (warps 2-9)
 constexpr int EPI_WARPS = 16;
 constexpr int THREADS = (2 + 8 + EPI_WARPS) * 32;
@@ -57,15 +59,22 @@ __host__ __device__ constexpr int img_bytes(bool q8_1) { return B_BYTES + (q8_1 
 __host__ __device__ constexpr int wsc_bytes(bool q4_1) { return (q4_1 ? 2 : 1) * 4 * BM * 4; }
 __host__ __device__ constexpr int op_bytes(bool q4_1) { return A_BYTES + img_bytes(q4_1) + wsc_bytes(q4_1); }
 __host__ __device__ constexpr int raw_bytes(int bb) { return BM * mf::stage_pitch(bb); }
+// Raw activation box of one segment (64 tokens x 8 blocks), without a workspace.
+__host__ __device__ constexpr int rawact_bytes(int abb) { return BN * 8 * abb; }
+__host__ __device__ constexpr int raw_stage_bytes(bool pre, int bb, int abb) {
+    return raw_bytes(bb) + (pre ? 0 : rawact_bytes(abb));
+}
 
 enum { B_RAW_FULL = 0, B_RAW_EMPTY = 2, B_OP_FULL = 4, B_OP_EMPTY = 7, B_ACC_FULL = 10, B_ACC_EMPTY = 12 };
 constexpr int OFF_BAR = 0;
 constexpr int OFF_TMEM = 128;
 constexpr int OFF_FLAG = 136;
 constexpr int OFF_RAW = 1024;
-__host__ __device__ constexpr int off_op(int bb) { return OFF_RAW + NRAW * raw_bytes(bb); }
-__host__ __device__ constexpr int smem_bytes(int bb, bool q4_1) {
-    return off_op(bb) + NOP * op_bytes(q4_1) + 1024;     // + alignment slack of the dynamic base
+__host__ __device__ constexpr int off_op(bool pre, int bb, int abb) {
+    return OFF_RAW + NRAW * raw_stage_bytes(pre, bb, abb);
+}
+__host__ __device__ constexpr int smem_bytes(bool pre, int bb, int abb) {
+    return off_op(pre, bb, abb) + nop(pre) * op_bytes(abb == 36) + 1024;   // + alignment slack of the dynamic base
 }
 
 struct Tc32Params {
@@ -177,8 +186,34 @@ __device__ __forceinline__ void convert_pair(const uint32_t (&w)[NW], uint8_t* d
     convert_block<WF, OFF + BB, NW>(w, dst + 512, d[1], mn[1]);   // next block: 4 core matrices on
 }
 
-template <int WF>
+// One activation block (Q8_0, or Q8_1 for Q4_1 weights) starting at byte OFF
+// of a 48-byte register window: its 32 quants as fp16 into four core-matrix
+// rows of the B tile (dst = the block's first row), its d_x (and s_x) into
+// the image's scale tables -- the values gemm32_tc_prep_kernel writes.
+template <int WF, int OFF>
+__device__ __forceinline__ void convert_act(const uint32_t (&w)[12], uint8_t* dst, float* dx, float* sx) {
+    constexpr int AQO = MF<WF>::AQO;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t o[4];
+        const uint32_t a = i == 0 ? win_u32<OFF + AQO, 12>(w) : i == 1 ? win_u32<OFF + AQO + 8, 12>(w)
+                         : i == 2 ? win_u32<OFF + AQO + 16, 12>(w) : win_u32<OFF + AQO + 24, 12>(w);
+        const uint32_t b = i == 0 ? win_u32<OFF + AQO + 4, 12>(w) : i == 1 ? win_u32<OFF + AQO + 12, 12>(w)
+                         : i == 2 ? win_u32<OFF + AQO + 20, 12>(w) : win_u32<OFF + AQO + 28, 12>(w);
+        s8x4_half(a, o[0], o[1]);
+        s8x4_half(b, o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    *dx = h2f(win_u16<OFF, 12>(w));
+    if constexpr (WF == CQ_Q4_1) *sx = h2f(win_u16<OFF + 2, 12>(w));
+}
+
+// PRE: the activation images come from the workspace (bulk copies);
+// otherwise the producer also loads the tokens' raw activation blocks with
+// each weight segment and the converters build the image in every CTA.
+template <int WF, bool PRE>
 __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                               const __grid_constant__ CUtensorMap amap,
                                                                const Tc32Params p) {
     pdl_trigger();
     pdl_wait();
@@ -186,9 +221,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
     constexpr bool Q41 = WF == CQ_Q4_1;
     constexpr int PITCH = mf::stage_pitch(F::BB);
     constexpr int RAWB = raw_bytes(F::BB);
+    constexpr int RSB = raw_stage_bytes(PRE, F::BB, F::ABB);
     constexpr int IMG = img_bytes(Q41);
     constexpr int OPB = op_bytes(Q41);
-    constexpr int OFF_OP = off_op(F::BB);
+    constexpr int NOP = nop(PRE);
+    constexpr int OFF_OP = off_op(PRE, F::BB, F::ABB);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
@@ -204,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             mbar_init(&bars[B_RAW_EMPTY + i], NCONV);
         }
         for (int i = 0; i < NOP; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], NCONV + 1);        // converters + the producer's image copy
+            mbar_init(&bars[B_OP_FULL + i], NCONV + (PRE ? 1 : 0));   // converters (+ the producer's image copy)
             mbar_init(&bars[B_OP_EMPTY + i], 1 + EPI_WARPS);   // the MMA commit + the epilogue's scale reads
         }
         for (int i = 0; i < 2; ++i) {
@@ -229,8 +266,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             for (int s = 0; 2 * s < nq && !abort_flag.get(); ++s) {
                 const int r = s % NRAW;
                 if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAWB);
-                tc::tma_load_2d(smem + OFF_RAW + r * RAWB, &wmap, s * 8 * F::BB / 2, n0, &bars[B_RAW_FULL + r]);
+                mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RSB);
+                tc::tma_load_2d(smem + OFF_RAW + r * RSB, &wmap, s * 8 * F::BB / 2, n0, &bars[B_RAW_FULL + r]);
+                if constexpr (!PRE) {
+                    // the tokens' 8 activation blocks of this segment; tokens past M read as zero
+                    tc::tma_load_2d(smem + OFF_RAW + r * RSB + RAWB, &amap, s * 8 * F::ABB / 2, m0,
+                                    &bars[B_RAW_FULL + r]);
+                    continue;
+                }
                 bool ok = true;
                 for (int h = 0; h < 2; ++h) {
                     const int q = 2 * s + h, st = q % NOP;
@@ -285,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             uint8_t* stg = smem + OFF_OP + st * OPB;
             float* wsd = reinterpret_cast<float*>(stg + A_BYTES + IMG);
             const int off = (4 * h + 2 * part) * F::BB;         // the two blocks' byte offset in the row
-            const uint8_t* win = smem + OFF_RAW + rs * RAWB + r * PITCH + (off & ~15);
+            const uint8_t* win = smem + OFF_RAW + rs * RSB + r * PITCH + (off & ~15);
             uint32_t w[NW];
 #pragma unroll
             for (int i = 0; i < NW / 4; ++i) {
@@ -304,6 +347,34 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             for (int bb = 0; bb < 2; ++bb) {
                 wsd[(2 * part + bb) * BM + r] = d[bb];
                 if constexpr (Q41) wsd[4 * BM + (2 * part + bb) * BM + r] = mn[bb];
+            }
+            if constexpr (!PRE) {
+                // The chunk's activation image: thread (block cb = tid / 64, token
+                // tk = tid % 64) -- cb is warp-uniform, so the block's offset in the
+                // token's 16-byte-aligned window is too. Rows of 8 blocks are 272
+                // (Q8_0) or 288 (Q8_1) bytes apart.
+                const int cb = tid >> 6, tk = tid & 63;
+                const int aoff = (4 * h + cb) * F::ABB;
+                const uint8_t* awin = smem + OFF_RAW + rs * RSB + RAWB + tk * (8 * F::ABB) + (aoff & ~15);
+                uint32_t aw[12];
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(awin + 16 * i);
+                    aw[4 * i] = v.x; aw[4 * i + 1] = v.y; aw[4 * i + 2] = v.z; aw[4 * i + 3] = v.w;
+                }
+                uint8_t* bdst = stg + A_BYTES + tile_off(tk, 32 * cb, KC);
+                float* dxp = reinterpret_cast<float*>(stg + A_BYTES + B_BYTES) + cb * BN + tk;
+                float* sxp = dxp + 4 * BN;
+                switch (aoff & 15) {
+                case 0: convert_act<WF, 0>(aw, bdst, dxp, sxp); break;
+                case 2: if constexpr (!Q41) convert_act<WF, 2>(aw, bdst, dxp, sxp); break;
+                case 4: convert_act<WF, 4>(aw, bdst, dxp, sxp); break;
+                case 6: if constexpr (!Q41) convert_act<WF, 6>(aw, bdst, dxp, sxp); break;
+                case 8: convert_act<WF, 8>(aw, bdst, dxp, sxp); break;
+                case 10: if constexpr (!Q41) convert_act<WF, 10>(aw, bdst, dxp, sxp); break;
+                case 12: convert_act<WF, 12>(aw, bdst, dxp, sxp); break;
+                default: if constexpr (!Q41) convert_act<WF, 14>(aw, bdst, dxp, sxp); break;
+                }
             }
             fence_proxy_async_smem();
             tc::mbar_arrive(&bars[B_OP_FULL + st]);
@@ -463,6 +534,30 @@ __global__ void __launch_bounds__(256) gemm32_tc_prep_kernel(const Tc32Params p,
     if constexpr (WF == CQ_Q4_1) dxs[4 * BN + b * BN + t] = s;
 }
 
+template <int WF, bool PRE>
+cudaError_t launch_mode(const DeviceInfo& dev, const CUtensorMap& wmap, const CUtensorMap& amap, const Tc32Params& p,
+                        unsigned tok_tiles, unsigned row_tiles, cudaStream_t s) {
+    using F = MF<WF>;
+    constexpr int SMEM = smem_bytes(PRE, F::BB, F::ABB);
+    if (SMEM > dev.smem_optin) return cudaErrorInvalidConfiguration;
+    static int raised[64] = {};
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e != cudaSuccess) return e;
+    if (devid >= 64 || !raised[devid]) {
+        e = cudaFuncSetAttribute(gemm32_tc_kernel<WF, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+        if (e != cudaSuccess) return e;
+        if (devid < 64) raised[devid] = 1;
+    }
+    if constexpr (PRE) {
+        e = launch_kernel(gemm32_tc_prep_kernel<WF>, dim3(static_cast<unsigned>(p.nchunk), tok_tiles), dim3(256), 0,
+                          s, p, const_cast<uint8_t*>(p.img));
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(gemm32_tc_kernel<WF, PRE>, dim3(tok_tiles, row_tiles), dim3(THREADS), SMEM, s, wmap, amap,
+                         p);
+}
+
 template <int WF>
 cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
                        float* y, void* workspace, cudaStream_t s) {
@@ -470,31 +565,32 @@ cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, c
     tc::EncodeTiledFn enc = tc::encode_tiled_fn();
     if (enc == nullptr) return cudaErrorNotSupported;
     const int nb = static_cast<int>(K / 32);
-    const int64_t wrow = static_cast<int64_t>(nb) * F::BB;
-    // Raw weights as a 2-D tensor of 2-byte elements [N rows][wrow / 2]; a box
-    // is one 8-block segment of 128 rows; rows past N read as zero.
-    CUtensorMap wmap;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(wrow / 2), static_cast<cuuint64_t>(N)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(wrow)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mf::stage_pitch(F::BB) / 2), BM};
+    const int64_t wrow = static_cast<int64_t>(nb) * F::BB, xrow = static_cast<int64_t>(nb) * F::ABB;
+    // Raw weights [N rows][wrow / 2] and activations [M rows][xrow / 2] as 2-D
+    // tensors of 2-byte elements; a box is one 8-block segment of 128 rows / 64
+    // tokens; rows past N and tokens past M read as zero.
+    CUtensorMap wmap, amap;
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    constexpr int SMEM = smem_bytes(F::BB, WF == CQ_Q4_1);
-    if (SMEM > dev.smem_optin) return cudaErrorInvalidConfiguration;
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(wrow / 2), static_cast<cuuint64_t>(N)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(wrow)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(mf::stage_pitch(F::BB) / 2), BM};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(xrow / 2), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(xrow)};
+        const cuuint32_t box[2] = {static_cast<cuuint32_t>(8 * F::ABB / 2), BN};
+        if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(xq), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     const int64_t row_tiles = (N + BM - 1) / BM;
     if (row_tiles > 65535) return cudaErrorInvalidValue;      // grid y limit (N above 8.4 M rows)
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
-    if (e != cudaSuccess) return e;
-    if (devid >= 64 || !raised[devid]) {
-        e = cudaFuncSetAttribute(gemm32_tc_kernel<WF>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = 1;
-    }
     Tc32Params p{};
     p.xq = static_cast<const uint8_t*>(xq);
     p.img = static_cast<const uint8_t*>(workspace);
@@ -505,11 +601,9 @@ cudaError_t launch_fmt(const DeviceInfo& dev, int64_t M, int64_t N, int64_t K, c
     p.nb = nb;
     p.nchunk = nb / 4;
     const unsigned tok_tiles = static_cast<unsigned>((M + BN - 1) / BN);
-    e = launch_kernel(gemm32_tc_prep_kernel<WF>, dim3(static_cast<unsigned>(p.nchunk), tok_tiles), dim3(256), 0, s, p,
-                      static_cast<uint8_t*>(workspace));
-    if (e != cudaSuccess) return e;
-    return launch_kernel(gemm32_tc_kernel<WF>, dim3(tok_tiles, static_cast<unsigned>(row_tiles)), dim3(THREADS),
-                         SMEM, s, wmap, p);
+    return workspace != nullptr
+               ? launch_mode<WF, true>(dev, wmap, amap, p, tok_tiles, static_cast<unsigned>(row_tiles), s)
+               : launch_mode<WF, false>(dev, wmap, amap, p, tok_tiles, static_cast<unsigned>(row_tiles), s);
 }
 
 }  // namespace

@@ -1,6 +1,6 @@
 // Exact integer block dots of the 32-element GGUF formats on mma.sync
-// m16n8k16 (fp16 operands, fp32 accumulators), shared by the batched GEMV
-// and the GEMM of Q4_0 / Q4_1 / Q8_0 weights.
+// m16n8k16 (fp16 operands, fp32 accumulators), for the batched GEMV; the
+// prefill GEMM of the same formats takes the block traits and byte helpers.
 //
 // Every weight quant enters the A operand as BIAS + v (v its value), built
 // from the packed bytes by one lop3 per pair; every activation quant enters B

@@ -171,7 +171,7 @@ cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const
  * Prefill GEMM, any M >= 0 (cera README "Supported models": batched-GEMM
  * prefill; alice-llm "Computation Path (Q4_K)"). Same operands and result as
  * cq_gemv; each row equals the cq_gemv result for that token bit for bit.
- * w_fmt: Q4_K (tcgen05 path) or Q4_0 / Q4_1 / Q8_0 (mma.sync path; cera
+ * w_fmt: Q4_K or Q4_0 / Q4_1 / Q8_0 (tcgen05 paths; cera
  * 0.5.3 README "Breaking changes in 0.4.0" holds a Q4_1 decode equal to
  * the batched prefill bit for bit). For Q4_0 / Q4_1 / Q8_0
  * the activation rows are read by TMA, so xq must be 16-byte aligned
@@ -188,10 +188,7 @@ cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
  * cq_gemm_workspace_size returns the bytes needed (0 for an unsupported
  * format or shape): ceil(M/128) * (K/256) * 70144 for Q4_K;
  * ceil(M/64) * (K/128) * 17408 for Q4_0 and Q8_0 (Q8_0 activations) and
- * ceil(M/64) * (K/128) * 18432 for Q4_1 (Q8_1 activations). For these three
- * formats cq_gemm_ws runs a different kernel from cq_gemm (tcgen05 with one
- * tensor-memory accumulator per 32-block, against mma.sync); the results
- * are the same bits. The workspace
+ * ceil(M/64) * (K/128) * 18432 for Q4_1 (Q8_1 activations). The workspace
  * must be 256-byte aligned; it is scratch (no state is kept between calls),
  * and two calls that may overlap on the GPU need separate workspaces.
  * Errors as cq_gemm, plus CQ_ERR_WORKSPACE (NULL or too small) and

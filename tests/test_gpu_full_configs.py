@@ -85,7 +85,8 @@ def test_prefill_gemm_sampled(orc):
 
 @pytest.mark.parametrize("fmt", ["q4_0", "q4_1", "q8_0"])
 def test_prefill_gemm_32_sampled(orc, fmt):
-    """The mma.sync GEMM of a 32-element format at M=512 N=14336 K=4096."""
+    """The prefill GEMM of a 32-element format at M=512 N=14336 K=4096, with and
+    without a workspace."""
     torch = torch_cuda()
     cq = cq_built()
     wfmt = cq.FMT[fmt]
