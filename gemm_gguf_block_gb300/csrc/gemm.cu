@@ -92,18 +92,6 @@ struct GemmParams {
 // fp16 tiles, then the mins operand.
 constexpr int IMG_BYTES = 2 * (BN * KH * 2) + BN * 16 * 2;     // 69632
 
-// Offset of element (r, k) in a K-major no-swizzle tile whose rows hold kt elements.
-__device__ __forceinline__ int tile_off(int r, int k, int kt) {
-    return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
-    if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
-    flag.set(1);
-    atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
-    return false;
-}
-
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -186,7 +174,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
             const uint64_t pol = policy_evict_first();
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 const int r = s % NRAW;
-                if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAW_BYTES);
                 tc::tma_load_2d(smem + OFF_RAW + r * RAW_BYTES, &wmap, 144 * s, n0, &bars[B_RAW_FULL + r]);
                 if constexpr (PRE) {
@@ -194,7 +182,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                     bool ok = true;
                     for (int h = 0; h < 2; ++h) {
                         const int q = 2 * s + h, st = q % NSTAGE;
-                        if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
+                        if (!tc::wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
                             ok = false;
                             break;
                         }
@@ -215,11 +203,11 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
             const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
             const uint32_t stage0 = smem_u32(smem + OFF_STAGE);
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
-                if (!wait_or_abort(&bars[B_ACC_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort(&bars[B_ACC_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
                 bool ok = true;
                 for (int h = 0; h < 2; ++h) {
                     const int q = 2 * s + h, st = q % NSTAGE;
-                    if (!wait_or_abort(&bars[B_OP_FULL + st], (q / NSTAGE) & 1, abort_flag, p.status)) {
+                    if (!tc::wait_or_abort(&bars[B_OP_FULL + st], (q / NSTAGE) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -277,8 +265,8 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
             if (abort_flag.get()) break;
             if constexpr (!PRE)
                 if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt);
-            if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
-            if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+            if (!tc::wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
+            if (!tc::wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
             // A: weight row r, group g = 2h + part: 32 low nibbles (sub-block 2g) and
             // 32 high nibbles (sub-block 2g + 1)
@@ -334,8 +322,8 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                         mw[j / 2] = h2_bits(__halves2half2(__int2half_rn(mn0), __int2half_rn(mn1)));
                     }
                     const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-                    *reinterpret_cast<uint4*>(am + tile_off(r, 0, 16)) = mv;
-                    *reinterpret_cast<uint4*>(am + tile_off(r, 8, 16)) = mv;
+                    *reinterpret_cast<uint4*>(am + tc::tile_off(r, 0, 16)) = mv;
+                    *reinterpret_cast<uint4*>(am + tc::tile_off(r, 8, 16)) = mv;
                 }
 #pragma unroll
                 for (int i = 0; i < 4 && !PRE; ++i) {
@@ -344,7 +332,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                     const int pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
                                    static_cast<int>(static_cast<int16_t>(v >> 16));
                     const int hq = pr >> 6;                                  // floor division by 64
-                    __half* bh = reinterpret_cast<__half*>(bm + tile_off(t, 0, 16));
+                    __half* bh = reinterpret_cast<__half*>(bm + tc::tile_off(t, 0, 16));
                     bh[j] = __int2half_rn(64 * hq);
                     bh[64 + j] = __int2half_rn(pr - 64 * hq);                // k = 8 + j: next core matrix (+128 B)
                 }
@@ -516,13 +504,13 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
             int8_to_half(__ldg(qw + 2 * g), o0);
             int8_to_half(__ldg(qw + 2 * g + 1), o1);
         }
-        *reinterpret_cast<uint4*>(bt + tile_off(t, 8 * g, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+        *reinterpret_cast<uint4*>(bt + tc::tile_off(t, 8 * g, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
     }
     if (h == 0) {
         dxs[(static_cast<int64_t>(tile) * ns + s) * BN + t] = on ? __ldg(reinterpret_cast<const float*>(blk)) : 0.0f;
     } else {
         // mins operand: token t = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
-        __half* bh = reinterpret_cast<__half*>(img + 2 * (BN * KH * 2) + tile_off(t, 0, 16));
+        __half* bh = reinterpret_cast<__half*>(img + 2 * (BN * KH * 2) + tc::tile_off(t, 0, 16));
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             int pr = 0;

@@ -87,18 +87,6 @@ struct Tc32Params {
     int nchunk;             // chunks (128 columns) per row
 };
 
-// Offset of element (r, k) in a K-major no-swizzle tile whose rows hold kt elements.
-__host__ __device__ constexpr int tile_off(int r, int k, int kt) {
-    return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
-}
-
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
-    if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
-    flag.set(1);
-    atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
-    return false;
-}
-
 // Four signed bytes -> two half2 holding the same integers, in byte order
 // (bytes 0, 1 | bytes 2, 3): the sign bits flipped (b + 128 as an unsigned
 // byte), each byte placed under a 0x64 high byte (binary16 1024 + (b + 128),
@@ -265,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
         if (lane == 0) {
             for (int s = 0; 2 * s < nq && !abort_flag.get(); ++s) {
                 const int r = s % NRAW;
-                if (!wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RSB);
                 tc::tma_load_2d(smem + OFF_RAW + r * RSB, &wmap, s * 8 * F::BB / 2, n0, &bars[B_RAW_FULL + r]);
                 if constexpr (!PRE) {
@@ -277,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
                 bool ok = true;
                 for (int h = 0; h < 2; ++h) {
                     const int q = 2 * s + h, st = q % NOP;
-                    if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) {
+                    if (!tc::wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
@@ -296,8 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
             const uint32_t op0 = smem_u32(smem + OFF_OP);
             for (int q = 0; q < nq && !abort_flag.get(); ++q) {
                 const int slot = q & 1, st = q % NOP;
-                if (!wait_or_abort(&bars[B_ACC_EMPTY + slot], ((q >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-                if (!wait_or_abort(&bars[B_OP_FULL + st], (q / NOP) & 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort(&bars[B_ACC_EMPTY + slot], ((q >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort(&bars[B_OP_FULL + st], (q / NOP) & 1, abort_flag, p.status)) break;
                 tc::fence_after();
                 const uint32_t a0 = op0 + st * OPB, b0 = a0 + A_BYTES;
                 for (int b = 0; b < 4; ++b)
@@ -323,8 +311,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
         for (int q = 0; q < nq; ++q) {
             const int s = q >> 1, h = q & 1, st = q % NOP, rs = s % NRAW;
             if (abort_flag.get()) break;
-            if (!wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) break;
-            if (!wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+            if (!tc::wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NOP) & 1) ^ 1, abort_flag, p.status)) break;
+            if (!tc::wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_OP + st * OPB;
             float* wsd = reinterpret_cast<float*>(stg + A_BYTES + IMG);
             const int off = (4 * h + 2 * part) * F::BB;         // the two blocks' byte offset in the row
@@ -335,7 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
                 const uint4 v = *reinterpret_cast<const uint4*>(win + 16 * i);
                 w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
-            uint8_t* dst = stg + tile_off(r, 64 * part, KC);
+            uint8_t* dst = stg + tc::tile_off(r, 64 * part, KC);
             float d[2], mn[2];
             switch (off & 15) {
             case 0: convert_pair<WF, 0>(w, dst, d, mn); break;
@@ -362,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
                     const uint4 v = *reinterpret_cast<const uint4*>(awin + 16 * i);
                     aw[4 * i] = v.x; aw[4 * i + 1] = v.y; aw[4 * i + 2] = v.z; aw[4 * i + 3] = v.w;
                 }
-                uint8_t* bdst = stg + A_BYTES + tile_off(tk, 32 * cb, KC);
+                uint8_t* bdst = stg + A_BYTES + tc::tile_off(tk, 32 * cb, KC);
                 float* dxp = reinterpret_cast<float*>(stg + A_BYTES + B_BYTES) + cb * BN + tk;
                 float* sxp = dxp + 4 * BN;
                 switch (aoff & 15) {
@@ -528,7 +516,7 @@ __global__ void __launch_bounds__(256) gemm32_tc_prep_kernel(const Tc32Params p,
         uint32_t o[4];
         s8x4_half(w[2 * i], o[0], o[1]);
         s8x4_half(w[2 * i + 1], o[2], o[3]);
-        *reinterpret_cast<uint4*>(dst + tile_off(t, 32 * b + 8 * i, KC)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + tc::tile_off(t, 32 * b + 8 * i, KC)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     dxs[b * BN + t] = d;
     if constexpr (WF == CQ_Q4_1) dxs[4 * BN + b * BN + t] = s;

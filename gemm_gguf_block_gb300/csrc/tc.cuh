@@ -24,6 +24,23 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// Byte offset of element (r, k) in a K-major, no-swizzle operand tile whose
+// rows hold kt fp16 elements: 8-row x 16-byte core matrices, adjacent along K
+// 128 bytes apart, 8-row groups kt * 16 bytes apart (the smem_desc below with
+// lbo = 128, sbo = kt * 16).
+__host__ __device__ constexpr int tile_off(int r, int k, int kt) {
+    return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// A role's bounded wait: on timeout it raises the CTA's abort flag and the
+// library status bit, so the other roles leave their loops too.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
+    if (mbar_wait_bounded(bar, parity, WAIT_LIMIT_NS)) return true;
+    flag.set(1);
+    atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
+    return false;
+}
+
 // ------------------------------------------------------------------- MMA
 // D[tmem] (+)= A[smem] * B[smem]^T, fp16 operands, fp32 accumulator.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
