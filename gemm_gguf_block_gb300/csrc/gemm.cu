@@ -107,14 +107,6 @@ __device__ __forceinline__ void nibbles_to_half(uint32_t w, __half2 sl, __half2 
     hi[0] = h2_bits(__hfma2(bits_h2(((p01 >> 4) & 0x000F000Fu) | 0x64006400u), sh, bh));
     hi[1] = h2_bits(__hfma2(bits_h2(((p23 >> 4) & 0x000F000Fu) | 0x64006400u), sh, bh));
 }
-// Four signed bytes -> two half2 holding the same integers.
-__device__ __forceinline__ void int8_to_half(uint32_t w, uint32_t (&o)[2]) {
-    const __half2 bias = bits_h2(0x64806480u);          // 1152 = 1024 + 128
-    const uint32_t p01 = __byte_perm(w, 0u, 0x4140);
-    const uint32_t p23 = __byte_perm(w, 0u, 0x4342);
-    o[0] = h2_bits(__hsub2(bits_h2((p01 ^ 0x00800080u) | 0x64006400u), bias));
-    o[1] = h2_bits(__hsub2(bits_h2((p23 ^ 0x00800080u) | 0x64006400u), bias));
-}
 
 __device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& mn) {
     auto byte = [](uint32_t w, int i) { return static_cast<int>((w >> (8 * i)) & 0xffu); };
@@ -303,7 +295,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                 const int t = 16 * cw + 8 * (i & 1) + (lane & 7);
                 const int word = 4 * (i >> 1) + (lane >> 3);
                 uint32_t o[2];
-                int8_to_half(cur[i], o);
+                tc::s8x4_half(cur[i], o[0], o[1]);
                 *reinterpret_cast<uint2*>(bt + (t >> 3) * (KH * 16) + (t & 7) * 16 + (word >> 1) * 128 +
                                           (word & 1) * 8) = make_uint2(o[0], o[1]);
             }
@@ -501,8 +493,8 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
     for (int g = 0; g < KH / 8; ++g) {       // 8 elements (one core-matrix row) per store
         uint32_t o0[2] = {0u, 0u}, o1[2] = {0u, 0u};
         if (on) {
-            int8_to_half(__ldg(qw + 2 * g), o0);
-            int8_to_half(__ldg(qw + 2 * g + 1), o1);
+            tc::s8x4_half(__ldg(qw + 2 * g), o0[0], o0[1]);
+            tc::s8x4_half(__ldg(qw + 2 * g + 1), o1[0], o1[1]);
         }
         *reinterpret_cast<uint4*>(bt + tc::tile_off(t, 8 * g, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
     }

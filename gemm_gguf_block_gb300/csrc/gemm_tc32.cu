@@ -87,16 +87,6 @@ struct Tc32Params {
     int nchunk;             // chunks (128 columns) per row
 };
 
-// Four signed bytes -> two half2 holding the same integers, in byte order
-// (bytes 0, 1 | bytes 2, 3): the sign bits flipped (b + 128 as an unsigned
-// byte), each byte placed under a 0x64 high byte (binary16 1024 + (b + 128),
-// exact), then 1152 subtracted.
-__device__ __forceinline__ void s8x4_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
-    const __half2 k1152 = mf::u2h(0x64806480u);
-    const uint32_t u = w ^ 0x80808080u;
-    o0 = mf::h2u(__hsub2(mf::u2h(__byte_perm(u, 0x64646464u, 0x4140)), k1152));
-    o1 = mf::h2u(__hsub2(mf::u2h(__byte_perm(u, 0x64646464u, 0x4342)), k1152));
-}
 // Nibbles of four bytes (selected by shift 0 = low, 4 = high) -> two half2
 // holding nibble - off (off = 1024 + bias: Q4_0 1032, Q4_1 1024).
 __device__ __forceinline__ void nib4_half(uint32_t w, int shift, __half2 off, uint32_t& o0, uint32_t& o1) {
@@ -132,8 +122,8 @@ __device__ __forceinline__ void convert_block(const uint32_t (&w)[NW], uint8_t* 
                              : i == 2 ? win_u32<BASE + 18, NW>(w) : win_u32<BASE + 26, NW>(w);
             const uint32_t b = i == 0 ? win_u32<BASE + 6, NW>(w) : i == 1 ? win_u32<BASE + 14, NW>(w)
                              : i == 2 ? win_u32<BASE + 22, NW>(w) : win_u32<BASE + 30, NW>(w);
-            s8x4_half(a, o[0], o[1]);
-            s8x4_half(b, o[2], o[3]);
+            tc::s8x4_half(a, o[0], o[1]);
+            tc::s8x4_half(b, o[2], o[3]);
             *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
         }
         d = h2f(win_u16<BASE, NW>(w));
@@ -188,8 +178,8 @@ __device__ __forceinline__ void convert_act(const uint32_t (&w)[12], uint8_t* ds
                          : i == 2 ? win_u32<OFF + AQO + 16, 12>(w) : win_u32<OFF + AQO + 24, 12>(w);
         const uint32_t b = i == 0 ? win_u32<OFF + AQO + 4, 12>(w) : i == 1 ? win_u32<OFF + AQO + 12, 12>(w)
                          : i == 2 ? win_u32<OFF + AQO + 20, 12>(w) : win_u32<OFF + AQO + 28, 12>(w);
-        s8x4_half(a, o[0], o[1]);
-        s8x4_half(b, o[2], o[3]);
+        tc::s8x4_half(a, o[0], o[1]);
+        tc::s8x4_half(b, o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + 128 * i) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     *dx = h2f(win_u16<OFF, 12>(w));
@@ -514,8 +504,8 @@ __global__ void __launch_bounds__(256) gemm32_tc_prep_kernel(const Tc32Params p,
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         uint32_t o[4];
-        s8x4_half(w[2 * i], o[0], o[1]);
-        s8x4_half(w[2 * i + 1], o[2], o[3]);
+        tc::s8x4_half(w[2 * i], o[0], o[1]);
+        tc::s8x4_half(w[2 * i + 1], o[2], o[3]);
         *reinterpret_cast<uint4*>(dst + tc::tile_off(t, 32 * b + 8 * i, KC)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
     dxs[b * BN + t] = d;

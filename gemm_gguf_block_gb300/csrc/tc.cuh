@@ -3,6 +3,7 @@
 // 2-D TMA tile loads, and the shared-memory matrix descriptors.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "cq_device.cuh"
 
@@ -30,6 +31,20 @@ __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::aft
 // lbo = 128, sbo = kt * 16).
 __host__ __device__ constexpr int tile_off(int r, int k, int kt) {
     return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
+// Four signed bytes -> two half2 holding the same integers, in byte order
+// (bytes 0, 1 | bytes 2, 3): the sign bits flipped (b + 128 as an unsigned
+// byte), each byte placed under a 0x64 high byte (binary16 1024 + (b + 128),
+// exact), then 1152 subtracted. The operand conversion of int8 quants.
+__device__ __forceinline__ void s8x4_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
+    const __half2 k1152 = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140), p23 = __byte_perm(u, 0x64646464u, 0x4342);
+    __half2 r01 = __hsub2(*reinterpret_cast<const __half2*>(&p01), k1152);
+    __half2 r23 = __hsub2(*reinterpret_cast<const __half2*>(&p23), k1152);
+    o0 = *reinterpret_cast<const uint32_t*>(&r01);
+    o1 = *reinterpret_cast<const uint32_t*>(&r23);
 }
 
 // A role's bounded wait: on timeout it raises the CTA's abort flag and the
