@@ -970,9 +970,14 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     if (N <= 0) return x != nullptr ? launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s) : cudaSuccess;
     // Several tokens: the tensor-core kernel when the activations fit its
     // shared memory (same fixed order, so the same bits). It stages quantized
-    // activations, so fp32 ones are quantized by their own launch first.
+    // activations, so fp32 ones are quantized by their own launch first. Q8_0
+    // at two or three tokens stays on the dp4a kernel below, whose work per token
+    // is lightest for Q8_0 (LM head 128256 x 4096: M = 2 88.2 us here against
+    // 112.6 on the tensor cores, M = 3 106.5 against 112.7, M = 4 131.1
+    // against 114.7; for Q4_0 and Q4_1 the tensor cores win or tie from M = 2).
     const int need = gemv_mma_smem(w_fmt, M, K);
-    if (M >= 2 && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled()) {
+    const bool dp4a_better = w_fmt == CQ_Q8_0 && M <= 3;
+    if (M >= 2 && !dp4a_better && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled()) {
         if (x != nullptr) {
             const cudaError_t e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
             if (e != cudaSuccess) return e;
