@@ -975,6 +975,18 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     // is lightest for Q8_0 (LM head 128256 x 4096: M = 2 88.2 us here against
     // 112.6 on the tensor cores, M = 3 106.5 against 112.7, M = 4 131.1
     // against 114.7; for Q4_0 and Q4_1 the tensor cores win or tie from M = 2).
+    // Q4_K with many tokens: the tcgen05 prefill GEMM (no workspace; its rows
+    // are the bits of this kernel's). Measured crossover: from M = 9 when the
+    // matrix has 8192 rows or more (14336 x 4096, M = 9: 65.5 -> 49.2 us;
+    // 128256 x 4096: 376.9 -> 309.2 us), from M = 14 for 4096 rows, which give
+    // the GEMM only 32 row tiles (4096 x 14336, M = 14: 160.8 -> 151.6 us).
+    if (w_fmt == CQ_Q4_K && (M >= 14 || (M >= 9 && N >= 8192))) {
+        if (x != nullptr) {
+            const cudaError_t e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_gemm(dev, w_fmt, M, N, K, W, xq, y, nullptr, s);
+    }
     const int need = gemv_mma_smem(w_fmt, M, K);
     const bool dp4a_better = w_fmt == CQ_Q8_0 && M <= 3;
     if (M >= 2 && !dp4a_better && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled()) {
