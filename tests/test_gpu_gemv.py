@@ -113,6 +113,24 @@ def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
         assert np.array_equal(y[:16].view(np.uint32), y16.view(np.uint32)), "batched GEMV rows differ"
 
 
+@pytest.mark.parametrize("N,Ms", [(8200, (8, 9)), (300, (13, 14))])
+def test_q4k_many_token_gemv_route(orc, N, Ms):
+    """cq_gemv sends Q4_K calls with many tokens to the prefill GEMM (from M = 9
+    when N >= 8192, from M = 14 below): both sides of each switch give the
+    single-token rows bit for bit and agree with the oracle."""
+    torch = torch_cuda()
+    cq = cq_built()
+    K = 1024
+    W, xq = _case(orc, 12, N, K, 16, seed=N)
+    Wd, xd = dev(torch, W), dev(torch, xq)
+    y1 = np.stack([cq.gemv_t(Wd, xd[m:m + 1], 12, K).cpu().numpy()[0] for m in range(max(Ms))])
+    for M in Ms:
+        yM = cq.gemv_t(Wd, xd[:M], 12, K).cpu().numpy()
+        assert np.array_equal(yM.view(np.uint32), y1[:M].view(np.uint32)), f"M={M} rows differ from M=1"
+    y_ref, at = orc.matmul(12, W, xq[:max(Ms)], K)
+    assert_within(y1, y_ref, at, what=f"q4_k {N}x{K}")
+
+
 @pytest.mark.parametrize("wfmt", FMTS)
 def test_zero_scales_and_empty(orc, wfmt):
     torch = torch_cuda()
