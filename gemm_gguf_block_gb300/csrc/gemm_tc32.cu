@@ -41,9 +41,8 @@ constexpr int BM = 128;          // weight rows per tile (MMA M, tensor-memory l
 constexpr int BN = 64;           // tokens per tile (MMA N)
 constexpr int KC = 128;          // K per chunk: four 32-blocks
 constexpr int NRAW = 2;          // raw stages (one 8-block segment each)
-// Operand stages (one chunk each): three with a workspace; two without, where
-// the raw stages also hold the tokens' activation blocks.
-__host__ __device__ constexpr int nop(bool pre) { return pre ? 3 : 2; }
+// Operand stages (one chunk each): three, unless the raw stages also hold the
+// tokens' activation blocks (no workspace) and three no longer fit.
 constexpr int NCONV = 256;       // converter threads (warps 2-9)
 constexpr int EPI_WARPS = 16;
 constexpr int THREADS = (2 + 8 + EPI_WARPS) * 32;
@@ -73,8 +72,14 @@ constexpr int OFF_RAW = 1024;
 __host__ __device__ constexpr int off_op(bool pre, int bb, int abb) {
     return OFF_RAW + NRAW * raw_stage_bytes(pre, bb, abb);
 }
+__host__ __device__ constexpr int smem_with(int nop, bool pre, int bb, int abb) {
+    return off_op(pre, bb, abb) + nop * op_bytes(abb == 36) + 1024;   // + alignment slack of the dynamic base
+}
+__host__ __device__ constexpr int nop(bool pre, int bb, int abb) {
+    return smem_with(3, pre, bb, abb) <= 227 * 1024 ? 3 : 2;
+}
 __host__ __device__ constexpr int smem_bytes(bool pre, int bb, int abb) {
-    return off_op(pre, bb, abb) + nop(pre) * op_bytes(abb == 36) + 1024;   // + alignment slack of the dynamic base
+    return smem_with(nop(pre, bb, abb), pre, bb, abb);
 }
 
 struct Tc32Params {
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm32_tc_kernel(const __grid_cons
     constexpr int RSB = raw_stage_bytes(PRE, F::BB, F::ABB);
     constexpr int IMG = img_bytes(Q41);
     constexpr int OPB = op_bytes(Q41);
-    constexpr int NOP = nop(PRE);
+    constexpr int NOP = nop(PRE, F::BB, F::ABB);
     constexpr int OFF_OP = off_op(PRE, F::BB, F::ABB);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
