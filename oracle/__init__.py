@@ -72,6 +72,8 @@ def lib():
             L.oracle_matmul_rows.restype = I
             L.oracle_moe.argtypes = [I64] * 5 + [P] * 12
             L.oracle_moe.restype = I
+            L.oracle_moe_down.argtypes = [I64] * 5 + [P] * 7
+            L.oracle_moe_down.restype = I
             L.oracle_swiglu.argtypes = [I, I64, I64, I64, P, P, P, P, P]
             L.oracle_swiglu.restype = I
             _lib = L
@@ -167,3 +169,23 @@ def moe(Wg, Wu, Wd, ids, rw, xq, K: int, F: int):
     if rc != 0:
         raise ValueError("oracle_moe rejected its arguments")
     return dict(y=y, y_abs=y_abs, h=h, hq=hq, gu_aux=aux)
+
+
+def moe_down(Wd, ids, rw, hq, K: int, F: int, valid=None):
+    """The routed FFN from given hidden quantisations on: per (token, slot) the
+    down projection of hq[t][s] (Q8_0 rows over F), combined with the router
+    weights, in fp64. Pairs with valid == 0 are skipped. Returns (y, y_abs), [T, K]."""
+    E = Wd.shape[0]
+    T, topk = ids.shape
+    Wd = np.ascontiguousarray(Wd, dtype=np.uint8)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    rw = np.ascontiguousarray(rw, dtype=np.float32)
+    hq = np.ascontiguousarray(hq, dtype=np.uint8).reshape(T, topk, row_bytes(Q8_0, F))
+    v = None if valid is None else np.ascontiguousarray(valid, dtype=np.int32).reshape(T, topk)
+    y = np.zeros((T, K))
+    y_abs = np.zeros((T, K))
+    rc = lib().oracle_moe_down(T, K, F, E, topk, _p(Wd), _p(ids), _p(rw), _p(v) if v is not None else None,
+                               _p(hq), _p(y), _p(y_abs))
+    if rc != 0:
+        raise ValueError("oracle_moe_down rejected its arguments")
+    return y, y_abs

@@ -420,6 +420,20 @@ int oracle_swiglu(int wfmt, int64_t M, int64_t F, int64_t K, const uint8_t* Wg, 
 
 /* --------------------------------------------------------- routed expert FFN */
 
+/* One (token, slot) pair's down projection, added into the token's output:
+ *   o = W_down[e] . hq   (K values, fp64; W_down[e] rows of F elements)
+ *   y[k] += w * o[k],  y_abs[k] += |w| * absterms(o[k])  (y_abs may be NULL) */
+static void moe_down_pair(int64_t K, int64_t F, const uint8_t* Wd_e, double w, const uint8_t* hq,
+                          double* y, double* y_abs)
+{
+    for (int64_t k = 0; k < K; k++) {
+        double ao;
+        double o = row_dot(ORC_Q4_0, Wd_e + k * (F / 32 * 18), hq, F, &ao);
+        y[k] += w * o;
+        if (y_abs) y_abs[k] += fabs(w) * ao;
+    }
+}
+
 /* For each token t and slot s (expert e = ids[t][s], router weight w = rw[t][s]):
  *   g = W_gate[e] . xq[t],  u = W_up[e] . xq[t]          (F values, fp64)
  *   h = silu(g) * u = g / (1 + exp(-g)) * u               (fp64)
@@ -469,12 +483,33 @@ int oracle_moe(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk,
             }
             oracle_quantize_q8_0(1, F, hf, hq_local);
             if (hq_out) memcpy(hq_out + (t * topk + s) * hr, hq_local, (size_t)hr);
-            for (int64_t k = 0; k < K; k++) {
-                double ao;
-                double o = row_dot(ORC_Q4_0, Wd + e * wdr + k * (F / 32 * 18), hq_local, F, &ao);
-                y[t * K + k] += w * o;
-                if (y_abs) y_abs[t * K + k] += fabs(w) * ao;
-            }
+            moe_down_pair(K, F, Wd + e * wdr, w, hq_local, y + t * K, y_abs ? y_abs + t * K : 0);
+        }
+    }
+    return ORC_OK;
+}
+
+/* The routed FFN's second half from given hidden quantisations (the same
+ * definition as oracle_moe from hq on): for token t and slot s with
+ * valid[t][s] != 0 (valid may be NULL: every pair), expert e = ids[t][s],
+ *   o = W_down[e] . hq[t][s],  y[t] = sum_s rw[t][s] * o   (fp64)
+ * and y_abs [T][K] = sum_s |rw| * absterms(o) (may be NULL). hq: [T][topk]
+ * rows of Q8_0 over F. ORC_BAD for shapes it cannot take or a valid pair's
+ * expert id outside [0, E). */
+int oracle_moe_down(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk, const uint8_t* Wd,
+                    const int32_t* ids, const float* rw, const int32_t* valid, const uint8_t* hq,
+                    double* y, double* y_abs)
+{
+    if (K % 256 || F % 256) return ORC_BAD;
+    int64_t wdr = K * (F / 32 * 18), hr = F / 32 * 34;
+    for (int64_t t = 0; t < T; t++) {
+        for (int64_t k = 0; k < K; k++) { y[t * K + k] = 0.0; if (y_abs) y_abs[t * K + k] = 0.0; }
+        for (int64_t s = 0; s < topk; s++) {
+            int64_t i = t * topk + s;
+            if (valid && !valid[i]) continue;
+            int e = ids[i];
+            if (e < 0 || e >= E) return ORC_BAD;
+            moe_down_pair(K, F, Wd + e * wdr, (double)rw[i], hq + i * hr, y + t * K, y_abs ? y_abs + t * K : 0);
         }
     }
     return ORC_OK;

@@ -386,6 +386,48 @@ def test_moe_brute_force(orc):
         assert np.all(np.abs(r["y"][t] - want) <= r["y_abs"][t] * 1e-13)
 
 
+def test_moe_down_brute_force(orc):
+    """The routed FFN from given hidden quantisations on (oracle_moe_down): every
+    pair's down projection of arbitrary Q8_0 rows, dequantized element by element
+    and summed in exact rationals, weighted and combined over the token's valid
+    slots; a pair marked invalid contributes nothing."""
+    K = F = 256
+    _, _, Wd, ids, rw, _ = _tiny_moe(seed=4, K=K, F=F)
+    T, topk = ids.shape
+    rng = np.random.default_rng(44)
+    hq = orc.quantize(orc.Q8_0, rng.standard_normal((T * topk, F)).astype(np.float32))
+    valid = np.ones((T, topk), np.int32)
+    valid[1, 0] = 0
+    y, ya = orc.moe_down(Wd, ids, rw, hq, K, F, valid)
+    for t in range(T):
+        acc = [Fraction(0)] * K
+        for s in range(topk):
+            if not valid[t, s]:
+                continue
+            for k in range(K):
+                acc[k] += Fraction(float(rw[t, s])) * _exact_dot(orc, 2, Wd[ids[t, s], k], hq[t * topk + s], F)
+        want = np.array([float(a) for a in acc])
+        assert np.all(np.abs(y[t] - want) <= ya[t] * 1e-13)
+    # the skipped pair: token 1's output is its other slot's alone
+    y1, _ = orc.moe_down(Wd, ids[1:2, 1:], rw[1:2, 1:], hq[3:4], K, F)
+    assert np.array_equal(y1[0], y[1])
+
+
+def test_moe_down_continues_moe(orc):
+    """Fed the whole routed FFN's own hidden quantisation, the second half gives
+    the same outputs and bounds bit for bit (one definition, one arithmetic)."""
+    K, F = 256, 512
+    Wg, Wu, Wd, ids, rw, x = _tiny_moe(seed=5, K=K, F=F)
+    xq = orc.quantize(orc.Q8_0, x)
+    r = orc.moe(Wg, Wu, Wd, ids, rw, xq, K, F)
+    y, ya = orc.moe_down(Wd, ids, rw, r["hq"], K, F)
+    assert np.array_equal(y, r["y"]) and np.array_equal(ya, r["y_abs"])
+    bad = ids.copy()
+    bad[0, 0] = Wd.shape[0]
+    with pytest.raises(ValueError):
+        orc.moe_down(Wd, bad, rw, r["hq"], K, F)
+
+
 def test_moe_router_weight_linearity_and_slot_order(orc):
     K = F = 256
     Wg, Wu, Wd, ids, rw, x = _tiny_moe(seed=1, K=K, F=F)
