@@ -43,6 +43,8 @@ SIGNATURES = {
     "cq_moe_gemv_noalloc": (_I, [_I, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P]),
     "cq_moe_workspace_offsets": (_I, [_I64, _I64, _I64, _I64, _I64, _P, _P, _P]),
     "cq_moe_read_status": (_I, [_P, _P, _P]),
+    "cq_moe_noalloc_read_status": (_I, [_P, _P]),
+    "cq_read_device_status": (_I, [_P, _P, _P]),
     "cq_read_global_status": (_I, [_P, _I]),
     "cq_status_string": (C.c_char_p, [_I]),
     "cq_set_option": (_I, [_I, _I64]),
@@ -146,6 +148,19 @@ def cq_moe_workspace_offsets(T, K, F, E, topk):
 def cq_moe_read_status(ws, stream=0):
     code = C.c_int32()
     st = lib().cq_moe_read_status(ws, C.addressof(code), stream)
+    return st, code.value
+
+
+def cq_moe_noalloc_read_status(stream=0):
+    code = C.c_int32()
+    st = lib().cq_moe_noalloc_read_status(C.addressof(code), stream)
+    return st, code.value
+
+
+def cq_read_device_status(ws=None, stream=0):
+    """(status, code) of a MoE workspace's status word, or (ws None) of the library's own word."""
+    code = C.c_int32()
+    st = lib().cq_read_device_status(ws, C.addressof(code), stream)
     return st, code.value
 
 

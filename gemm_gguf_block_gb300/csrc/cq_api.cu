@@ -3,8 +3,9 @@
 // was launched and nothing was written. See include/cq.h for the contract.
 #include <cstdint>
 #include <atomic>
-#include <cstdlib>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -51,12 +52,19 @@ namespace cq {
 std::atomic<int> g_weights_const{0};
 bool weights_const() { return g_weights_const.load(std::memory_order_relaxed) != 0; }
 
-bool pdl_enabled() {
-    static const bool v = [] {
-        const char* e = std::getenv("CQ_PDL");
-        return !(e && e[0] == '0');
-    }();
-    return v;
+std::mutex g_attr_mutex;
+std::map<std::pair<int, const void*>, int> g_attr_raised;
+
+cudaError_t raise_smem_limit(const void* kernel, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    int& have = g_attr_raised[{dev, kernel}];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) have = bytes;
+    return e;
 }
 
 cudaError_t device_info(DeviceInfo* out) {
@@ -286,6 +294,19 @@ cq_status cq_moe_gemv(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t 
                                    static_cast<int>(E), static_cast<int>(topk), W_gate, W_up, W_down, expert_ids,
                                    route_w, xq, y, workspace, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+cq_status cq_read_device_status(const void* workspace, int32_t* out_code, void* stream) {
+    if (out_code == nullptr) return CQ_ERR_INVALID_ARG;
+    if (workspace != nullptr) return cq_moe_read_status(workspace, out_code, stream);
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CQ_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_cq_status, sizeof v) != cudaSuccess) return CQ_ERR_CUDA;
+    const int z = 0;
+    if (v != 0 && cudaMemcpyToSymbol(g_cq_status, &z, sizeof z) != cudaSuccess) return CQ_ERR_CUDA;
+    *out_code = v;
+    if (v & CQ_DEV_WAIT_TIMEOUT) return CQ_ERR_TIMEOUT;
+    return v ? CQ_ERR_DEVICE_STATUS : CQ_OK;
 }
 
 cq_status cq_moe_read_status(const void* workspace, int32_t* out_code, void* stream) {

@@ -8,14 +8,12 @@
 
 namespace cq {
 
-// Programmatic dependent launch (on unless CQ_PDL=0): every kernel of the
-// library is launched so that it may start while the previous grid in the
+// Programmatic dependent launch: every kernel of the library is launched so that it may start while the previous grid in the
 // stream is still running; each kernel's first act is griddepcontrol.wait
 // (pdl_wait), which returns once the grids it depends on have completed and
 // their memory is visible, before any global memory is read or written. The
 // launch latency and the kernel's setup thus overlap the previous kernel's
 // tail, with the same ordering guarantees as a plain launch.
-bool pdl_enabled();
 // CQ_OPT_WEIGHTS_CONST (see include/cq.h).
 bool weights_const();
 
@@ -31,7 +29,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -43,6 +41,11 @@ struct DeviceInfo {
 
 // Cached per-device properties; status address from cudaGetSymbolAddress.
 cudaError_t device_info(DeviceInfo* out);
+
+// Raises `kernel`'s dynamic shared-memory limit on the current device to at
+// least `bytes` (cudaFuncSetAttribute), once per (device, kernel); safe to
+// call from several host threads.
+cudaError_t raise_smem_limit(const void* kernel, int bytes);
 
 cudaError_t launch_quantize(int act_fmt, int64_t M, int64_t K, const float* x, void* xq, cudaStream_t s);
 

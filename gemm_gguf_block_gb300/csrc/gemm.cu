@@ -561,17 +561,10 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (SMEM_BYTES > dev.smem_optin) return cudaErrorInvalidConfiguration;
-    static int raised[64][2] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
-    if (e != cudaSuccess) return e;
     const int pre = workspace != nullptr;
-    if (devid >= 64 || !raised[devid][pre]) {
-        e = cudaFuncSetAttribute(pre ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid][pre] = 1;
-    }
+    cudaError_t e = raise_smem_limit(
+        reinterpret_cast<const void*>(pre ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>), SMEM_BYTES);
+    if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
     if (pre) {
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),

@@ -528,15 +528,8 @@ cudaError_t launch_mode(const DeviceInfo& dev, const CUtensorMap& wmap, const CU
     using F = MF<WF>;
     constexpr int SMEM = smem_bytes(PRE, F::BB, F::ABB);
     if (SMEM > dev.smem_optin) return cudaErrorInvalidConfiguration;
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemm32_tc_kernel<WF, PRE>), SMEM);
     if (e != cudaSuccess) return e;
-    if (devid >= 64 || !raised[devid]) {
-        e = cudaFuncSetAttribute(gemm32_tc_kernel<WF, PRE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = 1;
-    }
     if constexpr (PRE) {
         e = launch_kernel(gemm32_tc_prep_kernel<WF>, dim3(static_cast<unsigned>(p.nchunk), tok_tiles), dim3(256), 0,
                           s, p, const_cast<uint8_t*>(p.img));

@@ -23,7 +23,6 @@
 // for token m in increasing k (for Q4_K: y = fma(d_x, t, y) per superblock) --
 // the fixed evaluation order of include/cq.h.
 #include <algorithm>
-#include <cstdlib>
 
 #include "cq_device.cuh"
 #include "cq_internal.h"
@@ -801,56 +800,13 @@ __global__ void __launch_bounds__(wpc_limit<WF, MT>() * 32) gemv_kernel(const Ge
     }
 }
 
-// CQ_GEMV_MMA=0 keeps several-token calls on the dp4a kernel (for A/B runs).
-bool mma_enabled() {
-    static const bool v = [] {
-        const char* e = std::getenv("CQ_GEMV_MMA");
-        return !(e && e[0] == '0');
-    }();
-    return v;
-}
-
-// CQ_GEMV_XREG=0 reads x from shared memory on every item (for A/B runs).
-bool xreg_enabled() {
-    static const bool v = [] {
-        const char* e = std::getenv("CQ_GEMV_XREG");
-        return !(e && e[0] == '0');
-    }();
-    return v;
-}
-
 // Items a warp prefetches into L2 past its ring before the dependency wait,
 // so DRAM stays busy while the preceding grids drain: 8 for Q8_0 (decode
 // step 118.9 -> 111.7 us), 4 for the 4-bit formats, whose CTAs run more
 // warps (more than that crowds the L2), none for Q6_K, whose items of four
 // rows already fill the L2 at four (standalone LM head 41.0 us with none,
-// 43.0 with 4, 47.1 with 8). CQ_GEMV_L2PF overrides.
-int l2_prefetch_items(int w_fmt) {
-    static const int v = [] {
-        const char* e = std::getenv("CQ_GEMV_L2PF");
-        return e ? std::max(0, std::atoi(e)) : -1;
-    }();
-    return v >= 0 ? v : w_fmt == CQ_Q8_0 ? 8 : w_fmt == CQ_Q6_K ? 0 : 4;
-}
-
-// Ring depth: CQ_GEMV_STAGES (2..4) overrides the choice, for tuning runs.
-int stage_override() {
-    static const int v = [] {
-        const char* e = std::getenv("CQ_GEMV_STAGES");
-        const int s = e ? std::atoi(e) : 0;
-        return (s >= 2 && s <= 4) ? s : 0;
-    }();
-    return v;
-}
-
-// Warps per CTA cap: CQ_GEMV_WPC overrides, for tuning runs.
-int wpc_override() {
-    static const int v = [] {
-        const char* e = std::getenv("CQ_GEMV_WPC");
-        return e ? std::atoi(e) : 0;
-    }();
-    return v;
-}
+// 43.0 with 4, 47.1 with 8).
+constexpr int l2_prefetch_items(int w_fmt) { return w_fmt == CQ_Q8_0 ? 8 : w_fmt == CQ_Q6_K ? 0 : 4; }
 
 template <int WF, int MT, bool SWI>
 cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cudaStream_t s) {
@@ -861,9 +817,8 @@ cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cu
     auto warps_for = [&](int S) { return std::min(wpc_limit<WF, MT>(), (budget - p.act_bytes) / warp_bytes(S)); };
     // Two stages a warp and as many warps as fit: at equal bytes in flight,
     // deeper rings ran slower (a landed stage waits behind an earlier one).
-    const int S = stage_override() > 0 ? stage_override() : 2;
+    constexpr int S = 2;
     int wpc = warps_for(S);
-    if (wpc_override() > 0) wpc = std::min(wpc, wpc_override());
     if (wpc < 1) return cudaErrorInvalidConfiguration;
     p.stages = S;
     p.warp_bytes = warp_bytes(S);
@@ -875,15 +830,8 @@ cudaError_t launch_typed(const DeviceInfo& dev, GemvParams p, int64_t groups, cu
     wpc = static_cast<int>(std::min<int64_t>(wpc, (warps + dev.sm_count - 1) / dev.sm_count));
     const unsigned grid = static_cast<unsigned>((warps + wpc - 1) / wpc);
     const int smem = p.act_bytes + wpc * p.warp_bytes;
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemv_kernel<WF, MT, SWI>), lim);
     if (e != cudaSuccess) return e;
-    if (devid >= 64 || raised[devid] < lim) {
-        e = cudaFuncSetAttribute(gemv_kernel<WF, MT, SWI>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = lim;
-    }
     cudaError_t le = launch_kernel(gemv_kernel<WF, MT, SWI>, dim3(grid), dim3(wpc * 32), smem, s, p);
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
@@ -949,7 +897,7 @@ cudaError_t launch_gemv_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, 
         p.B = std::max(p.R, std::min(32, rows_fit) / p.R * p.R);
         if (p.B * p.M * cpitch > CBUF_FLOATS) return cudaErrorInvalidValue;
         p.tok_pitch = tok_pitch;
-        p.xreg = x_in_regs<WF, 1>() && p.M == 1 && p.nseg == 1 && xreg_enabled() ? 1 : 0;
+        p.xreg = x_in_regs<WF, 1>() && p.M == 1 && p.nseg == 1 ? 1 : 0;
         p.wconst = weights_const() ? 1 : 0;
         p.l2pf = l2_prefetch_items(WF);
         p.act_bytes = (p.M * tok_pitch + 127) / 128 * 128;
@@ -989,7 +937,7 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     }
     const int need = gemv_mma_smem(w_fmt, M, K);
     const bool dp4a_better = w_fmt == CQ_Q8_0 && M <= 3;
-    if (M >= 2 && !dp4a_better && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024) && mma_enabled()) {
+    if (M >= 2 && !dp4a_better && need > 0 && need <= std::min(dev.smem_optin, 227 * 1024)) {
         if (x != nullptr) {
             const cudaError_t e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
             if (e != cudaSuccess) return e;

@@ -246,16 +246,9 @@ MmaSmem mma_smem(int bb, int M, int64_t K) {
 template <int WF, int NT>
 cudaError_t launch_mma_typed(const DeviceInfo& dev, MmaParams p, const CUtensorMap& map, cudaStream_t s) {
     const int smem = p.smem_stage + p.stages * p.stage_bytes;
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemv_mma_kernel<WF, NT>),
+                                           std::min(dev.smem_optin, 227 * 1024));
     if (e != cudaSuccess) return e;
-    if (devid >= 64 || raised[devid] < smem) {
-        e = cudaFuncSetAttribute(gemv_mma_kernel<WF, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 std::min(dev.smem_optin, 227 * 1024));
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = std::min(dev.smem_optin, 227 * 1024);
-    }
     const int tiles = (p.N + tile_rows(NT) - 1) / tile_rows(NT);
     const int grid = std::min(tiles, dev.sm_count);
     return launch_kernel(gemv_mma_kernel<WF, NT>, dim3(grid), dim3((consumers(NT) + 1) * 32), smem, s, map, p);

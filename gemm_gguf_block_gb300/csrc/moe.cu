@@ -257,3 +257,18 @@ extern "C" cq_status cq_moe_gemv_noalloc(cq_format w_fmt, int64_t T, int64_t K, 
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 
+extern "C" cq_status cq_moe_noalloc_read_status(int32_t* out_code, void* stream) {
+    if (out_code == nullptr) return CQ_ERR_INVALID_ARG;
+    uint8_t* scratch = nullptr;
+    if (cq::noalloc_scratch(&scratch) != cudaSuccess) return CQ_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CQ_ERR_CUDA;
+    int v = 0;
+    // The status word is the first section of the layout (offset 0) for every shape.
+    if (cudaMemcpy(&v, scratch + cq::moe_layout(1, 256, 256, 1, 1).status, sizeof v, cudaMemcpyDeviceToHost) !=
+        cudaSuccess)
+        return CQ_ERR_CUDA;
+    *out_code = v;
+    if (v & CQ_DEV_WAIT_TIMEOUT) return CQ_ERR_TIMEOUT;
+    return v ? CQ_ERR_DEVICE_STATUS : CQ_OK;
+}
+

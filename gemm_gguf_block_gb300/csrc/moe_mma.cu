@@ -430,15 +430,8 @@ cudaError_t launch_one(const DeviceInfo& dev, const CUtensorMap& m0, const CUten
     p.stages = std::min(8, (lim - fixed) / per_stage);
     if (p.stages < 2) return cudaErrorInvalidConfiguration;
     const int smem = fixed + p.stages * per_stage;
-    static int raised[64] = {};
-    int devid = 0;
-    cudaError_t e = cudaGetDevice(&devid);
+    cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(moe_mma_kernel<UP>), lim);
     if (e != cudaSuccess) return e;
-    if (devid >= 64 || !raised[devid]) {
-        e = cudaFuncSetAttribute(moe_mma_kernel<UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-        if (e != cudaSuccess) return e;
-        if (devid < 64) raised[devid] = 1;
-    }
     e = launch_kernel(moe_mma_kernel<UP>, dim3(p.rows_per_expert / ROWS, E), dim3(THREADS), smem, s, m0, m1, am, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

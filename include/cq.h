@@ -244,13 +244,19 @@ cq_status cq_moe_gemv(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t 
  * - Calls whose executions overlap on the GPU (two streams, or two host
  *   threads on one device) race on the shared array: serialise them.
  * - Expert-id errors are still skipped as in cq_moe_gemv; their status word
- *   lives in the shared array and is not exposed by this call.
+ *   lives in the shared array: read it with cq_moe_noalloc_read_status.
  */
 #define CQ_MOE_NOALLOC_MAX_BYTES (24u << 20)
 cq_status cq_moe_gemv_noalloc(cq_format w_fmt, int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk,
                               const void* W_gate, const void* W_up, const void* W_down,
                               const int32_t* expert_ids, const float* route_w, const void* xq, float* y,
                               void* stream);
+
+/* Synchronises `stream`, then copies the status word of the last
+ * cq_moe_gemv_noalloc call on the current device (CQ_DEV_* bits; 0 if none
+ * ran) to *out_code; the next call clears it. Return values as for
+ * cq_moe_read_status. Allocates nothing. */
+cq_status cq_moe_noalloc_read_status(int32_t* out_code, void* stream);
 
 /*
  * Byte offsets inside the MoE workspace, for inspection by tests: the status
@@ -263,6 +269,19 @@ cq_status cq_moe_workspace_offsets(int64_t T, int64_t K, int64_t F, int64_t E, i
 /* Synchronises `stream`, then copies the MoE workspace status word to *out_code.
  * Returns CQ_ERR_DEVICE_STATUS if any CQ_DEV_* bit is set, else CQ_OK. */
 cq_status cq_moe_read_status(const void* workspace, int32_t* out_code, void* stream);
+
+/*
+ * The status read-out of the boundary: synchronises `stream`, then copies a
+ * device status word to *out_code.
+ * - workspace != NULL: the status word of a cq_moe_gemv workspace (as
+ *   cq_moe_read_status); the next cq_moe_gemv on that workspace clears it.
+ * - workspace == NULL: the library's own status word (as
+ *   cq_read_global_status with clear = 1: read, then zeroed).
+ * Returns CQ_ERR_TIMEOUT if CQ_DEV_WAIT_TIMEOUT is set, CQ_ERR_DEVICE_STATUS
+ * if any other CQ_DEV_* bit is set, else CQ_OK; CQ_ERR_INVALID_ARG for a null
+ * out_code, CQ_ERR_CUDA if the synchronisation or the copy fails.
+ */
+cq_status cq_read_device_status(const void* workspace, int32_t* out_code, void* stream);
 
 /* Synchronises the current device, then reads (and, if clear != 0, zeroes) the
  * library's own status word, used by kernels that take no workspace (a copy

@@ -193,3 +193,21 @@ def test_moe_validation(L):
     assert call(topk=0) == cq.ERR_SHAPE
     assert call(E=300) == cq.ERR_SHAPE
     assert call(T=0) == cq.OK
+
+
+def test_status_readers_validate(L):
+    """The status read-outs reject a null out_code before touching the device."""
+    assert L.cq_read_device_status(None, None, None) == cq.ERR_INVALID_ARG
+    assert L.cq_read_device_status(A, None, None) == cq.ERR_INVALID_ARG
+    assert L.cq_moe_noalloc_read_status(None, None) == cq.ERR_INVALID_ARG
+    assert L.cq_moe_read_status(None, None, None) == cq.ERR_INVALID_ARG
+
+
+def test_library_reads_no_environment():
+    """Kernel choices are fixed in the code: no source of the library reads an
+    environment variable, so nothing outside a call's arguments and
+    cq_set_option can change which kernel runs."""
+    csrc = os.path.join(ROOT, "gemm_gguf_block_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        assert "getenv" not in text and "secure_getenv" not in text, name

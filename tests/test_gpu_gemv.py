@@ -93,7 +93,7 @@ def test_gemv_exact_arithmetic(orc, wfmt, N, K, M):
 @pytest.mark.parametrize("M,N,K", [(1, 33, 256), (17, 100, 512), (64, 257, 2048), (65, 129, 768),
                                    (130, 96, 4096), (200, 300, 1024)])
 def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
-    """cq_gemm (tcgen05 for Q4_K, mma.sync for the 32-element formats) against
+    """cq_gemm (tcgen05 kernels for Q4_K and for the 32-element formats) against
     the oracle, and each row against the single-token cq_gemv bit for bit;
     M and N ragged against the 64-token / 128-row tiles."""
     torch = torch_cuda()

@@ -14,6 +14,10 @@ legitimately land on either side. The checks therefore go in tiers:
 3. y within TOL * sum|terms| plus, per output, the largest change those
    ambiguous elements could make (one quantisation step each, times the down
    weight and the router weight).
+
+Beside tier 2, the down projection and the combine are checked on their own:
+the oracle recomputes them from the GPU's own hq bytes (oracle_moe_down), and
+y must then lie within TOL * sum|terms| with no allowance at all.
 """
 import numpy as np
 import pytest
@@ -89,7 +93,7 @@ def _run(orc, T, E, topk, K, F, seed, token_sample=None):
     y = y.cpu().numpy()
     tok = np.arange(T) if token_sample is None else token_sample
     r = orc.moe(Wg, Wu, Wd, ids[tok], rw[tok], xq[tok], K, F)
-    return dict(Wd=Wd, ids=ids[tok], rw=rw[tok], y=y[tok], h=h_gpu[tok], hq=hq_gpu[tok], r=r)
+    return dict(Wd=Wd, ids=ids[tok], rw=rw[tok], y=y[tok], h=h_gpu[tok], hq=hq_gpu[tok], r=r, orc=orc)
 
 
 def _check(c, K, F):
@@ -129,7 +133,17 @@ def _check(c, K, F):
     err = np.abs(c["y"].astype(np.float64) - r["y"])
     bound = TOL * r["y_abs"] + allow * 1.01
     assert np.all(err <= bound), f"y: {np.sum(err > bound)} outside the bound"
+    _check_down(c, K, F)
     return int(q_diff.sum()), int(mask.sum())
+
+
+def _check_down(c, K, F, valid=None):
+    """Down projection + combine against the oracle run on the GPU's own hq bytes:
+    within TOL * sum|terms|, no allowance."""
+    y2, ya2 = c["orc"].moe_down(c["Wd"], c["ids"], c["rw"], c["hq"], K, F, valid)
+    err = np.abs(c["y"].astype(np.float64) - y2)
+    bound = TOL * ya2
+    assert np.all(err <= bound), f"y from the GPU's hq: {np.sum(err > bound)} outside TOL * sum|terms|"
 
 
 def test_moe_small(orc):
@@ -160,7 +174,7 @@ def test_moe_many_pairs_per_expert(orc):
     st, so, ho, qo = cq.cq_moe_workspace_offsets(T, K, F, E, topk)
     wsn = ws.cpu().numpy()
     P = T * topk
-    c = dict(Wd=Wd, ids=ids, rw=rw, y=y.cpu().numpy(),
+    c = dict(Wd=Wd, ids=ids, rw=rw, y=y.cpu().numpy(), orc=orc,
              h=wsn[ho:ho + 4 * P * F].view(np.float32).reshape(T, topk, F),
              hq=wsn[qo:qo + P * (F // 32) * 34].reshape(T, topk, -1),
              r=orc.moe(Wg, Wu, Wd, ids, rw, xq, K, F))
@@ -194,11 +208,22 @@ def test_moe_bad_ids_flagged(orc):
                          dev(torch, xq), K, F)
         st, code = cq.cq_moe_read_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
         assert st == cq.ERR_DEVICE_STATUS and code & bit
-        # the rejected pair is skipped; every other token is unaffected
-        ok_t = [t for t in range(T) if all(0 <= ids2[t, s] < E for s in range(topk)) and ids2[t, 0] != ids2[t, 1]]
+        assert cq.cq_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == (st, code)
+        st, so, ho, qo = cq.cq_moe_workspace_offsets(T, K, F, E, topk)
+        wsn = ws.cpu().numpy()
+        P = T * topk
+        h_gpu = wsn[ho:ho + 4 * P * F].view(np.float32).reshape(T, topk, F)
+        hq_gpu = wsn[qo:qo + P * (F // 32) * 34].reshape(T, topk, -1)
+        yy = y.cpu().numpy()
+        # every token, the skipped pair left out: down + combine from the GPU's own hq
+        valid = np.array([[0 <= ids2[t, s] < E and ids2[t, s] not in ids2[t, :s] for s in range(topk)]
+                          for t in range(T)], np.int32)
+        _check_down(dict(orc=orc, Wd=Wd, ids=np.where(valid, ids2, 0), rw=rw, hq=hq_gpu, y=yy), K, F, valid)
+        # the tokens without a bad id: the full tiered check against the oracle
+        ok_t = [t for t in range(T) if valid[t].all()]
         r = orc.moe(Wg, Wu, Wd, ids2[ok_t], rw[ok_t], xq[ok_t], K, F)
-        yy = y.cpu().numpy()[ok_t]
-        assert np.all(np.abs(yy - r["y"]) <= 1e-3 * r["y_abs"] + 1e-30)
+        _check(dict(orc=orc, Wd=Wd, ids=ids2[ok_t], rw=rw[ok_t], y=yy[ok_t], h=h_gpu[ok_t], hq=hq_gpu[ok_t], r=r),
+               K, F)
     # a clean call afterwards reports a clear status
     y, ws = cq.moe_t(dev(torch, Wg), dev(torch, Wu), dev(torch, Wd), dev(torch, ids), dev(torch, rw),
                      dev(torch, xq), K, F)

@@ -69,3 +69,46 @@ def test_noalloc_rejects_before_launch():
     assert cq.cq_moe_gemv_noalloc(cq.Q4_0, 8, 300, 256, 4, 2, A, A, A, A, A, A, A) == cq.ERR_SHAPE
     assert cq.cq_moe_gemv_noalloc(cq.Q8_0, 8, 256, 256, 4, 2, A, A, A, A, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
     assert cq.cq_moe_gemv_noalloc(cq.Q4_0, 0, 256, 256, 4, 2, A, A, A, A, A, A, A) == cq.OK
+
+
+@pytest.mark.gpu
+def test_noalloc_full_routed_ffn_near_the_cap():
+    """The 256-token, 32-expert, 2048/1792 routed FFN, the workload the array is
+    sized for (17.7 MB of its 24 MiB): bit for bit what cq_moe_gemv gives."""
+    torch = torch_cuda()
+    cq_built()
+    stream = torch.cuda.current_stream().cuda_stream
+    Wg, Wu, Wd, ids, rw, x = synth.moe_ffn(0)
+    T, K = x.shape
+    E, F = Wg.shape[0], Wg.shape[1]
+    assert cq.cq_moe_workspace_size(T, K, F, E, 4) > (16 << 20)
+    t = [dev(torch, a) for a in (Wg, Wu, Wd, ids, rw)]
+    xq = cq.quantize_act_t(dev(torch, x), cq.Q8_0)
+    y_ws, _ = cq.moe_t(*t, xq, K, F)
+    y_na = torch.full((T, K), float("nan"), device="cuda")
+    st = cq.cq_moe_gemv_noalloc(cq.Q4_0, T, K, F, E, 4, *[a.data_ptr() for a in t], xq.data_ptr(),
+                                y_na.data_ptr(), stream)
+    assert st == cq.OK, cq.status_string(st)
+    assert cq.cq_moe_noalloc_read_status(stream) == (cq.OK, 0)
+    assert torch.equal(y_na.view(torch.int32), y_ws.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_noalloc_status_word_reports_and_clears():
+    """A repeated expert id is skipped and reported through the array's status
+    word; the next clean call clears it."""
+    torch = torch_cuda()
+    cq_built()
+    stream = torch.cuda.current_stream().cuda_stream
+    sh = dict(T=8, E=4, topk=2, K=256, F=256)
+    Wg, Wu, Wd, ids, rw, x = _problem(7, **sh)
+    xq = cq.quantize_act_t(dev(torch, x), cq.Q8_0)
+    y = torch.empty((sh["T"], sh["K"]), device="cuda")
+    for ids_call, want in ((np.where(np.arange(2)[None, :] == 1, ids[:, :1], ids), cq.DEV_DUP_EXPERT_ID),
+                           (ids, 0)):
+        t = [dev(torch, a) for a in (Wg, Wu, Wd, ids_call.astype(np.int32), rw)]
+        st = cq.cq_moe_gemv_noalloc(cq.Q4_0, sh["T"], sh["K"], sh["F"], sh["E"], sh["topk"],
+                                    *[a.data_ptr() for a in t], xq.data_ptr(), y.data_ptr(), stream)
+        assert st == cq.OK
+        st, code = cq.cq_moe_noalloc_read_status(stream)
+        assert code == want and st == (cq.ERR_DEVICE_STATUS if want else cq.OK)
