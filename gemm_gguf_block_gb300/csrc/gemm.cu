@@ -8,25 +8,40 @@
 //
 // Exact integer contraction on fp16 tensor cores. tcgen05 has no int8 MMA on
 // sm_103a, so the operands are fp16 values that hold integers exactly:
-//   A[n][k] = sc_j(n) * q4(n, k)   in [0, 945]   (weights, MMA M = 128 rows)
+//   A[n][k] = sc_j(n) * q4(n, k)   in [0, 945]    (weights, MMA M = 128 rows)
 //   B[m][k] = q8(m, k)             in [-127, 127] (tokens, MMA N = 128)
-// A superblock's products sum to at most 30.7e6 > 2^24 in magnitude, so each
-// superblock is split into two K = 128 halves, each accumulated in its own
-// fp32 tensor-memory accumulator (|partial| <= 15.4e6 < 2^24: exact). The min
-// term sum_j m_j * bsum_j is one more K = 16 MMA: A = [m_0..m_7, m_0..m_7],
-// B = [64 h_0..64 h_7, l_0..l_7] with bsum_j = 64 h_j + l_j, all exact in fp16.
-// The epilogue then applies, per (row, token, superblock), exactly the fixed
-// fp32 order of include/cq.h -- RN(h0 + h1) is (float)isum_sc; then
-// t = fma(d, S, -(dmin * I)) and y = fma(d_x, t, y) -- so every row equals the
-// cq_gemv row bit for bit.
+// A superblock's isum_sc = sum_j sc_j * S_j reaches 30.7e6 > 2^24, too much
+// for one exact fp32 accumulator, but with the correction
+//   C = 8 * sum_j sc_j * B_j   (B_j = bsum_2j + bsum_2j+1, the 32-element sums)
+// the accumulator starts at -C (one K = 16 MMA) and then takes the 256
+// products: after any subset S of them it holds
+//   sum_{k in S} sc (q4 - 8) q8 - sum_{k not in S} 8 sc q8,
+// whose magnitude is at most 256 * 504 * 127 = 16386048 < 2^24 whatever the
+// order of the additions -- every value the accumulator passes through is an
+// exact integer -- and it ends at X = isum_sc - C. A second copy of -C and
+// the min term I = sum_j m_j * B_j come from two more K = 16 MMAs:
+// A_C = [-8 sc_0..-8 sc_7 | the same], A_I = [m_0..m_7 | the same], B_min =
+// [64 h_0..64 h_7 | l_0..l_7] with B_j = 64 h_j + l_j, all exact in fp16
+// (|C| <= 8 * 63 * 8 * 4064 < 2^24). The epilogue then applies, per (row,
+// token, superblock), exactly the fixed fp32 order of include/cq.h --
+// RN(X - (-C)) is (float)isum_sc; then t = fma(d, S, -(dmin * I)) and
+// y = fma(d_x, t, y) -- so every row equals the cq_gemv row bit for bit.
 //
-// Warp roles (576 or 832 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
-// map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory and
-// one lane issues the MMAs; warps 2-9 convert raw weights and Q8_K
-// activations into fp16 tiles in the canonical K-major no-swizzle layout;
-// warps 10-17 (10-25 with the workspace) are the epilogue (tensor-memory
-// lanes 32*(warp%4)...). Every wait
-// is bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
+// Tensor memory: X in two alternating 128-column buffers, -C and I in 128
+// columns each. The MMAs of superblock s+1 fill the other X buffer while the
+// epilogue drains superblock s; only its two small -C / I MMAs wait for the
+// epilogue to have read the previous ones.
+//
+// Warp roles (864 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
+// map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory
+// and one lane issues the MMAs; warp 2, with a workspace, bulk-copies the
+// pre-converted activation operands (a warp of its own, so that the raw
+// weight boxes run ahead of the operand stages); warps 3-10 convert raw
+// weights (and, without a workspace, Q8_K activations) into fp16 tiles in
+// the canonical K-major no-swizzle layout and fill the min slot (A_C, A_I,
+// B_min, d_x); warps 11-26 are the epilogue (tensor-memory lanes
+// 32*(warp%4), 32 token columns each, y in registers). Every wait is
+// bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -43,37 +58,42 @@ constexpr int BN = 128;          // tokens per tile (MMA N)
 constexpr int KH = 128;          // K per operand stage (half a superblock)
 constexpr int NSTAGE = 2;        // operand stages
 constexpr int NRAW = 3;          // raw weight superblock stages
+constexpr int NMIN = 2;          // min slots (A_C, A_I, B_min of one superblock)
+constexpr int NDX = 4;           // scale slots (the tokens' d_x and the rows' d, dmin of one superblock)
 constexpr int RAW_BYTES = BM * 144;
 constexpr int A_BYTES = BM * KH * 2;        // 32 KB
 constexpr int B_BYTES = BN * KH * 2;        // 32 KB
-constexpr int AMIN_BYTES = BM * 16 * 2;     // 4 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int AC_BYTES = BM * 16 * 2;       // 4 KB
+constexpr int AI_BYTES = BM * 16 * 2;       // 4 KB
 constexpr int BMIN_BYTES = BN * 16 * 2;     // 4 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + AMIN_BYTES + BMIN_BYTES;
-constexpr int NCONV = 256;       // converter threads (warps 2-9)
-// Epilogue warps (from warp 10): 16 when the activations come pre-converted
-// (the converters then need few registers), each thread draining 32 token
-// columns of its row per superblock in 8-column loads; else 8 warps of 64
-// columns in 16-column loads.
-template <bool PRE> struct Epi {
-    static constexpr int WARPS = PRE ? 16 : 8;
-    static constexpr int THREADS = WARPS * 32;
-    static constexpr int COLS = BN / (WARPS / 4);      // token columns per thread
-    static constexpr int CW = PRE ? 8 : 16;            // columns per tensor-memory load
-};
-template <bool PRE> constexpr int kernel_threads() { return (2 + 8) * 32 + Epi<PRE>::THREADS; }
-constexpr uint32_t TMEM_COLS = 512;         // h0 | h1 | mins | y, 128 columns each
-constexpr uint32_t COL_H0 = 0, COL_H1 = 128, COL_MIN = 256, COL_Y = 384;
+constexpr int DX_BYTES = BN * 4;            // 512 B
+constexpr int SCL_BYTES = DX_BYTES + BM * 4;   // a scale slot: d_x [BN] fp32, then (d, dmin) [BM] as fp16 pairs
+constexpr int MIN_BYTES = AC_BYTES + AI_BYTES + BMIN_BYTES;   // 12288
+constexpr int NCONV = 256;                  // converter threads
+constexpr int CONV_WARPS = NCONV / 32;
+constexpr int EPI_WARPS = 16;
+constexpr int COLS = BN / (EPI_WARPS / 4);  // 32 token columns per epilogue thread
+constexpr int CONV_WARP0 = 3;               // first converter warp
+constexpr int EPI_WARP0 = CONV_WARP0 + 8;   // first epilogue warp
+constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
+constexpr uint32_t TMEM_COLS = 512;         // X0 | X1 | C | I, 128 columns each
+constexpr uint32_t COL_C = 256, COL_I = 384;
 
 // Shared-memory layout (offsets from the 1024-aligned dynamic base).
-constexpr int OFF_BAR = 0;                   // 16 barriers
-constexpr int OFF_TMEM = 128;                // tensor-memory base address
-constexpr int OFF_FLAG = 136;                // abort flag
-constexpr int OFF_DX = 256;                  // [2][BN] floats
-constexpr int OFF_RAW = 2048;
+constexpr int OFF_BAR = 0;                   // 27 barriers
+constexpr int OFF_TMEM = 256;                // tensor-memory base address
+constexpr int OFF_FLAG = 264;                // abort flag
+constexpr int OFF_RAW = 1024;
 constexpr int OFF_STAGE = OFF_RAW + NRAW * RAW_BYTES;
-constexpr int SMEM_BYTES = OFF_STAGE + NSTAGE * STAGE_BYTES + 1024;   // + alignment slack
+constexpr int OFF_MIN = OFF_STAGE + NSTAGE * STAGE_BYTES;
+constexpr int OFF_DX = OFF_MIN + NMIN * MIN_BYTES;
+constexpr int SMEM_BYTES = OFF_DX + NDX * SCL_BYTES + 1024;   // + alignment slack of the dynamic base
 
-enum { B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 8, B_ACC_FULL = 10, B_ACC_EMPTY = 11 };
+enum {
+    B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 8, B_MIN_FULL = 10, B_MIN_EMPTY = 12,
+    B_ACC_FULL = 14, B_X_EMPTY = 16, B_CI_EMPTY = 18, B_DX_FULL = 19, B_DX_EMPTY = 23
+};
 
 struct GemmParams {
     const uint8_t* W;
@@ -83,48 +103,92 @@ struct GemmParams {
     int M, N, ns;        // tokens, rows, superblocks per row
     int64_t wrow;        // bytes per weight row
     int64_t xrow;        // bytes per activation row
-    const uint8_t* bimg; // pre-converted B operands: [token tile][superblock] images of IMG_BYTES
-    const float* dxs;    // pre-gathered activation scales: [token tile][superblock][BN]
+    const uint8_t* bimg; // pre-converted activation operands: [token tile][superblock] images of IMG_BYTES
 };
 
 // One (token tile, superblock) image of the pre-converted activations, laid
-// out exactly as the B part of two operand stages: the K-half 0 and K-half 1
-// fp16 tiles, then the mins operand.
-constexpr int IMG_BYTES = 2 * (BN * KH * 2) + BN * 16 * 2;     // 69632
+// out as the B parts of the two operand stages (K-half 0, K-half 1), then the
+// B_min operand (the end of a min slot) and the tokens' d_x (a d_x slot).
+constexpr int IMG_BYTES = 2 * B_BYTES + BMIN_BYTES + DX_BYTES;   // 70144
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// Four nibble pairs (one byte each of w) -> the low nibbles as two half2 of
-// sl * q and the high nibbles as two half2 of sh * q, each exact:
-// (1024 + q) * s - 1024 * s in one fused multiply-add.
-__device__ __forceinline__ void nibbles_to_half(uint32_t w, __half2 sl, __half2 bl, __half2 sh, __half2 bh,
+// K order inside every 4-element group of both operand tiles: elements
+// (0, 2, 1, 3). The contraction sums over K, so any order shared by A and B
+// gives the same integers; this one lets both converters take bytes 0 and 2
+// (then 1 and 3) of a word into one half2 without byte permutes.
+//
+// Four nibble pairs (one byte each of w; low nibble = element i of the low
+// sub-block, high nibble = element i of the high one) -> lo = (q0, q2) * sl,
+// (q1, q3) * sl and hi = the same of the high nibbles times sh, each exact:
+// (1024 + q) * sl - 1024 sl for a low nibble, and (1024 + 16 q) * (sh / 16) -
+// 64 sh for a high nibble masked in place, each one fused multiply-add whose
+// exact result is representable.
+__device__ __forceinline__ void nibbles_to_half(uint32_t w, __half2 sl, __half2 bl, __half2 sh16, __half2 bh,
                                                 uint32_t (&lo)[2], uint32_t (&hi)[2]) {
-    const uint32_t p01 = __byte_perm(w, 0u, 0x4140);   // bytes 0, 1 -> halves 0, 1
-    const uint32_t p23 = __byte_perm(w, 0u, 0x4342);   // bytes 2, 3
-    lo[0] = h2_bits(__hfma2(bits_h2((p01 & 0x000F000Fu) | 0x64006400u), sl, bl));
-    lo[1] = h2_bits(__hfma2(bits_h2((p23 & 0x000F000Fu) | 0x64006400u), sl, bl));
-    hi[0] = h2_bits(__hfma2(bits_h2(((p01 >> 4) & 0x000F000Fu) | 0x64006400u), sh, bh));
-    hi[1] = h2_bits(__hfma2(bits_h2(((p23 >> 4) & 0x000F000Fu) | 0x64006400u), sh, bh));
+    const uint32_t w8 = w >> 8;                          // bytes 1, 3 into the half positions
+    lo[0] = h2_bits(__hfma2(bits_h2((w & 0x000F000Fu) | 0x64006400u), sl, bl));
+    lo[1] = h2_bits(__hfma2(bits_h2((w8 & 0x000F000Fu) | 0x64006400u), sl, bl));
+    hi[0] = h2_bits(__hfma2(bits_h2((w & 0x00F000F0u) | 0x64006400u), sh16, bh));
+    hi[1] = h2_bits(__hfma2(bits_h2((w8 & 0x00F000F0u) | 0x64006400u), sh16, bh));
 }
 
-__device__ __forceinline__ void q4k_scale_min(uint32_t s0, uint32_t s1, uint32_t s2, int j, int& sc, int& mn) {
-    auto byte = [](uint32_t w, int i) { return static_cast<int>((w >> (8 * i)) & 0xffu); };
-    if (j < 4) {
-        sc = byte(s0, j) & 63;
-        mn = byte(s1, j) & 63;
-    } else {
-        sc = (byte(s2, j - 4) & 15) | ((byte(s0, j - 4) >> 6) << 4);
-        mn = (byte(s2, j - 4) >> 4) | ((byte(s1, j - 4) >> 6) << 4);
-    }
+// Four signed bytes (elements 0..3) -> two half2 in the (0, 2, 1, 3) K order:
+// (b0, b2) and (b1, b3), each exact (see tc::s8x4_half).
+__device__ __forceinline__ void s8x4_half_0213(uint32_t w, uint32_t& o0, uint32_t& o1) {
+    const __half2 k1152 = bits_h2(0x64806480u);
+    const uint32_t u = w ^ 0x80808080u;
+    o0 = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4240)), k1152));
+    o1 = h2_bits(__hsub2(bits_h2(__byte_perm(u, 0x64646464u, 0x4341)), k1152));
 }
 
-// PRE: the activations come pre-converted (cq_gemm_ws): the producer
-// bulk-copies each stage's B operand and the converters handle only weights.
+// The sixteen 6-bit values of a Q4_K scale block (words s0, s1, s2 of its
+// twelve bytes), one per byte: sc[0] = sc_0..3, sc[1] = sc_4..7, mn[0] =
+// m_0..3, mn[1] = m_4..7. Bytes 0-3 hold sc_j and m_j in their low six bits
+// and the top two bits of sc_j+4, m_j+4 in bits 6-7; bytes 8-11 hold the low
+// nibbles of sc_j+4 (low) and m_j+4 (high).
+__device__ __forceinline__ void q4k_scales(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t (&sc)[2],
+                                           uint32_t (&mn)[2]) {
+    sc[0] = s0 & 0x3F3F3F3Fu;
+    mn[0] = s1 & 0x3F3F3F3Fu;
+    sc[1] = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
+    mn[1] = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+}
+
+// Bytes (selected by the byte_perm selector sel) of w under a 0x64 high byte:
+// half2 (1024 + v0, 1024 + v1), exact for bytes below 1024.
+__device__ __forceinline__ __half2 bytes_1024(uint32_t w, uint32_t sel) {
+    return bits_h2(__byte_perm(w, 0x64646464u, sel));
+}
+
+// B_min entries of one token: bsum pair word v (bsum_2j, bsum_2j+1) -> B_j =
+// 64 h + l with h = floor(B_j / 64), both parts exact in fp16.
+__device__ __forceinline__ void bmin_entry(uint32_t v, __half& hpart, __half& lpart) {
+    const int pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) + static_cast<int>(static_cast<int16_t>(v >> 16));
+    const int hq = pr >> 6;                                  // floor division by 64
+    hpart = __int2half_rn(64 * hq);
+    lpart = __int2half_rn(pr - 64 * hq);
+}
+
+// A converter warp's bounded wait, decided for the whole warp (its lanes then
+// leave a loop together, so the warp-wide arrivals below cannot hang).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
+    return __all_sync(0xffffffffu, tc::wait_or_abort_sleep(bar, parity, flag, status));
+}
+// One arrival for the warp, after every lane's prior writes (and, when they
+// feed the tensor cores, its proxy fence).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(bar);
+}
+
+// PRE: the activations come pre-converted (cq_gemm_ws): warp 2 bulk-copies
+// each stage's B operand and each min slot's B_min and d_x, and the
+// converters handle only weights.
 template <bool PRE>
-__global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
-                                                                             const GemmParams p) {
-    constexpr int NEPI = Epi<PRE>::THREADS;
+__global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                              const GemmParams p) {
     pdl_trigger();
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
@@ -132,7 +196,6 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_TMEM);
     const SmemFlag abort_flag{smem_u32(smem + OFF_FLAG)};
-    float* dxbuf = reinterpret_cast<float*>(smem + OFF_DX);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
     const int ns = p.ns;
@@ -140,14 +203,25 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
     if (threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(&bars[B_RAW_FULL + i], 1);
-            mbar_init(&bars[B_RAW_EMPTY + i], NCONV);
+            mbar_init(&bars[B_RAW_EMPTY + i], CONV_WARPS);
         }
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], PRE ? NCONV + 1 : NCONV);   // + the producer's copy
+            mbar_init(&bars[B_OP_FULL + i], CONV_WARPS + (PRE ? 1 : 0));   // + the activation copy
             mbar_init(&bars[B_OP_EMPTY + i], 1);
         }
-        mbar_init(&bars[B_ACC_FULL], 1);
-        mbar_init(&bars[B_ACC_EMPTY], NEPI);
+        for (int i = 0; i < NMIN; ++i) {
+            mbar_init(&bars[B_MIN_FULL + i], CONV_WARPS + (PRE ? 1 : 0));
+            mbar_init(&bars[B_MIN_EMPTY + i], 1);                      // the MMA commit
+        }
+        for (int i = 0; i < NDX; ++i) {
+            mbar_init(&bars[B_DX_FULL + i], BM / 32 + (PRE ? 1 : 0));  // the row-scale warps (+ the d_x copy)
+            mbar_init(&bars[B_DX_EMPTY + i], EPI_WARPS);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[B_ACC_FULL + i], 1);
+            mbar_init(&bars[B_X_EMPTY + i], EPI_WARPS);
+        }
+        mbar_init(&bars[B_CI_EMPTY], EPI_WARPS);
         abort_flag.set(0);
         fence_mbar_init();
     }
@@ -163,74 +237,105 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 const int r = s % NRAW;
-                if (!tc::wait_or_abort(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort_sleep(&bars[B_RAW_EMPTY + r], ((s / NRAW) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_RAW_FULL + r], RAW_BYTES);
                 tc::tma_load_2d(smem + OFF_RAW + r * RAW_BYTES, &wmap, 144 * s, n0, &bars[B_RAW_FULL + r]);
-                if constexpr (PRE) {
-                    const uint8_t* img = p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES;
-                    bool ok = true;
-                    for (int h = 0; h < 2; ++h) {
-                        const int q = 2 * s + h, st = q % NSTAGE;
-                        if (!tc::wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
-                        mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES + (h ? BMIN_BYTES : 0));
-                        bulk_g2s(stg + A_BYTES, img + h * B_BYTES, B_BYTES, &bars[B_OP_FULL + st], pol);
-                        if (h)
-                            bulk_g2s(stg + A_BYTES + B_BYTES + AMIN_BYTES, img + 2 * B_BYTES, BMIN_BYTES,
-                                     &bars[B_OP_FULL + st], pol);
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------ activation-operand copies
+        // Per superblock, in the order they are used: B_min into the min slot,
+        // the B operands of the two K halves, then d_x into its slot.
+        if (PRE && lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            for (int s = 0; s < ns && !abort_flag.get(); ++s) {
+                const uint8_t* img = p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES;
+                const int ms = s % NMIN;
+                if (!tc::wait_or_abort_sleep(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bars[B_MIN_FULL + ms], BMIN_BYTES);
+                bulk_g2s(smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES, img + 2 * B_BYTES, BMIN_BYTES,
+                         &bars[B_MIN_FULL + ms], pol);
+                bool ok = true;
+                for (int h = 0; h < 2; ++h) {
+                    const int q = 2 * s + h, st = q % NSTAGE;
+                    if (!tc::wait_or_abort_sleep(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
                     }
-                    if (!ok) break;
+                    mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES);
+                    bulk_g2s(smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES, img + h * B_BYTES, B_BYTES,
+                             &bars[B_OP_FULL + st], pol);
                 }
+                if (!ok) break;
+                const int ds = s % NDX;
+                if (!tc::wait_or_abort_sleep(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&bars[B_DX_FULL + ds], DX_BYTES);
+                bulk_g2s(smem + OFF_DX + ds * SCL_BYTES, img + 2 * B_BYTES + BMIN_BYTES, DX_BYTES,
+                         &bars[B_DX_FULL + ds], pol);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16_f32(BM, BN);
-            const uint32_t stage0 = smem_u32(smem + OFF_STAGE);
+            constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
+            // Descriptors of stage 0 and min slot 0; others differ only in the
+            // start-address field (bytes / 16), which no offset here overflows.
+            const uint64_t op_desc0 = tc::smem_desc(smem_u32(smem + OFF_STAGE), 128, KH * 16);
+            const uint64_t min_desc0 = tc::smem_desc(smem_u32(smem + OFF_MIN), 128, 256);
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
-                if (!tc::wait_or_abort(&bars[B_ACC_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
+                const int b = s & 1, ms = s % NMIN;
+                if (!tc::wait_or_abort_sleep(&bars[B_X_EMPTY + b], ((s >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+                if (!tc::wait_or_abort_sleep(&bars[B_MIN_FULL + ms], (s / NMIN) & 1, abort_flag, p.status)) break;
+                tc::fence_after();
+                const uint32_t xcol = tmem + static_cast<uint32_t>(b * BN);
+                const uint64_t acd = min_desc0 + static_cast<uint32_t>((ms * MIN_BYTES) >> 4);
+                const uint64_t bmd = acd + ((AC_BYTES + AI_BYTES) >> 4);
+                tc::mma_f16(xcol, acd, bmd, idesc, 0);                  // X = -C
                 bool ok = true;
                 for (int h = 0; h < 2; ++h) {
                     const int q = 2 * s + h, st = q % NSTAGE;
-                    if (!tc::wait_or_abort(&bars[B_OP_FULL + st], (q / NSTAGE) & 1, abort_flag, p.status)) {
+                    if (!tc::wait_or_abort_sleep(&bars[B_OP_FULL + st], (q / NSTAGE) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t a0 = stage0 + st * STAGE_BYTES;
-                    const uint32_t b0 = a0 + A_BYTES;
-                    for (int t = 0; t < KH / 16; ++t)
-                        tc::mma_f16(tmem + (h ? COL_H1 : COL_H0), tc::smem_desc(a0 + 256 * t, 128, KH * 16),
-                                    tc::smem_desc(b0 + 256 * t, 128, KH * 16), idesc, t > 0);
-                    if (h == 1)
-                        tc::mma_f16(tmem + COL_MIN, tc::smem_desc(b0 + B_BYTES, 128, 256),
-                                    tc::smem_desc(b0 + B_BYTES + AMIN_BYTES, 128, 256), idesc, 0);
+                    const uint64_t ad = op_desc0 + static_cast<uint32_t>((st * STAGE_BYTES) >> 4);
+                    const uint64_t bd = ad + (A_BYTES >> 4);
+#pragma unroll
+                    for (int t = 0; t < KH / 16; ++t) tc::mma_f16(xcol, ad + 16 * t, bd + 16 * t, idesc, 1);
                     tc::commit(&bars[B_OP_EMPTY + st]);
                 }
                 if (!ok) break;
-                tc::commit(&bars[B_ACC_FULL]);
+                if (!tc::wait_or_abort_sleep(&bars[B_CI_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
+                tc::fence_after();
+                tc::mma_f16(tmem + COL_C, acd, bmd, idesc, 0);          // -C
+                tc::mma_f16(tmem + COL_I, acd + (AC_BYTES >> 4), bmd, idesc, 0);                  // I
+                tc::commit(&bars[B_MIN_EMPTY + ms]);
+                tc::commit(&bars[B_ACC_FULL + b]);
             }
         }
-    } else if (warp < 10) {
+    } else if (warp < EPI_WARP0) {
         // --------------------------------------------------------- converters
-        // Weights: a thread pair per weight row (one 64-element group each),
-        // from the raw stage in shared memory. Activations: warp w converts
-        // tokens 16w..16w+15; each load instruction reads 16 bytes of 8 tokens
-        // (few cache lines) and each store fills whole core-matrix rows; the
-        // next stage's words are loaded one stage ahead.
-        const int tid = threadIdx.x - 64;               // 0..255
-        const int r = tid >> 1, part = tid & 1;         // weight row r, group part
-        const int cw = warp - 2;                        // converter warp 0..7
+        // Weights: thread (row r = tid % 128, part = tid / 128) converts one
+        // 64-element group of each half superblock (groups part and 2 + part)
+        // from the raw stage in shared memory; both groups' words are read at
+        // the first half. A quarter warp covers 8 consecutive rows, so its
+        // 16-byte loads (row pitch 144 bytes) and its stores into the A tile
+        // (row pitch 16 bytes within a core matrix) hit 8 distinct bank
+        // groups. Part 0 also writes the row's A_C entries, part 1 its A_I
+        // entries. Activations (without a workspace): warp w converts tokens
+        // 16w..16w+15; each load instruction reads 16 bytes of 8 tokens (few
+        // cache lines) and each store fills whole core-matrix rows; the next
+        // stage's words are loaded one stage ahead.
+        const int tid = threadIdx.x - 32 * CONV_WARP0;  // 0..255
+        const int r = tid & (BM - 1), part = tid >> 7;  // weight row r, group part
+        const int cw = warp - CONV_WARP0;               // converter warp 0..7
         const int a_row = (r >> 3) * (KH * 16) + (r & 7) * 16 + part * 1024;   // A tile row base (+ k offsets)
         uint32_t cur[16], nxt[16], bcur[4], bnxt[4];
-        auto fetch = [&](int q, uint32_t (&dst)[16], uint32_t (&bs)[4]) {
+        float dxcur = 0.0f, dxnxt = 0.0f;
+        auto fetch = [&](int q, uint32_t (&dst)[16], uint32_t (&bs)[4], float& dxv) {
             const int s = q >> 1, h = q & 1;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -240,7 +345,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                                            p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s + 4 + 128 * h) + word)
                                      : 0u;
             }
-            if (h == 1) {
+            if (h == 0) {
                 // bsum words: token 16cw + 4i + (lane >> 3), word lane & 7
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -249,39 +354,91 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                                               p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s + 260) + (lane & 7))
                                         : 0u;
                 }
+                const int token = m0 + tid;                 // tid < 128: this token's d_x
+                dxv = (tid < BN && token < p.M)
+                          ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s))
+                          : 0.0f;
             }
         };
-        if constexpr (!PRE) fetch(0, cur, bcur);
+        if constexpr (!PRE) fetch(0, cur, bcur, dxcur);
+        uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales and mins, one per byte
+        uint32_t qw[16];                                // the thread's quant words of both halves
         for (int q = 0; q < 2 * ns; ++q) {
             const int s = q >> 1, h = q & 1, st = q % NSTAGE, rs = s % NRAW;
-            if (abort_flag.get()) break;
+            if (__any_sync(0xffffffffu, abort_flag.get())) break;
             if constexpr (!PRE)
-                if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt);
-            if (!tc::wait_or_abort(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
-            if (!tc::wait_or_abort(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+                if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt, dxnxt);
+            if (h == 0) {
+                if (!warp_wait(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+                const uint8_t* raw = smem + OFF_RAW + rs * RAW_BYTES + r * 144;
+                const uint4 hdr = *reinterpret_cast<const uint4*>(raw);
+                q4k_scales(hdr.y, hdr.z, hdr.w, scw, mnw);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 + 32 * (2 * hh + part) + 16 * i);
+                        qw[8 * hh + 4 * i] = v.x; qw[8 * hh + 4 * i + 1] = v.y;
+                        qw[8 * hh + 4 * i + 2] = v.z; qw[8 * hh + 4 * i + 3] = v.w;
+                    }
+                // The superblock's min slot: A_C row r = [-8 sc_0 .. -8 sc_7] twice (part 0),
+                // A_I row r = [m_0 .. m_7] twice (part 1); without a workspace also
+                // B_min and d_x of the tile's tokens.
+                const int ms = s % NMIN;
+                if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) break;
+                uint8_t* slot = smem + OFF_MIN + ms * MIN_BYTES;
+                // -8 sc = (1024 + sc) * -8 + 8192 and m = (1024 + m) - 1024, both exact
+                uint32_t mw[4];
+                const uint32_t src[2] = {part == 0 ? scw[0] : mnw[0], part == 0 ? scw[1] : mnw[1]};
+                const __half2 mul = bits_h2(part == 0 ? 0xC800C800u : 0x3C003C00u);   // -8 or 1
+                const __half2 add = bits_h2(part == 0 ? 0x70007000u : 0xE400E400u);   // 8192 or -1024
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    mw[i] = h2_bits(__hfma2(bytes_1024(src[i >> 1], (i & 1) ? 0x4342u : 0x4140u), mul, add));
+                const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                uint8_t* atile = slot + part * AC_BYTES;
+                *reinterpret_cast<uint4*>(atile + tc::tile_off(r, 0, 16)) = mv;
+                *reinterpret_cast<uint4*>(atile + tc::tile_off(r, 8, 16)) = mv;
+                if constexpr (!PRE) {
+                    uint8_t* bm = slot + AC_BYTES + AI_BYTES;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int t = 16 * cw + 4 * i + (lane >> 3), j = lane & 7;
+                        __half* bh = reinterpret_cast<__half*>(bm + tc::tile_off(t, 0, 16));
+                        bmin_entry(bcur[i], bh[j], bh[64 + j]);         // k = 8 + j: next core matrix (+128 B)
+                    }
+                }
+                fence_proxy_async_smem();
+                warp_arrive(&bars[B_MIN_FULL + ms], lane);
+                if (tid < BM) {
+                    // the scale slot: row r's (d, dmin) word, and without a workspace token tid's d_x
+                    const int ds = s % NDX;
+                    if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
+                    uint8_t* scl = smem + OFF_DX + ds * SCL_BYTES;
+                    reinterpret_cast<uint32_t*>(scl + DX_BYTES)[r] = hdr.x;
+                    if constexpr (!PRE) reinterpret_cast<float*>(scl)[tid] = dxcur;
+                    warp_arrive(&bars[B_DX_FULL + ds], lane);
+                }
+            }
+            if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
             uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
             // A: weight row r, group g = 2h + part: 32 low nibbles (sub-block 2g) and
-            // 32 high nibbles (sub-block 2g + 1)
-            const uint8_t* raw = smem + OFF_RAW + rs * RAW_BYTES + r * 144;
-            const uint4 hdr = *reinterpret_cast<const uint4*>(raw);
+            // 32 high nibbles (sub-block 2g + 1), as sc * q
             {
-                const int g = 2 * h + part;
-                int sc_lo, sc_hi, mn_unused;
-                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g, sc_lo, mn_unused);
-                q4k_scale_min(hdr.y, hdr.z, hdr.w, 2 * g + 1, sc_hi, mn_unused);
-                const __half2 slo = __half2half2(__int2half_rn(sc_lo));
-                const __half2 shi = __half2half2(__int2half_rn(sc_hi));
-                const __half2 blo = __half2half2(__int2half_rn(-1024 * sc_lo));
-                const __half2 bhi = __half2half2(__int2half_rn(-1024 * sc_hi));
-                const uint4 q0 = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g);
-                const uint4 q1 = *reinterpret_cast<const uint4*>(raw + 32 + 32 * g);
-                const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                // sub-blocks 2g and 2g + 1 = bytes 2 part and 2 part + 1 of scw[h]
+                const __half2 k1024 = bits_h2(0x64006400u), km1024 = bits_h2(0xE400E400u);
+                const uint32_t sel_lo = part ? 0x4242u : 0x4040u, sel_hi = part ? 0x4343u : 0x4141u;
+                const uint32_t sw = h ? scw[1] : scw[0];
+                const __half2 slo = __hsub2(bytes_1024(sw, sel_lo), k1024);
+                const __half2 shi16 = __hmul2(__hsub2(bytes_1024(sw, sel_hi), k1024), bits_h2(0x2C002C00u));   // sc / 16
+                const __half2 blo = __hmul2(slo, km1024);
+                const __half2 bhi = __hmul2(shi16, km1024);                                                    // -64 sc
                 uint8_t* arow = stg + a_row;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {        // 8 elements (2 words) per core-matrix row
                     uint32_t l0[2], h0[2], l1[2], h1[2];
-                    nibbles_to_half(qw[2 * c], slo, blo, shi, bhi, l0, h0);
-                    nibbles_to_half(qw[2 * c + 1], slo, blo, shi, bhi, l1, h1);
+                    nibbles_to_half(h ? qw[8 + 2 * c] : qw[2 * c], slo, blo, shi16, bhi, l0, h0);
+                    nibbles_to_half(h ? qw[8 + 2 * c + 1] : qw[2 * c + 1], slo, blo, shi16, bhi, l1, h1);
                     *reinterpret_cast<uint4*>(arow + c * 128) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
                     *reinterpret_cast<uint4*>(arow + (4 + c) * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
                 }
@@ -295,169 +452,114 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
                 const int t = 16 * cw + 8 * (i & 1) + (lane & 7);
                 const int word = 4 * (i >> 1) + (lane >> 3);
                 uint32_t o[2];
-                tc::s8x4_half(cur[i], o[0], o[1]);
+                s8x4_half_0213(cur[i], o[0], o[1]);
                 *reinterpret_cast<uint2*>(bt + (t >> 3) * (KH * 16) + (t & 7) * 16 + (word >> 1) * 128 +
                                           (word & 1) * 8) = make_uint2(o[0], o[1]);
             }
-            if (h == 1) {
-                // mins MMA operands: A_min row r = [m_0..m_7, m_0..m_7] (part 0 threads),
-                // B_min token t = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
-                uint8_t* am = bt + B_BYTES;
-                uint8_t* bm = am + AMIN_BYTES;
-                if (part == 0) {
-                    uint32_t mw[4];
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        int sc0, mn0, sc1, mn1;
-                        q4k_scale_min(hdr.y, hdr.z, hdr.w, j, sc0, mn0);
-                        q4k_scale_min(hdr.y, hdr.z, hdr.w, j + 1, sc1, mn1);
-                        mw[j / 2] = h2_bits(__halves2half2(__int2half_rn(mn0), __int2half_rn(mn1)));
-                    }
-                    const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-                    *reinterpret_cast<uint4*>(am + tc::tile_off(r, 0, 16)) = mv;
-                    *reinterpret_cast<uint4*>(am + tc::tile_off(r, 8, 16)) = mv;
-                }
-#pragma unroll
-                for (int i = 0; i < 4 && !PRE; ++i) {
-                    const int t = 16 * cw + 4 * i + (lane >> 3), j = lane & 7;
-                    const uint32_t v = bcur[i];
-                    const int pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) +
-                                   static_cast<int>(static_cast<int16_t>(v >> 16));
-                    const int hq = pr >> 6;                                  // floor division by 64
-                    __half* bh = reinterpret_cast<__half*>(bm + tc::tile_off(t, 0, 16));
-                    bh[j] = __int2half_rn(64 * hq);
-                    bh[64 + j] = __int2half_rn(pr - 64 * hq);                // k = 8 + j: next core matrix (+128 B)
-                }
-            }
             fence_proxy_async_smem();
-            tc::mbar_arrive(&bars[B_OP_FULL + st]);
-            if (h == 1) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+            warp_arrive(&bars[B_OP_FULL + st], lane);
+            if (h == 1 && lane == 0) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+            if constexpr (!PRE) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
+                for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) bcur[i] = bnxt[i];
+                for (int i = 0; i < 4; ++i) bcur[i] = bnxt[i];
+                dxcur = dxnxt;
+            }
         }
     } else {
         // ----------------------------------------------------------- epilogue
-        // Warp w reads tensor-memory lanes 32*(w%4)..+31 (weight rows); the
-        // warps of column group (w-10)/4 take COLS consecutive token columns.
-        constexpr int COLS = Epi<PRE>::COLS, CW = Epi<PRE>::CW;
-        const int et = threadIdx.x - 320;               // 0..NEPI-1
+        // Warp w drains tensor-memory lanes 32*(w%4).. (weight rows) for the 32
+        // token columns of its column group, in 16x256b fragments: thread t holds
+        // rows 16h + t/4 + 8e (h, e in {0, 1}) and tokens 8g + 2(t%4) + u (g in
+        // 0..3, u in {0, 1}) of that slice, so it reads only its own token pairs'
+        // d_x (a warp-uniform scale vector would cost a shared-memory wavefront per
+        // quarter warp) and its rows' (d, dmin) from the scale slot.
         const int quarter = warp & 3;
-        const int c0 = ((warp - 10) >> 2) * COLS;       // first token column of this warp
-        const int row = n0 + quarter * 32 + lane;
-        const bool row_ok = row < p.N;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int token = m0 + et;                      // et < 128: loads one token's scale
-        auto fetch_scales = [&](int s, float& dxv, uint32_t& ddv) {
-            if constexpr (PRE)
-                dxv = et < BN ? __ldg(p.dxs + (static_cast<int64_t>(blockIdx.y) * ns + s) * BN + et) : 0.0f;
-            else
-                dxv = (et < BN && token < p.M)
-                          ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(token) * p.xrow +
-                                                                 292 * s))
-                          : 0.0f;
-            ddv = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(p.W + row * p.wrow + 144 * s)) : 0u;
-        };
-        float dx_next;
-        uint32_t dd_next;
-        fetch_scales(0, dx_next, dd_next);
-        float yr[PRE ? COLS : 1];                       // PRE: this thread's outputs
+        const int c0 = ((warp - EPI_WARP0) >> 2) * COLS;   // first token column of this warp
+        const int gq = lane >> 2, tq = lane & 3;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint64_t y[16];                                   // [h][e][g]: token pair u = 0, 1
 #pragma unroll
-        for (int i = 0; i < (PRE ? COLS : 1); ++i) yr[i] = 0.0f;
+        for (int i = 0; i < 16; ++i) y[i] = 0;
+        const uint64_t m1 = tc::pk(-1.0f, -1.0f);
+        bool ok = true;
         for (int s = 0; s < ns; ++s) {
-            // this superblock's activation scales and row scales, fetched one superblock ahead
-            if (et < BN) dxbuf[(s & 1) * BN + et] = dx_next;
-            const uint32_t dd = dd_next;
-            if (s + 1 < ns) fetch_scales(s + 1, dx_next, dd_next);
-            const float d = h2f(dd), ndmin = -h2f(dd >> 16);
-            // A bounded wait, then one decision for all epilogue warps (the named
-            // barrier also publishes dxbuf).
-            const bool got = mbar_wait_bounded(&bars[B_ACC_FULL], s & 1, WAIT_LIMIT_NS);
-            if (!tc::named_and(1, NEPI, got)) {
-                if (et == 0) { abort_flag.set(1); atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
+            const int b = s & 1, ds = s % NDX;
+            const bool got = mbar_wait_bounded_sleep(&bars[B_ACC_FULL + b], (s >> 1) & 1, WAIT_LIMIT_NS) &&
+                             mbar_wait_bounded_sleep(&bars[B_DX_FULL + ds], (s / NDX) & 1, WAIT_LIMIT_NS);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) { abort_flag.set(1); atomicOr(p.status, CQ_DEV_WAIT_TIMEOUT); }
+                ok = false;
                 break;
             }
             tc::fence_after();
-            // Fixed order: t = fma(d, RN(h0 + h1), -(dmin * I)); y = fma(d_x, t, y).
-            const uint64_t d2 = tc::pk(d, d), nm2 = tc::pk(ndmin, ndmin);
-            const float2* dx2 = reinterpret_cast<const float2*>(dxbuf + (s & 1) * BN + c0);
-            if constexpr (PRE) {
-                // y stays in registers (COLS per thread); three loads per chunk.
+            const float* dxs = reinterpret_cast<const float*>(smem + OFF_DX + ds * SCL_BYTES);
+            const uint32_t* dds = reinterpret_cast<const uint32_t*>(smem + OFF_DX + ds * SCL_BYTES + DX_BYTES);
+            // Fixed order: t = fma(d, RN(X - (-C)), -(dmin * I)); y = fma(d_x, t, y).
 #pragma unroll
-                for (int cb = 0; cb < COLS; cb += CW) {
-                    uint32_t h0[CW], h1[CW], mi[CW];
-                    tc::ldw<CW>(lane_addr + COL_H0 + c0 + cb, h0);
-                    tc::ldw<CW>(lane_addr + COL_H1 + c0 + cb, h1);
-                    tc::ldw<CW>(lane_addr + COL_MIN + c0 + cb, mi);
+            for (int h = 0; h < 2; ++h) {
+                uint64_t d2[2], nm2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const uint32_t dd = dds[quarter * 32 + 16 * h + 8 * e + gq];
+                    const float d = h2f(dd), ndmin = -h2f(dd >> 16);
+                    d2[e] = tc::pk(d, d);
+                    nm2[e] = tc::pk(ndmin, ndmin);
+                }
+                const uint32_t la = lane_base + (static_cast<uint32_t>(16 * h) << 16) + c0;
+#pragma unroll
+                for (int gp = 0; gp < 2; ++gp) {
+                    uint32_t xv[8], cv[8], iv[8];
+                    tc::ld16x256b_x2(la + b * BN + 16 * gp, xv);
+                    tc::ld16x256b_x2(la + COL_C + 16 * gp, cv);
+                    tc::ld16x256b_x2(la + COL_I + 16 * gp, iv);
                     tc::wait_ld();
 #pragma unroll
-                    for (int i = 0; i < CW; i += 2) {
-                        const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
-                                                    tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
-                        const uint64_t tn =
-                            tc::mul2(nm2, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
-                        const uint64_t t = tc::fma2(d2, S, tn);
-                        const float2 x = dx2[(cb + i) >> 1];
-                        tc::upk(tc::fma2(tc::pk(x.x, x.y), t, tc::pk(yr[cb + i], yr[cb + i + 1])), yr[cb + i],
-                                yr[cb + i + 1]);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int cb = 0; cb < COLS; cb += CW) {
-                    uint32_t h0[CW], h1[CW], mi[CW], yv[CW];
-                    tc::ldw<CW>(lane_addr + COL_H0 + c0 + cb, h0);
-                    tc::ldw<CW>(lane_addr + COL_H1 + c0 + cb, h1);
-                    tc::ldw<CW>(lane_addr + COL_MIN + c0 + cb, mi);
-                    if (s > 0) tc::ldw<CW>(lane_addr + COL_Y + c0 + cb, yv);
-                    tc::wait_ld();
+                    for (int gg = 0; gg < 2; ++gg) {
+                        const int g = 2 * gp + gg;
+                        const float2 dx = *reinterpret_cast<const float2*>(dxs + c0 + 8 * g + 2 * tq);
+                        const uint64_t dx2 = tc::pk(dx.x, dx.y);
 #pragma unroll
-                    for (int i = 0; i < CW; i += 2) {
-                        const uint64_t S = tc::add2(tc::pk(__uint_as_float(h0[i]), __uint_as_float(h0[i + 1])),
-                                                    tc::pk(__uint_as_float(h1[i]), __uint_as_float(h1[i + 1])));
-                        const uint64_t tn =
-                            tc::mul2(nm2, tc::pk(__uint_as_float(mi[i]), __uint_as_float(mi[i + 1])));
-                        const uint64_t t = tc::fma2(d2, S, tn);
-                        const float2 x = dx2[(cb + i) >> 1];
-                        const uint64_t yp = s > 0 ? tc::pk(__uint_as_float(yv[i]), __uint_as_float(yv[i + 1]))
-                                                  : tc::pk(0.0f, 0.0f);
-                        float lo, hi;
-                        tc::upk(tc::fma2(tc::pk(x.x, x.y), t, yp), lo, hi);
-                        yv[i] = __float_as_uint(lo);
-                        yv[i + 1] = __float_as_uint(hi);
-                    }
-                    tc::stw<CW>(lane_addr + COL_Y + c0 + cb, yv);
-                }
-                tc::wait_st();
-            }
-            tc::fence_before();
-            tc::mbar_arrive(&bars[B_ACC_EMPTY]);
-        }
-        if (__all_sync(0xffffffffu, !abort_flag.get())) {
-            // y[m][n] for this row: a warp's stores to one token are 32 consecutive floats.
-            if constexpr (PRE) {
-                if (row_ok) {
-#pragma unroll
-                    for (int i = 0; i < COLS; ++i) {
-                        const int m = m0 + c0 + i;
-                        if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = yr[i];
-                    }
-                }
-            } else {
-                for (int cb = 0; cb < COLS; cb += CW) {
-                    uint32_t yv[CW];
-                    tc::ldw<CW>(lane_addr + COL_Y + c0 + cb, yv);
-                    tc::wait_ld();
-                    if (row_ok) {
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) {
-                            const int m = m0 + c0 + cb + i;
-                            if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = __uint_as_float(yv[i]);
+                        for (int e = 0; e < 2; ++e) {
+                            const int i = 4 * gg + 2 * e;
+                            const uint64_t S = tc::fma2(tc::pk(__uint_as_float(cv[i]), __uint_as_float(cv[i + 1])), m1,
+                                                        tc::pk(__uint_as_float(xv[i]), __uint_as_float(xv[i + 1])));
+                            const uint64_t tn =
+                                tc::mul2(nm2[e], tc::pk(__uint_as_float(iv[i]), __uint_as_float(iv[i + 1])));
+                            const uint64_t t = tc::fma2(d2[e], S, tn);
+                            uint64_t& yy = y[(2 * h + e) * 4 + g];
+                            yy = tc::fma2(dx2, t, yy);
                         }
                     }
                 }
             }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&bars[B_X_EMPTY + b]);
+                tc::mbar_arrive(&bars[B_CI_EMPTY]);
+                tc::mbar_arrive(&bars[B_DX_EMPTY + ds]);
+            }
+        }
+        if (ok && __all_sync(0xffffffffu, !abort_flag.get())) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = n0 + quarter * 32 + 16 * h + 8 * e + gq;
+                    if (row >= p.N) continue;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        float v[2];
+                        tc::upk(y[(2 * h + e) * 4 + g], v[0], v[1]);
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int m = m0 + c0 + 8 * g + 2 * tq + u;
+                            if (m < p.M) p.y[static_cast<int64_t>(m) * p.N + row] = v[u];
+                        }
+                    }
+                }
         }
     }
 
@@ -467,7 +569,7 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
     __syncthreads();
     if (abort_flag.get() && threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) (void)mbar_wait_bounded(&bars[B_RAW_FULL + i], 0, WAIT_LIMIT_NS / 8);
-        (void)mbar_wait_bounded(&bars[B_ACC_FULL], 0, WAIT_LIMIT_NS / 8);
+        for (int i = 0; i < 2; ++i) (void)mbar_wait_bounded(&bars[B_ACC_FULL + i], 0, WAIT_LIMIT_NS / 8);
     }
     __syncthreads();
     tc::fence_after();
@@ -475,10 +577,10 @@ __global__ void __launch_bounds__(kernel_threads<PRE>(), 1) gemm_q4k_kernel(cons
 }
 
 // Pre-conversion of Q8_K activations for cq_gemm_ws: one CTA per (superblock
-// s, token tile), thread (token t, K-half h). Writes the tile's B operand
-// images -- the same values and layout the in-kernel converters produce --
-// and the activation scales.
-__global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint8_t* bimg, float* dxs) {
+// s, token tile), thread (token t, K-half h). Writes the tile's image -- the
+// B operands, B_min and d_x, the same values and layout the in-kernel
+// converters produce.
+__global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint8_t* bimg) {
     pdl_trigger();
     pdl_wait();
     const int s = blockIdx.x, tile = blockIdx.y, ns = p.ns;
@@ -493,27 +595,20 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
     for (int g = 0; g < KH / 8; ++g) {       // 8 elements (one core-matrix row) per store
         uint32_t o0[2] = {0u, 0u}, o1[2] = {0u, 0u};
         if (on) {
-            tc::s8x4_half(__ldg(qw + 2 * g), o0[0], o0[1]);
-            tc::s8x4_half(__ldg(qw + 2 * g + 1), o1[0], o1[1]);
+            s8x4_half_0213(__ldg(qw + 2 * g), o0[0], o0[1]);
+            s8x4_half_0213(__ldg(qw + 2 * g + 1), o1[0], o1[1]);
         }
         *reinterpret_cast<uint4*>(bt + tc::tile_off(t, 8 * g, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
     }
     if (h == 0) {
-        dxs[(static_cast<int64_t>(tile) * ns + s) * BN + t] = on ? __ldg(reinterpret_cast<const float*>(blk)) : 0.0f;
+        reinterpret_cast<float*>(img + 2 * B_BYTES + BMIN_BYTES)[t] =
+            on ? __ldg(reinterpret_cast<const float*>(blk)) : 0.0f;
     } else {
-        // mins operand: token t = [64 h_0 .. 64 h_7, l_0 .. l_7], bsum pair j = 64 h_j + l_j
-        __half* bh = reinterpret_cast<__half*>(img + 2 * (BN * KH * 2) + tc::tile_off(t, 0, 16));
+        // B_min: token t = [64 h_0 .. 64 h_7, l_0 .. l_7], B_j = 64 h_j + l_j
+        __half* bh = reinterpret_cast<__half*>(img + 2 * B_BYTES + tc::tile_off(t, 0, 16));
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            int pr = 0;
-            if (on) {
-                const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(blk + 260) + j);
-                pr = static_cast<int>(static_cast<int16_t>(v & 0xffffu)) + static_cast<int>(static_cast<int16_t>(v >> 16));
-            }
-            const int hq = pr >> 6;                                  // floor division by 64
-            bh[j] = __int2half_rn(64 * hq);
-            bh[64 + j] = __int2half_rn(pr - 64 * hq);                // k = 8 + j: next core matrix (+128 B)
-        }
+        for (int j = 0; j < 8; ++j)
+            bmin_entry(on ? __ldg(reinterpret_cast<const uint32_t*>(blk + 260) + j) : 0u, bh[j], bh[64 + j]);
     }
 }
 
@@ -524,7 +619,7 @@ size_t gemm_workspace_size(int w_fmt, int64_t M, int64_t K) {
     if (w_fmt != CQ_Q4_K) return gemm32_workspace_size(w_fmt, M, K);
     if (M <= 0) return 0;
     const int64_t cells = (M + BN - 1) / BN * (K / 256);
-    return static_cast<size_t>(cells) * (IMG_BYTES + BN * 4);
+    return static_cast<size_t>(cells) * IMG_BYTES;
 }
 
 cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, int64_t K, const void* W,
@@ -544,11 +639,7 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
     p.wrow = static_cast<int64_t>(p.ns) * 144;
     p.xrow = static_cast<int64_t>(p.ns) * 292;
     const int tiles_m = static_cast<int>((M + BN - 1) / BN);
-    if (workspace != nullptr) {
-        uint8_t* ws = static_cast<uint8_t*>(workspace);
-        p.bimg = ws;
-        p.dxs = reinterpret_cast<const float*>(ws + static_cast<int64_t>(tiles_m) * p.ns * IMG_BYTES);
-    }
+    if (workspace != nullptr) p.bimg = static_cast<const uint8_t*>(workspace);
     // Raw weights as a 2-D byte tensor [N rows][wrow bytes]; a box is one
     // superblock (144 bytes) of 128 rows; rows past N read as zero.
     CUtensorMap map;
@@ -568,11 +659,11 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
     const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
     if (pre) {
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
-                          dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg), const_cast<float*>(p.dxs));
+                          dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg));
         if (e != cudaSuccess) return e;
-        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(kernel_threads<true>()), SMEM_BYTES, s, map, p);
+        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
     }
-    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(kernel_threads<false>()), SMEM_BYTES, s, map, p);
+    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
 }
 
 }  // namespace cq

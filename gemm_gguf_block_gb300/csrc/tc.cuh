@@ -55,6 +55,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Sm
     atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
     return false;
 }
+// The same, parked between checks (mbar_wait_bounded_sleep): for roles that
+// share their schedulers with busy warps.
+__device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t parity, SmemFlag flag, int* status) {
+    if (mbar_wait_bounded_sleep(bar, parity, WAIT_LIMIT_NS)) return true;
+    flag.set(1);
+    atomicOr(status, CQ_DEV_WAIT_TIMEOUT);
+    return false;
+}
 
 // ------------------------------------------------------------------- MMA
 // D[tmem] (+)= A[smem] * B[smem]^T, fp16 operands, fp32 accumulator.
