@@ -168,6 +168,8 @@ def host_cpu():
             pass
     if isinstance(info.get("sockets"), int) and isinstance(info.get("cores_per_socket"), int):
         info["physical_cores"] = info["sockets"] * info["cores_per_socket"]
+    elif isinstance(info.get("logical_cpus"), int) and isinstance(info.get("threads_per_core"), int):
+        info["physical_cores"] = info["logical_cpus"] // max(1, info["threads_per_core"])
     return info
 
 
