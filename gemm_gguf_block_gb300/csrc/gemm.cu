@@ -37,11 +37,12 @@
 // and one lane issues the MMAs; warp 2, with a workspace, bulk-copies the
 // pre-converted activation operands (a warp of its own, so that the raw
 // weight boxes run ahead of the operand stages); warps 3-10 convert raw
-// weights (and, without a workspace, Q8_K activations) into fp16 tiles in
-// the canonical K-major no-swizzle layout and fill the min slot (A_C, A_I,
-// B_min, d_x); warps 11-26 are the epilogue (tensor-memory lanes
-// 32*(warp%4), 32 token columns each, y in registers). Every wait is
-// bounded; a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
+// weights into fp16 A tiles (K-major, no swizzle) and fill the min slot's
+// A_C and A_I; warps 11-26 are the epilogue (tensor-memory lanes
+// 32*(warp%4), 32 token columns each, y in registers) and, without a
+// workspace, also convert the Q8_K activations into the B tiles (K-major,
+// 128-byte swizzle), B_min and d_x. Every wait is bounded; a timeout flags
+// CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -57,7 +58,6 @@ constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;          // tokens per tile (MMA N)
 constexpr int KH = 128;          // K per operand stage (half a superblock)
 constexpr int NSTAGE = 2;        // operand stages
-constexpr int NRAW = 3;          // raw weight superblock stages
 constexpr int NMIN = 2;          // min slots (A_C, A_I, B_min of one superblock)
 constexpr int NDX = 4;           // scale slots (the tokens' d_x and the rows' d, dmin of one superblock)
 constexpr int RAW_BYTES = BM * 144;
@@ -80,15 +80,24 @@ constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;         // X0 | X1 | C | I, 128 columns each
 constexpr uint32_t COL_C = 256, COL_I = 384;
 
-// Shared-memory layout (offsets from the 1024-aligned dynamic base).
+constexpr int XS_BYTES = BN * 256;          // the next superblock's Q8_K quants of the tile's tokens
+// Shared-memory layout (offsets from the 1024-aligned dynamic base). Without
+// a workspace the raw weight ring is one stage shorter, which makes room for
+// the activation staging area XS.
 constexpr int OFF_BAR = 0;                   // 27 barriers
 constexpr int OFF_TMEM = 256;                // tensor-memory base address
 constexpr int OFF_FLAG = 264;                // abort flag
 constexpr int OFF_RAW = 1024;
-constexpr int OFF_STAGE = OFF_RAW + NRAW * RAW_BYTES;
-constexpr int OFF_MIN = OFF_STAGE + NSTAGE * STAGE_BYTES;
-constexpr int OFF_DX = OFF_MIN + NMIN * MIN_BYTES;
-constexpr int SMEM_BYTES = OFF_DX + NDX * SCL_BYTES + 1024;   // + alignment slack of the dynamic base
+template <bool PRE>
+struct Layout {
+    static constexpr int NRAW = PRE ? 3 : 2;   // raw weight superblock stages
+    static constexpr int OFF_STAGE = OFF_RAW + NRAW * RAW_BYTES;   // 1024-aligned (swizzled B tiles)
+    static constexpr int OFF_MIN = OFF_STAGE + NSTAGE * STAGE_BYTES;
+    static constexpr int OFF_DX = OFF_MIN + NMIN * MIN_BYTES;
+    static constexpr int OFF_XS = OFF_DX + NDX * SCL_BYTES;
+    static constexpr int SMEM_BYTES = OFF_XS + (PRE ? 0 : XS_BYTES) + 1024;   // + alignment slack of the base
+};
+static_assert(Layout<true>::OFF_STAGE % 1024 == 0 && Layout<false>::OFF_STAGE % 1024 == 0, "B tile alignment");
 
 enum {
     B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 8, B_MIN_FULL = 10, B_MIN_EMPTY = 12,
@@ -184,11 +193,15 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 }
 
 // PRE: the activations come pre-converted (cq_gemm_ws): warp 2 bulk-copies
-// each stage's B operand and each min slot's B_min and d_x, and the
-// converters handle only weights.
+// each stage's B operand and each min slot's B_min and d_x. Without it the
+// epilogue warps convert the Q8_K activations of superblock s+1 (between
+// draining superblocks s-1 and s). Either way the converters handle only
+// weights.
 template <bool PRE>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
+    using L = Layout<PRE>;
+    constexpr int NRAW = L::NRAW, OFF_STAGE = L::OFF_STAGE, OFF_MIN = L::OFF_MIN, OFF_DX = L::OFF_DX;
     pdl_trigger();
     pdl_wait();
     extern __shared__ uint8_t smem_raw[];
@@ -206,15 +219,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             mbar_init(&bars[B_RAW_EMPTY + i], CONV_WARPS);
         }
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], CONV_WARPS + (PRE ? 1 : 0));   // + the activation copy
+            mbar_init(&bars[B_OP_FULL + i], CONV_WARPS + (PRE ? 1 : EPI_WARPS));   // + the activation copy or converters
             mbar_init(&bars[B_OP_EMPTY + i], 1);
         }
         for (int i = 0; i < NMIN; ++i) {
-            mbar_init(&bars[B_MIN_FULL + i], CONV_WARPS + (PRE ? 1 : 0));
+            mbar_init(&bars[B_MIN_FULL + i], CONV_WARPS + (PRE ? 1 : EPI_WARPS));
             mbar_init(&bars[B_MIN_EMPTY + i], 1);                      // the MMA commit
         }
         for (int i = 0; i < NDX; ++i) {
-            mbar_init(&bars[B_DX_FULL + i], BM / 32 + (PRE ? 1 : 0));  // the row-scale warps (+ the d_x copy)
+            mbar_init(&bars[B_DX_FULL + i], BM / 32 + (PRE ? 1 : BN / 32));   // the row-scale warps + the d_x writers
             mbar_init(&bars[B_DX_EMPTY + i], EPI_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
@@ -282,7 +295,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
             // Descriptors of stage 0 and min slot 0; others differ only in the
             // start-address field (bytes / 16), which no offset here overflows.
+            // A tiles: no swizzle; B tiles: 128-byte swizzle (two 64-element
+            // column blocks of BN rows).
             const uint64_t op_desc0 = tc::smem_desc(smem_u32(smem + OFF_STAGE), 128, KH * 16);
+            const uint64_t b_desc0 = tc::smem_desc_sw128(smem_u32(smem + OFF_STAGE + A_BYTES), 1024);
             const uint64_t min_desc0 = tc::smem_desc(smem_u32(smem + OFF_MIN), 128, 256);
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 const int b = s & 1, ms = s % NMIN;
@@ -302,9 +318,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     }
                     tc::fence_after();
                     const uint64_t ad = op_desc0 + static_cast<uint32_t>((st * STAGE_BYTES) >> 4);
-                    const uint64_t bd = ad + (A_BYTES >> 4);
+                    const uint64_t bd = b_desc0 + static_cast<uint32_t>((st * STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int t = 0; t < KH / 16; ++t) tc::mma_f16(xcol, ad + 16 * t, bd + 16 * t, idesc, 1);
+                    for (int t = 0; t < KH / 16; ++t)
+                        tc::mma_f16(xcol, ad + 16 * t, bd + (t >> 2) * (BN * 128 / 16) + 2 * (t & 3), idesc, 1);
                     tc::commit(&bars[B_OP_EMPTY + st]);
                 }
                 if (!ok) break;
@@ -325,49 +342,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // 16-byte loads (row pitch 144 bytes) and its stores into the A tile
         // (row pitch 16 bytes within a core matrix) hit 8 distinct bank
         // groups. Part 0 also writes the row's A_C entries, part 1 its A_I
-        // entries. Activations (without a workspace): warp w converts tokens
-        // 16w..16w+15; each load instruction reads 16 bytes of 8 tokens (few
-        // cache lines) and each store fills whole core-matrix rows; the next
-        // stage's words are loaded one stage ahead.
+        // entries.
         const int tid = threadIdx.x - 32 * CONV_WARP0;  // 0..255
         const int r = tid & (BM - 1), part = tid >> 7;  // weight row r, group part
-        const int cw = warp - CONV_WARP0;               // converter warp 0..7
         const int a_row = (r >> 3) * (KH * 16) + (r & 7) * 16 + part * 1024;   // A tile row base (+ k offsets)
-        uint32_t cur[16], nxt[16], bcur[4], bnxt[4];
-        float dxcur = 0.0f, dxnxt = 0.0f;
-        auto fetch = [&](int q, uint32_t (&dst)[16], uint32_t (&bs)[4], float& dxv) {
-            const int s = q >> 1, h = q & 1;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int token = m0 + 16 * cw + 8 * (i & 1) + (lane & 7);
-                const int word = 4 * (i >> 1) + (lane >> 3);
-                dst[i] = token < p.M ? __ldg(reinterpret_cast<const uint32_t*>(
-                                           p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s + 4 + 128 * h) + word)
-                                     : 0u;
-            }
-            if (h == 0) {
-                // bsum words: token 16cw + 4i + (lane >> 3), word lane & 7
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int token = m0 + 16 * cw + 4 * i + (lane >> 3);
-                    bs[i] = token < p.M ? __ldg(reinterpret_cast<const uint32_t*>(
-                                              p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s + 260) + (lane & 7))
-                                        : 0u;
-                }
-                const int token = m0 + tid;                 // tid < 128: this token's d_x
-                dxv = (tid < BN && token < p.M)
-                          ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(token) * p.xrow + 292 * s))
-                          : 0.0f;
-            }
-        };
-        if constexpr (!PRE) fetch(0, cur, bcur, dxcur);
         uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales and mins, one per byte
         uint32_t qw[16];                                // the thread's quant words of both halves
         for (int q = 0; q < 2 * ns; ++q) {
             const int s = q >> 1, h = q & 1, st = q % NSTAGE, rs = s % NRAW;
             if (__any_sync(0xffffffffu, abort_flag.get())) break;
-            if constexpr (!PRE)
-                if (q + 1 < 2 * ns) fetch(q + 1, nxt, bnxt, dxnxt);
             if (h == 0) {
                 if (!warp_wait(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
                 const uint8_t* raw = smem + OFF_RAW + rs * RAW_BYTES + r * 144;
@@ -399,24 +382,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 uint8_t* atile = slot + part * AC_BYTES;
                 *reinterpret_cast<uint4*>(atile + tc::tile_off(r, 0, 16)) = mv;
                 *reinterpret_cast<uint4*>(atile + tc::tile_off(r, 8, 16)) = mv;
-                if constexpr (!PRE) {
-                    uint8_t* bm = slot + AC_BYTES + AI_BYTES;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int t = 16 * cw + 4 * i + (lane >> 3), j = lane & 7;
-                        __half* bh = reinterpret_cast<__half*>(bm + tc::tile_off(t, 0, 16));
-                        bmin_entry(bcur[i], bh[j], bh[64 + j]);         // k = 8 + j: next core matrix (+128 B)
-                    }
-                }
                 fence_proxy_async_smem();
                 warp_arrive(&bars[B_MIN_FULL + ms], lane);
                 if (tid < BM) {
-                    // the scale slot: row r's (d, dmin) word, and without a workspace token tid's d_x
+                    // the scale slot: row r's (d, dmin) word
                     const int ds = s % NDX;
                     if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
                     uint8_t* scl = smem + OFF_DX + ds * SCL_BYTES;
                     reinterpret_cast<uint32_t*>(scl + DX_BYTES)[r] = hdr.x;
-                    if constexpr (!PRE) reinterpret_cast<float*>(scl)[tid] = dxcur;
                     warp_arrive(&bars[B_DX_FULL + ds], lane);
                 }
             }
@@ -443,29 +416,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     *reinterpret_cast<uint4*>(arow + (4 + c) * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
                 }
             }
-            // B: tokens 16cw .. 16cw + 15; load i holds token 16cw + 8(i&1) + lane%8,
-            // quant word 4(i>>1) + lane/8 (elements 4*word .. +3 of the half), so a
-            // half-warp's 8-byte stores fill one 128-byte core matrix.
-            uint8_t* bt = stg + A_BYTES;
-#pragma unroll
-            for (int i = 0; i < 16 && !PRE; ++i) {
-                const int t = 16 * cw + 8 * (i & 1) + (lane & 7);
-                const int word = 4 * (i >> 1) + (lane >> 3);
-                uint32_t o[2];
-                s8x4_half_0213(cur[i], o[0], o[1]);
-                *reinterpret_cast<uint2*>(bt + (t >> 3) * (KH * 16) + (t & 7) * 16 + (word >> 1) * 128 +
-                                          (word & 1) * 8) = make_uint2(o[0], o[1]);
-            }
             fence_proxy_async_smem();
             warp_arrive(&bars[B_OP_FULL + st], lane);
             if (h == 1 && lane == 0) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
-            if constexpr (!PRE) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) cur[i] = nxt[i];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) bcur[i] = bnxt[i];
-                dxcur = dxnxt;
-            }
         }
     } else {
         // ----------------------------------------------------------- epilogue
@@ -475,7 +428,78 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // 0..3, u in {0, 1}) of that slice, so it reads only its own token pairs'
         // d_x (a warp-uniform scale vector would cost a shared-memory wavefront per
         // quarter warp) and its rows' (d, dmin) from the scale slot.
+        //
+        // Without a workspace these warps also write the activation operands
+        // of the next superblock: warp ew converts tokens 8ew..8ew+7 of both
+        // K halves, lane w holding quant word w of each (in the swizzled B
+        // tile a store instruction fills two whole 128-byte rows), thread etid
+        // the B_min entries 2(etid%4), +1 of token etid/4, and the first four
+        // warps the tokens' d_x. The quant words travel one superblock ahead
+        // by asynchronous copies into the staging area XS (each thread reads
+        // back only what it copied; a copy instruction covers 128 contiguous
+        // bytes of one token), the bsums and d_x in registers.
         const int quarter = warp & 3;
+        const int ew = warp - EPI_WARP0, etid = threadIdx.x - 32 * EPI_WARP0;
+        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + 8 * ew * 64 + lane;   // [token][64 words]
+        uint32_t bsw[2] = {0u, 0u};
+        float dxw = 0.0f;
+        auto fetch_b = [&](int s) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int tok = m0 + 8 * ew + i;
+                const uint32_t n = tok < p.M ? 4u : 0u;
+                const uint32_t* row = reinterpret_cast<const uint32_t*>(
+                    p.xq + static_cast<int64_t>(tok < p.M ? tok : 0) * p.xrow + 292 * s + 4) + lane;
+                cp_async4(xs + 64 * i, row, n);
+                cp_async4(xs + 64 * i + 32, row + 32, n);
+            }
+            cp_async_commit();
+            const int btok = m0 + (etid >> 2);
+            const uint32_t* bs = reinterpret_cast<const uint32_t*>(
+                p.xq + static_cast<int64_t>(btok < p.M ? btok : 0) * p.xrow + 292 * s + 260);
+            bsw[0] = btok < p.M ? __ldg(bs + 2 * (etid & 3)) : 0u;
+            bsw[1] = btok < p.M ? __ldg(bs + 2 * (etid & 3) + 1) : 0u;
+            const int dtok = m0 + etid;
+            dxw = (etid < BN && dtok < p.M)
+                      ? __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(dtok) * p.xrow + 292 * s))
+                      : 0.0f;
+        };
+        auto put_b = [&](int s) -> bool {
+            cp_async_wait_all();
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int q = 2 * s + h, st = q % NSTAGE;
+                if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) return false;
+                // word w = lane of token 8ew + i: elements 4w..4w+3, at tile_off_sw128(8ew + i, 4w)
+                uint8_t* bt = smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES + (lane >> 4) * (BN * 128) +
+                              ew * 1024 + (lane & 1) * 8;
+                const int c16 = (lane & 15) >> 1 << 4;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t o0, o1;
+                    s8x4_half_0213(xs[64 * i + 32 * h], o0, o1);
+                    *reinterpret_cast<uint2*>(bt + 128 * i + (c16 ^ (i << 4))) = make_uint2(o0, o1);
+                }
+                fence_proxy_async_smem();
+                warp_arrive(&bars[B_OP_FULL + st], lane);
+            }
+            const int ms = s % NMIN;
+            if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) return false;
+            __half* bh = reinterpret_cast<__half*>(smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES +
+                                                   tc::tile_off(etid >> 2, 0, 16));
+            const int j = 2 * (etid & 3);
+            bmin_entry(bsw[0], bh[j], bh[64 + j]);           // k = 8 + j: next core matrix (+128 B)
+            bmin_entry(bsw[1], bh[j + 1], bh[65 + j]);
+            fence_proxy_async_smem();
+            warp_arrive(&bars[B_MIN_FULL + ms], lane);
+            if (etid < BN) {
+                const int ds = s % NDX;
+                if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) return false;
+                reinterpret_cast<float*>(smem + OFF_DX + ds * SCL_BYTES)[etid] = dxw;
+                warp_arrive(&bars[B_DX_FULL + ds], lane);
+            }
+            return true;
+        };
         const int c0 = ((warp - EPI_WARP0) >> 2) * COLS;   // first token column of this warp
         const int gq = lane >> 2, tq = lane & 3;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -484,7 +508,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         for (int i = 0; i < 16; ++i) y[i] = 0;
         const uint64_t m1 = tc::pk(-1.0f, -1.0f);
         bool ok = true;
-        for (int s = 0; s < ns; ++s) {
+        if constexpr (!PRE) {
+            fetch_b(0);
+            ok = put_b(0);
+            if (ns > 1) fetch_b(1);
+        }
+        for (int s = 0; s < ns && ok; ++s) {
+            if constexpr (!PRE)
+                if (s + 1 < ns) {
+                    if (!put_b(s + 1)) {
+                        ok = false;
+                        break;
+                    }
+                    if (s + 2 < ns) fetch_b(s + 2);
+                }
             const int b = s & 1, ds = s % NDX;
             const bool got = mbar_wait_bounded_sleep(&bars[B_ACC_FULL + b], (s >> 1) & 1, WAIT_LIMIT_NS) &&
                              mbar_wait_bounded_sleep(&bars[B_DX_FULL + ds], (s / NDX) & 1, WAIT_LIMIT_NS);
@@ -542,6 +579,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 tc::mbar_arrive(&bars[B_DX_EMPTY + ds]);
             }
         }
+        if constexpr (!PRE) cp_async_wait_all();   // no copy into the staging area outlives the loop
         if (ok && __all_sync(0xffffffffu, !abort_flag.get())) {
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -598,7 +636,7 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
             s8x4_half_0213(__ldg(qw + 2 * g), o0[0], o0[1]);
             s8x4_half_0213(__ldg(qw + 2 * g + 1), o1[0], o1[1]);
         }
-        *reinterpret_cast<uint4*>(bt + tc::tile_off(t, 8 * g, KH)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
+        *reinterpret_cast<uint4*>(bt + tc::tile_off_sw128(t, 8 * g, BN)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
     }
     if (h == 0) {
         reinterpret_cast<float*>(img + 2 * B_BYTES + BMIN_BYTES)[t] =
@@ -651,19 +689,20 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (SMEM_BYTES > dev.smem_optin) return cudaErrorInvalidConfiguration;
     const int pre = workspace != nullptr;
+    const int smem_bytes = pre ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
+    if (smem_bytes > dev.smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = raise_smem_limit(
-        reinterpret_cast<const void*>(pre ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>), SMEM_BYTES);
+        reinterpret_cast<const void*>(pre ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>), smem_bytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
     if (pre) {
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
                           dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg));
         if (e != cudaSuccess) return e;
-        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
+        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(THREADS), smem_bytes, s, map, p);
     }
-    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(THREADS), SMEM_BYTES, s, map, p);
+    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(THREADS), smem_bytes, s, map, p);
 }
 
 }  // namespace cq

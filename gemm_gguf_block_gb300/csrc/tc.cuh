@@ -33,6 +33,16 @@ __host__ __device__ constexpr int tile_off(int r, int k, int kt) {
     return (r >> 3) * (kt * 16) + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
 }
 
+// Byte offset of element (r, k) in a K-major operand tile with the 128-byte
+// swizzle, rows of kt fp16 elements (kt a multiple of 64) for nr rows: the
+// tile is kt / 64 column blocks of nr 128-byte rows (64 elements each), block
+// b at b * nr * 128; inside a block the 16-byte chunk c of row r sits at
+// chunk position c ^ (r % 8) (the smem_desc_sw128 below, sbo = 1024, on a
+// 1024-byte aligned base).
+__host__ __device__ constexpr int tile_off_sw128(int r, int k, int nr) {
+    return (k >> 6) * (nr * 128) + r * 128 + ((((k >> 3) & 7) ^ (r & 7)) << 4) + (k & 7) * 2;
+}
+
 // Four signed bytes -> two half2 holding the same integers, in byte order
 // (bytes 0, 1 | bytes 2, 3): the sign bits flipped (b + 128 as an unsigned
 // byte), each byte placed under a 0x64 high byte (binary16 1024 + (b + 128),
@@ -98,6 +108,18 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
            | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16)
            | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32)
            | (1ull << 46);                            // descriptor version for the sm_100 family
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, K-major: 8-row x
+// 128-byte atoms (1024-byte aligned), sbo = byte distance between atoms along
+// the rows; the leading offset is unused (one MMA's K never leaves a row).
+// A K step of 16 fp16 elements inside the atom adds 32 bytes to the start.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu)
+           | (1ull << 16)                             // leading offset: 16 bytes, ignored
+           | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32)
+           | (1ull << 46)                             // descriptor version for the sm_100 family
+           | (2ull << 61);                            // 128-byte swizzle
 }
 
 // ----------------------------------------------------------- TMEM ld / st
