@@ -56,13 +56,14 @@ namespace {
 
 constexpr int BM = 128;          // weight rows per tile (MMA M, TMEM lanes)
 constexpr int BN = 128;          // tokens per tile (MMA N)
-constexpr int KH = 128;          // K per operand stage (half a superblock)
-constexpr int NSTAGE = 2;        // operand stages
+constexpr int KH = 128;          // K per thread of the workspace prep kernel (half a superblock)
+constexpr int KQ = 64;           // K per operand stage (a quarter superblock: one 64-element Q4_K group)
+constexpr int NSTAGE = 4;        // operand stages
 constexpr int NMIN = 2;          // min slots (A_C, A_I, B_min of one superblock)
 constexpr int NDX = 4;           // scale slots (the tokens' d_x and the rows' d, dmin of one superblock)
 constexpr int RAW_BYTES = BM * 144;
-constexpr int A_BYTES = BM * KH * 2;        // 32 KB
-constexpr int B_BYTES = BN * KH * 2;        // 32 KB
+constexpr int A_BYTES = BM * KQ * 2;        // 16 KB
+constexpr int B_BYTES = BN * KQ * 2;        // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int AC_BYTES = BM * 16 * 2;       // 4 KB
 constexpr int AI_BYTES = BM * 16 * 2;       // 4 KB
@@ -84,7 +85,7 @@ constexpr int XS_BYTES = BN * 256;          // the next superblock's Q8_K quants
 // Shared-memory layout (offsets from the 1024-aligned dynamic base). Without
 // a workspace the raw weight ring is one stage shorter, which makes room for
 // the activation staging area XS.
-constexpr int OFF_BAR = 0;                   // 27 barriers
+constexpr int OFF_BAR = 0;                   // 31 barriers
 constexpr int OFF_TMEM = 256;                // tensor-memory base address
 constexpr int OFF_FLAG = 264;                // abort flag
 constexpr int OFF_RAW = 1024;
@@ -100,9 +101,10 @@ struct Layout {
 static_assert(Layout<true>::OFF_STAGE % 1024 == 0 && Layout<false>::OFF_STAGE % 1024 == 0, "B tile alignment");
 
 enum {
-    B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 8, B_MIN_FULL = 10, B_MIN_EMPTY = 12,
-    B_ACC_FULL = 14, B_X_EMPTY = 16, B_CI_EMPTY = 18, B_DX_FULL = 19, B_DX_EMPTY = 23
+    B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 10, B_MIN_FULL = 14, B_MIN_EMPTY = 16,
+    B_ACC_FULL = 18, B_X_EMPTY = 20, B_CI_EMPTY = 22, B_DX_FULL = 23, B_DX_EMPTY = 27, N_BARS = 31
 };
+static_assert(N_BARS * 8 <= OFF_TMEM, "barriers overlap the tensor-memory address");
 
 struct GemmParams {
     const uint8_t* W;
@@ -116,9 +118,9 @@ struct GemmParams {
 };
 
 // One (token tile, superblock) image of the pre-converted activations, laid
-// out as the B parts of the two operand stages (K-half 0, K-half 1), then the
+// out as the B parts of the four operand stages (quarters 0..3), then the
 // B_min operand (the end of a min slot) and the tokens' d_x (a d_x slot).
-constexpr int IMG_BYTES = 2 * B_BYTES + BMIN_BYTES + DX_BYTES;   // 70144
+constexpr int IMG_BYTES = 4 * B_BYTES + BMIN_BYTES + DX_BYTES;   // 70144
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     } else if (warp == 2) {
         // ------------------------------------------ activation-operand copies
         // Per superblock, in the order they are used: B_min into the min slot,
-        // the B operands of the two K halves, then d_x into its slot.
+        // the B operands of the four K quarters, then d_x into its slot.
         if (PRE && lane == 0) {
             const uint64_t pol = policy_evict_first();
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
@@ -268,24 +270,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 const int ms = s % NMIN;
                 if (!tc::wait_or_abort_sleep(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_MIN_FULL + ms], BMIN_BYTES);
-                bulk_g2s(smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES, img + 2 * B_BYTES, BMIN_BYTES,
+                bulk_g2s(smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES, img + 4 * B_BYTES, BMIN_BYTES,
                          &bars[B_MIN_FULL + ms], pol);
                 bool ok = true;
-                for (int h = 0; h < 2; ++h) {
-                    const int q = 2 * s + h, st = q % NSTAGE;
+                for (int g = 0; g < 4; ++g) {
+                    const int q = 4 * s + g, st = q % NSTAGE;
                     if (!tc::wait_or_abort_sleep(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES);
-                    bulk_g2s(smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES, img + h * B_BYTES, B_BYTES,
+                    bulk_g2s(smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES, img + g * B_BYTES, B_BYTES,
                              &bars[B_OP_FULL + st], pol);
                 }
                 if (!ok) break;
                 const int ds = s % NDX;
                 if (!tc::wait_or_abort_sleep(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
                 mbar_arrive_expect_tx(&bars[B_DX_FULL + ds], DX_BYTES);
-                bulk_g2s(smem + OFF_DX + ds * SCL_BYTES, img + 2 * B_BYTES + BMIN_BYTES, DX_BYTES,
+                bulk_g2s(smem + OFF_DX + ds * SCL_BYTES, img + 4 * B_BYTES + BMIN_BYTES, DX_BYTES,
                          &bars[B_DX_FULL + ds], pol);
             }
         }
@@ -295,9 +297,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             constexpr uint32_t idesc = tc::idesc_f16_f32(BM, BN);
             // Descriptors of stage 0 and min slot 0; others differ only in the
             // start-address field (bytes / 16), which no offset here overflows.
-            // A tiles: no swizzle; B tiles: 128-byte swizzle (two 64-element
-            // column blocks of BN rows).
-            const uint64_t op_desc0 = tc::smem_desc(smem_u32(smem + OFF_STAGE), 128, KH * 16);
+            // A tiles: no swizzle; B tiles: 128-byte swizzle (one 64-element
+            // column block of BN rows).
+            const uint64_t op_desc0 = tc::smem_desc(smem_u32(smem + OFF_STAGE), 128, KQ * 16);
             const uint64_t b_desc0 = tc::smem_desc_sw128(smem_u32(smem + OFF_STAGE + A_BYTES), 1024);
             const uint64_t min_desc0 = tc::smem_desc(smem_u32(smem + OFF_MIN), 128, 256);
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
@@ -310,8 +312,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 const uint64_t bmd = acd + ((AC_BYTES + AI_BYTES) >> 4);
                 tc::mma_f16(xcol, acd, bmd, idesc, 0);                  // X = -C
                 bool ok = true;
-                for (int h = 0; h < 2; ++h) {
-                    const int q = 2 * s + h, st = q % NSTAGE;
+                for (int g = 0; g < 4; ++g) {
+                    const int q = 4 * s + g, st = q % NSTAGE;
                     if (!tc::wait_or_abort_sleep(&bars[B_OP_FULL + st], (q / NSTAGE) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
@@ -320,8 +322,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     const uint64_t ad = op_desc0 + static_cast<uint32_t>((st * STAGE_BYTES) >> 4);
                     const uint64_t bd = b_desc0 + static_cast<uint32_t>((st * STAGE_BYTES) >> 4);
 #pragma unroll
-                    for (int t = 0; t < KH / 16; ++t)
-                        tc::mma_f16(xcol, ad + 16 * t, bd + (t >> 2) * (BN * 128 / 16) + 2 * (t & 3), idesc, 1);
+                    for (int t = 0; t < KQ / 16; ++t) tc::mma_f16(xcol, ad + 16 * t, bd + 2 * t, idesc, 1);
                     tc::commit(&bars[B_OP_EMPTY + st]);
                 }
                 if (!ok) break;
@@ -335,38 +336,36 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         }
     } else if (warp < EPI_WARP0) {
         // --------------------------------------------------------- converters
-        // Weights: thread (row r = tid % 128, part = tid / 128) converts one
-        // 64-element group of each half superblock (groups part and 2 + part)
-        // from the raw stage in shared memory; both groups' words are read at
-        // the first half. A quarter warp covers 8 consecutive rows, so its
-        // 16-byte loads (row pitch 144 bytes) and its stores into the A tile
-        // (row pitch 16 bytes within a core matrix) hit 8 distinct bank
-        // groups. Part 0 also writes the row's A_C entries, part 1 its A_I
-        // entries.
+        // Weights: thread (row r = tid % 128, part = tid / 128) converts, in
+        // each quarter stage (64-element group g of the superblock), bytes
+        // 16 part .. 16 part + 15 of the group's 32 quant bytes: elements
+        // 16 part .. +15 of sub-block 2g (low nibbles) and of sub-block 2g + 1
+        // (high nibbles). All four groups' words are read, and the raw stage
+        // released, when the superblock starts. A quarter warp covers 8
+        // consecutive rows, so its 16-byte loads (row pitch 144 bytes) and its
+        // stores into the A tile (row pitch 16 bytes within a core matrix) hit
+        // 8 distinct bank groups. Part 0 also writes the row's A_C entries,
+        // part 1 its A_I entries.
         const int tid = threadIdx.x - 32 * CONV_WARP0;  // 0..255
-        const int r = tid & (BM - 1), part = tid >> 7;  // weight row r, group part
-        const int a_row = (r >> 3) * (KH * 16) + (r & 7) * 16 + part * 1024;   // A tile row base (+ k offsets)
+        const int r = tid & (BM - 1), part = tid >> 7;  // weight row r, byte half part
+        const int a_row = (r >> 3) * (KQ * 16) + (r & 7) * 16 + part * 256;   // A tile row base (+ k offsets)
         uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales and mins, one per byte
-        uint32_t qw[16];                                // the thread's quant words of both halves
-        for (int q = 0; q < 2 * ns; ++q) {
-            const int s = q >> 1, h = q & 1, st = q % NSTAGE, rs = s % NRAW;
+        uint32_t qw[16];                                // the thread's quant words, 4 per group
+        for (int s = 0; s < ns; ++s) {
+            const int rs = s % NRAW;
             if (__any_sync(0xffffffffu, abort_flag.get())) break;
-            if (h == 0) {
-                if (!warp_wait(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+            if (!warp_wait(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) break;
+            {
                 const uint8_t* raw = smem + OFF_RAW + rs * RAW_BYTES + r * 144;
                 const uint4 hdr = *reinterpret_cast<const uint4*>(raw);
                 q4k_scales(hdr.y, hdr.z, hdr.w, scw, mnw);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 + 32 * (2 * hh + part) + 16 * i);
-                        qw[8 * hh + 4 * i] = v.x; qw[8 * hh + 4 * i + 1] = v.y;
-                        qw[8 * hh + 4 * i + 2] = v.z; qw[8 * hh + 4 * i + 3] = v.w;
-                    }
+                for (int g = 0; g < 4; ++g) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g + 16 * part);
+                    qw[4 * g] = v.x; qw[4 * g + 1] = v.y; qw[4 * g + 2] = v.z; qw[4 * g + 3] = v.w;
+                }
                 // The superblock's min slot: A_C row r = [-8 sc_0 .. -8 sc_7] twice (part 0),
-                // A_I row r = [m_0 .. m_7] twice (part 1); without a workspace also
-                // B_min and d_x of the tile's tokens.
+                // A_I row r = [m_0 .. m_7] twice (part 1).
                 const int ms = s % NMIN;
                 if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) break;
                 uint8_t* slot = smem + OFF_MIN + ms * MIN_BYTES;
@@ -390,35 +389,44 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
                     uint8_t* scl = smem + OFF_DX + ds * SCL_BYTES;
                     reinterpret_cast<uint32_t*>(scl + DX_BYTES)[r] = hdr.x;
-                    warp_arrive(&bars[B_DX_FULL + ds], lane);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&bars[B_DX_FULL + ds]);
                 }
+                // every read of the raw stage is done (the arrive orders them before the refill)
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
             }
-            if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) break;
-            uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
-            // A: weight row r, group g = 2h + part: 32 low nibbles (sub-block 2g) and
-            // 32 high nibbles (sub-block 2g + 1), as sc * q
-            {
-                // sub-blocks 2g and 2g + 1 = bytes 2 part and 2 part + 1 of scw[h]
+            bool ok = true;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int q = 4 * s + g, st = q % NSTAGE;
+                if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                // A: weight row r, elements 16 part .. +15 of sub-blocks 2g (low nibbles, k = 16 part + ..)
+                // and 2g + 1 (high nibbles, k = 32 + 16 part + ..), as sc * q; their scales are bytes
+                // 2(g % 2) and 2(g % 2) + 1 of scw[g / 2]
                 const __half2 k1024 = bits_h2(0x64006400u), km1024 = bits_h2(0xE400E400u);
-                const uint32_t sel_lo = part ? 0x4242u : 0x4040u, sel_hi = part ? 0x4343u : 0x4141u;
-                const uint32_t sw = h ? scw[1] : scw[0];
-                const __half2 slo = __hsub2(bytes_1024(sw, sel_lo), k1024);
-                const __half2 shi16 = __hmul2(__hsub2(bytes_1024(sw, sel_hi), k1024), bits_h2(0x2C002C00u));   // sc / 16
+                const uint32_t sw = scw[g >> 1];
+                const __half2 slo = __hsub2(bytes_1024(sw, (g & 1) ? 0x4242u : 0x4040u), k1024);
+                const __half2 shi16 =
+                    __hmul2(__hsub2(bytes_1024(sw, (g & 1) ? 0x4343u : 0x4141u), k1024), bits_h2(0x2C002C00u));   // sc / 16
                 const __half2 blo = __hmul2(slo, km1024);
                 const __half2 bhi = __hmul2(shi16, km1024);                                                    // -64 sc
-                uint8_t* arow = stg + a_row;
+                uint8_t* arow = smem + OFF_STAGE + st * STAGE_BYTES + a_row;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {        // 8 elements (2 words) per core-matrix row
+                for (int c = 0; c < 2; ++c) {        // 8 elements (2 words) per core-matrix row
                     uint32_t l0[2], h0[2], l1[2], h1[2];
-                    nibbles_to_half(h ? qw[8 + 2 * c] : qw[2 * c], slo, blo, shi16, bhi, l0, h0);
-                    nibbles_to_half(h ? qw[8 + 2 * c + 1] : qw[2 * c + 1], slo, blo, shi16, bhi, l1, h1);
+                    nibbles_to_half(qw[4 * g + 2 * c], slo, blo, shi16, bhi, l0, h0);
+                    nibbles_to_half(qw[4 * g + 2 * c + 1], slo, blo, shi16, bhi, l1, h1);
                     *reinterpret_cast<uint4*>(arow + c * 128) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
-                    *reinterpret_cast<uint4*>(arow + (4 + c) * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
+                    *reinterpret_cast<uint4*>(arow + 512 + c * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
                 }
+                fence_proxy_async_smem();
+                warp_arrive(&bars[B_OP_FULL + st], lane);
             }
-            fence_proxy_async_smem();
-            warp_arrive(&bars[B_OP_FULL + st], lane);
-            if (h == 1 && lane == 0) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+            if (!ok) break;
         }
     } else {
         // ----------------------------------------------------------- epilogue
@@ -430,28 +438,30 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // quarter warp) and its rows' (d, dmin) from the scale slot.
         //
         // Without a workspace these warps also write the activation operands
-        // of the next superblock: warp ew converts tokens 8ew..8ew+7 of both
-        // K halves, lane w holding quant word w of each (in the swizzled B
-        // tile a store instruction fills two whole 128-byte rows), thread etid
-        // the B_min entries 2(etid%4), +1 of token etid/4, and the first four
-        // warps the tokens' d_x. The quant words travel one superblock ahead
-        // by asynchronous copies into the staging area XS (each thread reads
-        // back only what it copied; a copy instruction covers 128 contiguous
-        // bytes of one token), the bsums and d_x in registers.
+        // of the next superblock: thread etid the B_min entries 2(etid%4), +1
+        // of token etid/4, the first four warps the tokens' d_x, then per
+        // quarter stage warp ew converts tokens 8ew..8ew+7, lane l quant word
+        // l%16 of the quarter of tokens 8ew + 2i + l/16 (in the swizzled B tile
+        // a store instruction fills two whole 128-byte rows). The quant words
+        // travel one superblock ahead by asynchronous copies into the staging
+        // area XS (each thread reads back only what it copied; a copy
+        // instruction covers 64 contiguous bytes of each of two tokens), the
+        // bsums and d_x in registers.
         const int quarter = warp & 3;
         const int ew = warp - EPI_WARP0, etid = threadIdx.x - 32 * EPI_WARP0;
-        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + 8 * ew * 64 + lane;   // [token][64 words]
+        const int hi = lane >> 4, wq = lane & 15;
+        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + (8 * ew + hi) * 64 + wq;   // [token][64 words]
         uint32_t bsw[2] = {0u, 0u};
         float dxw = 0.0f;
         auto fetch_b = [&](int s) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int tok = m0 + 8 * ew + i;
+            for (int i = 0; i < 4; ++i) {
+                const int tok = m0 + 8 * ew + 2 * i + hi;
                 const uint32_t n = tok < p.M ? 4u : 0u;
                 const uint32_t* row = reinterpret_cast<const uint32_t*>(
-                    p.xq + static_cast<int64_t>(tok < p.M ? tok : 0) * p.xrow + 292 * s + 4) + lane;
-                cp_async4(xs + 64 * i, row, n);
-                cp_async4(xs + 64 * i + 32, row + 32, n);
+                    p.xq + static_cast<int64_t>(tok < p.M ? tok : 0) * p.xrow + 292 * s + 4) + wq;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) cp_async4(xs + 128 * i + 16 * g, row + 16 * g, n);
             }
             cp_async_commit();
             const int btok = m0 + (etid >> 2);
@@ -466,23 +476,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         };
         auto put_b = [&](int s) -> bool {
             cp_async_wait_all();
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int q = 2 * s + h, st = q % NSTAGE;
-                if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) return false;
-                // word w = lane of token 8ew + i: elements 4w..4w+3, at tile_off_sw128(8ew + i, 4w)
-                uint8_t* bt = smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES + (lane >> 4) * (BN * 128) +
-                              ew * 1024 + (lane & 1) * 8;
-                const int c16 = (lane & 15) >> 1 << 4;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    uint32_t o0, o1;
-                    s8x4_half_0213(xs[64 * i + 32 * h], o0, o1);
-                    *reinterpret_cast<uint2*>(bt + 128 * i + (c16 ^ (i << 4))) = make_uint2(o0, o1);
-                }
-                fence_proxy_async_smem();
-                warp_arrive(&bars[B_OP_FULL + st], lane);
-            }
             const int ms = s % NMIN;
             if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) return false;
             __half* bh = reinterpret_cast<__half*>(smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES +
@@ -497,6 +490,31 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) return false;
                 reinterpret_cast<float*>(smem + OFF_DX + ds * SCL_BYTES)[etid] = dxw;
                 warp_arrive(&bars[B_DX_FULL + ds], lane);
+            }
+            // word wq of token t = 8ew + 2i + hi: elements 4wq..4wq+3 of the quarter, at
+            // tile_off_sw128(t, 4wq) = 128 t + 16 ((wq / 2) ^ (t % 8)) + 8 (wq % 2)
+            const int cx = (((wq >> 1) ^ hi) << 4) + (wq & 1) * 8;
+            // two quarters per fence and arrival pair
+#pragma unroll
+            for (int g2 = 0; g2 < 4; g2 += 2) {
+#pragma unroll
+                for (int g = g2; g < g2 + 2; ++g) {
+                    const int q = 4 * s + g, st = q % NSTAGE;
+                    if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) return false;
+                    uint8_t* bt = smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES + (8 * ew + hi) * 128;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t o0, o1;
+                        s8x4_half_0213(xs[128 * i + 16 * g], o0, o1);
+                        *reinterpret_cast<uint2*>(bt + 256 * i + (cx ^ (i << 5))) = make_uint2(o0, o1);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&bars[B_OP_FULL + (4 * s + g2) % NSTAGE]);
+                    tc::mbar_arrive(&bars[B_OP_FULL + (4 * s + g2 + 1) % NSTAGE]);
+                }
             }
             return true;
         };
@@ -628,7 +646,7 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
     const uint8_t* blk = p.xq + static_cast<int64_t>(m) * p.xrow + 292 * s;
     uint8_t* img = bimg + (static_cast<int64_t>(tile) * ns + s) * IMG_BYTES;
     const uint32_t* qw = reinterpret_cast<const uint32_t*>(blk + 4 + 128 * h);
-    uint8_t* bt = img + h * (BN * KH * 2);
+    uint8_t* bt = img + 2 * h * B_BYTES;    // quarters 2h and 2h + 1
 #pragma unroll 4
     for (int g = 0; g < KH / 8; ++g) {       // 8 elements (one core-matrix row) per store
         uint32_t o0[2] = {0u, 0u}, o1[2] = {0u, 0u};
@@ -639,11 +657,11 @@ __global__ void __launch_bounds__(256) gemm_prep_kernel(const GemmParams p, uint
         *reinterpret_cast<uint4*>(bt + tc::tile_off_sw128(t, 8 * g, BN)) = make_uint4(o0[0], o0[1], o1[0], o1[1]);
     }
     if (h == 0) {
-        reinterpret_cast<float*>(img + 2 * B_BYTES + BMIN_BYTES)[t] =
+        reinterpret_cast<float*>(img + 4 * B_BYTES + BMIN_BYTES)[t] =
             on ? __ldg(reinterpret_cast<const float*>(blk)) : 0.0f;
     } else {
         // B_min: token t = [64 h_0 .. 64 h_7, l_0 .. l_7], B_j = 64 h_j + l_j
-        __half* bh = reinterpret_cast<__half*>(img + 2 * B_BYTES + tc::tile_off(t, 0, 16));
+        __half* bh = reinterpret_cast<__half*>(img + 4 * B_BYTES + tc::tile_off(t, 0, 16));
 #pragma unroll
         for (int j = 0; j < 8; ++j)
             bmin_entry(on ? __ldg(reinterpret_cast<const uint32_t*>(blk + 260) + j) : 0u, bh[j], bh[64 + j]);
