@@ -32,17 +32,23 @@
 // epilogue drains superblock s; only its two small -C / I MMAs wait for the
 // epilogue to have read the previous ones.
 //
-// Warp roles (864 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
+// Operands move through four stages of a quarter superblock each (K = 64,
+// one 64-element Q4_K group): 16 KB of A (weights) and 16 KB of B
+// (activations), so the MMA warp keeps up to three quarters queued while a
+// stage is refilled.
+//
+// Warp roles (896 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
 // map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory
 // and one lane issues the MMAs; warp 2, with a workspace, bulk-copies the
-// pre-converted activation operands (a warp of its own, so that the raw
-// weight boxes run ahead of the operand stages); warps 3-10 convert raw
-// weights into fp16 A tiles (K-major, no swizzle) and fill the min slot's
-// A_C and A_I; warps 11-26 are the epilogue (tensor-memory lanes
-// 32*(warp%4), 32 token columns each, y in registers) and, without a
-// workspace, also convert the Q8_K activations into the B tiles (K-major,
-// 128-byte swizzle), B_min and d_x. Every wait is bounded; a timeout flags
-// CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
+// pre-converted B operands (a warp of its own, so that the raw weight boxes
+// run ahead of the operand stages); warp 3 writes each superblock's min slot
+// (A_C, A_I; with a workspace also B_min by bulk copy) and scale slot (the
+// rows' d, dmin; with a workspace also d_x); warps 4-11 convert raw weights
+// into fp16 A tiles (K-major, no swizzle); warps 12-27 are the epilogue
+// (tensor-memory lanes 32*(warp%4), 32 token columns each, y in registers)
+// and, without a workspace, also convert the Q8_K activations into the B
+// tiles (K-major, 128-byte swizzle), B_min and d_x. Every wait is bounded;
+// a timeout flags CQ_DEV_WAIT_TIMEOUT and the CTA winds down.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -75,7 +81,8 @@ constexpr int NCONV = 256;                  // converter threads
 constexpr int CONV_WARPS = NCONV / 32;
 constexpr int EPI_WARPS = 16;
 constexpr int COLS = BN / (EPI_WARPS / 4);  // 32 token columns per epilogue thread
-constexpr int CONV_WARP0 = 3;               // first converter warp
+constexpr int SLOT_WARP = 3;                // writer of the min and scale slots
+constexpr int CONV_WARP0 = 4;               // first converter warp
 constexpr int EPI_WARP0 = CONV_WARP0 + 8;   // first epilogue warp
 constexpr int THREADS = (EPI_WARP0 + EPI_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;         // X0 | X1 | C | I, 128 columns each
@@ -218,18 +225,18 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(&bars[B_RAW_FULL + i], 1);
-            mbar_init(&bars[B_RAW_EMPTY + i], CONV_WARPS);
+            mbar_init(&bars[B_RAW_EMPTY + i], CONV_WARPS + 1);              // + the slot writer
         }
         for (int i = 0; i < NSTAGE; ++i) {
             mbar_init(&bars[B_OP_FULL + i], CONV_WARPS + (PRE ? 1 : EPI_WARPS));   // + the activation copy or converters
             mbar_init(&bars[B_OP_EMPTY + i], 1);
         }
         for (int i = 0; i < NMIN; ++i) {
-            mbar_init(&bars[B_MIN_FULL + i], CONV_WARPS + (PRE ? 1 : EPI_WARPS));
+            mbar_init(&bars[B_MIN_FULL + i], PRE ? 1 : 1 + EPI_WARPS);      // the slot writer (+ B_min writers)
             mbar_init(&bars[B_MIN_EMPTY + i], 1);                      // the MMA commit
         }
         for (int i = 0; i < NDX; ++i) {
-            mbar_init(&bars[B_DX_FULL + i], BM / 32 + (PRE ? 1 : BN / 32));   // the row-scale warps + the d_x writers
+            mbar_init(&bars[B_DX_FULL + i], PRE ? 1 : 1 + BN / 32);         // the slot writer (+ d_x writers)
             mbar_init(&bars[B_DX_EMPTY + i], EPI_WARPS);
         }
         for (int i = 0; i < 2; ++i) {
@@ -259,36 +266,91 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 tc::tma_load_2d(smem + OFF_RAW + r * RAW_BYTES, &wmap, 144 * s, n0, &bars[B_RAW_FULL + r]);
             }
         }
+    } else if (warp == SLOT_WARP) {
+        // ----------------------------------------------- min and scale slots
+        // Per superblock s, lane l takes weight rows l + 32i of the raw stage:
+        // their A_C rows [-8 sc_0 .. -8 sc_7] twice and A_I rows [m_0 .. m_7]
+        // twice (the min slot), and their (d, dmin) words (the scale slot).
+        // With a workspace, lane 0 also bulk-copies B_min and d_x into the
+        // same slots.
+        const uint64_t pol = policy_evict_first();
+        auto slots = [&](int s) -> bool {
+            const int rs = s % NRAW, ms = s % NMIN, ds = s % NDX;
+            const uint8_t* img = PRE ? p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES : nullptr;
+            if (!warp_wait(&bars[B_RAW_FULL + rs], (s / NRAW) & 1, abort_flag, p.status)) return false;
+            uint4 hdr[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                hdr[i] = *reinterpret_cast<const uint4*>(smem + OFF_RAW + rs * RAW_BYTES + (lane + 32 * i) * 144);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&bars[B_RAW_EMPTY + rs]);
+            if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) return false;
+            uint8_t* slot = smem + OFF_MIN + ms * MIN_BYTES;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = lane + 32 * i;
+                uint32_t sc[2], mn[2];
+                q4k_scales(hdr[i].y, hdr[i].z, hdr[i].w, sc, mn);
+                // -8 sc = (1024 + sc) * -8 + 8192 and m = (1024 + m) - 1024, both exact
+                uint32_t cw[4], iw[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t sel = (j & 1) ? 0x4342u : 0x4140u;
+                    cw[j] = h2_bits(__hfma2(bytes_1024(sc[j >> 1], sel), bits_h2(0xC800C800u), bits_h2(0x70007000u)));
+                    iw[j] = h2_bits(__hsub2(bytes_1024(mn[j >> 1], sel), bits_h2(0x64006400u)));
+                }
+                const uint4 cv = make_uint4(cw[0], cw[1], cw[2], cw[3]), iv = make_uint4(iw[0], iw[1], iw[2], iw[3]);
+                *reinterpret_cast<uint4*>(slot + tc::tile_off(r, 0, 16)) = cv;
+                *reinterpret_cast<uint4*>(slot + tc::tile_off(r, 8, 16)) = cv;
+                *reinterpret_cast<uint4*>(slot + AC_BYTES + tc::tile_off(r, 0, 16)) = iv;
+                *reinterpret_cast<uint4*>(slot + AC_BYTES + tc::tile_off(r, 8, 16)) = iv;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (PRE) {
+                    mbar_arrive_expect_tx(&bars[B_MIN_FULL + ms], BMIN_BYTES);
+                    bulk_g2s(slot + AC_BYTES + AI_BYTES, img + 4 * B_BYTES, BMIN_BYTES, &bars[B_MIN_FULL + ms], pol);
+                } else {
+                    tc::mbar_arrive(&bars[B_MIN_FULL + ms]);
+                }
+            }
+            if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) return false;
+            uint8_t* scl = smem + OFF_DX + ds * SCL_BYTES;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) reinterpret_cast<uint32_t*>(scl + DX_BYTES)[lane + 32 * i] = hdr[i].x;
+            __syncwarp();
+            if (lane == 0) {
+                if (PRE) {
+                    mbar_arrive_expect_tx(&bars[B_DX_FULL + ds], DX_BYTES);
+                    bulk_g2s(scl, img + 4 * B_BYTES + BMIN_BYTES, DX_BYTES, &bars[B_DX_FULL + ds], pol);
+                } else {
+                    tc::mbar_arrive(&bars[B_DX_FULL + ds]);
+                }
+            }
+            return true;
+        };
+        for (int s = 0; s < ns; ++s)
+            if (!slots(s)) break;
     } else if (warp == 2) {
-        // ------------------------------------------ activation-operand copies
-        // Per superblock, in the order they are used: B_min into the min slot,
-        // the B operands of the four K quarters, then d_x into its slot.
+        // ---------------------------------------------- activation operands
+        // With a workspace: the B operands of the four K quarters of each
+        // superblock, bulk-copied into the stages as they free up.
         if (PRE && lane == 0) {
             const uint64_t pol = policy_evict_first();
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 const uint8_t* img = p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES;
-                const int ms = s % NMIN;
-                if (!tc::wait_or_abort_sleep(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&bars[B_MIN_FULL + ms], BMIN_BYTES);
-                bulk_g2s(smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES, img + 4 * B_BYTES, BMIN_BYTES,
-                         &bars[B_MIN_FULL + ms], pol);
-                bool ok = true;
-                for (int g = 0; g < 4; ++g) {
+                bool got = true;
+                for (int g = 0; g < 4 && got; ++g) {
                     const int q = 4 * s + g, st = q % NSTAGE;
-                    if (!tc::wait_or_abort_sleep(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) {
-                        ok = false;
-                        break;
+                    got = tc::wait_or_abort_sleep(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status);
+                    if (got) {
+                        mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES);
+                        bulk_g2s(smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES, img + g * B_BYTES, B_BYTES,
+                                 &bars[B_OP_FULL + st], pol);
                     }
-                    mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES);
-                    bulk_g2s(smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES, img + g * B_BYTES, B_BYTES,
-                             &bars[B_OP_FULL + st], pol);
                 }
-                if (!ok) break;
-                const int ds = s % NDX;
-                if (!tc::wait_or_abort_sleep(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
-                mbar_arrive_expect_tx(&bars[B_DX_FULL + ds], DX_BYTES);
-                bulk_g2s(smem + OFF_DX + ds * SCL_BYTES, img + 4 * B_BYTES + BMIN_BYTES, DX_BYTES,
-                         &bars[B_DX_FULL + ds], pol);
+                if (!got) break;
             }
         }
     } else if (warp == 1) {
@@ -344,12 +406,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // released, when the superblock starts. A quarter warp covers 8
         // consecutive rows, so its 16-byte loads (row pitch 144 bytes) and its
         // stores into the A tile (row pitch 16 bytes within a core matrix) hit
-        // 8 distinct bank groups. Part 0 also writes the row's A_C entries,
-        // part 1 its A_I entries.
+        // 8 distinct bank groups.
         const int tid = threadIdx.x - 32 * CONV_WARP0;  // 0..255
         const int r = tid & (BM - 1), part = tid >> 7;  // weight row r, byte half part
         const int a_row = (r >> 3) * (KQ * 16) + (r & 7) * 16 + part * 256;   // A tile row base (+ k offsets)
-        uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales and mins, one per byte
+        uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales (and mins, unused here), one per byte
         uint32_t qw[16];                                // the thread's quant words, 4 per group
         for (int s = 0; s < ns; ++s) {
             const int rs = s % NRAW;
@@ -363,34 +424,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 for (int g = 0; g < 4; ++g) {
                     const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g + 16 * part);
                     qw[4 * g] = v.x; qw[4 * g + 1] = v.y; qw[4 * g + 2] = v.z; qw[4 * g + 3] = v.w;
-                }
-                // The superblock's min slot: A_C row r = [-8 sc_0 .. -8 sc_7] twice (part 0),
-                // A_I row r = [m_0 .. m_7] twice (part 1).
-                const int ms = s % NMIN;
-                if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) break;
-                uint8_t* slot = smem + OFF_MIN + ms * MIN_BYTES;
-                // -8 sc = (1024 + sc) * -8 + 8192 and m = (1024 + m) - 1024, both exact
-                uint32_t mw[4];
-                const uint32_t src[2] = {part == 0 ? scw[0] : mnw[0], part == 0 ? scw[1] : mnw[1]};
-                const __half2 mul = bits_h2(part == 0 ? 0xC800C800u : 0x3C003C00u);   // -8 or 1
-                const __half2 add = bits_h2(part == 0 ? 0x70007000u : 0xE400E400u);   // 8192 or -1024
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    mw[i] = h2_bits(__hfma2(bytes_1024(src[i >> 1], (i & 1) ? 0x4342u : 0x4140u), mul, add));
-                const uint4 mv = make_uint4(mw[0], mw[1], mw[2], mw[3]);
-                uint8_t* atile = slot + part * AC_BYTES;
-                *reinterpret_cast<uint4*>(atile + tc::tile_off(r, 0, 16)) = mv;
-                *reinterpret_cast<uint4*>(atile + tc::tile_off(r, 8, 16)) = mv;
-                fence_proxy_async_smem();
-                warp_arrive(&bars[B_MIN_FULL + ms], lane);
-                if (tid < BM) {
-                    // the scale slot: row r's (d, dmin) word
-                    const int ds = s % NDX;
-                    if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) break;
-                    uint8_t* scl = smem + OFF_DX + ds * SCL_BYTES;
-                    reinterpret_cast<uint32_t*>(scl + DX_BYTES)[r] = hdr.x;
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&bars[B_DX_FULL + ds]);
                 }
                 // every read of the raw stage is done (the arrive orders them before the refill)
                 __syncwarp();
