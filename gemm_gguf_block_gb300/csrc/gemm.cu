@@ -202,10 +202,10 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 }
 
 // PRE: the activations come pre-converted (cq_gemm_ws): warp 2 bulk-copies
-// each stage's B operand and each min slot's B_min and d_x. Without it the
-// epilogue warps convert the Q8_K activations of superblock s+1 (between
-// draining superblocks s-1 and s). Either way the converters handle only
-// weights.
+// each stage's B operand, warp 3 each min slot's B_min and each scale slot's
+// d_x. Without it the epilogue warps convert the Q8_K activations of
+// superblock s+1 (between draining superblocks s-1 and s). Either way the
+// converters handle only weights.
 template <bool PRE>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
