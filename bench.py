@@ -531,17 +531,42 @@ def case_q4_0_small(c, cq, synth, peaks, seed):
         b.record(s)
         b.synchronize()
         lat.append(a.elapsed_time(b))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        cs = torch.cuda.current_stream().cuda_stream
-        for i in range(copies):
-            one(i, cs)
-    g.replay()
-    torch.cuda.synchronize()
-    ms = time_calls(torch, g.replay, max(3, c.iters), 2)
-    return {"device_us_one_call": 1e3 * statistics.median(lat), "rotated_gbs": copies * W.nbytes / ms / 1e6,
-            "rotated_us_per_call": 1e3 * ms / copies,
-            "rotation": f"{copies} copies ({copies * W.nbytes / 2**20:.0f} MiB > L2) in one CUDA graph"}
+    def graph_us(call):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream().cuda_stream
+            for i in range(copies):
+                call(i, cs)
+        g.replay()
+        torch.cuda.synchronize()
+        us = 1e3 * time_calls(torch, g.replay, max(3, c.iters), 2) / copies
+        del g
+        return us
+
+    us_rot = graph_us(one)
+    # The launch floor: the same kernel and launch path with almost no work
+    # (8 weight rows), back to back in a graph and as one cold call; and the
+    # full call with its weights resident in L2 (no rotation).
+    tiny = lambda i=0, sh=None: cq.cq_gemv(cq.Q4_0, 1, 8, K, Wd[i].data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                           sh if sh is not None else c.stream())
+    us_floor = graph_us(tiny)
+    us_l2 = graph_us(lambda i, sh: one(0, sh))
+    lat_tiny = []
+    for _ in range(5 * c.iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)
+        a.record(s)
+        tiny()
+        b.record(s)
+        b.synchronize()
+        lat_tiny.append(a.elapsed_time(b))
+    return {"device_us_one_call": 1e3 * statistics.median(lat), "rotated_gbs": W.nbytes / us_rot / 1e3,
+            "rotated_us_per_call": us_rot,
+            "rotation": f"{copies} copies ({copies * W.nbytes / 2**20:.0f} MiB > L2) in one CUDA graph",
+            "launch_floor": {"graph_us_per_launch_8_rows": us_floor, "device_us_one_call_8_rows":
+                             1e3 * statistics.median(lat_tiny), "graph_us_per_call_l2_resident": us_l2,
+                             "note": "same kernel with 8 of 2048 rows: launch, prologue and one pass of the "
+                                     "pipeline with no streaming"}}
 
 
 CASES = {"prefill_gemm_q4_k": case_gemm, "prefill_gemm_32": case_gemm_32, "moe_q4_0": case_moe, "lm_head_q4_1": case_lm_head,
