@@ -92,9 +92,9 @@ constexpr int XS_BYTES = BN * 256;          // the next superblock's Q8_K quants
 // Shared-memory layout (offsets from the 1024-aligned dynamic base). Without
 // a workspace the raw weight ring is one stage shorter, which makes room for
 // the activation staging area XS.
-constexpr int OFF_BAR = 0;                   // 31 barriers
-constexpr int OFF_TMEM = 256;                // tensor-memory base address
-constexpr int OFF_FLAG = 264;                // abort flag
+constexpr int OFF_BAR = 0;                   // 35 barriers
+constexpr int OFF_TMEM = 512;                // tensor-memory base address
+constexpr int OFF_FLAG = 520;                // abort flag
 constexpr int OFF_RAW = 1024;
 template <bool PRE>
 struct Layout {
@@ -109,7 +109,7 @@ static_assert(Layout<true>::OFF_STAGE % 1024 == 0 && Layout<false>::OFF_STAGE % 
 
 enum {
     B_RAW_FULL = 0, B_RAW_EMPTY = 3, B_OP_FULL = 6, B_OP_EMPTY = 10, B_MIN_FULL = 14, B_MIN_EMPTY = 16,
-    B_ACC_FULL = 18, B_X_EMPTY = 20, B_CI_EMPTY = 22, B_DX_FULL = 23, B_DX_EMPTY = 27, N_BARS = 31
+    B_ACC_FULL = 18, B_X_EMPTY = 20, B_CI_EMPTY = 22, B_DX_FULL = 23, B_DX_EMPTY = 27, B_SLICE = 31, N_BARS = 35
 };
 static_assert(N_BARS * 8 <= OFF_TMEM, "barriers overlap the tensor-memory address");
 
@@ -206,10 +206,18 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 // d_x. Without it the epilogue warps convert the Q8_K activations of
 // superblock s+1 (between draining superblocks s-1 and s). Either way the
 // converters handle only weights.
-template <bool PRE>
+//
+// CS: CTAs per cluster along the token tiles (1 or 2). With 2, the pair
+// shares the weight conversion: each CTA converts rows RPC*rank .. +RPC-1 of
+// every A quarter into its own stage, and warp 2 bulk-copies that slice into
+// the peer's stage (completing on the peer's operand barrier). The MMAs of
+// both CTAs release a stage together (multicast commits, two arrivals).
+template <bool PRE, int CS>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
     using L = Layout<PRE>;
+    constexpr int RPC = BM / CS;                    // weight rows this CTA converts
+    constexpr int SLICE_BYTES = RPC * KQ * 2;       // their part of an A quarter (contiguous 8-row groups)
     constexpr int NRAW = L::NRAW, OFF_STAGE = L::OFF_STAGE, OFF_MIN = L::OFF_MIN, OFF_DX = L::OFF_DX;
     pdl_trigger();
     pdl_wait();
@@ -228,8 +236,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             mbar_init(&bars[B_RAW_EMPTY + i], CONV_WARPS + 1);              // + the slot writer
         }
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], CONV_WARPS + (PRE ? 1 : EPI_WARPS));   // + the activation copy or converters
-            mbar_init(&bars[B_OP_EMPTY + i], 1);
+            mbar_init(&bars[B_OP_FULL + i], 1 + (PRE ? 0 : EPI_WARPS));   // warp 2 (+ the activation converters)
+            mbar_init(&bars[B_OP_EMPTY + i], CS);                         // the MMA commits of the cluster's CTAs
+            mbar_init(&bars[B_SLICE + i], CONV_WARPS);                    // this CTA's weight slice converted
         }
         for (int i = 0; i < NMIN; ++i) {
             mbar_init(&bars[B_MIN_FULL + i], PRE ? 1 : 1 + EPI_WARPS);      // the slot writer (+ B_min writers)
@@ -253,6 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     }
     tc::fence_before();
     __syncthreads();
+    if constexpr (CS > 1) tc::cluster_sync();   // the peer's barriers exist before anything reaches them
     tc::fence_after();
     const uint32_t tmem = *tmem_holder;
 
@@ -333,24 +343,39 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         for (int s = 0; s < ns; ++s)
             if (!slots(s)) break;
     } else if (warp == 2) {
-        // ---------------------------------------------- activation operands
-        // With a workspace: the B operands of the four K quarters of each
-        // superblock, bulk-copied into the stages as they free up.
-        if (PRE && lane == 0) {
+        // ------------------------------------------------ operand copies
+        // Per quarter, once the stage is free in every CTA of the cluster:
+        // with a workspace, the pre-converted B operand (bulk copy); with a
+        // cluster, this CTA's converted weight slice into the peer's stage.
+        // Its arrival on the stage's barrier certifies the local slice and
+        // expects the peer's.
+        if (lane == 0) {
             const uint64_t pol = policy_evict_first();
+            const uint32_t peer = CS > 1 ? (tc::cluster_rank() ^ 1u) : 0u;
+            const uint32_t slice_off = CS > 1 ? (peer ^ 1u) * SLICE_BYTES : 0u;
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
-                const uint8_t* img = p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES;
+                const uint8_t* img = PRE ? p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES : nullptr;
                 bool got = true;
                 for (int g = 0; g < 4 && got; ++g) {
                     const int q = 4 * s + g, st = q % NSTAGE;
+                    uint64_t* full = &bars[B_OP_FULL + st];
+                    uint8_t* stg = smem + OFF_STAGE + st * STAGE_BYTES;
                     got = tc::wait_or_abort_sleep(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status);
-                    if (got) {
-                        mbar_arrive_expect_tx(&bars[B_OP_FULL + st], B_BYTES);
-                        bulk_g2s(smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES, img + g * B_BYTES, B_BYTES,
-                                 &bars[B_OP_FULL + st], pol);
+                    if (!got) break;
+                    if (PRE) {
+                        tc::mbar_expect_tx(full, B_BYTES);
+                        bulk_g2s(stg + A_BYTES, img + g * B_BYTES, B_BYTES, full, pol);
+                    }
+                    got = tc::wait_or_abort_sleep(&bars[B_SLICE + st], (q / NSTAGE) & 1, abort_flag, p.status);
+                    if (!got) break;
+                    if constexpr (CS > 1) {
+                        tc::bulk_s2peer(tc::cluster_addr(smem_u32(stg + slice_off), peer), stg + slice_off, SLICE_BYTES,
+                                        tc::cluster_addr(smem_u32(full), peer));
+                        mbar_arrive_expect_tx(full, SLICE_BYTES);
+                    } else {
+                        tc::mbar_arrive(full);
                     }
                 }
-                if (!got) break;
             }
         }
     } else if (warp == 1) {
@@ -385,7 +410,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     const uint64_t bd = b_desc0 + static_cast<uint32_t>((st * STAGE_BYTES) >> 4);
 #pragma unroll
                     for (int t = 0; t < KQ / 16; ++t) tc::mma_f16(xcol, ad + 16 * t, bd + 2 * t, idesc, 1);
-                    tc::commit(&bars[B_OP_EMPTY + st]);
+                    if constexpr (CS > 1)
+                        tc::commit_multicast(&bars[B_OP_EMPTY + st], static_cast<uint16_t>((1u << CS) - 1u));
+                    else
+                        tc::commit(&bars[B_OP_EMPTY + st]);
                 }
                 if (!ok) break;
                 if (!tc::wait_or_abort_sleep(&bars[B_CI_EMPTY], (s & 1) ^ 1, abort_flag, p.status)) break;
@@ -398,20 +426,22 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         }
     } else if (warp < EPI_WARP0) {
         // --------------------------------------------------------- converters
-        // Weights: thread (row r = tid % 128, part = tid / 128) converts, in
-        // each quarter stage (64-element group g of the superblock), bytes
-        // 16 part .. 16 part + 15 of the group's 32 quant bytes: elements
-        // 16 part .. +15 of sub-block 2g (low nibbles) and of sub-block 2g + 1
-        // (high nibbles). All four groups' words are read, and the raw stage
-        // released, when the superblock starts. A quarter warp covers 8
-        // consecutive rows, so its 16-byte loads (row pitch 144 bytes) and its
+        // Weights: this CTA's RPC rows. Thread (row r = RPC*rank + tid % RPC,
+        // part = tid / RPC) converts, in each quarter stage (64-element group
+        // g of the superblock), bytes PB*part .. +PB-1 of the group's 32 quant
+        // bytes: those elements of sub-block 2g (low nibbles) and of sub-block
+        // 2g + 1 (high nibbles). All four groups' words are read, and the raw
+        // stage released, when the superblock starts. A quarter warp covers 8
+        // consecutive rows, so its loads (row pitch 144 bytes) and its 16-byte
         // stores into the A tile (row pitch 16 bytes within a core matrix) hit
         // 8 distinct bank groups.
+        constexpr int NPART = NCONV / RPC, PB = 32 / NPART, WPG = PB / 4;   // parts, bytes and words per part
         const int tid = threadIdx.x - 32 * CONV_WARP0;  // 0..255
-        const int r = tid & (BM - 1), part = tid >> 7;  // weight row r, byte half part
-        const int a_row = (r >> 3) * (KQ * 16) + (r & 7) * 16 + part * 256;   // A tile row base (+ k offsets)
+        const int part = tid / RPC;
+        const int r = RPC * static_cast<int>(CS > 1 ? tc::cluster_rank() : 0u) + tid % RPC;
+        const int a_row = (r >> 3) * (KQ * 16) + (r & 7) * 16 + part * (WPG / 2) * 128;   // A tile row base
         uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales (and mins, unused here), one per byte
-        uint32_t qw[16];                                // the thread's quant words, 4 per group
+        uint32_t qw[4 * WPG];                           // the thread's quant words, WPG per group
         for (int s = 0; s < ns; ++s) {
             const int rs = s % NRAW;
             if (__any_sync(0xffffffffu, abort_flag.get())) break;
@@ -422,8 +452,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 q4k_scales(hdr.y, hdr.z, hdr.w, scw, mnw);
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g + 16 * part);
-                    qw[4 * g] = v.x; qw[4 * g + 1] = v.y; qw[4 * g + 2] = v.z; qw[4 * g + 3] = v.w;
+                    if constexpr (WPG == 4) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(raw + 16 + 32 * g + 16 * part);
+                        qw[4 * g] = v.x; qw[4 * g + 1] = v.y; qw[4 * g + 2] = v.z; qw[4 * g + 3] = v.w;
+                    } else {
+                        const uint2 v = *reinterpret_cast<const uint2*>(raw + 16 + 32 * g + 8 * part);
+                        qw[2 * g] = v.x; qw[2 * g + 1] = v.y;
+                    }
                 }
                 // every read of the raw stage is done (the arrive orders them before the refill)
                 __syncwarp();
@@ -437,8 +472,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     ok = false;
                     break;
                 }
-                // A: weight row r, elements 16 part .. +15 of sub-blocks 2g (low nibbles, k = 16 part + ..)
-                // and 2g + 1 (high nibbles, k = 32 + 16 part + ..), as sc * q; their scales are bytes
+                // A: weight row r, elements PB part .. of sub-blocks 2g (low nibbles, k = PB part + ..)
+                // and 2g + 1 (high nibbles, k = 32 + PB part + ..), as sc * q; their scales are bytes
                 // 2(g % 2) and 2(g % 2) + 1 of scw[g / 2]
                 const __half2 k1024 = bits_h2(0x64006400u), km1024 = bits_h2(0xE400E400u);
                 const uint32_t sw = scw[g >> 1];
@@ -449,15 +484,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 const __half2 bhi = __hmul2(shi16, km1024);                                                    // -64 sc
                 uint8_t* arow = smem + OFF_STAGE + st * STAGE_BYTES + a_row;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {        // 8 elements (2 words) per core-matrix row
+                for (int c = 0; c < WPG / 2; ++c) {  // 8 elements (2 words) per core-matrix row
                     uint32_t l0[2], h0[2], l1[2], h1[2];
-                    nibbles_to_half(qw[4 * g + 2 * c], slo, blo, shi16, bhi, l0, h0);
-                    nibbles_to_half(qw[4 * g + 2 * c + 1], slo, blo, shi16, bhi, l1, h1);
+                    nibbles_to_half(qw[WPG * g + 2 * c], slo, blo, shi16, bhi, l0, h0);
+                    nibbles_to_half(qw[WPG * g + 2 * c + 1], slo, blo, shi16, bhi, l1, h1);
                     *reinterpret_cast<uint4*>(arow + c * 128) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
                     *reinterpret_cast<uint4*>(arow + 512 + c * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
                 }
-                fence_proxy_async_smem();
-                warp_arrive(&bars[B_OP_FULL + st], lane);
+                fence_proxy_async_smem();   // for the local MMAs and warp 2's copy to the peer
+                warp_arrive(&bars[B_SLICE + st], lane);
             }
             if (!ok) break;
         }
@@ -659,8 +694,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     if (abort_flag.get() && threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) (void)mbar_wait_bounded(&bars[B_RAW_FULL + i], 0, WAIT_LIMIT_NS / 8);
         for (int i = 0; i < 2; ++i) (void)mbar_wait_bounded(&bars[B_ACC_FULL + i], 0, WAIT_LIMIT_NS / 8);
+        if (CS > 1) {   // let a copy the peer issued before it gave up land in this CTA's shared memory
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 50000u) __nanosleep(1000);
+        }
     }
     __syncthreads();
+    // The peer may still copy into, or arrive on, this CTA's shared memory
+    // until it is done: neither leaves before both are.
+    if constexpr (CS > 1) tc::cluster_sync();
     tc::fence_after();
     if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
@@ -741,19 +783,27 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int pre = workspace != nullptr;
+    // Token tiles in pairs (a two-CTA cluster sharing the weight conversion)
+    // when their number is even.
+    const int cs = tiles_m % 2 == 0 ? 2 : 1;
     const int smem_bytes = pre ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
     if (smem_bytes > dev.smem_optin) return cudaErrorInvalidConfiguration;
-    cudaError_t e = raise_smem_limit(
-        reinterpret_cast<const void*>(pre ? gemm_q4k_kernel<true> : gemm_q4k_kernel<false>), smem_bytes);
+    const void* kern = pre ? (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<true, 2>)
+                                      : reinterpret_cast<const void*>(gemm_q4k_kernel<true, 1>))
+                           : (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<false, 2>)
+                                      : reinterpret_cast<const void*>(gemm_q4k_kernel<false, 1>));
+    cudaError_t e = raise_smem_limit(kern, smem_bytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
     if (pre) {
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
                           dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg));
         if (e != cudaSuccess) return e;
-        return launch_kernel(gemm_q4k_kernel<true>, grid, dim3(THREADS), smem_bytes, s, map, p);
+        if (cs == 2) return launch_kernel_cluster_y(gemm_q4k_kernel<true, 2>, grid, dim3(THREADS), smem_bytes, s, 2u, map, p);
+        return launch_kernel(gemm_q4k_kernel<true, 1>, grid, dim3(THREADS), smem_bytes, s, map, p);
     }
-    return launch_kernel(gemm_q4k_kernel<false>, grid, dim3(THREADS), smem_bytes, s, map, p);
+    if (cs == 2) return launch_kernel_cluster_y(gemm_q4k_kernel<false, 2>, grid, dim3(THREADS), smem_bytes, s, 2u, map, p);
+    return launch_kernel(gemm_q4k_kernel<false, 1>, grid, dim3(THREADS), smem_bytes, s, map, p);
 }
 
 }  // namespace cq

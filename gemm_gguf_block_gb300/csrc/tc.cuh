@@ -74,6 +74,40 @@ __device__ __forceinline__ bool wait_or_abort_sleep(uint64_t* bar, uint32_t pari
     return false;
 }
 
+// ---------------------------------------------------------------- cluster
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `local` (a shared::cta address) in the CTA
+// of rank `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(local), "r"(rank));
+    return a;
+}
+// Every thread of every CTA of the cluster: arrive (release) and wait
+// (acquire). Orders barrier initialisation before peers' remote operations,
+// and keeps a CTA's shared memory alive until its peers are done with it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory to a peer's (dst and its barrier as
+// shared::cluster addresses), completing `bytes` transactions on that barrier.
+__device__ __forceinline__ void bulk_s2peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t peer_bar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "r"(smem_u32(src)), "r"(bytes), "r"(peer_bar)
+                 : "memory");
+}
+// Raise the expected transaction count of the barrier's current phase
+// without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------- MMA
 // D[tmem] (+)= A[smem] * B[smem]^T, fp16 operands, fp32 accumulator.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -88,6 +122,13 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 // Arrive once on `bar` when every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+// The same, arriving on the barrier at this offset in every CTA of the
+// cluster whose rank bit is set in `mask`.
+__device__ __forceinline__ void commit_multicast(uint64_t* bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 ::"r"(smem_u32(bar)), "h"(mask)
                  : "memory");
 }
 
