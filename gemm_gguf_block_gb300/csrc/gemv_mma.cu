@@ -8,9 +8,11 @@
 //
 // Per 32-element block the integer dot is an exact fp16 tensor-core product,
 // mma.sync m16n8k16 twice per block. The weight operand holds BIAS + v for a
-// quant of value v, built from the packed bytes by one lop3 per pair, and
-// the accumulator starts at -BIAS * sum(x): every operand and partial sum is
-// an integer below 2^23, so the result is the exact integer dot. The block's
+// quant of value v (4-bit high nibbles: 1024 + 16 v against activations
+// scaled by 1/16), built from the packed bytes by one lop3 per pair, and the
+// accumulator starts at minus the matching multiple of the activation sums:
+// every operand and partial sum is an integer below 2^23, so the result is
+// the exact integer dot (mma_frag.cuh). The block's
 // scale terms are then applied on the CUDA cores, two tokens per f32x2
 // instruction, in the library's fixed order (include/cq.h):
 // c = fma(d_w * d_x, isum, c) [+ fma(m_w, s_x, c) for Q4_1] over four
@@ -99,8 +101,8 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
     }
     // Stage the activations once. Per (token m, block b): the 32 quants as
     // fp16 in four 16-byte chunks, chunk t = elements [4t, 4t+2, 4t+1, 4t+3,
-    // 16+4t, 18+4t, 17+4t, 19+4t] (lane t's B fragments of both k-steps);
-    // per (block b, token pair j): {d_x, d_x', -BIAS*sum(q), -BIAS*sum(q')}
+    // 16+4t, 18+4t, 17+4t, 19+4t] (lane t's B fragments of both k-steps, see
+    // mf::act_frags); per (block b, token pair j): {d_x, d_x', bias, bias'}
     // and, for Q8_1, {s_x, s_x'}. Tokens >= M are zero.
     {
         float* sc = reinterpret_cast<float*>(smem + p.smem_scale);
@@ -109,15 +111,15 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
             const int m = i / p.nb, b = i - m * p.nb;
             uint4 ch[4] = {};
             float d = 0.0f, sx = 0.0f;
-            int sum = 0;
-            if (m < p.M) mf::act_frags<WF>(p.xq + (static_cast<int64_t>(m) * p.nb + b) * F::ABB, ch, d, sx, sum);
+            int bias = 0;
+            if (m < p.M) mf::act_frags<WF>(p.xq + (static_cast<int64_t>(m) * p.nb + b) * F::ABB, ch, d, sx, bias);
             uint4* dst = reinterpret_cast<uint4*>(smem + p.smem_act + m * p.act_pitch + 64 * b);
 #pragma unroll
             for (int t = 0; t < 4; ++t) dst[t] = ch[t];
             const int j = m >> 1, hi = m & 1;
             float* e = sc + (b * NPAIR + j) * 4;
             e[hi] = d;
-            e[2 + hi] = static_cast<float>(-F::BIAS * sum);
+            e[2 + hi] = static_cast<float>(bias);
             if constexpr (WF == CQ_Q4_1) sc[p.nb * NPAIR * 4 + (b * NPAIR + j) * 2 + hi] = sx;
         }
     }

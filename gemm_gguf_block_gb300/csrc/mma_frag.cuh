@@ -6,7 +6,11 @@
 // from the packed bytes by one lop3 per pair; every activation quant enters B
 // as its exact fp16 value; the accumulator starts at -BIAS * sum(x). All
 // operands and partial sums are integers below 2^23, so the two chained
-// k-steps of a block give the exact integer dot.
+// k-steps of a block give the exact integer dot. For the 4-bit formats the
+// high nibbles (k-step 1) are masked in place: A = 1024 + 16 n, with the
+// k-step's activations pre-scaled by 1/16 (exact in fp16), so that
+// A * B = 64 x + n x and the accumulator starts at
+// -(BIAS_LO * sum(x_lo) + BIAS_HI * sum(x_hi)) instead.
 //
 // The k order inside a 32-block: k-step 0 takes elements 0..15, k-step 1
 // elements 16..31; within a k-step, fragment column 2t holds element 4t,
@@ -28,9 +32,17 @@ namespace mf {
 // BB / QO: weight block bytes and offset of its quants; ABB / AQO: the same
 // for the paired activation block; BIAS: the A operand holds BIAS + v.
 template <int WF> struct MF;
-template <> struct MF<CQ_Q4_0> { static constexpr int BB = 18, QO = 2, ABB = 34, AQO = 2, BIAS = 1032; };
-template <> struct MF<CQ_Q4_1> { static constexpr int BB = 20, QO = 4, ABB = 36, AQO = 4, BIAS = 1024; };
-template <> struct MF<CQ_Q8_0> { static constexpr int BB = 34, QO = 2, ABB = 34, AQO = 2, BIAS = 1152; };
+// BIAS_LO / BIAS_HI: the accumulator's start per unit of the activation sums of
+// k-step 0 (elements 0..15) and k-step 1 (16..31).
+template <> struct MF<CQ_Q4_0> {
+    static constexpr int BB = 18, QO = 2, ABB = 34, AQO = 2, BIAS = 1032, BIAS_LO = 1032, BIAS_HI = 72;
+};
+template <> struct MF<CQ_Q4_1> {
+    static constexpr int BB = 20, QO = 4, ABB = 36, AQO = 4, BIAS = 1024, BIAS_LO = 1024, BIAS_HI = 64;
+};
+template <> struct MF<CQ_Q8_0> {
+    static constexpr int BB = 34, QO = 2, ABB = 34, AQO = 2, BIAS = 1152, BIAS_LO = 1152, BIAS_HI = 1152;
+};
 
 // Bytes per weight row in a stage of 8 blocks, padded for Q4_1 (160 -> 176
 // bytes: 44 words, so the 8 rows one load instruction touches fall in 8
@@ -82,12 +94,14 @@ __device__ __forceinline__ void a_frags(uint32_t q0a, uint32_t q1a, uint32_t q0b
         a1[0] = s8pair_1152(q0b);        a1[1] = s8pair_1152(q1b);
         a1[2] = s8pair_1152(q0b >> 8);   a1[3] = s8pair_1152(q1b >> 8);
     } else {
-        // q?a: bytes 4t..4t+3; low nibbles = elements 4t.., high = 16+4t..
-        constexpr uint32_t SEL = 0x000F000Fu, SET = 0x64006400u;
-        a0[0] = and_or(q0a, SEL, SET);         a0[1] = and_or(q1a, SEL, SET);
-        a0[2] = and_or(q0a >> 8, SEL, SET);    a0[3] = and_or(q1a >> 8, SEL, SET);
-        a1[0] = and_or(q0a >> 4, SEL, SET);    a1[1] = and_or(q1a >> 4, SEL, SET);
-        a1[2] = and_or(q0a >> 12, SEL, SET);   a1[3] = and_or(q1a >> 12, SEL, SET);
+        // q?a: bytes 4t..4t+3; low nibbles = elements 4t.. (1024 + n), high
+        // nibbles = elements 16+4t.. masked in place (1024 + 16 n)
+        constexpr uint32_t LO = 0x000F000Fu, HI = 0x00F000F0u, SET = 0x64006400u;
+        const uint32_t s0 = q0a >> 8, s1 = q1a >> 8;
+        a0[0] = and_or(q0a, LO, SET);    a0[1] = and_or(q1a, LO, SET);
+        a0[2] = and_or(s0, LO, SET);     a0[3] = and_or(s1, LO, SET);
+        a1[0] = and_or(q0a, HI, SET);    a1[1] = and_or(q1a, HI, SET);
+        a1[2] = and_or(s0, HI, SET);     a1[3] = and_or(s1, HI, SET);
         (void)q0b;
         (void)q1b;
     }
@@ -139,19 +153,25 @@ __device__ __forceinline__ void weight_frags(const uint8_t* w0, const uint8_t* w
 
 // One activation block (Q8_0 or Q8_1 at blk) as the B operand: four 16-byte
 // chunks, chunk t = fp16 of elements [4t, 4t+2, 4t+1, 4t+3, 16+4t, 18+4t,
-// 17+4t, 19+4t] (lane t's B fragments of both k-steps); its d, its s (Q8_1)
-// and the sum of its quants.
+// 17+4t, 19+4t] (lane t's B fragments of both k-steps; for the 4-bit weight
+// formats the k-step 1 half scaled by 1/16); its d, its s (Q8_1) and the
+// accumulator's start -(BIAS_LO * sum(q_0..15) + BIAS_HI * sum(q_16..31)).
 template <int WF>
-__device__ __forceinline__ void act_frags(const uint8_t* blk, uint4 (&ch)[4], float& d, float& s, int& sum) {
+__device__ __forceinline__ void act_frags(const uint8_t* blk, uint4 (&ch)[4], float& d, float& s, int& bias) {
     using F = MF<WF>;
     const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
     uint32_t w[8];
-    sum = 0;
+    int sum_lo = 0, sum_hi = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         w[j] = __byte_perm(h[F::AQO / 2 + 2 * j], h[F::AQO / 2 + 2 * j + 1], 0x5410);
-        sum = __dp4a(static_cast<int>(w[j]), 0x01010101, sum);
+        if (j < 4) sum_lo = __dp4a(static_cast<int>(w[j]), 0x01010101, sum_lo);
+        else sum_hi = __dp4a(static_cast<int>(w[j]), 0x01010101, sum_hi);
     }
+    bias = -(F::BIAS_LO * sum_lo + F::BIAS_HI * sum_hi);
+    constexpr bool HI16 = WF != CQ_Q8_0;
+    const __half2 k16 = __halves2half2(__ushort_as_half(HI16 ? 0x2C00 : 0x3C00),
+                                       __ushort_as_half(HI16 ? 0x2C00 : 0x3C00));   // 1/16 or 1
     d = h2f(h[0]);
     s = WF == CQ_Q4_1 ? h2f(h[1]) : 0.0f;
     // exact fp16 of the signed bytes: (1152 + b) - 1152
@@ -160,8 +180,8 @@ __device__ __forceinline__ void act_frags(const uint8_t* blk, uint4 (&ch)[4], fl
     for (int t = 0; t < 4; ++t) {
         const uint32_t e02 = h2u(__hsub2(u2h(s8pair_1152(w[t])), k1152));
         const uint32_t e13 = h2u(__hsub2(u2h(s8pair_1152(w[t] >> 8)), k1152));
-        const uint32_t f02 = h2u(__hsub2(u2h(s8pair_1152(w[t + 4])), k1152));
-        const uint32_t f13 = h2u(__hsub2(u2h(s8pair_1152(w[t + 4] >> 8)), k1152));
+        const uint32_t f02 = h2u(__hmul2(__hsub2(u2h(s8pair_1152(w[t + 4])), k1152), k16));
+        const uint32_t f13 = h2u(__hmul2(__hsub2(u2h(s8pair_1152(w[t + 4] >> 8)), k1152), k16));
         ch[t] = make_uint4(e02, e13, f02, f13);
     }
 }
