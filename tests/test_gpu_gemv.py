@@ -91,11 +91,13 @@ def test_gemv_exact_arithmetic(orc, wfmt, N, K, M):
 
 @pytest.mark.parametrize("wfmt", FMTS)
 @pytest.mark.parametrize("M,N,K", [(1, 33, 256), (17, 100, 512), (64, 257, 2048), (65, 129, 768),
-                                   (130, 96, 4096), (200, 300, 1024)])
+                                   (130, 96, 4096), (200, 300, 1024), (300, 200, 512), (700, 130, 256)])
 def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
     """cq_gemm (tcgen05 kernels for Q4_K and for the 32-element formats) against
     the oracle, and each row against the single-token cq_gemv bit for bit;
-    M and N ragged against the 64-token / 128-row tiles."""
+    M and N ragged against the 64-token / 128-row tiles. For Q4_K the token
+    tile counts 1, 2, 3 and 6 cover single CTAs (odd counts) and CTA pairs
+    sharing the weight conversion (even counts, one and three pairs)."""
     torch = torch_cuda()
     cq = cq_built()
     W, xq = _case(orc, wfmt, N, K, M, seed=wfmt * 31 + M + N + K)
