@@ -208,17 +208,25 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 // superblock s+1 (between draining superblocks s-1 and s). Either way the
 // converters handle only weights.
 //
-// CS: CTAs per cluster along the token tiles (1 or 2). With 2, the pair
-// shares the weight conversion: each CTA converts rows RPC*rank .. +RPC-1 of
-// every A quarter into its own stage, and warp 2 bulk-copies that slice into
-// the peer's stage (completing on the peer's operand barrier). The MMAs of
-// both CTAs release a stage together (multicast commits, two arrivals).
+// CS: CTAs per cluster (1 or 2). A pair shares one conversion, and warp 2
+// bulk-copies each CTA's converted slice of a stage into the peer's stage
+// (completing on the peer's operand barrier); the MMAs of both CTAs release a
+// stage together (multicast commits, two arrivals).
+//   with a workspace (SHARE_A): the pair holds token tiles 2i, 2i+1 of the
+//     same 128 weight rows; each CTA converts weight rows 64*rank .. +63 of
+//     every A quarter;
+//   without one (SHARE_B): the pair holds weight tiles 2j, 2j+1 of the same
+//     128 tokens; each CTA's epilogue warps convert tokens 64*rank .. +63 of
+//     every B quarter.
 template <bool PRE, int CS>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
     using L = Layout<PRE>;
-    constexpr int RPC = BM / CS;                    // weight rows this CTA converts
-    constexpr int SLICE_BYTES = RPC * KQ * 2;       // their part of an A quarter (contiguous 8-row groups)
+    constexpr bool SHARE_A = CS > 1 && PRE, SHARE_B = CS > 1 && !PRE;
+    constexpr int RPC = SHARE_A ? BM / CS : BM;     // weight rows this CTA converts
+    constexpr int TPC = SHARE_B ? BN / CS : BN;     // tokens whose B quarters this CTA converts
+    // the slice of a stage copied to the peer: contiguous 8-row groups of the A tile, or 128-byte token rows of B
+    constexpr int SLICE_BYTES = SHARE_A ? RPC * KQ * 2 : TPC * 128;
     constexpr int NRAW = L::NRAW, OFF_STAGE = L::OFF_STAGE, OFF_MIN = L::OFF_MIN, OFF_DX = L::OFF_DX;
     pdl_trigger();
     pdl_wait();
@@ -237,9 +245,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
             mbar_init(&bars[B_RAW_EMPTY + i], CONV_WARPS + 1);              // + the slot writer
         }
         for (int i = 0; i < NSTAGE; ++i) {
-            mbar_init(&bars[B_OP_FULL + i], 1 + (PRE ? 0 : EPI_WARPS));   // warp 2 (+ the activation converters)
+            // warp 2, plus the converters of whatever operand is not copied through it
+            mbar_init(&bars[B_OP_FULL + i], 1 + (SHARE_B ? CONV_WARPS : (PRE ? 0 : EPI_WARPS)));
             mbar_init(&bars[B_OP_EMPTY + i], CS);                         // the MMA commits of the cluster's CTAs
-            mbar_init(&bars[B_SLICE + i], CONV_WARPS);                    // this CTA's weight slice converted
+            mbar_init(&bars[B_SLICE + i], SHARE_B ? EPI_WARPS : CONV_WARPS);   // this CTA's slice converted
         }
         for (int i = 0; i < NMIN; ++i) {
             mbar_init(&bars[B_MIN_FULL + i], PRE ? 1 : 1 + EPI_WARPS);      // the slot writer (+ B_min writers)
@@ -347,13 +356,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // ------------------------------------------------ operand copies
         // Per quarter, once the stage is free in every CTA of the cluster:
         // with a workspace, the pre-converted B operand (bulk copy); with a
-        // cluster, this CTA's converted weight slice into the peer's stage.
-        // Its arrival on the stage's barrier certifies the local slice and
-        // expects the peer's.
+        // cluster, this CTA's converted slice (of A, or of B) into the peer's
+        // stage. Its arrival on the stage's barrier certifies the local slice
+        // and expects the peer's.
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             const uint32_t peer = CS > 1 ? (tc::cluster_rank() ^ 1u) : 0u;
-            const uint32_t slice_off = CS > 1 ? (peer ^ 1u) * SLICE_BYTES : 0u;
+            const uint32_t slice_off = CS > 1 ? (SHARE_B ? A_BYTES : 0u) + (peer ^ 1u) * SLICE_BYTES : 0u;
             for (int s = 0; s < ns && !abort_flag.get(); ++s) {
                 const uint8_t* img = PRE ? p.bimg + (static_cast<int64_t>(blockIdx.y) * ns + s) * IMG_BYTES : nullptr;
                 bool got = true;
@@ -439,7 +448,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         constexpr int NPART = NCONV / RPC, PB = 32 / NPART, WPG = PB / 4;   // parts, bytes and words per part
         const int tid = threadIdx.x - 32 * CONV_WARP0;  // 0..255
         const int part = tid / RPC;
-        const int r = RPC * static_cast<int>(CS > 1 ? tc::cluster_rank() : 0u) + tid % RPC;
+        const int r = RPC * static_cast<int>(SHARE_A ? tc::cluster_rank() : 0u) + tid % RPC;
         const int a_row = (r >> 3) * (KQ * 16) + (r & 7) * 16 + part * (WPG / 2) * 128;   // A tile row base
         uint32_t scw[2] = {0u, 0u}, mnw[2] = {0u, 0u};  // the row's scales (and mins, unused here), one per byte
         uint32_t qw[4 * WPG];                           // the thread's quant words, WPG per group
@@ -492,8 +501,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                     *reinterpret_cast<uint4*>(arow + c * 128) = make_uint4(l0[0], l0[1], l1[0], l1[1]);
                     *reinterpret_cast<uint4*>(arow + 512 + c * 128) = make_uint4(h0[0], h0[1], h1[0], h1[1]);
                 }
-                fence_proxy_async_smem();   // for the local MMAs and warp 2's copy to the peer
-                warp_arrive(&bars[B_SLICE + st], lane);
+                fence_proxy_async_smem();   // for the local MMAs (and warp 2's copy to the peer)
+                warp_arrive(&bars[(SHARE_B ? B_OP_FULL : B_SLICE) + st], lane);
             }
             if (!ok) break;
         }
@@ -509,23 +518,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // Without a workspace these warps also write the activation operands
         // of the next superblock: thread etid the B_min entries 2(etid%4), +1
         // of token etid/4, the first four warps the tokens' d_x, then per
-        // quarter stage warp ew converts tokens 8ew..8ew+7, lane l quant word
-        // l%16 of the quarter of tokens 8ew + 2i + l/16 (in the swizzled B tile
-        // a store instruction fills two whole 128-byte rows). The quant words
-        // travel one superblock ahead by asynchronous copies into the staging
-        // area XS (each thread reads back only what it copied; a copy
-        // instruction covers 64 contiguous bytes of each of two tokens), the
-        // bsums and d_x in registers.
+        // quarter stage warp ew converts TPW tokens, tb + TPW*ew + 2i + l/16
+        // for lane l (quant word l%16 of the quarter; in the swizzled B tile a
+        // store instruction fills two whole 128-byte rows) -- all 128 tokens,
+        // or this CTA's half of them in a pair. The quant words travel one
+        // superblock ahead by asynchronous copies into the staging area XS
+        // (each thread reads back only what it copied; a copy instruction
+        // covers 64 contiguous bytes of each of two tokens), the bsums and d_x
+        // in registers.
+        constexpr int TPW = TPC / EPI_WARPS, NI = TPW / 2;   // tokens per warp, token pairs per warp
         const int quarter = warp & 3;
         const int ew = warp - EPI_WARP0, etid = threadIdx.x - 32 * EPI_WARP0;
         const int hi = lane >> 4, wq = lane & 15;
-        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + (8 * ew + hi) * 64 + wq;   // [token][64 words]
+        const int tb = TPC * static_cast<int>(SHARE_B ? tc::cluster_rank() : 0u) + TPW * ew + hi;   // token of pair 0
+        uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + tb * 64 + wq;   // [token][64 words]
         uint32_t bsw[2] = {0u, 0u};
         float dxw = 0.0f;
         auto fetch_b = [&](int s) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int tok = m0 + 8 * ew + 2 * i + hi;
+            for (int i = 0; i < NI; ++i) {
+                const int tok = m0 + tb + 2 * i;
                 const uint32_t n = tok < p.M ? 4u : 0u;
                 const uint32_t* row = reinterpret_cast<const uint32_t*>(
                     p.xq + static_cast<int64_t>(tok < p.M ? tok : 0) * p.xrow + 292 * s + 4) + wq;
@@ -560,9 +572,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 reinterpret_cast<float*>(smem + OFF_DX + ds * SCL_BYTES)[etid] = dxw;
                 warp_arrive(&bars[B_DX_FULL + ds], lane);
             }
-            // word wq of token t = 8ew + 2i + hi: elements 4wq..4wq+3 of the quarter, at
-            // tile_off_sw128(t, 4wq) = 128 t + 16 ((wq / 2) ^ (t % 8)) + 8 (wq % 2)
-            const int cx = (((wq >> 1) ^ hi) << 4) + (wq & 1) * 8;
+            // word wq of token t = tb + 2i: elements 4wq..4wq+3 of the quarter, at
+            // tile_off_sw128(t, 4wq) = 128 t + 16 ((wq / 2) ^ (t % 8)) + 8 (wq % 2), t % 8 = (tb % 8) ^ 2i
+            const int cx = (((wq >> 1) ^ (tb & 7)) << 4) + (wq & 1) * 8;
             // two quarters per fence and arrival pair
 #pragma unroll
             for (int g2 = 0; g2 < 4; g2 += 2) {
@@ -570,19 +582,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 for (int g = g2; g < g2 + 2; ++g) {
                     const int q = 4 * s + g, st = q % NSTAGE;
                     if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status)) return false;
-                    uint8_t* bt = smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES + (8 * ew + hi) * 128;
+                    uint8_t* bt = smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES + tb * 128;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
+                    for (int i = 0; i < NI; ++i) {
                         uint32_t o0, o1;
                         s8x4_half_0213(xs[128 * i + 16 * g], o0, o1);
                         *reinterpret_cast<uint2*>(bt + 256 * i + (cx ^ (i << 5))) = make_uint2(o0, o1);
                     }
                 }
-                fence_proxy_async_smem();
+                fence_proxy_async_smem();   // for the local MMAs (and warp 2's copy to the peer)
                 __syncwarp();
                 if (lane == 0) {
-                    tc::mbar_arrive(&bars[B_OP_FULL + (4 * s + g2) % NSTAGE]);
-                    tc::mbar_arrive(&bars[B_OP_FULL + (4 * s + g2 + 1) % NSTAGE]);
+                    constexpr int BAR = SHARE_B ? B_SLICE : B_OP_FULL;
+                    tc::mbar_arrive(&bars[BAR + (4 * s + g2) % NSTAGE]);
+                    tc::mbar_arrive(&bars[BAR + (4 * s + g2 + 1) % NSTAGE]);
                 }
             }
             return true;
@@ -784,9 +797,11 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int pre = workspace != nullptr;
-    // Token tiles in pairs (a two-CTA cluster sharing the weight conversion)
-    // when their number is even.
-    const int cs = tiles_m % 2 == 0 ? 2 : 1;
+    const int tiles_n = static_cast<int>((N + BM - 1) / BM);
+    // Two-CTA clusters when the paired dimension is even: with a workspace
+    // token tiles (sharing the weight conversion), without one weight tiles
+    // (sharing the activation conversion).
+    const int cs = (pre ? tiles_m : tiles_n) % 2 == 0 ? 2 : 1;
     const int smem_bytes = pre ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
     if (smem_bytes > dev.smem_optin) return cudaErrorInvalidConfiguration;
     const void* kern = pre ? (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<true, 2>)
@@ -800,10 +815,12 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
                           dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg));
         if (e != cudaSuccess) return e;
-        if (cs == 2) return launch_kernel_cluster_y(gemm_q4k_kernel<true, 2>, grid, dim3(THREADS), smem_bytes, s, 2u, map, p);
+        if (cs == 2)
+            return launch_kernel_cluster(gemm_q4k_kernel<true, 2>, grid, dim3(THREADS), smem_bytes, s, dim3(1, 2, 1), map, p);
         return launch_kernel(gemm_q4k_kernel<true, 1>, grid, dim3(THREADS), smem_bytes, s, map, p);
     }
-    if (cs == 2) return launch_kernel_cluster_y(gemm_q4k_kernel<false, 2>, grid, dim3(THREADS), smem_bytes, s, 2u, map, p);
+    if (cs == 2)
+        return launch_kernel_cluster(gemm_q4k_kernel<false, 2>, grid, dim3(THREADS), smem_bytes, s, dim3(2, 1, 1), map, p);
     return launch_kernel(gemm_q4k_kernel<false, 1>, grid, dim3(THREADS), smem_bytes, s, map, p);
 }
 
