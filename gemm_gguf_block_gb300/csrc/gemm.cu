@@ -40,9 +40,10 @@
 // Warp roles (896 threads): warp 0 TMA producer of raw Q4_K tiles (2-D tensor
 // map, 128 rows x 144 bytes per superblock); warp 1 allocates tensor memory
 // and one lane issues the MMAs; warp 2 bulk-copies, with a workspace, the
-// pre-converted B operands and, in a CTA pair, this CTA's converted weight
-// slice into the peer's stage (a warp of its own, so that the raw weight
-// boxes run ahead of the operand stages); warp 3 writes each superblock's min slot
+// pre-converted B operands and, in a CTA pair, this CTA's converted slice of
+// each stage (weights with a workspace, activations without) into the peer's
+// stage (a warp of its own, so that the raw weight boxes run ahead of the
+// operand stages); warp 3 writes each superblock's min slot
 // (A_C, A_I; with a workspace also B_min by bulk copy) and scale slot (the
 // rows' d, dmin; with a workspace also d_x); warps 4-11 convert raw weights
 // into fp16 A tiles (K-major, no swizzle); warps 12-27 are the epilogue
