@@ -219,7 +219,10 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 //   without one (SHARE_B): the pair holds weight tiles 2j, 2j+1 of the same
 //     128 tokens; each CTA's epilogue warps convert tokens 64*rank .. +63 of
 //     every B quarter.
-template <bool PRE, int CS>
+//
+// SPLIT (no workspace, single CTAs, at most 96 tokens): the short-tile
+// epilogue described below.
+template <bool PRE, int CS, bool SPLIT>
 __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_constant__ CUtensorMap wmap,
                                                               const GemmParams p) {
     using L = Layout<PRE>;
@@ -240,6 +243,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
     const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
     const int ns = p.ns;
 
+    // A short last token tile without a workspace (at most 96 tokens, a whole
+    // column group of the drain idle): the epilogue warps of the idle column
+    // groups write the activation operands, the others only drain.
+    const int t_valid = min(BN, p.M - m0);
+    const int ngroups = (t_valid + COLS - 1) / COLS;
+    const bool split = SPLIT && ngroups < EPI_WARPS / 4;
+    const int n_drain = split ? 4 * ngroups : EPI_WARPS;           // drain warps
+    const int n_act = split ? EPI_WARPS - n_drain : EPI_WARPS;      // activation-writing warps
     if (threadIdx.x == 0) {
         for (int i = 0; i < NRAW; ++i) {
             mbar_init(&bars[B_RAW_FULL + i], 1);
@@ -247,23 +258,23 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         }
         for (int i = 0; i < NSTAGE; ++i) {
             // warp 2, plus the converters of whatever operand is not copied through it
-            mbar_init(&bars[B_OP_FULL + i], 1 + (SHARE_B ? CONV_WARPS : (PRE ? 0 : EPI_WARPS)));
+            mbar_init(&bars[B_OP_FULL + i], 1 + (SHARE_B ? CONV_WARPS : (PRE ? 0 : n_act)));
             mbar_init(&bars[B_OP_EMPTY + i], CS);                         // the MMA commits of the cluster's CTAs
-            mbar_init(&bars[B_SLICE + i], SHARE_B ? EPI_WARPS : CONV_WARPS);   // this CTA's slice converted
+            mbar_init(&bars[B_SLICE + i], SHARE_B ? n_act : CONV_WARPS);  // this CTA's slice converted
         }
         for (int i = 0; i < NMIN; ++i) {
-            mbar_init(&bars[B_MIN_FULL + i], PRE ? 1 : 1 + EPI_WARPS);      // the slot writer (+ B_min writers)
+            mbar_init(&bars[B_MIN_FULL + i], PRE ? 1 : 1 + n_act);          // the slot writer (+ B_min writers)
             mbar_init(&bars[B_MIN_EMPTY + i], 1);                      // the MMA commit
         }
         for (int i = 0; i < NDX; ++i) {
-            mbar_init(&bars[B_DX_FULL + i], PRE ? 1 : 1 + BN / 32);         // the slot writer (+ d_x writers)
-            mbar_init(&bars[B_DX_EMPTY + i], EPI_WARPS);
+            mbar_init(&bars[B_DX_FULL + i], PRE ? 1 : 1 + (split ? n_act : BN / 32));   // the slot writer (+ d_x writers)
+            mbar_init(&bars[B_DX_EMPTY + i], n_drain);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[B_ACC_FULL + i], 1);
-            mbar_init(&bars[B_X_EMPTY + i], EPI_WARPS);
+            mbar_init(&bars[B_X_EMPTY + i], n_drain);
         }
-        mbar_init(&bars[B_CI_EMPTY], EPI_WARPS);
+        mbar_init(&bars[B_CI_EMPTY], n_drain);
         abort_flag.set(0);
         fence_mbar_init();
     }
@@ -527,10 +538,84 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         // (each thread reads back only what it copied; a copy instruction
         // covers 64 contiguous bytes of each of two tokens), the bsums and d_x
         // in registers.
+        //
+        // In a short tile without a workspace (split), warps ew >= n_drain only
+        // write the activation operands, all superblocks in turn as stages
+        // free up: the B rows of the valid tokens this CTA converts (token
+        // pair j = aw, aw + n_act, ..., lane l: token 2j + l/16, quant word
+        // l%16), B_min and d_x of all valid tokens; the other warps only drain.
         constexpr int TPW = TPC / EPI_WARPS, NI = TPW / 2;   // tokens per warp, token pairs per warp
         const int quarter = warp & 3;
         const int ew = warp - EPI_WARP0, etid = threadIdx.x - 32 * EPI_WARP0;
         const int hi = lane >> 4, wq = lane & 15;
+        if (split && ew >= n_drain) {
+            const int aw = ew - n_drain;
+            const int tlo = TPC * static_cast<int>(SHARE_B ? tc::cluster_rank() : 0u);   // first token converted here
+            const int thi = min(tlo + TPC, t_valid);
+            const int npairs = thi > tlo ? (thi - tlo + 1) / 2 : 0;
+            uint32_t* xsb = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + wq;   // [token][64 words]
+            auto afetch = [&](int s) {
+                for (int j = aw; j < npairs; j += n_act) {
+                    const int t = tlo + 2 * j + hi;
+                    const uint32_t n = t < thi ? 4u : 0u;
+                    const uint32_t* row = reinterpret_cast<const uint32_t*>(
+                        p.xq + static_cast<int64_t>(m0 + (t < thi ? t : 0)) * p.xrow + 292 * s + 4) + wq;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) cp_async4(xsb + 64 * t + 16 * g, row + 16 * g, n);
+                }
+                cp_async_commit();
+            };
+            auto aput = [&](int s) -> bool {
+                cp_async_wait_all();
+                const int ms = s % NMIN, ds = s % NDX;
+                if (!warp_wait(&bars[B_MIN_EMPTY + ms], ((s / NMIN) & 1) ^ 1, abort_flag, p.status)) return false;
+                uint8_t* bm = smem + OFF_MIN + ms * MIN_BYTES + AC_BYTES + AI_BYTES;
+                for (int it = 32 * aw + lane; it < 8 * t_valid; it += 32 * n_act) {   // (token, bsum pair word)
+                    const int t = it >> 3, j = it & 7;
+                    const uint32_t v = __ldg(reinterpret_cast<const uint32_t*>(
+                                                 p.xq + static_cast<int64_t>(m0 + t) * p.xrow + 292 * s + 260) + j);
+                    __half* bh = reinterpret_cast<__half*>(bm + tc::tile_off(t, 0, 16));
+                    bmin_entry(v, bh[j], bh[64 + j]);
+                }
+                fence_proxy_async_smem();
+                warp_arrive(&bars[B_MIN_FULL + ms], lane);
+                if (!warp_wait(&bars[B_DX_EMPTY + ds], ((s / NDX) & 1) ^ 1, abort_flag, p.status)) return false;
+                for (int t = 32 * aw + lane; t < t_valid; t += 32 * n_act)
+                    reinterpret_cast<float*>(smem + OFF_DX + ds * SCL_BYTES)[t] =
+                        __ldg(reinterpret_cast<const float*>(p.xq + static_cast<int64_t>(m0 + t) * p.xrow + 292 * s));
+                warp_arrive(&bars[B_DX_FULL + ds], lane);
+#pragma unroll
+                for (int g2 = 0; g2 < 4; g2 += 2) {
+#pragma unroll
+                    for (int g = g2; g < g2 + 2; ++g) {
+                        const int q = 4 * s + g, st = q % NSTAGE;
+                        if (!warp_wait(&bars[B_OP_EMPTY + st], ((q / NSTAGE) & 1) ^ 1, abort_flag, p.status))
+                            return false;
+                        uint8_t* bstage = smem + OFF_STAGE + st * STAGE_BYTES + A_BYTES;
+                        for (int j = aw; j < npairs; j += n_act) {
+                            const int t = tlo + 2 * j + hi;
+                            uint32_t o0, o1;
+                            s8x4_half_0213(xsb[64 * t + 16 * g], o0, o1);
+                            *reinterpret_cast<uint2*>(bstage + tc::tile_off_sw128(t, 4 * wq, BN)) = make_uint2(o0, o1);
+                        }
+                    }
+                    fence_proxy_async_smem();   // for the local MMAs (and warp 2's copy to the peer)
+                    __syncwarp();
+                    if (lane == 0) {
+                        constexpr int BAR = SHARE_B ? B_SLICE : B_OP_FULL;
+                        tc::mbar_arrive(&bars[BAR + (4 * s + g2) % NSTAGE]);
+                        tc::mbar_arrive(&bars[BAR + (4 * s + g2 + 1) % NSTAGE]);
+                    }
+                }
+                return true;
+            };
+            afetch(0);
+            for (int s = 0; s < ns; ++s) {
+                if (!aput(s)) break;
+                if (s + 1 < ns) afetch(s + 1);
+            }
+            cp_async_wait_all();   // no copy into the staging area outlives the loop
+        } else {
         const int tb = TPC * static_cast<int>(SHARE_B ? tc::cluster_rank() : 0u) + TPW * ew + hi;   // token of pair 0
         uint32_t* xs = reinterpret_cast<uint32_t*>(smem + L::OFF_XS) + tb * 64 + wq;   // [token][64 words]
         uint32_t bsw[2] = {0u, 0u};
@@ -613,13 +698,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
         for (int i = 0; i < 16; ++i) y[i] = 0;
         const uint64_t m1 = tc::pk(-1.0f, -1.0f);
         bool ok = true;
-        if constexpr (!PRE) {
+        if (!PRE && !split) {
             fetch_b(0);
             ok = put_b(0);
             if (ns > 1) fetch_b(1);
         }
         for (int s = 0; s < ns && ok; ++s) {
-            if constexpr (!PRE)
+            if (!PRE && !split)
                 if (s + 1 < ns) {
                     if (!put_b(s + 1)) {
                         ok = false;
@@ -686,7 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                 tc::mbar_arrive(&bars[B_DX_EMPTY + ds]);
             }
         }
-        if constexpr (!PRE) cp_async_wait_all();   // no copy into the staging area outlives the loop
+        if (!PRE) cp_async_wait_all();   // no copy into the staging area outlives the loop
         if (ok && __all_sync(0xffffffffu, !abort_flag.get())) {
 #pragma unroll
             for (int h = 0; h < 2; ++h)
@@ -705,6 +790,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_q4k_kernel(const __grid_const
                         }
                     }
                 }
+        }
         }
     }
 
@@ -808,13 +894,17 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
     // Two-CTA clusters when the paired dimension is even: with a workspace
     // token tiles (sharing the weight conversion), without one weight tiles
     // (sharing the activation conversion).
-    const int cs = (pre ? tiles_m : tiles_n) % 2 == 0 ? 2 : 1;
+    // A single short token tile without a workspace (M <= 96) runs alone, with
+    // the split epilogue.
+    const bool short_tile = !pre && M <= 3 * (BN / 4);
+    const int cs = !short_tile && (pre ? tiles_m : tiles_n) % 2 == 0 ? 2 : 1;
     const int smem_bytes = pre ? Layout<true>::SMEM_BYTES : Layout<false>::SMEM_BYTES;
     if (smem_bytes > dev.smem_optin) return cudaErrorInvalidConfiguration;
-    const void* kern = pre ? (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<true, 2>)
-                                      : reinterpret_cast<const void*>(gemm_q4k_kernel<true, 1>))
-                           : (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<false, 2>)
-                                      : reinterpret_cast<const void*>(gemm_q4k_kernel<false, 1>));
+    const void* kern = pre ? (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<true, 2, false>)
+                                      : reinterpret_cast<const void*>(gemm_q4k_kernel<true, 1, false>))
+                           : short_tile ? reinterpret_cast<const void*>(gemm_q4k_kernel<false, 1, true>)
+                           : (cs == 2 ? reinterpret_cast<const void*>(gemm_q4k_kernel<false, 2, false>)
+                                      : reinterpret_cast<const void*>(gemm_q4k_kernel<false, 1, false>));
     cudaError_t e = raise_smem_limit(kern, smem_bytes);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((N + BM - 1) / BM), static_cast<unsigned>(tiles_m));
@@ -823,12 +913,15 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
                           dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg));
         if (e != cudaSuccess) return e;
         if (cs == 2)
-            return launch_kernel_cluster(gemm_q4k_kernel<true, 2>, grid, dim3(THREADS), smem_bytes, s, dim3(1, 2, 1), map, p);
-        return launch_kernel(gemm_q4k_kernel<true, 1>, grid, dim3(THREADS), smem_bytes, s, map, p);
+            return launch_kernel_cluster(gemm_q4k_kernel<true, 2, false>, grid, dim3(THREADS), smem_bytes, s, dim3(1, 2, 1),
+                                         map, p);
+        return launch_kernel(gemm_q4k_kernel<true, 1, false>, grid, dim3(THREADS), smem_bytes, s, map, p);
     }
+    if (short_tile) return launch_kernel(gemm_q4k_kernel<false, 1, true>, grid, dim3(THREADS), smem_bytes, s, map, p);
     if (cs == 2)
-        return launch_kernel_cluster(gemm_q4k_kernel<false, 2>, grid, dim3(THREADS), smem_bytes, s, dim3(2, 1, 1), map, p);
-    return launch_kernel(gemm_q4k_kernel<false, 1>, grid, dim3(THREADS), smem_bytes, s, map, p);
+        return launch_kernel_cluster(gemm_q4k_kernel<false, 2, false>, grid, dim3(THREADS), smem_bytes, s, dim3(2, 1, 1),
+                                     map, p);
+    return launch_kernel(gemm_q4k_kernel<false, 1, false>, grid, dim3(THREADS), smem_bytes, s, map, p);
 }
 
 }  // namespace cq

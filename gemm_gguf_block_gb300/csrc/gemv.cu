@@ -925,10 +925,12 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     // against 114.7; for Q4_0 and Q4_1 the tensor cores win or tie from M = 2).
     // Q4_K with many tokens: the tcgen05 prefill GEMM (no workspace; its rows
     // are the bits of this kernel's). Measured crossover: from M = 9 when the
-    // matrix has 8192 rows or more (14336 x 4096, M = 9: 65.5 -> 49.2 us;
-    // 128256 x 4096: 376.9 -> 309.2 us), from M = 14 for 4096 rows, which give
-    // the GEMM only 32 row tiles (4096 x 14336, M = 14: 160.8 -> 151.6 us).
-    if (w_fmt == CQ_Q4_K && (M >= 14 || (M >= 9 && N >= 8192))) {
+    // matrix has 8192 rows or more (14336 x 4096: 47.1 us here at M = 8, 41.0
+    // through the GEMM at M = 8..16; 128256 x 4096: 262.3 here at M = 8, 292.9
+    // through the GEMM), from M = 11 for 4096 rows, which give the GEMM only
+    // 32 row tiles (4096 x 14336: 110.6 / 131.1 us here at M = 10 / 11, 114.7 /
+    // 116.7 through the GEMM).
+    if (w_fmt == CQ_Q4_K && (M >= 11 || (M >= 9 && N >= 8192))) {
         if (x != nullptr) {
             const cudaError_t e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
             if (e != cudaSuccess) return e;
