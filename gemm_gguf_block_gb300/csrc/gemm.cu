@@ -912,15 +912,23 @@ cudaError_t launch_gemm(const DeviceInfo& dev, int w_fmt, int64_t M, int64_t N, 
         e = launch_kernel(gemm_prep_kernel, dim3(static_cast<unsigned>(p.ns), static_cast<unsigned>(tiles_m)),
                           dim3(256), 0, s, p, const_cast<uint8_t*>(p.bimg));
         if (e != cudaSuccess) return e;
-        if (cs == 2)
-            return launch_kernel_cluster(gemm_q4k_kernel<true, 2, false>, grid, dim3(THREADS), smem_bytes, s, dim3(1, 2, 1),
-                                         map, p);
+        // A cluster launch the device cannot place (e.g. too few SMs in a
+        // partition) is refused before anything runs: fall back to single CTAs.
+        if (cs == 2 && launch_kernel_cluster(gemm_q4k_kernel<true, 2, false>, grid, dim3(THREADS), smem_bytes, s,
+                                             dim3(1, 2, 1), map, p) == cudaSuccess)
+            return cudaSuccess;
+        if (cs == 2) (void)cudaGetLastError();   // the refused launch's error is not the caller's
+        e = raise_smem_limit(reinterpret_cast<const void*>(gemm_q4k_kernel<true, 1, false>), smem_bytes);
+        if (e != cudaSuccess) return e;
         return launch_kernel(gemm_q4k_kernel<true, 1, false>, grid, dim3(THREADS), smem_bytes, s, map, p);
     }
     if (short_tile) return launch_kernel(gemm_q4k_kernel<false, 1, true>, grid, dim3(THREADS), smem_bytes, s, map, p);
-    if (cs == 2)
-        return launch_kernel_cluster(gemm_q4k_kernel<false, 2, false>, grid, dim3(THREADS), smem_bytes, s, dim3(2, 1, 1),
-                                     map, p);
+    if (cs == 2 && launch_kernel_cluster(gemm_q4k_kernel<false, 2, false>, grid, dim3(THREADS), smem_bytes, s,
+                                         dim3(2, 1, 1), map, p) == cudaSuccess)
+        return cudaSuccess;
+    if (cs == 2) (void)cudaGetLastError();
+    e = raise_smem_limit(reinterpret_cast<const void*>(gemm_q4k_kernel<false, 1, false>), smem_bytes);
+    if (e != cudaSuccess) return e;
     return launch_kernel(gemm_q4k_kernel<false, 1, false>, grid, dim3(THREADS), smem_bytes, s, map, p);
 }
 
