@@ -76,6 +76,10 @@ def lib():
             L.oracle_moe_down.restype = I
             L.oracle_swiglu.argtypes = [I, I64, I64, I64, P, P, P, P, P]
             L.oracle_swiglu.restype = I
+            L.oracle_repack_size.argtypes = [I, I64, I64]
+            L.oracle_repack_size.restype = I64
+            L.oracle_repack.argtypes = [I, I64, I64, P, P]
+            L.oracle_repack.restype = I
             _lib = L
     return _lib
 
@@ -189,3 +193,20 @@ def moe_down(Wd, ids, rw, hq, K: int, F: int, valid=None):
     if rc != 0:
         raise ValueError("oracle_moe_down rejected its arguments")
     return y, y_abs
+
+
+def repack_size(fmt: int, N: int, K: int) -> int:
+    """Bytes of the packed layout of an N x K weight matrix (-1 if not packable)."""
+    return lib().oracle_repack_size(fmt, N, K)
+
+
+def repack(fmt: int, W: np.ndarray, K: int) -> np.ndarray:
+    """The packed layout (cq_repack's, include/cq.h) of W [N, row_bytes], as uint8 bytes."""
+    W = np.ascontiguousarray(W, dtype=np.uint8)
+    size = repack_size(fmt, W.shape[0], K)
+    if size < 0:
+        raise ValueError("oracle_repack_size rejected its arguments")
+    out = np.zeros(size, np.uint8)
+    if lib().oracle_repack(fmt, W.shape[0], K, _p(W), _p(out)) != 0:
+        raise ValueError("oracle_repack rejected its arguments")
+    return out

@@ -514,3 +514,60 @@ int oracle_moe_down(int64_t T, int64_t K, int64_t F, int64_t E, int64_t topk, co
     }
     return ORC_OK;
 }
+
+/* ---------------------------------------------------------- offline weight repack */
+
+/* The packed weight layout of cq_repack, written out byte by byte from its
+ * definition (the library's own layout, specified in include/cq.h). The pages
+ * repack weights at load for their NPU and CPU kernels -- cera README,
+ * "Qualcomm Hexagon" -> "Accelerated Kernels" (Q4_0 / Q8_0 weights repacked
+ * into tiles); alice-llm docs, "Phase 6 -> Block-Packed Weight Layout" (rows
+ * interleaved so that one load serves several rows) -- but print no layout for
+ * a GPU, so the layout itself is a reading: rows in groups of 16, K in
+ * segments of 4 blocks; the unit (group G, segment s) of 64 * BB bytes sits at
+ * byte (s * ceil(N / 16) + G) * 64 * BB and holds
+ *   - per row r of the group: the scale fields of blocks 0..3 of the segment
+ *     (Q4_1: d, m = block bytes 0..3; Q4_0 / Q8_0: d = block bytes 0..1), rows
+ *     16 (Q4_1) or 8 bytes apart;
+ *   - then, per half h (Q8_0: h = 0, 1; Q4_0 / Q4_1: h = 0), per row r, per
+ *     lane t = 0..3, per block j = 0..3: quant bytes 16h + 4t .. 16h + 4t + 3 of
+ *     block j (offsets within the block's quant array).
+ * Rows at or past N are zero. Returns the packed size in bytes, or -1. */
+int64_t oracle_repack_size(int fmt, int64_t N, int64_t K)
+{
+    int64_t bb = fmt == ORC_Q4_0 ? 18 : fmt == ORC_Q4_1 ? 20 : fmt == ORC_Q8_0 ? 34 : 0;
+    if (bb == 0 || N < 0 || K <= 0 || K % 256 != 0) return -1;
+    return (N + 15) / 16 * (K / 128) * 64 * bb;
+}
+
+int oracle_repack(int fmt, int64_t N, int64_t K, const uint8_t* W, uint8_t* out)
+{
+    int64_t size = oracle_repack_size(fmt, N, K);
+    if (size < 0) return ORC_BAD;
+    int64_t bb = fmt == ORC_Q4_0 ? 18 : fmt == ORC_Q4_1 ? 20 : 34;
+    int64_t ng = (N + 15) / 16, ns = K / 128, unit = 64 * bb, wrow = K / 32 * bb;
+    int scale_bytes = fmt == ORC_Q4_1 ? 4 : 2;       /* per block */
+    int quant_off = fmt == ORC_Q4_1 ? 4 : 2;         /* quants' offset in the block */
+    int halves = fmt == ORC_Q8_0 ? 2 : 1;
+    int64_t scale_region = 16 * 4 * scale_bytes;
+    memset(out, 0, (size_t)size);
+    for (int64_t s = 0; s < ns; s++)
+        for (int64_t G = 0; G < ng; G++) {
+            uint8_t* u = out + (s * ng + G) * unit;
+            for (int r = 0; r < 16; r++) {
+                int64_t row = 16 * G + r;
+                if (row >= N) continue;
+                for (int j = 0; j < 4; j++) {
+                    const uint8_t* blk = W + row * wrow + (4 * s + j) * bb;
+                    for (int i = 0; i < scale_bytes; i++)
+                        u[r * 4 * scale_bytes + j * scale_bytes + i] = blk[i];
+                    for (int h = 0; h < halves; h++)
+                        for (int t = 0; t < 4; t++)
+                            for (int i = 0; i < 4; i++)
+                                u[scale_region + h * 1024 + ((r * 4 + t) * 4 + j) * 4 + i] =
+                                    blk[quant_off + 16 * h + 4 * t + i];
+                }
+            }
+        }
+    return ORC_OK;
+}

@@ -14,6 +14,9 @@ half-away rounding) fails at least one of them:
   the fp64 rounding of its own sum.
 * Quantizer invariants: |q| <= 127, the amax element hits +-127, the
   reconstruction error is at most half a step, Q8_K block sums equal the sums.
+* Offline repack: byte offsets worked out by hand from the packed layout's
+  definition, and an inverse written as array reshapes that must give back
+  the weights exactly, with zero padding rows.
 """
 import math
 import os
@@ -526,3 +529,74 @@ def test_swiglu_zero_scales_give_zero(orc, which):
     xq = orc.quantize(orc.Q8_K, x)
     h, _ = orc.swiglu(orc.Q4_K, Wg, Wu, xq, K)
     assert np.all(h == 0)
+
+
+# ------------------------------------------------------------ offline repack
+# The packed layout is the library's own (include/cq.h, cq_repack): units of
+# 16 rows x 4 blocks, segment-major; per row the blocks' scale fields, then per
+# (half, row, lane t, block j) the quant bytes 16h + 4t .. 16h + 4t + 3.
+
+def _identity_rows(N, row_bytes):
+    """Weight bytes that name their own position: (7 n + 3 b + 1) mod 251."""
+    n = np.arange(N)[:, None]
+    b = np.arange(row_bytes)[None, :]
+    return ((7 * n + 3 * b + 1) % 251).astype(np.uint8)
+
+
+def test_repack_hand_offsets(orc):
+    """Byte offsets worked out by hand from the layout definition."""
+    W = _identity_rows(17, 160)                  # Q4_1, K = 256: 8 blocks of 20 bytes
+    P = orc.repack(orc.Q4_1, W, 256)
+    assert P.size == 2 * 2 * 1280                # 2 groups x 2 segments x 64 * 20
+    assert list(P[0:4]) == list(W[0, 0:4])       # row 0, block 0: d, m
+    assert list(P[24:28]) == list(W[1, 40:44])   # row 1, block 2: at 1*16 + 2*4
+    assert list(P[364:368]) == list(W[1, 72:76]) # row 1, lane 2, block 3: 256 + ((1*4+2)*4+3)*4
+    assert list(P[1280:1284]) == list(W[16, 0:4])            # group 1 (row 16), segment 0
+    assert not P[1280 + 16:1280 + 256].any()                 # rows 17..31: no scales
+    assert not P[1280 + 256 + 64:2560].any()                 # rows 17..31: no quants
+    assert list(P[2560:2564]) == list(W[0, 80:84])           # group 0, segment 1: block 4
+    W8 = _identity_rows(16, 272)                 # Q8_0, K = 256: 8 blocks of 34 bytes
+    P8 = orc.repack(orc.Q8_0, W8, 256)
+    assert P8.size == 2 * 2176
+    assert list(P8[26:28]) == list(W8[3, 34:36])             # row 3, block 1: d at 3*8 + 1*2
+    assert list(P8[1328:1332]) == list(W8[2, 30:34])         # half 1, row 2, lane 3, block 0
+    W4 = _identity_rows(3, 144)                  # Q4_0, K = 256
+    P4 = orc.repack(orc.Q4_0, W4, 256)
+    assert P4.size == 2 * 1152
+    assert list(P4[148:152]) == list(W4[0, 24:28])           # row 0, lane 1, block 1: 128 + 5*4
+    assert list(P4[22:24]) == list(W4[2, 54:56])             # row 2, block 3: d at 2*8 + 3*2
+
+
+def _unpack(fmt, P, N, K):
+    """Inverse of the layout, written as array reshapes (scatter form)."""
+    bb = {2: 18, 3: 20, 8: 34}[fmt]
+    sb = 4 if fmt == 3 else 2
+    halves = 2 if fmt == 8 else 1
+    ng, ns = (N + 15) // 16, K // 128
+    U = P.reshape(ns, ng, 64 * bb)
+    scales = U[:, :, :64 * sb].reshape(ns, ng, 16, 4, sb)
+    quants = U[:, :, 64 * sb:].reshape(ns, ng, halves, 16, 4, 4, 4)          # s, G, h, r, t, j, byte
+    quants = quants.transpose(1, 3, 0, 5, 2, 4, 6).reshape(ng * 16, ns * 4, halves * 16)
+    scales = scales.transpose(1, 2, 0, 3, 4).reshape(ng * 16, ns * 4, sb)
+    blocks = np.concatenate([scales, quants], axis=2)                        # row, block, bytes
+    assert blocks.shape[2] == bb
+    return blocks.reshape(ng * 16, K // 32 * bb)
+
+
+@pytest.mark.parametrize("fmt", [2, 3, 8])
+@pytest.mark.parametrize("N,K", [(1, 256), (15, 512), (16, 256), (33, 768)])
+def test_repack_inverse_roundtrip(orc, fmt, N, K):
+    """Unpacking by the inverse reshapes gives back W; padding rows are zero."""
+    rng = np.random.default_rng(fmt * 100 + N + K)
+    W = rng.integers(0, 256, (N, orc.row_bytes(fmt, K)), dtype=np.uint8)
+    P = orc.repack(fmt, W, K)
+    assert P.size == (N + 15) // 16 * 16 * orc.row_bytes(fmt, K)
+    Wb = _unpack(fmt, P, N, K)
+    assert np.array_equal(Wb[:N], W)
+    assert not Wb[N:].any()
+
+
+def test_repack_rejects(orc):
+    assert orc.repack_size(orc.Q4_K, 16, 256) == -1
+    assert orc.repack_size(orc.Q4_0, 16, 128) == -1
+    assert orc.repack_size(orc.Q4_0, 0, 256) == 0
