@@ -19,9 +19,15 @@
 // blocks, y = y + c per chunk. Every (row, token) chain lives in one thread,
 // so each row equals the single-token GEMV row bit for bit.
 //
-// A persistent CTA (8 consumer warps of 16 rows each + 1 producer warp)
-// stages the tokens' activations once as fp16 in shared memory, then streams
-// 128-row weight tiles through a ring of 2-D TMA boxes (128 rows x 8 blocks).
+// A persistent CTA stages the tokens' activations once as fp16 in shared
+// memory, then a producer warp streams weight tiles of 16 * RW * RG rows
+// through a ring of 2-D TMA boxes (the tile's rows x 8 blocks). Each of the RG
+// consumer warps owns RW row groups of 16 rows and all the tokens (NT n-tiles
+// of 8). The activation fragments and scale records a warp reads from shared
+// memory per block serve all its row groups: with one row group per warp they
+// made two thirds of the shared-memory wavefronts and kept that pipe about
+// 60% busy, so the long tiles take two (7 warps x 32 rows for up to 8
+// tokens, 6 x 32 for up to 16).
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -34,14 +40,15 @@
 namespace cq {
 namespace {
 
-constexpr int SEG_BLOCKS = 8;       // 32-blocks per stage (256 elements)
 constexpr int MAX_STAGES = 4;
-// Consumer warps (16 rows each) per CTA.
-__host__ __device__ constexpr int consumers(int) { return 8; }
-__host__ __device__ constexpr int tile_rows(int NT) { return 16 * consumers(NT); }
 
 using mf::MF;
 using mf::stage_pitch;
+
+// Bytes per weight row in a stage of sb blocks: 8 blocks as the shared
+// stage_pitch; 4 Q4_1 blocks are 80 bytes (20 words: the 8 rows one load
+// instruction touches fall in 8 different bank groups).
+__host__ __device__ constexpr int seg_pitch(int bb, int sb) { return sb == 8 ? stage_pitch(bb) : sb * bb; }
 
 struct MmaParams {
     const uint8_t* W;
@@ -59,22 +66,25 @@ struct MmaParams {
     int smem_stage;     // offset of the weight stages
 };
 
-template <int WF, int NT>
-__global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
+template <int WF, int RG, int NT, int RW, int SB>
+__global__ void __launch_bounds__((RG + 1) * 32, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const MmaParams p) {
     pdl_trigger();
     pdl_wait();
     using F = MF<WF>;
     constexpr int NPAIR = NT * 4;                  // token pairs
-    constexpr int CONSUMERS = consumers(NT);
-    constexpr int ROWS = tile_rows(NT);
+    constexpr int CONSUMERS = RG;
+    constexpr int ROWS = 16 * RW * RG;
+    constexpr int NBOX = (ROWS + 255) / 256;      // TMA boxes per stage
+    static_assert(ROWS % NBOX == 0, "tile rows split evenly into boxes");
+    static_assert(seg_pitch(F::BB, SB) % 16 == 0, "a stage row is a whole number of 16-byte units");
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + MAX_STAGES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages;
     const int tiles = (p.N + ROWS - 1) / ROWS;
-    const int nseg = p.nb / SEG_BLOCKS;
+    const int nseg = p.nb / SB;
     const int my_tiles = blockIdx.x < tiles ? (tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t steps = static_cast<int64_t>(my_tiles) * nseg;
 
@@ -84,9 +94,11 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
         const int tile = blockIdx.x + static_cast<int>(k / nseg) * gridDim.x;
         const int seg = static_cast<int>(k % nseg);
         mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(p.stage_bytes));
-        // x counts 2-byte elements of the row
-        tc::tma_load_2d(smem + p.smem_stage + st * p.stage_bytes, &wmap, seg * SEG_BLOCKS * F::BB / 2, tile * ROWS,
-                        &full[st]);
+        // x counts 2-byte elements of the row; a box holds at most 256 rows
+#pragma unroll
+        for (int j = 0; j < NBOX; ++j)
+            tc::tma_load_2d(smem + p.smem_stage + st * p.stage_bytes + j * (ROWS / NBOX) * seg_pitch(F::BB, SB), &wmap,
+                            seg * SB * F::BB / 2, tile * ROWS + j * (ROWS / NBOX), &full[st]);
     };
     // The weight stream starts before the activations are staged: the first
     // S stages need no release.
@@ -139,18 +151,21 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
         }
     } else {
         // -------------------------------------------------------- consumers
+        // Tile rows 16 RW w .. 16 RW (w + 1) - 1, all tokens.
         const int g = lane >> 2, t = lane & 3;
         const uint8_t* act = smem + p.smem_act + g * p.act_pitch + 16 * t;
         const float4* sc4 = reinterpret_cast<const float4*>(smem + p.smem_scale) + t;
         const float2* sx2 = reinterpret_cast<const float2*>(smem + p.smem_scale + p.nb * NPAIR * 16) + t;
-        const int seg_row_bytes = stage_pitch(F::BB);
-        uint64_t c[NT][2], y[NT][2];   // (row g | row g+8) x (token 8n+2t, 8n+2t+1)
+        constexpr int seg_row_bytes = seg_pitch(F::BB, SB);
+        uint64_t c[RW][NT][2], y[RW][NT][2];   // group r: (row g | row g+8) x (token 8n+2t, 8n+2t+1)
         int64_t k = 0;
         bool ok = true;
         for (int ti = 0; ti < my_tiles && ok; ++ti) {
             const int tile = blockIdx.x + ti * gridDim.x;
 #pragma unroll
-            for (int n = 0; n < NT; ++n) y[n][0] = y[n][1] = 0;
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int n = 0; n < NT; ++n) y[r][n][0] = y[r][n][1] = 0;
             for (int seg = 0; seg < nseg; ++seg, ++k) {
                 const int st = static_cast<int>(k % S);
                 if (!mbar_wait_bounded(&full[st], static_cast<uint32_t>((k / S) & 1), WAIT_LIMIT_NS)) {
@@ -158,61 +173,78 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
                     ok = false;
                     break;
                 }
-                const uint8_t* rg = smem + p.smem_stage + st * p.stage_bytes + (16 * warp + g) * seg_row_bytes;
-                const uint8_t* rg8 = rg + 8 * seg_row_bytes;
+                const uint8_t* r0p = smem + p.smem_stage + st * p.stage_bytes + (16 * RW * warp + g) * seg_row_bytes;
 #pragma unroll 4
-                for (int bi = 0; bi < SEG_BLOCKS; ++bi) {
-                    const int b = seg * SEG_BLOCKS + bi;          // block index along K
-                    uint32_t a0[4], a1[4];
-                    uint64_t dw0, dw1, mw0, mw1;
-                    mf::weight_frags<WF>(rg + bi * F::BB, rg8 + bi * F::BB, t, a0, a1, dw0, dw1, mw0, mw1);
+                for (int bi = 0; bi < SB; ++bi) {
+                    const int b = seg * SB + bi;                  // block index along K
+                    uint32_t a0[RW][4], a1[RW][4];
+                    uint64_t dw0[RW], dw1[RW], mw0[RW], mw1[RW];
+#pragma unroll
+                    for (int r = 0; r < RW; ++r) {
+                        const uint8_t* wr = r0p + 16 * r * seg_row_bytes + bi * F::BB;
+                        mf::weight_frags<WF>(wr, wr + 8 * seg_row_bytes, t, a0[r], a1[r], dw0[r], dw1[r], mw0[r],
+                                             mw1[r]);
+                    }
                     if ((b & 3) == 0) {
 #pragma unroll
-                        for (int n = 0; n < NT; ++n) c[n][0] = c[n][1] = 0;
+                        for (int r = 0; r < RW; ++r)
+#pragma unroll
+                            for (int n = 0; n < NT; ++n) c[r][n][0] = c[r][n][1] = 0;
                     }
 #pragma unroll
                     for (int n = 0; n < NT; ++n) {
                         const uint4 bv = *reinterpret_cast<const uint4*>(act + 8 * n * p.act_pitch + 64 * b);
                         const float4 s4 = sc4[b * NPAIR + 4 * n];
-                        float acc[4];
-                        mf::mma16816c(acc, a0, bv.x, bv.y, s4.z, s4.w);
-                        mf::mma16816acc(acc, a1, bv.z, bv.w);
                         const uint64_t dx = tc::pk(s4.x, s4.y);
-                        // c = fma(d_w * d_x, isum, c) per element, two tokens per instruction
-                        c[n][0] = tc::fma2(tc::mul2(dw0, dx), tc::pk(acc[0], acc[1]), c[n][0]);
-                        c[n][1] = tc::fma2(tc::mul2(dw1, dx), tc::pk(acc[2], acc[3]), c[n][1]);
+                        uint64_t sx = 0;
                         if constexpr (WF == CQ_Q4_1) {
                             const float2 s2 = sx2[b * NPAIR + 4 * n];
-                            const uint64_t sx = tc::pk(s2.x, s2.y);
-                            c[n][0] = tc::fma2(mw0, sx, c[n][0]);
-                            c[n][1] = tc::fma2(mw1, sx, c[n][1]);
+                            sx = tc::pk(s2.x, s2.y);
+                        }
+#pragma unroll
+                        for (int r = 0; r < RW; ++r) {
+                            float acc[4];
+                            mf::mma16816c(acc, a0[r], bv.x, bv.y, s4.z, s4.w);
+                            mf::mma16816acc(acc, a1[r], bv.z, bv.w);
+                            // c = fma(d_w * d_x, isum, c) per element, two tokens per instruction
+                            c[r][n][0] = tc::fma2(tc::mul2(dw0[r], dx), tc::pk(acc[0], acc[1]), c[r][n][0]);
+                            c[r][n][1] = tc::fma2(tc::mul2(dw1[r], dx), tc::pk(acc[2], acc[3]), c[r][n][1]);
+                            if constexpr (WF == CQ_Q4_1) {
+                                c[r][n][0] = tc::fma2(mw0[r], sx, c[r][n][0]);
+                                c[r][n][1] = tc::fma2(mw1[r], sx, c[r][n][1]);
+                            }
                         }
                     }
                     if ((b & 3) == 3) {
 #pragma unroll
-                        for (int n = 0; n < NT; ++n) {
-                            y[n][0] = tc::add2(y[n][0], c[n][0]);
-                            y[n][1] = tc::add2(y[n][1], c[n][1]);
-                        }
+                        for (int r = 0; r < RW; ++r)
+#pragma unroll
+                            for (int n = 0; n < NT; ++n) {
+                                y[r][n][0] = tc::add2(y[r][n][0], c[r][n][0]);
+                                y[r][n][1] = tc::add2(y[r][n][1], c[r][n][1]);
+                            }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&empty[st]);
             }
             if (!ok) break;
-            // y[token][row]: rows 16w+g and 16w+g+8, tokens 8n+2t, 8n+2t+1
-            const int r0 = tile * ROWS + 16 * warp + g;
+            // y[token][row]: rows 16 (RW w + r) + g (+ 8), tokens 8n+2t, 8n+2t+1
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int m0 = 8 * n + 2 * t;
+            for (int r = 0; r < RW; ++r) {
+                const int r0 = tile * ROWS + 16 * (RW * warp + r) + g;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float v[2];
-                    tc::upk(y[n][h], v[0], v[1]);
-                    const int row = r0 + 8 * h;
+                for (int n = 0; n < NT; ++n) {
+                    const int m0 = 8 * n + 2 * t;
 #pragma unroll
-                    for (int i = 0; i < 2; ++i)
-                        if (row < p.N && m0 + i < p.M) p.y[static_cast<int64_t>(m0 + i) * p.N + row] = v[i];
+                    for (int h = 0; h < 2; ++h) {
+                        float v[2];
+                        tc::upk(y[r][n][h], v[0], v[1]);
+                        const int row = r0 + 8 * h;
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+                            if (row < p.N && m0 + i < p.M) p.y[static_cast<int64_t>(m0 + i) * p.N + row] = v[i];
+                    }
                 }
             }
         }
@@ -225,35 +257,68 @@ __global__ void __launch_bounds__((consumers(NT) + 1) * 32, 1)
     }
 }
 
-// Shared-memory layout for M tokens, K columns: barriers, the fp16
-// activation tile, the scale table, then `stages` weight stages.
+// Shared-memory layout for M tokens, K columns and RG row groups: barriers,
+// the fp16 activation tile, the scale table, then the weight stages.
 struct MmaSmem {
     int act_pitch, act, scale, stage, stage_bytes, fixed;
 };
-MmaSmem mma_smem(int bb, int M, int64_t K) {
+MmaSmem mma_smem(int bb, int M, int64_t K, int rows, int sb) {
     MmaSmem m{};
     const int NT = M <= 8 ? 1 : 2;
-    const int ROWS = tile_rows(NT);
     const int nb = static_cast<int>(K / 32);
     m.act_pitch = static_cast<int>(K) * 2 + 64;      // 64 mod 128: token rows g, g+1 on different bank halves
     m.act = 1024;
     m.scale = m.act + (NT * 8 * m.act_pitch + 127) / 128 * 128;
     const int scale_bytes = nb * NT * 4 * (bb == 20 ? 24 : 16);
     m.stage = m.scale + (scale_bytes + 1023) / 1024 * 1024;
-    m.stage_bytes = ROWS * stage_pitch(bb);
+    m.stage_bytes = rows * seg_pitch(bb, sb);
     m.fixed = m.stage;
     return m;
 }
 
-template <int WF, int NT>
+// Tile shapes: RG consumer warps x RW row groups of 16 rows, SB blocks per
+// stage. Each warp streams its rows over all of K, so a CTA's time goes with
+// the rows of its largest share of tiles. Of the shapes that fit with their
+// stages, the first in order of preference whose rows per CTA are within a
+// slack of the least is taken: for up to 8 tokens 14 x 32 rows (Q4_1 with
+// 4-block stages), then 7 x 32, then 8 x 16; for up to 16 tokens 12 x 16, then
+// 8 x 16 (two row groups per warp at 16 tokens leave too few warps). The
+// 128256-row LM head gets 2 tiles of 448 rows per SM, the same 896 rows as 7
+// tiles of 128.
+struct TileShape {
+    int rg, rw, sb;
+    int rows() const { return 16 * rg * rw; }
+};
+TileShape choose_tile(int bb, int M, int64_t N, int64_t K, int sms, int lim) {
+    const TileShape cand1[] = {{14, 2, bb == 20 ? 4 : 8}, {7, 2, 8}, {8, 1, 8}};
+    const TileShape cand2[] = {{12, 1, 8}, {8, 1, 8}};
+    const TileShape* cand = M <= 8 ? cand1 : cand2;
+    const int nc = M <= 8 ? 3 : 2;
+    const int min_stages = M <= 8 ? 3 : 2;
+    auto rows_per_cta = [&](int rows) {
+        const int64_t tiles = (N + rows - 1) / rows;
+        return (tiles + sms - 1) / sms * rows;
+    };
+    int64_t best = INT64_MAX;
+    for (int i = 0; i < nc; ++i) best = std::min(best, rows_per_cta(cand[i].rows()));
+    const int64_t slack = M <= 8 ? 0 : best / 8;
+    for (int i = 0; i < nc - 1; ++i) {
+        const MmaSmem L = mma_smem(bb, M, K, cand[i].rows(), cand[i].sb);
+        if ((lim - L.fixed) / L.stage_bytes >= min_stages && rows_per_cta(cand[i].rows()) <= best + slack)
+            return cand[i];
+    }
+    return cand[nc - 1];
+}
+
+template <int WF, int RG, int NT, int RW, int SB>
 cudaError_t launch_mma_typed(const DeviceInfo& dev, MmaParams p, const CUtensorMap& map, cudaStream_t s) {
     const int smem = p.smem_stage + p.stages * p.stage_bytes;
-    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemv_mma_kernel<WF, NT>),
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemv_mma_kernel<WF, RG, NT, RW, SB>),
                                            std::min(dev.smem_optin, 227 * 1024));
     if (e != cudaSuccess) return e;
-    const int tiles = (p.N + tile_rows(NT) - 1) / tile_rows(NT);
+    const int tiles = (p.N + 16 * RW * RG - 1) / (16 * RW * RG);
     const int grid = std::min(tiles, dev.sm_count);
-    return launch_kernel(gemv_mma_kernel<WF, NT>, dim3(grid), dim3((consumers(NT) + 1) * 32), smem, s, map, p);
+    return launch_kernel(gemv_mma_kernel<WF, RG, NT, RW, SB>, dim3(grid), dim3((RG + 1) * 32), smem, s, map, p);
 }
 
 template <int WF>
@@ -273,8 +338,9 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
     p.nb = static_cast<int>(K / 32);
     p.wrow = static_cast<int64_t>(p.nb) * F::BB;
     const int NT = M <= 8 ? 1 : 2;
-    const MmaSmem L = mma_smem(F::BB, M, K);
     const int lim = std::min(dev.smem_optin, 227 * 1024);
+    const TileShape T = choose_tile(F::BB, M, N, K, dev.sm_count, lim);
+    const MmaSmem L = mma_smem(F::BB, M, K, T.rows(), T.sb);
     p.act_pitch = L.act_pitch;
     p.stage_bytes = L.stage_bytes;
     p.smem_act = L.act;
@@ -283,18 +349,28 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
     p.stages = std::min(MAX_STAGES, (lim - L.fixed) / L.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidConfiguration;
     // Raw weights as a 2-D tensor of 2-byte elements [N rows][wrow/2]; a box is
-    // 8 blocks of one tile's rows.
+    // SB blocks of one tile's rows.
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.wrow / 2), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.wrow)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(stage_pitch(F::BB) / 2),
-                               static_cast<cuuint32_t>(tile_rows(NT))};
+    const int nbox = (T.rows() + 255) / 256;
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(seg_pitch(F::BB, T.sb) / 2),
+                               static_cast<cuuint32_t>(T.rows() / nbox)};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(W), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    return NT == 1 ? launch_mma_typed<WF, 1>(dev, p, map, s) : launch_mma_typed<WF, 2>(dev, p, map, s);
+    if (NT == 2)
+        return T.rg == 12 ? launch_mma_typed<WF, 12, 2, 1, 8>(dev, p, map, s)
+                          : launch_mma_typed<WF, 8, 2, 1, 8>(dev, p, map, s);
+    if (T.rg == 14) {
+        if constexpr (WF == CQ_Q4_1) {
+            if (T.sb == 4) return launch_mma_typed<WF, 14, 1, 2, 4>(dev, p, map, s);
+        }
+        return launch_mma_typed<WF, 14, 1, 2, 8>(dev, p, map, s);
+    }
+    return T.rw == 2 ? launch_mma_typed<WF, 7, 1, 2, 8>(dev, p, map, s) : launch_mma_typed<WF, 8, 1, 1, 8>(dev, p, map, s);
 }
 
 }  // namespace
@@ -304,7 +380,7 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
 int gemv_mma_smem(int w_fmt, int M, int64_t K) {
     if (w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) return 0;
     const int bb = w_fmt == CQ_Q4_0 ? 18 : w_fmt == CQ_Q4_1 ? 20 : 34;
-    const MmaSmem L = mma_smem(bb, M, K);
+    const MmaSmem L = mma_smem(bb, M, K, 128, 8);
     return L.fixed + 2 * L.stage_bytes;
 }
 

@@ -265,3 +265,29 @@ def test_gemv_largest_k(orc, wfmt):
     assert_within(y, y_ref, at, what=f"K={K}")
     y1 = cq.gemv_t(dev(torch, W), dev(torch, xq[1:2]), wfmt, K).cpu().numpy()[0]
     assert np.array_equal(y[1].view(np.uint32), y1.view(np.uint32))
+
+
+@pytest.mark.parametrize("wfmt", [2, 3, 8])
+@pytest.mark.parametrize("tail", ["ragged", "empty_box"])
+def test_batched_gemv_long_tiles(orc, wfmt, tail):
+    """Row counts that make the batched tensor-core GEMV take its long tiles
+    (448 rows of 14 warps x 32 for up to 8 tokens with Q4_1, 224 rows of 7 x 32
+    for Q4_0, 192 rows of 12 x 16 for up to 16 tokens): one tile of 448 rows
+    per SM, the last one ragged, or with its second 224-row box wholly past N.
+    Sampled rows against the oracle, every row of M = 2..16 bit for bit equal
+    to M = 1."""
+    torch = torch_cuda()
+    cq = cq_built()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    N = sms * 448 - 37 if tail == "ragged" else (sms - 1) * 448 + 100
+    K = 512
+    W, xq = _case(orc, wfmt, N, K, 16, seed=wfmt * 31 + N)
+    Wd, xd = dev(torch, W), dev(torch, xq)
+    single = np.stack([cq.gemv_t(Wd, xd[m:m + 1], wfmt, K).cpu().numpy()[0] for m in range(16)])
+    idx = np.unique(np.concatenate([np.arange(0, 500), np.arange(N - 700, N),
+                                    np.linspace(0, N - 1, 200).astype(np.int64)]))
+    y_ref, at = orc.matmul(wfmt, W[idx], xq, K)
+    assert_within(single[:, idx], y_ref, at, what=f"fmt {wfmt} N={N} M=1")
+    for M in (2, 4, 8, 9, 16):
+        yM = cq.gemv_t(Wd, xd[:M], wfmt, K).cpu().numpy()
+        assert np.array_equal(yM.view(np.uint32), single[:M].view(np.uint32)), f"M={M} rows differ from M=1"
