@@ -426,14 +426,20 @@ def case_lm_head(c, cq, synth, peaks, seed, ms_list=(1, 4, 8, 16)):
     N, K = W.shape[0], x.shape[1]
     Wd, xd = c.dev(W), c.dev(x)
     xq = cq.quantize_act_t(xd, cq.Q8_1)
+    # the same head repacked once (cq_repack) and read by cq_gemv_packed
+    Wp = cq.repack_t(Wd, cq.Q4_1, K)
     res = {}
     for M in ms_list:
         y = c.torch.empty((M, N), dtype=c.torch.float32, device="cuda")
         ms = c.time(lambda: cq.cq_gemv(cq.Q4_1, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
         res[str(M)] = {"ms": ms, "weight_gbs": W.nbytes / ms / 1e6, "hbm_frac": W.nbytes / ms / 1e6 / peaks["hbm"]}
+        pms = c.time(lambda: cq.cq_gemv_packed(cq.Q4_1, M, N, K, Wp.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                               c.stream()))
+        res[str(M)]["packed"] = {"ms": pms, "weight_gbs": W.nbytes / pms / 1e6}
     if "1" in res:
         for M in res:
             res[M]["t_over_t1"] = res[M]["ms"] / res["1"]["ms"]
+            res[M]["packed"]["t_over_t1"] = res[M]["packed"]["ms"] / res["1"]["ms"]
     return res
 
 

@@ -49,6 +49,9 @@ SIGNATURES = {
     "cq_status_string": (C.c_char_p, [_I]),
     "cq_set_option": (_I, [_I, _I64]),
     "cq_selftest_wait_timeout": (_I, [_I64, _P, _P]),
+    "cq_repack_size": (_SZ, [_I, _I64, _I64]),
+    "cq_repack": (_I, [_I, _I64, _I64, _P, _P, _P]),
+    "cq_gemv_packed": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
 }
 
 OPT_WEIGHTS_CONST = 1
@@ -115,6 +118,18 @@ def cq_selftest_wait_timeout(limit_ns, stream=0):
 
 def cq_set_option(opt, value):
     return lib().cq_set_option(opt, value)
+
+
+def cq_repack_size(w_fmt, N, K):
+    return lib().cq_repack_size(w_fmt, N, K)
+
+
+def cq_repack(w_fmt, N, K, W, Wp, stream=0):
+    return lib().cq_repack(w_fmt, N, K, W, Wp, stream)
+
+
+def cq_gemv_packed(w_fmt, M, N, K, Wp, xq, y, stream=0):
+    return lib().cq_gemv_packed(w_fmt, M, N, K, Wp, xq, y, stream)
 
 
 def cq_gemm_workspace_size(w_fmt, M, N, K):
@@ -205,6 +220,28 @@ def gemv_t(W, xq, w_fmt: int, K: int, out=None):
     N, M = W.shape[0], xq.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=W.device)
     _check("cq_gemv", cq_gemv(w_fmt, M, N, K, W.data_ptr(), xq.data_ptr(), y.data_ptr(), _stream_handle()))
+    return y
+
+
+def repack_t(W, w_fmt: int, K: int):
+    """cq_repack: W uint8 [N, row_bytes] -> the packed layout, uint8 [cq_repack_size]."""
+    torch = _torch()
+    N = W.shape[0]
+    size = cq_repack_size(w_fmt, N, K)
+    if size == 0 and N > 0:
+        raise CqError("cq_repack_size", ERR_SHAPE)
+    Wp = torch.empty(size, dtype=torch.uint8, device=W.device)
+    _check("cq_repack", cq_repack(w_fmt, N, K, W.data_ptr(), Wp.data_ptr(), _stream_handle()))
+    return Wp
+
+
+def gemv_packed_t(Wp, xq, w_fmt: int, N: int, K: int, out=None):
+    """cq_gemv_packed: Wp from repack_t; xq uint8 [M, act_row_bytes] (M <= 16) -> fp32 [M, N]."""
+    torch = _torch()
+    M = xq.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=Wp.device)
+    _check("cq_gemv_packed", cq_gemv_packed(w_fmt, M, N, K, Wp.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                            _stream_handle()))
     return y
 
 

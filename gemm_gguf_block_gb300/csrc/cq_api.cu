@@ -133,6 +133,40 @@ cq_status cq_gemv(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* 
     return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 
+size_t cq_repack_size(cq_format w_fmt, int64_t N, int64_t K) {
+    if (N < 0 || K > K_MAX) return 0;
+    return static_cast<size_t>(cq::repack_size(w_fmt, N, K));
+}
+
+cq_status cq_repack(cq_format w_fmt, int64_t N, int64_t K, const void* W, void* Wp, void* stream) {
+    if (w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(1, N, K);
+    if (st != CQ_OK) return st;
+    if (N == 0) return CQ_OK;
+    if (W == nullptr || Wp == nullptr) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(Wp)) return CQ_ERR_ALIGNMENT;
+    cudaError_t e = cq::launch_repack(w_fmt, N, K, W, Wp, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
+cq_status cq_gemv_packed(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* Wp, const void* xq, float* y,
+                         void* stream) {
+    if (w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) return CQ_ERR_UNSUPPORTED_FORMAT;
+    cq_status st = check_shape(M, N, K);
+    if (st != CQ_OK) return st;
+    if (M > 16) return CQ_ERR_SHAPE;
+    if (M == 0 || N == 0) return CQ_OK;
+    if (Wp == nullptr || xq == nullptr || y == nullptr) return CQ_ERR_INVALID_ARG;
+    if (!aligned16(Wp) || !aligned4(xq) || !aligned16(y)) return CQ_ERR_ALIGNMENT;
+    cq::DeviceInfo dev;
+    if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
+    const int need = cq::gemv_packed_smem(w_fmt, static_cast<int>(M), K);
+    if (need > (dev.smem_optin < 227 * 1024 ? dev.smem_optin : 227 * 1024)) return CQ_ERR_SHAPE;
+    cudaError_t e = cq::launch_gemv_packed(dev, w_fmt, static_cast<int>(M), N, K, Wp, xq, y,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+}
+
 cq_status cq_set_option(cq_option opt, int64_t value) {
     if (opt != CQ_OPT_WEIGHTS_CONST || (value != 0 && value != 1)) return CQ_ERR_INVALID_ARG;
     cq::g_weights_const.store(static_cast<int>(value), std::memory_order_relaxed);

@@ -90,6 +90,14 @@ int gemv_mma_smem(int w_fmt, int M, int64_t K);
 cudaError_t launch_gemv_mma(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                             const void* xq, float* y, cudaStream_t s);
 
+// The same kernel on weights in the packed layout of cq_repack (1 <= M <= 16),
+// the shared memory it needs at least, and the repack itself.
+int gemv_packed_smem(int w_fmt, int M, int64_t K);
+cudaError_t launch_gemv_packed(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* Wp,
+                               const void* xq, float* y, cudaStream_t s);
+int64_t repack_size(int w_fmt, int64_t N, int64_t K);
+cudaError_t launch_repack(int w_fmt, int64_t N, int64_t K, const void* W, void* Wp, cudaStream_t s);
+
 // Prefill GEMM (any M): y rows equal the cq_gemv rows bit for bit. With a
 // workspace (gemm_workspace_size bytes, 256-byte aligned) the activations are
 // converted once up front instead of in every CTA.

@@ -64,9 +64,71 @@ struct MmaParams {
     int smem_act;       // offset of the staged activations
     int smem_scale;     // offset of the per-(block, token pair) scale table
     int smem_stage;     // offset of the weight stages
+    int ngroups;        // packed weights: 16-row groups (ceil(N / 16))
 };
 
-template <int WF, int RG, int NT, int RW, int SB>
+// Packed weights (cq_repack): a unit of 16 rows x 4 blocks is 64 * BB bytes,
+// the rows' scale fields (4 * PK_SCALE bytes per row) first, then the quant
+// words, per (half, row, lane t) the words of blocks 0..3 as 16 bytes.
+template <int WF> struct Pk {
+    static constexpr int UNIT = 64 * MF<WF>::BB;
+    static constexpr int SCALE = WF == CQ_Q4_1 ? 4 : 2;     // scale bytes per block
+    static constexpr int QUANTS = 64 * SCALE;               // offset of the quant words
+};
+__device__ __forceinline__ uint32_t word(const uint4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// One unit's share of a lane for rows g and g+8 of a row group: quant words of
+// blocks 0..3 (and, Q8_0, the second halves) and the scale fields.
+template <int WF>
+struct PkRows {
+    uint4 q0, q1, q0b, q1b, s0, s1;
+    __device__ __forceinline__ void load(const uint8_t* unit, int g, int t) {
+        const uint8_t* q = unit + Pk<WF>::QUANTS + 16 * (4 * g + t);
+        q0 = *reinterpret_cast<const uint4*>(q);
+        q1 = *reinterpret_cast<const uint4*>(q + 16 * 32);
+        if constexpr (WF == CQ_Q8_0) {
+            q0b = *reinterpret_cast<const uint4*>(q + 1024);
+            q1b = *reinterpret_cast<const uint4*>(q + 1024 + 16 * 32);
+        }
+        if constexpr (WF == CQ_Q4_1) {
+            s0 = *reinterpret_cast<const uint4*>(unit + 16 * g);
+            s1 = *reinterpret_cast<const uint4*>(unit + 16 * (g + 8));
+        } else {
+            const uint2 a = *reinterpret_cast<const uint2*>(unit + 8 * g);
+            const uint2 b = *reinterpret_cast<const uint2*>(unit + 8 * (g + 8));
+            s0 = make_uint4(a.x, a.y, 0, 0);
+            s1 = make_uint4(b.x, b.y, 0, 0);
+        }
+    }
+    // Block j's A fragments and (v, v) scale pairs, as mf::weight_frags gives them.
+    __device__ __forceinline__ void frags(int j, uint32_t (&a0)[4], uint32_t (&a1)[4], uint64_t& dw0, uint64_t& dw1,
+                                          uint64_t& mw0, uint64_t& mw1) const {
+        uint32_t qb0 = 0, qb1 = 0;
+        if constexpr (WF == CQ_Q8_0) {
+            qb0 = word(q0b, j);
+            qb1 = word(q1b, j);
+        }
+        mf::a_frags<WF>(word(q0, j), word(q1, j), qb0, qb1, a0, a1);
+        if constexpr (WF == CQ_Q4_1) {
+            const uint32_t dm0 = word(s0, j), dm1 = word(s1, j);
+            const float d0 = h2f(dm0), d1 = h2f(dm1), m0 = h2f(dm0 >> 16), m1 = h2f(dm1 >> 16);
+            dw0 = tc::pk(d0, d0);
+            dw1 = tc::pk(d1, d1);
+            mw0 = tc::pk(m0, m0);
+            mw1 = tc::pk(m1, m1);
+        } else {
+            const uint32_t w0 = word(s0, j >> 1), w1 = word(s1, j >> 1);
+            const float d0 = h2f(j & 1 ? w0 >> 16 : w0), d1 = h2f(j & 1 ? w1 >> 16 : w1);
+            dw0 = tc::pk(d0, d0);
+            dw1 = tc::pk(d1, d1);
+            mw0 = mw1 = 0;
+        }
+    }
+};
+
+template <int WF, int RG, int NT, int RW, int SB, bool PK>
 __global__ void __launch_bounds__((RG + 1) * 32, 1)
     gemv_mma_kernel(const __grid_constant__ CUtensorMap wmap, const MmaParams p) {
     pdl_trigger();
@@ -77,7 +139,9 @@ __global__ void __launch_bounds__((RG + 1) * 32, 1)
     constexpr int ROWS = 16 * RW * RG;
     constexpr int NBOX = (ROWS + 255) / 256;      // TMA boxes per stage
     static_assert(ROWS % NBOX == 0, "tile rows split evenly into boxes");
-    static_assert(seg_pitch(F::BB, SB) % 16 == 0, "a stage row is a whole number of 16-byte units");
+    static_assert(PK || seg_pitch(F::BB, SB) % 16 == 0, "a stage row is a whole number of 16-byte units");
+    static_assert(!PK || (SB == 4 && RW * RG * 16 == ROWS), "packed stages are one unit per row group");
+    constexpr int GPT = ROWS / 16;                // 16-row groups per tile
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + MAX_STAGES;
@@ -93,6 +157,17 @@ __global__ void __launch_bounds__((RG + 1) * 32, 1)
         const int st = static_cast<int>(k % S);
         const int tile = blockIdx.x + static_cast<int>(k / nseg) * gridDim.x;
         const int seg = static_cast<int>(k % nseg);
+        if constexpr (PK) {
+            // the tile's groups of segment seg are one contiguous range
+            const int g0 = tile * GPT;
+            const int ng = min(GPT, p.ngroups - g0);
+            const uint32_t bytes = static_cast<uint32_t>(ng * Pk<WF>::UNIT);
+            mbar_arrive_expect_tx(&full[st], bytes);
+            bulk_g2s(smem + p.smem_stage + st * p.stage_bytes,
+                     p.W + (static_cast<int64_t>(seg) * p.ngroups + g0) * Pk<WF>::UNIT, bytes, &full[st],
+                     policy_evict_first());
+            return;
+        }
         mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(p.stage_bytes));
         // x counts 2-byte elements of the row; a box holds at most 256 rows
 #pragma unroll
@@ -174,6 +249,12 @@ __global__ void __launch_bounds__((RG + 1) * 32, 1)
                     break;
                 }
                 const uint8_t* r0p = smem + p.smem_stage + st * p.stage_bytes + (16 * RW * warp + g) * seg_row_bytes;
+                PkRows<WF> pk[PK ? RW : 1];
+                if constexpr (PK) {
+#pragma unroll
+                    for (int r = 0; r < RW; ++r)
+                        pk[r].load(smem + p.smem_stage + st * p.stage_bytes + (RW * warp + r) * Pk<WF>::UNIT, g, t);
+                }
 #pragma unroll 4
                 for (int bi = 0; bi < SB; ++bi) {
                     const int b = seg * SB + bi;                  // block index along K
@@ -181,9 +262,13 @@ __global__ void __launch_bounds__((RG + 1) * 32, 1)
                     uint64_t dw0[RW], dw1[RW], mw0[RW], mw1[RW];
 #pragma unroll
                     for (int r = 0; r < RW; ++r) {
-                        const uint8_t* wr = r0p + 16 * r * seg_row_bytes + bi * F::BB;
-                        mf::weight_frags<WF>(wr, wr + 8 * seg_row_bytes, t, a0[r], a1[r], dw0[r], dw1[r], mw0[r],
-                                             mw1[r]);
+                        if constexpr (PK) {
+                            pk[r].frags(bi, a0[r], a1[r], dw0[r], dw1[r], mw0[r], mw1[r]);
+                        } else {
+                            const uint8_t* wr = r0p + 16 * r * seg_row_bytes + bi * F::BB;
+                            mf::weight_frags<WF>(wr, wr + 8 * seg_row_bytes, t, a0[r], a1[r], dw0[r], dw1[r], mw0[r],
+                                                 mw1[r]);
+                        }
                     }
                     if ((b & 3) == 0) {
 #pragma unroll
@@ -285,14 +370,18 @@ MmaSmem mma_smem(int bb, int M, int64_t K, int rows, int sb) {
 // 8 x 16 (two row groups per warp at 16 tokens leave too few warps). The
 // 128256-row LM head gets 2 tiles of 448 rows per SM, the same 896 rows as 7
 // tiles of 128.
+// Packed weights (one 4-block unit per row group and stage) take the same
+// shapes with 4-block stages for every format.
 struct TileShape {
     int rg, rw, sb;
     int rows() const { return 16 * rg * rw; }
 };
-TileShape choose_tile(int bb, int M, int64_t N, int64_t K, int sms, int lim) {
+TileShape choose_tile(int bb, int M, int64_t N, int64_t K, int sms, int lim, bool pk) {
     const TileShape cand1[] = {{14, 2, bb == 20 ? 4 : 8}, {7, 2, 8}, {8, 1, 8}};
     const TileShape cand2[] = {{12, 1, 8}, {8, 1, 8}};
-    const TileShape* cand = M <= 8 ? cand1 : cand2;
+    const TileShape pk1[] = {{14, 2, 4}, {7, 2, 4}, {8, 1, 4}};
+    const TileShape pk2[] = {{12, 1, 4}, {8, 1, 4}};
+    const TileShape* cand = pk ? (M <= 8 ? pk1 : pk2) : (M <= 8 ? cand1 : cand2);
     const int nc = M <= 8 ? 3 : 2;
     const int min_stages = M <= 8 ? 3 : 2;
     auto rows_per_cta = [&](int rows) {
@@ -310,23 +399,21 @@ TileShape choose_tile(int bb, int M, int64_t N, int64_t K, int sms, int lim) {
     return cand[nc - 1];
 }
 
-template <int WF, int RG, int NT, int RW, int SB>
+template <int WF, int RG, int NT, int RW, int SB, bool PK = false>
 cudaError_t launch_mma_typed(const DeviceInfo& dev, MmaParams p, const CUtensorMap& map, cudaStream_t s) {
     const int smem = p.smem_stage + p.stages * p.stage_bytes;
-    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemv_mma_kernel<WF, RG, NT, RW, SB>),
+    const cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(gemv_mma_kernel<WF, RG, NT, RW, SB, PK>),
                                            std::min(dev.smem_optin, 227 * 1024));
     if (e != cudaSuccess) return e;
     const int tiles = (p.N + 16 * RW * RG - 1) / (16 * RW * RG);
     const int grid = std::min(tiles, dev.sm_count);
-    return launch_kernel(gemv_mma_kernel<WF, RG, NT, RW, SB>, dim3(grid), dim3((RG + 1) * 32), smem, s, map, p);
+    return launch_kernel(gemv_mma_kernel<WF, RG, NT, RW, SB, PK>, dim3(grid), dim3((RG + 1) * 32), smem, s, map, p);
 }
 
 template <int WF>
 cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, const void* W, const void* xq,
-                           float* y, cudaStream_t s) {
+                           float* y, bool pk, cudaStream_t s) {
     using F = MF<WF>;
-    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
-    if (enc == nullptr) return cudaErrorNotSupported;
     MmaParams p{};
     p.W = static_cast<const uint8_t*>(W);
     p.xq = static_cast<const uint8_t*>(xq);
@@ -339,7 +426,7 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
     p.wrow = static_cast<int64_t>(p.nb) * F::BB;
     const int NT = M <= 8 ? 1 : 2;
     const int lim = std::min(dev.smem_optin, 227 * 1024);
-    const TileShape T = choose_tile(F::BB, M, N, K, dev.sm_count, lim);
+    const TileShape T = choose_tile(F::BB, M, N, K, dev.sm_count, lim, pk);
     const MmaSmem L = mma_smem(F::BB, M, K, T.rows(), T.sb);
     p.act_pitch = L.act_pitch;
     p.stage_bytes = L.stage_bytes;
@@ -348,6 +435,19 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
     p.smem_stage = L.stage;
     p.stages = std::min(MAX_STAGES, (lim - L.fixed) / L.stage_bytes);
     if (p.stages < 2) return cudaErrorInvalidConfiguration;
+    if (pk) {
+        // packed weights: each stage is one bulk copy, no tensor map
+        p.ngroups = static_cast<int>((N + 15) / 16);
+        const CUtensorMap none{};
+        if (NT == 2)
+            return T.rg == 12 ? launch_mma_typed<WF, 12, 2, 1, 4, true>(dev, p, none, s)
+                              : launch_mma_typed<WF, 8, 2, 1, 4, true>(dev, p, none, s);
+        if (T.rg == 14) return launch_mma_typed<WF, 14, 1, 2, 4, true>(dev, p, none, s);
+        return T.rw == 2 ? launch_mma_typed<WF, 7, 1, 2, 4, true>(dev, p, none, s)
+                         : launch_mma_typed<WF, 8, 1, 1, 4, true>(dev, p, none, s);
+    }
+    tc::EncodeTiledFn enc = tc::encode_tiled_fn();
+    if (enc == nullptr) return cudaErrorNotSupported;
     // Raw weights as a 2-D tensor of 2-byte elements [N rows][wrow/2]; a box is
     // SB blocks of one tile's rows.
     CUtensorMap map;
@@ -387,9 +487,26 @@ int gemv_mma_smem(int w_fmt, int M, int64_t K) {
 cudaError_t launch_gemv_mma(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* W,
                             const void* xq, float* y, cudaStream_t s) {
     switch (w_fmt) {
-    case CQ_Q4_0: return launch_mma_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q4_1: return launch_mma_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, s);
-    case CQ_Q8_0: return launch_mma_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, s);
+    case CQ_Q4_0: return launch_mma_fmt<CQ_Q4_0>(dev, M, N, K, W, xq, y, false, s);
+    case CQ_Q4_1: return launch_mma_fmt<CQ_Q4_1>(dev, M, N, K, W, xq, y, false, s);
+    case CQ_Q8_0: return launch_mma_fmt<CQ_Q8_0>(dev, M, N, K, W, xq, y, false, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int gemv_packed_smem(int w_fmt, int M, int64_t K) {
+    if (w_fmt != CQ_Q4_0 && w_fmt != CQ_Q4_1 && w_fmt != CQ_Q8_0) return 0;
+    const int bb = w_fmt == CQ_Q4_0 ? 18 : w_fmt == CQ_Q4_1 ? 20 : 34;
+    const MmaSmem L = mma_smem(bb, M, K, 128, 4);
+    return L.fixed + 2 * L.stage_bytes;
+}
+
+cudaError_t launch_gemv_packed(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int64_t K, const void* Wp,
+                               const void* xq, float* y, cudaStream_t s) {
+    switch (w_fmt) {
+    case CQ_Q4_0: return launch_mma_fmt<CQ_Q4_0>(dev, M, N, K, Wp, xq, y, true, s);
+    case CQ_Q4_1: return launch_mma_fmt<CQ_Q4_1>(dev, M, N, K, Wp, xq, y, true, s);
+    case CQ_Q8_0: return launch_mma_fmt<CQ_Q8_0>(dev, M, N, K, Wp, xq, y, true, s);
     default: return cudaErrorInvalidValue;
     }
 }

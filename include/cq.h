@@ -168,6 +168,49 @@ cq_status cq_gemv_swiglu(cq_format w_fmt, int64_t M, int64_t F, int64_t K, const
                          const void* W_up, const void* xq, float* h, void* stream);
 
 /*
+ * Offline weight repack for the batched decode path (cera README "Qualcomm
+ * Hexagon" -> "Accelerated Kernels": weights repacked into tiles once, at
+ * load; alice-llm docs "Phase 6 -> Block-Packed Weight Layout": rows
+ * interleaved so that one load serves several rows; ggml's "repacked" CPU
+ * kernels). w_fmt in {Q4_0, Q4_1, Q8_0}; W: N rows of K/32 blocks (GGUF
+ * order), DEVICE, 16-byte aligned; Wp: cq_repack_size(w_fmt, N, K) bytes of
+ * DEVICE memory, 16-byte aligned, owned by the caller (0 from cq_repack_size
+ * for another format or a K that is not a positive multiple of 256).
+ *
+ * The packed layout, byte for byte (BB = 18, 20, 34 bytes per block):
+ *   - rows in groups of 16 (G = 0 .. ceil(N/16) - 1; rows >= N are zero),
+ *     K in segments of 4 blocks (s = 0 .. K/128 - 1);
+ *   - the unit (G, s) is 64 * BB bytes at byte (s * ceil(N/16) + G) * 64 * BB
+ *     (segment-major: the units of one segment for consecutive groups are
+ *     one contiguous range);
+ *   - inside a unit, for row r = 0..15 of the group: the scale fields of
+ *     blocks j = 0..3 of the segment, in block order (Q4_1: d then m, 4 bytes
+ *     per block, 16 per row; Q4_0 / Q8_0: d, 2 bytes per block, 8 per row);
+ *   - then, at 64 * (4 or 2) bytes, for half h (Q8_0: 0 and 1; Q4_0 / Q4_1: 0),
+ *     row r, lane t = 0..3, block j = 0..3: bytes 16h + 4t .. 16h + 4t + 3 of
+ *     block j's quant array (4 bytes each; 16 bytes per (h, r, t)).
+ * Total ceil(N/16) * 16 * K/32 * BB bytes: the GGUF bytes plus the zero rows.
+ * Asynchronous on `stream`; W is not modified. Errors: CQ_ERR_UNSUPPORTED_FORMAT,
+ * CQ_ERR_SHAPE (as cq_gemv), CQ_ERR_INVALID_ARG, CQ_ERR_ALIGNMENT, CQ_ERR_CUDA.
+ */
+size_t cq_repack_size(cq_format w_fmt, int64_t N, int64_t K);
+cq_status cq_repack(cq_format w_fmt, int64_t N, int64_t K, const void* W, void* Wp, void* stream);
+
+/*
+ * cq_gemv on repacked weights: Wp as cq_repack wrote it from an N x K matrix
+ * W of w_fmt (Q4_0, Q4_1, Q8_0), 16-byte aligned. y equals cq_gemv(W) bit for
+ * bit (the same fixed order). 1 <= M <= 16 (M > 16: CQ_ERR_SHAPE). The
+ * kernel keeps the tokens' activations in shared memory: CQ_ERR_SHAPE when
+ * they and two weight stages do not fit, which every format avoids for K up
+ * to 10752 at M <= 8 and up to 5376 at M <= 16. Each stage of the
+ * weight stream is one contiguous bulk copy, and each lane reads its quants of
+ * four blocks in one 16-byte load instead of one or three loads per block.
+ * Errors as cq_gemv.
+ */
+cq_status cq_gemv_packed(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* Wp, const void* xq,
+                         float* y, void* stream);
+
+/*
  * Prefill GEMM, any M >= 0 (cera README "Supported models": batched-GEMM
  * prefill; alice-llm "Computation Path (Q4_K)"). Same operands and result as
  * cq_gemv; each row equals the cq_gemv result for that token bit for bit.

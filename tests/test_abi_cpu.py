@@ -211,3 +211,29 @@ def test_library_reads_no_environment():
     for name in sorted(os.listdir(csrc)):
         text = open(os.path.join(csrc, name)).read()
         assert "getenv" not in text and "secure_getenv" not in text, name
+
+
+def test_repack_validation(L):
+    assert cq.cq_repack_size(cq.Q4_0, 16, 256) == 16 * 8 * 18
+    assert cq.cq_repack_size(cq.Q4_1, 17, 256) == 32 * 8 * 20       # rows padded to 16
+    assert cq.cq_repack_size(cq.Q8_0, 1, 512) == 16 * 16 * 34
+    assert cq.cq_repack_size(cq.Q4_K, 16, 256) == 0
+    assert cq.cq_repack_size(cq.Q4_0, 16, 100) == 0
+    f = cq.cq_repack
+    assert f(cq.Q4_K, 16, 256, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q4_0, 16, 100, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q4_0, -1, 256, A, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_0, 16, 256, None, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_0, 16, 256, A, None) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_0, 16, 256, A + 2, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_0, 16, 256, A, A + 8) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_0, 0, 256, None, None) == cq.OK
+    g = cq.cq_gemv_packed
+    assert g(cq.Q4_K, 1, 8, 256, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert g(cq.Q4_1, 17, 8, 256, A, A, A) == cq.ERR_SHAPE
+    assert g(cq.Q4_1, 1, 8, 100, A, A, A) == cq.ERR_SHAPE
+    assert g(cq.Q4_1, 1, 8, 256, None, A, A) == cq.ERR_INVALID_ARG
+    assert g(cq.Q4_1, 1, 8, 256, A + 4, A, A) == cq.ERR_ALIGNMENT
+    assert g(cq.Q4_1, 1, 8, 256, A, A + 2, A) == cq.ERR_ALIGNMENT
+    assert g(cq.Q4_1, 1, 8, 256, A, A, A + 4) == cq.ERR_ALIGNMENT
+    assert g(cq.Q4_1, 0, 8, 256, None, None, None) == cq.OK
