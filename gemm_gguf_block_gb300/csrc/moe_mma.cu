@@ -11,9 +11,10 @@
 // projection the gate and up rows of the same f land in one stage); the
 // pairs' 272-byte Q8_0 activation segments arrive in the same stage, four
 // rows per TMA gather4 (64 single copies per segment cost as much as the
-// rest of the weight stream), then are converted to fp16 in shared memory. Per 32-block the integer dot is an exact fp16
-// mma.sync m16n8k16 product (two chained k-steps; every partial sum is an
-// integer below 2^23), and the block's scale term is accumulated as
+// rest of the weight stream), then are converted to fp16 in shared memory.
+// Per 32-block the integer dot is an exact fp16 mma.sync m16n8k16 product
+// (two chained k-steps on the fragments of mma_frag.cuh; every partial sum is
+// an integer below 2^23), and the block's scale term is accumulated as
 // y = fma(d_w * d_x, isum, y) in increasing k.
 //   up:   warp w computes gate and up rows f0+16w.. for the pairs; the CTA
 //         then writes h = silu(g) * u (fp32) and its Q8_0 blocks hq for the
@@ -25,6 +26,7 @@
 
 #include "cq_device.cuh"
 #include "cq_internal.h"
+#include "mma_frag.cuh"
 #include "tc.cuh"
 
 namespace cq {
@@ -68,8 +70,6 @@ struct MoeMmaParams {
     int stages;
 };
 
-__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 // D = A * B + C (C given), and D += A * B.
 __device__ __forceinline__ void mma16816c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
@@ -86,21 +86,6 @@ __device__ __forceinline__ void mma16816acc(float (&d)[4], const uint32_t (&a)[4
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Q4_0 nibbles n of two bytes as half2 (1024 + n): the low nibbles (elements
-// j, j+1 of the block) and the high ones (j+16, j+17). 1024 + n is exact in
-// binary16 and costs no subtraction; the offset 1024 + 8 per element comes
-// back out through the accumulator's starting value, -1032 * sum(x).
-__device__ __forceinline__ void q4_biased(uint32_t two_bytes, uint32_t& lo, uint32_t& hi) {
-    const uint32_t p = __byte_perm(two_bytes, 0u, 0x4140);
-    lo = (p & 0x000F000Fu) | 0x64006400u;
-    hi = ((p >> 4) & 0x000F000Fu) | 0x64006400u;
-}
-// Four signed bytes as two half2.
-__device__ __forceinline__ void s8x4_to_half(uint32_t w, uint32_t& o0, uint32_t& o1) {
-    o0 = h2u(__hsub2(u2h((__byte_perm(w, 0u, 0x4140) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
-    o1 = h2u(__hsub2(u2h((__byte_perm(w, 0u, 0x4342) ^ 0x00800080u) | 0x64006400u), u2h(0x64806480u)));
 }
 
 struct Smem {
@@ -120,56 +105,29 @@ __device__ __forceinline__ int chunk_pos(int b, int c) { return 64 * b + 16 * (c
 
 // Converts the stage's raw Q8_0 segments (272 bytes per pair, pairs past np
 // read as zero) for the first 8 * NT pairs: item = (token it / 8, block it % 8).
-// Chunk c of a block holds k = [2c, 2c+1 | 2c+8, 2c+9 | 16+2c, 17+2c | 24+2c, 25+2c],
-// the order lane t = c of an m16n8k16 B fragment reads with one 16-byte load.
+// Chunk c of a block is lane c's B fragments of both k-steps in the order of
+// mma_frag.cuh (mf::act_frags: the Q4_0 weights' high nibbles are masked in
+// place, so the k-step 1 half is scaled by 1/16), and the bias is the
+// accumulator's start for the weights' BIAS + v encoding.
 template <int NT>
 __device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, int np, int ct) {
     float* bqf = reinterpret_cast<float*>(sm.bq);
     float* dxf = reinterpret_cast<float*>(sm.dx);
     for (int it = ct; it < 8 * NT * SEGB; it += CONSUMERS * 32) {
         const int tk = it >> 3, b = it & 7;
-        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        float d = 0.0f;
-        int sx = 0;
-        if (tk < np) {
-            const uint16_t* src = reinterpret_cast<const uint16_t*>(raw + raw_off(tk) + b * 34);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                w[j] = static_cast<uint32_t>(src[1 + 2 * j]) | (static_cast<uint32_t>(src[2 + 2 * j]) << 16);
-                sx = __dp4a(static_cast<int>(w[j]), 0x01010101, sx);
-            }
-            d = h2f(src[0]);
-        }
-        uint32_t hv[16];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s8x4_to_half(w[j], hv[2 * j], hv[2 * j + 1]);
+        uint4 ch[4] = {};
+        float d = 0.0f, unused;
+        int ibias = 0;
+        if (tk < np) mf::act_frags<CQ_Q4_0>(raw + raw_off(tk) + b * 34, ch, d, unused, ibias);
         uint8_t* row = sm.act + tk * ACT_PITCH;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(row + chunk_pos(b, c)) = make_uint4(hv[c], hv[c + 4], hv[c + 8], hv[c + 12]);
+        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(row + chunk_pos(b, c)) = ch[c];
         const int j = b * SCL_PITCH + (tk >> 1), hi = tk & 1;
-        const float bias = static_cast<float>(-1032 * sx);
+        const float bias = static_cast<float>(ibias);
         bqf[4 * j + hi] = bias;
         bqf[4 * j + 2 + hi] = bias;
         dxf[2 * j + hi] = d;
     }
-}
-
-// Row g and g + 8 of a 16-row slice, one 32-block: the two k-steps' A
-// fragments (1024 + n) and the rows' d_w as (d, d) pairs.
-__device__ __forceinline__ void load_wfrag(const uint8_t* w0, int t, uint32_t (&f0)[4], uint32_t (&f1)[4],
-                                           uint64_t& d0, uint64_t& d1) {
-    const uint8_t* w1 = w0 + 8 * (SEGB * 18);
-    const uint16_t* q0 = reinterpret_cast<const uint16_t*>(w0 + 2);
-    const uint16_t* q1 = reinterpret_cast<const uint16_t*>(w1 + 2);
-    q4_biased(q0[t], f0[0], f1[0]);
-    q4_biased(q1[t], f0[1], f1[1]);
-    q4_biased(q0[t + 4], f0[2], f1[2]);
-    q4_biased(q1[t + 4], f0[3], f1[3]);
-    const float a = h2f(*reinterpret_cast<const uint16_t*>(w0));
-    const float c = h2f(*reinterpret_cast<const uint16_t*>(w1));
-    d0 = tc::pk(a, a);
-    d1 = tc::pk(c, c);
 }
 
 // One pass over the expert's K for up to 8 * NT pairs. Accumulators hold
@@ -197,12 +155,16 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
         convert_acts<NT>(stage + NMAT * BOX_BYTES, sm, np, ct);
         tc::named_and(1, CONSUMERS * 32, true);
         const uint8_t* wa = stage + (16 * warp + g) * (SEGB * 18);
-#pragma unroll 1
+#pragma unroll 2
         for (int b = 0; b < SEGB; ++b) {
             uint32_t fa0[4], fa1[4], fb0[4], fb1[4];
-            uint64_t dwa0, dwa1, dwb0 = 0, dwb1 = 0;
-            load_wfrag(wa + b * 18, t, fa0, fa1, dwa0, dwa1);
-            if constexpr (UP) load_wfrag(wa + BOX_BYTES + b * 18, t, fb0, fb1, dwb0, dwb1);
+            uint64_t dwa0, dwa1, dwb0 = 0, dwb1 = 0, m_unused[2];
+            constexpr int RB = SEGB * 18;     // bytes per weight row in a stage
+            mf::weight_frags<CQ_Q4_0>(wa + b * 18, wa + 8 * RB + b * 18, t, fa0, fa1, dwa0, dwa1, m_unused[0],
+                                      m_unused[1]);
+            if constexpr (UP)
+                mf::weight_frags<CQ_Q4_0>(wa + BOX_BYTES + b * 18, wa + BOX_BYTES + 8 * RB + b * 18, t, fb0, fb1,
+                                          dwb0, dwb1, m_unused[0], m_unused[1]);
             const uint8_t* ab = sm.act + g * ACT_PITCH + chunk_pos(b, t);
             const float4* sq = sm.bq + b * SCL_PITCH + t;
             const float2* sd = sm.dx + b * SCL_PITCH + t;
