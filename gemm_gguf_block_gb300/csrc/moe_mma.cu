@@ -41,13 +41,13 @@ constexpr int BOX_BYTES = ROWS * SEGB * 18;        // one matrix, one segment: 1
 constexpr int ACT_PITCH = 512 + 64;                 // bytes per token per segment (fp16) + pad:
                                                     // 36 x 16 B, so lanes' 16-byte reads miss each other's banks
 constexpr int ACT_BYTES = TOK * ACT_PITCH;          // 36864
-// Scale tables, per (32-block b, token pair j), pitch 33 entries per block so
-// the converters' stores spread over banks: the accumulator biases as the
-// quad {bias[2j], bias[2j+1], bias[2j], bias[2j+1]} -- the mma's C fragment
-// as loaded, four consecutive registers -- and the scales {d_x[2j], d_x[2j+1]}.
+// Scale records, per (32-block b, token pair j), pitch 33 records per block
+// so the converters' stores spread over banks: {d_x[2j], d_x[2j+1], bias[2j],
+// bias[2j+1]}, one 16-byte load per lane and n-tile (the scales as an f32x2
+// pair, the biases for the mma's C fragment). One record measured 2% faster
+// than a bias quad and a separate scale pair.
 constexpr int SCL_PITCH = TOK / 2 + 1;
-constexpr int BQ_BYTES = SEGB * SCL_PITCH * 16;     // 4224
-constexpr int SCL_BYTES = (BQ_BYTES + SEGB * SCL_PITCH * 8 + 127) / 128 * 128;   // keeps the stages 128-byte aligned
+constexpr int SCL_BYTES = (SEGB * SCL_PITCH * 16 + 127) / 128 * 128;   // 4224: keeps the stages 128-byte aligned
 constexpr int RAWA = SEGB * 34;                     // one token's Q8_0 segment: 272 bytes
 // The pairs' raw segments arrive four at a time (one TMA gather4 of four
 // activation rows); each group of four starts on a 128-byte boundary.
@@ -93,8 +93,7 @@ struct Smem {
     uint64_t* empty;
     int* pairs;        // [TOK] pair ids of the pass
     uint8_t* act;      // [TOK][ACT_PITCH] fp16 activations of one segment
-    float4* bq;        // [SEGB][SCL_PITCH] accumulator bias quads
-    float2* dx;        // [SEGB][SCL_PITCH] activation scale pairs
+    float4* sq;        // [SEGB][SCL_PITCH] scale records
     uint8_t* wst;      // [stages][stage bytes]
 };
 
@@ -111,8 +110,7 @@ __device__ __forceinline__ int chunk_pos(int b, int c) { return 64 * b + 16 * (c
 // accumulator's start for the weights' BIAS + v encoding.
 template <int NT>
 __device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, int np, int ct) {
-    float* bqf = reinterpret_cast<float*>(sm.bq);
-    float* dxf = reinterpret_cast<float*>(sm.dx);
+    float* sqf = reinterpret_cast<float*>(sm.sq);
     for (int it = ct; it < 8 * NT * SEGB; it += CONSUMERS * 32) {
         const int tk = it >> 3, b = it & 7;
         uint4 ch[4] = {};
@@ -124,9 +122,8 @@ __device__ __forceinline__ void convert_acts(const uint8_t* raw, const Smem sm, 
         for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(row + chunk_pos(b, c)) = ch[c];
         const int j = b * SCL_PITCH + (tk >> 1), hi = tk & 1;
         const float bias = static_cast<float>(ibias);
-        bqf[4 * j + hi] = bias;
-        bqf[4 * j + 2 + hi] = bias;
-        dxf[2 * j + hi] = d;
+        sqf[4 * j + hi] = d;
+        sqf[4 * j + 2 + hi] = bias;
     }
 }
 
@@ -155,7 +152,7 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
         convert_acts<NT>(stage + NMAT * BOX_BYTES, sm, np, ct);
         tc::named_and(1, CONSUMERS * 32, true);
         const uint8_t* wa = stage + (16 * warp + g) * (SEGB * 18);
-#pragma unroll 2
+#pragma unroll 4
         for (int b = 0; b < SEGB; ++b) {
             uint32_t fa0[4], fa1[4], fb0[4], fb1[4];
             uint64_t dwa0, dwa1, dwb0 = 0, dwb1 = 0, m_unused[2];
@@ -166,14 +163,13 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
                 mf::weight_frags<CQ_Q4_0>(wa + BOX_BYTES + b * 18, wa + BOX_BYTES + 8 * RB + b * 18, t, fb0, fb1,
                                           dwb0, dwb1, m_unused[0], m_unused[1]);
             const uint8_t* ab = sm.act + g * ACT_PITCH + chunk_pos(b, t);
-            const float4* sq = sm.bq + b * SCL_PITCH + t;
-            const float2* sd = sm.dx + b * SCL_PITCH + t;
+            const float4* sq = sm.sq + b * SCL_PITCH + t;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 const uint4 bv = *reinterpret_cast<const uint4*>(ab + 8 * n * ACT_PITCH);
-                const float4 bias = sq[4 * n];
-                const float2 dv = sd[4 * n];
-                const uint64_t dx = tc::pk(dv.x, dv.y);
+                const float4 r4 = sq[4 * n];
+                const uint64_t dx = tc::pk(r4.x, r4.y);
+                const float4 bias = make_float4(r4.z, r4.w, r4.z, r4.w);
                 float c[4];
                 mma16816c(c, fa0, bv.x, bv.y, bias);
                 mma16816acc(c, fa1, bv.z, bv.w);
@@ -274,8 +270,7 @@ __global__ void __launch_bounds__(THREADS, 1) moe_mma_kernel(const __grid_consta
     sm.empty = sm.full + 8;
     sm.pairs = reinterpret_cast<int*>(smem + 256);
     sm.act = smem + 1024;
-    sm.bq = reinterpret_cast<float4*>(sm.act + ACT_BYTES);
-    sm.dx = reinterpret_cast<float2*>(sm.act + ACT_BYTES + BQ_BYTES);
+    sm.sq = reinterpret_cast<float4*>(sm.act + ACT_BYTES);
     sm.wst = smem + 1024 + ACT_BYTES + SCL_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = p.order[blockIdx.y], r0 = blockIdx.x * ROWS;
