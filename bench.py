@@ -356,7 +356,8 @@ def rotated_graph_us(torch, make_call, nbytes, launches_min=60, reps=5):
 
 def case_gemm(c, cq, synth, peaks, seed):
     """Prefill GEMM: Q4_K, M=512, K=4096, N=14336, through cq_gemm_ws (activations
-    converted once into a workspace) and through cq_gemm (converted per tile)."""
+    converted once into the caller's workspace), cq_gemm (the same with a
+    workspace from the library's pool) and cq_gemm_noalloc (converted per tile)."""
     W, x = synth.prefill_q4_k(seed)
     M, K = x.shape
     N = W.shape[0]
@@ -368,17 +369,20 @@ def case_gemm(c, cq, synth, peaks, seed):
     ms = c.time(lambda: cq.cq_gemm_ws(cq.Q4_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), ws.data_ptr(),
                                       need, c.stream()))
     ms_plain = c.time(lambda: cq.cq_gemm(cq.Q4_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(), c.stream()))
+    ms_na = c.time(lambda: cq.cq_gemm_noalloc(cq.Q4_K, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                              c.stream()))
     tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
     return {"shape": f"M={M} N={N} K={K}", "call": "cq_gemm_ws", "ms": ms, "int8_equiv_tops": tops,
             "peak_tflops": peaks["bf16"], "peak_note": "fp16 tensor peak = measured bf16 x 1",
             "frac": tops / peaks["bf16"], "cq_gemm_ms": ms_plain,
-            "cq_gemm_tops": 2.0 * M * N * K / (ms_plain * 1e-3) / 1e12}
+            "cq_gemm_tops": 2.0 * M * N * K / (ms_plain * 1e-3) / 1e12, "cq_gemm_noalloc_ms": ms_na}
 
 
 def case_gemm_32(c, cq, synth, peaks, seed, fmts=("q8_0", "q4_0", "q4_1")):
     """Prefill GEMM of the 32-element formats (tcgen05 kernel): M=512, K=4096,
     N=14336 per format, through cq_gemm_ws (activation operand images built
-    once into a workspace) and through cq_gemm (built in every CTA)."""
+    once into a workspace), through cq_gemm (the same, workspace from the
+    library's pool) and through cq_gemm_noalloc (built in every CTA)."""
     res = {}
     for fmt in fmts:
         wfmt = cq.FMT[fmt]
@@ -394,9 +398,11 @@ def case_gemm_32(c, cq, synth, peaks, seed, fmts=("q8_0", "q4_0", "q4_1")):
                                           need, c.stream()))
         ms_plain = c.time(lambda: cq.cq_gemm(wfmt, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(),
                                              c.stream()))
+        ms_na = c.time(lambda: cq.cq_gemm_noalloc(wfmt, M, N, K, Wd.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                                  c.stream()))
         tops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
         res[fmt] = {"shape": f"M={M} N={N} K={K}", "call": "cq_gemm_ws", "ms": ms, "int8_equiv_tops": tops,
-                    "frac_of_fp16_peak": tops / peaks["bf16"], "cq_gemm_ms": ms_plain}
+                    "frac_of_fp16_peak": tops / peaks["bf16"], "cq_gemm_ms": ms_plain, "cq_gemm_noalloc_ms": ms_na}
         del Wd, xq, y, ws
     return res
 

@@ -36,6 +36,7 @@ SIGNATURES = {
     "cq_gemv_x": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "cq_gemv_swiglu": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "cq_gemm": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "cq_gemm_noalloc": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P]),
     "cq_gemm_workspace_size": (_SZ, [_I, _I64, _I64, _I64]),
     "cq_gemm_ws": (_I, [_I, _I64, _I64, _I64, _P, _P, _P, _P, _SZ, _P]),
     "cq_moe_workspace_size": (_SZ, [_I64, _I64, _I64, _I64, _I64]),
@@ -107,6 +108,10 @@ def cq_gemv_swiglu(w_fmt, M, F, K, W_gate, W_up, xq, h, stream=0):
 
 def cq_gemm(w_fmt, M, N, K, W, xq, y, stream=0):
     return lib().cq_gemm(w_fmt, M, N, K, W, xq, y, stream)
+
+
+def cq_gemm_noalloc(w_fmt, M, N, K, W, xq, y, stream=0):
+    return lib().cq_gemm_noalloc(w_fmt, M, N, K, W, xq, y, stream)
 
 
 def cq_selftest_wait_timeout(limit_ns, stream=0):
@@ -273,6 +278,15 @@ def gemm_t(W, xq, w_fmt: int, K: int, out=None):
     N, M = W.shape[0], xq.shape[0]
     y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=W.device)
     _check("cq_gemm", cq_gemm(w_fmt, M, N, K, W.data_ptr(), xq.data_ptr(), y.data_ptr(), _stream_handle()))
+    return y
+
+
+def gemm_noalloc_t(W, xq, w_fmt: int, K: int, out=None):
+    torch = _torch()
+    N, M = W.shape[0], xq.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=W.device)
+    _check("cq_gemm_noalloc", cq_gemm_noalloc(w_fmt, M, N, K, W.data_ptr(), xq.data_ptr(), y.data_ptr(),
+                                              _stream_handle()))
     return y
 
 

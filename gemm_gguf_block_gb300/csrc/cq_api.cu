@@ -67,6 +67,56 @@ cudaError_t raise_smem_limit(const void* kernel, int bytes) {
     return e;
 }
 
+// Library-owned stream-ordered scratch: one memory pool per device, created on
+// first use, keeping up to 512 MB between calls so that steady-state
+// allocations map no new memory.
+std::mutex g_pool_mutex;
+bool g_pool_ready[MAX_DEVICES];
+cudaMemPool_t g_pool[MAX_DEVICES];
+
+void* scratch_alloc(size_t bytes, cudaStream_t s) {
+    int dev = 0;
+    if (bytes == 0 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return nullptr;
+    // No allocation while the stream is being captured into a graph: the
+    // caller then takes its allocation-free path.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (cap != cudaStreamCaptureStatusNone) return nullptr;
+    cudaMemPool_t pool;
+    {
+        std::lock_guard<std::mutex> lock(g_pool_mutex);
+        if (!g_pool_ready[dev]) {
+            cudaMemPoolProps props{};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if (cudaMemPoolCreate(&g_pool[dev], &props) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return nullptr;
+            }
+            uint64_t keep = uint64_t(512) << 20;
+            (void)cudaMemPoolSetAttribute(g_pool[dev], cudaMemPoolAttrReleaseThreshold, &keep);
+            g_pool_ready[dev] = true;
+        }
+        pool = g_pool[dev];
+    }
+    void* p = nullptr;
+    if (cudaMallocFromPoolAsync(&p, bytes, pool, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if ((reinterpret_cast<uintptr_t>(p) & 255u) != 0) {   // the GEMM workspaces want 256-byte alignment
+        (void)cudaFreeAsync(p, s);
+        return nullptr;
+    }
+    return p;
+}
+
+cudaError_t scratch_free(void* p, cudaStream_t s) { return p != nullptr ? cudaFreeAsync(p, s) : cudaSuccess; }
+
 cudaError_t device_info(DeviceInfo* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -238,8 +288,11 @@ namespace {
 // take an optional workspace (cq_gemm_ws).
 bool is_gemm_fmt(int f) { return f == CQ_Q4_K || f == CQ_Q4_0 || f == CQ_Q4_1 || f == CQ_Q8_0; }
 
+// with_ws: the caller's workspace (cq_gemm_ws). Otherwise scratch = true takes
+// the workspace from the library's pool when it can (cq_gemm), and false never
+// allocates (cq_gemm_noalloc).
 cq_status gemm_common(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
-                      void* workspace, size_t workspace_bytes, bool with_ws, void* stream) {
+                      void* workspace, size_t workspace_bytes, bool with_ws, void* stream, bool scratch = false) {
     if (!is_gemm_fmt(w_fmt)) return CQ_ERR_UNSUPPORTED_FORMAT;
     cq_status st = check_shape(M, N, K);
     if (st != CQ_OK) return st;
@@ -255,9 +308,12 @@ cq_status gemm_common(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const vo
     if (cq::device_info(&dev) != cudaSuccess) return CQ_ERR_CUDA;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     void* ws = need > 0 ? workspace : nullptr;
+    void* own = !with_ws && scratch ? cq::scratch_alloc(cq::gemm_workspace_size(w_fmt, M, K), s) : nullptr;
+    if (own != nullptr) ws = own;
     const cudaError_t e = w_fmt == CQ_Q4_K ? cq::launch_gemm(dev, w_fmt, M, N, K, W, xq, y, ws, s)
                                            : cq::launch_gemm_tc32(dev, w_fmt, M, N, K, W, xq, y, ws, s);
-    return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+    const cudaError_t f = cq::scratch_free(own, s);
+    return e == cudaSuccess && f == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -266,7 +322,12 @@ extern "C" {
 
 cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
                   void* stream) {
-    return gemm_common(w_fmt, M, N, K, W, xq, y, nullptr, 0, false, stream);
+    return gemm_common(w_fmt, M, N, K, W, xq, y, nullptr, 0, false, stream, true);
+}
+
+cq_status cq_gemm_noalloc(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq, float* y,
+                          void* stream) {
+    return gemm_common(w_fmt, M, N, K, W, xq, y, nullptr, 0, false, stream, false);
 }
 
 size_t cq_gemm_workspace_size(cq_format w_fmt, int64_t M, int64_t N, int64_t K) {

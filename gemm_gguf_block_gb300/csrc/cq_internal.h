@@ -64,6 +64,13 @@ struct DeviceInfo {
 // Cached per-device properties; status address from cudaGetSymbolAddress.
 cudaError_t device_info(DeviceInfo* out);
 
+// Stream-ordered scratch from the library's per-device memory pool: bytes on
+// `s` (256-byte aligned), or nullptr when the pool cannot supply them or the
+// stream is being captured (callers then take an allocation-free path).
+// scratch_free(p, s) returns it on `s` after the work queued before it.
+void* scratch_alloc(size_t bytes, cudaStream_t s);
+cudaError_t scratch_free(void* p, cudaStream_t s);
+
 // Raises `kernel`'s dynamic shared-memory limit on the current device to at
 // least `bytes` (cudaFuncSetAttribute), once per (device, kernel); safe to
 // call from several host threads.

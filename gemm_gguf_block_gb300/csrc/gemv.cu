@@ -923,19 +923,27 @@ cudaError_t launch_gemv(const DeviceInfo& dev, int w_fmt, int M, int64_t N, int6
     // is lightest for Q8_0 (LM head 128256 x 4096: M = 2 88.2 us here against
     // 112.6 on the tensor cores, M = 3 106.5 against 112.7, M = 4 131.1
     // against 114.7; for Q4_0 and Q4_1 the tensor cores win or tie from M = 2).
-    // Q4_K with many tokens: the tcgen05 prefill GEMM (no workspace; its rows
-    // are the bits of this kernel's). Measured crossover: from M = 9 when the
-    // matrix has 8192 rows or more (14336 x 4096: 47.1 us here at M = 8, 41.0
-    // through the GEMM at M = 8..16; 128256 x 4096: 262.3 here at M = 8, 292.9
-    // through the GEMM), from M = 11 for 4096 rows, which give the GEMM only
-    // 32 row tiles (4096 x 14336: 110.6 / 131.1 us here at M = 10 / 11, 114.7 /
-    // 116.7 through the GEMM).
-    if (w_fmt == CQ_Q4_K && (M >= 11 || (M >= 9 && N >= 8192))) {
-        if (x != nullptr) {
-            const cudaError_t e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
-            if (e != cudaSuccess) return e;
+    // Q4_K with many tokens: the tcgen05 prefill GEMM (its rows are the bits of
+    // this kernel's). With the activation workspace from the library's pool the
+    // GEMM costs the same from 1 to 128 tokens (14336 x 4096: 38.0 us; 4096 x
+    // 14336: 95-97; 128256 x 4096: 202-204), and this kernel passes it at M = 7
+    // for 8192 rows or more (M = 6 / 7: 38.9 / 43.0 us and 206.8 / 225.3 here)
+    // and at M = 8 below (4096 x 14336: 90.1 / 100.4 us here at M = 7 / 8).
+    // Without a workspace (stream capture, or the pool short of memory) the
+    // GEMM converts the activations in every CTA, and the crossover measured
+    // for that is M = 9 for 8192 rows or more (14336 x 4096: 47.1 us here at
+    // M = 8, 41.0 through the GEMM) and M = 11 below (4096 x 14336: 110.6 /
+    // 131.1 us here at M = 10 / 11, 114.7 / 116.7 through the GEMM).
+    if (w_fmt == CQ_Q4_K && M >= 7) {
+        const bool tall = N >= 8192;
+        void* ws = M >= (tall ? 7 : 8) ? scratch_alloc(gemm_workspace_size(w_fmt, M, K), s) : nullptr;
+        if (ws != nullptr || M >= 11 || (M >= 9 && tall)) {
+            cudaError_t e = cudaSuccess;
+            if (x != nullptr) e = launch_quantize(afmt, M, K, x, const_cast<void*>(xq), s);
+            if (e == cudaSuccess) e = launch_gemm(dev, w_fmt, M, N, K, W, xq, y, ws, s);
+            const cudaError_t f = scratch_free(ws, s);
+            return e != cudaSuccess ? e : f;
         }
-        return launch_gemm(dev, w_fmt, M, N, K, W, xq, y, nullptr, s);
     }
     const int need = gemv_mma_smem(w_fmt, M, K);
     const bool dp4a_better = w_fmt == CQ_Q8_0 && M <= 3;

@@ -220,9 +220,27 @@ cq_status cq_gemv_packed(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const
  * the activation rows are read by TMA, so xq must be 16-byte aligned
  * (CQ_ERR_ALIGNMENT otherwise). M < 2^31. Other formats return
  * CQ_ERR_UNSUPPORTED_FORMAT.
+ * Memory: the activation workspace of cq_gemm_ws (cq_gemm_workspace_size
+ * bytes) comes from a memory pool the library owns, one per device, created
+ * on first use and keeping up to 512 MB between calls. It is allocated
+ * (cudaMallocFromPoolAsync) and freed (cudaFreeAsync) on `stream`, around the
+ * kernels. While `stream` is being captured into a graph, or when the pool
+ * cannot supply the bytes, the call runs cq_gemm_noalloc's kernels instead:
+ * same bits either way. cq_gemv routes Q4_K calls here from 7 tokens (8 for
+ * matrices of fewer than 8192 rows) when the pool supplies the workspace, and
+ * from 9 (11) tokens without it.
  */
 cq_status cq_gemm(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
                   float* y, void* stream);
+
+/*
+ * cq_gemm that never allocates: every CTA converts the activations of its
+ * token tile itself instead of reading them once converted from a workspace
+ * (slower: Q4_K 512 x 14336 x 4096 157.7 us against about 104 us). Same
+ * arguments, errors and bits as cq_gemm.
+ */
+cq_status cq_gemm_noalloc(cq_format w_fmt, int64_t M, int64_t N, int64_t K, const void* W, const void* xq,
+                          float* y, void* stream);
 
 /*
  * cq_gemm with a caller-owned device workspace: the quantized activations are

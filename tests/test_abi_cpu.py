@@ -237,3 +237,14 @@ def test_repack_validation(L):
     assert g(cq.Q4_1, 1, 8, 256, A, A + 2, A) == cq.ERR_ALIGNMENT
     assert g(cq.Q4_1, 1, 8, 256, A, A, A + 4) == cq.ERR_ALIGNMENT
     assert g(cq.Q4_1, 0, 8, 256, None, None, None) == cq.OK
+
+
+def test_gemm_noalloc_validation(L):
+    f = cq.cq_gemm_noalloc
+    assert f(99, 1, 8, 256, A, A, A) == cq.ERR_UNSUPPORTED_FORMAT
+    assert f(cq.Q4_K, 1, 8, 100, A, A, A) == cq.ERR_SHAPE
+    assert f(cq.Q4_K, -1, 8, 256, A, A, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_K, 1, 8, 256, None, A, A) == cq.ERR_INVALID_ARG
+    assert f(cq.Q4_K, 1, 8, 256, A + 4, A, A) == cq.ERR_ALIGNMENT
+    assert f(cq.Q4_0, 1, 8, 256, A, A + 4, A) == cq.ERR_ALIGNMENT        # TMA-read activations: 16 bytes
+    assert f(cq.Q4_K, 0, 8, 256, None, None, None) == cq.OK

@@ -94,7 +94,9 @@ def test_gemv_exact_arithmetic(orc, wfmt, N, K, M):
                                    (130, 96, 4096), (200, 300, 1024), (300, 200, 512), (700, 130, 256)])
 def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
     """cq_gemm (tcgen05 kernels for Q4_K and for the 32-element formats) against
-    the oracle, and each row against the single-token cq_gemv bit for bit;
+    the oracle; cq_gemm_ws and cq_gemm_noalloc (the kernels that convert the
+    activations in every CTA) give its bits; each row against the single-token
+    cq_gemv bit for bit;
     M and N ragged against the 64-token / 128-row tiles. For Q4_K the token
     tile counts 1, 2, 3 and 6 cover single CTAs (odd counts) and CTA pairs
     sharing the weight conversion (even counts, one and three pairs)."""
@@ -107,6 +109,8 @@ def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
     assert_within(y, y_ref, at, what=f"gemm fmt {wfmt}")
     y_ws = cq.gemm_ws_t(Wd, xd, wfmt, K).cpu().numpy()
     assert np.array_equal(y.view(np.uint32), y_ws.view(np.uint32)), "cq_gemm_ws differs from cq_gemm"
+    y_na = cq.gemm_noalloc_t(Wd, xd, wfmt, K).cpu().numpy()
+    assert np.array_equal(y.view(np.uint32), y_na.view(np.uint32)), "cq_gemm_noalloc differs from cq_gemm"
     for m in sorted({0, 1, M // 2, M - 1} & set(range(M))):
         y1 = cq.gemv_t(Wd, xd[m:m + 1], wfmt, K).cpu().numpy()[0]
         assert np.array_equal(y[m].view(np.uint32), y1.view(np.uint32)), f"row {m}"
@@ -115,10 +119,11 @@ def test_gemm_rows_equal_gemv(orc, wfmt, M, N, K):
         assert np.array_equal(y[:16].view(np.uint32), y16.view(np.uint32)), "batched GEMV rows differ"
 
 
-@pytest.mark.parametrize("N,Ms", [(8200, (8, 9)), (300, (10, 11))])
+@pytest.mark.parametrize("N,Ms", [(8200, (6, 7, 8, 9)), (300, (7, 8, 10, 11))])
 def test_q4k_many_token_gemv_route(orc, N, Ms):
-    """cq_gemv sends Q4_K calls with many tokens to the prefill GEMM (from M = 9
-    when N >= 8192, from M = 11 below): both sides of each switch give the
+    """cq_gemv sends Q4_K calls with many tokens to the prefill GEMM (with the
+    library's pooled workspace from M = 7 when N >= 8192 and from M = 8 below;
+    without one from M = 9 and M = 11): both sides of each switch give the
     single-token rows bit for bit and agree with the oracle."""
     torch = torch_cuda()
     cq = cq_built()
