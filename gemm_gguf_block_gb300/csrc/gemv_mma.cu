@@ -385,7 +385,10 @@ TileShape choose_tile(int bb, int M, int64_t N, int64_t K, int sms, int lim, boo
     const TileShape pk2[] = {{7, 2, 4}, {12, 1, 4}, {8, 1, 4}};
     const TileShape* cand = pk ? (M <= 8 ? pk1 : pk2) : (M <= 8 ? cand1 : cand2);
     const int nc = 3;
-    const int min_stages = M <= 8 ? 3 : 2;
+    // Three stages up to 8 tokens, except for Q8_0, whose 272-byte rows fit
+    // only two of the 7 x 32 tile: two of those measured faster than three of
+    // 8 x 16 (LM head M = 4: 110.5 against 114.6 us).
+    const int min_stages = M <= 8 && bb != 34 ? 3 : 2;
     auto rows_per_cta = [&](int rows) {
         const int64_t tiles = (N + rows - 1) / rows;
         return (tiles + sms - 1) / sms * rows;
