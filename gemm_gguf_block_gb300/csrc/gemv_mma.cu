@@ -366,12 +366,13 @@ MmaSmem mma_smem(int bb, int M, int64_t K, int rows, int sb) {
 // the rows of its largest share of tiles. Of the shapes that fit with their
 // stages, the first in order of preference whose rows per CTA are within a
 // slack of the least is taken: for up to 8 tokens 14 x 32 rows (Q4_1 with
-// 4-block stages), then 7 x 32, then 8 x 16; for up to 16 tokens 7 x 32
-// (at 16 tokens the activation fragments and scale records a warp reads per
-// block are most of the shared-memory traffic, and a second row group halves
-// them per row; 14 warps would not fit their registers), then 12 x 16, then
-// 8 x 16. The 128256-row LM head gets 2 tiles of 448 rows per SM up to 8
-// tokens and 4 of 224 up to 16, the same 896 rows as 7 tiles of 128.
+// 4-block stages), then 7 x 32, then 8 x 16; for up to 16 tokens 9 x 32 for
+// Q4_1 (4-block stages) and 7 x 32 for the others (at 16 tokens the
+// activation fragments and scale records a warp reads per block are most of
+// the shared-memory traffic, and a second row group halves them per row; 14
+// warps would not fit their registers), then 12 x 16, then 8 x 16. The
+// 128256-row LM head gets 2 tiles of 448 rows per SM up to 8 tokens (the same
+// 896 rows as 7 tiles of 128) and, for Q4_1, 3 of 288 up to 16.
 // Packed weights (one 4-block unit per row group and stage) take the same
 // shapes with 4-block stages for every format.
 struct TileShape {
@@ -380,9 +381,9 @@ struct TileShape {
 };
 TileShape choose_tile(int bb, int M, int64_t N, int64_t K, int sms, int lim, bool pk) {
     const TileShape cand1[] = {{14, 2, bb == 20 ? 4 : 8}, {7, 2, 8}, {8, 1, 8}};
-    const TileShape cand2[] = {{7, 2, bb == 20 ? 4 : 8}, {12, 1, 8}, {8, 1, 8}};
+    const TileShape cand2[] = {bb == 20 ? TileShape{9, 2, 4} : TileShape{7, 2, 8}, {12, 1, 8}, {8, 1, 8}};
     const TileShape pk1[] = {{14, 2, 4}, {7, 2, 4}, {8, 1, 4}};
-    const TileShape pk2[] = {{7, 2, 4}, {12, 1, 4}, {8, 1, 4}};
+    const TileShape pk2[] = {bb == 20 ? TileShape{9, 2, 4} : TileShape{7, 2, 4}, {12, 1, 4}, {8, 1, 4}};
     const TileShape* cand = pk ? (M <= 8 ? pk1 : pk2) : (M <= 8 ? cand1 : cand2);
     const int nc = 3;
     // Three stages up to 8 tokens, except for Q8_0, whose 272-byte rows fit
@@ -445,6 +446,9 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
         p.ngroups = static_cast<int>((N + 15) / 16);
         const CUtensorMap none{};
         if (NT == 2) {
+            if constexpr (WF == CQ_Q4_1) {
+                if (T.rg == 9) return launch_mma_typed<WF, 9, 2, 2, 4, true>(dev, p, none, s);
+            }
             if (T.rg == 7) return launch_mma_typed<WF, 7, 2, 2, 4, true>(dev, p, none, s);
             return T.rg == 12 ? launch_mma_typed<WF, 12, 2, 1, 4, true>(dev, p, none, s)
                               : launch_mma_typed<WF, 8, 2, 1, 4, true>(dev, p, none, s);
@@ -469,6 +473,9 @@ cudaError_t launch_mma_fmt(const DeviceInfo& dev, int M, int64_t N, int64_t K, c
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     if (NT == 2) {
+        if constexpr (WF == CQ_Q4_1) {
+            if (T.rg == 9) return launch_mma_typed<WF, 9, 2, 2, 4>(dev, p, map, s);
+        }
         if (T.rg == 7) {
             if constexpr (WF == CQ_Q4_1) {
                 if (T.sb == 4) return launch_mma_typed<WF, 7, 2, 2, 4>(dev, p, map, s);
