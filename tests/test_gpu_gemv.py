@@ -296,3 +296,29 @@ def test_batched_gemv_long_tiles(orc, wfmt, tail):
     for M in (2, 4, 8, 9, 16):
         yM = cq.gemv_t(Wd, xd[:M], wfmt, K).cpu().numpy()
         assert np.array_equal(yM.view(np.uint32), single[:M].view(np.uint32)), f"M={M} rows differ from M=1"
+
+
+@pytest.mark.parametrize("wfmt,M,N,K", [(12, 130, 300, 1024), (12, 9, 8200, 512), (2, 70, 200, 512)])
+def test_gemm_under_graph_capture(orc, wfmt, M, N, K):
+    """cq_gemm (and cq_gemv's Q4_K route to it at M = 9) captured into a CUDA
+    graph: the library's pool is not used while the stream is capturing, so the
+    graph holds the allocation-free kernels; its replay gives the bits of the
+    eager call, which took its workspace from the pool."""
+    torch = torch_cuda()
+    cq = cq_built()
+    W, xq = _case(orc, wfmt, N, K, M, seed=wfmt * 5 + M + N)
+    Wd, xd = dev(torch, W), dev(torch, xq)
+    call = (lambda out: cq.gemv_t(Wd, xd, wfmt, K, out=out)) if M <= 16 else \
+        (lambda out: cq.gemm_t(Wd, xd, wfmt, K, out=out))
+    y_eager = call(None).clone()
+    cq.gemm_noalloc_t(Wd, xd, wfmt, K)        # the allocation-free kernels' attributes set outside capture
+    torch.cuda.synchronize()
+    y = torch.zeros_like(y_eager)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(y)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), y_eager.cpu().numpy().view(np.uint32))
