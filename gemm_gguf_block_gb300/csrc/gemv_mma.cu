@@ -1,4 +1,6 @@
-// Batched GEMV for 2 <= M <= 16 tokens on the tensor cores (Q4_0, Q4_1, Q8_0).
+// Batched GEMV for up to 16 tokens on the tensor cores (Q4_0, Q4_1, Q8_0):
+// cq_gemv from 2 tokens, and cq_gemv_packed (weights repacked by cq_repack)
+// from 1.
 //
 // cera README "Other features" and 0.5 release notes: the speculative-decoding
 // verify path projects all 1 + k positions through the LM head in one batched
@@ -21,13 +23,14 @@
 //
 // A persistent CTA stages the tokens' activations once as fp16 in shared
 // memory, then a producer warp streams weight tiles of 16 * RW * RG rows
-// through a ring of 2-D TMA boxes (the tile's rows x 8 blocks). Each of the RG
-// consumer warps owns RW row groups of 16 rows and all the tokens (NT n-tiles
-// of 8). The activation fragments and scale records a warp reads from shared
-// memory per block serve all its row groups: with one row group per warp they
-// made two thirds of the shared-memory wavefronts and kept that pipe about
-// 60% busy, so the long tiles take two (7 warps x 32 rows for up to 8
-// tokens, 6 x 32 for up to 16).
+// through a ring of stages: 2-D TMA boxes of the tile's rows x 8 or 4 blocks
+// (GGUF layout), or one bulk copy of the tile's 16-row x 4-block units
+// (packed layout). Each of the RG consumer warps owns RW row groups of 16 rows
+// and all the tokens (NT n-tiles of 8). The activation fragments and scale
+// records a warp reads from shared memory per block serve all its row groups:
+// with one row group per warp they made two thirds of the shared-memory
+// wavefronts and kept that pipe about 60% busy, so the long tiles take two
+// (choose_tile below).
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -68,7 +71,7 @@ struct MmaParams {
 };
 
 // Packed weights (cq_repack): a unit of 16 rows x 4 blocks is 64 * BB bytes,
-// the rows' scale fields (4 * PK_SCALE bytes per row) first, then the quant
+// the rows' scale fields (4 * SCALE bytes per row) first, then the quant
 // words, per (half, row, lane t) the words of blocks 0..3 as 16 bytes.
 template <int WF> struct Pk {
     static constexpr int UNIT = 64 * MF<WF>::BB;
