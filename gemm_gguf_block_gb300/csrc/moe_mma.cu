@@ -152,7 +152,10 @@ __device__ __forceinline__ bool run_pass(const MoeMmaParams& p, const Smem sm, i
         convert_acts<NT>(stage + NMAT * BOX_BYTES, sm, np, ct);
         tc::named_and(1, CONSUMERS * 32, true);
         const uint8_t* wa = stage + (16 * warp + g) * (SEGB * 18);
-#pragma unroll 4
+        // Unrolled twice for gate + up (four times measured 107 -> 114 us: a
+        // longer body, instruction fetch stalls) and four times for the down
+        // projection (87 -> 82 us).
+#pragma unroll(UP ? 2 : 4)
         for (int b = 0; b < SEGB; ++b) {
             uint32_t fa0[4], fa1[4], fb0[4], fb1[4];
             uint64_t dwa0, dwa1, dwb0 = 0, dwb1 = 0, m_unused[2];
